@@ -1,0 +1,241 @@
+"""CPU oracle for the ZeRO shard step (ctypes wrapper over zs_oracle.c).
+
+TEST INFRASTRUCTURE ONLY: imported by the tests, the smoke check and the
+benchmark's CPU-baseline leg, never by the library.  The C source states the
+pages and readings it follows.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SO = os.path.join(_HERE, "libzsoracle.so")
+FP16, BF16 = 0, 1
+
+_i64p = ctypes.POINTER(ctypes.c_int64)
+_u64p = ctypes.POINTER(ctypes.c_uint64)
+_f32p = ctypes.POINTER(ctypes.c_float)
+_f64p = ctypes.POINTER(ctypes.c_double)
+_u16p = ctypes.POINTER(ctypes.c_uint16)
+
+
+class HParams(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_double), ("beta1", ctypes.c_double), ("beta2", ctypes.c_double),
+                ("eps", ctypes.c_double), ("weight_decay", ctypes.c_double)]
+
+
+class Scaler(ctypes.Structure):
+    _fields_ = [("scale", ctypes.c_double), ("min_scale", ctypes.c_double),
+                ("window", ctypes.c_int32), ("clean_count", ctypes.c_int32),
+                ("hysteresis", ctypes.c_int32), ("hyst_left", ctypes.c_int32),
+                ("dynamic", ctypes.c_int32), ("pad_", ctypes.c_int32)]
+
+
+def make_hparams(lr, beta1, beta2, eps, weight_decay) -> HParams:
+    """Hyper-parameters as the fp32 values the library receives."""
+    f = lambda x: float(np.float32(x))  # noqa: E731
+    return HParams(f(lr), f(beta1), f(beta2), f(eps), f(weight_decay))
+
+
+def make_scaler(scale, min_scale=1.0, window=1000, hysteresis=1, dynamic=True) -> Scaler:
+    return Scaler(float(scale), float(min_scale), int(window), 0, int(hysteresis),
+                  int(hysteresis), 1 if dynamic else 0, 0)
+
+
+def _stale(out, srcs):
+    if not os.path.exists(out):
+        return True
+    t = os.path.getmtime(out)
+    return any(os.path.getmtime(s) > t for s in srcs)
+
+
+def build(force: bool = False) -> str:
+    srcs = [os.path.join(_HERE, "zs_oracle.c"), os.path.join(_HERE, "zs_oracle.h")]
+    if force or _stale(SO, srcs):
+        tmp = SO + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O1", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared",
+                               "-o", tmp, srcs[0], "-lm"])
+        os.replace(tmp, SO)
+    return SO
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is not None:
+        return _lib
+    L = ctypes.CDLL(build())
+    L.zso_partition.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _i64p, _i64p]
+    L.zso_shard_range.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                  _i64p, _i64p, _i64p]
+    L.zso_state_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, _u64p]
+    L.zso_half_to_double.argtypes = [ctypes.c_uint16, ctypes.c_int32]
+    L.zso_half_to_double.restype = ctypes.c_double
+    L.zso_f32_to_half.argtypes = [ctypes.c_float, ctypes.c_int32]
+    L.zso_f32_to_half.restype = ctypes.c_uint16
+    L.zso_half_to_double_array.argtypes = [_u16p, ctypes.c_int64, ctypes.c_int32, _f64p]
+    L.zso_f32_to_half_array.argtypes = [_f32p, ctypes.c_int64, ctypes.c_int32, _u16p]
+    PP = ctypes.POINTER(_u16p)
+    L.zso_reduce_accumulate.argtypes = [PP, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, _f32p,
+                                        ctypes.c_int32]
+    L.zso_any_nonfinite.argtypes = [PP, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64]
+    L.zso_any_nonfinite.restype = ctypes.c_int32
+    L.zso_adamw_apply.argtypes = [_f32p, ctypes.c_int64, ctypes.c_double, _f32p, _f32p, _f32p,
+                                  _u16p, ctypes.c_int32, ctypes.POINTER(HParams), ctypes.c_int64]
+    L.zso_scaler_update.argtypes = [ctypes.POINTER(Scaler), ctypes.c_int32]
+    L.zso_shard_step.argtypes = [PP, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                 ctypes.c_int64, _f32p, _f32p, _f32p, _f32p, _u16p,
+                                 ctypes.POINTER(HParams), _i64p, ctypes.POINTER(Scaler),
+                                 ctypes.c_int32]
+    L.zso_shard_step.restype = ctypes.c_int32
+    _lib = L
+    return L
+
+
+def _p(a, t):
+    return a.ctypes.data_as(t)
+
+
+def _check_u16(a):
+    assert a.dtype == np.uint16 and a.flags.c_contiguous
+    return a
+
+
+def _check_f32(a):
+    assert a.dtype == np.float32 and a.flags.c_contiguous
+    return a
+
+
+def _ptr_array(slices):
+    arr = (_u16p * len(slices))()
+    for i, s in enumerate(slices):
+        arr[i] = _p(_check_u16(s), _u16p)
+    return arr
+
+
+def partition(psi: int, n: int, align: int = 64):
+    a, b = ctypes.c_int64(), ctypes.c_int64()
+    if lib().zso_partition(psi, n, align, ctypes.byref(a), ctypes.byref(b)) != 0:
+        raise ValueError("bad partition arguments")
+    return a.value, b.value
+
+
+def shard_range(psi: int, shard_len: int, n: int, rank: int):
+    b, ve, pe = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    if lib().zso_shard_range(psi, shard_len, n, rank, ctypes.byref(b), ctypes.byref(ve),
+                             ctypes.byref(pe)) != 0:
+        raise ValueError("bad shard range arguments")
+    return b.value, ve.value, pe.value
+
+
+def state_bytes(psi: int, shard_len: int, stage: int) -> int:
+    out = ctypes.c_uint64()
+    if lib().zso_state_bytes(psi, shard_len, stage, ctypes.byref(out)) != 0:
+        raise ValueError("bad stage")
+    return out.value
+
+
+def half_to_double(bits: np.ndarray, dtype: int) -> np.ndarray:
+    bits = np.ascontiguousarray(bits, dtype=np.uint16)
+    out = np.empty(bits.shape, dtype=np.float64)
+    lib().zso_half_to_double_array(_p(bits, _u16p), bits.size, dtype, _p(out, _f64p))
+    return out
+
+
+def f32_to_half(x: np.ndarray, dtype: int) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint16)
+    lib().zso_f32_to_half_array(_p(x, _f32p), x.size, dtype, _p(out, _u16p))
+    return out
+
+
+def reduce_accumulate(slices, dtype: int, acc: np.ndarray, first: bool):
+    _check_f32(acc)
+    for s in slices:
+        assert s.shape[0] >= acc.shape[0]
+    lib().zso_reduce_accumulate(_ptr_array(slices), len(slices), dtype, acc.shape[0],
+                                _p(acc, _f32p), 1 if first else 0)
+
+
+def any_nonfinite(slices, dtype: int, count: int) -> int:
+    return int(lib().zso_any_nonfinite(_ptr_array(slices), len(slices), dtype, count))
+
+
+def adamw_apply(acc, grad_div, master, m, v, half_out, dtype, hp: HParams, t: int):
+    for a in (acc, master, m, v):
+        _check_f32(a)
+    _check_u16(half_out)
+    lib().zso_adamw_apply(_p(acc, _f32p), acc.shape[0], float(grad_div), _p(master, _f32p),
+                          _p(m, _f32p), _p(v, _f32p), _p(half_out, _u16p), dtype,
+                          ctypes.byref(hp), t)
+
+
+def scaler_update(sc: Scaler, overflow: int):
+    lib().zso_scaler_update(ctypes.byref(sc), int(overflow))
+
+
+@dataclass
+class ShardState:
+    """fp32 master / m / v and the half copy of one shard (or of any range)."""
+    master: np.ndarray
+    m: np.ndarray
+    v: np.ndarray
+    half: np.ndarray
+
+    @classmethod
+    def from_master(cls, master: np.ndarray, dtype: int):
+        master = np.array(master, dtype=np.float32)
+        return cls(master, np.zeros_like(master), np.zeros_like(master),
+                   f32_to_half(master, dtype))
+
+    def copy(self):
+        return ShardState(self.master.copy(), self.m.copy(), self.v.copy(), self.half.copy())
+
+
+def shard_step(grads, dtype: int, state: ShardState, hp: HParams, t: int, sc: Scaler,
+               extra_overflow: int = 0):
+    """One step of one owned-shard view.  grads[k][r] = rank r's slice in
+    micro-step k.  Returns (overflow, new t, acc)."""
+    g = len(grads)
+    n = len(grads[0])
+    count = state.master.shape[0]
+    flat = [s for micro in grads for s in micro]
+    acc = np.zeros(count, dtype=np.float32)
+    tt = ctypes.c_int64(t)
+    ovf = lib().zso_shard_step(_ptr_array(flat), g, n, dtype, count, _p(acc, _f32p),
+                               _p(state.master, _f32p), _p(state.m, _f32p), _p(state.v, _f32p),
+                               _p(state.half, _u16p), ctypes.byref(hp), ctypes.byref(tt),
+                               ctypes.byref(sc), int(extra_overflow))
+    return int(ovf), tt.value, acc
+
+
+def multi_shard_step(grads_per_shard, dtype: int, states, hp: HParams, t: int, sc: Scaler):
+    """One step of all N ranks' shards with a global overflow flag (every
+    rank skips together): reduce each shard, OR the flags, then update every
+    shard with the same step count and scale, then update the scale once.
+    grads_per_shard[q][k][r] = rank r's slice of shard q in micro-step k."""
+    flag = 0
+    accs = []
+    for q, grads in enumerate(grads_per_shard):
+        count = states[q].master.shape[0]
+        acc = np.zeros(count, dtype=np.float32)
+        for k, micro in enumerate(grads):
+            reduce_accumulate(micro, dtype, acc, first=(k == 0))
+            flag |= any_nonfinite(micro, dtype, count)
+        accs.append(acc)
+    if not flag:
+        t += 1
+        n = len(grads_per_shard[0][0])
+        g = len(grads_per_shard[0])
+        for q, st in enumerate(states):
+            adamw_apply(accs[q], float(n) * g * sc.scale, st.master, st.m, st.v, st.half, dtype,
+                        hp, t)
+    scaler_update(sc, flag)
+    return flag, t, accs

@@ -1,0 +1,109 @@
+/*
+ * CPU oracle for the ZeRO-partitioned mixed-precision optimizer shard step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Plain, slow, single-threaded C in fp64 (fp32
+ * only where the step itself is defined in fp32: the gradient accumulator and
+ * the stored optimizer state).  Only the tests, the smoke check and the CPU
+ * baseline leg of the benchmark load it; the CUDA library never does, and it
+ * shares no code with the CUDA library.
+ *
+ * Sources (page title, section):
+ *  - DeepSpeed Complete Guide (youngju.dev), §2 memory table: fp16 params and
+ *    grads (2 bytes each), fp32 master params, Adam momentum and variance
+ *    (4 bytes each), 16 bytes per parameter in all.
+ *  - same page, §2.1 (ZeRO-1: optimizer state split N ways, each rank updates
+ *    only its shard), §2.2 (ZeRO-2: gradients split too; each rank accumulates
+ *    only the gradients of its shard, delivered by reduce-scatter), §2.3
+ *    (ZeRO-3: parameters split too).
+ *  - same page, §4.1 and §4.2: AdamW with eps 1e-8; fp16 dynamic loss scale
+ *    starting at 2^16, loss_scale_window clean steps before an increase,
+ *    hysteresis overflows before a decrease, min_loss_scale.
+ *  - same page, §4.3: train batch = micro batch x accumulation steps x world
+ *    size, so the applied gradient is the mean over ranks and micro-steps.
+ *  - DeepSpeed (aibars.net), core features: fp16 training, gradient
+ *    accumulation, dynamic loss scaling.
+ *
+ * Readings where the pages are silent:
+ *  - Adam is the textbook bias-corrected form with eps added to sqrt(v_hat),
+ *    and AdamW's decay is decoupled: p -= lr * (m_hat/(sqrt(v_hat)+eps) + wd*p).
+ *  - The accumulator is fp32; per element it adds the slices in micro-step
+ *    order, then rank order 0..N-1, starting from +0.0, one IEEE fp32 add each.
+ *  - Overflow = any +-inf or NaN in any input slice of the step; a skipped
+ *    step leaves master, m, v, the half copy and the Adam step count as they
+ *    were.
+ *  - The scale doubles when `window` consecutive clean steps have passed since
+ *    the last overflow or increase; it halves (not below min_scale) on the
+ *    `hysteresis`-th overflow since the last decrease.
+ *  - Hyper-parameters are taken as the fp32 values the library receives;
+ *    the arithmetic of one step is fp64; master, m and v are rounded to fp32
+ *    (nearest even) between steps and the half copy is the fp32 master
+ *    rounded to nearest even.
+ *
+ * Parity pins (tests/test_oracle_pins.py): memory closed forms; shard bounds
+ * by enumeration; exact-rational sums and an order-sensitive case for the
+ * accumulator; Adam closed forms at t=1, at every t under a constant gradient
+ * and at t=2 for two given gradients; decoupled decay at g=0; the hand-worked
+ * scaler trace; half rounding against numpy (fp16) and torch (bf16) over
+ * every fp16 pattern and crafted ties; shard union and bucket invariance.
+ * Multi-step values under random gradients beyond those closed forms rest on
+ * the oracle alone: parity unpinned.
+ */
+#ifndef ZS_ORACLE_H
+#define ZS_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ZSO_FP16 0
+#define ZSO_BF16 1
+
+typedef struct {
+  double lr, beta1, beta2, eps, weight_decay;
+} zso_hparams;
+
+typedef struct {
+  double scale, min_scale;
+  int32_t window, clean_count, hysteresis, hyst_left, dynamic, pad_;
+} zso_scaler;
+
+/* Partition (§2.1-§2.3): psi_pad = round_up(psi, n*align); shard_len = psi_pad/n. */
+int zso_partition(int64_t psi, int32_t n, int32_t align, int64_t* psi_pad, int64_t* shard_len);
+/* Rank r owns [r*E, (r+1)*E); its valid part ends at min((r+1)*E, psi), clamped to begin. */
+int zso_shard_range(int64_t psi, int64_t shard_len, int32_t n, int32_t rank, int64_t* begin,
+                    int64_t* valid_end, int64_t* padded_end);
+/* Per-rank model-state bytes by ZeRO stage 0..3 (§2 table, §2.1-§2.3), with E = shard_len. */
+int zso_state_bytes(int64_t psi, int64_t shard_len, int32_t stage, uint64_t* bytes);
+
+double zso_half_to_double(uint16_t bits, int32_t dtype);
+uint16_t zso_f32_to_half(float x, int32_t dtype);
+/* Array forms of the two conversions above. */
+void zso_half_to_double_array(const uint16_t* bits, int64_t count, int32_t dtype, double* out);
+void zso_f32_to_half_array(const float* x, int64_t count, int32_t dtype, uint16_t* out);
+
+/* acc[i] = (first ? +0.0f : acc[i]) + s_0[i] + s_1[i] + ... (fp32, in order). */
+void zso_reduce_accumulate(const uint16_t* const* slices, int32_t n, int32_t dtype, int64_t count,
+                           float* acc, int32_t first);
+/* 1 iff any element of any slice is +-inf or NaN. */
+int32_t zso_any_nonfinite(const uint16_t* const* slices, int32_t n, int32_t dtype, int64_t count);
+/* Clean-step update of one range: g = acc / grad_div, then AdamW at step t (1-based). */
+void zso_adamw_apply(const float* acc, int64_t count, double grad_div, float* master, float* m,
+                     float* v, uint16_t* half_out, int32_t dtype, const zso_hparams* hp, int64_t t);
+void zso_scaler_update(zso_scaler* s, int32_t overflow);
+
+/* One optimizer step of one owned-shard view.  grads holds g*n pointers,
+ * micro-step major: grads[k*n + r] is rank r's slice in micro-step k.
+ * extra_overflow is OR'd into the step's flag (other shards' flags).
+ * Returns the flag; advances *t only on a clean step. */
+int32_t zso_shard_step(const uint16_t* const* grads, int32_t g, int32_t n, int32_t dtype,
+                       int64_t count, float* acc, float* master, float* m, float* v,
+                       uint16_t* half_out, const zso_hparams* hp, int64_t* t, zso_scaler* sc,
+                       int32_t extra_overflow);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif
