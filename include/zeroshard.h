@@ -1,0 +1,228 @@
+/*
+ * zeroshard: the data-parallel hot path of ZeRO mixed-precision training on
+ * one GB300 (sm_103a) -- the optimizer step of the parameter shard this GPU
+ * owns.
+ *
+ * What the step computes (DeepSpeed Complete Guide, youngju.dev):
+ *  - §2 memory table: fp16 (or bf16) parameters and gradients, fp32 master
+ *    parameters, fp32 Adam momentum and variance (2+2+4+4+4 = 16 bytes per
+ *    parameter).
+ *  - §2.1 ZeRO-1: master/momentum/variance are split into N shards; each rank
+ *    updates only its own shard and an all-gather rebuilds the parameters.
+ *  - §2.2 ZeRO-2: gradients are split too; reduce-scatter hands each rank the
+ *    sum of all ranks' gradients over its shard, which it accumulates;
+ *    gradients travel in buckets of reduce_bucket_size elements.
+ *  - §2.3 ZeRO-3: parameters are split as well (16 bytes / N per parameter).
+ *  - §4.2 fp16 settings: dynamic loss scale starting at 2^initial_scale_power,
+ *    raised after loss_scale_window clean steps, lowered after `hysteresis`
+ *    overflows, never below min_loss_scale; bf16 needs no loss scaling.
+ *  - §4.3: the global batch is micro batch x accumulation steps x world size,
+ *    so the applied gradient is the mean over ranks and micro-steps.
+ *  - §4.1: the optimizer is AdamW with eps 1e-8.
+ *
+ * The N data-parallel ranks are simulated on one GPU: the caller holds, in
+ * this GPU's HBM, each rank's slice of the owned shard (what a reduce-scatter
+ * would sum).  The library sums them in fp32 in rank order 0..N-1 onto an
+ * fp32 accumulator (micro-step by micro-step), flags any +-inf/NaN before any
+ * state is written, and on a clean step applies bias-corrected AdamW with
+ * decoupled weight decay to the fp32 master/m/v and writes the half copy
+ * (round to nearest even) that an all-gather would consume.  On overflow the
+ * step leaves all state untouched and the loss scale is lowered.
+ *
+ * Conventions for every call:
+ *  - Ownership: every array is caller-owned DEVICE memory on the context's
+ *    device; `grads` is a HOST array of n device pointers, read during the
+ *    call only.  A context owns only a few device words and a pinned host
+ *    mirror.  Arrays must not overlap.
+ *  - Layout: contiguous 1-D arrays of `count` elements; half arrays hold
+ *    IEEE binary16 (ZS_FP16) or bfloat16 (ZS_BF16) bit patterns.
+ *  - Alignment: every device pointer must be 16-byte aligned (ZS_ERR_ALIGN);
+ *    count may be any value >= 0 (a ragged tail is handled).
+ *  - Limits: 1 <= n <= ZS_MAX_RANKS.
+ *  - Ordering: all work is issued on `stream` in order; only zs_shard_step,
+ *    zs_scaler_update and zs_ctx_timing synchronise that stream.
+ *  - Errors: a non-zero zs_status; zs_last_error(ctx) gives the message.
+ *    Overflow of the gradients is a result, not an error.
+ *  - Threads: a context is used by one host thread at a time.
+ */
+#ifndef ZEROSHARD_H
+#define ZEROSHARD_H
+
+#include <stdint.h>
+#include <cuda_runtime.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ZS_MAX_RANKS 256
+#define ZS_DEFAULT_ALIGN 64
+
+typedef enum {
+  ZS_OK = 0,
+  ZS_ERR_ARG = -1,     /* a null pointer, a negative size, n out of range */
+  ZS_ERR_ALIGN = -2,   /* a device pointer not 16-byte aligned */
+  ZS_ERR_DTYPE = -3,   /* dtype is neither ZS_FP16 nor ZS_BF16 */
+  ZS_ERR_CUDA = -4,    /* a CUDA runtime error (message in zs_last_error) */
+  ZS_ERR_TIMEOUT = -5  /* reserved: a bounded device wait gave up */
+} zs_status;
+
+typedef enum { ZS_FP16 = 0, ZS_BF16 = 1 } zs_dtype;
+
+/* Shard layout of a flat parameter buffer (§2.1-§2.3). */
+typedef struct {
+  int64_t psi;        /* number of parameters */
+  int64_t psi_pad;    /* psi rounded up to a multiple of n * align */
+  int64_t shard_len;  /* psi_pad / n: elements each rank owns, padding included */
+  int32_t n;          /* data-parallel ranks */
+  int32_t align;      /* alignment unit in elements */
+} zs_partition;
+
+/* AdamW hyper-parameters (§4.1), as fp32. */
+typedef struct {
+  float lr, beta1, beta2, eps, weight_decay;
+} zs_adam_hparams;
+
+/* Loss-scale state (§4.2), caller-owned, host memory.  dynamic = 0 keeps the
+ * scale fixed (bf16, or a static loss_scale); overflow still skips the step. */
+typedef struct {
+  float scale;          /* current loss scale S */
+  float min_scale;      /* min_loss_scale */
+  int32_t window;       /* loss_scale_window: clean steps before S doubles */
+  int32_t clean_count;  /* consecutive clean steps since the last overflow or increase */
+  int32_t hysteresis;   /* overflows before S halves */
+  int32_t hyst_left;    /* overflows still tolerated before the next halving */
+  int32_t dynamic;      /* 1: dynamic scaling, 0: static */
+} zs_scaler;
+
+typedef struct zs_ctx zs_ctx;
+
+/* ---------------------------------------------------------------- host-only */
+
+/* Partition psi parameters over n ranks (§2.1-§2.3): psi_pad = psi rounded up
+ * to a multiple of n*align_elems, shard_len = psi_pad/n; rank r owns flat
+ * indices [r*shard_len, (r+1)*shard_len), of which those >= psi are padding.
+ * psi >= 0, 1 <= n <= ZS_MAX_RANKS, align_elems >= 1 (ZS_DEFAULT_ALIGN = 64
+ * keeps every shard 16-byte aligned for both fp32 and half arrays). */
+zs_status zs_init_partition(int64_t psi, int32_t n, int32_t align_elems, zs_partition* out);
+
+/* Rank `rank`'s range: begin = rank*shard_len, padded_end = begin+shard_len,
+ * valid_end = max(begin, min(padded_end, psi)). */
+zs_status zs_shard_range(const zs_partition* p, int32_t rank, int64_t* begin, int64_t* valid_end,
+                         int64_t* padded_end);
+
+/* Per-rank model-state bytes for ZeRO stage 0..3 (§2 table, §2.1-§2.3), with
+ * E = shard_len: 16*psi, 4*psi + 12*E, 2*psi + 14*E, 16*E. */
+zs_status zs_model_state_bytes(const zs_partition* p, int32_t stage, uint64_t* bytes);
+
+/* Fill a scaler: hyst_left = hysteresis, clean_count = 0.  §4.2 defaults are
+ * scale 2^16, window 1000, hysteresis 2, min_scale 1. */
+zs_status zs_scaler_init(zs_scaler* s, float scale, float min_scale, int32_t window,
+                         int32_t hysteresis, int32_t dynamic);
+
+/* ---------------------------------------------------------------- context */
+
+/* Create a context on the current CUDA device.  It owns: the step's overflow
+ * flag (a device int32, zero at creation), a device result word and a pinned
+ * host mirror.  *ctx is set to NULL on failure. */
+zs_status zs_ctx_create(zs_ctx** ctx);
+zs_status zs_ctx_destroy(zs_ctx* ctx);
+/* Message of the last failed call on ctx ("" if none).  Valid until the next call. */
+const char* zs_last_error(const zs_ctx* ctx);
+/* Device address of the context's step overflow flag: zs_grad_accum ORs into
+ * it and zs_shard_step consumes and clears it.  A multi-GPU caller can
+ * all-reduce (MAX) this int32 in place before the last call of the step. */
+zs_status zs_ctx_overflow_flag(zs_ctx* ctx, int32_t** d_flag);
+
+/* ---------------------------------------------------------------- the step */
+
+/* Micro-steps 1..G-1 of a step (§2.2, §4.3): for i in [0, count)
+ *   acc[i] = (first ? +0.0f : acc[i]) + grads[0][i] + ... + grads[n-1][i]
+ * in fp32, in that order, and OR into the context's step flag whether any
+ * result is +-inf/NaN (a non-finite input always yields one).  Call it once
+ * per micro-step (first = 1 for the step's first) and, if the shard is split
+ * into buckets, once per bucket with sub-range pointers; results do not depend
+ * on the bucketing. */
+zs_status zs_grad_accum(zs_ctx* ctx, const void* const* grads, int32_t n, zs_dtype dt,
+                        int64_t count, float* acc, int32_t first, cudaStream_t stream);
+
+/* Two-phase form for a flag that spans several shards, buckets or GPUs.
+ * Phase 1: as zs_grad_accum, ORing into the caller's device int32 *d_flag.
+ * With acc == NULL it only checks (reads the slices, writes nothing else). */
+zs_status zs_reduce_check(zs_ctx* ctx, const void* const* grads, int32_t n, zs_dtype dt,
+                          int64_t count, float* acc, int32_t first, int32_t* d_flag,
+                          cudaStream_t stream);
+
+/* Phase 2: if *d_flag != 0 nothing is written.  Otherwise, per element,
+ *   s = acc[i] (or +0 if acc == NULL), then s += grads[r][i] for r = 0..n-1
+ *       when grads != NULL (the last micro-step, re-read instead of stored),
+ *   g = s / grad_div               (grad_div = N * G * S: mean and unscale)
+ *   m = beta1*m + (1-beta1)*g ;  v = beta2*v + (1-beta2)*g*g
+ *   p = p - lr * ( (m/(1-beta1^step)) / (sqrt(v/(1-beta2^step)) + eps) + wd*p )
+ *   half_out[i] = round_to_nearest_even(p)
+ * step is Adam's 1-based count of applied updates, this one included. */
+zs_status zs_apply(zs_ctx* ctx, const int32_t* d_flag, const void* const* grads, int32_t n,
+                   zs_dtype dt, const float* acc, int64_t count, float grad_div, float* master,
+                   float* m, float* v, void* half_out, const zs_adam_hparams* hp, int64_t step,
+                   cudaStream_t stream);
+
+/* Loss-scale update after phase 2 (§4.2), run on the device from *d_flag:
+ * overflow -> clean_count = 0 and, if dynamic, hyst_left -= 1 and at 0
+ * scale = max(scale/2, min_scale), hyst_left = hysteresis;
+ * clean -> if dynamic, clean_count += 1 and at window scale *= 2,
+ * clean_count = 0.  Writes *scaler and *overflow_out (may be NULL) and
+ * synchronises `stream`.  Does not clear *d_flag. */
+zs_status zs_scaler_update(zs_ctx* ctx, const int32_t* d_flag, zs_scaler* scaler,
+                           int32_t* overflow_out, cudaStream_t stream);
+
+/* The whole last call of a step for one owned shard (§2.1, §2.2, §4.2):
+ * grads are the n slices of the step's LAST micro-step; micro-steps
+ * 1..accum_steps-1 must already be in acc via zs_grad_accum.  It resolves the
+ * step's overflow (the context flag, OR this call's slices) before writing any
+ * state, applies AdamW with grad_div = n * accum_steps * scaler->scale,
+ * updates *scaler, writes *overflow_out and *new_scale_out (either may be
+ * NULL), clears the context flag and synchronises `stream`.
+ * acc may be NULL only when accum_steps == 1.  When n < 4 (or acc is NULL)
+ * the last slices are checked, then re-read by the update (2n bytes per
+ * element) instead of summed into acc and read back (8 bytes per element).
+ * The caller advances `step` only if *overflow_out == 0. */
+zs_status zs_shard_step(zs_ctx* ctx, const void* const* grads, int32_t n, zs_dtype dt,
+                        int64_t count, float* acc, int32_t accum_steps, float* master, float* m,
+                        float* v, void* half_out, const zs_adam_hparams* hp, int64_t step,
+                        zs_scaler* scaler, int32_t* overflow_out, float* new_scale_out,
+                        cudaStream_t stream);
+
+/* ---------------------------------------------------------------- measurement */
+
+/* HBM roofline probe: copy `bytes` from src to dst (read_only = 0), or only
+ * read src (read_only = 1; dst receives at most 16 bytes).  bytes must be a
+ * multiple of 16. */
+zs_status zs_copy_peak(zs_ctx* ctx, const void* src, void* dst, int64_t bytes, int32_t read_only,
+                       cudaStream_t stream);
+
+/* Kernel kinds for the timing counters. */
+typedef enum {
+  ZS_KERNEL_REDUCE = 0,          /* fp32 accumulate of n slices (+ flag) */
+  ZS_KERNEL_CHECK = 1,           /* flag-only pass over n slices */
+  ZS_KERNEL_APPLY = 2,           /* AdamW + cast from the accumulator */
+  ZS_KERNEL_APPLY_RECOMPUTE = 3, /* AdamW + cast, re-reading the last slices */
+  ZS_KERNEL_SCALER = 4,          /* standalone loss-scale update */
+  ZS_KERNEL_COPY = 5,            /* roofline probe */
+  ZS_KERNEL_KINDS = 6
+} zs_kernel_kind;
+
+/* When enabled, each launch is bracketed by CUDA events on its stream. */
+zs_status zs_ctx_set_timing(zs_ctx* ctx, int32_t enable);
+/* Device time (ms), launches and elements of one kernel kind since the last
+ * reset; waits for the recorded events. */
+zs_status zs_ctx_timing(zs_ctx* ctx, int32_t kind, double* total_ms, int64_t* launches,
+                        int64_t* elements);
+zs_status zs_ctx_timing_reset(zs_ctx* ctx);
+/* Kernels launched by this context since creation (always counted). */
+zs_status zs_ctx_launch_count(const zs_ctx* ctx, int64_t* launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZEROSHARD_H */

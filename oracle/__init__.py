@@ -87,6 +87,8 @@ def lib():
                                         ctypes.c_int32]
     L.zso_any_nonfinite.argtypes = [PP, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64]
     L.zso_any_nonfinite.restype = ctypes.c_int32
+    L.zso_any_nonfinite_f32.argtypes = [_f32p, ctypes.c_int64]
+    L.zso_any_nonfinite_f32.restype = ctypes.c_int32
     L.zso_adamw_apply.argtypes = [_f32p, ctypes.c_int64, ctypes.c_double, _f32p, _f32p, _f32p,
                                   _u16p, ctypes.c_int32, ctypes.POINTER(HParams), ctypes.c_int64]
     L.zso_scaler_update.argtypes = [ctypes.POINTER(Scaler), ctypes.c_int32]
@@ -168,6 +170,11 @@ def any_nonfinite(slices, dtype: int, count: int) -> int:
     return int(lib().zso_any_nonfinite(_ptr_array(slices), len(slices), dtype, count))
 
 
+def any_nonfinite_f32(x: np.ndarray) -> int:
+    _check_f32(x)
+    return int(lib().zso_any_nonfinite_f32(_p(x, _f32p), x.shape[0]))
+
+
 def adamw_apply(acc, grad_div, master, m, v, half_out, dtype, hp: HParams, t: int):
     for a in (acc, master, m, v):
         _check_f32(a)
@@ -229,6 +236,7 @@ def multi_shard_step(grads_per_shard, dtype: int, states, hp: HParams, t: int, s
         for k, micro in enumerate(grads):
             reduce_accumulate(micro, dtype, acc, first=(k == 0))
             flag |= any_nonfinite(micro, dtype, count)
+        flag |= any_nonfinite_f32(acc)
         accs.append(acc)
     if not flag:
         t += 1

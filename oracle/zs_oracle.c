@@ -157,6 +157,13 @@ int32_t zso_any_nonfinite(const uint16_t* const* slices, int32_t n, int32_t dtyp
   return 0;
 }
 
+int32_t zso_any_nonfinite_f32(const float* x, int64_t count) {
+  for (int64_t i = 0; i < count; ++i) {
+    if (isnan(x[i]) || isinf(x[i])) return 1;
+  }
+  return 0;
+}
+
 /* ---- AdamW on the fp32 master shard, then the half copy (§2.1, §4.1) ---- */
 
 void zso_adamw_apply(const float* acc, int64_t count, double grad_div, float* master, float* m,
@@ -215,6 +222,7 @@ int32_t zso_shard_step(const uint16_t* const* grads, int32_t g, int32_t n, int32
   int32_t ovf = extra_overflow != 0;
   for (int32_t k = 0; k < g && !ovf; ++k) ovf = zso_any_nonfinite(grads + (size_t)k * n, n,
                                                                   dtype, count);
+  if (!ovf) ovf = zso_any_nonfinite_f32(acc, count);
   if (!ovf) {
     *t += 1;
     zso_adamw_apply(acc, count, (double)n * (double)g * sc->scale, master, m, v, half_out, dtype,

@@ -28,9 +28,11 @@
  *    and AdamW's decay is decoupled: p -= lr * (m_hat/(sqrt(v_hat)+eps) + wd*p).
  *  - The accumulator is fp32; per element it adds the slices in micro-step
  *    order, then rank order 0..N-1, starting from +0.0, one IEEE fp32 add each.
- *  - Overflow = any +-inf or NaN in any input slice of the step; a skipped
- *    step leaves master, m, v, the half copy and the Adam step count as they
- *    were.
+ *  - Overflow = any +-inf or NaN in any input slice of the step, or an fp32
+ *    accumulated gradient that is not finite (finite bf16 inputs near the top
+ *    of their range can sum past the fp32 maximum; fp16 inputs cannot); a
+ *    skipped step leaves master, m, v, the half copy and the Adam step count
+ *    as they were.
  *  - The scale doubles when `window` consecutive clean steps have passed since
  *    the last overflow or increase; it halves (not below min_scale) on the
  *    `hysteresis`-th overflow since the last decrease.
@@ -88,6 +90,8 @@ void zso_reduce_accumulate(const uint16_t* const* slices, int32_t n, int32_t dty
                            float* acc, int32_t first);
 /* 1 iff any element of any slice is +-inf or NaN. */
 int32_t zso_any_nonfinite(const uint16_t* const* slices, int32_t n, int32_t dtype, int64_t count);
+/* 1 iff any fp32 value is +-inf or NaN (an accumulator that overflowed). */
+int32_t zso_any_nonfinite_f32(const float* x, int64_t count);
 /* Clean-step update of one range: g = acc / grad_div, then AdamW at step t (1-based). */
 void zso_adamw_apply(const float* acc, int64_t count, double grad_div, float* master, float* m,
                      float* v, uint16_t* half_out, int32_t dtype, const zso_hparams* hp, int64_t t);

@@ -1,0 +1,99 @@
+"""Full-size workloads, in the launch configuration the benchmark times
+(bench.DeviceWorkload: zs_grad_accum for micro-steps 1..G-1, zs_shard_step
+for the last), checked against the oracle on sampled elements.
+
+The step is elementwise once the step's overflow flag is known, so the oracle
+replays every step on a sample of the owned shard: 2^16 seeded positions, the
+first and last 4096 elements, both sides of every tensor boundary inside the
+shard, every injected index and the padding edge.  Its flag comes from the
+sample (which holds every injection) OR the injection schedule; natural
+gradients cannot overflow (Irwin-Hall |z| <= 6, so |g| <= 6*sigma*S < 65504
+for the fp16 workloads), and the GPU's full-scan flag must equal it.
+The loss scale that generates each step's gradients is the oracle's.
+ZS_FULLSIZE_STEPS caps the step count (default: the workload's own).
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+REL, ABS = 1e-6, 1e-9
+
+
+def sample_positions(wl, begin, E, valid):
+    rng = np.random.default_rng(0)
+    pos = [rng.integers(0, E, 1 << 16), np.arange(min(4096, E)), np.arange(max(0, E - 4096), E)]
+    for _, b, e in wl.tensor_ranges():
+        for x in (b - 2, b - 1, b, b + 1, e - 1, e):
+            if begin <= x < begin + E:
+                pos.append(np.array([x - begin]))
+    for j in wl.injections:
+        if begin <= j.index < begin + E:
+            pos.append(np.array([j.index - begin]))
+    if valid < E:
+        pos.append(np.array([valid - 1, valid, E - 1]))
+    return np.unique(np.concatenate(pos).astype(np.int64))
+
+
+def half_ulps(a, b):
+    def ordered(x):
+        x = x.astype(np.int32)
+        return np.where(x & 0x8000, -(x & 0x7FFF), x & 0x7FFF)
+    return np.abs(ordered(a) - ordered(b))
+
+
+@pytest.mark.parametrize("name", ["gpt2-small-n8", "decoder-1.3b-n16", "llama7b-zero3-n64",
+                                  "llama7b-n1"])
+def test_fullsize_sampled(name):
+    import bench
+    import zero_mixed_precision_shard_gb300 as zs
+    torch.cuda.set_device(0)
+    wl = synth.WORKLOADS[name]
+    steps = min(wl.steps, int(os.environ.get("ZS_FULLSIZE_STEPS", wl.steps)))
+    ctx = zs.Ctx()
+    W = bench.DeviceWorkload(wl, shard=0)
+    E, begin = W.E, W.begin
+    valid = W.valid_end - W.begin
+    pos = sample_positions(wl, begin, E, valid)
+    gidx = begin + pos
+    st = oracle.ShardState.from_master(synth.host_master(wl, gidx), wl.dtype_code)
+    hp_o = oracle.make_hparams(wl.lr, wl.beta1, wl.beta2, wl.eps, wl.weight_decay)
+    sc_o = oracle.make_scaler(wl.scale0, wl.min_scale, wl.window, wl.hysteresis, wl.dynamic)
+    t_o = 0
+    pos_d = torch.from_numpy(pos).cuda()
+    flags = []
+    for s in range(1, steps + 1):
+        W.fill_grads(s, sc_o.scale, inject=True)
+        grads = [[synth.host_grad_bits(wl, gidx, s, k + 1, r, sc_o.scale) for r in range(wl.n)]
+                 for k in range(wl.g)]
+        scheduled = any(begin <= j.index < begin + E for j in wl.injections_at(s))
+        ovf_o, t_o, _ = oracle.shard_step(grads, wl.dtype_code, st, hp_o, t_o, sc_o,
+                                          extra_overflow=int(scheduled))
+        ovf = W.step(ctx)
+        assert ovf == ovf_o, f"step {s}"
+        assert W.scaler.scale == sc_o.scale, f"step {s}"
+        flags.append(ovf)
+    assert W.t == t_o
+    expect = [1 if any(begin <= j.index < begin + E for j in wl.injections_at(s)) else 0
+              for s in range(1, steps + 1)]
+    assert flags == expect
+    got = {k: getattr(W, k).index_select(0, pos_d).cpu().numpy()
+           for k in ("master", "m", "v", "half")}
+    for k in ("master", "m", "v"):
+        want = getattr(st, k).astype(np.float64)
+        err = np.abs(got[k].astype(np.float64) - want)
+        assert (err <= REL * np.abs(want) + ABS).all(), (k, float((err / (REL * np.abs(want) + ABS)).max()))
+    assert half_ulps(got["half"].view(np.uint16), st.half).max() <= 1
+    # padding stays zero
+    if valid < E:
+        tail = W.master[valid:]
+        assert torch.count_nonzero(tail).item() == 0
+    ctx.close()
+    del W
+    torch.cuda.empty_cache()

@@ -1,0 +1,379 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle on the same
+seeded inputs: bit-exact accumulators and flags, AdamW state within
+1e-6 relative + 1e-9 absolute, half copies within 1 ulp, exact scales and skip
+decisions.  Sizes span several CTAs' worth of vectors plus ragged tails."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+FP16, BF16 = 0, 1
+REL, ABS = 1e-6, 1e-9
+
+
+@pytest.fixture(scope="module")
+def zs():
+    import zero_mixed_precision_shard_gb300 as pkg
+    torch.cuda.set_device(0)
+    return pkg
+
+
+@pytest.fixture(scope="module")
+def ctx(zs):
+    c = zs.Ctx()
+    yield c
+    c.close()
+
+
+def lib_half(x, dtype):
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    if dtype == FP16:
+        return x.astype(np.float16).view(np.uint16)
+    return torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def dev16(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda()
+
+
+def host16(t):
+    return t.cpu().numpy().view(np.uint16)
+
+
+def rand_grads(rng, n, count, dtype, scale=1024.0):
+    out = []
+    for r in range(n):
+        x = rng.standard_normal(count) * 1e-3 * scale * np.exp2(rng.integers(-6, 6, count))
+        x[rng.random(count) < 0.01] = 0.0
+        x[rng.random(count) < 0.01] = -0.0
+        out.append(lib_half(x.astype(np.float32), dtype))
+    return out
+
+
+def assert_state_close(got, want, name):
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    err = np.abs(got - want)
+    tol = REL * np.abs(want) + ABS
+    bad = err > tol
+    assert not bad.any(), (f"{name}: {bad.sum()} elements out of tolerance, worst "
+                           f"{(err / tol).max():.3g}x at {np.argmax(err / tol)}")
+
+
+def half_ulps(a, b):
+    """Distance in units in the last place between two half bit-pattern arrays."""
+    def ordered(x):
+        x = x.astype(np.int32)
+        return np.where(x & 0x8000, -(x & 0x7FFF), x & 0x7FFF)
+    return np.abs(ordered(a) - ordered(b))
+
+
+# ---------------------------------------------------------------- reduce
+
+CASES = [(n, c) for n in (1, 2, 3, 4, 5, 8, 9, 16, 64) for c in (0, 1, 7, 8, 9, 1000, 65541)]
+CASES += [(256, 4099), (255, 17)]
+
+
+@pytest.mark.parametrize("dtype", [FP16, BF16])
+@pytest.mark.parametrize("n,count", CASES)
+def test_grad_accum_bit_exact(zs, ctx, dtype, n, count):
+    rng = np.random.default_rng(1000 * n + count)
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    acc_d = torch.full((max(count, 1),), 123.0, dtype=torch.float32, device="cuda")
+    acc_o = np.zeros(count, np.float32)
+    for k in range(3):
+        g = rand_grads(rng, n, count, dtype)
+        zs.zs_reduce_check(ctx, [dev16(s) for s in g], dtype, count, acc_d, k == 0, flag)
+        oracle.reduce_accumulate(g, dtype, acc_o, first=(k == 0))
+    got = acc_d[:count].cpu().numpy()
+    assert got.tobytes() == acc_o.tobytes()
+    assert flag.item() == 0
+    # check-only form: flag only, nothing written
+    before = acc_d.clone()
+    zs.zs_reduce_check(ctx, [dev16(s) for s in g], dtype, count, None, True, flag)
+    assert flag.item() == 0 and torch.equal(before, acc_d)
+
+
+@pytest.mark.parametrize("dtype", [FP16, BF16])
+@pytest.mark.parametrize("where", ["first", "body", "tail", "last_rank"])
+@pytest.mark.parametrize("kind", ["inf", "-inf", "nan"])
+def test_overflow_flag(zs, ctx, dtype, where, kind):
+    rng = np.random.default_rng(7)
+    n, count = 5, 8 * 1000 + 5
+    g = rand_grads(rng, n, count, dtype)
+    bits = {"inf": 0x7C00 if dtype == FP16 else 0x7F80,
+            "-inf": 0xFC00 if dtype == FP16 else 0xFF80,
+            "nan": 0x7E00 if dtype == FP16 else 0x7FC0}[kind]
+    r, i = {"first": (0, 0), "body": (2, 4321), "tail": (1, count - 2),
+            "last_rank": (n - 1, count // 2)}[where]
+    g[r][i] = bits
+    assert oracle.any_nonfinite(g, dtype, count) == 1
+    for acc in (torch.zeros(count, dtype=torch.float32, device="cuda"), None):
+        flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+        zs.zs_reduce_check(ctx, [dev16(s) for s in g], dtype, count, acc, True, flag)
+        assert flag.item() == 1
+
+
+def test_bf16_finite_sum_overflow_is_flagged(zs, ctx):
+    big = lib_half(np.full(16, 3.0e38, np.float32), BF16)
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    acc = torch.zeros(16, dtype=torch.float32, device="cuda")
+    zs.zs_reduce_check(ctx, [dev16(big), dev16(big)], BF16, 16, acc, True, flag)
+    assert flag.item() == 1 and torch.isinf(acc).all()
+    acc_o = np.zeros(16, np.float32)
+    oracle.reduce_accumulate([big, big], BF16, acc_o, True)
+    assert oracle.any_nonfinite_f32(acc_o) == 1
+
+
+# ---------------------------------------------------------------- apply
+
+def random_state(rng, count):
+    master = (rng.standard_normal(count) * 0.02).astype(np.float32)
+    m = (rng.standard_normal(count) * 1e-4).astype(np.float32)
+    v = (rng.random(count) * 1e-7).astype(np.float32)
+    return master, m, v
+
+
+@pytest.mark.parametrize("dtype", [FP16, BF16])
+@pytest.mark.parametrize("count", [1, 9, 4096, 100003])
+@pytest.mark.parametrize("t,wd", [(1, 0.0), (2, 0.01), (10, 0.1), (1000, 0.0)])
+def test_apply_matches_oracle(zs, ctx, dtype, count, t, wd):
+    rng = np.random.default_rng(count + t)
+    master, m, v = random_state(rng, count)
+    n, g, S = 8, 4, 65536.0
+    acc = (rng.standard_normal(count) * 1e-3 * n * g * S).astype(np.float32)
+    acc[:min(count, 3)] = 0.0
+    hp_o = oracle.make_hparams(1e-4, 0.9, 0.999, 1e-8, wd)
+    st = oracle.ShardState(master.copy(), m.copy(), v.copy(), np.zeros(count, np.uint16))
+    oracle.adamw_apply(acc, n * g * S, st.master, st.m, st.v, st.half, dtype, hp_o, t)
+    d = [torch.from_numpy(a.copy()).cuda() for a in (acc, master, m, v)]
+    half = torch.zeros(count, dtype=torch.int16, device="cuda")
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    hp = zs.make_hparams(1e-4, 0.9, 0.999, 1e-8, wd)
+    zs.zs_apply(ctx, flag, None, dtype, d[0], count, n * g * S, d[1], d[2], d[3], half, hp, t)
+    assert_state_close(d[1].cpu().numpy(), st.master, "master")
+    assert_state_close(d[2].cpu().numpy(), st.m, "m")
+    assert_state_close(d[3].cpu().numpy(), st.v, "v")
+    assert half_ulps(host16(half), st.half).max() <= 1
+    # a set flag writes nothing
+    flag.fill_(1)
+    snap = [x.clone() for x in d[1:]] + [half.clone()]
+    zs.zs_apply(ctx, flag, None, dtype, d[0], count, n * g * S, d[1], d[2], d[3], half, hp, t + 1)
+    for a, b in zip(snap, d[1:] + [half]):
+        assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("dtype", [FP16, BF16])
+@pytest.mark.parametrize("with_acc", [False, True])
+def test_apply_recompute_matches_oracle(zs, ctx, dtype, with_acc):
+    rng = np.random.default_rng(11)
+    n, count, S = 3, 50001, 256.0
+    master, m, v = random_state(rng, count)
+    g_prev = rand_grads(rng, n, count, dtype, S)
+    g_last = rand_grads(rng, n, count, dtype, S)
+    acc_o = np.zeros(count, np.float32)
+    G = 1
+    if with_acc:
+        oracle.reduce_accumulate(g_prev, dtype, acc_o, True)
+        G = 2
+    oracle.reduce_accumulate(g_last, dtype, acc_o, not with_acc)
+    hp_o = oracle.make_hparams(1e-3, 0.9, 0.999, 1e-8, 0.01)
+    st = oracle.ShardState(master.copy(), m.copy(), v.copy(), np.zeros(count, np.uint16))
+    oracle.adamw_apply(acc_o, n * G * S, st.master, st.m, st.v, st.half, dtype, hp_o, 3)
+    acc = None
+    if with_acc:
+        acc = torch.zeros(count, dtype=torch.float32, device="cuda")
+        f0 = torch.zeros(1, dtype=torch.int32, device="cuda")
+        zs.zs_reduce_check(ctx, [dev16(s) for s in g_prev], dtype, count, acc, True, f0)
+    d = [torch.from_numpy(a.copy()).cuda() for a in (master, m, v)]
+    half = torch.zeros(count, dtype=torch.int16, device="cuda")
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    hp = zs.make_hparams(1e-3, 0.9, 0.999, 1e-8, 0.01)
+    zs.zs_apply(ctx, flag, [dev16(s) for s in g_last], dtype, acc, count, n * G * S, d[0], d[1],
+                d[2], half, hp, 3)
+    assert_state_close(d[0].cpu().numpy(), st.master, "master")
+    assert_state_close(d[1].cpu().numpy(), st.m, "m")
+    assert_state_close(d[2].cpu().numpy(), st.v, "v")
+    assert half_ulps(host16(half), st.half).max() <= 1
+
+
+# ---------------------------------------------------------------- whole steps
+
+def run_shard_steps(zs, ctx, dtype, n, G, count, steps, seed, inject=None, acc_mode="auto"):
+    """Drive zs_grad_accum + zs_shard_step on the GPU and oracle.shard_step on
+    the host for `steps` steps; the oracle's scale drives input generation."""
+    rng = np.random.default_rng(seed)
+    master0 = (rng.standard_normal(count) * 0.02).astype(np.float32)
+    st = oracle.ShardState.from_master(master0, dtype)
+    hp_vals = (1e-3, 0.9, 0.999, 1e-8, 0.01)
+    hp_o = oracle.make_hparams(*hp_vals)
+    dynamic = dtype == FP16
+    sc_o = oracle.make_scaler(1024.0 if dynamic else 1.0, 1.0, 3, 1, dynamic)
+    sc = zs.zs_scaler_init(sc_o.scale, 1.0, 3, 1, dynamic)
+    hp = zs.make_hparams(*hp_vals)
+    master = torch.from_numpy(master0.copy()).cuda()
+    m = torch.zeros_like(master)
+    v = torch.zeros_like(master)
+    half = torch.zeros(count, dtype=torch.int16, device="cuda")
+    acc = torch.zeros(count, dtype=torch.float32, device="cuda")
+    if acc_mode == "none":
+        acc = None
+    t_o = t = 0
+    flags = []
+    for s in range(1, steps + 1):
+        grads = [rand_grads(rng, n, count, dtype, sc_o.scale) for _ in range(G)]
+        if inject and s in inject:
+            k, r, i, bits = inject[s]
+            grads[k][r][i] = bits
+        ovf_o, t_o, _ = oracle.shard_step(grads, dtype, st, hp_o, t_o, sc_o)
+        dg = [[dev16(x) for x in micro] for micro in grads]
+        for k in range(G - 1):
+            zs.zs_grad_accum(ctx, dg[k], dtype, count, acc, k == 0)
+        ovf, new_scale = zs.zs_shard_step(ctx, dg[G - 1], dtype, count, acc, G, master, m, v,
+                                          half, hp, t + 1, sc)
+        if not ovf:
+            t += 1
+        assert ovf == ovf_o, f"step {s}"
+        assert new_scale == sc_o.scale and sc.scale == sc_o.scale, f"step {s}"
+        assert (sc.clean_count, sc.hyst_left) == (sc_o.clean_count, sc_o.hyst_left)
+        flags.append(ovf)
+    assert t == t_o
+    assert_state_close(master.cpu().numpy(), st.master, "master")
+    assert_state_close(m.cpu().numpy(), st.m, "m")
+    assert_state_close(v.cpu().numpy(), st.v, "v")
+    assert half_ulps(host16(half), st.half).max() <= 1
+    return flags, (master, m, v, half)
+
+
+@pytest.mark.parametrize("dtype", [FP16, BF16])
+@pytest.mark.parametrize("n,G,count", [(1, 1, 4099), (2, 3, 10007), (4, 1, 8192 + 3),
+                                       (8, 2, 20011), (16, 1, 777)])
+def test_shard_step_sequence(zs, ctx, dtype, n, G, count):
+    inf = 0x7C00 if dtype == FP16 else 0x7F80
+    inject = {3: (G - 1, n - 1, count - 1, inf), 5: (0, 0, count // 2, 0x7E00 if dtype == FP16
+                                                      else 0x7FC0)}
+    flags, _ = run_shard_steps(zs, ctx, dtype, n, G, count, 10, seed=n * 100 + G, inject=inject)
+    assert flags == [0, 0, 1, 0, 1, 0, 0, 0, 0, 0]
+
+
+@pytest.mark.parametrize("n", [4, 8])
+def test_materialise_and_recompute_agree_bitwise(zs, ctx, n):
+    _, a = run_shard_steps(zs, ctx, FP16, n, 1, 5003, 4, seed=5, acc_mode="auto")
+    _, b = run_shard_steps(zs, ctx, FP16, n, 1, 5003, 4, seed=5, acc_mode="none")
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_zero_count_step_still_updates_scale(zs, ctx):
+    sc = zs.zs_scaler_init(1024.0, 1.0, 1, 1, True)
+    e = torch.zeros(8, dtype=torch.float32, device="cuda")
+    h = torch.zeros(8, dtype=torch.int16, device="cuda")
+    g = [torch.zeros(8, dtype=torch.int16, device="cuda")]
+    ovf, s = zs.zs_shard_step(ctx, g, FP16, 0, None, 1, e, e, e, h, zs.make_hparams(1e-3), 1, sc)
+    assert ovf == 0 and s == 2048.0
+
+
+def test_flat_1m_two_ranks_all_shards(zs, ctx):
+    """The 2-rank flat workload (Ψ = 2^20, fp16, +inf at step 5 on rank 1) in
+    full: both shards per step with one global flag (two-phase calls),
+    against the oracle's union of shard steps."""
+    wl = synth.WORKLOADS["flat-1m-n2"]
+    psi_pad, E = oracle.partition(wl.psi, wl.n)
+    idx = np.arange(wl.psi, dtype=np.int64)
+    master0 = synth.host_master(wl, idx)
+    states = [oracle.ShardState.from_master(master0[q * E:(q + 1) * E], FP16) for q in range(2)]
+    hp_o = oracle.make_hparams(wl.lr, wl.beta1, wl.beta2, wl.eps, wl.weight_decay)
+    sc_o = oracle.make_scaler(wl.scale0, wl.min_scale, wl.window, wl.hysteresis, wl.dynamic)
+    hp = zs.make_hparams(wl.lr, wl.beta1, wl.beta2, wl.eps, wl.weight_decay)
+    sc = zs.zs_scaler_init(wl.scale0, wl.min_scale, wl.window, wl.hysteresis, wl.dynamic)
+    dev = [dict(master=torch.from_numpy(master0[q * E:(q + 1) * E].copy()).cuda(),
+                m=torch.zeros(E, device="cuda"), v=torch.zeros(E, device="cuda"),
+                half=torch.zeros(E, dtype=torch.int16, device="cuda")) for q in range(2)]
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t_o = t = 0
+    flags = []
+    for s in range(1, wl.steps + 1):
+        full = [synth.host_grad_bits(wl, idx, s, 1, r, sc_o.scale) for r in range(2)]
+        per = [[[np.ascontiguousarray(f[q * E:(q + 1) * E]) for f in full]] for q in range(2)]
+        ovf_o, t_o, _ = oracle.multi_shard_step(per, FP16, states, hp_o, t_o, sc_o)
+        full_d = [dev16(f) for f in full]
+        flag.zero_()
+        for q in range(2):  # n = 2 < 4: check pass, then the update re-reads the slices
+            zs.zs_reduce_check(ctx, [f[q * E:(q + 1) * E] for f in full_d], FP16, E, None, True,
+                               flag)
+        for q in range(2):
+            zs.zs_apply(ctx, flag, [f[q * E:(q + 1) * E] for f in full_d], FP16, None, E,
+                        float(wl.n * wl.g * sc.scale), dev[q]["master"], dev[q]["m"],
+                        dev[q]["v"], dev[q]["half"], hp, t + 1)
+        ovf = zs.zs_scaler_update(ctx, flag, sc)
+        if not ovf:
+            t += 1
+        assert ovf == ovf_o and sc.scale == sc_o.scale
+        flags.append(ovf)
+    assert flags == [0, 0, 0, 0, 1, 0, 0, 0, 0, 0] and sc.scale == 2.0 ** 15 and t == t_o == 9
+    for q in range(2):
+        assert_state_close(dev[q]["master"].cpu().numpy(), states[q].master, "master")
+        assert_state_close(dev[q]["m"].cpu().numpy(), states[q].m, "m")
+        assert_state_close(dev[q]["v"].cpu().numpy(), states[q].v, "v")
+        assert half_ulps(host16(dev[q]["half"]), states[q].half).max() <= 1
+
+
+def test_bucketed_calls_equal_whole_shard(zs, ctx):
+    rng = np.random.default_rng(9)
+    n, count, bucket = 8, 100_000, 9_992
+    g = [rand_grads(rng, n, count, FP16) for _ in range(2)]
+    master, m, v = random_state(rng, count)
+    hp = zs.make_hparams(1e-3, 0.9, 0.999, 1e-8, 0.01)
+    outs = []
+    for bsz in (count, bucket):
+        acc = torch.zeros(count, dtype=torch.float32, device="cuda")
+        d = [torch.from_numpy(a.copy()).cuda() for a in (master, m, v)]
+        half = torch.zeros(count, dtype=torch.int16, device="cuda")
+        flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+        gd = [[dev16(x) for x in micro] for micro in g]
+        for b in range(0, count, bsz):
+            e = min(count, b + bsz)
+            for k in range(2):
+                zs.zs_reduce_check(ctx, [x[b:e] for x in gd[k]], FP16, e - b, acc[b:e], k == 0,
+                                   flag)
+        for b in range(0, count, bsz):
+            e = min(count, b + bsz)
+            zs.zs_apply(ctx, flag, None, FP16, acc[b:e], e - b, n * 2 * 1024.0, d[0][b:e],
+                        d[1][b:e], d[2][b:e], half[b:e], hp, 1)
+        outs.append([acc] + d + [half])
+    for x, y in zip(*outs):
+        assert torch.equal(x, y)
+
+
+def test_argument_errors(zs, ctx):
+    x = torch.zeros(64, dtype=torch.float32, device="cuda")
+    h = torch.zeros(64, dtype=torch.int16, device="cuda")
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    with pytest.raises(zs.ZsError) as e:
+        zs.zs_grad_accum(ctx, [h[1:]], FP16, 8, x, True)
+    assert e.value.status == zs.ZS_ERR_ALIGN
+    with pytest.raises(zs.ZsError) as e:
+        zs.zs_grad_accum(ctx, [h], 7, 8, x, True)
+    assert e.value.status == zs.ZS_ERR_DTYPE
+    with pytest.raises(zs.ZsError) as e:
+        zs.zs_grad_accum(ctx, [], FP16, 8, x, True)
+    assert e.value.status == zs.ZS_ERR_ARG
+    with pytest.raises(zs.ZsError) as e:
+        zs.zs_apply(ctx, flag, None, FP16, x, 8, 1.0, x, x, x, h, zs.make_hparams(1e-3), 0)
+    assert e.value.status == zs.ZS_ERR_ARG
+    assert "step" in zs.lib.zs_last_error(ctx.handle).decode()
+    with pytest.raises(zs.ZsError) as e:
+        zs.zs_grad_accum(ctx, [h] * 257, FP16, 8, x, True)
+    assert e.value.status == zs.ZS_ERR_ARG
+
+
+def test_copy_probe_copies(zs, ctx):
+    src = torch.arange(1 << 20, dtype=torch.int32, device="cuda")
+    dst = torch.zeros_like(src)
+    zs.zs_copy_peak(ctx, src, dst, src.numel() * 4, False)
+    assert torch.equal(src, dst)
+    zs.zs_copy_peak(ctx, src, dst, src.numel() * 4, True)

@@ -441,3 +441,16 @@ def test_flat_workload_scale_trajectory_small():
     assert flags == [0, 0, 0, 0, 1, 0, 0, 0, 0, 0]
     assert sc.scale == 2.0 ** 15 and t == 9
     assert math.isfinite(float(np.abs(states[0].master).max()))
+
+
+def test_bf16_sum_past_fp32_max_is_an_overflow():
+    # two finite bf16 values near 3e38 sum past the fp32 maximum: the step skips
+    hp = oracle.make_hparams(1e-4, 0.9, 0.999, 1e-8, 0.0)
+    st = oracle.ShardState.from_master(np.array([0.5, 0.25], np.float32), BF16)
+    before = st.copy()
+    big = _h([3.0e38, 1.0], BF16)
+    assert oracle.any_nonfinite([big, big], BF16, 2) == 0
+    sc = oracle.make_scaler(1.0, dynamic=False)
+    ovf, t, acc = oracle.shard_step([[big, big]], BF16, st, hp, 0, sc)
+    assert ovf == 1 and t == 0 and np.isinf(acc[0])
+    assert st.master.tobytes() == before.master.tobytes()

@@ -1,0 +1,296 @@
+"""Python binding of libzeroshard (the C ABI in include/zeroshard.h).
+
+Argument marshalling only: every call goes to the CUDA library, whose
+kernels do all of the work.  Tensors are torch CUDA tensors (or raw device
+addresses as ints); streams are torch streams, raw handles, or None for the
+current torch stream.  Importing this module fails loudly if the library has
+not been built (see build()); there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_ROOT = os.path.dirname(_HERE)
+LIB_PATH = os.path.join(_HERE, "libzeroshard.so")
+HEADER = os.path.join(_ROOT, "include", "zeroshard.h")
+SOURCES = [os.path.join(_HERE, "csrc", "zeroshard.cu"), os.path.join(_HERE, "csrc", "zs_kernels.cuh"),
+           HEADER]
+
+ZS_OK, ZS_ERR_ARG, ZS_ERR_ALIGN, ZS_ERR_DTYPE, ZS_ERR_CUDA, ZS_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
+ZS_FP16, ZS_BF16 = 0, 1
+ZS_MAX_RANKS = 256
+ZS_DEFAULT_ALIGN = 64
+(ZS_KERNEL_REDUCE, ZS_KERNEL_CHECK, ZS_KERNEL_APPLY, ZS_KERNEL_APPLY_RECOMPUTE, ZS_KERNEL_SCALER,
+ ZS_KERNEL_COPY) = range(6)
+KERNEL_NAMES = ["reduce", "check", "apply", "apply_recompute", "scaler", "copy"]
+_STATUS = {0: "ZS_OK", -1: "ZS_ERR_ARG", -2: "ZS_ERR_ALIGN", -3: "ZS_ERR_DTYPE", -4: "ZS_ERR_CUDA",
+           -5: "ZS_ERR_TIMEOUT"}
+
+
+def build_cmd(out: str = LIB_PATH):
+    return ["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo",
+            "-std=c++17", "-I", os.path.join(_ROOT, "include"), "-Xcompiler", "-fPIC", "-shared",
+            "-o", out, SOURCES[0]]
+
+
+def build(force: bool = False) -> str:
+    """Compile libzeroshard.so in-tree with nvcc for sm_103a."""
+    stale = not os.path.exists(LIB_PATH) or any(
+        os.path.getmtime(s) > os.path.getmtime(LIB_PATH) for s in SOURCES)
+    if force or stale:
+        tmp = LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(build_cmd(tmp))
+        os.replace(tmp, LIB_PATH)
+    return LIB_PATH
+
+
+class ZsError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{_STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+class zs_partition(ctypes.Structure):
+    _fields_ = [("psi", ctypes.c_int64), ("psi_pad", ctypes.c_int64),
+                ("shard_len", ctypes.c_int64), ("n", ctypes.c_int32), ("align", ctypes.c_int32)]
+
+
+class zs_adam_hparams(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
+                ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float)]
+
+
+class zs_scaler(ctypes.Structure):
+    _fields_ = [("scale", ctypes.c_float), ("min_scale", ctypes.c_float),
+                ("window", ctypes.c_int32), ("clean_count", ctypes.c_int32),
+                ("hysteresis", ctypes.c_int32), ("hyst_left", ctypes.c_int32),
+                ("dynamic", ctypes.c_int32)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with zero_mixed_precision_shard_gb300.build() "
+            "or __graft_entry__.build(); there is no CPU fallback")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+    i64p, i32p, u64p = (ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32),
+                        ctypes.POINTER(ctypes.c_uint64))
+    pp = ctypes.POINTER(ctypes.c_void_p)
+    sig = {
+        "zs_init_partition": [i64, i32, i32, ctypes.POINTER(zs_partition)],
+        "zs_shard_range": [ctypes.POINTER(zs_partition), i32, i64p, i64p, i64p],
+        "zs_model_state_bytes": [ctypes.POINTER(zs_partition), i32, u64p],
+        "zs_scaler_init": [ctypes.POINTER(zs_scaler), f32, f32, i32, i32, i32],
+        "zs_ctx_create": [ctypes.POINTER(vp)],
+        "zs_ctx_destroy": [vp],
+        "zs_ctx_overflow_flag": [vp, ctypes.POINTER(vp)],
+        "zs_grad_accum": [vp, pp, i32, i32, i64, vp, i32, vp],
+        "zs_reduce_check": [vp, pp, i32, i32, i64, vp, i32, vp, vp],
+        "zs_apply": [vp, vp, pp, i32, i32, vp, i64, f32, vp, vp, vp, vp,
+                     ctypes.POINTER(zs_adam_hparams), i64, vp],
+        "zs_scaler_update": [vp, vp, ctypes.POINTER(zs_scaler), i32p, vp],
+        "zs_shard_step": [vp, pp, i32, i32, i64, vp, i32, vp, vp, vp, vp,
+                          ctypes.POINTER(zs_adam_hparams), i64, ctypes.POINTER(zs_scaler), i32p,
+                          ctypes.POINTER(ctypes.c_float), vp],
+        "zs_copy_peak": [vp, vp, vp, i64, i32, vp],
+        "zs_ctx_set_timing": [vp, i32],
+        "zs_ctx_timing": [vp, i32, ctypes.POINTER(ctypes.c_double), i64p, i64p],
+        "zs_ctx_timing_reset": [vp],
+        "zs_ctx_launch_count": [vp, i64p],
+    }
+    for name, args in sig.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    L.zs_last_error.argtypes = [vp]
+    L.zs_last_error.restype = ctypes.c_char_p
+    return L
+
+
+lib = _load()
+
+
+def _addr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _ptrs(tensors):
+    arr = (ctypes.c_void_p * len(tensors))()
+    for i, t in enumerate(tensors):
+        arr[i] = _addr(t)
+    return arr
+
+
+def _dtype(dt) -> int:
+    if isinstance(dt, int):
+        return dt
+    s = str(dt)
+    if s in ("fp16", "torch.float16"):
+        return ZS_FP16
+    if s in ("bf16", "torch.bfloat16"):
+        return ZS_BF16
+    raise ValueError(f"unsupported gradient dtype {dt}")
+
+
+class Ctx:
+    """A zs_ctx on the current CUDA device."""
+
+    def __init__(self):
+        h = ctypes.c_void_p()
+        rc = lib.zs_ctx_create(ctypes.byref(h))
+        if rc != ZS_OK:
+            raise ZsError(rc, "zs_ctx_create failed")
+        self.handle = h
+
+    def check(self, rc: int):
+        if rc != ZS_OK:
+            raise ZsError(rc, lib.zs_last_error(self.handle).decode())
+
+    def close(self):
+        if self.handle:
+            lib.zs_ctx_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def overflow_flag_ptr(self) -> int:
+        p = ctypes.c_void_p()
+        self.check(lib.zs_ctx_overflow_flag(self.handle, ctypes.byref(p)))
+        return p.value
+
+    def set_timing(self, enable: bool):
+        self.check(lib.zs_ctx_set_timing(self.handle, 1 if enable else 0))
+
+    def timing(self, kind: int):
+        ms, n, el = ctypes.c_double(), ctypes.c_int64(), ctypes.c_int64()
+        self.check(lib.zs_ctx_timing(self.handle, kind, ctypes.byref(ms), ctypes.byref(n),
+                                     ctypes.byref(el)))
+        return ms.value, n.value, el.value
+
+    def timing_reset(self):
+        self.check(lib.zs_ctx_timing_reset(self.handle))
+
+    @property
+    def launch_count(self) -> int:
+        n = ctypes.c_int64()
+        self.check(lib.zs_ctx_launch_count(self.handle, ctypes.byref(n)))
+        return n.value
+
+
+@dataclass
+class Partition:
+    psi: int
+    psi_pad: int
+    shard_len: int
+    n: int
+    align: int
+
+    def _c(self):
+        return zs_partition(self.psi, self.psi_pad, self.shard_len, self.n, self.align)
+
+
+def zs_init_partition(psi: int, n: int, align_elems: int = ZS_DEFAULT_ALIGN) -> Partition:
+    p = zs_partition()
+    rc = lib.zs_init_partition(psi, n, align_elems, ctypes.byref(p))
+    if rc != ZS_OK:
+        raise ZsError(rc, f"zs_init_partition({psi}, {n}, {align_elems})")
+    return Partition(p.psi, p.psi_pad, p.shard_len, p.n, p.align)
+
+
+def zs_shard_range(p: Partition, rank: int):
+    b, ve, pe = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    cp = p._c()
+    rc = lib.zs_shard_range(ctypes.byref(cp), rank, ctypes.byref(b), ctypes.byref(ve),
+                            ctypes.byref(pe))
+    if rc != ZS_OK:
+        raise ZsError(rc, f"zs_shard_range(rank={rank})")
+    return b.value, ve.value, pe.value
+
+
+def zs_model_state_bytes(p: Partition, stage: int) -> int:
+    out = ctypes.c_uint64()
+    cp = p._c()
+    rc = lib.zs_model_state_bytes(ctypes.byref(cp), stage, ctypes.byref(out))
+    if rc != ZS_OK:
+        raise ZsError(rc, f"zs_model_state_bytes(stage={stage})")
+    return out.value
+
+
+def zs_scaler_init(scale: float, min_scale: float = 1.0, window: int = 1000,
+                   hysteresis: int = 2, dynamic: bool = True) -> zs_scaler:
+    s = zs_scaler()
+    rc = lib.zs_scaler_init(ctypes.byref(s), scale, min_scale, window, hysteresis,
+                            1 if dynamic else 0)
+    if rc != ZS_OK:
+        raise ZsError(rc, "zs_scaler_init")
+    return s
+
+
+def make_hparams(lr, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0) -> zs_adam_hparams:
+    return zs_adam_hparams(lr, beta1, beta2, eps, weight_decay)
+
+
+def zs_grad_accum(ctx: Ctx, grads, dt, count: int, acc, first: bool, stream=None):
+    ctx.check(lib.zs_grad_accum(ctx.handle, _ptrs(grads), len(grads), _dtype(dt), count,
+                                _addr(acc), 1 if first else 0, _stream(stream)))
+
+
+def zs_reduce_check(ctx: Ctx, grads, dt, count: int, acc, first: bool, d_flag, stream=None):
+    ctx.check(lib.zs_reduce_check(ctx.handle, _ptrs(grads), len(grads), _dtype(dt), count,
+                                  _addr(acc), 1 if first else 0, _addr(d_flag), _stream(stream)))
+
+
+def zs_apply(ctx: Ctx, d_flag, grads, dt, acc, count: int, grad_div: float, master, m, v,
+             half_out, hp: zs_adam_hparams, step: int, stream=None):
+    g = _ptrs(grads) if grads is not None else None
+    n = len(grads) if grads is not None else 0
+    ctx.check(lib.zs_apply(ctx.handle, _addr(d_flag), g, n, _dtype(dt), _addr(acc), count,
+                           grad_div, _addr(master), _addr(m), _addr(v), _addr(half_out),
+                           ctypes.byref(hp), step, _stream(stream)))
+
+
+def zs_scaler_update(ctx: Ctx, d_flag, scaler: zs_scaler, stream=None) -> int:
+    ovf = ctypes.c_int32()
+    ctx.check(lib.zs_scaler_update(ctx.handle, _addr(d_flag), ctypes.byref(scaler),
+                                   ctypes.byref(ovf), _stream(stream)))
+    return ovf.value
+
+
+def zs_shard_step(ctx: Ctx, grads, dt, count: int, acc, accum_steps: int, master, m, v,
+                  half_out, hp: zs_adam_hparams, step: int, scaler: zs_scaler, stream=None):
+    """Returns (overflow, new_scale); *scaler is updated in place."""
+    ovf = ctypes.c_int32()
+    ns = ctypes.c_float()
+    ctx.check(lib.zs_shard_step(ctx.handle, _ptrs(grads), len(grads), _dtype(dt), count,
+                                _addr(acc), accum_steps, _addr(master), _addr(m), _addr(v),
+                                _addr(half_out), ctypes.byref(hp), step, ctypes.byref(scaler),
+                                ctypes.byref(ovf), ctypes.byref(ns), _stream(stream)))
+    return ovf.value, ns.value
+
+
+def zs_copy_peak(ctx: Ctx, src, dst, nbytes: int, read_only: bool = False, stream=None):
+    ctx.check(lib.zs_copy_peak(ctx.handle, _addr(src), _addr(dst), nbytes,
+                               1 if read_only else 0, _stream(stream)))

@@ -1,0 +1,569 @@
+// C ABI of the ZeRO shard step (declarations and contracts in zeroshard.h):
+// argument checks, launch shapes, the per-step host/device handshake and the
+// optional per-kernel event timing.  Every step of the arithmetic runs in
+// the kernels of zs_kernels.cuh.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <unordered_map>
+#include <vector>
+
+#include "zeroshard.h"
+#include "zs_kernels.cuh"
+
+struct zs_ctx {
+  int device = 0;
+  int sms = 0;
+  int32_t* d_flag = nullptr;          // the step's overflow flag
+  zs::StepResult* d_result = nullptr;  // written by the loss-scale update
+  zs::StepResult* h_result = nullptr;  // pinned mirror
+  std::string err;
+  std::unordered_map<const void*, int> occupancy;  // resident CTAs per SM, per kernel
+  int64_t launches = 0;
+  // timing
+  bool timing = false;
+  struct Rec {
+    int kind;
+    cudaEvent_t start, stop;
+    int64_t elements;
+  };
+  std::vector<Rec> pending;
+  std::vector<cudaEvent_t> pool;
+  double total_ms[ZS_KERNEL_KINDS] = {};
+  int64_t total_launches[ZS_KERNEL_KINDS] = {};
+  int64_t total_elements[ZS_KERNEL_KINDS] = {};
+};
+
+namespace {
+
+zs_status fail(zs_ctx* c, zs_status code, const char* fmt, ...) {
+  if (c != nullptr) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    c->err = buf;
+  }
+  return code;
+}
+
+zs_status cuda_fail(zs_ctx* c, cudaError_t e, const char* what) {
+  return fail(c, ZS_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+cudaEvent_t take_event(zs_ctx* c) {
+  if (!c->pool.empty()) {
+    cudaEvent_t e = c->pool.back();
+    c->pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Bracket one launch with events when timing is on.
+struct LaunchScope {
+  zs_ctx* c;
+  cudaStream_t s;
+  int kind;
+  int64_t elements;
+  cudaEvent_t start = nullptr;
+  LaunchScope(zs_ctx* c_, cudaStream_t s_, int kind_, int64_t el)
+      : c(c_), s(s_), kind(kind_), elements(el) {
+    if (c->timing) {
+      start = take_event(c);
+      if (start) cudaEventRecord(start, s);
+    }
+  }
+  void done() {
+    c->launches += 1;
+    if (c->timing && start) {
+      cudaEvent_t stop = take_event(c);
+      if (stop) {
+        cudaEventRecord(stop, s);
+        c->pending.push_back({kind, start, stop, elements});
+      } else {
+        c->pool.push_back(start);
+      }
+    }
+  }
+};
+
+template <typename K>
+int grid_for(zs_ctx* c, K kernel, int64_t items) {
+  const void* key = reinterpret_cast<const void*>(kernel);
+  auto it = c->occupancy.find(key);
+  int per_sm;
+  if (it == c->occupancy.end()) {
+    per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, zs::kThreads, 0) !=
+            cudaSuccess ||
+        per_sm < 1)
+      per_sm = 1;
+    c->occupancy.emplace(key, per_sm);
+  } else {
+    per_sm = it->second;
+  }
+  const int64_t cap = (int64_t)per_sm * c->sms;
+  int64_t need = (items + zs::kThreads - 1) / zs::kThreads;
+  if (need < 1) need = 1;
+  return (int)(need < cap ? need : cap);
+}
+
+zs_status check_ctx(zs_ctx* c) {
+  if (c == nullptr) return ZS_ERR_ARG;
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(c, e, "cudaGetDevice");
+  if (dev != c->device)
+    return fail(c, ZS_ERR_ARG, "current device %d is not the context's device %d", dev,
+                c->device);
+  c->err.clear();
+  return ZS_OK;
+}
+
+zs_status check_slices(zs_ctx* c, const void* const* grads, int32_t n, int64_t count,
+                       zs::SlicePtrs* out) {
+  if (n < 1 || n > ZS_MAX_RANKS)
+    return fail(c, ZS_ERR_ARG, "n = %d is outside [1, %d]", n, ZS_MAX_RANKS);
+  if (grads == nullptr) return fail(c, ZS_ERR_ARG, "grads is NULL");
+  std::memset(out, 0, sizeof(*out));
+  for (int r = 0; r < n; ++r) {
+    if (count > 0 && grads[r] == nullptr) return fail(c, ZS_ERR_ARG, "grads[%d] is NULL", r);
+    if (!aligned16(grads[r]))
+      return fail(c, ZS_ERR_ALIGN, "grads[%d] is not 16-byte aligned", r);
+    out->p[r] = static_cast<const uint4*>(grads[r]);
+  }
+  return ZS_OK;
+}
+
+zs_status check_array(zs_ctx* c, const void* p, const char* name, int64_t count) {
+  if (count > 0 && p == nullptr) return fail(c, ZS_ERR_ARG, "%s is NULL", name);
+  if (!aligned16(p)) return fail(c, ZS_ERR_ALIGN, "%s is not 16-byte aligned", name);
+  return ZS_OK;
+}
+
+#define ZS_TRY(x)                       \
+  do {                                  \
+    zs_status st_ = (x);                \
+    if (st_ != ZS_OK) return st_;       \
+  } while (0)
+
+template <int DT>
+zs_status launch_reduce(zs_ctx* c, const zs::SlicePtrs& sp, int32_t n, float* acc, int64_t count,
+                        bool read_acc, bool store, int32_t* flag, cudaStream_t s) {
+  const int64_t items = (count >> 3) > 7 ? (count >> 3) : 8;
+  const int kind = store ? ZS_KERNEL_REDUCE : ZS_KERNEL_CHECK;
+  LaunchScope ls(c, s, kind, count);
+  if (read_acc && store) {
+    auto k = zs::k_reduce<DT, true, true>;
+    k<<<grid_for(c, k, items), zs::kThreads, 0, s>>>(sp, n, acc, count, flag);
+  } else if (store) {
+    auto k = zs::k_reduce<DT, false, true>;
+    k<<<grid_for(c, k, items), zs::kThreads, 0, s>>>(sp, n, acc, count, flag);
+  } else if (read_acc) {
+    auto k = zs::k_reduce<DT, true, false>;
+    k<<<grid_for(c, k, items), zs::kThreads, 0, s>>>(sp, n, acc, count, flag);
+  } else {
+    auto k = zs::k_reduce<DT, false, false>;
+    k<<<grid_for(c, k, items), zs::kThreads, 0, s>>>(sp, n, acc, count, flag);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(c, e, "reduce launch");
+  ls.done();
+  return ZS_OK;
+}
+
+zs_status reduce_any(zs_ctx* c, zs_dtype dt, const zs::SlicePtrs& sp, int32_t n, float* acc,
+                     int64_t count, bool read_acc, bool store, int32_t* flag, cudaStream_t s) {
+  if (dt == ZS_FP16) return launch_reduce<ZS_FP16>(c, sp, n, acc, count, read_acc, store, flag, s);
+  return launch_reduce<ZS_BF16>(c, sp, n, acc, count, read_acc, store, flag, s);
+}
+
+zs::AdamArgs adam_args(const zs_adam_hparams* hp, int64_t step, float grad_div) {
+  zs::AdamArgs a;
+  a.lr = hp->lr;
+  a.beta1 = hp->beta1;
+  a.omb1 = 1.0f - hp->beta1;
+  a.beta2 = hp->beta2;
+  a.omb2 = 1.0f - hp->beta2;
+  a.eps = hp->eps;
+  a.wd = hp->weight_decay;
+  const double t = (double)step;
+  a.inv_bc1 = (float)(1.0 / (1.0 - std::pow((double)hp->beta1, t)));
+  a.inv_bc2 = (float)(1.0 / (1.0 - std::pow((double)hp->beta2, t)));
+  a.grad_div = grad_div;
+  return a;
+}
+
+template <int DT>
+zs_status launch_apply(zs_ctx* c, const int32_t* flag, const zs::SlicePtrs& sp, int32_t n,
+                       bool recompute, const float* acc, int64_t count, const zs::AdamArgs& ad,
+                       float* master, float* m, float* v, void* half_out,
+                       const zs_scaler* scaler_in, zs::StepResult* result, cudaStream_t s) {
+  const int64_t items = (count >> 3) > 7 ? (count >> 3) : 8;
+  zs_scaler sc_in{};
+  if (scaler_in) sc_in = *scaler_in;
+  uint16_t* ho = static_cast<uint16_t*>(half_out);
+  LaunchScope ls(c, s, recompute ? ZS_KERNEL_APPLY_RECOMPUTE : ZS_KERNEL_APPLY, count);
+  const bool has_acc = acc != nullptr;
+  if (!recompute) {
+    auto k = zs::k_apply<DT, true, false>;
+    k<<<grid_for(c, k, items), zs::kThreads, 0, s>>>(flag, sp, n, acc, master, m, v, ho, count,
+                                                      ad, sc_in, result);
+  } else if (has_acc) {
+    auto k = zs::k_apply<DT, true, true>;
+    k<<<grid_for(c, k, items), zs::kThreads, 0, s>>>(flag, sp, n, acc, master, m, v, ho, count,
+                                                      ad, sc_in, result);
+  } else {
+    auto k = zs::k_apply<DT, false, true>;
+    k<<<grid_for(c, k, items), zs::kThreads, 0, s>>>(flag, sp, n, acc, master, m, v, ho, count,
+                                                      ad, sc_in, result);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(c, e, "apply launch");
+  ls.done();
+  return ZS_OK;
+}
+
+zs_status apply_any(zs_ctx* c, zs_dtype dt, const int32_t* flag, const zs::SlicePtrs& sp,
+                    int32_t n, bool recompute, const float* acc, int64_t count,
+                    const zs::AdamArgs& ad, float* master, float* m, float* v, void* half_out,
+                    const zs_scaler* scaler_in, zs::StepResult* result, cudaStream_t s) {
+  if (dt == ZS_FP16)
+    return launch_apply<ZS_FP16>(c, flag, sp, n, recompute, acc, count, ad, master, m, v,
+                                 half_out, scaler_in, result, s);
+  return launch_apply<ZS_BF16>(c, flag, sp, n, recompute, acc, count, ad, master, m, v, half_out,
+                               scaler_in, result, s);
+}
+
+zs_status check_hparams(zs_ctx* c, const zs_adam_hparams* hp, int64_t step) {
+  if (hp == nullptr) return fail(c, ZS_ERR_ARG, "hparams is NULL");
+  if (step < 1) return fail(c, ZS_ERR_ARG, "step must be >= 1 (got %lld)", (long long)step);
+  if (!(hp->beta1 >= 0.0f && hp->beta1 < 1.0f) || !(hp->beta2 >= 0.0f && hp->beta2 < 1.0f))
+    return fail(c, ZS_ERR_ARG, "betas must lie in [0, 1)");
+  if (!(hp->eps > 0.0f) || !std::isfinite(hp->lr) || !std::isfinite(hp->weight_decay))
+    return fail(c, ZS_ERR_ARG, "eps must be > 0 and lr, weight_decay finite");
+  return ZS_OK;
+}
+
+zs_status check_scaler(zs_ctx* c, const zs_scaler* s) {
+  if (s == nullptr) return fail(c, ZS_ERR_ARG, "scaler is NULL");
+  if (!(s->scale > 0.0f) || !std::isfinite(s->scale) || !(s->min_scale > 0.0f) ||
+      s->window < 1 || s->hysteresis < 1)
+    return fail(c, ZS_ERR_ARG, "scaler needs scale > 0, min_scale > 0, window >= 1, hysteresis >= 1");
+  return ZS_OK;
+}
+
+zs_status finish_step(zs_ctx* c, zs_scaler* scaler, int32_t* overflow_out, float* new_scale_out,
+                      int32_t* flag_to_clear, cudaStream_t s) {
+  cudaError_t e = cudaMemcpyAsync(c->h_result, c->d_result, sizeof(zs::StepResult),
+                                  cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return cuda_fail(c, e, "result copy");
+  if (flag_to_clear) {
+    e = cudaMemsetAsync(flag_to_clear, 0, sizeof(int32_t), s);
+    if (e != cudaSuccess) return cuda_fail(c, e, "flag reset");
+  }
+  e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(c, e, "step synchronisation");
+  *scaler = c->h_result->scaler;
+  if (overflow_out) *overflow_out = c->h_result->overflow;
+  if (new_scale_out) *new_scale_out = c->h_result->scaler.scale;
+  return ZS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+zs_status zs_init_partition(int64_t psi, int32_t n, int32_t align_elems, zs_partition* out) {
+  if (out == nullptr || psi < 0 || n < 1 || n > ZS_MAX_RANKS || align_elems < 1) return ZS_ERR_ARG;
+  const int64_t unit = (int64_t)n * align_elems;
+  if (psi > INT64_MAX - unit) return ZS_ERR_ARG;
+  const int64_t psi_pad = (psi + unit - 1) / unit * unit;
+  out->psi = psi;
+  out->psi_pad = psi_pad;
+  out->shard_len = psi_pad / n;
+  out->n = n;
+  out->align = align_elems;
+  return ZS_OK;
+}
+
+zs_status zs_shard_range(const zs_partition* p, int32_t rank, int64_t* begin, int64_t* valid_end,
+                         int64_t* padded_end) {
+  if (p == nullptr || begin == nullptr || valid_end == nullptr || padded_end == nullptr ||
+      rank < 0 || rank >= p->n)
+    return ZS_ERR_ARG;
+  const int64_t b = (int64_t)rank * p->shard_len;
+  const int64_t e = b + p->shard_len;
+  int64_t ve = e < p->psi ? e : p->psi;
+  if (ve < b) ve = b;
+  *begin = b;
+  *valid_end = ve;
+  *padded_end = e;
+  return ZS_OK;
+}
+
+zs_status zs_model_state_bytes(const zs_partition* p, int32_t stage, uint64_t* bytes) {
+  if (p == nullptr || bytes == nullptr) return ZS_ERR_ARG;
+  const uint64_t P = (uint64_t)p->psi, E = (uint64_t)p->shard_len;
+  const uint64_t half = 2, full = 4;  // bytes per element
+  switch (stage) {
+    case 0: *bytes = (half + half + 3 * full) * P; return ZS_OK;
+    case 1: *bytes = (half + half) * P + 3 * full * E; return ZS_OK;
+    case 2: *bytes = half * P + (half + 3 * full) * E; return ZS_OK;
+    case 3: *bytes = (half + half + 3 * full) * E; return ZS_OK;
+    default: return ZS_ERR_ARG;
+  }
+}
+
+zs_status zs_scaler_init(zs_scaler* s, float scale, float min_scale, int32_t window,
+                         int32_t hysteresis, int32_t dynamic) {
+  if (s == nullptr || !(scale > 0.0f) || !(min_scale > 0.0f) || window < 1 || hysteresis < 1)
+    return ZS_ERR_ARG;
+  s->scale = scale;
+  s->min_scale = min_scale;
+  s->window = window;
+  s->clean_count = 0;
+  s->hysteresis = hysteresis;
+  s->hyst_left = hysteresis;
+  s->dynamic = dynamic ? 1 : 0;
+  return ZS_OK;
+}
+
+zs_status zs_ctx_create(zs_ctx** out) {
+  if (out == nullptr) return ZS_ERR_ARG;
+  *out = nullptr;
+  zs_ctx* c = new zs_ctx();
+  cudaError_t e = cudaGetDevice(&c->device);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&c->sms, cudaDevAttrMultiProcessorCount, c->device);
+  if (e == cudaSuccess) e = cudaMalloc(&c->d_flag, sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMemset(c->d_flag, 0, sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMalloc(&c->d_result, sizeof(zs::StepResult));
+  if (e == cudaSuccess) e = cudaMemset(c->d_result, 0, sizeof(zs::StepResult));
+  if (e == cudaSuccess) e = cudaMallocHost(&c->h_result, sizeof(zs::StepResult));
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    if (c->d_flag) cudaFree(c->d_flag);
+    if (c->d_result) cudaFree(c->d_result);
+    if (c->h_result) cudaFreeHost(c->h_result);
+    delete c;
+    return ZS_ERR_CUDA;
+  }
+  *out = c;
+  return ZS_OK;
+}
+
+zs_status zs_ctx_destroy(zs_ctx* c) {
+  if (c == nullptr) return ZS_ERR_ARG;
+  for (auto& r : c->pending) {
+    cudaEventSynchronize(r.stop);
+    cudaEventDestroy(r.start);
+    cudaEventDestroy(r.stop);
+  }
+  for (auto ev : c->pool) cudaEventDestroy(ev);
+  cudaFree(c->d_flag);
+  cudaFree(c->d_result);
+  cudaFreeHost(c->h_result);
+  delete c;
+  return ZS_OK;
+}
+
+const char* zs_last_error(const zs_ctx* c) { return c ? c->err.c_str() : "null context"; }
+
+zs_status zs_ctx_overflow_flag(zs_ctx* c, int32_t** d_flag) {
+  if (c == nullptr || d_flag == nullptr) return ZS_ERR_ARG;
+  *d_flag = c->d_flag;
+  return ZS_OK;
+}
+
+zs_status zs_reduce_check(zs_ctx* c, const void* const* grads, int32_t n, zs_dtype dt,
+                          int64_t count, float* acc, int32_t first, int32_t* d_flag,
+                          cudaStream_t stream) {
+  ZS_TRY(check_ctx(c));
+  if (dt != ZS_FP16 && dt != ZS_BF16) return fail(c, ZS_ERR_DTYPE, "unknown dtype %d", (int)dt);
+  if (count < 0) return fail(c, ZS_ERR_ARG, "count < 0");
+  if (d_flag == nullptr) return fail(c, ZS_ERR_ARG, "d_flag is NULL");
+  zs::SlicePtrs sp;
+  ZS_TRY(check_slices(c, grads, n, count, &sp));
+  ZS_TRY(check_array(c, acc, "acc", 0));
+  if (count == 0) return ZS_OK;
+  if (acc == nullptr && !first)
+    return fail(c, ZS_ERR_ARG, "a check-only call (acc == NULL) must have first = 1");
+  return reduce_any(c, dt, sp, n, acc, count, acc != nullptr && !first, acc != nullptr, d_flag,
+                    stream);
+}
+
+zs_status zs_grad_accum(zs_ctx* c, const void* const* grads, int32_t n, zs_dtype dt,
+                        int64_t count, float* acc, int32_t first, cudaStream_t stream) {
+  ZS_TRY(check_ctx(c));
+  if (count > 0 && acc == nullptr) return fail(c, ZS_ERR_ARG, "acc is NULL");
+  return zs_reduce_check(c, grads, n, dt, count, acc, first, c->d_flag, stream);
+}
+
+zs_status zs_apply(zs_ctx* c, const int32_t* d_flag, const void* const* grads, int32_t n,
+                   zs_dtype dt, const float* acc, int64_t count, float grad_div, float* master,
+                   float* m, float* v, void* half_out, const zs_adam_hparams* hp, int64_t step,
+                   cudaStream_t stream) {
+  ZS_TRY(check_ctx(c));
+  if (dt != ZS_FP16 && dt != ZS_BF16) return fail(c, ZS_ERR_DTYPE, "unknown dtype %d", (int)dt);
+  if (count < 0) return fail(c, ZS_ERR_ARG, "count < 0");
+  if (d_flag == nullptr) return fail(c, ZS_ERR_ARG, "d_flag is NULL");
+  if (!(grad_div > 0.0f) || !std::isfinite(grad_div))
+    return fail(c, ZS_ERR_ARG, "grad_div must be a positive finite number");
+  ZS_TRY(check_hparams(c, hp, step));
+  zs::SlicePtrs sp;
+  std::memset(&sp, 0, sizeof sp);
+  const bool recompute = grads != nullptr;
+  if (recompute) ZS_TRY(check_slices(c, grads, n, count, &sp));
+  if (!recompute && count > 0 && acc == nullptr)
+    return fail(c, ZS_ERR_ARG, "need acc, grads or both");
+  ZS_TRY(check_array(c, acc, "acc", 0));
+  ZS_TRY(check_array(c, master, "master", count));
+  ZS_TRY(check_array(c, m, "m", count));
+  ZS_TRY(check_array(c, v, "v", count));
+  ZS_TRY(check_array(c, half_out, "half_out", count));
+  if (count == 0) return ZS_OK;
+  const zs::AdamArgs ad = adam_args(hp, step, grad_div);
+  return apply_any(c, dt, d_flag, sp, recompute ? n : 0, recompute, acc, count, ad, master, m, v,
+                   half_out, nullptr, nullptr, stream);
+}
+
+zs_status zs_scaler_update(zs_ctx* c, const int32_t* d_flag, zs_scaler* scaler,
+                           int32_t* overflow_out, cudaStream_t stream) {
+  ZS_TRY(check_ctx(c));
+  if (d_flag == nullptr) return fail(c, ZS_ERR_ARG, "d_flag is NULL");
+  ZS_TRY(check_scaler(c, scaler));
+  LaunchScope ls(c, stream, ZS_KERNEL_SCALER, 1);
+  zs::k_scaler<<<1, 32, 0, stream>>>(d_flag, *scaler, c->d_result);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(c, e, "scaler launch");
+  ls.done();
+  return finish_step(c, scaler, overflow_out, nullptr, nullptr, stream);
+}
+
+zs_status zs_shard_step(zs_ctx* c, const void* const* grads, int32_t n, zs_dtype dt,
+                        int64_t count, float* acc, int32_t accum_steps, float* master, float* m,
+                        float* v, void* half_out, const zs_adam_hparams* hp, int64_t step,
+                        zs_scaler* scaler, int32_t* overflow_out, float* new_scale_out,
+                        cudaStream_t stream) {
+  ZS_TRY(check_ctx(c));
+  if (dt != ZS_FP16 && dt != ZS_BF16) return fail(c, ZS_ERR_DTYPE, "unknown dtype %d", (int)dt);
+  if (count < 0) return fail(c, ZS_ERR_ARG, "count < 0");
+  if (accum_steps < 1) return fail(c, ZS_ERR_ARG, "accum_steps must be >= 1");
+  if (accum_steps > 1 && acc == nullptr && count > 0)
+    return fail(c, ZS_ERR_ARG, "acc is required when accum_steps > 1");
+  ZS_TRY(check_hparams(c, hp, step));
+  ZS_TRY(check_scaler(c, scaler));
+  zs::SlicePtrs sp;
+  ZS_TRY(check_slices(c, grads, n, count, &sp));
+  ZS_TRY(check_array(c, acc, "acc", 0));
+  ZS_TRY(check_array(c, master, "master", count));
+  ZS_TRY(check_array(c, m, "m", count));
+  ZS_TRY(check_array(c, v, "v", count));
+  ZS_TRY(check_array(c, half_out, "half_out", count));
+  const double div = (double)n * (double)accum_steps * (double)scaler->scale;
+  const float grad_div = (float)div;
+  if (!(grad_div > 0.0f) || !std::isfinite(grad_div))
+    return fail(c, ZS_ERR_ARG, "n * accum_steps * scale is not a positive finite fp32");
+  const zs::AdamArgs ad = adam_args(hp, step, grad_div);
+  const bool recompute = (n < 4) || acc == nullptr;
+  if (count > 0) {
+    if (recompute) {
+      // fp16: finite halves cannot sum past the fp32 maximum, so a check of
+      // the last slices alone decides; bf16 sums on top of acc as the update will.
+      const bool with_acc = (dt == ZS_BF16) && accum_steps > 1;
+      ZS_TRY(reduce_any(c, dt, sp, n, with_acc ? acc : nullptr, count, with_acc, false, c->d_flag,
+                        stream));
+    } else {
+      ZS_TRY(reduce_any(c, dt, sp, n, acc, count, accum_steps > 1, true, c->d_flag, stream));
+    }
+  }
+  ZS_TRY(apply_any(c, dt, c->d_flag, sp, recompute ? n : 0, recompute,
+                   accum_steps > 1 || !recompute ? acc : nullptr, count, ad, master, m, v,
+                   half_out, scaler, c->d_result, stream));
+  return finish_step(c, scaler, overflow_out, new_scale_out, c->d_flag, stream);
+}
+
+zs_status zs_copy_peak(zs_ctx* c, const void* src, void* dst, int64_t bytes, int32_t read_only,
+                       cudaStream_t stream) {
+  ZS_TRY(check_ctx(c));
+  if (bytes < 0 || bytes % 16 != 0) return fail(c, ZS_ERR_ARG, "bytes must be a multiple of 16");
+  ZS_TRY(check_array(c, src, "src", bytes));
+  ZS_TRY(check_array(c, dst, "dst", 1));
+  if (bytes == 0) return ZS_OK;
+  const int64_t nvec = bytes / 16;
+  LaunchScope ls(c, stream, ZS_KERNEL_COPY, bytes);
+  if (read_only) {
+    zs::k_read<<<grid_for(c, zs::k_read, nvec / 4 + 1), zs::kThreads, 0, stream>>>(
+        static_cast<const uint4*>(src), nvec, static_cast<uint4*>(dst), 0x9E3779B9u);
+  } else {
+    zs::k_copy<<<grid_for(c, zs::k_copy, nvec / 4 + 1), zs::kThreads, 0, stream>>>(
+        static_cast<const uint4*>(src), static_cast<uint4*>(dst), nvec);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(c, e, "copy launch");
+  ls.done();
+  return ZS_OK;
+}
+
+zs_status zs_ctx_set_timing(zs_ctx* c, int32_t enable) {
+  if (c == nullptr) return ZS_ERR_ARG;
+  c->timing = enable != 0;
+  return ZS_OK;
+}
+
+static zs_status drain_timing(zs_ctx* c) {
+  for (auto& r : c->pending) {
+    cudaError_t e = cudaEventSynchronize(r.stop);
+    if (e != cudaSuccess) return cuda_fail(c, e, "event synchronise");
+    float ms = 0.0f;
+    e = cudaEventElapsedTime(&ms, r.start, r.stop);
+    if (e != cudaSuccess) return cuda_fail(c, e, "event elapsed time");
+    c->total_ms[r.kind] += ms;
+    c->total_launches[r.kind] += 1;
+    c->total_elements[r.kind] += r.elements;
+    c->pool.push_back(r.start);
+    c->pool.push_back(r.stop);
+  }
+  c->pending.clear();
+  return ZS_OK;
+}
+
+zs_status zs_ctx_timing(zs_ctx* c, int32_t kind, double* total_ms, int64_t* launches,
+                        int64_t* elements) {
+  if (c == nullptr || kind < 0 || kind >= ZS_KERNEL_KINDS) return ZS_ERR_ARG;
+  ZS_TRY(drain_timing(c));
+  if (total_ms) *total_ms = c->total_ms[kind];
+  if (launches) *launches = c->total_launches[kind];
+  if (elements) *elements = c->total_elements[kind];
+  return ZS_OK;
+}
+
+zs_status zs_ctx_timing_reset(zs_ctx* c) {
+  if (c == nullptr) return ZS_ERR_ARG;
+  ZS_TRY(drain_timing(c));
+  for (int k = 0; k < ZS_KERNEL_KINDS; ++k) {
+    c->total_ms[k] = 0.0;
+    c->total_launches[k] = 0;
+    c->total_elements[k] = 0;
+  }
+  return ZS_OK;
+}
+
+zs_status zs_ctx_launch_count(const zs_ctx* c, int64_t* launches) {
+  if (c == nullptr || launches == nullptr) return ZS_ERR_ARG;
+  *launches = c->launches;
+  return ZS_OK;
+}
+
+}  // extern "C"
