@@ -10,15 +10,9 @@ from __future__ import annotations
 
 import ctypes
 import os
-import subprocess
 from dataclasses import dataclass
 
-_HERE = os.path.dirname(os.path.abspath(__file__))
-_ROOT = os.path.dirname(_HERE)
-LIB_PATH = os.path.join(_HERE, "libzeroshard.so")
-HEADER = os.path.join(_ROOT, "include", "zeroshard.h")
-SOURCES = [os.path.join(_HERE, "csrc", "zeroshard.cu"), os.path.join(_HERE, "csrc", "zs_kernels.cuh"),
-           HEADER]
+from ._build import HEADER, LIB_PATH, SOURCES, build, build_cmd  # noqa: F401,E402
 
 ZS_OK, ZS_ERR_ARG, ZS_ERR_ALIGN, ZS_ERR_DTYPE, ZS_ERR_CUDA, ZS_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
 ZS_FP16, ZS_BF16 = 0, 1
@@ -29,23 +23,6 @@ ZS_DEFAULT_ALIGN = 64
 KERNEL_NAMES = ["reduce", "check", "apply", "apply_recompute", "scaler", "copy"]
 _STATUS = {0: "ZS_OK", -1: "ZS_ERR_ARG", -2: "ZS_ERR_ALIGN", -3: "ZS_ERR_DTYPE", -4: "ZS_ERR_CUDA",
            -5: "ZS_ERR_TIMEOUT"}
-
-
-def build_cmd(out: str = LIB_PATH):
-    return ["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo",
-            "-std=c++17", "-I", os.path.join(_ROOT, "include"), "-Xcompiler", "-fPIC", "-shared",
-            "-o", out, SOURCES[0]]
-
-
-def build(force: bool = False) -> str:
-    """Compile libzeroshard.so in-tree with nvcc for sm_103a."""
-    stale = not os.path.exists(LIB_PATH) or any(
-        os.path.getmtime(s) > os.path.getmtime(LIB_PATH) for s in SOURCES)
-    if force or stale:
-        tmp = LIB_PATH + f".tmp{os.getpid()}"
-        subprocess.check_call(build_cmd(tmp))
-        os.replace(tmp, LIB_PATH)
-    return LIB_PATH
 
 
 class ZsError(RuntimeError):
