@@ -332,10 +332,11 @@ def run_ours(args):
     ctx = zs.Ctx()
     probe = copy_probe(zs, ctx) if not args.skip_probe else {}
 
-    W = DeviceWorkload(wl, shard=0)
+    W = DeviceWorkload(wl, shard=0, count=args.elements)
     W.fill_grads(1, wl.scale0, inject=False)
     torch.cuda.synchronize()
-    E, valid = W.E, W.valid_end - W.begin
+    E = W.E
+    valid = min(W.valid_end - W.begin, E)
     flag = torch.zeros(1, dtype=torch.int32, device="cuda") if world > 1 else None
 
     def one_step():
@@ -426,7 +427,8 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
             "config": {
-                "workload": wl.name, "params": wl.psi, "owned_params": valid,
+                "workload": wl.name + (f" (first {E} elements)" if args.elements else ""),
+                "params": wl.psi, "owned_params": valid,
                 "shard_len": E, "n_ranks_simulated": wl.n, "accum_steps": wl.g,
                 "grad_dtype": wl.dtype, "optimizer": "AdamW" if wl.weight_decay else "Adam",
                 "parallelism": "replicas + overflow-flag all-reduce" if world > 1 else "1 GPU",
@@ -496,7 +498,7 @@ def run_e2e(zs, ctx, W: DeviceWorkload, steps: int):
     b.record()
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
-    valid = W.valid_end - W.begin
+    valid = min(W.valid_end - W.begin, W.E)
     h2d = wl.g * wl.n * W.E * 2
     return {"value": valid / (ms * 1e-3), "unit": "params/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": 8, "ms_per_step": ms, "steps": steps,
@@ -515,6 +517,8 @@ def main(argv=None):
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-probe", action="store_true")
+    ap.add_argument("--elements", type=int, default=None,
+                    help="truncate the owned shard to its first ELEMENTS elements (profiling)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

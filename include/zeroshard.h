@@ -123,8 +123,9 @@ zs_status zs_scaler_init(zs_scaler* s, float scale, float min_scale, int32_t win
 /* ---------------------------------------------------------------- context */
 
 /* Create a context on the current CUDA device.  It owns: the step's overflow
- * flag (a device int32, zero at creation), a device result word and a pinned
- * host mirror.  *ctx is set to NULL on failure. */
+ * flag (a device int32, zero at creation), a device result word, 32 KB of
+ * scratch for the clipping norm's partial sums, and pinned host mirrors.
+ * *ctx is set to NULL on failure. */
 zs_status zs_ctx_create(zs_ctx** ctx);
 zs_status zs_ctx_destroy(zs_ctx* ctx);
 /* Message of the last failed call on ctx ("" if none).  Valid until the next call. */
@@ -192,6 +193,44 @@ zs_status zs_shard_step(zs_ctx* ctx, const void* const* grads, int32_t n, zs_dty
                         zs_scaler* scaler, int32_t* overflow_out, float* new_scale_out,
                         cudaStream_t stream);
 
+/* ---------------------------------------------------------------- clipping */
+
+/* Global-norm gradient clipping (§4.1 gradient_clipping; §5.1: engine.step()
+ * includes gradient clipping).  The pages give the knob, not the formula; the
+ * usual one is used: norm = L2 norm of the averaged, unscaled gradient of the
+ * whole model; coef = max_norm / (norm + 1e-6) if that is below 1, else 1;
+ * the update uses g * coef.
+ *
+ * Phase 1b (after the flag phase, before phase 2): *d_sumsq (device fp64) =
+ *   sum over i in [0, count) of ((acc[i] or +0) + grads[0][i] + ... +
+ *   grads[n-1][i])^2 / grad_div^2,
+ * with grads == NULL when the sums are already in acc.  Deterministic (fixed
+ * summation order for a given count and device).  A caller holding several
+ * shards, buckets or GPUs adds their values (an all-reduce) before phase 2.
+ * Uses the context's scratch (per-CTA partial sums). */
+zs_status zs_grad_sumsq(zs_ctx* ctx, const void* const* grads, int32_t n, zs_dtype dt,
+                        const float* acc, int64_t count, float grad_div, double* d_sumsq,
+                        cudaStream_t stream);
+
+/* Phase 2 with clipping: zs_apply with g multiplied by the coefficient
+ * computed on the device from *d_sumsq and max_norm (max_norm <= 0: no
+ * clipping). */
+zs_status zs_apply_clipped(zs_ctx* ctx, const int32_t* d_flag, const double* d_sumsq,
+                           float max_norm, const void* const* grads, int32_t n, zs_dtype dt,
+                           const float* acc, int64_t count, float grad_div, float* master,
+                           float* m, float* v, void* half_out, const zs_adam_hparams* hp,
+                           int64_t step, cudaStream_t stream);
+
+/* zs_shard_step with global-norm clipping, where the owned shard holds the
+ * whole gradient whose norm is clipped (one rank; or a caller that clips per
+ * shard).  *grad_norm_out (may be NULL) gets the norm, 0 on a skipped step. */
+zs_status zs_shard_step_clipped(zs_ctx* ctx, const void* const* grads, int32_t n, zs_dtype dt,
+                                int64_t count, float* acc, int32_t accum_steps, float* master,
+                                float* m, float* v, void* half_out, const zs_adam_hparams* hp,
+                                int64_t step, zs_scaler* scaler, float max_norm,
+                                int32_t* overflow_out, float* new_scale_out,
+                                float* grad_norm_out, cudaStream_t stream);
+
 /* ---------------------------------------------------------------- measurement */
 
 /* HBM roofline probe: copy `bytes` from src to dst (read_only = 0), or only
@@ -208,7 +247,8 @@ typedef enum {
   ZS_KERNEL_APPLY_RECOMPUTE = 3, /* AdamW + cast, re-reading the last slices */
   ZS_KERNEL_SCALER = 4,          /* standalone loss-scale update */
   ZS_KERNEL_COPY = 5,            /* roofline probe */
-  ZS_KERNEL_KINDS = 6
+  ZS_KERNEL_SUMSQ = 6,           /* clipping: sum of squares (+ its finalize) */
+  ZS_KERNEL_KINDS = 7
 } zs_kernel_kind;
 
 /* When enabled, each launch is bracketed by CUDA events on its stream. */

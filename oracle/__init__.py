@@ -92,11 +92,20 @@ def lib():
     L.zso_adamw_apply.argtypes = [_f32p, ctypes.c_int64, ctypes.c_double, _f32p, _f32p, _f32p,
                                   _u16p, ctypes.c_int32, ctypes.POINTER(HParams), ctypes.c_int64]
     L.zso_scaler_update.argtypes = [ctypes.POINTER(Scaler), ctypes.c_int32]
+    L.zso_grad_sumsq.argtypes = [_f32p, ctypes.c_int64, ctypes.c_double]
+    L.zso_grad_sumsq.restype = ctypes.c_double
+    L.zso_clip_coef.argtypes = [ctypes.c_double, ctypes.c_double]
+    L.zso_clip_coef.restype = ctypes.c_double
+    L.zso_adamw_apply_clipped.argtypes = [_f32p, ctypes.c_int64, ctypes.c_double, ctypes.c_double,
+                                          _f32p, _f32p, _f32p, _u16p, ctypes.c_int32,
+                                          ctypes.POINTER(HParams), ctypes.c_int64]
     L.zso_shard_step.argtypes = [PP, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                  ctypes.c_int64, _f32p, _f32p, _f32p, _f32p, _u16p,
                                  ctypes.POINTER(HParams), _i64p, ctypes.POINTER(Scaler),
                                  ctypes.c_int32]
     L.zso_shard_step.restype = ctypes.c_int32
+    L.zso_shard_step_clipped.argtypes = L.zso_shard_step.argtypes + [ctypes.c_double, _f64p]
+    L.zso_shard_step_clipped.restype = ctypes.c_int32
     _lib = L
     return L
 
@@ -184,6 +193,24 @@ def adamw_apply(acc, grad_div, master, m, v, half_out, dtype, hp: HParams, t: in
                           ctypes.byref(hp), t)
 
 
+def grad_sumsq(acc: np.ndarray, grad_div: float) -> float:
+    _check_f32(acc)
+    return float(lib().zso_grad_sumsq(_p(acc, _f32p), acc.shape[0], float(grad_div)))
+
+
+def clip_coef(sumsq_total: float, max_norm: float) -> float:
+    return float(lib().zso_clip_coef(float(sumsq_total), float(max_norm)))
+
+
+def adamw_apply_clipped(acc, grad_div, coef, master, m, v, half_out, dtype, hp: HParams, t: int):
+    for a in (acc, master, m, v):
+        _check_f32(a)
+    _check_u16(half_out)
+    lib().zso_adamw_apply_clipped(_p(acc, _f32p), acc.shape[0], float(grad_div), float(coef),
+                                  _p(master, _f32p), _p(m, _f32p), _p(v, _f32p),
+                                  _p(half_out, _u16p), dtype, ctypes.byref(hp), t)
+
+
 def scaler_update(sc: Scaler, overflow: int):
     lib().zso_scaler_update(ctypes.byref(sc), int(overflow))
 
@@ -207,23 +234,29 @@ class ShardState:
 
 
 def shard_step(grads, dtype: int, state: ShardState, hp: HParams, t: int, sc: Scaler,
-               extra_overflow: int = 0):
+               extra_overflow: int = 0, max_norm: float = 0.0, return_norm: bool = False):
     """One step of one owned-shard view.  grads[k][r] = rank r's slice in
-    micro-step k.  Returns (overflow, new t, acc)."""
+    micro-step k.  Returns (overflow, new t, acc) (and the gradient norm when
+    return_norm)."""
     g = len(grads)
     n = len(grads[0])
     count = state.master.shape[0]
     flat = [s for micro in grads for s in micro]
     acc = np.zeros(count, dtype=np.float32)
     tt = ctypes.c_int64(t)
-    ovf = lib().zso_shard_step(_ptr_array(flat), g, n, dtype, count, _p(acc, _f32p),
-                               _p(state.master, _f32p), _p(state.m, _f32p), _p(state.v, _f32p),
-                               _p(state.half, _u16p), ctypes.byref(hp), ctypes.byref(tt),
-                               ctypes.byref(sc), int(extra_overflow))
+    norm = ctypes.c_double(0.0)
+    ovf = lib().zso_shard_step_clipped(_ptr_array(flat), g, n, dtype, count, _p(acc, _f32p),
+                                       _p(state.master, _f32p), _p(state.m, _f32p),
+                                       _p(state.v, _f32p), _p(state.half, _u16p),
+                                       ctypes.byref(hp), ctypes.byref(tt), ctypes.byref(sc),
+                                       int(extra_overflow), float(max_norm), ctypes.byref(norm))
+    if return_norm:
+        return int(ovf), tt.value, acc, norm.value
     return int(ovf), tt.value, acc
 
 
-def multi_shard_step(grads_per_shard, dtype: int, states, hp: HParams, t: int, sc: Scaler):
+def multi_shard_step(grads_per_shard, dtype: int, states, hp: HParams, t: int, sc: Scaler,
+                     max_norm: float = 0.0):
     """One step of all N ranks' shards with a global overflow flag (every
     rank skips together): reduce each shard, OR the flags, then update every
     shard with the same step count and scale, then update the scale once.
@@ -242,8 +275,11 @@ def multi_shard_step(grads_per_shard, dtype: int, states, hp: HParams, t: int, s
         t += 1
         n = len(grads_per_shard[0][0])
         g = len(grads_per_shard[0])
+        div = float(n) * g * sc.scale
+        coef = 1.0
+        if max_norm > 0:
+            coef = clip_coef(sum(grad_sumsq(a, div) for a in accs), max_norm)
         for q, st in enumerate(states):
-            adamw_apply(accs[q], float(n) * g * sc.scale, st.master, st.m, st.v, st.half, dtype,
-                        hp, t)
+            adamw_apply_clipped(accs[q], div, coef, st.master, st.m, st.v, st.half, dtype, hp, t)
     scaler_update(sc, flag)
     return flag, t, accs

@@ -166,14 +166,14 @@ int32_t zso_any_nonfinite_f32(const float* x, int64_t count) {
 
 /* ---- AdamW on the fp32 master shard, then the half copy (§2.1, §4.1) ---- */
 
-void zso_adamw_apply(const float* acc, int64_t count, double grad_div, float* master, float* m,
-                     float* v, uint16_t* half_out, int32_t dtype, const zso_hparams* hp,
-                     int64_t t) {
+void zso_adamw_apply_clipped(const float* acc, int64_t count, double grad_div, double coef,
+                             float* master, float* m, float* v, uint16_t* half_out,
+                             int32_t dtype, const zso_hparams* hp, int64_t t) {
   const double b1 = hp->beta1, b2 = hp->beta2;
   const double bc1 = 1.0 - pow(b1, (double)t);
   const double bc2 = 1.0 - pow(b2, (double)t);
   for (int64_t i = 0; i < count; ++i) {
-    double g = (double)acc[i] / grad_div; /* unscale and average */
+    double g = (double)acc[i] / grad_div * coef; /* unscale, average, clip */
     double p = (double)master[i];
     double m1 = b1 * (double)m[i] + (1.0 - b1) * g;
     double v1 = b2 * (double)v[i] + (1.0 - b2) * g * g;
@@ -185,6 +185,27 @@ void zso_adamw_apply(const float* acc, int64_t count, double grad_div, float* ma
     v[i] = (float)v1;
     half_out[i] = zso_f32_to_half(master[i], dtype);
   }
+}
+
+void zso_adamw_apply(const float* acc, int64_t count, double grad_div, float* master, float* m,
+                     float* v, uint16_t* half_out, int32_t dtype, const zso_hparams* hp,
+                     int64_t t) {
+  zso_adamw_apply_clipped(acc, count, grad_div, 1.0, master, m, v, half_out, dtype, hp, t);
+}
+
+double zso_grad_sumsq(const float* acc, int64_t count, double grad_div) {
+  double s = 0.0;
+  for (int64_t i = 0; i < count; ++i) {
+    double g = (double)acc[i] / grad_div;
+    s += g * g;
+  }
+  return s;
+}
+
+double zso_clip_coef(double sumsq_total, double max_norm) {
+  if (!(max_norm > 0.0)) return 1.0;
+  double c = max_norm / (sqrt(sumsq_total) + 1e-6);
+  return c < 1.0 ? c : 1.0;
 }
 
 /* ---- dynamic loss scale (§4.2) ------------------------------------------ */
@@ -213,21 +234,37 @@ void zso_scaler_update(zso_scaler* s, int32_t overflow) {
 
 /* ---- one step of one owned shard ---------------------------------------- */
 
-int32_t zso_shard_step(const uint16_t* const* grads, int32_t g, int32_t n, int32_t dtype,
-                       int64_t count, float* acc, float* master, float* m, float* v,
-                       uint16_t* half_out, const zso_hparams* hp, int64_t* t, zso_scaler* sc,
-                       int32_t extra_overflow) {
+int32_t zso_shard_step_clipped(const uint16_t* const* grads, int32_t g, int32_t n, int32_t dtype,
+                               int64_t count, float* acc, float* master, float* m, float* v,
+                               uint16_t* half_out, const zso_hparams* hp, int64_t* t,
+                               zso_scaler* sc, int32_t extra_overflow, double max_norm,
+                               double* norm_out) {
   for (int32_t k = 0; k < g; ++k) zso_reduce_accumulate(grads + (size_t)k * n, n, dtype, count,
                                                         acc, k == 0);
   int32_t ovf = extra_overflow != 0;
   for (int32_t k = 0; k < g && !ovf; ++k) ovf = zso_any_nonfinite(grads + (size_t)k * n, n,
                                                                   dtype, count);
   if (!ovf) ovf = zso_any_nonfinite_f32(acc, count);
+  if (norm_out) *norm_out = 0.0;
   if (!ovf) {
     *t += 1;
-    zso_adamw_apply(acc, count, (double)n * (double)g * sc->scale, master, m, v, half_out, dtype,
-                    hp, *t);
+    const double div = (double)n * (double)g * sc->scale;
+    double coef = 1.0;
+    if (max_norm > 0.0) {
+      const double sumsq = zso_grad_sumsq(acc, count, div);
+      coef = zso_clip_coef(sumsq, max_norm);
+      if (norm_out) *norm_out = sqrt(sumsq);
+    }
+    zso_adamw_apply_clipped(acc, count, div, coef, master, m, v, half_out, dtype, hp, *t);
   }
   zso_scaler_update(sc, ovf);
   return ovf;
+}
+
+int32_t zso_shard_step(const uint16_t* const* grads, int32_t g, int32_t n, int32_t dtype,
+                       int64_t count, float* acc, float* master, float* m, float* v,
+                       uint16_t* half_out, const zso_hparams* hp, int64_t* t, zso_scaler* sc,
+                       int32_t extra_overflow) {
+  return zso_shard_step_clipped(grads, g, n, dtype, count, acc, master, m, v, half_out, hp, t,
+                                sc, extra_overflow, 0.0, NULL);
 }

@@ -97,6 +97,18 @@ void zso_adamw_apply(const float* acc, int64_t count, double grad_div, float* ma
                      float* v, uint16_t* half_out, int32_t dtype, const zso_hparams* hp, int64_t t);
 void zso_scaler_update(zso_scaler* s, int32_t overflow);
 
+/* Global-norm gradient clipping (§4.1 gradient_clipping, §5.1 "step() includes
+ * gradient clipping"; the formula is the usual one, not printed on the pages):
+ * sumsq = sum over the range of (acc[i] / grad_div)^2 in fp64, index order;
+ * the norm of the whole model is the square root of the sum over all shards;
+ * coef = max_norm / (norm + 1e-6) if that is below 1, else 1 (max_norm <= 0:
+ * no clipping); the update then uses g = acc[i] / grad_div * coef. */
+double zso_grad_sumsq(const float* acc, int64_t count, double grad_div);
+double zso_clip_coef(double sumsq_total, double max_norm);
+void zso_adamw_apply_clipped(const float* acc, int64_t count, double grad_div, double coef,
+                             float* master, float* m, float* v, uint16_t* half_out,
+                             int32_t dtype, const zso_hparams* hp, int64_t t);
+
 /* One optimizer step of one owned-shard view.  grads holds g*n pointers,
  * micro-step major: grads[k*n + r] is rank r's slice in micro-step k.
  * extra_overflow is OR'd into the step's flag (other shards' flags).
@@ -105,6 +117,15 @@ int32_t zso_shard_step(const uint16_t* const* grads, int32_t g, int32_t n, int32
                        int64_t count, float* acc, float* master, float* m, float* v,
                        uint16_t* half_out, const zso_hparams* hp, int64_t* t, zso_scaler* sc,
                        int32_t extra_overflow);
+
+/* zso_shard_step with global-norm clipping over this view (the view is the
+ * whole model, or the caller accepts the view's own norm); *norm_out gets the
+ * gradient norm (0 on a skipped step). */
+int32_t zso_shard_step_clipped(const uint16_t* const* grads, int32_t g, int32_t n, int32_t dtype,
+                               int64_t count, float* acc, float* master, float* m, float* v,
+                               uint16_t* half_out, const zso_hparams* hp, int64_t* t,
+                               zso_scaler* sc, int32_t extra_overflow, double max_norm,
+                               double* norm_out);
 
 #ifdef __cplusplus
 }

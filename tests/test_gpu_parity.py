@@ -203,7 +203,8 @@ def test_apply_recompute_matches_oracle(zs, ctx, dtype, with_acc):
 
 # ---------------------------------------------------------------- whole steps
 
-def run_shard_steps(zs, ctx, dtype, n, G, count, steps, seed, inject=None, acc_mode="auto"):
+def run_shard_steps(zs, ctx, dtype, n, G, count, steps, seed, inject=None, acc_mode="auto",
+                    window=3, hysteresis=1):
     """Drive zs_grad_accum + zs_shard_step on the GPU and oracle.shard_step on
     the host for `steps` steps; the oracle's scale drives input generation."""
     rng = np.random.default_rng(seed)
@@ -212,8 +213,8 @@ def run_shard_steps(zs, ctx, dtype, n, G, count, steps, seed, inject=None, acc_m
     hp_vals = (1e-3, 0.9, 0.999, 1e-8, 0.01)
     hp_o = oracle.make_hparams(*hp_vals)
     dynamic = dtype == FP16
-    sc_o = oracle.make_scaler(1024.0 if dynamic else 1.0, 1.0, 3, 1, dynamic)
-    sc = zs.zs_scaler_init(sc_o.scale, 1.0, 3, 1, dynamic)
+    sc_o = oracle.make_scaler(1024.0 if dynamic else 1.0, 1.0, window, hysteresis, dynamic)
+    sc = zs.zs_scaler_init(sc_o.scale, 1.0, window, hysteresis, dynamic)
     hp = zs.make_hparams(*hp_vals)
     master = torch.from_numpy(master0.copy()).cuda()
     m = torch.zeros_like(master)
@@ -258,6 +259,16 @@ def test_shard_step_sequence(zs, ctx, dtype, n, G, count):
                                                       else 0x7FC0)}
     flags, _ = run_shard_steps(zs, ctx, dtype, n, G, count, 10, seed=n * 100 + G, inject=inject)
     assert flags == [0, 0, 1, 0, 1, 0, 0, 0, 0, 0]
+
+
+def test_hysteresis_two(zs, ctx):
+    """hysteresis 2: the scale halves on every second overflow since the last
+    decrease; the device scaler must follow the oracle's step by step."""
+    inf = 0x7C00
+    inject = {s: (0, 0, 17, inf) for s in (1, 3, 4, 5, 9)}
+    flags, _ = run_shard_steps(zs, ctx, FP16, 2, 1, 1001, 10, seed=3, inject=inject, window=2,
+                               hysteresis=2)
+    assert flags == [1, 0, 1, 1, 1, 0, 0, 0, 1, 0]
 
 
 @pytest.mark.parametrize("n", [4, 8])

@@ -454,3 +454,74 @@ def test_bf16_sum_past_fp32_max_is_an_overflow():
     ovf, t, acc = oracle.shard_step([[big, big]], BF16, st, hp, 0, sc)
     assert ovf == 1 and t == 0 and np.isinf(acc[0])
     assert st.master.tobytes() == before.master.tobytes()
+
+
+# ---------------------------------------------------------------- clipping
+
+def test_clip_coefficient_closed_form():
+    # n equal gradients c: norm = |c|·sqrt(n); coef = max_norm / (norm + 1e-6) when below 1
+    n, c, div = 400, 0.0625, 2.0 ** 18
+    acc = np.full(n, c * div, np.float32)
+    sumsq = oracle.grad_sumsq(acc, div)
+    assert abs(sumsq - n * c * c) <= 1e-12 * n * c * c
+    norm = c * math.sqrt(n)  # 1.25
+    assert abs(oracle.clip_coef(sumsq, 0.25) - 0.25 / (norm + 1e-6)) < 1e-15
+    assert oracle.clip_coef(sumsq, 2.0) == 1.0        # under the limit: untouched
+    assert oracle.clip_coef(sumsq, 0.0) == 1.0        # disabled
+
+
+def test_clipped_first_step_moments():
+    # t=1 from m=v=0: m1 = (1-β1)·ĝ·coef and v1 = (1-β2)·(ĝ·coef)², coef from the whole vector
+    hp = oracle.make_hparams(1e-3, 0.9, 0.999, 1e-8, 0.0)
+    rng = np.random.default_rng(12)
+    ghat = rng.standard_normal(1000) * 0.1
+    div = 1024.0
+    acc = (ghat * div).astype(np.float32)
+    ghat = acc.astype(np.float64) / div
+    norm = math.sqrt(float((ghat ** 2).sum()))
+    coef = 0.5 / (norm + 1e-6)
+    assert coef < 1
+    st = oracle.ShardState.from_master(np.zeros(1000, np.float32), FP16)
+    sumsq = oracle.grad_sumsq(acc, div)
+    oracle.adamw_apply_clipped(acc, div, oracle.clip_coef(sumsq, 0.5), st.master, st.m, st.v,
+                               st.half, FP16, hp, 1)
+    want_m = (1 - hp.beta1) * ghat * coef
+    want_v = (1 - hp.beta2) * (ghat * coef) ** 2
+    assert np.all(np.abs(st.m - want_m) <= 1e-6 * np.abs(want_m) + 1e-12)
+    assert np.all(np.abs(st.v - want_v) <= 1e-6 * np.abs(want_v) + 1e-15)
+
+
+def test_unclipped_step_is_bitwise_the_plain_step():
+    rng = np.random.default_rng(13)
+    n, g, count = 2, 2, 777
+    hp = oracle.make_hparams(1e-4, 0.9, 0.999, 1e-8, 0.01)
+    master0 = (rng.standard_normal(count) * 0.02).astype(np.float32)
+    grads = [_rand_slices(rng, n, count, 512.0) for _ in range(g)]
+    a = oracle.ShardState.from_master(master0, FP16)
+    b = oracle.ShardState.from_master(master0, FP16)
+    oracle.shard_step(grads, FP16, a, hp, 0, oracle.make_scaler(512.0))
+    _, _, _, norm = oracle.shard_step(grads, FP16, b, hp, 0, oracle.make_scaler(512.0),
+                                      max_norm=1e9, return_norm=True)
+    assert norm > 0
+    for k in ("master", "m", "v", "half"):
+        assert getattr(a, k).tobytes() == getattr(b, k).tobytes()
+
+
+def test_clipped_shard_union_uses_the_global_norm():
+    rng = np.random.default_rng(14)
+    psi, n = 2048, 4
+    psi_pad, E = oracle.partition(psi, n, 64)
+    hp = oracle.make_hparams(1e-3, 0.9, 0.999, 1e-8, 0.0)
+    master0 = (rng.standard_normal(psi_pad) * 0.02).astype(np.float32)
+    full_g = [[_lib_half((rng.standard_normal(psi_pad) * 0.5 * 256).astype(np.float32), FP16)
+               for _ in range(n)]]
+    whole = oracle.ShardState.from_master(master0, FP16)
+    _, _, _, norm = oracle.shard_step(full_g, FP16, whole, hp, 0, oracle.make_scaler(256.0),
+                                      max_norm=0.1, return_norm=True)
+    assert norm > 0.1   # clipping active
+    shards = [oracle.ShardState.from_master(master0[q * E:(q + 1) * E], FP16) for q in range(n)]
+    per = [[[np.ascontiguousarray(s[q * E:(q + 1) * E]) for s in full_g[0]]] for q in range(n)]
+    oracle.multi_shard_step(per, FP16, shards, hp, 0, oracle.make_scaler(256.0), max_norm=0.1)
+    cat = np.concatenate([s.master for s in shards])
+    # the global norm is a sum of per-shard sums (fp64 grouping may differ in the last bit)
+    assert np.all(np.abs(cat - whole.master) <= np.spacing(np.abs(whole.master)))

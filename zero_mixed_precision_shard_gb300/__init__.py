@@ -19,8 +19,8 @@ ZS_FP16, ZS_BF16 = 0, 1
 ZS_MAX_RANKS = 256
 ZS_DEFAULT_ALIGN = 64
 (ZS_KERNEL_REDUCE, ZS_KERNEL_CHECK, ZS_KERNEL_APPLY, ZS_KERNEL_APPLY_RECOMPUTE, ZS_KERNEL_SCALER,
- ZS_KERNEL_COPY) = range(6)
-KERNEL_NAMES = ["reduce", "check", "apply", "apply_recompute", "scaler", "copy"]
+ ZS_KERNEL_COPY, ZS_KERNEL_SUMSQ) = range(7)
+KERNEL_NAMES = ["reduce", "check", "apply", "apply_recompute", "scaler", "copy", "sumsq"]
 _STATUS = {0: "ZS_OK", -1: "ZS_ERR_ARG", -2: "ZS_ERR_ALIGN", -3: "ZS_ERR_DTYPE", -4: "ZS_ERR_CUDA",
            -5: "ZS_ERR_TIMEOUT"}
 
@@ -75,6 +75,13 @@ def _load():
                           ctypes.POINTER(zs_adam_hparams), i64, ctypes.POINTER(zs_scaler), i32p,
                           ctypes.POINTER(ctypes.c_float), vp],
         "zs_copy_peak": [vp, vp, vp, i64, i32, vp],
+        "zs_grad_sumsq": [vp, pp, i32, i32, vp, i64, f32, vp, vp],
+        "zs_apply_clipped": [vp, vp, vp, f32, pp, i32, i32, vp, i64, f32, vp, vp, vp, vp,
+                             ctypes.POINTER(zs_adam_hparams), i64, vp],
+        "zs_shard_step_clipped": [vp, pp, i32, i32, i64, vp, i32, vp, vp, vp, vp,
+                                  ctypes.POINTER(zs_adam_hparams), i64, ctypes.POINTER(zs_scaler),
+                                  f32, i32p, ctypes.POINTER(ctypes.c_float),
+                                  ctypes.POINTER(ctypes.c_float), vp],
         "zs_ctx_set_timing": [vp, i32],
         "zs_ctx_timing": [vp, i32, ctypes.POINTER(ctypes.c_double), i64p, i64p],
         "zs_ctx_timing_reset": [vp],
@@ -266,6 +273,39 @@ def zs_shard_step(ctx: Ctx, grads, dt, count: int, acc, accum_steps: int, master
                                 _addr(half_out), ctypes.byref(hp), step, ctypes.byref(scaler),
                                 ctypes.byref(ovf), ctypes.byref(ns), _stream(stream)))
     return ovf.value, ns.value
+
+
+def zs_grad_sumsq(ctx: Ctx, grads, dt, acc, count: int, grad_div: float, d_sumsq, stream=None):
+    g = _ptrs(grads) if grads is not None else None
+    n = len(grads) if grads is not None else 0
+    ctx.check(lib.zs_grad_sumsq(ctx.handle, g, n, _dtype(dt), _addr(acc), count, grad_div,
+                                _addr(d_sumsq), _stream(stream)))
+
+
+def zs_apply_clipped(ctx: Ctx, d_flag, d_sumsq, max_norm: float, grads, dt, acc, count: int,
+                     grad_div: float, master, m, v, half_out, hp: zs_adam_hparams, step: int,
+                     stream=None):
+    g = _ptrs(grads) if grads is not None else None
+    n = len(grads) if grads is not None else 0
+    ctx.check(lib.zs_apply_clipped(ctx.handle, _addr(d_flag), _addr(d_sumsq), max_norm, g, n,
+                                   _dtype(dt), _addr(acc), count, grad_div, _addr(master),
+                                   _addr(m), _addr(v), _addr(half_out), ctypes.byref(hp), step,
+                                   _stream(stream)))
+
+
+def zs_shard_step_clipped(ctx: Ctx, grads, dt, count: int, acc, accum_steps: int, master, m, v,
+                          half_out, hp: zs_adam_hparams, step: int, scaler: zs_scaler,
+                          max_norm: float, stream=None):
+    """Returns (overflow, new_scale, grad_norm); *scaler is updated in place."""
+    ovf = ctypes.c_int32()
+    ns = ctypes.c_float()
+    gn = ctypes.c_float()
+    ctx.check(lib.zs_shard_step_clipped(ctx.handle, _ptrs(grads), len(grads), _dtype(dt), count,
+                                        _addr(acc), accum_steps, _addr(master), _addr(m),
+                                        _addr(v), _addr(half_out), ctypes.byref(hp), step,
+                                        ctypes.byref(scaler), max_norm, ctypes.byref(ovf),
+                                        ctypes.byref(ns), ctypes.byref(gn), _stream(stream)))
+    return ovf.value, ns.value, gn.value
 
 
 def zs_copy_peak(ctx: Ctx, src, dst, nbytes: int, read_only: bool = False, stream=None):

@@ -6,7 +6,8 @@ import subprocess
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _ROOT = os.path.dirname(_HERE)
-LIB_PATH = os.path.join(_HERE, "libzeroshard.so")
+# ZEROSHARD_LIB points the binding at another build of the same library.
+LIB_PATH = os.environ.get("ZEROSHARD_LIB", os.path.join(_HERE, "libzeroshard.so"))
 HEADER = os.path.join(_ROOT, "include", "zeroshard.h")
 SOURCES = [os.path.join(_HERE, "csrc", "zeroshard.cu"), os.path.join(_HERE, "csrc", "zs_kernels.cuh"),
            HEADER]

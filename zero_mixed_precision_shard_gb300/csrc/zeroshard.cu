@@ -15,10 +15,17 @@
 #include "zeroshard.h"
 #include "zs_kernels.cuh"
 
+// Capacity of the per-CTA partial sums of the clipping norm (one double each).
+#define ZS_SUMSQ_MAX_PARTS 4096
+
 struct zs_ctx {
   int device = 0;
   int sms = 0;
   int32_t* d_flag = nullptr;          // the step's overflow flag
+  double* d_partials = nullptr;        // scratch: per-CTA sums of squares
+  double* d_sumsq = nullptr;           // the step's squared gradient norm (zs_shard_step_clipped)
+  float* d_coef = nullptr;             // scratch: clipping coefficient
+  double* h_sumsq = nullptr;           // pinned mirror of d_sumsq
   zs::StepResult* d_result = nullptr;  // written by the loss-scale update
   zs::StepResult* h_result = nullptr;  // pinned mirror
   std::string err;
@@ -98,7 +105,7 @@ struct LaunchScope {
 };
 
 template <typename K>
-int grid_for(zs_ctx* c, K kernel, int64_t items) {
+int grid_for(zs_ctx* c, K kernel, int64_t items, int waves = ZS_GRID_WAVES) {
   const void* key = reinterpret_cast<const void*>(kernel);
   auto it = c->occupancy.find(key);
   int per_sm;
@@ -112,10 +119,14 @@ int grid_for(zs_ctx* c, K kernel, int64_t items) {
   } else {
     per_sm = it->second;
   }
-  const int64_t cap = (int64_t)per_sm * c->sms;
   int64_t need = (items + zs::kThreads - 1) / zs::kThreads;
   if (need < 1) need = 1;
-  return (int)(need < cap ? need : cap);
+  if (waves > 0) {
+    const int64_t cap = (int64_t)per_sm * c->sms * waves;
+    if (need > cap) need = cap;
+  }
+  if (need > 0x7fffffff) need = 0x7fffffff;
+  return (int)need;
 }
 
 zs_status check_ctx(zs_ctx* c) {
@@ -157,24 +168,46 @@ zs_status check_array(zs_ctx* c, const void* p, const char* name, int64_t count)
     if (st_ != ZS_OK) return st_;       \
   } while (0)
 
+int vpt_for(int32_t n) {
+  if (n <= 2) return ZS_VPT_SMALL_N;
+  if (n <= 8) return ZS_VPT_MID_N;
+  return 1;
+}
+
+template <int DT, bool RA, bool ST, int VPT>
+void launch_reduce_k(zs_ctx* c, const zs::SlicePtrs& sp, int32_t n, float* acc, int64_t count,
+                     int32_t* flag, cudaStream_t s) {
+  const int64_t units = (count >> 3) / VPT + 8;
+  auto k = zs::k_reduce<DT, RA, ST, VPT>;
+  const int waves = ST ? ZS_GRID_WAVES : ZS_CHECK_WAVES;
+  k<<<grid_for(c, k, units, waves), zs::kThreads, 0, s>>>(sp, n, acc, count, flag);
+}
+
+template <int DT, bool RA, bool ST>
+void launch_reduce_v(zs_ctx* c, const zs::SlicePtrs& sp, int32_t n, float* acc, int64_t count,
+                     int32_t* flag, cudaStream_t s) {
+  const int vpt = (!ST && n <= 2) ? ZS_CHECK_VPT : vpt_for(n);
+  switch (vpt) {
+    case 8: launch_reduce_k<DT, RA, ST, 8>(c, sp, n, acc, count, flag, s); break;
+    case 4: launch_reduce_k<DT, RA, ST, 4>(c, sp, n, acc, count, flag, s); break;
+    case 2: launch_reduce_k<DT, RA, ST, 2>(c, sp, n, acc, count, flag, s); break;
+    default: launch_reduce_k<DT, RA, ST, 1>(c, sp, n, acc, count, flag, s); break;
+  }
+}
+
 template <int DT>
 zs_status launch_reduce(zs_ctx* c, const zs::SlicePtrs& sp, int32_t n, float* acc, int64_t count,
                         bool read_acc, bool store, int32_t* flag, cudaStream_t s) {
-  const int64_t items = (count >> 3) > 7 ? (count >> 3) : 8;
   const int kind = store ? ZS_KERNEL_REDUCE : ZS_KERNEL_CHECK;
   LaunchScope ls(c, s, kind, count);
   if (read_acc && store) {
-    auto k = zs::k_reduce<DT, true, true>;
-    k<<<grid_for(c, k, items), zs::kThreads, 0, s>>>(sp, n, acc, count, flag);
+    launch_reduce_v<DT, true, true>(c, sp, n, acc, count, flag, s);
   } else if (store) {
-    auto k = zs::k_reduce<DT, false, true>;
-    k<<<grid_for(c, k, items), zs::kThreads, 0, s>>>(sp, n, acc, count, flag);
+    launch_reduce_v<DT, false, true>(c, sp, n, acc, count, flag, s);
   } else if (read_acc) {
-    auto k = zs::k_reduce<DT, true, false>;
-    k<<<grid_for(c, k, items), zs::kThreads, 0, s>>>(sp, n, acc, count, flag);
+    launch_reduce_v<DT, true, false>(c, sp, n, acc, count, flag, s);
   } else {
-    auto k = zs::k_reduce<DT, false, false>;
-    k<<<grid_for(c, k, items), zs::kThreads, 0, s>>>(sp, n, acc, count, flag);
+    launch_reduce_v<DT, false, false>(c, sp, n, acc, count, flag, s);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(c, e, "reduce launch");
@@ -204,29 +237,43 @@ zs::AdamArgs adam_args(const zs_adam_hparams* hp, int64_t step, float grad_div) 
   return a;
 }
 
+template <int DT, bool HA, bool RC>
+void launch_apply_k(zs_ctx* c, const int32_t* flag, const zs::SlicePtrs& sp, int32_t n,
+                    const float* acc, int64_t count, const zs::AdamArgs& ad, float* master,
+                    float* m, float* v, uint16_t* ho, const zs_scaler& sc_in,
+                    zs::StepResult* result, const float* coef, cudaStream_t s) {
+  constexpr int VPT = ZS_APPLY_VPT;
+  const int64_t units = (count >> 3) / VPT + 8;
+  if (coef != nullptr) {
+    auto k = zs::k_apply<DT, HA, RC, VPT, true>;
+    k<<<grid_for(c, k, units), zs::kThreads, 0, s>>>(flag, sp, n, acc, master, m, v, ho, count,
+                                                     ad, sc_in, result, coef);
+  } else {
+    auto k = zs::k_apply<DT, HA, RC, VPT, false>;
+    k<<<grid_for(c, k, units), zs::kThreads, 0, s>>>(flag, sp, n, acc, master, m, v, ho, count,
+                                                     ad, sc_in, result, nullptr);
+  }
+}
+
 template <int DT>
 zs_status launch_apply(zs_ctx* c, const int32_t* flag, const zs::SlicePtrs& sp, int32_t n,
                        bool recompute, const float* acc, int64_t count, const zs::AdamArgs& ad,
                        float* master, float* m, float* v, void* half_out,
-                       const zs_scaler* scaler_in, zs::StepResult* result, cudaStream_t s) {
-  const int64_t items = (count >> 3) > 7 ? (count >> 3) : 8;
+                       const zs_scaler* scaler_in, zs::StepResult* result, const float* coef,
+                       cudaStream_t s) {
   zs_scaler sc_in{};
   if (scaler_in) sc_in = *scaler_in;
   uint16_t* ho = static_cast<uint16_t*>(half_out);
   LaunchScope ls(c, s, recompute ? ZS_KERNEL_APPLY_RECOMPUTE : ZS_KERNEL_APPLY, count);
-  const bool has_acc = acc != nullptr;
   if (!recompute) {
-    auto k = zs::k_apply<DT, true, false>;
-    k<<<grid_for(c, k, items), zs::kThreads, 0, s>>>(flag, sp, n, acc, master, m, v, ho, count,
-                                                      ad, sc_in, result);
-  } else if (has_acc) {
-    auto k = zs::k_apply<DT, true, true>;
-    k<<<grid_for(c, k, items), zs::kThreads, 0, s>>>(flag, sp, n, acc, master, m, v, ho, count,
-                                                      ad, sc_in, result);
+    launch_apply_k<DT, true, false>(c, flag, sp, n, acc, count, ad, master, m, v, ho, sc_in,
+                                    result, coef, s);
+  } else if (acc != nullptr) {
+    launch_apply_k<DT, true, true>(c, flag, sp, n, acc, count, ad, master, m, v, ho, sc_in,
+                                   result, coef, s);
   } else {
-    auto k = zs::k_apply<DT, false, true>;
-    k<<<grid_for(c, k, items), zs::kThreads, 0, s>>>(flag, sp, n, acc, master, m, v, ho, count,
-                                                      ad, sc_in, result);
+    launch_apply_k<DT, false, true>(c, flag, sp, n, acc, count, ad, master, m, v, ho, sc_in,
+                                    result, coef, s);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(c, e, "apply launch");
@@ -237,12 +284,57 @@ zs_status launch_apply(zs_ctx* c, const int32_t* flag, const zs::SlicePtrs& sp, 
 zs_status apply_any(zs_ctx* c, zs_dtype dt, const int32_t* flag, const zs::SlicePtrs& sp,
                     int32_t n, bool recompute, const float* acc, int64_t count,
                     const zs::AdamArgs& ad, float* master, float* m, float* v, void* half_out,
-                    const zs_scaler* scaler_in, zs::StepResult* result, cudaStream_t s) {
+                    const zs_scaler* scaler_in, zs::StepResult* result, cudaStream_t s,
+                    const float* coef = nullptr) {
   if (dt == ZS_FP16)
     return launch_apply<ZS_FP16>(c, flag, sp, n, recompute, acc, count, ad, master, m, v,
-                                 half_out, scaler_in, result, s);
+                                 half_out, scaler_in, result, coef, s);
   return launch_apply<ZS_BF16>(c, flag, sp, n, recompute, acc, count, ad, master, m, v, half_out,
-                               scaler_in, result, s);
+                               scaler_in, result, coef, s);
+}
+
+// Sum of squares of the final gradient sums of a range, then / grad_div^2,
+// into *out (device).  Grid capped at ZS_SUMSQ_MAX_PARTS CTAs (one partial each).
+template <int DT, bool HA, bool RC>
+void launch_sumsq_k(zs_ctx* c, const zs::SlicePtrs& sp, int32_t n, const float* acc,
+                    int64_t count, double* partials, int* nparts, cudaStream_t s) {
+  auto k = zs::k_sumsq<DT, HA, RC>;
+  int grid = grid_for(c, k, (count >> 3) + 8, 1);
+  if (grid > ZS_SUMSQ_MAX_PARTS) grid = ZS_SUMSQ_MAX_PARTS;
+  *nparts = grid;
+  k<<<grid, zs::kThreads, 0, s>>>(sp, n, acc, count, partials);
+}
+
+zs_status sumsq_any(zs_ctx* c, zs_dtype dt, const zs::SlicePtrs& sp, int32_t n, bool recompute,
+                    const float* acc, int64_t count, float grad_div, double* partials,
+                    double* out, cudaStream_t s) {
+  LaunchScope ls(c, s, ZS_KERNEL_SUMSQ, count);
+  int nparts = 0;
+  const bool ha = acc != nullptr;
+  if (dt == ZS_FP16) {
+    if (recompute && ha) launch_sumsq_k<ZS_FP16, true, true>(c, sp, n, acc, count, partials, &nparts, s);
+    else if (recompute) launch_sumsq_k<ZS_FP16, false, true>(c, sp, n, acc, count, partials, &nparts, s);
+    else launch_sumsq_k<ZS_FP16, true, false>(c, sp, n, acc, count, partials, &nparts, s);
+  } else {
+    if (recompute && ha) launch_sumsq_k<ZS_BF16, true, true>(c, sp, n, acc, count, partials, &nparts, s);
+    else if (recompute) launch_sumsq_k<ZS_BF16, false, true>(c, sp, n, acc, count, partials, &nparts, s);
+    else launch_sumsq_k<ZS_BF16, true, false>(c, sp, n, acc, count, partials, &nparts, s);
+  }
+  const double div = (double)grad_div;
+  zs::k_sumsq_finalize<<<1, zs::kThreads, 0, s>>>(partials, nparts, 1.0 / (div * div), out);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(c, e, "sumsq launch");
+  ls.done();
+  c->launches += 1;  // the finalize kernel
+  return ZS_OK;
+}
+
+zs_status clip_coef_launch(zs_ctx* c, const double* d_sumsq, float max_norm, cudaStream_t s) {
+  zs::k_clip_coef<<<1, 32, 0, s>>>(d_sumsq, max_norm, c->d_coef);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(c, e, "clip coefficient launch");
+  c->launches += 1;
+  return ZS_OK;
 }
 
 zs_status check_hparams(zs_ctx* c, const zs_adam_hparams* hp, int64_t step) {
@@ -351,11 +443,20 @@ zs_status zs_ctx_create(zs_ctx** out) {
   if (e == cudaSuccess) e = cudaMalloc(&c->d_result, sizeof(zs::StepResult));
   if (e == cudaSuccess) e = cudaMemset(c->d_result, 0, sizeof(zs::StepResult));
   if (e == cudaSuccess) e = cudaMallocHost(&c->h_result, sizeof(zs::StepResult));
+  if (e == cudaSuccess) e = cudaMalloc(&c->d_partials, ZS_SUMSQ_MAX_PARTS * sizeof(double));
+  if (e == cudaSuccess) e = cudaMalloc(&c->d_sumsq, sizeof(double));
+  if (e == cudaSuccess) e = cudaMemset(c->d_sumsq, 0, sizeof(double));
+  if (e == cudaSuccess) e = cudaMalloc(&c->d_coef, sizeof(float));
+  if (e == cudaSuccess) e = cudaMallocHost(&c->h_sumsq, sizeof(double));
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     if (c->d_flag) cudaFree(c->d_flag);
     if (c->d_result) cudaFree(c->d_result);
     if (c->h_result) cudaFreeHost(c->h_result);
+    if (c->d_partials) cudaFree(c->d_partials);
+    if (c->d_sumsq) cudaFree(c->d_sumsq);
+    if (c->d_coef) cudaFree(c->d_coef);
+    if (c->h_sumsq) cudaFreeHost(c->h_sumsq);
     delete c;
     return ZS_ERR_CUDA;
   }
@@ -374,6 +475,10 @@ zs_status zs_ctx_destroy(zs_ctx* c) {
   cudaFree(c->d_flag);
   cudaFree(c->d_result);
   cudaFreeHost(c->h_result);
+  cudaFree(c->d_partials);
+  cudaFree(c->d_sumsq);
+  cudaFree(c->d_coef);
+  cudaFreeHost(c->h_sumsq);
   delete c;
   return ZS_OK;
 }
@@ -451,17 +556,19 @@ zs_status zs_scaler_update(zs_ctx* c, const int32_t* d_flag, zs_scaler* scaler,
   return finish_step(c, scaler, overflow_out, nullptr, nullptr, stream);
 }
 
-zs_status zs_shard_step(zs_ctx* c, const void* const* grads, int32_t n, zs_dtype dt,
-                        int64_t count, float* acc, int32_t accum_steps, float* master, float* m,
-                        float* v, void* half_out, const zs_adam_hparams* hp, int64_t step,
-                        zs_scaler* scaler, int32_t* overflow_out, float* new_scale_out,
-                        cudaStream_t stream) {
+static zs_status shard_step_impl(zs_ctx* c, const void* const* grads, int32_t n, zs_dtype dt,
+                                 int64_t count, float* acc, int32_t accum_steps, float* master,
+                                 float* m, float* v, void* half_out, const zs_adam_hparams* hp,
+                                 int64_t step, zs_scaler* scaler, float max_norm,
+                                 int32_t* overflow_out, float* new_scale_out,
+                                 float* grad_norm_out, cudaStream_t stream) {
   ZS_TRY(check_ctx(c));
   if (dt != ZS_FP16 && dt != ZS_BF16) return fail(c, ZS_ERR_DTYPE, "unknown dtype %d", (int)dt);
   if (count < 0) return fail(c, ZS_ERR_ARG, "count < 0");
   if (accum_steps < 1) return fail(c, ZS_ERR_ARG, "accum_steps must be >= 1");
   if (accum_steps > 1 && acc == nullptr && count > 0)
     return fail(c, ZS_ERR_ARG, "acc is required when accum_steps > 1");
+  if (!std::isfinite(max_norm)) return fail(c, ZS_ERR_ARG, "max_norm must be finite");
   ZS_TRY(check_hparams(c, hp, step));
   ZS_TRY(check_scaler(c, scaler));
   zs::SlicePtrs sp;
@@ -477,6 +584,8 @@ zs_status zs_shard_step(zs_ctx* c, const void* const* grads, int32_t n, zs_dtype
     return fail(c, ZS_ERR_ARG, "n * accum_steps * scale is not a positive finite fp32");
   const zs::AdamArgs ad = adam_args(hp, step, grad_div);
   const bool recompute = (n < 4) || acc == nullptr;
+  const bool clip = max_norm > 0.0f;
+  const float* acc_in = (accum_steps > 1 || !recompute) ? acc : nullptr;
   if (count > 0) {
     if (recompute) {
       // fp16: finite halves cannot sum past the fp32 maximum, so a check of
@@ -488,10 +597,106 @@ zs_status zs_shard_step(zs_ctx* c, const void* const* grads, int32_t n, zs_dtype
       ZS_TRY(reduce_any(c, dt, sp, n, acc, count, accum_steps > 1, true, c->d_flag, stream));
     }
   }
-  ZS_TRY(apply_any(c, dt, c->d_flag, sp, recompute ? n : 0, recompute,
-                   accum_steps > 1 || !recompute ? acc : nullptr, count, ad, master, m, v,
-                   half_out, scaler, c->d_result, stream));
-  return finish_step(c, scaler, overflow_out, new_scale_out, c->d_flag, stream);
+  if (clip) {
+    if (count > 0) {
+      ZS_TRY(sumsq_any(c, dt, sp, recompute ? n : 0, recompute, acc_in, count, grad_div,
+                       c->d_partials, c->d_sumsq, stream));
+    } else {
+      cudaError_t e = cudaMemsetAsync(c->d_sumsq, 0, sizeof(double), stream);
+      if (e != cudaSuccess) return cuda_fail(c, e, "sumsq reset");
+    }
+    ZS_TRY(clip_coef_launch(c, c->d_sumsq, max_norm, stream));
+    cudaError_t e = cudaMemcpyAsync(c->h_sumsq, c->d_sumsq, sizeof(double),
+                                    cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "sumsq copy");
+  }
+  ZS_TRY(apply_any(c, dt, c->d_flag, sp, recompute ? n : 0, recompute, acc_in, count, ad, master,
+                   m, v, half_out, scaler, c->d_result, stream, clip ? c->d_coef : nullptr));
+  ZS_TRY(finish_step(c, scaler, overflow_out, new_scale_out, c->d_flag, stream));
+  if (grad_norm_out) {
+    *grad_norm_out = 0.0f;
+    if (clip && c->h_result->overflow == 0) *grad_norm_out = (float)std::sqrt(*c->h_sumsq);
+  }
+  return ZS_OK;
+}
+
+zs_status zs_shard_step(zs_ctx* c, const void* const* grads, int32_t n, zs_dtype dt,
+                        int64_t count, float* acc, int32_t accum_steps, float* master, float* m,
+                        float* v, void* half_out, const zs_adam_hparams* hp, int64_t step,
+                        zs_scaler* scaler, int32_t* overflow_out, float* new_scale_out,
+                        cudaStream_t stream) {
+  return shard_step_impl(c, grads, n, dt, count, acc, accum_steps, master, m, v, half_out, hp,
+                         step, scaler, 0.0f, overflow_out, new_scale_out, nullptr, stream);
+}
+
+zs_status zs_shard_step_clipped(zs_ctx* c, const void* const* grads, int32_t n, zs_dtype dt,
+                                int64_t count, float* acc, int32_t accum_steps, float* master,
+                                float* m, float* v, void* half_out, const zs_adam_hparams* hp,
+                                int64_t step, zs_scaler* scaler, float max_norm,
+                                int32_t* overflow_out, float* new_scale_out,
+                                float* grad_norm_out, cudaStream_t stream) {
+  return shard_step_impl(c, grads, n, dt, count, acc, accum_steps, master, m, v, half_out, hp,
+                         step, scaler, max_norm, overflow_out, new_scale_out, grad_norm_out,
+                         stream);
+}
+
+zs_status zs_grad_sumsq(zs_ctx* c, const void* const* grads, int32_t n, zs_dtype dt,
+                        const float* acc, int64_t count, float grad_div, double* d_sumsq,
+                        cudaStream_t stream) {
+  ZS_TRY(check_ctx(c));
+  if (dt != ZS_FP16 && dt != ZS_BF16) return fail(c, ZS_ERR_DTYPE, "unknown dtype %d", (int)dt);
+  if (count < 0) return fail(c, ZS_ERR_ARG, "count < 0");
+  if (d_sumsq == nullptr) return fail(c, ZS_ERR_ARG, "d_sumsq is NULL");
+  if (!(grad_div > 0.0f) || !std::isfinite(grad_div))
+    return fail(c, ZS_ERR_ARG, "grad_div must be a positive finite number");
+  zs::SlicePtrs sp;
+  std::memset(&sp, 0, sizeof sp);
+  const bool recompute = grads != nullptr;
+  if (recompute) ZS_TRY(check_slices(c, grads, n, count, &sp));
+  if (!recompute && count > 0 && acc == nullptr)
+    return fail(c, ZS_ERR_ARG, "need acc, grads or both");
+  ZS_TRY(check_array(c, acc, "acc", 0));
+  if (count == 0) {
+    cudaError_t e = cudaMemsetAsync(d_sumsq, 0, sizeof(double), stream);
+    return e == cudaSuccess ? ZS_OK : cuda_fail(c, e, "sumsq reset");
+  }
+  return sumsq_any(c, dt, sp, recompute ? n : 0, recompute, acc, count, grad_div, c->d_partials,
+                   d_sumsq, stream);
+}
+
+zs_status zs_apply_clipped(zs_ctx* c, const int32_t* d_flag, const double* d_sumsq,
+                           float max_norm, const void* const* grads, int32_t n, zs_dtype dt,
+                           const float* acc, int64_t count, float grad_div, float* master,
+                           float* m, float* v, void* half_out, const zs_adam_hparams* hp,
+                           int64_t step, cudaStream_t stream) {
+  ZS_TRY(check_ctx(c));
+  if (!std::isfinite(max_norm)) return fail(c, ZS_ERR_ARG, "max_norm must be finite");
+  if (max_norm <= 0.0f)
+    return zs_apply(c, d_flag, grads, n, dt, acc, count, grad_div, master, m, v, half_out, hp,
+                    step, stream);
+  if (d_sumsq == nullptr) return fail(c, ZS_ERR_ARG, "d_sumsq is NULL");
+  if (dt != ZS_FP16 && dt != ZS_BF16) return fail(c, ZS_ERR_DTYPE, "unknown dtype %d", (int)dt);
+  if (count < 0) return fail(c, ZS_ERR_ARG, "count < 0");
+  if (d_flag == nullptr) return fail(c, ZS_ERR_ARG, "d_flag is NULL");
+  if (!(grad_div > 0.0f) || !std::isfinite(grad_div))
+    return fail(c, ZS_ERR_ARG, "grad_div must be a positive finite number");
+  ZS_TRY(check_hparams(c, hp, step));
+  zs::SlicePtrs sp;
+  std::memset(&sp, 0, sizeof sp);
+  const bool recompute = grads != nullptr;
+  if (recompute) ZS_TRY(check_slices(c, grads, n, count, &sp));
+  if (!recompute && count > 0 && acc == nullptr)
+    return fail(c, ZS_ERR_ARG, "need acc, grads or both");
+  ZS_TRY(check_array(c, acc, "acc", 0));
+  ZS_TRY(check_array(c, master, "master", count));
+  ZS_TRY(check_array(c, m, "m", count));
+  ZS_TRY(check_array(c, v, "v", count));
+  ZS_TRY(check_array(c, half_out, "half_out", count));
+  if (count == 0) return ZS_OK;
+  ZS_TRY(clip_coef_launch(c, d_sumsq, max_norm, stream));
+  const zs::AdamArgs ad = adam_args(hp, step, grad_div);
+  return apply_any(c, dt, d_flag, sp, recompute ? n : 0, recompute, acc, count, ad, master, m, v,
+                   half_out, nullptr, nullptr, stream, c->d_coef);
 }
 
 zs_status zs_copy_peak(zs_ctx* c, const void* src, void* dst, int64_t bytes, int32_t read_only,

@@ -7,11 +7,16 @@
 //  * 16-byte vector accesses (8 half elements, or 2 x 4 fp32) issued by
 //    consecutive threads, so every warp request is 512 contiguous bytes of
 //    each array;
-//  * grid = resident CTAs per SM x SM count, grid-stride loops, so every SM
-//    keeps its full complement of loads in flight across the whole array;
+//  * one thread per 8-element unit (VPT units for the flag-only pass): the
+//    grid covers the array once, CTAs retire and are replaced in address
+//    order, which measured ~13% faster on GB300 than persistent grid-stride
+//    grids of resident-CTAs x 152 SMs (those are kept for the bounded
+//    sum-of-squares pass, whose partials array has a fixed size);
 //  * the rank slices are loaded 8 (or 4) at a time before the ordered adds,
 //    so each thread has up to 8 independent 16-byte loads outstanding;
-//  * read-once gradient slices use evict-first loads (ld.global.cs);
+//  * read-once gradient slices, the accumulator and the optimizer state use
+//    evict-first loads/stores (ld/st.global.cs): nothing is re-read within L2
+//    lifetime at the sizes that matter;
 //  * the N rank pointers travel as a __grid_constant__ parameter block, read
 //    from the constant bank without a local-memory copy;
 //  * the overflow flag is a CTA-wide OR (__syncthreads_or) and one atomicOr
@@ -30,9 +35,43 @@
 
 #include "zeroshard.h"
 
+// Launch-shape constants (chosen by measurement on GB300; see the profiles).
+#ifndef ZS_THREADS
+#define ZS_THREADS 256
+#endif
+#ifndef ZS_VPT_SMALL_N  // vector units per thread per trip when n <= 2
+#define ZS_VPT_SMALL_N 1
+#endif
+#ifndef ZS_VPT_MID_N  // ... when 2 < n <= 8
+#define ZS_VPT_MID_N 1
+#endif
+#ifndef ZS_APPLY_VPT
+#define ZS_APPLY_VPT 1
+#endif
+#ifndef ZS_GRID_WAVES  // grid = waves x resident CTAs per SM x SMs; 0 = one thread per unit
+#define ZS_GRID_WAVES 0
+#endif
+#ifndef ZS_ACC_STREAM  // 1: evict-first hints on the fp32 accumulator too
+#define ZS_ACC_STREAM 1
+#endif
+#ifndef ZS_CHECK_VPT  // vector units per thread of the flag-only pass
+#define ZS_CHECK_VPT 8
+#endif
+#ifndef ZS_CHECK_WAVES  // grid waves of the flag-only pass (0 = one thread per VPT units)
+#define ZS_CHECK_WAVES 0
+#endif
+#ifndef ZS_MIN_BLOCKS  // __launch_bounds__ minimum resident CTAs per SM (0 = unset)
+#define ZS_MIN_BLOCKS 0
+#endif
+#if ZS_MIN_BLOCKS > 0
+#define ZS_BOUNDS __launch_bounds__(ZS_THREADS, ZS_MIN_BLOCKS)
+#else
+#define ZS_BOUNDS __launch_bounds__(ZS_THREADS)
+#endif
+
 namespace zs {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = ZS_THREADS;
 
 struct SlicePtrs {
   const uint4* p[ZS_MAX_RANKS];
@@ -86,27 +125,33 @@ __device__ __forceinline__ void add8(float a[8], const uint4 h) {
   }
 }
 
-// a += slice_0[vi] + ... + slice_{n-1}[vi] (vector unit vi = 8 elements),
-// sequential in rank order; loads are issued in groups before their adds.
-template <int DT>
-__device__ __forceinline__ void sum_slices8(const SlicePtrs& s, int n, int64_t vi, float a[8]) {
+// a[j] += slice_0[vi[j]] + ... + slice_{n-1}[vi[j]] for the VPT vector units
+// of this trip (8 elements each), sequential in rank order for every element;
+// 8 loads are issued before their adds.  Units with ok[j] false are skipped.
+template <int DT, int VPT>
+__device__ __forceinline__ void sum_slices(const SlicePtrs& s, int n, const int64_t (&vi)[VPT],
+                                           const bool (&ok)[VPT], float (&a)[VPT][8]) {
+  constexpr int CH = 8 / VPT;
   int r = 0;
-  for (; r + 8 <= n; r += 8) {
-    uint4 h[8];
+  for (; r + CH <= n; r += CH) {
+    uint4 h[VPT][CH];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) h[j] = __ldcs(s.p[r + j] + vi);
+    for (int c = 0; c < CH; ++c) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) add8<DT>(a, h[j]);
+      for (int j = 0; j < VPT; ++j)
+        h[j][c] = ok[j] ? __ldcs(s.p[r + c] + vi[j]) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+#pragma unroll
+      for (int j = 0; j < VPT; ++j) add8<DT>(a[j], h[j][c]);
+    }
   }
-  if (r + 4 <= n) {
-    uint4 h[4];
+  for (; r < n; ++r) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) h[j] = __ldcs(s.p[r + j] + vi);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) add8<DT>(a, h[j]);
-    r += 4;
+    for (int j = 0; j < VPT; ++j)
+      if (ok[j]) add8<DT>(a[j], __ldcs(s.p[r] + vi[j]));
   }
-  for (; r < n; ++r) add8<DT>(a, __ldcs(s.p[r] + vi));
 }
 
 template <int DT>
@@ -130,15 +175,38 @@ __device__ __forceinline__ void store8(float* p, const float a[8]) {
   *reinterpret_cast<float4*>(p + 4) = make_float4(a[4], a[5], a[6], a[7]);
 }
 
+__device__ __forceinline__ void load8_acc(const float* p, float a[8]) {
+#if ZS_ACC_STREAM
+  const float4 x0 = __ldcs(reinterpret_cast<const float4*>(p));
+  const float4 x1 = __ldcs(reinterpret_cast<const float4*>(p + 4));
+  a[0] = x0.x; a[1] = x0.y; a[2] = x0.z; a[3] = x0.w;
+  a[4] = x1.x; a[5] = x1.y; a[6] = x1.z; a[7] = x1.w;
+#else
+  load8(p, a);
+#endif
+}
+
+__device__ __forceinline__ void store8_acc(float* p, const float a[8]) {
+#if ZS_ACC_STREAM
+  __stcs(reinterpret_cast<float4*>(p), make_float4(a[0], a[1], a[2], a[3]));
+  __stcs(reinterpret_cast<float4*>(p + 4), make_float4(a[4], a[5], a[6], a[7]));
+#else
+  store8(p, a);
+#endif
+}
+
 __device__ __forceinline__ void store8_cs(float* p, const float a[8]) {
   __stcs(reinterpret_cast<float4*>(p), make_float4(a[0], a[1], a[2], a[3]));
   __stcs(reinterpret_cast<float4*>(p + 4), make_float4(a[4], a[5], a[6], a[7]));
 }
 
-// One bias-corrected AdamW update with decoupled decay, fp32.
+// One bias-corrected AdamW update with decoupled decay, fp32.  With CLIP the
+// averaged gradient is multiplied by the global-norm clipping coefficient.
+template <bool CLIP = false>
 __device__ __forceinline__ void adamw1(const AdamArgs& ad, float sum, float& p, float& m,
-                                       float& v) {
-  const float g = __fdiv_rn(sum, ad.grad_div);
+                                       float& v, float coef = 1.0f) {
+  float g = __fdiv_rn(sum, ad.grad_div);
+  if constexpr (CLIP) g = __fmul_rn(g, coef);
   m = __fmaf_rn(ad.beta1, m, __fmul_rn(ad.omb1, g));
   v = __fmaf_rn(ad.beta2, v, __fmul_rn(ad.omb2, __fmul_rn(g, g)));
   const float m_hat = __fmul_rn(m, ad.inv_bc1);
@@ -172,29 +240,41 @@ __device__ __forceinline__ void scaler_step(zs_scaler s, int overflow, StepResul
 
 // ---------------------------------------------------------------- kernels
 
-// Reduce + accumulate + flag.  FIRST: start from +0.0f instead of acc.
+// Reduce + accumulate + flag.  READ_ACC: start from acc (else +0.0f).
 // STORE: write the sums back to acc (otherwise only the flag is produced).
-// READ_ACC: start from acc (FIRST must be false).
-template <int DT, bool READ_ACC, bool STORE>
-__global__ void __launch_bounds__(kThreads)
+// VPT vector units per thread per trip, `stride` apart so each load
+// instruction of a warp covers 512 contiguous bytes.
+template <int DT, bool READ_ACC, bool STORE, int VPT>
+__global__ void ZS_BOUNDS
     k_reduce(const __grid_constant__ SlicePtrs s, int n, float* __restrict__ acc, int64_t count,
              int32_t* __restrict__ flag) {
   const int64_t nvec = count >> 3;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
   bool bad = false;
-  for (int64_t vi = tid; vi < nvec; vi += stride) {
-    float a[8];
-    if constexpr (READ_ACC) {
-      load8(acc + vi * 8, a);
-    } else {
+  for (int64_t base = tid; base < nvec; base += stride * VPT) {
+    int64_t vi[VPT];
+    bool ok[VPT];
+    float a[VPT][8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) a[k] = 0.0f;
+    for (int j = 0; j < VPT; ++j) {
+      vi[j] = base + j * stride;
+      ok[j] = vi[j] < nvec;
+      if (READ_ACC && ok[j]) {
+        load8_acc(acc + vi[j] * 8, a[j]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) a[j][k] = 0.0f;
+      }
     }
-    sum_slices8<DT>(s, n, vi, a);
+    sum_slices<DT, VPT>(s, n, vi, ok, a);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) bad |= not_finite(a[k]);
-    if constexpr (STORE) store8(acc + vi * 8, a);
+    for (int j = 0; j < VPT; ++j) {
+      if (!ok[j]) continue;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) bad |= not_finite(a[j][k]);
+      if constexpr (STORE) store8_acc(acc + vi[j] * 8, a[j]);
+    }
   }
   const int64_t tail = count - nvec * 8;
   if (tid < tail) {
@@ -210,42 +290,59 @@ __global__ void __launch_bounds__(kThreads)
 // AdamW + cast.  HAS_ACC: the sum starts from acc (else +0.0f).  RECOMPUTE:
 // the last micro-step's slices are added here.  When `result` is non-null,
 // thread 0 of CTA 0 also performs the loss-scale update from the flag.
-template <int DT, bool HAS_ACC, bool RECOMPUTE>
-__global__ void __launch_bounds__(kThreads)
+template <int DT, bool HAS_ACC, bool RECOMPUTE, int VPT, bool CLIP = false>
+__global__ void ZS_BOUNDS
     k_apply(const int32_t* __restrict__ flag, const __grid_constant__ SlicePtrs s, int n,
             const float* __restrict__ acc, float* __restrict__ master, float* __restrict__ mom,
             float* __restrict__ var, uint16_t* __restrict__ half_out, int64_t count, AdamArgs ad,
-            zs_scaler scaler_in, StepResult* __restrict__ result) {
+            zs_scaler scaler_in, StepResult* __restrict__ result,
+            const float* __restrict__ clip_coef = nullptr) {
   const int32_t overflow = *flag;
   if (result != nullptr && blockIdx.x == 0 && threadIdx.x == 0)
     scaler_step(scaler_in, overflow, result);
   if (overflow != 0) return;
+  float coef = 1.0f;
+  if constexpr (CLIP) coef = *clip_coef;
   const int64_t nvec = count >> 3;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
-  for (int64_t vi = tid; vi < nvec; vi += stride) {
-    float a[8];
-    if constexpr (HAS_ACC) {
-      load8(acc + vi * 8, a);
-    } else {
+  for (int64_t base = tid; base < nvec; base += stride * VPT) {
+    int64_t vi[VPT];
+    bool ok[VPT];
+    float a[VPT][8];
+    float p[VPT][8], m[VPT][8], v[VPT][8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) a[k] = 0.0f;
+    for (int j = 0; j < VPT; ++j) {
+      vi[j] = base + j * stride;
+      ok[j] = vi[j] < nvec;
+      if (HAS_ACC && ok[j]) {
+        load8_acc(acc + vi[j] * 8, a[j]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) a[j][k] = 0.0f;
+      }
+      if (ok[j]) {
+        load8(master + vi[j] * 8, p[j]);
+        load8(mom + vi[j] * 8, m[j]);
+        load8(var + vi[j] * 8, v[j]);
+      }
     }
-    if constexpr (RECOMPUTE) sum_slices8<DT>(s, n, vi, a);
-    float p[8], m[8], v[8];
-    load8(master + vi * 8, p);
-    load8(mom + vi * 8, m);
-    load8(var + vi * 8, v);
-    uint32_t h[4];
+    if constexpr (RECOMPUTE) sum_slices<DT, VPT>(s, n, vi, ok, a);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) adamw1(ad, a[k], p[k], m[k], v[k]);
+    for (int j = 0; j < VPT; ++j) {
+      if (!ok[j]) continue;
+      uint32_t h[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
-      h[k] = float_to_half_bits<DT>(p[2 * k]) | (float_to_half_bits<DT>(p[2 * k + 1]) << 16);
-    store8_cs(master + vi * 8, p);
-    store8_cs(mom + vi * 8, m);
-    store8_cs(var + vi * 8, v);
-    __stcs(reinterpret_cast<uint4*>(half_out) + vi, make_uint4(h[0], h[1], h[2], h[3]));
+      for (int k = 0; k < 8; ++k) adamw1<CLIP>(ad, a[j][k], p[j][k], m[j][k], v[j][k], coef);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        h[k] = float_to_half_bits<DT>(p[j][2 * k]) |
+               (float_to_half_bits<DT>(p[j][2 * k + 1]) << 16);
+      store8_cs(master + vi[j] * 8, p[j]);
+      store8_cs(mom + vi[j] * 8, m[j]);
+      store8_cs(var + vi[j] * 8, v[j]);
+      __stcs(reinterpret_cast<uint4*>(half_out) + vi[j], make_uint4(h[0], h[1], h[2], h[3]));
+    }
   }
   const int64_t tail = count - nvec * 8;
   if (tid < tail) {
@@ -253,11 +350,105 @@ __global__ void __launch_bounds__(kThreads)
     float a = HAS_ACC ? acc[i] : 0.0f;
     if constexpr (RECOMPUTE) a = sum_slices1<DT>(s, n, i, a);
     float p = master[i], m = mom[i], v = var[i];
-    adamw1(ad, a, p, m, v);
+    adamw1<CLIP>(ad, a, p, m, v, coef);
     master[i] = p;
     mom[i] = m;
     var[i] = v;
     half_out[i] = (uint16_t)float_to_half_bits<DT>(p);
+  }
+}
+
+// ---------------------------------------------------------------- clipping
+
+// Square of one final gradient sum, accumulated in fp64.  Squares are formed
+// in fp32 unless they would overflow it (|a| > 1e18).
+__device__ __forceinline__ double sq8(const float a[8]) {
+  float q[8];
+  bool big = false;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    q[k] = __fmul_rn(a[k], a[k]);
+    big |= fabsf(a[k]) > 1e18f;
+  }
+  if (big) {
+    double d = 0.0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) d += (double)a[k] * (double)a[k];
+    return d;
+  }
+  const float s01 = __fadd_rn(q[0], q[1]), s23 = __fadd_rn(q[2], q[3]);
+  const float s45 = __fadd_rn(q[4], q[5]), s67 = __fadd_rn(q[6], q[7]);
+  return (double)__fadd_rn(__fadd_rn(s01, s23), __fadd_rn(s45, s67));
+}
+
+// Fixed-order CTA sum of one double per thread; the result is valid in thread 0.
+__device__ __forceinline__ double block_sum(double x) {
+  __shared__ double warp_part[kThreads / 32];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x += __shfl_down_sync(0xffffffffu, x, off);
+  if ((threadIdx.x & 31) == 0) warp_part[threadIdx.x >> 5] = x;
+  __syncthreads();
+  double t = 0.0;
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < kThreads / 32; ++w) t += warp_part[w];
+  }
+  return t;
+}
+
+// Per-CTA partial sums of squares of the final gradient sums
+// (acc (or +0) + the n slices), grid-stride over a grid of at most the
+// partials' capacity, one double per CTA into `partials`.
+template <int DT, bool HAS_ACC, bool RECOMPUTE>
+__global__ void ZS_BOUNDS k_sumsq(const __grid_constant__ SlicePtrs s, int n,
+                                  const float* __restrict__ acc, int64_t count,
+                                  double* __restrict__ partials) {
+  const int64_t nvec = count >> 3;
+  const int64_t stride = (int64_t)gridDim.x * kThreads;
+  const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+  double t = 0.0;
+  for (int64_t vi = tid; vi < nvec; vi += stride) {
+    int64_t v1[1] = {vi};
+    bool ok[1] = {true};
+    float a[1][8];
+    if constexpr (HAS_ACC) {
+      load8_acc(acc + vi * 8, a[0]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) a[0][k] = 0.0f;
+    }
+    if constexpr (RECOMPUTE) sum_slices<DT, 1>(s, n, v1, ok, a);
+    t += sq8(a[0]);
+  }
+  const int64_t tail = count - nvec * 8;
+  if (tid < tail) {
+    const int64_t i = nvec * 8 + tid;
+    float a = HAS_ACC ? acc[i] : 0.0f;
+    if constexpr (RECOMPUTE) a = sum_slices1<DT>(s, n, i, a);
+    t += (double)a * (double)a;
+  }
+  t = block_sum(t);
+  if (threadIdx.x == 0) partials[blockIdx.x] = t;
+}
+
+// One CTA: out = (sum of partials, fixed order) / grad_div^2.
+__global__ void k_sumsq_finalize(const double* __restrict__ partials, int nparts, double inv_div2,
+                                 double* __restrict__ out) {
+  double t = 0.0;
+  for (int i = threadIdx.x; i < nparts; i += kThreads) t += partials[i];
+  t = block_sum(t);
+  if (threadIdx.x == 0) *out = t * inv_div2;
+}
+
+// coef = max_norm / (sqrt(sumsq) + 1e-6) if that is below 1, else 1.
+__global__ void k_clip_coef(const double* __restrict__ sumsq, float max_norm,
+                            float* __restrict__ coef) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    double c = 1.0;
+    if (max_norm > 0.0f) {
+      const double q = (double)max_norm / (sqrt(*sumsq) + 1e-6);
+      if (q < 1.0) c = q;
+    }
+    *coef = (float)c;
   }
 }
 
