@@ -64,7 +64,8 @@ typedef enum {
   ZS_ERR_ALIGN = -2,   /* a device pointer not 16-byte aligned */
   ZS_ERR_DTYPE = -3,   /* dtype is neither ZS_FP16 nor ZS_BF16 */
   ZS_ERR_CUDA = -4,    /* a CUDA runtime error (message in zs_last_error) */
-  ZS_ERR_TIMEOUT = -5  /* reserved: a bounded device wait gave up */
+  ZS_ERR_TIMEOUT = -5, /* reserved: a bounded device wait gave up */
+  ZS_ERR_LIMIT = -6    /* count beyond ZS_NOALLOC_MAX_COUNT (zs_grad_sumsq_noalloc) */
 } zs_status;
 
 typedef enum { ZS_FP16 = 0, ZS_BF16 = 1 } zs_dtype;
@@ -230,6 +231,34 @@ zs_status zs_shard_step_clipped(zs_ctx* ctx, const void* const* grads, int32_t n
                                 int64_t step, zs_scaler* scaler, float max_norm,
                                 int32_t* overflow_out, float* new_scale_out,
                                 float* grad_norm_out, cudaStream_t stream);
+
+/* Allocation-free form of zs_grad_sumsq.  The pages have no counterpart: this
+ * exists for callers that cannot call cudaMalloc -- code that must not grow
+ * device memory (a framework that owns all of it through its own planner or
+ * arena, an out-of-memory handler that still wants the gradient norm) and
+ * code that cannot create a zs_ctx, whose creation allocates.
+ *
+ * Same result and arguments as zs_grad_sumsq, without a context.  Its scratch
+ * (one fp64 partial sum per 16,384 elements) is a fixed static device array
+ * of ZS_NOALLOC_MAX_PARTS doubles (128 KB) that every GPU loading this library
+ * holds until exit, so count is limited to ZS_NOALLOC_MAX_COUNT elements;
+ * larger counts return ZS_ERR_LIMIT before any work.  The call allocates
+ * nothing: no cudaMalloc, cudaFree or allocating library routine.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Every call on a device shares the array and
+ * leaves its partial sums in it; each call overwrites the slots it reads, so
+ * nothing has to start at zero, but calls whose kernels overlap on the GPU
+ * (different streams, no ordering) race on it -- serialise them.
+ * Errors: ZS_ERR_ARG / ZS_ERR_ALIGN / ZS_ERR_DTYPE as for zs_grad_sumsq,
+ * ZS_ERR_LIMIT for count > ZS_NOALLOC_MAX_COUNT, ZS_ERR_CUDA for a runtime
+ * failure (no message: there is no context). */
+#define ZS_NOALLOC_MAX_PARTS 16384
+#define ZS_NOALLOC_ELEMS_PER_PART 16384
+#define ZS_NOALLOC_MAX_COUNT ((int64_t)ZS_NOALLOC_MAX_PARTS * ZS_NOALLOC_ELEMS_PER_PART)
+zs_status zs_grad_sumsq_noalloc(const void* const* grads, int32_t n, zs_dtype dt,
+                                const float* acc, int64_t count, float grad_div,
+                                double* d_sumsq, cudaStream_t stream);
 
 /* ---------------------------------------------------------------- measurement */
 

@@ -15,6 +15,8 @@ from dataclasses import dataclass
 from ._build import HEADER, LIB_PATH, SOURCES, build, build_cmd  # noqa: F401,E402
 
 ZS_OK, ZS_ERR_ARG, ZS_ERR_ALIGN, ZS_ERR_DTYPE, ZS_ERR_CUDA, ZS_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
+ZS_ERR_LIMIT = -6
+ZS_NOALLOC_MAX_COUNT = 16384 * 16384
 ZS_FP16, ZS_BF16 = 0, 1
 ZS_MAX_RANKS = 256
 ZS_DEFAULT_ALIGN = 64
@@ -22,7 +24,7 @@ ZS_DEFAULT_ALIGN = 64
  ZS_KERNEL_COPY, ZS_KERNEL_SUMSQ) = range(7)
 KERNEL_NAMES = ["reduce", "check", "apply", "apply_recompute", "scaler", "copy", "sumsq"]
 _STATUS = {0: "ZS_OK", -1: "ZS_ERR_ARG", -2: "ZS_ERR_ALIGN", -3: "ZS_ERR_DTYPE", -4: "ZS_ERR_CUDA",
-           -5: "ZS_ERR_TIMEOUT"}
+           -5: "ZS_ERR_TIMEOUT", -6: "ZS_ERR_LIMIT"}
 
 
 class ZsError(RuntimeError):
@@ -76,6 +78,7 @@ def _load():
                           ctypes.POINTER(ctypes.c_float), vp],
         "zs_copy_peak": [vp, vp, vp, i64, i32, vp],
         "zs_grad_sumsq": [vp, pp, i32, i32, vp, i64, f32, vp, vp],
+        "zs_grad_sumsq_noalloc": [pp, i32, i32, vp, i64, f32, vp, vp],
         "zs_apply_clipped": [vp, vp, vp, f32, pp, i32, i32, vp, i64, f32, vp, vp, vp, vp,
                              ctypes.POINTER(zs_adam_hparams), i64, vp],
         "zs_shard_step_clipped": [vp, pp, i32, i32, i64, vp, i32, vp, vp, vp, vp,
@@ -280,6 +283,16 @@ def zs_grad_sumsq(ctx: Ctx, grads, dt, acc, count: int, grad_div: float, d_sumsq
     n = len(grads) if grads is not None else 0
     ctx.check(lib.zs_grad_sumsq(ctx.handle, g, n, _dtype(dt), _addr(acc), count, grad_div,
                                 _addr(d_sumsq), _stream(stream)))
+
+
+def zs_grad_sumsq_noalloc(grads, dt, acc, count: int, grad_div: float, d_sumsq, stream=None):
+    """Allocation-free zs_grad_sumsq (no context; count <= ZS_NOALLOC_MAX_COUNT)."""
+    g = _ptrs(grads) if grads is not None else None
+    n = len(grads) if grads is not None else 0
+    rc = lib.zs_grad_sumsq_noalloc(g, n, _dtype(dt), _addr(acc), count, grad_div,
+                                   _addr(d_sumsq), _stream(stream))
+    if rc != ZS_OK:
+        raise ZsError(rc, "zs_grad_sumsq_noalloc failed")
 
 
 def zs_apply_clipped(ctx: Ctx, d_flag, d_sumsq, max_norm: float, grads, dt, acc, count: int,

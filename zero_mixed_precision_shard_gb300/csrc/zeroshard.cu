@@ -8,6 +8,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <unordered_map>
 #include <vector>
@@ -772,3 +773,87 @@ zs_status zs_ctx_launch_count(const zs_ctx* c, int64_t* launches) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- allocation-free norm
+
+// Scratch of zs_grad_sumsq_noalloc: one fp64 partial sum per CTA, in static
+// device memory (each device that loads the library holds it until exit).
+// In host code this name is only a stand-in; kernels get the device address
+// looked up below.
+static __device__ __align__(256) double zs_noalloc_partials[ZS_NOALLOC_MAX_PARTS];
+
+namespace {
+
+constexpr int kNoallocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+double* g_noalloc_scratch[kNoallocMaxDevices] = {};
+
+// Device address of the static scratch on the current device, looked up once
+// per device with that device current.
+cudaError_t noalloc_scratch(double** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kNoallocMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_scratch[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, zs_noalloc_partials);
+    if (e != cudaSuccess) return e;
+    g_noalloc_scratch[dev] = static_cast<double*>(p);
+  }
+  *out = g_noalloc_scratch[dev];
+  return cudaSuccess;
+}
+
+template <int DT, bool HA, bool RC>
+void launch_sumsq_noalloc(const zs::SlicePtrs& sp, int32_t n, const float* acc, int64_t count,
+                          double* partials, int grid, cudaStream_t s) {
+  zs::k_sumsq<DT, HA, RC><<<grid, zs::kThreads, 0, s>>>(sp, n, acc, count, partials);
+}
+
+}  // namespace
+
+extern "C" zs_status zs_grad_sumsq_noalloc(const void* const* grads, int32_t n, zs_dtype dt,
+                                           const float* acc, int64_t count, float grad_div,
+                                           double* d_sumsq, cudaStream_t stream) {
+  if (count < 0) return ZS_ERR_ARG;
+  if (count > ZS_NOALLOC_MAX_COUNT) return ZS_ERR_LIMIT;
+  if (dt != ZS_FP16 && dt != ZS_BF16) return ZS_ERR_DTYPE;
+  if (d_sumsq == nullptr || !(grad_div > 0.0f) || !std::isfinite(grad_div)) return ZS_ERR_ARG;
+  if (!aligned16(acc) || !aligned16(d_sumsq)) return ZS_ERR_ALIGN;
+  zs::SlicePtrs sp;
+  std::memset(&sp, 0, sizeof sp);
+  const bool recompute = grads != nullptr;
+  if (recompute) {
+    if (n < 1 || n > ZS_MAX_RANKS) return ZS_ERR_ARG;
+    for (int r = 0; r < n; ++r) {
+      if (count > 0 && grads[r] == nullptr) return ZS_ERR_ARG;
+      if (!aligned16(grads[r])) return ZS_ERR_ALIGN;
+      sp.p[r] = static_cast<const uint4*>(grads[r]);
+    }
+  } else if (count > 0 && acc == nullptr) {
+    return ZS_ERR_ARG;
+  }
+  double* partials = nullptr;
+  if (noalloc_scratch(&partials) != cudaSuccess) return ZS_ERR_CUDA;
+  // one CTA (and one partial) per ZS_NOALLOC_ELEMS_PER_PART elements: each
+  // thread takes ZS_NOALLOC_ELEMS_PER_PART / (8 * kThreads) vector units
+  int64_t grid64 = (count + ZS_NOALLOC_ELEMS_PER_PART - 1) / ZS_NOALLOC_ELEMS_PER_PART;
+  if (grid64 < 1) grid64 = 1;
+  const int grid = (int)grid64;  // <= ZS_NOALLOC_MAX_PARTS by the count limit
+  const int nn = recompute ? n : 0;
+  const bool ha = acc != nullptr;
+  if (dt == ZS_FP16) {
+    if (recompute && ha) launch_sumsq_noalloc<ZS_FP16, true, true>(sp, nn, acc, count, partials, grid, stream);
+    else if (recompute) launch_sumsq_noalloc<ZS_FP16, false, true>(sp, nn, acc, count, partials, grid, stream);
+    else launch_sumsq_noalloc<ZS_FP16, true, false>(sp, nn, acc, count, partials, grid, stream);
+  } else {
+    if (recompute && ha) launch_sumsq_noalloc<ZS_BF16, true, true>(sp, nn, acc, count, partials, grid, stream);
+    else if (recompute) launch_sumsq_noalloc<ZS_BF16, false, true>(sp, nn, acc, count, partials, grid, stream);
+    else launch_sumsq_noalloc<ZS_BF16, true, false>(sp, nn, acc, count, partials, grid, stream);
+  }
+  const double div = (double)grad_div;
+  zs::k_sumsq_finalize<<<1, zs::kThreads, 0, stream>>>(partials, grid, 1.0 / (div * div), d_sumsq);
+  return cudaGetLastError() == cudaSuccess ? ZS_OK : ZS_ERR_CUDA;
+}
