@@ -95,6 +95,12 @@ class DeviceWorkload:
         return self.wl.dtype_code
 
     def slices(self, k: int):
+        if not hasattr(self, "_ptr_arrays"):
+            self._ptr_arrays = [self.zs.pointer_array(self.grads[j, r] for r in range(self.wl.n))
+                                for j in range(self.wl.g)]
+        return self._ptr_arrays[k]
+
+    def slice_tensors(self, k: int):
         return [self.grads[k, r] for r in range(self.wl.n)]
 
     def fill_grads(self, step: int, scale: float, inject: bool = True):
@@ -125,7 +131,8 @@ class DeviceWorkload:
     def launch_plan(self):
         """(kind, alg bytes per element) of every kernel one step launches."""
         n, g = self.wl.n, self.wl.g
-        plan = [("reduce", kernel_alg_bytes("reduce", n, first=(k == 0))) for k in range(g - 1)]
+        plan = [("reduce_first" if k == 0 else "reduce",
+                 kernel_alg_bytes("reduce", n, first=(k == 0))) for k in range(g - 1)]
         recompute = n < 4 or self.acc is None
         if recompute:
             with_acc = self.wl.dtype == "bf16" and g > 1
@@ -133,7 +140,8 @@ class DeviceWorkload:
             plan.append(("apply_recompute", kernel_alg_bytes("apply_recompute", n,
                                                              with_acc=g > 1)))
         else:
-            plan.append(("reduce", kernel_alg_bytes("reduce", n, first=(g == 1))))
+            plan.append(("reduce_first" if g == 1 else "reduce",
+                         kernel_alg_bytes("reduce", n, first=(g == 1))))
             plan.append(("apply", kernel_alg_bytes("apply", n)))
         return plan
 
@@ -218,6 +226,27 @@ def measured_peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def recorded_traffic(workload: str, kind: str, elements_per_launch: float):
+    """DRAM bytes per launch of `kind` from the ncu summary in profiles/traffic.json,
+    scaled by elements; None unless that capture was taken of this workload
+    with the kernel sources as they are now."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f)
+        for rel, digest in rec["sources_sha256"].items():
+            with open(os.path.join(ROOT, rel), "rb") as f:
+                if hashlib.sha256(f.read()).hexdigest() != digest:
+                    return None
+        if rec.get("workload") != workload:
+            return None
+        per = rec["bytes_per_elem"].get(kind)
+        return None if per is None else per * elements_per_launch
+    except (OSError, KeyError, ValueError):
+        return None
 
 
 def dist_env():
@@ -407,9 +436,13 @@ def run_ours(args):
     dom = max(kinds, key=lambda k: kinds[k]["ms"])
     peak, peak_kind = measured_peaks()
     step_bytes = alg_bytes_per_elem_step(wl.n, wl.g) * E
+    per_launch_elems = kinds[dom]["elements"] / kinds[dom]["launches"]
+    traffic = recorded_traffic(wl.name, dom, per_launch_elems) if not args.elements else None
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(kinds[dom]["gbs"], 1),
                 "peak": peak, "unit": "GB/s", "frac": round(kinds[dom]["gbs"] / peak, 4),
-                "traffic": None, "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})"}
+                "traffic": traffic, "traffic_unit": "bytes per launch",
+                "alg_bytes_per_launch": kinds[dom]["alg_bytes_per_elem"] * per_launch_elems,
+                "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})"}
 
     # end to end: gradients copied from pinned host memory every micro-step
     e2e = None

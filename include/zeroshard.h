@@ -270,14 +270,15 @@ zs_status zs_copy_peak(zs_ctx* ctx, const void* src, void* dst, int64_t bytes, i
 
 /* Kernel kinds for the timing counters. */
 typedef enum {
-  ZS_KERNEL_REDUCE = 0,          /* fp32 accumulate of n slices (+ flag) */
+  ZS_KERNEL_REDUCE = 0,          /* fp32 accumulate of n slices onto acc (+ flag) */
   ZS_KERNEL_CHECK = 1,           /* flag-only pass over n slices */
   ZS_KERNEL_APPLY = 2,           /* AdamW + cast from the accumulator */
   ZS_KERNEL_APPLY_RECOMPUTE = 3, /* AdamW + cast, re-reading the last slices */
   ZS_KERNEL_SCALER = 4,          /* standalone loss-scale update */
   ZS_KERNEL_COPY = 5,            /* roofline probe */
   ZS_KERNEL_SUMSQ = 6,           /* clipping: sum of squares (+ its finalize) */
-  ZS_KERNEL_KINDS = 7
+  ZS_KERNEL_REDUCE_FIRST = 7,    /* first micro-step: sum of n slices into acc (+ flag) */
+  ZS_KERNEL_KINDS = 8
 } zs_kernel_kind;
 
 /* When enabled, each launch is bracketed by CUDA events on its stream. */

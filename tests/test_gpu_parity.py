@@ -101,9 +101,10 @@ def test_grad_accum_bit_exact(zs, ctx, dtype, n, count):
 @pytest.mark.parametrize("dtype", [FP16, BF16])
 @pytest.mark.parametrize("where", ["first", "body", "tail", "last_rank"])
 @pytest.mark.parametrize("kind", ["inf", "-inf", "nan"])
-def test_overflow_flag(zs, ctx, dtype, where, kind):
+@pytest.mark.parametrize("n", [1, 5])
+def test_overflow_flag(zs, ctx, dtype, where, kind, n):
     rng = np.random.default_rng(7)
-    n, count = 5, 8 * 1000 + 5
+    count = 8 * 1000 + 5
     g = rand_grads(rng, n, count, dtype)
     bits = {"inf": 0x7C00 if dtype == FP16 else 0x7F80,
             "-inf": 0xFC00 if dtype == FP16 else 0xFF80,

@@ -21,8 +21,9 @@ ZS_FP16, ZS_BF16 = 0, 1
 ZS_MAX_RANKS = 256
 ZS_DEFAULT_ALIGN = 64
 (ZS_KERNEL_REDUCE, ZS_KERNEL_CHECK, ZS_KERNEL_APPLY, ZS_KERNEL_APPLY_RECOMPUTE, ZS_KERNEL_SCALER,
- ZS_KERNEL_COPY, ZS_KERNEL_SUMSQ) = range(7)
-KERNEL_NAMES = ["reduce", "check", "apply", "apply_recompute", "scaler", "copy", "sumsq"]
+ ZS_KERNEL_COPY, ZS_KERNEL_SUMSQ, ZS_KERNEL_REDUCE_FIRST) = range(8)
+KERNEL_NAMES = ["reduce", "check", "apply", "apply_recompute", "scaler", "copy", "sumsq",
+                "reduce_first"]
 _STATUS = {0: "ZS_OK", -1: "ZS_ERR_ARG", -2: "ZS_ERR_ALIGN", -3: "ZS_ERR_DTYPE", -4: "ZS_ERR_CUDA",
            -5: "ZS_ERR_TIMEOUT", -6: "ZS_ERR_LIMIT"}
 
@@ -120,10 +121,17 @@ def _stream(s) -> int | None:
 
 
 def _ptrs(tensors):
+    if isinstance(tensors, ctypes.Array):  # prebuilt by the caller (see pointer_array)
+        return tensors
     arr = (ctypes.c_void_p * len(tensors))()
     for i, t in enumerate(tensors):
         arr[i] = _addr(t)
     return arr
+
+
+def pointer_array(tensors):
+    """A reusable host array of device pointers for the `grads` arguments."""
+    return _ptrs(list(tensors))
 
 
 def _dtype(dt) -> int:

@@ -199,9 +199,16 @@ void launch_reduce_v(zs_ctx* c, const zs::SlicePtrs& sp, int32_t n, float* acc, 
 template <int DT>
 zs_status launch_reduce(zs_ctx* c, const zs::SlicePtrs& sp, int32_t n, float* acc, int64_t count,
                         bool read_acc, bool store, int32_t* flag, cudaStream_t s) {
-  const int kind = store ? ZS_KERNEL_REDUCE : ZS_KERNEL_CHECK;
+  const int kind = store ? (read_acc ? ZS_KERNEL_REDUCE : ZS_KERNEL_REDUCE_FIRST)
+                         : ZS_KERNEL_CHECK;
   LaunchScope ls(c, s, kind, count);
-  if (read_acc && store) {
+  if (!store && !read_acc && (DT == ZS_FP16 || n == 1)) {
+    // flag only, from the raw bit patterns (exact here: see k_check_bits)
+    constexpr int VPT = ZS_CHECK_VPT;
+    auto k = zs::k_check_bits<DT, VPT>;
+    k<<<grid_for(c, k, (count >> 3) / VPT + 8, ZS_CHECK_WAVES), zs::kThreads, 0, s>>>(sp, n, count,
+                                                                                     flag);
+  } else if (read_acc && store) {
     launch_reduce_v<DT, true, true>(c, sp, n, acc, count, flag, s);
   } else if (store) {
     launch_reduce_v<DT, false, true>(c, sp, n, acc, count, flag, s);
