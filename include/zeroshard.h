@@ -194,6 +194,28 @@ zs_status zs_shard_step(zs_ctx* ctx, const void* const* grads, int32_t n, zs_dty
                         zs_scaler* scaler, int32_t* overflow_out, float* new_scale_out,
                         cudaStream_t stream);
 
+/* ---------------------------------------------------------------- half accumulator */
+
+/* Variant whose accumulator is kept in the gradient's own 2-byte format, as
+ * the pages count gradients (2 bytes per parameter, §2 table; 2Ψ/N per rank
+ * under ZeRO-2, §2.2).  Per micro-step and element the ranks are summed in
+ * fp32 on top of the widened accumulator (same order as zs_grad_accum) and the
+ * sum is rounded to nearest even into acc_half; a sum past the half maximum
+ * rounds to infinity and makes the step overflow.  It moves 4 fewer bytes per
+ * element per carried micro-step than the fp32 accumulator, at the cost of one
+ * rounding per micro-step.  acc_half: count halves, 16-byte aligned. */
+zs_status zs_grad_accum_halfacc(zs_ctx* ctx, const void* const* grads, int32_t n, zs_dtype dt,
+                                int64_t count, void* acc_half, int32_t first,
+                                cudaStream_t stream);
+/* The last call of a step with the half accumulator (always sums the last
+ * micro-step into acc_half, then updates from it); otherwise as zs_shard_step. */
+zs_status zs_shard_step_halfacc(zs_ctx* ctx, const void* const* grads, int32_t n, zs_dtype dt,
+                                int64_t count, void* acc_half, int32_t accum_steps,
+                                float* master, float* m, float* v, void* half_out,
+                                const zs_adam_hparams* hp, int64_t step, zs_scaler* scaler,
+                                int32_t* overflow_out, float* new_scale_out,
+                                cudaStream_t stream);
+
 /* ---------------------------------------------------------------- clipping */
 
 /* Global-norm gradient clipping (§4.1 gradient_clipping; §5.1: engine.step()
@@ -259,6 +281,53 @@ zs_status zs_shard_step_clipped(zs_ctx* ctx, const void* const* grads, int32_t n
 zs_status zs_grad_sumsq_noalloc(const void* const* grads, int32_t n, zs_dtype dt,
                                 const float* acc, int64_t count, float grad_div,
                                 double* d_sumsq, cudaStream_t stream);
+
+/* ---------------------------------------------------------------- capture-friendly step */
+
+/* Learning-rate schedules named in §4.4 (LRRangeTest, OneCycle and
+ * WarmupCosineLR are named there too but not built).  The pages give
+ * WarmupDecayLR's knobs (warmup_min_lr, warmup_max_lr, warmup_num_steps,
+ * total_num_steps, warmup_type "linear"); the formulas are the plain linear
+ * reading, at Adam's step t (1-based count of applied updates):
+ *   ZS_LR_CONSTANT:      max_lr
+ *   ZS_LR_WARMUP:        min_lr + (max_lr - min_lr) * min(1, t / warmup_steps)
+ *   ZS_LR_WARMUP_DECAY:  the warmup for t <= warmup_steps, then
+ *                        max_lr * max(0, (total_steps - t) / (total_steps - warmup_steps)) */
+typedef enum { ZS_LR_CONSTANT = 0, ZS_LR_WARMUP = 1, ZS_LR_WARMUP_DECAY = 2 } zs_lr_kind;
+typedef struct {
+  int32_t kind;          /* zs_lr_kind */
+  int32_t pad_;
+  int64_t warmup_steps;  /* warmup_num_steps */
+  int64_t total_steps;   /* total_num_steps */
+  float min_lr, max_lr;  /* warmup_min_lr, warmup_max_lr */
+} zs_lr_schedule;
+
+/* Step state kept in DEVICE memory (caller-owned, 8-byte aligned, 56 bytes):
+ * the loss scaler, Adam's step count and the last step's outcome.  The caller
+ * initialises it (e.g. by copying a host struct whose scaler came from
+ * zs_scaler_init, with step = iterations = 0) and may read it back at any time. */
+typedef struct {
+  zs_scaler scaler;    /* loss-scale state (§4.2) */
+  int32_t overflow;    /* 1 if the last step was skipped */
+  int64_t step;        /* applied updates so far */
+  int64_t iterations;  /* steps run so far, skipped ones included */
+  float lr;            /* learning rate of the last applied update */
+  float grad_div;      /* N * G * S of the last step */
+} zs_device_state;
+
+/* zs_shard_step without any host round trip: the scale, Adam's step count and
+ * the learning rate are read from and written to *d_state on the device, the
+ * learning rate follows *sched (NULL: hp->lr throughout), nothing is copied
+ * to the host and the stream is not synchronised.  A whole step -- the
+ * zs_grad_accum calls plus this one -- can therefore be captured once in a
+ * CUDA graph and replayed every step (make one uncaptured call first so the
+ * launch shapes are cached).  Per-kernel timing is not recorded here.
+ * Otherwise identical to zs_shard_step (same kernels, same arithmetic). */
+zs_status zs_shard_step_async(zs_ctx* ctx, const void* const* grads, int32_t n, zs_dtype dt,
+                              int64_t count, float* acc, int32_t accum_steps, float* master,
+                              float* m, float* v, void* half_out, const zs_adam_hparams* hp,
+                              const zs_lr_schedule* sched, zs_device_state* d_state,
+                              cudaStream_t stream);
 
 /* ---------------------------------------------------------------- measurement */
 

@@ -92,6 +92,16 @@ def lib():
     L.zso_adamw_apply.argtypes = [_f32p, ctypes.c_int64, ctypes.c_double, _f32p, _f32p, _f32p,
                                   _u16p, ctypes.c_int32, ctypes.POINTER(HParams), ctypes.c_int64]
     L.zso_scaler_update.argtypes = [ctypes.POINTER(Scaler), ctypes.c_int32]
+    L.zso_reduce_accumulate_half.argtypes = [PP, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
+                                             _u16p, ctypes.c_int32]
+    L.zso_shard_step_halfacc.argtypes = [PP, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                         ctypes.c_int64, _u16p, _f32p, _f32p, _f32p, _u16p,
+                                         ctypes.POINTER(HParams), _i64p, ctypes.POINTER(Scaler),
+                                         ctypes.c_int32]
+    L.zso_shard_step_halfacc.restype = ctypes.c_int32
+    L.zso_lr_at.argtypes = [ctypes.c_int32, ctypes.c_double, ctypes.c_double, ctypes.c_int64,
+                            ctypes.c_int64, ctypes.c_int64]
+    L.zso_lr_at.restype = ctypes.c_double
     L.zso_grad_sumsq.argtypes = [_f32p, ctypes.c_int64, ctypes.c_double]
     L.zso_grad_sumsq.restype = ctypes.c_double
     L.zso_clip_coef.argtypes = [ctypes.c_double, ctypes.c_double]
@@ -193,6 +203,15 @@ def adamw_apply(acc, grad_div, master, m, v, half_out, dtype, hp: HParams, t: in
                           ctypes.byref(hp), t)
 
 
+LR_CONSTANT, LR_WARMUP, LR_WARMUP_DECAY = 0, 1, 2
+
+
+def lr_at(kind: int, min_lr: float, max_lr: float, warmup_steps: int, total_steps: int,
+          t: int) -> float:
+    return float(lib().zso_lr_at(kind, float(min_lr), float(max_lr), int(warmup_steps),
+                                 int(total_steps), int(t)))
+
+
 def grad_sumsq(acc: np.ndarray, grad_div: float) -> float:
     _check_f32(acc)
     return float(lib().zso_grad_sumsq(_p(acc, _f32p), acc.shape[0], float(grad_div)))
@@ -252,6 +271,29 @@ def shard_step(grads, dtype: int, state: ShardState, hp: HParams, t: int, sc: Sc
                                        int(extra_overflow), float(max_norm), ctypes.byref(norm))
     if return_norm:
         return int(ovf), tt.value, acc, norm.value
+    return int(ovf), tt.value, acc
+
+
+def reduce_accumulate_half(slices, dtype: int, acc_half: np.ndarray, first: bool):
+    _check_u16(acc_half)
+    lib().zso_reduce_accumulate_half(_ptr_array(slices), len(slices), dtype, acc_half.shape[0],
+                                     _p(acc_half, _u16p), 1 if first else 0)
+
+
+def shard_step_halfacc(grads, dtype: int, state: ShardState, hp: HParams, t: int, sc: Scaler,
+                       extra_overflow: int = 0):
+    """shard_step with the half-precision accumulator.  Returns (overflow, t, acc_half)."""
+    g = len(grads)
+    n = len(grads[0])
+    count = state.master.shape[0]
+    flat = [s for micro in grads for s in micro]
+    acc = np.zeros(count, dtype=np.uint16)
+    tt = ctypes.c_int64(t)
+    ovf = lib().zso_shard_step_halfacc(_ptr_array(flat), g, n, dtype, count, _p(acc, _u16p),
+                                       _p(state.master, _f32p), _p(state.m, _f32p),
+                                       _p(state.v, _f32p), _p(state.half, _u16p),
+                                       ctypes.byref(hp), ctypes.byref(tt), ctypes.byref(sc),
+                                       int(extra_overflow))
     return int(ovf), tt.value, acc
 
 

@@ -208,6 +208,66 @@ double zso_clip_coef(double sumsq_total, double max_norm) {
   return c < 1.0 ? c : 1.0;
 }
 
+/* ---- half-precision accumulator variant (§2 table, §2.2) ---------------- */
+
+void zso_reduce_accumulate_half(const uint16_t* const* slices, int32_t n, int32_t dtype,
+                                int64_t count, uint16_t* acc_half, int32_t first) {
+  for (int64_t i = 0; i < count; ++i) {
+    float a = first ? 0.0f : (float)zso_half_to_double(acc_half[i], dtype);
+    for (int32_t r = 0; r < n; ++r) a = a + (float)zso_half_to_double(slices[r][i], dtype);
+    acc_half[i] = zso_f32_to_half(a, dtype);
+  }
+}
+
+int32_t zso_shard_step_halfacc(const uint16_t* const* grads, int32_t g, int32_t n,
+                               int32_t dtype, int64_t count, uint16_t* acc_half, float* master,
+                               float* m, float* v, uint16_t* half_out, const zso_hparams* hp,
+                               int64_t* t, zso_scaler* sc, int32_t extra_overflow) {
+  for (int32_t k = 0; k < g; ++k)
+    zso_reduce_accumulate_half(grads + (size_t)k * n, n, dtype, count, acc_half, k == 0);
+  int32_t ovf = extra_overflow != 0;
+  for (int32_t k = 0; k < g && !ovf; ++k) ovf = zso_any_nonfinite(grads + (size_t)k * n, n,
+                                                                  dtype, count);
+  const uint16_t* accp[1] = {acc_half};
+  if (!ovf) ovf = zso_any_nonfinite(accp, 1, dtype, count);
+  if (!ovf) {
+    *t += 1;
+    const double div = (double)n * (double)g * sc->scale;
+    const double b1 = hp->beta1, b2 = hp->beta2;
+    const double bc1 = 1.0 - pow(b1, (double)*t);
+    const double bc2 = 1.0 - pow(b2, (double)*t);
+    for (int64_t i = 0; i < count; ++i) {
+      double gi = zso_half_to_double(acc_half[i], dtype) / div;
+      double p = (double)master[i];
+      double m1 = b1 * (double)m[i] + (1.0 - b1) * gi;
+      double v1 = b2 * (double)v[i] + (1.0 - b2) * gi * gi;
+      double p1 = p - hp->lr * ((m1 / bc1) / (sqrt(v1 / bc2) + hp->eps) + hp->weight_decay * p);
+      master[i] = (float)p1;
+      m[i] = (float)m1;
+      v[i] = (float)v1;
+      half_out[i] = zso_f32_to_half(master[i], dtype);
+    }
+  }
+  zso_scaler_update(sc, ovf);
+  return ovf;
+}
+
+/* ---- learning-rate schedules (§4.4) ------------------------------------ */
+
+double zso_lr_at(int32_t kind, double min_lr, double max_lr, int64_t warmup_steps,
+                 int64_t total_steps, int64_t t) {
+  if (kind == ZSO_LR_CONSTANT) return max_lr;
+  double frac = warmup_steps > 0 ? (double)t / (double)warmup_steps : 1.0;
+  if (frac > 1.0) frac = 1.0;
+  double warm = min_lr + (max_lr - min_lr) * frac;
+  if (kind == ZSO_LR_WARMUP || t <= warmup_steps) return warm;
+  /* ZSO_LR_WARMUP_DECAY after the warmup */
+  if (total_steps <= warmup_steps) return 0.0;
+  double rest = (double)(total_steps - t) / (double)(total_steps - warmup_steps);
+  if (rest < 0.0) rest = 0.0;
+  return max_lr * rest;
+}
+
 /* ---- dynamic loss scale (§4.2) ------------------------------------------ */
 
 void zso_scaler_update(zso_scaler* s, int32_t overflow) {

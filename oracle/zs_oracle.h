@@ -118,6 +118,34 @@ int32_t zso_shard_step(const uint16_t* const* grads, int32_t g, int32_t n, int32
                        uint16_t* half_out, const zso_hparams* hp, int64_t* t, zso_scaler* sc,
                        int32_t extra_overflow);
 
+/* Half-precision accumulator variant: the accumulated gradient is kept in the
+ * gradient's own 2-byte format, as the pages' accounting counts gradients
+ * (2 bytes per parameter, §2 table; 2Ψ/N per rank under ZeRO-2, §2.2).  Per
+ * micro-step and element: a = (first ? +0.0f : acc_half as fp32) + s_0 + ...
+ * + s_{n-1} in fp32, rank order, then acc_half = a rounded to nearest even.
+ * A sum past the half maximum rounds to infinity and makes the step
+ * overflow.  The update reads the half accumulator (exactly converted). */
+void zso_reduce_accumulate_half(const uint16_t* const* slices, int32_t n, int32_t dtype,
+                                int64_t count, uint16_t* acc_half, int32_t first);
+int32_t zso_shard_step_halfacc(const uint16_t* const* grads, int32_t g, int32_t n,
+                               int32_t dtype, int64_t count, uint16_t* acc_half, float* master,
+                               float* m, float* v, uint16_t* half_out, const zso_hparams* hp,
+                               int64_t* t, zso_scaler* sc, int32_t extra_overflow);
+
+/* Learning-rate schedules named in §4.4 (the pages give WarmupDecayLR's knobs:
+ * warmup_min_lr, warmup_max_lr, warmup_num_steps, total_num_steps,
+ * warmup_type "linear"; the formulas are the plain linear reading), at the
+ * Adam step t (1-based count of applied updates, this one included):
+ *   ZSO_LR_CONSTANT:      max_lr
+ *   ZSO_LR_WARMUP:        min_lr + (max_lr - min_lr) * min(1, t / warmup_steps)
+ *   ZSO_LR_WARMUP_DECAY:  the warmup above for t <= warmup_steps, then
+ *                         max_lr * max(0, (total_steps - t) / (total_steps - warmup_steps)) */
+#define ZSO_LR_CONSTANT 0
+#define ZSO_LR_WARMUP 1
+#define ZSO_LR_WARMUP_DECAY 2
+double zso_lr_at(int32_t kind, double min_lr, double max_lr, int64_t warmup_steps,
+                 int64_t total_steps, int64_t t);
+
 /* zso_shard_step with global-norm clipping over this view (the view is the
  * whole model, or the caller accepts the view's own norm); *norm_out gets the
  * gradient norm (0 on a skipped step). */

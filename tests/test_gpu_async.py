@@ -1,0 +1,123 @@
+"""The capture-friendly step (zs_shard_step_async, device-resident scaler,
+Adam step count and learning-rate schedule) against the oracle, eagerly and
+replayed from a CUDA graph: exact flags, scales and step counts, state within
+1e-6 relative + 1e-9 absolute, half copies within 1 ulp."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+FP16, BF16 = 0, 1
+REL, ABS = 1e-6, 1e-9
+
+
+@pytest.fixture(scope="module")
+def zs():
+    import zero_mixed_precision_shard_gb300 as pkg
+    torch.cuda.set_device(0)
+    return pkg
+
+
+@pytest.fixture(scope="module")
+def ctx(zs):
+    c = zs.Ctx()
+    yield c
+    c.close()
+
+
+def lib_half(x, dtype):
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    if dtype == FP16:
+        return x.astype(np.float16).view(np.uint16)
+    return torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def close(got, want, name):
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    err = np.abs(got - want)
+    tol = REL * np.abs(want) + ABS
+    assert (err <= tol).all(), (name, float((err / tol).max()))
+
+
+def ulps(a, b):
+    def o(x):
+        x = x.astype(np.int32)
+        return np.where(x & 0x8000, -(x & 0x7FFF), x & 0x7FFF)
+    return np.abs(o(a) - o(b))
+
+
+SCHED = (oracle.LR_WARMUP_DECAY, 1e-5, 1e-3, 3, 9)   # kind, min, max, warmup, total
+
+
+def _run(zs, ctx, dtype, n, G, count, steps, graph, inject):
+    rng = np.random.default_rng(n * 10 + G + (100 if graph else 0))
+    master0 = (rng.standard_normal(count) * 0.02).astype(np.float32)
+    st = oracle.ShardState.from_master(master0, dtype)
+    dyn = dtype == FP16
+    sc_o = oracle.make_scaler(512.0 if dyn else 1.0, 1.0, 2, 1, dyn)
+    kind, mn, mx, wu, tot = SCHED
+    sched = zs.make_schedule(kind, mn, mx, wu, tot)
+    hp = zs.make_hparams(mx, 0.9, 0.999, 1e-8, 0.01)
+    state = zs.DeviceState(zs.zs_scaler_init(sc_o.scale, 1.0, 2, 1, dyn))
+    master = torch.from_numpy(master0.copy()).cuda()
+    m, v = torch.zeros_like(master), torch.zeros_like(master)
+    half = torch.zeros(count, dtype=torch.int16, device="cuda")
+    acc = torch.zeros(count, dtype=torch.float32, device="cuda")
+    gbuf = torch.zeros((G, n, count), dtype=torch.int16, device="cuda")
+    ptrs = [zs.pointer_array(gbuf[k, r] for r in range(n)) for k in range(G)]
+
+    def step_calls():
+        for k in range(G - 1):
+            zs.zs_grad_accum(ctx, ptrs[k], dtype, count, acc, k == 0)
+        zs.zs_shard_step_async(ctx, ptrs[G - 1], dtype, count, acc, G, master, m, v, half, hp,
+                               sched, state)
+
+    g = None
+    t_o = 0
+    for s in range(1, steps + 1):
+        grads = [[lib_half((rng.standard_normal(count) * 1e-2 * sc_o.scale).astype(np.float32),
+                           dtype) for _ in range(n)] for _ in range(G)]
+        if s in inject:
+            grads[G - 1][n - 1][count - 1] = 0x7C00 if dtype == FP16 else 0x7F80
+        host = np.stack([np.stack(mc) for mc in grads]).view(np.int16)
+        gbuf.copy_(torch.from_numpy(host))
+        lr_t = oracle.lr_at(kind, mn, mx, wu, tot, t_o + 1)
+        hp_o = oracle.make_hparams(lr_t, 0.9, 0.999, 1e-8, 0.01)
+        ovf_o, t_o, _ = oracle.shard_step(grads, dtype, st, hp_o, t_o, sc_o)
+        if graph:
+            if g is None:
+                step_calls()               # uncaptured first call: caches launch shapes
+                torch.cuda.synchronize()
+                # undo nothing: that call was step s; capture the next steps
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    step_calls()
+            else:
+                g.replay()
+        else:
+            step_calls()
+        d = state.read()
+        assert d.overflow == ovf_o, f"step {s}"
+        assert d.scaler.scale == sc_o.scale and d.scaler.clean_count == sc_o.clean_count
+        assert d.step == t_o and d.iterations == s
+        if not ovf_o:
+            assert d.lr == np.float32(lr_t)
+    close(master.cpu().numpy(), st.master, "master")
+    close(m.cpu().numpy(), st.m, "m")
+    close(v.cpu().numpy(), st.v, "v")
+    assert ulps(half.cpu().numpy().view(np.uint16), st.half).max() <= 1
+
+
+@pytest.mark.parametrize("dtype", [FP16, BF16])
+@pytest.mark.parametrize("n,G,count", [(1, 3, 20_011), (2, 1, 8_192), (8, 2, 40_003)])
+def test_async_steps_match_oracle(zs, ctx, dtype, n, G, count):
+    _run(zs, ctx, dtype, n, G, count, 12, graph=False, inject={4, 5})
+
+
+@pytest.mark.parametrize("n,G,count", [(1, 3, 20_011), (8, 2, 40_003)])
+def test_graph_replayed_steps_match_oracle(zs, ctx, n, G, count):
+    _run(zs, ctx, FP16, n, G, count, 12, graph=True, inject={6})

@@ -1,0 +1,119 @@
+"""The half-precision accumulator variant on the GPU against the oracle:
+bit-exact half accumulators and flags (including sums that round past the
+fp16 maximum), and multi-step state within 1e-6 relative + 1e-9 absolute."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+FP16, BF16 = 0, 1
+REL, ABS = 1e-6, 1e-9
+
+
+@pytest.fixture(scope="module")
+def zs():
+    import zero_mixed_precision_shard_gb300 as pkg
+    torch.cuda.set_device(0)
+    return pkg
+
+
+@pytest.fixture(scope="module")
+def ctx(zs):
+    c = zs.Ctx()
+    yield c
+    c.close()
+
+
+def lib_half(x, dtype):
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    if dtype == FP16:
+        return x.astype(np.float16).view(np.uint16)
+    return torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def dev16(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda()
+
+
+def close(got, want, name):
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    err = np.abs(got - want)
+    tol = REL * np.abs(want) + ABS
+    assert (err <= tol).all(), (name, float((err / tol).max()))
+
+
+def ulps(a, b):
+    def o(x):
+        x = x.astype(np.int32)
+        return np.where(x & 0x8000, -(x & 0x7FFF), x & 0x7FFF)
+    return np.abs(o(a) - o(b))
+
+
+@pytest.mark.parametrize("dtype", [FP16, BF16])
+@pytest.mark.parametrize("n,count", [(1, 1), (1, 65541), (2, 9), (5, 10007), (16, 4099)])
+def test_halfacc_accumulate_bit_exact(zs, ctx, dtype, n, count):
+    rng = np.random.default_rng(n + count)
+    acc_d = torch.zeros(count, dtype=torch.int16, device="cuda")
+    acc_o = np.zeros(count, np.uint16)
+    for k in range(3):
+        g = [lib_half((rng.standard_normal(count) * 300).astype(np.float32), dtype)
+             for _ in range(n)]
+        zs.zs_grad_accum_halfacc(ctx, [dev16(x) for x in g], dtype, count, acc_d, k == 0)
+        oracle.reduce_accumulate_half(g, dtype, acc_o, k == 0)
+    assert acc_d.cpu().numpy().view(np.uint16).tobytes() == acc_o.tobytes()
+
+
+def test_halfacc_sum_rounding_past_fp16_max_overflows(zs, ctx):
+    count = 17
+    big = lib_half(np.full(count, 40000.0, np.float32), FP16)
+    acc = torch.zeros(count, dtype=torch.int16, device="cuda")
+    master = torch.full((count,), 0.5, dtype=torch.float32, device="cuda")
+    m, v = torch.zeros_like(master), torch.zeros_like(master)
+    half = torch.zeros(count, dtype=torch.int16, device="cuda")
+    sc = zs.zs_scaler_init(1024.0, 1.0, 1000, 1, True)
+    zs.zs_grad_accum_halfacc(ctx, [dev16(big)], FP16, count, acc, True)
+    ovf, ns = zs.zs_shard_step_halfacc(ctx, [dev16(big)], FP16, count, acc, 2, master, m, v, half,
+                                       zs.make_hparams(1e-3), 1, sc)
+    assert ovf == 1 and ns == 512.0
+    assert torch.all(master == 0.5)
+
+
+@pytest.mark.parametrize("dtype", [FP16, BF16])
+@pytest.mark.parametrize("n,G,count", [(1, 8, 30_011), (4, 2, 20_000), (16, 1, 5_003)])
+def test_halfacc_shard_steps(zs, ctx, dtype, n, G, count):
+    rng = np.random.default_rng(n * 3 + G)
+    master0 = (rng.standard_normal(count) * 0.02).astype(np.float32)
+    st = oracle.ShardState.from_master(master0, dtype)
+    dyn = dtype == FP16
+    sc_o = oracle.make_scaler(256.0 if dyn else 1.0, 1.0, 3, 1, dyn)
+    sc = zs.zs_scaler_init(sc_o.scale, 1.0, 3, 1, dyn)
+    hp_v = (1e-3, 0.9, 0.999, 1e-8, 0.01)
+    hp_o, hp = oracle.make_hparams(*hp_v), zs.make_hparams(*hp_v)
+    master = torch.from_numpy(master0.copy()).cuda()
+    m, v = torch.zeros_like(master), torch.zeros_like(master)
+    half = torch.zeros(count, dtype=torch.int16, device="cuda")
+    acc = torch.zeros(count, dtype=torch.int16, device="cuda")
+    t = t_o = 0
+    for s in range(1, 9):
+        grads = [[lib_half((rng.standard_normal(count) * 1e-2 * sc_o.scale).astype(np.float32),
+                           dtype) for _ in range(n)] for _ in range(G)]
+        if s == 4:
+            grads[0][n - 1][count // 3] = 0x7E00 if dtype == FP16 else 0x7FC0
+        ovf_o, t_o, _ = oracle.shard_step_halfacc(grads, dtype, st, hp_o, t_o, sc_o)
+        dg = [[dev16(x) for x in micro] for micro in grads]
+        for k in range(G - 1):
+            zs.zs_grad_accum_halfacc(ctx, dg[k], dtype, count, acc, k == 0)
+        ovf, ns = zs.zs_shard_step_halfacc(ctx, dg[G - 1], dtype, count, acc, G, master, m, v,
+                                           half, hp, t + 1, sc)
+        if not ovf:
+            t += 1
+        assert ovf == ovf_o and ns == sc_o.scale, f"step {s}"
+    assert t == t_o
+    close(master.cpu().numpy(), st.master, "master")
+    close(m.cpu().numpy(), st.m, "m")
+    close(v.cpu().numpy(), st.v, "v")
+    assert ulps(half.cpu().numpy().view(np.uint16), st.half).max() <= 1

@@ -525,3 +525,80 @@ def test_clipped_shard_union_uses_the_global_norm():
     cat = np.concatenate([s.master for s in shards])
     # the global norm is a sum of per-shard sums (fp64 grouping may differ in the last bit)
     assert np.all(np.abs(cat - whole.master) <= np.spacing(np.abs(whole.master)))
+
+
+# ---------------------------------------------------------------- LR schedules (§4.4)
+
+def test_warmup_decay_schedule_of_the_pages():
+    # §4.4's WarmupDecayLR example: min 0, max 3e-4, 2000 warmup steps, 100000 total, linear
+    lr = lambda t: oracle.lr_at(oracle.LR_WARMUP_DECAY, 0.0, 3e-4, 2000, 100000, t)  # noqa: E731
+    assert lr(0) == 0.0
+    assert lr(1000) == pytest.approx(1.5e-4, rel=1e-15)       # half way up
+    assert lr(2000) == pytest.approx(3e-4, rel=1e-15)         # peak at the end of warmup
+    assert lr(51000) == pytest.approx(1.5e-4, rel=1e-15)      # half way down
+    assert lr(100000) == 0.0 and lr(150000) == 0.0            # decayed to zero, stays there
+    ts = np.arange(0, 100001, 97)
+    vals = np.array([lr(int(t)) for t in ts])
+    up = ts <= 2000
+    assert np.all(np.diff(vals[up]) > 0) and np.all(np.diff(vals[~up]) <= 0)
+
+
+def test_warmup_and_constant_schedules():
+    w = lambda t: oracle.lr_at(oracle.LR_WARMUP, 1e-5, 1e-3, 100, 0, t)  # noqa: E731
+    assert w(0) == 1e-5 and w(50) == pytest.approx(5.05e-4) and w(100) == 1e-3
+    assert w(10 ** 6) == 1e-3                                  # flat after warmup
+    assert oracle.lr_at(oracle.LR_CONSTANT, 0.0, 2e-4, 10, 20, 7) == 2e-4
+    assert oracle.lr_at(oracle.LR_WARMUP, 0.0, 2e-4, 0, 0, 1) == 2e-4  # no warmup
+
+
+# ---------------------------------------------------------------- half accumulator
+
+def test_half_accumulator_rounds_each_micro_step():
+    # fp16 spacing at 2048 is 2: a carried half accumulator loses the odd unit that an
+    # fp32 accumulator keeps
+    one, big = _h([1.0]), _h([2048.0])
+    acc_h = np.zeros(1, np.uint16)
+    oracle.reduce_accumulate_half([big], FP16, acc_h, True)
+    oracle.reduce_accumulate_half([one], FP16, acc_h, False)   # 2049 -> ties to even: 2048
+    assert oracle.half_to_double(acc_h, FP16)[0] == 2048.0
+    acc_f = np.zeros(1, np.float32)
+    oracle.reduce_accumulate([big], FP16, acc_f, True)
+    oracle.reduce_accumulate([one], FP16, acc_f, False)
+    assert acc_f[0] == 2049.0
+    # within one micro-step the ranks still sum in fp32 before the single rounding
+    acc_h[:] = 0
+    oracle.reduce_accumulate_half([big, one, one], FP16, acc_h, True)   # 2050 exactly
+    assert oracle.half_to_double(acc_h, FP16)[0] == 2050.0
+
+
+def test_half_accumulator_overflow_skips():
+    # 40000 + 30000 is finite in fp32 but rounds past 65504: the step skips
+    hp = oracle.make_hparams(1e-3, 0.9, 0.999, 1e-8, 0.0)
+    st = oracle.ShardState.from_master(np.array([0.1], np.float32), FP16)
+    before = st.copy()
+    sc = oracle.make_scaler(1024.0)
+    ovf, t, acc = oracle.shard_step_halfacc([[_h([40000.0])], [_h([30000.0])]], FP16, st, hp,
+                                            0, sc)
+    assert ovf == 1 and t == 0 and acc[0] == 0x7C00 and sc.scale == 512.0
+    assert st.master.tobytes() == before.master.tobytes()
+    # the fp32 accumulator does not overflow on the same inputs
+    st2 = oracle.ShardState.from_master(np.array([0.1], np.float32), FP16)
+    ovf2, _, _ = oracle.shard_step([[_h([40000.0])], [_h([30000.0])]], FP16, st2, hp, 0,
+                                   oracle.make_scaler(1024.0))
+    assert ovf2 == 0
+
+
+def test_half_accumulator_equals_fp32_when_sums_are_representable():
+    # integer gradients with small sums are exact in both accumulators: same step, bitwise
+    rng = np.random.default_rng(40)
+    n, g, count = 3, 3, 500
+    grads = [[_h(rng.integers(-20, 20, count).astype(np.float32)) for _ in range(n)]
+             for _ in range(g)]
+    hp = oracle.make_hparams(1e-3, 0.9, 0.999, 1e-8, 0.01)
+    master0 = (rng.standard_normal(count) * 0.02).astype(np.float32)
+    a = oracle.ShardState.from_master(master0, FP16)
+    b = oracle.ShardState.from_master(master0, FP16)
+    oracle.shard_step(grads, FP16, a, hp, 0, oracle.make_scaler(16.0))
+    oracle.shard_step_halfacc(grads, FP16, b, hp, 0, oracle.make_scaler(16.0))
+    for k in ("master", "m", "v", "half"):
+        assert getattr(a, k).tobytes() == getattr(b, k).tobytes()

@@ -51,6 +51,21 @@ class zs_scaler(ctypes.Structure):
                 ("dynamic", ctypes.c_int32)]
 
 
+class zs_lr_schedule(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("pad_", ctypes.c_int32),
+                ("warmup_steps", ctypes.c_int64), ("total_steps", ctypes.c_int64),
+                ("min_lr", ctypes.c_float), ("max_lr", ctypes.c_float)]
+
+
+class zs_device_state(ctypes.Structure):
+    _fields_ = [("scaler", zs_scaler), ("overflow", ctypes.c_int32), ("step", ctypes.c_int64),
+                ("iterations", ctypes.c_int64), ("lr", ctypes.c_float),
+                ("grad_div", ctypes.c_float)]
+
+
+ZS_LR_CONSTANT, ZS_LR_WARMUP, ZS_LR_WARMUP_DECAY = 0, 1, 2
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(
@@ -78,6 +93,13 @@ def _load():
                           ctypes.POINTER(zs_adam_hparams), i64, ctypes.POINTER(zs_scaler), i32p,
                           ctypes.POINTER(ctypes.c_float), vp],
         "zs_copy_peak": [vp, vp, vp, i64, i32, vp],
+        "zs_grad_accum_halfacc": [vp, pp, i32, i32, i64, vp, i32, vp],
+        "zs_shard_step_halfacc": [vp, pp, i32, i32, i64, vp, i32, vp, vp, vp, vp,
+                                  ctypes.POINTER(zs_adam_hparams), i64, ctypes.POINTER(zs_scaler),
+                                  i32p, ctypes.POINTER(ctypes.c_float), vp],
+        "zs_shard_step_async": [vp, pp, i32, i32, i64, vp, i32, vp, vp, vp, vp,
+                                ctypes.POINTER(zs_adam_hparams), ctypes.POINTER(zs_lr_schedule),
+                                vp, vp],
         "zs_grad_sumsq": [vp, pp, i32, i32, vp, i64, f32, vp, vp],
         "zs_grad_sumsq_noalloc": [pp, i32, i32, vp, i64, f32, vp, vp],
         "zs_apply_clipped": [vp, vp, vp, f32, pp, i32, i32, vp, i64, f32, vp, vp, vp, vp,
@@ -327,6 +349,58 @@ def zs_shard_step_clipped(ctx: Ctx, grads, dt, count: int, acc, accum_steps: int
                                         ctypes.byref(scaler), max_norm, ctypes.byref(ovf),
                                         ctypes.byref(ns), ctypes.byref(gn), _stream(stream)))
     return ovf.value, ns.value, gn.value
+
+
+class DeviceState:
+    """A zs_device_state in device memory (a 56-byte torch buffer)."""
+
+    def __init__(self, scaler: zs_scaler, step: int = 0, device=None):
+        import torch
+        assert ctypes.sizeof(zs_device_state) == 56
+        st = zs_device_state()
+        st.scaler = scaler
+        st.step = step
+        host = torch.frombuffer(bytearray(bytes(st)), dtype=torch.uint8)
+        self.buf = host.to(device or torch.device("cuda", torch.cuda.current_device()))
+
+    def data_ptr(self) -> int:
+        return self.buf.data_ptr()
+
+    def read(self) -> zs_device_state:
+        return zs_device_state.from_buffer_copy(self.buf.cpu().numpy().tobytes())
+
+
+def make_schedule(kind: int, min_lr: float, max_lr: float, warmup_steps: int = 0,
+                  total_steps: int = 0) -> zs_lr_schedule:
+    return zs_lr_schedule(kind, 0, warmup_steps, total_steps, min_lr, max_lr)
+
+
+def zs_shard_step_async(ctx: Ctx, grads, dt, count: int, acc, accum_steps: int, master, m, v,
+                        half_out, hp: zs_adam_hparams, sched, d_state, stream=None):
+    ctx.check(lib.zs_shard_step_async(ctx.handle, _ptrs(grads), len(grads), _dtype(dt), count,
+                                      _addr(acc), accum_steps, _addr(master), _addr(m), _addr(v),
+                                      _addr(half_out), ctypes.byref(hp),
+                                      ctypes.byref(sched) if sched is not None else None,
+                                      _addr(d_state), _stream(stream)))
+
+
+def zs_grad_accum_halfacc(ctx: Ctx, grads, dt, count: int, acc_half, first: bool, stream=None):
+    ctx.check(lib.zs_grad_accum_halfacc(ctx.handle, _ptrs(grads), len(grads), _dtype(dt), count,
+                                        _addr(acc_half), 1 if first else 0, _stream(stream)))
+
+
+def zs_shard_step_halfacc(ctx: Ctx, grads, dt, count: int, acc_half, accum_steps: int, master,
+                          m, v, half_out, hp: zs_adam_hparams, step: int, scaler: zs_scaler,
+                          stream=None):
+    """Returns (overflow, new_scale); *scaler is updated in place."""
+    ovf = ctypes.c_int32()
+    ns = ctypes.c_float()
+    ctx.check(lib.zs_shard_step_halfacc(ctx.handle, _ptrs(grads), len(grads), _dtype(dt), count,
+                                        _addr(acc_half), accum_steps, _addr(master), _addr(m),
+                                        _addr(v), _addr(half_out), ctypes.byref(hp), step,
+                                        ctypes.byref(scaler), ctypes.byref(ovf),
+                                        ctypes.byref(ns), _stream(stream)))
+    return ovf.value, ns.value
 
 
 def zs_copy_peak(ctx: Ctx, src, dst, nbytes: int, read_only: bool = False, stream=None):

@@ -26,6 +26,7 @@ struct zs_ctx {
   double* d_partials = nullptr;        // scratch: per-CTA sums of squares
   double* d_sumsq = nullptr;           // the step's squared gradient norm (zs_shard_step_clipped)
   float* d_coef = nullptr;             // scratch: clipping coefficient
+  zs::AdamArgs* d_args = nullptr;      // scratch: per-step constants of the async step
   double* h_sumsq = nullptr;           // pinned mirror of d_sumsq
   zs::StepResult* d_result = nullptr;  // written by the loss-scale update
   zs::StepResult* h_result = nullptr;  // pinned mirror
@@ -255,11 +256,12 @@ void launch_apply_k(zs_ctx* c, const int32_t* flag, const zs::SlicePtrs& sp, int
   if (coef != nullptr) {
     auto k = zs::k_apply<DT, HA, RC, VPT, true>;
     k<<<grid_for(c, k, units), zs::kThreads, 0, s>>>(flag, sp, n, acc, master, m, v, ho, count,
-                                                     ad, sc_in, result, coef);
+                                                     ad, sc_in, result, coef, nullptr, nullptr);
   } else {
     auto k = zs::k_apply<DT, HA, RC, VPT, false>;
     k<<<grid_for(c, k, units), zs::kThreads, 0, s>>>(flag, sp, n, acc, master, m, v, ho, count,
-                                                     ad, sc_in, result, nullptr);
+                                                     ad, sc_in, result, nullptr, nullptr,
+                                                     nullptr);
   }
 }
 
@@ -380,6 +382,86 @@ zs_status finish_step(zs_ctx* c, zs_scaler* scaler, int32_t* overflow_out, float
   return ZS_OK;
 }
 
+template <int DT, bool HA, bool RC>
+void launch_apply_dev_k(zs_ctx* c, const int32_t* flag, const zs::SlicePtrs& sp, int32_t n,
+                               const float* acc, int64_t count, float* master, float* m, float* v,
+                               uint16_t* ho, const zs::AdamArgs* ad_dev, zs_device_state* st,
+                               cudaStream_t s) {
+  constexpr int VPT = ZS_APPLY_VPT;
+  const int64_t units = (count >> 3) / VPT + 8;
+  auto k = zs::k_apply<DT, HA, RC, VPT, false, true>;
+  const zs::AdamArgs unused{};
+  const zs_scaler unused_sc{};
+  k<<<grid_for(c, k, units), zs::kThreads, 0, s>>>(flag, sp, n, acc, master, m, v, ho, count,
+                                                   unused, unused_sc, nullptr, nullptr, ad_dev,
+                                                   st);
+}
+
+template <int DT>
+void apply_dev(zs_ctx* c, const int32_t* flag, const zs::SlicePtrs& sp, int32_t n,
+                      bool recompute, const float* acc, int64_t count, float* master, float* m,
+                      float* v, uint16_t* ho, const zs::AdamArgs* ad_dev, zs_device_state* st,
+                      cudaStream_t s) {
+  if (!recompute)
+    launch_apply_dev_k<DT, true, false>(c, flag, sp, n, acc, count, master, m, v, ho, ad_dev, st, s);
+  else if (acc != nullptr)
+    launch_apply_dev_k<DT, true, true>(c, flag, sp, n, acc, count, master, m, v, ho, ad_dev, st, s);
+  else
+    launch_apply_dev_k<DT, false, true>(c, flag, sp, n, acc, count, master, m, v, ho, ad_dev, st, s);
+}
+
+// Half-precision accumulator variants (always materialise the sums).
+template <int DT, bool RA>
+void launch_reduce_hacc_k(zs_ctx* c, const zs::SlicePtrs& sp, int32_t n, float* acc,
+                          int64_t count, int32_t* flag, cudaStream_t s) {
+  const int64_t units = (count >> 3) + 8;
+  auto k = zs::k_reduce<DT, RA, true, 1, true>;
+  k<<<grid_for(c, k, units), zs::kThreads, 0, s>>>(sp, n, acc, count, flag);
+}
+
+zs_status reduce_hacc(zs_ctx* c, zs_dtype dt, const zs::SlicePtrs& sp, int32_t n, void* acc,
+                      int64_t count, bool read_acc, int32_t* flag, cudaStream_t s) {
+  LaunchScope ls(c, s, read_acc ? ZS_KERNEL_REDUCE : ZS_KERNEL_REDUCE_FIRST, count);
+  float* a = static_cast<float*>(acc);
+  if (dt == ZS_FP16) {
+    if (read_acc) launch_reduce_hacc_k<ZS_FP16, true>(c, sp, n, a, count, flag, s);
+    else launch_reduce_hacc_k<ZS_FP16, false>(c, sp, n, a, count, flag, s);
+  } else {
+    if (read_acc) launch_reduce_hacc_k<ZS_BF16, true>(c, sp, n, a, count, flag, s);
+    else launch_reduce_hacc_k<ZS_BF16, false>(c, sp, n, a, count, flag, s);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(c, e, "reduce launch");
+  ls.done();
+  return ZS_OK;
+}
+
+zs_status apply_hacc(zs_ctx* c, zs_dtype dt, const int32_t* flag, const void* acc, int64_t count,
+                     const zs::AdamArgs& ad, float* master, float* m, float* v, void* half_out,
+                     const zs_scaler* scaler_in, zs::StepResult* result, cudaStream_t s) {
+  LaunchScope ls(c, s, ZS_KERNEL_APPLY, count);
+  zs::SlicePtrs sp;
+  std::memset(&sp, 0, sizeof sp);
+  const float* a = static_cast<const float*>(acc);
+  uint16_t* ho = static_cast<uint16_t*>(half_out);
+  const int64_t units = (count >> 3) + 8;
+  if (dt == ZS_FP16) {
+    auto k = zs::k_apply<ZS_FP16, true, false, 1, false, false, true>;
+    k<<<grid_for(c, k, units), zs::kThreads, 0, s>>>(flag, sp, 0, a, master, m, v, ho, count, ad,
+                                                     *scaler_in, result, nullptr, nullptr,
+                                                     nullptr);
+  } else {
+    auto k = zs::k_apply<ZS_BF16, true, false, 1, false, false, true>;
+    k<<<grid_for(c, k, units), zs::kThreads, 0, s>>>(flag, sp, 0, a, master, m, v, ho, count, ad,
+                                                     *scaler_in, result, nullptr, nullptr,
+                                                     nullptr);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(c, e, "apply launch");
+  ls.done();
+  return ZS_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -456,6 +538,7 @@ zs_status zs_ctx_create(zs_ctx** out) {
   if (e == cudaSuccess) e = cudaMemset(c->d_sumsq, 0, sizeof(double));
   if (e == cudaSuccess) e = cudaMalloc(&c->d_coef, sizeof(float));
   if (e == cudaSuccess) e = cudaMallocHost(&c->h_sumsq, sizeof(double));
+  if (e == cudaSuccess) e = cudaMalloc(&c->d_args, sizeof(zs::AdamArgs));
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     if (c->d_flag) cudaFree(c->d_flag);
@@ -465,6 +548,7 @@ zs_status zs_ctx_create(zs_ctx** out) {
     if (c->d_sumsq) cudaFree(c->d_sumsq);
     if (c->d_coef) cudaFree(c->d_coef);
     if (c->h_sumsq) cudaFreeHost(c->h_sumsq);
+    if (c->d_args) cudaFree(c->d_args);
     delete c;
     return ZS_ERR_CUDA;
   }
@@ -487,6 +571,7 @@ zs_status zs_ctx_destroy(zs_ctx* c) {
   cudaFree(c->d_sumsq);
   cudaFree(c->d_coef);
   cudaFreeHost(c->h_sumsq);
+  cudaFree(c->d_args);
   delete c;
   return ZS_OK;
 }
@@ -646,6 +731,113 @@ zs_status zs_shard_step_clipped(zs_ctx* c, const void* const* grads, int32_t n, 
   return shard_step_impl(c, grads, n, dt, count, acc, accum_steps, master, m, v, half_out, hp,
                          step, scaler, max_norm, overflow_out, new_scale_out, grad_norm_out,
                          stream);
+}
+
+zs_status zs_shard_step_async(zs_ctx* c, const void* const* grads, int32_t n, zs_dtype dt,
+                              int64_t count, float* acc, int32_t accum_steps, float* master,
+                              float* m, float* v, void* half_out, const zs_adam_hparams* hp,
+                              const zs_lr_schedule* sched, zs_device_state* d_state,
+                              cudaStream_t stream) {
+  ZS_TRY(check_ctx(c));
+  if (dt != ZS_FP16 && dt != ZS_BF16) return fail(c, ZS_ERR_DTYPE, "unknown dtype %d", (int)dt);
+  if (count < 0) return fail(c, ZS_ERR_ARG, "count < 0");
+  if (accum_steps < 1) return fail(c, ZS_ERR_ARG, "accum_steps must be >= 1");
+  if (accum_steps > 1 && acc == nullptr && count > 0)
+    return fail(c, ZS_ERR_ARG, "acc is required when accum_steps > 1");
+  if (d_state == nullptr) return fail(c, ZS_ERR_ARG, "d_state is NULL");
+  if ((reinterpret_cast<uintptr_t>(d_state) & 7u) != 0)
+    return fail(c, ZS_ERR_ALIGN, "d_state is not 8-byte aligned");
+  ZS_TRY(check_hparams(c, hp, 1));
+  if (sched != nullptr && (sched->kind < ZS_LR_CONSTANT || sched->kind > ZS_LR_WARMUP_DECAY ||
+                           sched->warmup_steps < 0 || !std::isfinite(sched->min_lr) ||
+                           !std::isfinite(sched->max_lr)))
+    return fail(c, ZS_ERR_ARG, "bad learning-rate schedule");
+  zs::SlicePtrs sp;
+  ZS_TRY(check_slices(c, grads, n, count, &sp));
+  ZS_TRY(check_array(c, acc, "acc", 0));
+  ZS_TRY(check_array(c, master, "master", count));
+  ZS_TRY(check_array(c, m, "m", count));
+  ZS_TRY(check_array(c, v, "v", count));
+  ZS_TRY(check_array(c, half_out, "half_out", count));
+  const bool recompute = (n < 4) || acc == nullptr;
+  const float* acc_in = (accum_steps > 1 || !recompute) ? acc : nullptr;
+  // the async step is meant for capture: no event timing inside it
+  const bool timing = c->timing;
+  c->timing = false;
+  zs_status st = ZS_OK;
+  if (count > 0) {
+    if (recompute) {
+      const bool with_acc = (dt == ZS_BF16) && accum_steps > 1;
+      st = reduce_any(c, dt, sp, n, with_acc ? acc : nullptr, count, with_acc, false, c->d_flag,
+                      stream);
+    } else {
+      st = reduce_any(c, dt, sp, n, acc, count, accum_steps > 1, true, c->d_flag, stream);
+    }
+  }
+  c->timing = timing;
+  ZS_TRY(st);
+  zs_lr_schedule sc{};
+  if (sched) sc = *sched;
+  zs::k_step_prologue<<<1, 32, 0, stream>>>(d_state, n, accum_steps, *hp, sc, sched ? 1 : 0,
+                                            c->d_args);
+  c->launches += 1;
+  uint16_t* ho = static_cast<uint16_t*>(half_out);
+  if (dt == ZS_FP16)
+    apply_dev<ZS_FP16>(c, c->d_flag, sp, recompute ? n : 0, recompute, acc_in, count, master, m,
+                       v, ho, c->d_args, d_state, stream);
+  else
+    apply_dev<ZS_BF16>(c, c->d_flag, sp, recompute ? n : 0, recompute, acc_in, count, master, m,
+                       v, ho, c->d_args, d_state, stream);
+  c->launches += 1;
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(c, e, "async step launch");
+  e = cudaMemsetAsync(c->d_flag, 0, sizeof(int32_t), stream);
+  if (e != cudaSuccess) return cuda_fail(c, e, "flag reset");
+  return ZS_OK;
+}
+
+zs_status zs_grad_accum_halfacc(zs_ctx* c, const void* const* grads, int32_t n, zs_dtype dt,
+                                int64_t count, void* acc_half, int32_t first,
+                                cudaStream_t stream) {
+  ZS_TRY(check_ctx(c));
+  if (dt != ZS_FP16 && dt != ZS_BF16) return fail(c, ZS_ERR_DTYPE, "unknown dtype %d", (int)dt);
+  if (count < 0) return fail(c, ZS_ERR_ARG, "count < 0");
+  zs::SlicePtrs sp;
+  ZS_TRY(check_slices(c, grads, n, count, &sp));
+  ZS_TRY(check_array(c, acc_half, "acc_half", count));
+  if (count == 0) return ZS_OK;
+  return reduce_hacc(c, dt, sp, n, acc_half, count, !first, c->d_flag, stream);
+}
+
+zs_status zs_shard_step_halfacc(zs_ctx* c, const void* const* grads, int32_t n, zs_dtype dt,
+                                int64_t count, void* acc_half, int32_t accum_steps,
+                                float* master, float* m, float* v, void* half_out,
+                                const zs_adam_hparams* hp, int64_t step, zs_scaler* scaler,
+                                int32_t* overflow_out, float* new_scale_out,
+                                cudaStream_t stream) {
+  ZS_TRY(check_ctx(c));
+  if (dt != ZS_FP16 && dt != ZS_BF16) return fail(c, ZS_ERR_DTYPE, "unknown dtype %d", (int)dt);
+  if (count < 0) return fail(c, ZS_ERR_ARG, "count < 0");
+  if (accum_steps < 1) return fail(c, ZS_ERR_ARG, "accum_steps must be >= 1");
+  ZS_TRY(check_hparams(c, hp, step));
+  ZS_TRY(check_scaler(c, scaler));
+  zs::SlicePtrs sp;
+  ZS_TRY(check_slices(c, grads, n, count, &sp));
+  ZS_TRY(check_array(c, acc_half, "acc_half", count));
+  ZS_TRY(check_array(c, master, "master", count));
+  ZS_TRY(check_array(c, m, "m", count));
+  ZS_TRY(check_array(c, v, "v", count));
+  ZS_TRY(check_array(c, half_out, "half_out", count));
+  const double div = (double)n * (double)accum_steps * (double)scaler->scale;
+  const float grad_div = (float)div;
+  if (!(grad_div > 0.0f) || !std::isfinite(grad_div))
+    return fail(c, ZS_ERR_ARG, "n * accum_steps * scale is not a positive finite fp32");
+  const zs::AdamArgs ad = adam_args(hp, step, grad_div);
+  if (count > 0)
+    ZS_TRY(reduce_hacc(c, dt, sp, n, acc_half, count, accum_steps > 1, c->d_flag, stream));
+  ZS_TRY(apply_hacc(c, dt, c->d_flag, acc_half, count, ad, master, m, v, half_out, scaler,
+                    c->d_result, stream));
+  return finish_step(c, scaler, overflow_out, new_scale_out, c->d_flag, stream);
 }
 
 zs_status zs_grad_sumsq(zs_ctx* c, const void* const* grads, int32_t n, zs_dtype dt,

@@ -195,6 +195,35 @@ __device__ __forceinline__ void store8_acc(float* p, const float a[8]) {
 #endif
 }
 
+// Half-precision accumulator: 8 halves <-> 8 floats (exact widening; RNE narrowing).
+template <int DT>
+__device__ __forceinline__ void load8_hacc(const float* p, int64_t vi, float a[8]) {
+  const uint4 h = __ldcs(reinterpret_cast<const uint4*>(p) + vi);
+  const uint32_t w[4] = {h.x, h.y, h.z, h.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    a[2 * k] = half_bits_to_float<DT>(w[k] & 0xFFFFu);
+    a[2 * k + 1] = half_bits_to_float<DT>(w[k] >> 16);
+  }
+}
+
+// Rounds a[] to the half format in place (so a[] holds what is stored) and
+// returns the packed bits; *bad |= any rounded value is not finite.
+template <int DT>
+__device__ __forceinline__ uint4 round8_hacc(float a[8], bool* bad) {
+  uint32_t w[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t lo = float_to_half_bits<DT>(a[2 * k]);
+    const uint32_t hi = float_to_half_bits<DT>(a[2 * k + 1]);
+    a[2 * k] = half_bits_to_float<DT>(lo);
+    a[2 * k + 1] = half_bits_to_float<DT>(hi);
+    *bad |= not_finite(a[2 * k]) | not_finite(a[2 * k + 1]);
+    w[k] = lo | (hi << 16);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 __device__ __forceinline__ void store8_cs(float* p, const float a[8]) {
   __stcs(reinterpret_cast<float4*>(p), make_float4(a[0], a[1], a[2], a[3]));
   __stcs(reinterpret_cast<float4*>(p + 4), make_float4(a[4], a[5], a[6], a[7]));
@@ -215,7 +244,7 @@ __device__ __forceinline__ void adamw1(const AdamArgs& ad, float sum, float& p, 
   p = __fsub_rn(p, __fmul_rn(ad.lr, __fmaf_rn(ad.wd, p, upd)));
 }
 
-__device__ __forceinline__ void scaler_step(zs_scaler s, int overflow, StepResult* out) {
+__device__ __forceinline__ zs_scaler next_scaler(zs_scaler s, int overflow) {
   if (overflow) {
     s.clean_count = 0;
     if (s.dynamic) {
@@ -233,9 +262,61 @@ __device__ __forceinline__ void scaler_step(zs_scaler s, int overflow, StepResul
       s.clean_count = 0;
     }
   }
+  return s;
+}
+
+__device__ __forceinline__ void scaler_step(zs_scaler s, int overflow, StepResult* out) {
   out->overflow = overflow ? 1 : 0;
   out->pad_ = 0;
-  out->scaler = s;
+  out->scaler = next_scaler(s, overflow);
+}
+
+// End-of-step update of the device-resident state (one thread).
+__device__ __forceinline__ void device_state_step(zs_device_state* st, int overflow,
+                                                  const AdamArgs& ad) {
+  st->scaler = next_scaler(st->scaler, overflow);
+  st->overflow = overflow ? 1 : 0;
+  st->iterations += 1;
+  st->grad_div = ad.grad_div;
+  if (!overflow) {
+    st->step += 1;
+    st->lr = ad.lr;
+  }
+}
+
+// Learning rate of a schedule at Adam step t (fp64, rounded to fp32 once).
+__device__ __forceinline__ float lr_at(const zs_lr_schedule& sc, int64_t t) {
+  const double mn = sc.min_lr, mx = sc.max_lr;
+  if (sc.kind == ZS_LR_CONSTANT) return (float)mx;
+  double frac = sc.warmup_steps > 0 ? (double)t / (double)sc.warmup_steps : 1.0;
+  if (frac > 1.0) frac = 1.0;
+  const double warm = mn + (mx - mn) * frac;
+  if (sc.kind == ZS_LR_WARMUP || t <= sc.warmup_steps) return (float)warm;
+  if (sc.total_steps <= sc.warmup_steps) return 0.0f;
+  double rest = (double)(sc.total_steps - t) / (double)(sc.total_steps - sc.warmup_steps);
+  if (rest < 0.0) rest = 0.0;
+  return (float)(mx * rest);
+}
+
+// Per-step constants of the update from the device-resident state: Adam's t,
+// the scheduled learning rate, the bias corrections and N*G*S.
+__global__ void k_step_prologue(const zs_device_state* __restrict__ st, int n, int accum_steps,
+                                zs_adam_hparams hp, zs_lr_schedule sched, int has_sched,
+                                AdamArgs* __restrict__ out) {
+  if (blockIdx.x != 0 || threadIdx.x != 0) return;
+  const int64_t t = st->step + 1;
+  AdamArgs a;
+  a.lr = has_sched ? lr_at(sched, t) : hp.lr;
+  a.beta1 = hp.beta1;
+  a.omb1 = 1.0f - hp.beta1;
+  a.beta2 = hp.beta2;
+  a.omb2 = 1.0f - hp.beta2;
+  a.eps = hp.eps;
+  a.wd = hp.weight_decay;
+  a.inv_bc1 = (float)(1.0 / (1.0 - pow((double)hp.beta1, (double)t)));
+  a.inv_bc2 = (float)(1.0 / (1.0 - pow((double)hp.beta2, (double)t)));
+  a.grad_div = (float)((double)n * (double)accum_steps * (double)st->scaler.scale);
+  *out = a;
 }
 
 // ---------------------------------------------------------------- kernels
@@ -244,10 +325,12 @@ __device__ __forceinline__ void scaler_step(zs_scaler s, int overflow, StepResul
 // STORE: write the sums back to acc (otherwise only the flag is produced).
 // VPT vector units per thread per trip, `stride` apart so each load
 // instruction of a warp covers 512 contiguous bytes.
-template <int DT, bool READ_ACC, bool STORE, int VPT>
+template <int DT, bool READ_ACC, bool STORE, int VPT, bool HACC = false>
 __global__ void ZS_BOUNDS
     k_reduce(const __grid_constant__ SlicePtrs s, int n, float* __restrict__ acc, int64_t count,
              int32_t* __restrict__ flag) {
+  // HACC: acc holds count halves of the gradient's format; each sum is rounded
+  // to it, and the flag tests the rounded value.
   const int64_t nvec = count >> 3;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
@@ -261,7 +344,11 @@ __global__ void ZS_BOUNDS
       vi[j] = base + j * stride;
       ok[j] = vi[j] < nvec;
       if (READ_ACC && ok[j]) {
-        load8_acc(acc + vi[j] * 8, a[j]);
+        if constexpr (HACC) {
+          load8_hacc<DT>(acc, vi[j], a[j]);
+        } else {
+          load8_acc(acc + vi[j] * 8, a[j]);
+        }
       } else {
 #pragma unroll
         for (int k = 0; k < 8; ++k) a[j][k] = 0.0f;
@@ -271,18 +358,32 @@ __global__ void ZS_BOUNDS
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
       if (!ok[j]) continue;
+      if constexpr (HACC) {
+        const uint4 h = round8_hacc<DT>(a[j], &bad);
+        if constexpr (STORE) __stcs(reinterpret_cast<uint4*>(acc) + vi[j], h);
+      } else {
 #pragma unroll
-      for (int k = 0; k < 8; ++k) bad |= not_finite(a[j][k]);
-      if constexpr (STORE) store8_acc(acc + vi[j] * 8, a[j]);
+        for (int k = 0; k < 8; ++k) bad |= not_finite(a[j][k]);
+        if constexpr (STORE) store8_acc(acc + vi[j] * 8, a[j]);
+      }
     }
   }
   const int64_t tail = count - nvec * 8;
   if (tid < tail) {
     const int64_t i = nvec * 8 + tid;
-    float a = READ_ACC ? acc[i] : 0.0f;
-    a = sum_slices1<DT>(s, n, i, a);
-    bad |= not_finite(a);
-    if constexpr (STORE) acc[i] = a;
+    if constexpr (HACC) {
+      uint16_t* ah = reinterpret_cast<uint16_t*>(acc);
+      float a = READ_ACC ? half_bits_to_float<DT>(ah[i]) : 0.0f;
+      a = sum_slices1<DT>(s, n, i, a);
+      const uint32_t b = float_to_half_bits<DT>(a);
+      bad |= not_finite(half_bits_to_float<DT>(b));
+      if constexpr (STORE) ah[i] = (uint16_t)b;
+    } else {
+      float a = READ_ACC ? acc[i] : 0.0f;
+      a = sum_slices1<DT>(s, n, i, a);
+      bad |= not_finite(a);
+      if constexpr (STORE) acc[i] = a;
+    }
   }
   if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(flag, 1);
 }
@@ -330,16 +431,25 @@ __global__ void ZS_BOUNDS k_check_bits(const __grid_constant__ SlicePtrs s, int 
 // AdamW + cast.  HAS_ACC: the sum starts from acc (else +0.0f).  RECOMPUTE:
 // the last micro-step's slices are added here.  When `result` is non-null,
 // thread 0 of CTA 0 also performs the loss-scale update from the flag.
-template <int DT, bool HAS_ACC, bool RECOMPUTE, int VPT, bool CLIP = false>
+template <int DT, bool HAS_ACC, bool RECOMPUTE, int VPT, bool CLIP = false, bool DEV = false,
+          bool HACC = false>
 __global__ void ZS_BOUNDS
     k_apply(const int32_t* __restrict__ flag, const __grid_constant__ SlicePtrs s, int n,
             const float* __restrict__ acc, float* __restrict__ master, float* __restrict__ mom,
-            float* __restrict__ var, uint16_t* __restrict__ half_out, int64_t count, AdamArgs ad,
-            zs_scaler scaler_in, StepResult* __restrict__ result,
-            const float* __restrict__ clip_coef = nullptr) {
+            float* __restrict__ var, uint16_t* __restrict__ half_out, int64_t count,
+            AdamArgs ad_host, zs_scaler scaler_in, StepResult* __restrict__ result,
+            const float* __restrict__ clip_coef = nullptr,
+            const AdamArgs* __restrict__ ad_dev = nullptr,
+            zs_device_state* __restrict__ dstate = nullptr) {
   const int32_t overflow = *flag;
-  if (result != nullptr && blockIdx.x == 0 && threadIdx.x == 0)
-    scaler_step(scaler_in, overflow, result);
+  AdamArgs ad = ad_host;
+  if constexpr (DEV) {
+    ad = *ad_dev;
+    if (blockIdx.x == 0 && threadIdx.x == 0) device_state_step(dstate, overflow, ad);
+  } else {
+    if (result != nullptr && blockIdx.x == 0 && threadIdx.x == 0)
+      scaler_step(scaler_in, overflow, result);
+  }
   if (overflow != 0) return;
   float coef = 1.0f;
   if constexpr (CLIP) coef = *clip_coef;
@@ -356,7 +466,11 @@ __global__ void ZS_BOUNDS
       vi[j] = base + j * stride;
       ok[j] = vi[j] < nvec;
       if (HAS_ACC && ok[j]) {
-        load8_acc(acc + vi[j] * 8, a[j]);
+        if constexpr (HACC) {
+          load8_hacc<DT>(acc, vi[j], a[j]);
+        } else {
+          load8_acc(acc + vi[j] * 8, a[j]);
+        }
       } else {
 #pragma unroll
         for (int k = 0; k < 8; ++k) a[j][k] = 0.0f;
@@ -368,6 +482,11 @@ __global__ void ZS_BOUNDS
       }
     }
     if constexpr (RECOMPUTE) sum_slices<DT, VPT>(s, n, vi, ok, a);
+    if constexpr (HACC && RECOMPUTE) {
+      bool unused = false;  // the flag pass already saw any overflow
+#pragma unroll
+      for (int j = 0; j < VPT; ++j) (void)round8_hacc<DT>(a[j], &unused);
+    }
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
       if (!ok[j]) continue;
@@ -387,8 +506,14 @@ __global__ void ZS_BOUNDS
   const int64_t tail = count - nvec * 8;
   if (tid < tail) {
     const int64_t i = nvec * 8 + tid;
-    float a = HAS_ACC ? acc[i] : 0.0f;
+    float a;
+    if constexpr (HACC) {
+      a = HAS_ACC ? half_bits_to_float<DT>(reinterpret_cast<const uint16_t*>(acc)[i]) : 0.0f;
+    } else {
+      a = HAS_ACC ? acc[i] : 0.0f;
+    }
     if constexpr (RECOMPUTE) a = sum_slices1<DT>(s, n, i, a);
+    if constexpr (HACC && RECOMPUTE) a = half_bits_to_float<DT>(float_to_half_bits<DT>(a));
     float p = master[i], m = mom[i], v = var[i];
     adamw1<CLIP>(ad, a, p, m, v, coef);
     master[i] = p;
