@@ -39,21 +39,23 @@ METRIC = "ZeRO shard-step params/s"
 
 # ---------------------------------------------------------------- byte model
 
-def alg_bytes_per_elem_step(n: int, g: int) -> int:
+def alg_bytes_per_elem_step(n: int, g: int, acc_bytes: int = 4) -> int:
     """Algorithmic bytes per owned element per step: read every gradient once
-    (2·N·G), carry the fp32 accumulator between micro-steps (8·(G-1)), read
-    and write master/m/v (24) and write the half copy (2)."""
-    return 2 * n * g + 8 * (g - 1) + 26
+    (2·N·G), carry the accumulator between micro-steps (2·acc_bytes·(G-1):
+    8 for fp32, 4 for the half accumulator), read and write master/m/v (24)
+    and write the half copy (2)."""
+    return 2 * n * g + 2 * acc_bytes * (g - 1) + 26
 
 
-def kernel_alg_bytes(kind: str, n: int, first: bool = False, with_acc: bool = False) -> int:
+def kernel_alg_bytes(kind: str, n: int, first: bool = False, with_acc: bool = False,
+                     acc_bytes: int = 4) -> int:
     """Algorithmic bytes per element of one launch of each kernel kind."""
     if kind == "reduce":
-        return 2 * n + (4 if first else 8)
+        return 2 * n + (acc_bytes if first else 2 * acc_bytes)
     if kind == "check":
         return 2 * n + (4 if with_acc else 0)
     if kind == "apply":
-        return 4 + 12 + 14
+        return acc_bytes + 12 + 14
     if kind == "apply_recompute":
         return (4 if with_acc else 0) + 2 * n + 26
     raise ValueError(kind)
@@ -65,7 +67,8 @@ class DeviceWorkload:
     """HBM-resident buffers of one owned shard of a workload: G x N gradient
     slices (half), the fp32 accumulator, fp32 master / m / v and the half copy."""
 
-    def __init__(self, wl: synth.Workload, shard: int = 0, device=None, count: int | None = None):
+    def __init__(self, wl: synth.Workload, shard: int = 0, device=None, count: int | None = None,
+                 acc: str = "fp32"):
         import torch
         import zero_mixed_precision_shard_gb300 as zs
         self.zs = zs
@@ -77,8 +80,12 @@ class DeviceWorkload:
         self.E = self.part.shard_len if count is None else count
         E, n, g = self.E, wl.n, wl.g
         self.grads = torch.empty((g, n, E), dtype=torch.int16, device=self.dev)
-        need_acc = g > 1 or n >= 4
-        self.acc = torch.empty(E, dtype=torch.float32, device=self.dev) if need_acc else None
+        self.acc_kind = acc
+        if acc == "half":
+            self.acc = torch.empty(E, dtype=torch.int16, device=self.dev)
+        else:
+            need_acc = g > 1 or n >= 4
+            self.acc = torch.empty(E, dtype=torch.float32, device=self.dev) if need_acc else None
         self.master = torch.empty(E, dtype=torch.float32, device=self.dev)
         self.m = torch.zeros(E, dtype=torch.float32, device=self.dev)
         self.v = torch.zeros(E, dtype=torch.float32, device=self.dev)
@@ -119,6 +126,15 @@ class DeviceWorkload:
     def step(self, ctx) -> int:
         """One optimizer step through the C ABI; returns the overflow flag."""
         zs, wl = self.zs, self.wl
+        if self.acc_kind == "half":
+            for k in range(wl.g - 1):
+                zs.zs_grad_accum_halfacc(ctx, self.slices(k), self.dt, self.E, self.acc, k == 0)
+            ovf, _ = zs.zs_shard_step_halfacc(ctx, self.slices(wl.g - 1), self.dt, self.E,
+                                              self.acc, wl.g, self.master, self.m, self.v,
+                                              self.half, self.hp, self.t + 1, self.scaler)
+            if not ovf:
+                self.t += 1
+            return ovf
         for k in range(wl.g - 1):
             zs.zs_grad_accum(ctx, self.slices(k), self.dt, self.E, self.acc, k == 0)
         ovf, _ = zs.zs_shard_step(ctx, self.slices(wl.g - 1), self.dt, self.E, self.acc, wl.g,
@@ -128,9 +144,22 @@ class DeviceWorkload:
             self.t += 1
         return ovf
 
+    def step_async_calls(self, ctx, state):
+        """The calls of one step on the device-resident path (capturable)."""
+        zs, wl = self.zs, self.wl
+        for k in range(wl.g - 1):
+            zs.zs_grad_accum(ctx, self.slices(k), self.dt, self.E, self.acc, k == 0)
+        zs.zs_shard_step_async(ctx, self.slices(wl.g - 1), self.dt, self.E, self.acc, wl.g,
+                               self.master, self.m, self.v, self.half, self.hp, None, state)
+
     def launch_plan(self):
         """(kind, alg bytes per element) of every kernel one step launches."""
         n, g = self.wl.n, self.wl.g
+        if self.acc_kind == "half":
+            plan = [("reduce_first" if k == 0 else "reduce",
+                     kernel_alg_bytes("reduce", n, first=(k == 0), acc_bytes=2)) for k in range(g)]
+            plan.append(("apply", kernel_alg_bytes("apply", n, acc_bytes=2)))
+            return plan
         plan = [("reduce_first" if k == 0 else "reduce",
                  kernel_alg_bytes("reduce", n, first=(k == 0))) for k in range(g - 1)]
         recompute = n < 4 or self.acc is None
@@ -361,14 +390,29 @@ def run_ours(args):
     ctx = zs.Ctx()
     probe = copy_probe(zs, ctx) if not args.skip_probe else {}
 
-    W = DeviceWorkload(wl, shard=0, count=args.elements)
+    W = DeviceWorkload(wl, shard=0, count=args.elements, acc=args.acc)
     W.fill_grads(1, wl.scale0, inject=False)
     torch.cuda.synchronize()
     E = W.E
     valid = min(W.valid_end - W.begin, E)
     flag = torch.zeros(1, dtype=torch.int32, device="cuda") if world > 1 else None
 
+    graph = None
+    dstate = None
+    if args.graph:
+        if world > 1 or args.acc != "fp32":
+            raise SystemExit("--graph runs the fp32-accumulator path on one GPU")
+        dstate = zs.DeviceState(W.scaler)
+        W.step_async_calls(ctx, dstate)      # uncaptured first call caches launch shapes
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            W.step_async_calls(ctx, dstate)
+
     def one_step():
+        if graph is not None:
+            graph.replay()
+            return 0
         if world == 1:
             return W.step(ctx)
         # replicas: each rank runs its own copy of the shard step; the one
@@ -411,6 +455,8 @@ def run_ours(args):
             dist.barrier()
     ctx.set_timing(False)
     launches = ctx.launch_count - l0
+    if graph is not None:  # replays bypass the context's counter: kernels per captured step
+        launches = args.steps * (len(plan) + 1)
     ms = ev0.elapsed_time(ev1)
     if world > 1:
         t = torch.tensor([ms], dtype=torch.float64, device="cuda")
@@ -433,9 +479,13 @@ def run_ours(args):
         avg_b = sum(per_launch) / len(per_launch) if per_launch else 0
         d["alg_bytes_per_elem"] = avg_b
         d["gbs"] = avg_b * (d["elements"] / d["launches"]) / (d["ms"] / d["launches"] * 1e-3) / 1e9
+    if not kinds:  # graph replay: no per-kernel events inside the graph
+        kinds = {"step": {"ms": ms, "launches": args.steps, "elements": E * args.steps,
+                          "alg_bytes_per_elem": step_bytes / E}}
+        kinds["step"]["gbs"] = step_bytes / (per_step_ms * 1e-3) / 1e9
     dom = max(kinds, key=lambda k: kinds[k]["ms"])
     peak, peak_kind = measured_peaks()
-    step_bytes = alg_bytes_per_elem_step(wl.n, wl.g) * E
+    step_bytes = alg_bytes_per_elem_step(wl.n, wl.g, 2 if args.acc == "half" else 4) * E
     per_launch_elems = kinds[dom]["elements"] / kinds[dom]["launches"]
     traffic = recorded_traffic(wl.name, dom, per_launch_elems) if not args.elements else None
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(kinds[dom]["gbs"], 1),
@@ -465,6 +515,9 @@ def run_ours(args):
                 "shard_len": E, "n_ranks_simulated": wl.n, "accum_steps": wl.g,
                 "grad_dtype": wl.dtype, "optimizer": "AdamW" if wl.weight_decay else "Adam",
                 "parallelism": "replicas + overflow-flag all-reduce" if world > 1 else "1 GPU",
+                "accumulator": args.acc,
+                "api": "CUDA graph of zs_grad_accum + zs_shard_step_async" if args.graph
+                       else "zs_grad_accum + zs_shard_step",
                 "l2": "inputs larger than L2 (129 MB): no flush needed",
                 "inputs": "gradients generated once on the device (step-1 values, no "
                           "injections) and reused by every timed step",
@@ -550,6 +603,10 @@ def main(argv=None):
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-probe", action="store_true")
+    ap.add_argument("--acc", default="fp32", choices=["fp32", "half"],
+                    help="accumulator format (half: zs_*_halfacc entry points)")
+    ap.add_argument("--graph", action="store_true",
+                    help="replay each step from a CUDA graph (device-resident scaler)")
     ap.add_argument("--elements", type=int, default=None,
                     help="truncate the owned shard to its first ELEMENTS elements (profiling)")
     args = ap.parse_args(argv)

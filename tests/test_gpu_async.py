@@ -50,7 +50,8 @@ def ulps(a, b):
     return np.abs(o(a) - o(b))
 
 
-SCHED = (oracle.LR_WARMUP_DECAY, 1e-5, 1e-3, 3, 9)   # kind, min, max, warmup, total
+# kind, min, max, warmup, total; the rates as the fp32 values the library receives
+SCHED = (oracle.LR_WARMUP_DECAY, float(np.float32(1e-5)), float(np.float32(1e-3)), 3, 9)
 
 
 def _run(zs, ctx, dtype, n, G, count, steps, graph, inject):

@@ -111,6 +111,7 @@ def test_overflow_flag(zs, ctx, dtype, where, kind, n):
             "nan": 0x7E00 if dtype == FP16 else 0x7FC0}[kind]
     r, i = {"first": (0, 0), "body": (2, 4321), "tail": (1, count - 2),
             "last_rank": (n - 1, count // 2)}[where]
+    r = min(r, n - 1)
     g[r][i] = bits
     assert oracle.any_nonfinite(g, dtype, count) == 1
     for acc in (torch.zeros(count, dtype=torch.float32, device="cuda"), None):
