@@ -309,32 +309,28 @@ def copy_probe(zs, ctx, nbytes: int = 4 << 30, reps: int = 5):
     return out
 
 
-def cpu_baseline(wl: synth.Workload, budget_s: float = 12.0):
+def cpu_baseline(wl: synth.Workload, budget_s: float = 12.0, max_steps: int = 10):
     """The oracle, as it stands (single-threaded C, fp64), on a contiguous
-    sample of the owned shard: G micro-steps x N ranks of gradients, one full
-    step.  Input generation is outside the timed call."""
+    sample of the owned shard (G micro-steps x N ranks of gradients): whole
+    steps are repeated on the sample until about budget_s seconds of oracle
+    time have passed.  Input generation is outside the timed calls."""
     import oracle
-    count = 1 << 14
+    count = min(1 << 24, max(1 << 14, (1 << 27) // (wl.n * wl.g)))
     idx0 = np.arange(count, dtype=np.int64)
-    rate = None
-    elapsed = 0.0
-    while True:
-        grads = [[synth.host_grad_bits(wl, idx0, 1, k + 1, r, wl.scale0, inject=False)
-                  for r in range(wl.n)] for k in range(wl.g)]
-        st = oracle.ShardState.from_master(synth.host_master(wl, idx0), wl.dtype_code)
-        hp = oracle.make_hparams(wl.lr, wl.beta1, wl.beta2, wl.eps, wl.weight_decay)
-        sc = oracle.make_scaler(wl.scale0, wl.min_scale, wl.window, wl.hysteresis, wl.dynamic)
+    grads = [[synth.host_grad_bits(wl, idx0, 1, k + 1, r, wl.scale0, inject=False)
+              for r in range(wl.n)] for k in range(wl.g)]
+    st = oracle.ShardState.from_master(synth.host_master(wl, idx0), wl.dtype_code)
+    hp = oracle.make_hparams(wl.lr, wl.beta1, wl.beta2, wl.eps, wl.weight_decay)
+    sc = oracle.make_scaler(wl.scale0, wl.min_scale, wl.window, wl.hysteresis, wl.dynamic)
+    t, steps, elapsed = 0, 0, 0.0
+    while steps < max_steps and elapsed < budget_s:
         t0 = time.perf_counter()
-        oracle.shard_step(grads, wl.dtype_code, st, hp, 0, sc)
-        elapsed = time.perf_counter() - t0
-        rate = count / elapsed
-        if elapsed > budget_s / 4 or count >= (1 << 24):
-            break
-        count = min(1 << 24, int(count * max(2.0, min(16.0, budget_s / 3 / max(elapsed, 1e-4)))))
-        idx0 = np.arange(count, dtype=np.int64)
-    return {"value": rate, "unit": "params/s", "cores": 1, "kind": "oracle",
-            "sample": f"{count} contiguous elements of the owned shard, {wl.g} micro-steps x "
-                      f"{wl.n} ranks, one step ({elapsed:.2f} s)"}
+        _, t, _ = oracle.shard_step(grads, wl.dtype_code, st, hp, t, sc)
+        elapsed += time.perf_counter() - t0
+        steps += 1
+    return {"value": count * steps / elapsed, "unit": "params/s", "cores": 1, "kind": "oracle",
+            "sample": f"{count} contiguous elements of the owned shard ({wl.g} micro-steps x "
+                      f"{wl.n} ranks), {steps} steps, {elapsed:.1f} s of oracle time"}
 
 
 # ---------------------------------------------------------------- arms

@@ -40,7 +40,8 @@
  *    count may be any value >= 0 (a ragged tail is handled).
  *  - Limits: 1 <= n <= ZS_MAX_RANKS.
  *  - Ordering: all work is issued on `stream` in order; only zs_shard_step,
- *    zs_scaler_update and zs_ctx_timing synchronise that stream.
+ *    zs_shard_step_clipped, zs_shard_step_halfacc, zs_scaler_update and
+ *    zs_ctx_timing synchronise that stream (zs_shard_step_async never does).
  *  - Errors: a non-zero zs_status; zs_last_error(ctx) gives the message.
  *    Overflow of the gradients is a result, not an error.
  *  - Threads: a context is used by one host thread at a time.

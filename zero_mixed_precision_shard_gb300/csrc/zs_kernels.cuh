@@ -79,8 +79,11 @@ struct SlicePtrs {
 
 // Per-launch constants of the AdamW update, computed on the host once per
 // call (bias corrections in double, rounded to fp32).
+// The bias corrections 1/(1-beta^t) are carried as fp32 pairs (hi + lo) so
+// that their rounding does not bias every element of a step the same way.
 struct AdamArgs {
   float lr, beta1, omb1, beta2, omb2, eps, wd, inv_bc1, inv_bc2, grad_div;
+  float inv_bc1_lo, inv_bc2_lo;
 };
 
 // Result of the loss-scale update, written by one thread of the update kernel.
@@ -238,10 +241,10 @@ __device__ __forceinline__ void adamw1(const AdamArgs& ad, float sum, float& p, 
   if constexpr (CLIP) g = __fmul_rn(g, coef);
   m = __fmaf_rn(ad.beta1, m, __fmul_rn(ad.omb1, g));
   v = __fmaf_rn(ad.beta2, v, __fmul_rn(ad.omb2, __fmul_rn(g, g)));
-  const float m_hat = __fmul_rn(m, ad.inv_bc1);
-  const float v_hat = __fmul_rn(v, ad.inv_bc2);
+  const float m_hat = __fmaf_rn(m, ad.inv_bc1, __fmul_rn(m, ad.inv_bc1_lo));
+  const float v_hat = __fmaf_rn(v, ad.inv_bc2, __fmul_rn(v, ad.inv_bc2_lo));
   const float upd = __fdiv_rn(m_hat, __fadd_rn(__fsqrt_rn(v_hat), ad.eps));
-  p = __fsub_rn(p, __fmul_rn(ad.lr, __fmaf_rn(ad.wd, p, upd)));
+  p = __fmaf_rn(-ad.lr, __fmaf_rn(ad.wd, p, upd), p);
 }
 
 __device__ __forceinline__ zs_scaler next_scaler(zs_scaler s, int overflow) {
@@ -313,8 +316,12 @@ __global__ void k_step_prologue(const zs_device_state* __restrict__ st, int n, i
   a.omb2 = 1.0f - hp.beta2;
   a.eps = hp.eps;
   a.wd = hp.weight_decay;
-  a.inv_bc1 = (float)(1.0 / (1.0 - pow((double)hp.beta1, (double)t)));
-  a.inv_bc2 = (float)(1.0 / (1.0 - pow((double)hp.beta2, (double)t)));
+  const double ib1 = 1.0 / (1.0 - pow((double)hp.beta1, (double)t));
+  const double ib2 = 1.0 / (1.0 - pow((double)hp.beta2, (double)t));
+  a.inv_bc1 = (float)ib1;
+  a.inv_bc2 = (float)ib2;
+  a.inv_bc1_lo = (float)(ib1 - (double)a.inv_bc1);
+  a.inv_bc2_lo = (float)(ib2 - (double)a.inv_bc2);
   a.grad_div = (float)((double)n * (double)accum_steps * (double)st->scaler.scale);
   *out = a;
 }
