@@ -393,6 +393,8 @@ def run_ours(args):
     valid = min(W.valid_end - W.begin, E)
     flag = torch.zeros(1, dtype=torch.int32, device="cuda") if world > 1 else None
 
+    if world > 1 and args.acc != "fp32":
+        raise SystemExit("--acc half runs on one GPU")
     graph = None
     dstate = None
     if args.graph:
@@ -414,21 +416,28 @@ def run_ours(args):
         # replicas: each rank runs its own copy of the shard step; the one
         # real exchange is the overflow flag, all-reduced on the device before
         # any state is written, so every rank skips together
-        flag.zero_()
-        for k in range(wl.g):
-            last = k == wl.g - 1
-            if last and W.acc is None:
-                zs.zs_reduce_check(ctx, W.slices(k), W.dt, E, None, True, flag)
-            else:
-                zs.zs_reduce_check(ctx, W.slices(k), W.dt, E, W.acc, k == 0, flag)
-        dist.all_reduce(flag, op=dist.ReduceOp.MAX)
-        zs.zs_apply(ctx, flag, W.slices(wl.g - 1) if W.acc is None else None, W.dt, W.acc, E,
-                    float(wl.n * wl.g * W.scaler.scale), W.master, W.m, W.v, W.half, W.hp,
-                    W.t + 1)
-        ovf = zs.zs_scaler_update(ctx, flag, W.scaler)
-        if not ovf:
-            W.t += 1
-        return ovf
+        from zero_mixed_precision_shard_gb300.dp import dp_shard_step
+
+        def reduce_last(f):
+            f.zero_()
+            for k in range(wl.g):
+                if k == wl.g - 1 and W.acc is None:
+                    zs.zs_reduce_check(ctx, W.slices(k), W.dt, E, None, True, f)
+                else:
+                    zs.zs_reduce_check(ctx, W.slices(k), W.dt, E, W.acc, k == 0, f)
+
+        def apply(f):
+            zs.zs_apply(ctx, f, W.slices(wl.g - 1) if W.acc is None else None, W.dt, W.acc, E,
+                        float(wl.n * wl.g * W.scaler.scale), W.master, W.m, W.v, W.half, W.hp,
+                        W.t + 1)
+
+        def scaler_update(f):
+            ovf = zs.zs_scaler_update(ctx, f, W.scaler)
+            if not ovf:
+                W.t += 1
+            return ovf
+
+        return dp_shard_step(reduce_last, apply, scaler_update, flag)
 
     for _ in range(args.warmup):
         one_step()

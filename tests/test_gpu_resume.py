@@ -19,11 +19,15 @@ def zs():
 
 
 def make_grads(step, n, g, count, scale):
+    """[g][n] slices of `count` halves; rows padded to 8 elements so every
+    slice starts 16-byte aligned."""
     rng = np.random.default_rng(1000 + step)
-    x = (rng.standard_normal((g, n, count)) * 1e-2 * scale).astype(np.float16)
+    pad = (count + 7) // 8 * 8
+    x = np.zeros((g, n, pad), np.float16)
+    x[:, :, :count] = (rng.standard_normal((g, n, count)) * 1e-2 * scale).astype(np.float16)
     if step == 4:
         x[0, n - 1, 7] = np.inf
-    return torch.from_numpy(x.view(np.int16)).cuda()
+    return torch.from_numpy(x.view(np.int16)).cuda()[:, :, :count]
 
 
 def run(zs, ctx, state, first_step, last_step, n, g, count):

@@ -13,6 +13,8 @@
 #include <unordered_map>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "zeroshard.h"
 #include "zs_kernels.cuh"
 
@@ -48,6 +50,12 @@ struct zs_ctx {
 };
 
 namespace {
+
+// NVTX range around each entry point (visible to ncu/nsys; a no-op otherwise).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
 
 zs_status fail(zs_ctx* c, zs_status code, const char* fmt, ...) {
   if (c != nullptr) {
@@ -591,6 +599,7 @@ zs_status zs_ctx_overflow_flag(zs_ctx* c, int32_t** d_flag) {
 zs_status zs_reduce_check(zs_ctx* c, const void* const* grads, int32_t n, zs_dtype dt,
                           int64_t count, float* acc, int32_t first, int32_t* d_flag,
                           cudaStream_t stream) {
+  NvtxRange nvtx_("zs_reduce_check");
   ZS_TRY(check_ctx(c));
   if (dt != ZS_FP16 && dt != ZS_BF16) return fail(c, ZS_ERR_DTYPE, "unknown dtype %d", (int)dt);
   if (count < 0) return fail(c, ZS_ERR_ARG, "count < 0");
@@ -607,6 +616,7 @@ zs_status zs_reduce_check(zs_ctx* c, const void* const* grads, int32_t n, zs_dty
 
 zs_status zs_grad_accum(zs_ctx* c, const void* const* grads, int32_t n, zs_dtype dt,
                         int64_t count, float* acc, int32_t first, cudaStream_t stream) {
+  NvtxRange nvtx_("zs_grad_accum");
   ZS_TRY(check_ctx(c));
   if (count > 0 && acc == nullptr) return fail(c, ZS_ERR_ARG, "acc is NULL");
   return zs_reduce_check(c, grads, n, dt, count, acc, first, c->d_flag, stream);
@@ -616,6 +626,7 @@ zs_status zs_apply(zs_ctx* c, const int32_t* d_flag, const void* const* grads, i
                    zs_dtype dt, const float* acc, int64_t count, float grad_div, float* master,
                    float* m, float* v, void* half_out, const zs_adam_hparams* hp, int64_t step,
                    cudaStream_t stream) {
+  NvtxRange nvtx_("zs_apply");
   ZS_TRY(check_ctx(c));
   if (dt != ZS_FP16 && dt != ZS_BF16) return fail(c, ZS_ERR_DTYPE, "unknown dtype %d", (int)dt);
   if (count < 0) return fail(c, ZS_ERR_ARG, "count < 0");
@@ -642,6 +653,7 @@ zs_status zs_apply(zs_ctx* c, const int32_t* d_flag, const void* const* grads, i
 
 zs_status zs_scaler_update(zs_ctx* c, const int32_t* d_flag, zs_scaler* scaler,
                            int32_t* overflow_out, cudaStream_t stream) {
+  NvtxRange nvtx_("zs_scaler_update");
   ZS_TRY(check_ctx(c));
   if (d_flag == nullptr) return fail(c, ZS_ERR_ARG, "d_flag is NULL");
   ZS_TRY(check_scaler(c, scaler));
@@ -722,6 +734,7 @@ zs_status zs_shard_step(zs_ctx* c, const void* const* grads, int32_t n, zs_dtype
                         float* v, void* half_out, const zs_adam_hparams* hp, int64_t step,
                         zs_scaler* scaler, int32_t* overflow_out, float* new_scale_out,
                         cudaStream_t stream) {
+  NvtxRange nvtx_("zs_shard_step");
   return shard_step_impl(c, grads, n, dt, count, acc, accum_steps, master, m, v, half_out, hp,
                          step, scaler, 0.0f, overflow_out, new_scale_out, nullptr, stream);
 }
@@ -732,6 +745,7 @@ zs_status zs_shard_step_clipped(zs_ctx* c, const void* const* grads, int32_t n, 
                                 int64_t step, zs_scaler* scaler, float max_norm,
                                 int32_t* overflow_out, float* new_scale_out,
                                 float* grad_norm_out, cudaStream_t stream) {
+  NvtxRange nvtx_("zs_shard_step_clipped");
   return shard_step_impl(c, grads, n, dt, count, acc, accum_steps, master, m, v, half_out, hp,
                          step, scaler, max_norm, overflow_out, new_scale_out, grad_norm_out,
                          stream);
@@ -742,6 +756,7 @@ zs_status zs_shard_step_async(zs_ctx* c, const void* const* grads, int32_t n, zs
                               float* m, float* v, void* half_out, const zs_adam_hparams* hp,
                               const zs_lr_schedule* sched, zs_device_state* d_state,
                               cudaStream_t stream) {
+  NvtxRange nvtx_("zs_shard_step_async");
   ZS_TRY(check_ctx(c));
   if (dt != ZS_FP16 && dt != ZS_BF16) return fail(c, ZS_ERR_DTYPE, "unknown dtype %d", (int)dt);
   if (count < 0) return fail(c, ZS_ERR_ARG, "count < 0");
@@ -803,6 +818,7 @@ zs_status zs_shard_step_async(zs_ctx* c, const void* const* grads, int32_t n, zs
 zs_status zs_grad_accum_halfacc(zs_ctx* c, const void* const* grads, int32_t n, zs_dtype dt,
                                 int64_t count, void* acc_half, int32_t first,
                                 cudaStream_t stream) {
+  NvtxRange nvtx_("zs_grad_accum_halfacc");
   ZS_TRY(check_ctx(c));
   if (dt != ZS_FP16 && dt != ZS_BF16) return fail(c, ZS_ERR_DTYPE, "unknown dtype %d", (int)dt);
   if (count < 0) return fail(c, ZS_ERR_ARG, "count < 0");
@@ -819,6 +835,7 @@ zs_status zs_shard_step_halfacc(zs_ctx* c, const void* const* grads, int32_t n, 
                                 const zs_adam_hparams* hp, int64_t step, zs_scaler* scaler,
                                 int32_t* overflow_out, float* new_scale_out,
                                 cudaStream_t stream) {
+  NvtxRange nvtx_("zs_shard_step_halfacc");
   ZS_TRY(check_ctx(c));
   if (dt != ZS_FP16 && dt != ZS_BF16) return fail(c, ZS_ERR_DTYPE, "unknown dtype %d", (int)dt);
   if (count < 0) return fail(c, ZS_ERR_ARG, "count < 0");
@@ -847,6 +864,7 @@ zs_status zs_shard_step_halfacc(zs_ctx* c, const void* const* grads, int32_t n, 
 zs_status zs_grad_sumsq(zs_ctx* c, const void* const* grads, int32_t n, zs_dtype dt,
                         const float* acc, int64_t count, float grad_div, double* d_sumsq,
                         cudaStream_t stream) {
+  NvtxRange nvtx_("zs_grad_sumsq");
   ZS_TRY(check_ctx(c));
   if (dt != ZS_FP16 && dt != ZS_BF16) return fail(c, ZS_ERR_DTYPE, "unknown dtype %d", (int)dt);
   if (count < 0) return fail(c, ZS_ERR_ARG, "count < 0");
@@ -873,6 +891,7 @@ zs_status zs_apply_clipped(zs_ctx* c, const int32_t* d_flag, const double* d_sum
                            const float* acc, int64_t count, float grad_div, float* master,
                            float* m, float* v, void* half_out, const zs_adam_hparams* hp,
                            int64_t step, cudaStream_t stream) {
+  NvtxRange nvtx_("zs_apply_clipped");
   ZS_TRY(check_ctx(c));
   if (!std::isfinite(max_norm)) return fail(c, ZS_ERR_ARG, "max_norm must be finite");
   if (max_norm <= 0.0f)
@@ -905,6 +924,7 @@ zs_status zs_apply_clipped(zs_ctx* c, const int32_t* d_flag, const double* d_sum
 
 zs_status zs_copy_peak(zs_ctx* c, const void* src, void* dst, int64_t bytes, int32_t read_only,
                        cudaStream_t stream) {
+  NvtxRange nvtx_("zs_copy_peak");
   ZS_TRY(check_ctx(c));
   if (bytes < 0 || bytes % 16 != 0) return fail(c, ZS_ERR_ARG, "bytes must be a multiple of 16");
   ZS_TRY(check_array(c, src, "src", bytes));
