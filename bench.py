@@ -484,13 +484,13 @@ def run_ours(args):
         avg_b = sum(per_launch) / len(per_launch) if per_launch else 0
         d["alg_bytes_per_elem"] = avg_b
         d["gbs"] = avg_b * (d["elements"] / d["launches"]) / (d["ms"] / d["launches"] * 1e-3) / 1e9
+    step_bytes = alg_bytes_per_elem_step(wl.n, wl.g, 2 if args.acc == "half" else 4) * E
     if not kinds:  # graph replay: no per-kernel events inside the graph
         kinds = {"step": {"ms": ms, "launches": args.steps, "elements": E * args.steps,
                           "alg_bytes_per_elem": step_bytes / E}}
         kinds["step"]["gbs"] = step_bytes / (per_step_ms * 1e-3) / 1e9
     dom = max(kinds, key=lambda k: kinds[k]["ms"])
     peak, peak_kind = measured_peaks()
-    step_bytes = alg_bytes_per_elem_step(wl.n, wl.g, 2 if args.acc == "half" else 4) * E
     per_launch_elems = kinds[dom]["elements"] / kinds[dom]["launches"]
     traffic = recorded_traffic(wl.name, dom, per_launch_elems) if not args.elements else None
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(kinds[dom]["gbs"], 1),
