@@ -86,6 +86,27 @@ cudaEvent_t take_event(zs_ctx* c) {
   return e;
 }
 
+// Folds finished timing records into the totals without blocking, so a
+// context that keeps timing on for a long run holds a bounded set of events.
+void fold_finished(zs_ctx* c) {
+  size_t keep = 0;
+  for (size_t i = 0; i < c->pending.size(); ++i) {
+    auto& r = c->pending[i];
+    float ms = 0.0f;
+    if (cudaEventQuery(r.stop) == cudaSuccess &&
+        cudaEventElapsedTime(&ms, r.start, r.stop) == cudaSuccess) {
+      c->total_ms[r.kind] += ms;
+      c->total_launches[r.kind] += 1;
+      c->total_elements[r.kind] += r.elements;
+      c->pool.push_back(r.start);
+      c->pool.push_back(r.stop);
+    } else {
+      c->pending[keep++] = r;
+    }
+  }
+  c->pending.resize(keep);
+}
+
 // Bracket one launch with events when timing is on.
 struct LaunchScope {
   zs_ctx* c;
@@ -107,6 +128,7 @@ struct LaunchScope {
       if (stop) {
         cudaEventRecord(stop, s);
         c->pending.push_back({kind, start, stop, elements});
+        if (c->pending.size() >= 1024) fold_finished(c);
       } else {
         c->pool.push_back(start);
       }
@@ -196,7 +218,9 @@ void launch_reduce_k(zs_ctx* c, const zs::SlicePtrs& sp, int32_t n, float* acc, 
 template <int DT, bool RA, bool ST>
 void launch_reduce_v(zs_ctx* c, const zs::SlicePtrs& sp, int32_t n, float* acc, int64_t count,
                      int32_t* flag, cudaStream_t s) {
-  const int vpt = (!ST && n <= 2) ? ZS_CHECK_VPT : vpt_for(n);
+  const int vpt = (!ST && n <= 2)  ? ZS_CHECK_VPT
+                  : (!RA && n <= 2) ? ZS_VPT_FIRST_SMALL_N
+                                    : vpt_for(n);
   switch (vpt) {
     case 8: launch_reduce_k<DT, RA, ST, 8>(c, sp, n, acc, count, flag, s); break;
     case 4: launch_reduce_k<DT, RA, ST, 4>(c, sp, n, acc, count, flag, s); break;
@@ -426,8 +450,9 @@ void apply_dev(zs_ctx* c, const int32_t* flag, const zs::SlicePtrs& sp, int32_t 
 template <int DT, bool RA>
 void launch_reduce_hacc_k(zs_ctx* c, const zs::SlicePtrs& sp, int32_t n, float* acc,
                           int64_t count, int32_t* flag, cudaStream_t s) {
-  const int64_t units = (count >> 3) + 8;
-  auto k = zs::k_reduce<DT, RA, true, 1, true>;
+  constexpr int VPT = ZS_HACC_VPT;
+  const int64_t units = (count >> 3) / VPT + 8;
+  auto k = zs::k_reduce<DT, RA, true, VPT, true>;
   k<<<grid_for(c, k, units), zs::kThreads, 0, s>>>(sp, n, acc, count, flag);
 }
 

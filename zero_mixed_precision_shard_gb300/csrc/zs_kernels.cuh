@@ -42,6 +42,12 @@
 #ifndef ZS_VPT_SMALL_N  // vector units per thread per trip when n <= 2
 #define ZS_VPT_SMALL_N 1
 #endif
+#ifndef ZS_VPT_FIRST_SMALL_N  // ... for the first micro-step (no accumulator read), n <= 2
+#define ZS_VPT_FIRST_SMALL_N 1
+#endif
+#ifndef ZS_HACC_VPT  // vector units per thread of the half-accumulator reduce
+#define ZS_HACC_VPT 1
+#endif
 #ifndef ZS_VPT_MID_N  // ... when 2 < n <= 8
 #define ZS_VPT_MID_N 1
 #endif
