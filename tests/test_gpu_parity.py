@@ -393,3 +393,23 @@ def test_copy_probe_copies(zs, ctx):
     zs.zs_copy_peak(ctx, src, dst, src.numel() * 4, False)
     assert torch.equal(src, dst)
     zs.zs_copy_peak(ctx, src, dst, src.numel() * 4, True)
+
+
+def test_timing_counters_over_many_launches(zs):
+    """Per-kernel event timing: every launch is counted, finished records are
+    folded without blocking, and the totals survive more than a thousand
+    launches with timing left on."""
+    ctx = zs.Ctx()
+    count = 4096
+    g = [torch.zeros(count, dtype=torch.int16, device="cuda")]
+    acc = torch.zeros(count, dtype=torch.float32, device="cuda")
+    ctx.set_timing(True)
+    for k in range(1500):
+        zs.zs_grad_accum(ctx, g, FP16, count, acc, k == 0)
+    ms, n_later, el = ctx.timing(zs.ZS_KERNEL_REDUCE)
+    _, n_first, _ = ctx.timing(zs.ZS_KERNEL_REDUCE_FIRST)
+    assert n_first == 1 and n_later == 1499 and el == 1499 * count and ms > 0
+    ctx.timing_reset()
+    assert ctx.timing(zs.ZS_KERNEL_REDUCE) == (0.0, 0, 0)
+    assert ctx.launch_count == 1500
+    ctx.close()
