@@ -413,3 +413,28 @@ def test_timing_counters_over_many_launches(zs):
     assert ctx.timing(zs.ZS_KERNEL_REDUCE) == (0.0, 0, 0)
     assert ctx.launch_count == 1500
     ctx.close()
+
+
+def test_context_flag_is_the_step_flag(zs):
+    """zs_ctx_overflow_flag exposes the flag zs_grad_accum ORs into: a caller
+    can hand it to the two-phase calls (or all-reduce it) and zs_shard_step
+    clears it."""
+    ctx = zs.Ctx()
+    count = 1000
+    bad = np.zeros(count, np.uint16)
+    bad[3] = 0x7C00
+    acc = torch.zeros(count, dtype=torch.float32, device="cuda")
+    zs.zs_grad_accum(ctx, [dev16(bad)], FP16, count, acc, True)
+    sc = zs.zs_scaler_init(64.0, 1.0, 1000, 1, True)
+    assert zs.zs_scaler_update(ctx, ctx.overflow_flag_ptr, sc) == 1 and sc.scale == 32.0
+    master = torch.zeros(count, dtype=torch.float32, device="cuda")
+    m, v = torch.zeros_like(master), torch.zeros_like(master)
+    half = torch.zeros(count, dtype=torch.int16, device="cuda")
+    good = dev16(np.zeros(count, np.uint16))
+    ovf, _ = zs.zs_shard_step(ctx, [good], FP16, count, acc, 2, master, m, v, half,
+                              zs.make_hparams(1e-3), 1, sc)
+    assert ovf == 1   # micro-step 1's inf still counts
+    ovf, _ = zs.zs_shard_step(ctx, [good], FP16, count, None, 1, master, m, v, half,
+                              zs.make_hparams(1e-3), 1, sc)
+    assert ovf == 0   # the previous step cleared the flag
+    ctx.close()

@@ -602,3 +602,57 @@ def test_half_accumulator_equals_fp32_when_sums_are_representable():
     oracle.shard_step_halfacc(grads, FP16, b, hp, 0, oracle.make_scaler(16.0))
     for k in ("master", "m", "v", "half"):
         assert getattr(a, k).tobytes() == getattr(b, k).tobytes()
+
+
+# ---------------------------------------------------------------- randomized invariants
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_union_and_bucket_invariance(seed):
+    """Random layouts: the union of N shard steps (global flag, one scale) equals
+    the unpartitioned step bit for bit, and so does any bucketing of one shard."""
+    rng = np.random.default_rng(100 + seed)
+    psi = int(rng.integers(1, 3000))
+    n = int(rng.integers(1, 9))
+    g = int(rng.integers(1, 4))
+    align = int(rng.choice([1, 8, 64]))
+    dtype = int(rng.integers(0, 2))
+    psi_pad, E = oracle.partition(psi, n, align)
+    hp = oracle.make_hparams(float(rng.choice([1e-4, 3e-4, 1e-3])), 0.9, 0.999, 1e-8,
+                             float(rng.choice([0.0, 0.01, 0.1])))
+    master0 = np.zeros(psi_pad, np.float32)
+    master0[:psi] = rng.standard_normal(psi) * 0.02
+    scale = 256.0 if dtype == FP16 else 1.0
+    grads = []
+    for _ in range(g):
+        micro = []
+        for _ in range(n):
+            x = np.zeros(psi_pad, np.float32)
+            x[:psi] = rng.standard_normal(psi) * 1e-2 * scale
+            micro.append(_lib_half(x, dtype))
+        grads.append(micro)
+    if rng.random() < 0.3:
+        grads[int(rng.integers(0, g))][int(rng.integers(0, n))][int(rng.integers(0, psi))] = \
+            0x7C00 if dtype == FP16 else 0x7F80
+    full = oracle.ShardState.from_master(master0, dtype)
+    sc_a = oracle.make_scaler(scale, dynamic=(dtype == FP16))
+    ovf_a, t_a, acc_full = oracle.shard_step(grads, dtype, full, hp, 0, sc_a)
+    shards = [oracle.ShardState.from_master(master0[q * E:(q + 1) * E], dtype) for q in range(n)]
+    per = [[[np.ascontiguousarray(s[q * E:(q + 1) * E]) for s in micro] for micro in grads]
+           for q in range(n)]
+    sc_b = oracle.make_scaler(scale, dynamic=(dtype == FP16))
+    ovf_b, t_b, _ = oracle.multi_shard_step(per, dtype, shards, hp, 0, sc_b)
+    assert (ovf_a, t_a, sc_a.scale) == (ovf_b, t_b, sc_b.scale)
+    for name in ("master", "m", "v", "half"):
+        cat = np.concatenate([getattr(s, name) for s in shards])
+        assert cat.tobytes() == getattr(full, name).tobytes()
+    # bucketing of shard 0's accumulation
+    bucket = int(rng.integers(1, max(2, E)))
+    acc_b = np.zeros(E, np.float32)
+    for b in range(0, E, bucket):
+        e = min(E, b + bucket)
+        part = np.zeros(e - b, np.float32)
+        for k in range(g):
+            oracle.reduce_accumulate([np.ascontiguousarray(s[b:e]) for s in per[0][k]], dtype,
+                                     part, first=(k == 0))
+        acc_b[b:e] = part
+    assert acc_b.tobytes() == acc_full[:E].tobytes()
