@@ -247,7 +247,11 @@ zs_status zs_apply_clipped(zs_ctx* ctx, const int32_t* d_flag, const double* d_s
 
 /* zs_shard_step with global-norm clipping, where the owned shard holds the
  * whole gradient whose norm is clipped (one rank; or a caller that clips per
- * shard).  *grad_norm_out (may be NULL) gets the norm, 0 on a skipped step. */
+ * shard).  *grad_norm_out (may be NULL) gets the norm, 0 on a skipped step.
+ * The norm is computed inside the last micro-step's pass (the one that sums
+ * into acc, or the flag pass of the re-read path, which then also reads acc),
+ * so clipping adds no pass over the shard; its per-CTA partial sums live in
+ * context scratch that grows to the grid size on first use. */
 zs_status zs_shard_step_clipped(zs_ctx* ctx, const void* const* grads, int32_t n, zs_dtype dt,
                                 int64_t count, float* acc, int32_t accum_steps, float* master,
                                 float* m, float* v, void* half_out, const zs_adam_hparams* hp,

@@ -29,6 +29,8 @@ struct zs_ctx {
   double* d_sumsq = nullptr;           // the step's squared gradient norm (zs_shard_step_clipped)
   float* d_coef = nullptr;             // scratch: clipping coefficient
   zs::AdamArgs* d_args = nullptr;      // scratch: per-step constants of the async step
+  double* d_norm_parts = nullptr;      // scratch: per-CTA norm partials of the fused pass
+  int norm_cap = 0;                    // capacity of d_norm_parts (doubles)
   double* h_sumsq = nullptr;           // pinned mirror of d_sumsq
   zs::StepResult* d_result = nullptr;  // written by the loss-scale update
   zs::StepResult* h_result = nullptr;  // pinned mirror
@@ -212,7 +214,57 @@ void launch_reduce_k(zs_ctx* c, const zs::SlicePtrs& sp, int32_t n, float* acc, 
   const int64_t units = (count >> 3) / VPT + 8;
   auto k = zs::k_reduce<DT, RA, ST, VPT>;
   const int waves = ST ? ZS_GRID_WAVES : ZS_CHECK_WAVES;
-  k<<<grid_for(c, k, units, waves), zs::kThreads, 0, s>>>(sp, n, acc, count, flag);
+  k<<<grid_for(c, k, units, waves), zs::kThreads, 0, s>>>(sp, n, acc, count, flag, nullptr);
+}
+
+// The last micro-step's pass with the clipping norm fused in: per-CTA sums of
+// squares of the final sums into the context's partials (grown on demand).
+template <int DT, bool RA, bool ST>
+zs_status launch_reduce_norm_k(zs_ctx* c, const zs::SlicePtrs& sp, int32_t n, float* acc,
+                               int64_t count, int32_t* flag, int* nparts, cudaStream_t s) {
+  auto k = zs::k_reduce<DT, RA, ST, 1, false, true>;
+  const int grid = grid_for(c, k, (count >> 3) + 8, ZS_GRID_WAVES);
+  if (grid > c->norm_cap) {
+    if (c->d_norm_parts) cudaFree(c->d_norm_parts);
+    c->d_norm_parts = nullptr;
+    c->norm_cap = 0;
+    const int cap = (grid + 4095) / 4096 * 4096;
+    cudaError_t e = cudaMalloc(&c->d_norm_parts, (size_t)cap * sizeof(double));
+    if (e != cudaSuccess) return cuda_fail(c, e, "norm partials");
+    c->norm_cap = cap;
+  }
+  k<<<grid, zs::kThreads, 0, s>>>(sp, n, acc, count, flag, c->d_norm_parts);
+  *nparts = grid;
+  return ZS_OK;
+}
+
+zs_status reduce_norm_any(zs_ctx* c, zs_dtype dt, const zs::SlicePtrs& sp, int32_t n, float* acc,
+                          int64_t count, bool read_acc, bool store, int32_t* flag, float grad_div,
+                          double* out, cudaStream_t s) {
+  const int kind = store ? (read_acc ? ZS_KERNEL_REDUCE : ZS_KERNEL_REDUCE_FIRST)
+                         : ZS_KERNEL_CHECK;
+  LaunchScope ls(c, s, kind, count);
+  int nparts = 0;
+  zs_status st;
+  if (dt == ZS_FP16) {
+    if (store && read_acc) st = launch_reduce_norm_k<ZS_FP16, true, true>(c, sp, n, acc, count, flag, &nparts, s);
+    else if (store) st = launch_reduce_norm_k<ZS_FP16, false, true>(c, sp, n, acc, count, flag, &nparts, s);
+    else if (read_acc) st = launch_reduce_norm_k<ZS_FP16, true, false>(c, sp, n, acc, count, flag, &nparts, s);
+    else st = launch_reduce_norm_k<ZS_FP16, false, false>(c, sp, n, acc, count, flag, &nparts, s);
+  } else {
+    if (store && read_acc) st = launch_reduce_norm_k<ZS_BF16, true, true>(c, sp, n, acc, count, flag, &nparts, s);
+    else if (store) st = launch_reduce_norm_k<ZS_BF16, false, true>(c, sp, n, acc, count, flag, &nparts, s);
+    else if (read_acc) st = launch_reduce_norm_k<ZS_BF16, true, false>(c, sp, n, acc, count, flag, &nparts, s);
+    else st = launch_reduce_norm_k<ZS_BF16, false, false>(c, sp, n, acc, count, flag, &nparts, s);
+  }
+  if (st != ZS_OK) return st;
+  const double div = (double)grad_div;
+  zs::k_sumsq_finalize<<<1, zs::kThreads, 0, s>>>(c->d_norm_parts, nparts, 1.0 / (div * div), out);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(c, e, "reduce launch");
+  ls.done();
+  c->launches += 1;  // the finalize kernel
+  return ZS_OK;
 }
 
 template <int DT, bool RA, bool ST>
@@ -453,7 +505,7 @@ void launch_reduce_hacc_k(zs_ctx* c, const zs::SlicePtrs& sp, int32_t n, float* 
   constexpr int VPT = ZS_HACC_VPT;
   const int64_t units = (count >> 3) / VPT + 8;
   auto k = zs::k_reduce<DT, RA, true, VPT, true>;
-  k<<<grid_for(c, k, units), zs::kThreads, 0, s>>>(sp, n, acc, count, flag);
+  k<<<grid_for(c, k, units), zs::kThreads, 0, s>>>(sp, n, acc, count, flag, nullptr);
 }
 
 zs_status reduce_hacc(zs_ctx* c, zs_dtype dt, const zs::SlicePtrs& sp, int32_t n, void* acc,
@@ -609,6 +661,7 @@ zs_status zs_ctx_destroy(zs_ctx* c) {
   cudaFree(c->d_coef);
   cudaFreeHost(c->h_sumsq);
   cudaFree(c->d_args);
+  if (c->d_norm_parts) cudaFree(c->d_norm_parts);
   delete c;
   return ZS_OK;
 }
@@ -720,7 +773,13 @@ static zs_status shard_step_impl(zs_ctx* c, const void* const* grads, int32_t n,
   const bool recompute = (n < 4) || acc == nullptr;
   const bool clip = max_norm > 0.0f;
   const float* acc_in = (accum_steps > 1 || !recompute) ? acc : nullptr;
-  if (count > 0) {
+  if (count > 0 && clip) {
+    // the last micro-step's pass also produces the clipping norm: materialise
+    // (sums into acc) or, on the re-read path, sums acc + the last slices
+    const bool read = recompute ? acc_in != nullptr : accum_steps > 1;
+    ZS_TRY(reduce_norm_any(c, dt, sp, n, recompute ? const_cast<float*>(acc_in) : acc, count,
+                           read, !recompute, c->d_flag, grad_div, c->d_sumsq, stream));
+  } else if (count > 0) {
     if (recompute) {
       // fp16: finite halves cannot sum past the fp32 maximum, so a check of
       // the last slices alone decides; bf16 sums on top of acc as the update will.
@@ -732,10 +791,7 @@ static zs_status shard_step_impl(zs_ctx* c, const void* const* grads, int32_t n,
     }
   }
   if (clip) {
-    if (count > 0) {
-      ZS_TRY(sumsq_any(c, dt, sp, recompute ? n : 0, recompute, acc_in, count, grad_div,
-                       c->d_partials, c->d_sumsq, stream));
-    } else {
+    if (count == 0) {
       cudaError_t e = cudaMemsetAsync(c->d_sumsq, 0, sizeof(double), stream);
       if (e != cudaSuccess) return cuda_fail(c, e, "sumsq reset");
     }

@@ -334,16 +334,54 @@ __global__ void k_step_prologue(const zs_device_state* __restrict__ st, int n, i
 
 // ---------------------------------------------------------------- kernels
 
+// Square of one final gradient sum, accumulated in fp64.  Squares are formed
+// in fp32 unless they would overflow it (|a| > 1e18).
+__device__ __forceinline__ double sq8(const float a[8]) {
+  float q[8];
+  bool big = false;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    q[k] = __fmul_rn(a[k], a[k]);
+    big |= fabsf(a[k]) > 1e18f;
+  }
+  if (big) {
+    double d = 0.0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) d += (double)a[k] * (double)a[k];
+    return d;
+  }
+  const float s01 = __fadd_rn(q[0], q[1]), s23 = __fadd_rn(q[2], q[3]);
+  const float s45 = __fadd_rn(q[4], q[5]), s67 = __fadd_rn(q[6], q[7]);
+  return (double)__fadd_rn(__fadd_rn(s01, s23), __fadd_rn(s45, s67));
+}
+
+// Fixed-order CTA sum of one double per thread; the result is valid in thread 0.
+__device__ __forceinline__ double block_sum(double x) {
+  __shared__ double warp_part[kThreads / 32];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x += __shfl_down_sync(0xffffffffu, x, off);
+  if ((threadIdx.x & 31) == 0) warp_part[threadIdx.x >> 5] = x;
+  __syncthreads();
+  double t = 0.0;
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < kThreads / 32; ++w) t += warp_part[w];
+  }
+  return t;
+}
+
 // Reduce + accumulate + flag.  READ_ACC: start from acc (else +0.0f).
 // STORE: write the sums back to acc (otherwise only the flag is produced).
 // VPT vector units per thread per trip, `stride` apart so each load
 // instruction of a warp covers 512 contiguous bytes.
-template <int DT, bool READ_ACC, bool STORE, int VPT, bool HACC = false>
+template <int DT, bool READ_ACC, bool STORE, int VPT, bool HACC = false, bool NORM = false>
 __global__ void ZS_BOUNDS
     k_reduce(const __grid_constant__ SlicePtrs s, int n, float* __restrict__ acc, int64_t count,
-             int32_t* __restrict__ flag) {
+             int32_t* __restrict__ flag, double* __restrict__ partials = nullptr) {
   // HACC: acc holds count halves of the gradient's format; each sum is rounded
   // to it, and the flag tests the rounded value.
+  // NORM: also writes this CTA's sum of squares of the sums to partials[blockIdx.x]
+  // (the clipping norm of the last micro-step, fused into its pass).
+  double sq = 0.0;
   const int64_t nvec = count >> 3;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
@@ -379,6 +417,7 @@ __global__ void ZS_BOUNDS
         for (int k = 0; k < 8; ++k) bad |= not_finite(a[j][k]);
         if constexpr (STORE) store8_acc(acc + vi[j] * 8, a[j]);
       }
+      if constexpr (NORM) sq += sq8(a[j]);
     }
   }
   const int64_t tail = count - nvec * 8;
@@ -396,7 +435,12 @@ __global__ void ZS_BOUNDS
       a = sum_slices1<DT>(s, n, i, a);
       bad |= not_finite(a);
       if constexpr (STORE) acc[i] = a;
+      if constexpr (NORM) sq += (double)a * (double)a;
     }
+  }
+  if constexpr (NORM) {
+    sq = block_sum(sq);
+    if (threadIdx.x == 0) partials[blockIdx.x] = sq;
   }
   if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(flag, 1);
 }
@@ -537,41 +581,6 @@ __global__ void ZS_BOUNDS
 }
 
 // ---------------------------------------------------------------- clipping
-
-// Square of one final gradient sum, accumulated in fp64.  Squares are formed
-// in fp32 unless they would overflow it (|a| > 1e18).
-__device__ __forceinline__ double sq8(const float a[8]) {
-  float q[8];
-  bool big = false;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    q[k] = __fmul_rn(a[k], a[k]);
-    big |= fabsf(a[k]) > 1e18f;
-  }
-  if (big) {
-    double d = 0.0;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) d += (double)a[k] * (double)a[k];
-    return d;
-  }
-  const float s01 = __fadd_rn(q[0], q[1]), s23 = __fadd_rn(q[2], q[3]);
-  const float s45 = __fadd_rn(q[4], q[5]), s67 = __fadd_rn(q[6], q[7]);
-  return (double)__fadd_rn(__fadd_rn(s01, s23), __fadd_rn(s45, s67));
-}
-
-// Fixed-order CTA sum of one double per thread; the result is valid in thread 0.
-__device__ __forceinline__ double block_sum(double x) {
-  __shared__ double warp_part[kThreads / 32];
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) x += __shfl_down_sync(0xffffffffu, x, off);
-  if ((threadIdx.x & 31) == 0) warp_part[threadIdx.x >> 5] = x;
-  __syncthreads();
-  double t = 0.0;
-  if (threadIdx.x == 0) {
-    for (int w = 0; w < kThreads / 32; ++w) t += warp_part[w];
-  }
-  return t;
-}
 
 // Per-CTA partial sums of squares of the final gradient sums
 // (acc (or +0) + the n slices), grid-stride over a grid of at most the
