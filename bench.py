@@ -68,7 +68,7 @@ class DeviceWorkload:
     slices (half), the fp32 accumulator, fp32 master / m / v and the half copy."""
 
     def __init__(self, wl: synth.Workload, shard: int = 0, device=None, count: int | None = None,
-                 acc: str = "fp32"):
+                 acc: str = "fp32", clip: float = 0.0):
         import torch
         import zero_mixed_precision_shard_gb300 as zs
         self.zs = zs
@@ -81,6 +81,7 @@ class DeviceWorkload:
         E, n, g = self.E, wl.n, wl.g
         self.grads = torch.empty((g, n, E), dtype=torch.int16, device=self.dev)
         self.acc_kind = acc
+        self.clip = clip
         if acc == "half":
             self.acc = torch.empty(E, dtype=torch.int16, device=self.dev)
         else:
@@ -137,9 +138,14 @@ class DeviceWorkload:
             return ovf
         for k in range(wl.g - 1):
             zs.zs_grad_accum(ctx, self.slices(k), self.dt, self.E, self.acc, k == 0)
-        ovf, _ = zs.zs_shard_step(ctx, self.slices(wl.g - 1), self.dt, self.E, self.acc, wl.g,
-                                  self.master, self.m, self.v, self.half, self.hp, self.t + 1,
-                                  self.scaler)
+        if self.clip > 0:
+            ovf, _, self.grad_norm = zs.zs_shard_step_clipped(
+                ctx, self.slices(wl.g - 1), self.dt, self.E, self.acc, wl.g, self.master, self.m,
+                self.v, self.half, self.hp, self.t + 1, self.scaler, self.clip)
+        else:
+            ovf, _ = zs.zs_shard_step(ctx, self.slices(wl.g - 1), self.dt, self.E, self.acc,
+                                      wl.g, self.master, self.m, self.v, self.half, self.hp,
+                                      self.t + 1, self.scaler)
         if not ovf:
             self.t += 1
         return ovf
@@ -164,7 +170,8 @@ class DeviceWorkload:
                  kernel_alg_bytes("reduce", n, first=(k == 0))) for k in range(g - 1)]
         recompute = n < 4 or self.acc is None
         if recompute:
-            with_acc = self.wl.dtype == "bf16" and g > 1
+            # the flag pass reads acc too for bf16, or to fold in the clipping norm
+            with_acc = g > 1 and (self.wl.dtype == "bf16" or self.clip > 0)
             plan.append(("check", kernel_alg_bytes("check", n, with_acc=with_acc)))
             plan.append(("apply_recompute", kernel_alg_bytes("apply_recompute", n,
                                                              with_acc=g > 1)))
@@ -386,7 +393,7 @@ def run_ours(args):
     ctx = zs.Ctx()
     probe = copy_probe(zs, ctx) if not args.skip_probe else {}
 
-    W = DeviceWorkload(wl, shard=0, count=args.elements, acc=args.acc)
+    W = DeviceWorkload(wl, shard=0, count=args.elements, acc=args.acc, clip=args.clip)
     W.fill_grads(1, wl.scale0, inject=False)
     torch.cuda.synchronize()
     E = W.E
@@ -398,8 +405,8 @@ def run_ours(args):
     graph = None
     dstate = None
     if args.graph:
-        if world > 1 or args.acc != "fp32":
-            raise SystemExit("--graph runs the fp32-accumulator path on one GPU")
+        if world > 1 or args.acc != "fp32" or args.clip:
+            raise SystemExit("--graph runs the unclipped fp32-accumulator path on one GPU")
         dstate = zs.DeviceState(W.scaler)
         W.step_async_calls(ctx, dstate)      # uncaptured first call caches launch shapes
         torch.cuda.synchronize()
@@ -521,6 +528,7 @@ def run_ours(args):
                 "grad_dtype": wl.dtype, "optimizer": "AdamW" if wl.weight_decay else "Adam",
                 "parallelism": "replicas + overflow-flag all-reduce" if world > 1 else "1 GPU",
                 "accumulator": args.acc,
+                "clip_max_norm": args.clip or None,
                 "api": "CUDA graph of zs_grad_accum + zs_shard_step_async" if args.graph
                        else "zs_grad_accum + zs_shard_step",
                 "l2": "inputs larger than L2 (129 MB): no flush needed",
@@ -610,6 +618,8 @@ def main(argv=None):
     ap.add_argument("--skip-probe", action="store_true")
     ap.add_argument("--acc", default="fp32", choices=["fp32", "half"],
                     help="accumulator format (half: zs_*_halfacc entry points)")
+    ap.add_argument("--clip", type=float, default=0.0,
+                    help="global-norm gradient clipping at this max norm (zs_shard_step_clipped)")
     ap.add_argument("--graph", action="store_true",
                     help="replay each step from a CUDA graph (device-resident scaler)")
     ap.add_argument("--elements", type=int, default=None,
