@@ -259,7 +259,19 @@ zs_status reduce_norm_any(zs_ctx* c, zs_dtype dt, const zs::SlicePtrs& sp, int32
   }
   if (st != ZS_OK) return st;
   const double div = (double)grad_div;
-  zs::k_sumsq_finalize<<<1, zs::kThreads, 0, s>>>(c->d_norm_parts, nparts, 1.0 / (div * div), out);
+  const double* parts = c->d_norm_parts;
+  if (nparts > ZS_SUMSQ_MAX_PARTS) {
+    // one partial per CTA of a full grid can be millions: fold them into at
+    // most ZS_SUMSQ_MAX_PARTS chunk sums first (fixed order, deterministic)
+    const int64_t chunk = (nparts + ZS_SUMSQ_MAX_PARTS - 1) / ZS_SUMSQ_MAX_PARTS;
+    const int blocks = (int)((nparts + chunk - 1) / chunk);
+    zs::k_partials_reduce<<<blocks, zs::kThreads, 0, s>>>(c->d_norm_parts, nparts, chunk,
+                                                         c->d_partials);
+    c->launches += 1;
+    parts = c->d_partials;
+    nparts = blocks;
+  }
+  zs::k_sumsq_finalize<<<1, zs::kThreads, 0, s>>>(parts, nparts, 1.0 / (div * div), out);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(c, e, "reduce launch");
   ls.done();

@@ -617,6 +617,19 @@ __global__ void ZS_BOUNDS k_sumsq(const __grid_constant__ SlicePtrs s, int n,
   if (threadIdx.x == 0) partials[blockIdx.x] = t;
 }
 
+// First level of the fixed-order sum of many partials: CTA b sums the
+// contiguous chunk [b*chunk, min((b+1)*chunk, nparts)) into out[b].
+__global__ void k_partials_reduce(const double* __restrict__ partials, int64_t nparts,
+                                  int64_t chunk, double* __restrict__ out) {
+  const int64_t b0 = (int64_t)blockIdx.x * chunk;
+  int64_t b1 = b0 + chunk;
+  if (b1 > nparts) b1 = nparts;
+  double t = 0.0;
+  for (int64_t i = b0 + threadIdx.x; i < b1; i += kThreads) t += partials[i];
+  t = block_sum(t);
+  if (threadIdx.x == 0) out[blockIdx.x] = t;
+}
+
 // One CTA: out = (sum of partials, fixed order) / grad_div^2.
 __global__ void k_sumsq_finalize(const double* __restrict__ partials, int nparts, double inv_div2,
                                  double* __restrict__ out) {
