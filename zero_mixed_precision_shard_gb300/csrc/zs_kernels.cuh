@@ -369,6 +369,31 @@ __device__ __forceinline__ double block_sum(double x) {
   return t;
 }
 
+// fp32 sum of 8 squares as a fixed tree (no overflow check).
+__device__ __forceinline__ float sq8f(const float a[8]) {
+  const float s01 = __fmaf_rn(a[1], a[1], __fmul_rn(a[0], a[0]));
+  const float s23 = __fmaf_rn(a[3], a[3], __fmul_rn(a[2], a[2]));
+  const float s45 = __fmaf_rn(a[5], a[5], __fmul_rn(a[4], a[4]));
+  const float s67 = __fmaf_rn(a[7], a[7], __fmul_rn(a[6], a[6]));
+  return __fadd_rn(__fadd_rn(s01, s23), __fadd_rn(s45, s67));
+}
+
+// CTA sum of one fp32 per thread: fixed-pattern warp shuffles in fp32, the
+// warp totals added in fp64 by thread 0 (valid there).  GB300's fp64 rate is
+// low, so the per-element work stays in fp32.
+__device__ __forceinline__ double block_sum_f(float x) {
+  __shared__ float warp_part_f[kThreads / 32];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x = __fadd_rn(x, __shfl_down_sync(0xffffffffu, x, off));
+  if ((threadIdx.x & 31) == 0) warp_part_f[threadIdx.x >> 5] = x;
+  __syncthreads();
+  double t = 0.0;
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < kThreads / 32; ++w) t += (double)warp_part_f[w];
+  }
+  return t;
+}
+
 // Reduce + accumulate + flag.  READ_ACC: start from acc (else +0.0f).
 // STORE: write the sums back to acc (otherwise only the flag is produced).
 // VPT vector units per thread per trip, `stride` apart so each load
@@ -380,8 +405,12 @@ __global__ void ZS_BOUNDS
   // HACC: acc holds count halves of the gradient's format; each sum is rounded
   // to it, and the flag tests the rounded value.
   // NORM: also writes this CTA's sum of squares of the sums to partials[blockIdx.x]
-  // (the clipping norm of the last micro-step, fused into its pass).
-  double sq = 0.0;
+  // (the clipping norm of the last micro-step, fused into its pass): squares
+  // and the CTA reduction in fp32, the CTA total in fp64; a CTA holding a sum
+  // above 1e18 in magnitude (whose square could overflow fp32) reduces in fp64.
+  float sqf = 0.0f;
+  double sqd = 0.0;
+  bool big = false;
   const int64_t nvec = count >> 3;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
@@ -417,7 +446,18 @@ __global__ void ZS_BOUNDS
         for (int k = 0; k < 8; ++k) bad |= not_finite(a[j][k]);
         if constexpr (STORE) store8_acc(acc + vi[j] * 8, a[j]);
       }
-      if constexpr (NORM) sq += sq8(a[j]);
+      if constexpr (NORM) {
+        bool b = false;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) b |= fabsf(a[j][k]) > 1e18f;
+        if (b) {
+          big = true;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) sqd += (double)a[j][k] * (double)a[j][k];
+        } else {
+          sqf = __fadd_rn(sqf, sq8f(a[j]));
+        }
+      }
     }
   }
   const int64_t tail = count - nvec * 8;
@@ -435,12 +475,24 @@ __global__ void ZS_BOUNDS
       a = sum_slices1<DT>(s, n, i, a);
       bad |= not_finite(a);
       if constexpr (STORE) acc[i] = a;
-      if constexpr (NORM) sq += (double)a * (double)a;
+      if constexpr (NORM) {
+        if (fabsf(a) > 1e18f) {
+          big = true;
+          sqd += (double)a * (double)a;
+        } else {
+          sqf = __fmaf_rn(a, a, sqf);
+        }
+      }
     }
   }
   if constexpr (NORM) {
-    sq = block_sum(sq);
-    if (threadIdx.x == 0) partials[blockIdx.x] = sq;
+    double total;
+    if (__syncthreads_or(big)) {
+      total = block_sum((double)sqf + sqd);
+    } else {
+      total = block_sum_f(sqf);
+    }
+    if (threadIdx.x == 0) partials[blockIdx.x] = total;
   }
   if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(flag, 1);
 }
@@ -592,7 +644,11 @@ __global__ void ZS_BOUNDS k_sumsq(const __grid_constant__ SlicePtrs s, int n,
   const int64_t nvec = count >> 3;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+  // fp32 partial sums of squares flushed to fp64 every 8 vectors (GB300's fp64
+  // rate is low); vectors with a sum above 1e18 in magnitude square in fp64.
   double t = 0.0;
+  float f = 0.0f;
+  int pending = 0;
   for (int64_t vi = tid; vi < nvec; vi += stride) {
     int64_t v1[1] = {vi};
     bool ok[1] = {true};
@@ -604,8 +660,21 @@ __global__ void ZS_BOUNDS k_sumsq(const __grid_constant__ SlicePtrs s, int n,
       for (int k = 0; k < 8; ++k) a[0][k] = 0.0f;
     }
     if constexpr (RECOMPUTE) sum_slices<DT, 1>(s, n, v1, ok, a);
-    t += sq8(a[0]);
+    bool b = false;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) b |= fabsf(a[0][k]) > 1e18f;
+    if (b) {
+      t += sq8(a[0]);
+    } else {
+      f = __fadd_rn(f, sq8f(a[0]));
+      if (++pending == 8) {
+        t += (double)f;
+        f = 0.0f;
+        pending = 0;
+      }
+    }
   }
+  t += (double)f;
   const int64_t tail = count - nvec * 8;
   if (tid < tail) {
     const int64_t i = nvec * 8 + tid;
