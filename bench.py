@@ -393,7 +393,8 @@ def run_ours(args):
     ctx = zs.Ctx()
     probe = copy_probe(zs, ctx) if not args.skip_probe else {}
 
-    W = DeviceWorkload(wl, shard=0, count=args.elements, acc=args.acc, clip=args.clip)
+    # with several GPUs, rank r owns shard r mod N (a ZeRO job's rank r owns shard r)
+    W = DeviceWorkload(wl, shard=rank % wl.n, count=args.elements, acc=args.acc, clip=args.clip)
     W.fill_grads(1, wl.scale0, inject=False)
     torch.cuda.synchronize()
     E = W.E
@@ -475,7 +476,12 @@ def run_ours(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
     per_step_ms = ms / args.steps
-    value = valid * world / (per_step_ms * 1e-3)
+    owned_total = valid
+    if world > 1:
+        v = torch.tensor([valid], dtype=torch.float64, device="cuda")
+        dist.all_reduce(v)
+        owned_total = int(v.item())
+    value = owned_total / (per_step_ms * 1e-3)
 
     # per-kernel times and the dominant kernel's roofline
     kinds = {}
