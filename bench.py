@@ -34,7 +34,7 @@ import numpy as np  # noqa: E402
 import synth  # noqa: E402
 
 DEFAULT_WORKLOAD = "llama7b-n1"
-METRIC = "ZeRO shard-step params/s"
+METRIC = "ZeRO shard-step params/s and achieved HBM GB/s vs measured GB300 peak"
 
 
 # ---------------------------------------------------------------- byte model
@@ -547,6 +547,8 @@ def run_ours(args):
                 "kernels": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv)
                                 for kk, vv in d.items()} for k, d in kinds.items()},
             },
+            "achieved_gbs": round(step_bytes / (per_step_ms * 1e-3) / 1e9, 1),
+            "achieved_frac_of_peak": round(step_bytes / (per_step_ms * 1e-3) / 1e9 / peak, 4),
             "roofline": roofline,
             "clocks": clocks.summary(),
             "gpu_launches": launches,
