@@ -334,6 +334,52 @@ zs_status zs_shard_step_async(zs_ctx* ctx, const void* const* grads, int32_t n, 
                               const zs_lr_schedule* sched, zs_device_state* d_state,
                               cudaStream_t stream);
 
+/* ---------------------------------------------------------------- engine */
+
+/* The training-loop interface of §5.1 (model_engine.backward(loss) then
+ * model_engine.step() for every micro-batch; model_engine.global_steps), for
+ * one owned shard, on top of the calls above:
+ *   zs_engine_backward(e, grads): this micro-batch's n rank slices (what the
+ *     reduce-scatter of its gradient buckets would deliver); micro-batches
+ *     1..G-1 are summed into acc at once, the G-th is kept for the step;
+ *   zs_engine_step(e, ...): after every backward; at the accumulation boundary
+ *     (the G-th micro-batch, §4.3) it runs the optimizer step -- zs_shard_step,
+ *     or zs_shard_step_clipped when max_grad_norm > 0 -- with the learning rate
+ *     of the schedule at Adam's next step, advances the counts and returns the
+ *     overflow flag and the new scale; otherwise it does nothing.
+ * The engine borrows the caller's buffers (they must outlive it) and owns the
+ * loss scaler and the step counts.  The grads pointer arrays are copied; the
+ * slices themselves must stay valid until the step that consumes them. */
+typedef struct {
+  int32_t n;                 /* simulated data-parallel ranks */
+  zs_dtype dt;               /* gradient format */
+  int64_t count;             /* elements of the owned shard */
+  int32_t accum_steps;       /* micro-batches per optimizer step (G) */
+  float* acc;                /* count floats (may be NULL only when G == 1) */
+  float *master, *m, *v;     /* count floats each */
+  void* half_out;            /* count halves */
+  zs_adam_hparams hp;        /* hp.lr is used when has_schedule == 0 */
+  zs_lr_schedule schedule;   /* used when has_schedule != 0 */
+  int32_t has_schedule;
+  zs_scaler scaler;          /* initial loss-scale state */
+  float max_grad_norm;       /* gradient_clipping; <= 0 disables */
+} zs_engine_config;
+
+typedef struct zs_engine zs_engine;
+
+zs_status zs_engine_create(zs_ctx* ctx, const zs_engine_config* cfg, zs_engine** out);
+zs_status zs_engine_destroy(zs_engine* e);
+zs_status zs_engine_backward(zs_engine* e, const void* const* grads, cudaStream_t stream);
+/* *stepped = 1 when this call ran the optimizer step; then *overflow_out,
+ * *scale_out and *grad_norm_out (0 unless clipping) describe it.  Any output
+ * pointer may be NULL. */
+zs_status zs_engine_step(zs_engine* e, int32_t* stepped, int32_t* overflow_out, float* scale_out,
+                         float* grad_norm_out, cudaStream_t stream);
+/* global_steps: optimizer steps run (skipped ones included), as §5.1 prints;
+ * applied_steps: Adam's step count; micro_steps: backward calls so far. */
+zs_status zs_engine_state(const zs_engine* e, int64_t* global_steps, int64_t* applied_steps,
+                          int64_t* micro_steps, zs_scaler* scaler);
+
 /* ---------------------------------------------------------------- measurement */
 
 /* HBM roofline probe: copy `bytes` from src to dst (read_only = 0), or only

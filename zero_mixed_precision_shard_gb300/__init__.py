@@ -66,6 +66,15 @@ class zs_device_state(ctypes.Structure):
 ZS_LR_CONSTANT, ZS_LR_WARMUP, ZS_LR_WARMUP_DECAY = 0, 1, 2
 
 
+class zs_engine_config(ctypes.Structure):
+    _fields_ = [("n", ctypes.c_int32), ("dt", ctypes.c_int32), ("count", ctypes.c_int64),
+                ("accum_steps", ctypes.c_int32), ("acc", ctypes.c_void_p),
+                ("master", ctypes.c_void_p), ("m", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("half_out", ctypes.c_void_p), ("hp", zs_adam_hparams),
+                ("schedule", zs_lr_schedule), ("has_schedule", ctypes.c_int32),
+                ("scaler", zs_scaler), ("max_grad_norm", ctypes.c_float)]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(
@@ -93,6 +102,12 @@ def _load():
                           ctypes.POINTER(zs_adam_hparams), i64, ctypes.POINTER(zs_scaler), i32p,
                           ctypes.POINTER(ctypes.c_float), vp],
         "zs_copy_peak": [vp, vp, vp, i64, i32, vp],
+        "zs_engine_create": [vp, ctypes.POINTER(zs_engine_config), ctypes.POINTER(vp)],
+        "zs_engine_destroy": [vp],
+        "zs_engine_backward": [vp, pp, vp],
+        "zs_engine_step": [vp, i32p, i32p, ctypes.POINTER(ctypes.c_float),
+                           ctypes.POINTER(ctypes.c_float), vp],
+        "zs_engine_state": [vp, i64p, i64p, i64p, ctypes.POINTER(zs_scaler)],
         "zs_grad_accum_halfacc": [vp, pp, i32, i32, i64, vp, i32, vp],
         "zs_shard_step_halfacc": [vp, pp, i32, i32, i64, vp, i32, vp, vp, vp, vp,
                                   ctypes.POINTER(zs_adam_hparams), i64, ctypes.POINTER(zs_scaler),
@@ -401,6 +416,56 @@ def zs_shard_step_halfacc(ctx: Ctx, grads, dt, count: int, acc_half, accum_steps
                                         ctypes.byref(scaler), ctypes.byref(ovf),
                                         ctypes.byref(ns), _stream(stream)))
     return ovf.value, ns.value
+
+
+class Engine:
+    """zs_engine: backward() per micro-batch, step() after each (§5.1's loop)."""
+
+    def __init__(self, ctx: Ctx, n, dt, count, accum_steps, acc, master, m, v, half_out,
+                 hp: zs_adam_hparams, scaler: zs_scaler, schedule=None, max_grad_norm=0.0):
+        cfg = zs_engine_config()
+        cfg.n, cfg.dt, cfg.count, cfg.accum_steps = n, _dtype(dt), count, accum_steps
+        cfg.acc, cfg.master, cfg.m, cfg.v = _addr(acc), _addr(master), _addr(m), _addr(v)
+        cfg.half_out = _addr(half_out)
+        cfg.hp = hp
+        if schedule is not None:
+            cfg.schedule = schedule
+            cfg.has_schedule = 1
+        cfg.scaler = scaler
+        cfg.max_grad_norm = max_grad_norm
+        self.ctx = ctx
+        self.handle = ctypes.c_void_p()
+        ctx.check(lib.zs_engine_create(ctx.handle, ctypes.byref(cfg), ctypes.byref(self.handle)))
+
+    def backward(self, grads, stream=None):
+        self.ctx.check(lib.zs_engine_backward(self.handle, _ptrs(grads), _stream(stream)))
+
+    def step(self, stream=None):
+        """Returns None between boundaries, else (overflow, new_scale, grad_norm)."""
+        st, ovf = ctypes.c_int32(), ctypes.c_int32()
+        sc, gn = ctypes.c_float(), ctypes.c_float()
+        self.ctx.check(lib.zs_engine_step(self.handle, ctypes.byref(st), ctypes.byref(ovf),
+                                          ctypes.byref(sc), ctypes.byref(gn), _stream(stream)))
+        return (ovf.value, sc.value, gn.value) if st.value else None
+
+    def state(self):
+        g, a, mi = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        sc = zs_scaler()
+        lib.zs_engine_state(self.handle, ctypes.byref(g), ctypes.byref(a), ctypes.byref(mi),
+                            ctypes.byref(sc))
+        return {"global_steps": g.value, "applied_steps": a.value, "micro_steps": mi.value,
+                "scaler": sc}
+
+    def close(self):
+        if self.handle:
+            lib.zs_engine_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def zs_copy_peak(ctx: Ctx, src, dst, nbytes: int, read_only: bool = False, stream=None):

@@ -1038,6 +1038,120 @@ zs_status zs_copy_peak(zs_ctx* c, const void* src, void* dst, int64_t bytes, int
   return ZS_OK;
 }
 
+// ---------------------------------------------------------------- engine
+
+}  // extern "C"
+
+struct zs_engine {
+  zs_ctx* ctx = nullptr;
+  zs_engine_config cfg{};
+  int32_t micro = 0;                // backward calls in the current step
+  std::vector<const void*> last;    // the G-th micro-batch's slices
+  int64_t global_steps = 0, applied = 0, micro_total = 0;
+};
+
+namespace {
+
+// The schedules' learning rate at Adam step t, computed the way the device
+// prologue does (fp64, one rounding to fp32).
+float host_lr_at(const zs_lr_schedule& sc, int64_t t) {
+  const double mn = sc.min_lr, mx = sc.max_lr;
+  if (sc.kind == ZS_LR_CONSTANT) return (float)mx;
+  double frac = sc.warmup_steps > 0 ? (double)t / (double)sc.warmup_steps : 1.0;
+  if (frac > 1.0) frac = 1.0;
+  const double warm = mn + (mx - mn) * frac;
+  if (sc.kind == ZS_LR_WARMUP || t <= sc.warmup_steps) return (float)warm;
+  if (sc.total_steps <= sc.warmup_steps) return 0.0f;
+  double rest = (double)(sc.total_steps - t) / (double)(sc.total_steps - sc.warmup_steps);
+  if (rest < 0.0) rest = 0.0;
+  return (float)(mx * rest);
+}
+
+}  // namespace
+
+extern "C" {
+
+zs_status zs_engine_create(zs_ctx* c, const zs_engine_config* cfg, zs_engine** out) {
+  if (out == nullptr) return ZS_ERR_ARG;
+  *out = nullptr;
+  ZS_TRY(check_ctx(c));
+  if (cfg == nullptr) return fail(c, ZS_ERR_ARG, "cfg is NULL");
+  if (cfg->n < 1 || cfg->n > ZS_MAX_RANKS) return fail(c, ZS_ERR_ARG, "n out of range");
+  if (cfg->dt != ZS_FP16 && cfg->dt != ZS_BF16) return fail(c, ZS_ERR_DTYPE, "unknown dtype");
+  if (cfg->count < 0 || cfg->accum_steps < 1) return fail(c, ZS_ERR_ARG, "bad count or accum_steps");
+  if (cfg->accum_steps > 1 && cfg->acc == nullptr && cfg->count > 0)
+    return fail(c, ZS_ERR_ARG, "acc is required when accum_steps > 1");
+  ZS_TRY(check_hparams(c, &cfg->hp, 1));
+  ZS_TRY(check_scaler(c, &cfg->scaler));
+  if (cfg->has_schedule &&
+      (cfg->schedule.kind < ZS_LR_CONSTANT || cfg->schedule.kind > ZS_LR_WARMUP_DECAY))
+    return fail(c, ZS_ERR_ARG, "bad learning-rate schedule");
+  zs_engine* e = new zs_engine();
+  e->ctx = c;
+  e->cfg = *cfg;
+  *out = e;
+  return ZS_OK;
+}
+
+zs_status zs_engine_destroy(zs_engine* e) {
+  if (e == nullptr) return ZS_ERR_ARG;
+  delete e;
+  return ZS_OK;
+}
+
+zs_status zs_engine_backward(zs_engine* e, const void* const* grads, cudaStream_t stream) {
+  if (e == nullptr) return ZS_ERR_ARG;
+  NvtxRange nvtx_("zs_engine_backward");
+  zs_ctx* c = e->ctx;
+  const zs_engine_config& f = e->cfg;
+  if (e->micro >= f.accum_steps)
+    return fail(c, ZS_ERR_ARG, "zs_engine_step must follow the last micro-batch's backward");
+  if (grads == nullptr) return fail(c, ZS_ERR_ARG, "grads is NULL");
+  if (e->micro < f.accum_steps - 1) {
+    ZS_TRY(zs_grad_accum(c, grads, f.n, f.dt, f.count, f.acc, e->micro == 0 ? 1 : 0, stream));
+  } else {
+    e->last.assign(grads, grads + f.n);
+  }
+  e->micro += 1;
+  e->micro_total += 1;
+  return ZS_OK;
+}
+
+zs_status zs_engine_step(zs_engine* e, int32_t* stepped, int32_t* overflow_out, float* scale_out,
+                         float* grad_norm_out, cudaStream_t stream) {
+  if (e == nullptr) return ZS_ERR_ARG;
+  NvtxRange nvtx_("zs_engine_step");
+  const zs_engine_config& f = e->cfg;
+  if (stepped) *stepped = 0;
+  if (e->micro < f.accum_steps) return ZS_OK;  // not at the accumulation boundary
+  zs_adam_hparams hp = f.hp;
+  if (f.has_schedule) hp.lr = host_lr_at(f.schedule, e->applied + 1);
+  int32_t ovf = 0;
+  float scale = 0.0f, norm = 0.0f;
+  ZS_TRY(shard_step_impl(e->ctx, e->last.data(), f.n, f.dt, f.count, f.acc, f.accum_steps,
+                         f.master, f.m, f.v, f.half_out, &hp, e->applied + 1, &e->cfg.scaler,
+                         f.max_grad_norm > 0.0f ? f.max_grad_norm : 0.0f, &ovf, &scale, &norm,
+                         stream));
+  e->micro = 0;
+  e->global_steps += 1;
+  if (!ovf) e->applied += 1;
+  if (stepped) *stepped = 1;
+  if (overflow_out) *overflow_out = ovf;
+  if (scale_out) *scale_out = scale;
+  if (grad_norm_out) *grad_norm_out = norm;
+  return ZS_OK;
+}
+
+zs_status zs_engine_state(const zs_engine* e, int64_t* global_steps, int64_t* applied_steps,
+                          int64_t* micro_steps, zs_scaler* scaler) {
+  if (e == nullptr) return ZS_ERR_ARG;
+  if (global_steps) *global_steps = e->global_steps;
+  if (applied_steps) *applied_steps = e->applied;
+  if (micro_steps) *micro_steps = e->micro_total;
+  if (scaler) *scaler = e->cfg.scaler;
+  return ZS_OK;
+}
+
 zs_status zs_ctx_set_timing(zs_ctx* c, int32_t enable) {
   if (c == nullptr) return ZS_ERR_ARG;
   c->timing = enable != 0;
