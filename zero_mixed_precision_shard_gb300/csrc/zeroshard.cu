@@ -20,6 +20,15 @@
 
 // Capacity of the per-CTA partial sums of the clipping norm (one double each).
 #define ZS_SUMSQ_MAX_PARTS 4096
+// Accumulators up to this size keep an evict-last L2 policy (they are read
+// back by the next micro-step and by the update; L2 is 129 MB on GB300).
+#ifndef ZS_ACC_KEEP_MAX_BYTES
+#define ZS_ACC_KEEP_MAX_BYTES (64ll << 20)
+#endif
+
+static inline uint32_t acc_keep_for(int64_t count) {
+  return count * 4 <= ZS_ACC_KEEP_MAX_BYTES ? 1u : 0u;
+}
 
 struct zs_ctx {
   int device = 0;
@@ -214,7 +223,8 @@ void launch_reduce_k(zs_ctx* c, const zs::SlicePtrs& sp, int32_t n, float* acc, 
   const int64_t units = (count >> 3) / VPT + 8;
   auto k = zs::k_reduce<DT, RA, ST, VPT>;
   const int waves = ST ? ZS_GRID_WAVES : ZS_CHECK_WAVES;
-  k<<<grid_for(c, k, units, waves), zs::kThreads, 0, s>>>(sp, n, acc, count, flag, nullptr);
+  k<<<grid_for(c, k, units, waves), zs::kThreads, 0, s>>>(sp, n, acc, count, flag, nullptr,
+                                                          acc_keep_for(count));
 }
 
 // The last micro-step's pass with the clipping norm fused in: per-CTA sums of
@@ -233,7 +243,8 @@ zs_status launch_reduce_norm_k(zs_ctx* c, const zs::SlicePtrs& sp, int32_t n, fl
     if (e != cudaSuccess) return cuda_fail(c, e, "norm partials");
     c->norm_cap = cap;
   }
-  k<<<grid, zs::kThreads, 0, s>>>(sp, n, acc, count, flag, c->d_norm_parts);
+  k<<<grid, zs::kThreads, 0, s>>>(sp, n, acc, count, flag, c->d_norm_parts,
+                                  acc_keep_for(count));
   *nparts = grid;
   return ZS_OK;
 }
@@ -356,12 +367,13 @@ void launch_apply_k(zs_ctx* c, const int32_t* flag, const zs::SlicePtrs& sp, int
   if (coef != nullptr) {
     auto k = zs::k_apply<DT, HA, RC, VPT, true>;
     k<<<grid_for(c, k, units), zs::kThreads, 0, s>>>(flag, sp, n, acc, master, m, v, ho, count,
-                                                     ad, sc_in, result, coef, nullptr, nullptr);
+                                                     ad, sc_in, result, coef, nullptr, nullptr,
+                                                     acc_keep_for(count));
   } else {
     auto k = zs::k_apply<DT, HA, RC, VPT, false>;
     k<<<grid_for(c, k, units), zs::kThreads, 0, s>>>(flag, sp, n, acc, master, m, v, ho, count,
                                                      ad, sc_in, result, nullptr, nullptr,
-                                                     nullptr);
+                                                     nullptr, acc_keep_for(count));
   }
 }
 
@@ -494,7 +506,7 @@ void launch_apply_dev_k(zs_ctx* c, const int32_t* flag, const zs::SlicePtrs& sp,
   const zs_scaler unused_sc{};
   k<<<grid_for(c, k, units), zs::kThreads, 0, s>>>(flag, sp, n, acc, master, m, v, ho, count,
                                                    unused, unused_sc, nullptr, nullptr, ad_dev,
-                                                   st);
+                                                   st, acc_keep_for(count));
 }
 
 template <int DT>
@@ -517,7 +529,7 @@ void launch_reduce_hacc_k(zs_ctx* c, const zs::SlicePtrs& sp, int32_t n, float* 
   constexpr int VPT = ZS_HACC_VPT;
   const int64_t units = (count >> 3) / VPT + 8;
   auto k = zs::k_reduce<DT, RA, true, VPT, true>;
-  k<<<grid_for(c, k, units), zs::kThreads, 0, s>>>(sp, n, acc, count, flag, nullptr);
+  k<<<grid_for(c, k, units), zs::kThreads, 0, s>>>(sp, n, acc, count, flag, nullptr, 0u);
 }
 
 zs_status reduce_hacc(zs_ctx* c, zs_dtype dt, const zs::SlicePtrs& sp, int32_t n, void* acc,
@@ -550,12 +562,12 @@ zs_status apply_hacc(zs_ctx* c, zs_dtype dt, const int32_t* flag, const void* ac
     auto k = zs::k_apply<ZS_FP16, true, false, 1, false, false, true>;
     k<<<grid_for(c, k, units), zs::kThreads, 0, s>>>(flag, sp, 0, a, master, m, v, ho, count, ad,
                                                      *scaler_in, result, nullptr, nullptr,
-                                                     nullptr);
+                                                     nullptr, 0u);
   } else {
     auto k = zs::k_apply<ZS_BF16, true, false, 1, false, false, true>;
     k<<<grid_for(c, k, units), zs::kThreads, 0, s>>>(flag, sp, 0, a, master, m, v, ho, count, ad,
                                                      *scaler_in, result, nullptr, nullptr,
-                                                     nullptr);
+                                                     nullptr, 0u);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(c, e, "apply launch");

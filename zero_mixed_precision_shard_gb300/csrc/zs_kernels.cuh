@@ -57,8 +57,8 @@
 #ifndef ZS_GRID_WAVES  // grid = waves x resident CTAs per SM x SMs; 0 = one thread per unit
 #define ZS_GRID_WAVES 0
 #endif
-#ifndef ZS_ACC_STREAM  // 1: evict-first hints on the fp32 accumulator too
-#define ZS_ACC_STREAM 1
+#ifndef ZS_ACC_STREAM  // accumulator L2 hints: 0 default, 1 evict-first, 2 evict-last,
+#define ZS_ACC_STREAM 3 // 3 chosen per call by size (acc_keep)
 #endif
 #ifndef ZS_CHECK_VPT  // vector units per thread of the flag-only pass
 #define ZS_CHECK_VPT 8
@@ -184,8 +184,48 @@ __device__ __forceinline__ void store8(float* p, const float a[8]) {
   *reinterpret_cast<float4*>(p + 4) = make_float4(a[4], a[5], a[6], a[7]);
 }
 
+// L2 policy for the accumulator: evict-last while it fits comfortably in L2
+// (it is read back by the next micro-step and the update), evict-first when
+// it is larger than L2 and would only push other lines out.
+__device__ __forceinline__ uint64_t acc_policy(uint32_t keep) {
+  uint64_t pol;
+  if (keep) {
+    asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  } else {
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  }
+  return pol;
+}
+
+__device__ __forceinline__ void load8_acc_pol(const float* p, float a[8], uint64_t pol) {
+  float4 x0, x1;
+  asm volatile("ld.global.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=f"(x0.x), "=f"(x0.y), "=f"(x0.z), "=f"(x0.w) : "l"(p), "l"(pol));
+  asm volatile("ld.global.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=f"(x1.x), "=f"(x1.y), "=f"(x1.z), "=f"(x1.w) : "l"(p + 4), "l"(pol));
+  a[0] = x0.x; a[1] = x0.y; a[2] = x0.z; a[3] = x0.w;
+  a[4] = x1.x; a[5] = x1.y; a[6] = x1.z; a[7] = x1.w;
+}
+
+__device__ __forceinline__ void store8_acc_pol(float* p, const float a[8], uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1,%2,%3,%4}, %5;"
+               :: "l"(p), "f"(a[0]), "f"(a[1]), "f"(a[2]), "f"(a[3]), "l"(pol) : "memory");
+  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1,%2,%3,%4}, %5;"
+               :: "l"(p + 4), "f"(a[4]), "f"(a[5]), "f"(a[6]), "f"(a[7]), "l"(pol) : "memory");
+}
+
 __device__ __forceinline__ void load8_acc(const float* p, float a[8]) {
-#if ZS_ACC_STREAM
+#if ZS_ACC_STREAM == 2
+  uint64_t pol;
+  asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  float4 x0, x1;
+  asm volatile("ld.global.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=f"(x0.x), "=f"(x0.y), "=f"(x0.z), "=f"(x0.w) : "l"(p), "l"(pol));
+  asm volatile("ld.global.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=f"(x1.x), "=f"(x1.y), "=f"(x1.z), "=f"(x1.w) : "l"(p + 4), "l"(pol));
+  a[0] = x0.x; a[1] = x0.y; a[2] = x0.z; a[3] = x0.w;
+  a[4] = x1.x; a[5] = x1.y; a[6] = x1.z; a[7] = x1.w;
+#elif ZS_ACC_STREAM
   const float4 x0 = __ldcs(reinterpret_cast<const float4*>(p));
   const float4 x1 = __ldcs(reinterpret_cast<const float4*>(p + 4));
   a[0] = x0.x; a[1] = x0.y; a[2] = x0.z; a[3] = x0.w;
@@ -196,11 +236,36 @@ __device__ __forceinline__ void load8_acc(const float* p, float a[8]) {
 }
 
 __device__ __forceinline__ void store8_acc(float* p, const float a[8]) {
-#if ZS_ACC_STREAM
+#if ZS_ACC_STREAM == 2
+  uint64_t pol;
+  asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1,%2,%3,%4}, %5;"
+               :: "l"(p), "f"(a[0]), "f"(a[1]), "f"(a[2]), "f"(a[3]), "l"(pol) : "memory");
+  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1,%2,%3,%4}, %5;"
+               :: "l"(p + 4), "f"(a[4]), "f"(a[5]), "f"(a[6]), "f"(a[7]), "l"(pol) : "memory");
+#elif ZS_ACC_STREAM
   __stcs(reinterpret_cast<float4*>(p), make_float4(a[0], a[1], a[2], a[3]));
   __stcs(reinterpret_cast<float4*>(p + 4), make_float4(a[4], a[5], a[6], a[7]));
 #else
   store8(p, a);
+#endif
+}
+
+__device__ __forceinline__ void acc_ld(const float* p, float a[8], uint64_t pol) {
+#if ZS_ACC_STREAM == 3
+  load8_acc_pol(p, a, pol);
+#else
+  (void)pol;
+  load8_acc(p, a);
+#endif
+}
+
+__device__ __forceinline__ void acc_st(float* p, const float a[8], uint64_t pol) {
+#if ZS_ACC_STREAM == 3
+  store8_acc_pol(p, a, pol);
+#else
+  (void)pol;
+  store8_acc(p, a);
 #endif
 }
 
@@ -401,7 +466,8 @@ __device__ __forceinline__ double block_sum_f(float x) {
 template <int DT, bool READ_ACC, bool STORE, int VPT, bool HACC = false, bool NORM = false>
 __global__ void ZS_BOUNDS
     k_reduce(const __grid_constant__ SlicePtrs s, int n, float* __restrict__ acc, int64_t count,
-             int32_t* __restrict__ flag, double* __restrict__ partials = nullptr) {
+             int32_t* __restrict__ flag, double* __restrict__ partials, uint32_t acc_keep) {
+  const uint64_t pol = acc_policy(acc_keep);
   // HACC: acc holds count halves of the gradient's format; each sum is rounded
   // to it, and the flag tests the rounded value.
   // NORM: also writes this CTA's sum of squares of the sums to partials[blockIdx.x]
@@ -427,7 +493,7 @@ __global__ void ZS_BOUNDS
         if constexpr (HACC) {
           load8_hacc<DT>(acc, vi[j], a[j]);
         } else {
-          load8_acc(acc + vi[j] * 8, a[j]);
+          acc_ld(acc + vi[j] * 8, a[j], pol);
         }
       } else {
 #pragma unroll
@@ -444,7 +510,7 @@ __global__ void ZS_BOUNDS
       } else {
 #pragma unroll
         for (int k = 0; k < 8; ++k) bad |= not_finite(a[j][k]);
-        if constexpr (STORE) store8_acc(acc + vi[j] * 8, a[j]);
+        if constexpr (STORE) acc_st(acc + vi[j] * 8, a[j], pol);
       }
       if constexpr (NORM) {
         bool b = false;
@@ -547,10 +613,10 @@ __global__ void ZS_BOUNDS
             const float* __restrict__ acc, float* __restrict__ master, float* __restrict__ mom,
             float* __restrict__ var, uint16_t* __restrict__ half_out, int64_t count,
             AdamArgs ad_host, zs_scaler scaler_in, StepResult* __restrict__ result,
-            const float* __restrict__ clip_coef = nullptr,
-            const AdamArgs* __restrict__ ad_dev = nullptr,
-            zs_device_state* __restrict__ dstate = nullptr) {
+            const float* __restrict__ clip_coef, const AdamArgs* __restrict__ ad_dev,
+            zs_device_state* __restrict__ dstate, uint32_t acc_keep) {
   const int32_t overflow = *flag;
+  const uint64_t pol = acc_policy(acc_keep);
   AdamArgs ad = ad_host;
   if constexpr (DEV) {
     ad = *ad_dev;
@@ -578,7 +644,7 @@ __global__ void ZS_BOUNDS
         if constexpr (HACC) {
           load8_hacc<DT>(acc, vi[j], a[j]);
         } else {
-          load8_acc(acc + vi[j] * 8, a[j]);
+          acc_ld(acc + vi[j] * 8, a[j], pol);
         }
       } else {
 #pragma unroll
