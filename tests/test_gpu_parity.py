@@ -438,3 +438,56 @@ def test_context_flag_is_the_step_flag(zs):
                               zs.make_hparams(1e-3), 1, sc)
     assert ovf == 0   # the previous step cleared the flag
     ctx.close()
+
+
+def test_two_contexts_on_two_streams(zs):
+    """Contexts are independent: two shards stepped concurrently on two
+    streams (each context with its own flag) equal the same steps run one
+    after the other."""
+    rng = np.random.default_rng(55)
+    count, n = 200_003, 4
+    grads = [[rand_grads(rng, n, count, FP16, 256.0)] for _ in range(2)]
+    grads[1][0][2][9] = 0x7C00   # shard 1 overflows, shard 0 does not
+    master0 = [(rng.standard_normal(count) * 0.02).astype(np.float32) for _ in range(2)]
+
+    def run(concurrent):
+        ctxs = [zs.Ctx(), zs.Ctx()]
+        streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+        outs = []
+        bufs = []
+        for q in range(2):
+            master = torch.from_numpy(master0[q].copy()).cuda()
+            bufs.append((master, torch.zeros_like(master), torch.zeros_like(master),
+                         torch.zeros(count, dtype=torch.int16, device="cuda"),
+                         torch.zeros(count, dtype=torch.float32, device="cuda"),
+                         [dev16(x) for x in grads[q][0]]))
+        torch.cuda.synchronize()
+        scalers = [zs.zs_scaler_init(256.0, 1.0, 1000, 1, True) for _ in range(2)]
+        res = [None, None]
+        import threading
+
+        def work(q):
+            master, m, v, half, acc, g = bufs[q]
+            res[q] = zs.zs_shard_step(ctxs[q], g, FP16, count, acc, 1, master, m, v, half,
+                                      zs.make_hparams(1e-4), 1, scalers[q], streams[q])
+        if concurrent:
+            ts = [threading.Thread(target=work, args=(q,)) for q in range(2)]
+            for t in ts:
+                t.start()
+            for t in ts:
+                t.join()
+        else:
+            for q in range(2):
+                work(q)
+        torch.cuda.synchronize()
+        for q in range(2):
+            outs.append([b.clone() for b in bufs[q][:4]])
+            ctxs[q].close()
+        return res, outs
+
+    r1, o1 = run(True)
+    r2, o2 = run(False)
+    assert r1 == r2 and r1[0][0] == 0 and r1[1][0] == 1
+    for a, b in zip(o1, o2):
+        for x, y in zip(a, b):
+            assert torch.equal(x, y)
