@@ -95,6 +95,8 @@ typedef struct {
   int32_t hysteresis;   /* overflows before S halves */
   int32_t hyst_left;    /* overflows still tolerated before the next halving */
   int32_t dynamic;      /* 1: dynamic scaling, 0: static */
+  int32_t consecutive_hysteresis; /* 1: a clean step restores hyst_left, so only
+                                     consecutive overflows lower the scale */
 } zs_scaler;
 
 typedef struct zs_ctx zs_ctx;
@@ -117,8 +119,9 @@ zs_status zs_shard_range(const zs_partition* p, int32_t rank, int64_t* begin, in
  * E = shard_len: 16*psi, 4*psi + 12*E, 2*psi + 14*E, 16*E. */
 zs_status zs_model_state_bytes(const zs_partition* p, int32_t stage, uint64_t* bytes);
 
-/* Fill a scaler: hyst_left = hysteresis, clean_count = 0.  §4.2 defaults are
- * scale 2^16, window 1000, hysteresis 2, min_scale 1. */
+/* Fill a scaler: hyst_left = hysteresis, clean_count = 0,
+ * consecutive_hysteresis = 0 (set the field to 1 for the §4.2 knob of that
+ * name).  §4.2 defaults are scale 2^16, window 1000, hysteresis 2, min_scale 1. */
 zs_status zs_scaler_init(zs_scaler* s, float scale, float min_scale, int32_t window,
                          int32_t hysteresis, int32_t dynamic);
 
@@ -173,7 +176,7 @@ zs_status zs_apply(zs_ctx* ctx, const int32_t* d_flag, const void* const* grads,
  * overflow -> clean_count = 0 and, if dynamic, hyst_left -= 1 and at 0
  * scale = max(scale/2, min_scale), hyst_left = hysteresis;
  * clean -> if dynamic, clean_count += 1 and at window scale *= 2,
- * clean_count = 0.  Writes *scaler and *overflow_out (may be NULL) and
+ * clean_count = 0; with consecutive_hysteresis also hyst_left = hysteresis.  Writes *scaler and *overflow_out (may be NULL) and
  * synchronises `stream`.  Does not clear *d_flag. */
 zs_status zs_scaler_update(zs_ctx* ctx, const int32_t* d_flag, zs_scaler* scaler,
                            int32_t* overflow_out, cudaStream_t stream);
@@ -307,13 +310,14 @@ typedef struct {
   float min_lr, max_lr;  /* warmup_min_lr, warmup_max_lr */
 } zs_lr_schedule;
 
-/* Step state kept in DEVICE memory (caller-owned, 8-byte aligned, 56 bytes):
+/* Step state kept in DEVICE memory (caller-owned, 8-byte aligned, 64 bytes):
  * the loss scaler, Adam's step count and the last step's outcome.  The caller
  * initialises it (e.g. by copying a host struct whose scaler came from
  * zs_scaler_init, with step = iterations = 0) and may read it back at any time. */
 typedef struct {
   zs_scaler scaler;    /* loss-scale state (§4.2) */
   int32_t overflow;    /* 1 if the last step was skipped */
+  int32_t pad_;
   int64_t step;        /* applied updates so far */
   int64_t iterations;  /* steps run so far, skipped ones included */
   float lr;            /* learning rate of the last applied update */

@@ -33,7 +33,7 @@ class Scaler(ctypes.Structure):
     _fields_ = [("scale", ctypes.c_double), ("min_scale", ctypes.c_double),
                 ("window", ctypes.c_int32), ("clean_count", ctypes.c_int32),
                 ("hysteresis", ctypes.c_int32), ("hyst_left", ctypes.c_int32),
-                ("dynamic", ctypes.c_int32), ("pad_", ctypes.c_int32)]
+                ("dynamic", ctypes.c_int32), ("consecutive", ctypes.c_int32)]
 
 
 def make_hparams(lr, beta1, beta2, eps, weight_decay) -> HParams:
@@ -42,9 +42,10 @@ def make_hparams(lr, beta1, beta2, eps, weight_decay) -> HParams:
     return HParams(f(lr), f(beta1), f(beta2), f(eps), f(weight_decay))
 
 
-def make_scaler(scale, min_scale=1.0, window=1000, hysteresis=1, dynamic=True) -> Scaler:
+def make_scaler(scale, min_scale=1.0, window=1000, hysteresis=1, dynamic=True,
+                consecutive=False) -> Scaler:
     return Scaler(float(scale), float(min_scale), int(window), 0, int(hysteresis),
-                  int(hysteresis), 1 if dynamic else 0, 0)
+                  int(hysteresis), 1 if dynamic else 0, 1 if consecutive else 0)
 
 
 def _stale(out, srcs):

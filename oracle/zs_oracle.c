@@ -289,6 +289,7 @@ void zso_scaler_update(zso_scaler* s, int32_t overflow) {
       s->scale *= 2.0;
       s->clean_count = 0;
     }
+    if (s->consecutive) s->hyst_left = s->hysteresis;
   }
 }
 

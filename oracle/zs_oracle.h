@@ -35,7 +35,9 @@
  *    as they were.
  *  - The scale doubles when `window` consecutive clean steps have passed since
  *    the last overflow or increase; it halves (not below min_scale) on the
- *    `hysteresis`-th overflow since the last decrease.
+ *    `hysteresis`-th overflow since the last decrease; with
+ *    consecutive_hysteresis (a §4.2 knob the pages name but do not define) a
+ *    clean step restores the count, so only consecutive overflows halve it.
  *  - Hyper-parameters are taken as the fp32 values the library receives;
  *    the arithmetic of one step is fp64; master, m and v are rounded to fp32
  *    (nearest even) between steps and the half copy is the fp32 master
@@ -68,7 +70,7 @@ typedef struct {
 
 typedef struct {
   double scale, min_scale;
-  int32_t window, clean_count, hysteresis, hyst_left, dynamic, pad_;
+  int32_t window, clean_count, hysteresis, hyst_left, dynamic, consecutive;
 } zso_scaler;
 
 /* Partition (§2.1-§2.3): psi_pad = round_up(psi, n*align); shard_len = psi_pad/n. */

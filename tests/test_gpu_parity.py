@@ -209,7 +209,7 @@ def test_apply_recompute_matches_oracle(zs, ctx, dtype, with_acc):
 # ---------------------------------------------------------------- whole steps
 
 def run_shard_steps(zs, ctx, dtype, n, G, count, steps, seed, inject=None, acc_mode="auto",
-                    window=3, hysteresis=1):
+                    window=3, hysteresis=1, consecutive=False):
     """Drive zs_grad_accum + zs_shard_step on the GPU and oracle.shard_step on
     the host for `steps` steps; the oracle's scale drives input generation."""
     rng = np.random.default_rng(seed)
@@ -218,8 +218,9 @@ def run_shard_steps(zs, ctx, dtype, n, G, count, steps, seed, inject=None, acc_m
     hp_vals = (1e-3, 0.9, 0.999, 1e-8, 0.01)
     hp_o = oracle.make_hparams(*hp_vals)
     dynamic = dtype == FP16
-    sc_o = oracle.make_scaler(1024.0 if dynamic else 1.0, 1.0, window, hysteresis, dynamic)
-    sc = zs.zs_scaler_init(sc_o.scale, 1.0, window, hysteresis, dynamic)
+    sc_o = oracle.make_scaler(1024.0 if dynamic else 1.0, 1.0, window, hysteresis, dynamic,
+                              consecutive)
+    sc = zs.zs_scaler_init(sc_o.scale, 1.0, window, hysteresis, dynamic, consecutive)
     hp = zs.make_hparams(*hp_vals)
     master = torch.from_numpy(master0.copy()).cuda()
     m = torch.zeros_like(master)
@@ -274,6 +275,16 @@ def test_hysteresis_two(zs, ctx):
     flags, _ = run_shard_steps(zs, ctx, FP16, 2, 1, 1001, 10, seed=3, inject=inject, window=2,
                                hysteresis=2)
     assert flags == [1, 0, 1, 1, 1, 0, 0, 0, 1, 0]
+
+
+@pytest.mark.parametrize("consecutive", [False, True])
+def test_consecutive_hysteresis(zs, ctx, consecutive):
+    """hysteresis 2 with and without consecutive_hysteresis: the device scaler
+    follows the oracle step by step (the two settings diverge at step 3)."""
+    inject = {s: (0, 0, 17, 0x7C00) for s in (1, 3, 4, 7, 9, 10)}
+    flags, _ = run_shard_steps(zs, ctx, FP16, 2, 1, 1001, 11, seed=4, inject=inject, window=100,
+                               hysteresis=2, consecutive=consecutive)
+    assert flags == [1, 0, 1, 1, 0, 0, 1, 0, 1, 1, 0]
 
 
 @pytest.mark.parametrize("n", [4, 8])

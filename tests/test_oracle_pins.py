@@ -308,7 +308,7 @@ def test_scaler_traces(golden_dir):
     g = json.load(open(os.path.join(golden_dir, "scaler_traces.json")))
     for tr in g["traces"]:
         sc = oracle.make_scaler(tr["scale0"], tr["min_scale"], tr["window"], tr["hysteresis"],
-                                tr["dynamic"])
+                                tr["dynamic"], tr.get("consecutive_hysteresis", False))
         applied = 0
         got = []
         for s in range(1, tr["steps"] + 1):

@@ -48,7 +48,7 @@ class zs_scaler(ctypes.Structure):
     _fields_ = [("scale", ctypes.c_float), ("min_scale", ctypes.c_float),
                 ("window", ctypes.c_int32), ("clean_count", ctypes.c_int32),
                 ("hysteresis", ctypes.c_int32), ("hyst_left", ctypes.c_int32),
-                ("dynamic", ctypes.c_int32)]
+                ("dynamic", ctypes.c_int32), ("consecutive_hysteresis", ctypes.c_int32)]
 
 
 class zs_lr_schedule(ctypes.Structure):
@@ -58,7 +58,8 @@ class zs_lr_schedule(ctypes.Structure):
 
 
 class zs_device_state(ctypes.Structure):
-    _fields_ = [("scaler", zs_scaler), ("overflow", ctypes.c_int32), ("step", ctypes.c_int64),
+    _fields_ = [("scaler", zs_scaler), ("overflow", ctypes.c_int32), ("pad_", ctypes.c_int32),
+                ("step", ctypes.c_int64),
                 ("iterations", ctypes.c_int64), ("lr", ctypes.c_float),
                 ("grad_div", ctypes.c_float)]
 
@@ -272,12 +273,14 @@ def zs_model_state_bytes(p: Partition, stage: int) -> int:
 
 
 def zs_scaler_init(scale: float, min_scale: float = 1.0, window: int = 1000,
-                   hysteresis: int = 2, dynamic: bool = True) -> zs_scaler:
+                   hysteresis: int = 2, dynamic: bool = True,
+                   consecutive_hysteresis: bool = False) -> zs_scaler:
     s = zs_scaler()
     rc = lib.zs_scaler_init(ctypes.byref(s), scale, min_scale, window, hysteresis,
                             1 if dynamic else 0)
     if rc != ZS_OK:
         raise ZsError(rc, "zs_scaler_init")
+    s.consecutive_hysteresis = 1 if consecutive_hysteresis else 0
     return s
 
 
@@ -367,11 +370,11 @@ def zs_shard_step_clipped(ctx: Ctx, grads, dt, count: int, acc, accum_steps: int
 
 
 class DeviceState:
-    """A zs_device_state in device memory (a 56-byte torch buffer)."""
+    """A zs_device_state in device memory (a 64-byte torch buffer)."""
 
     def __init__(self, scaler: zs_scaler, step: int = 0, device=None):
         import torch
-        assert ctypes.sizeof(zs_device_state) == 56
+        assert ctypes.sizeof(zs_device_state) == 64
         st = zs_device_state()
         st.scaler = scaler
         st.step = step

@@ -631,6 +631,7 @@ zs_status zs_scaler_init(zs_scaler* s, float scale, float min_scale, int32_t win
   s->hysteresis = hysteresis;
   s->hyst_left = hysteresis;
   s->dynamic = dynamic ? 1 : 0;
+  s->consecutive_hysteresis = 0;
   return ZS_OK;
 }
 

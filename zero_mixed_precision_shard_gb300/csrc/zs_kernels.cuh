@@ -335,6 +335,7 @@ __device__ __forceinline__ zs_scaler next_scaler(zs_scaler s, int overflow) {
       s.scale = s.scale * 2.0f;
       s.clean_count = 0;
     }
+    if (s.consecutive_hysteresis) s.hyst_left = s.hysteresis;
   }
   return s;
 }
