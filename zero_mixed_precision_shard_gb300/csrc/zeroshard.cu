@@ -232,8 +232,9 @@ void launch_reduce_k(zs_ctx* c, const zs::SlicePtrs& sp, int32_t n, float* acc, 
 template <int DT, bool RA, bool ST>
 zs_status launch_reduce_norm_k(zs_ctx* c, const zs::SlicePtrs& sp, int32_t n, float* acc,
                                int64_t count, int32_t* flag, int* nparts, cudaStream_t s) {
-  auto k = zs::k_reduce<DT, RA, ST, 1, false, true>;
-  const int grid = grid_for(c, k, (count >> 3) + 8, ZS_GRID_WAVES);
+  constexpr int VPT = ZS_NORM_VPT;
+  auto k = zs::k_reduce<DT, RA, ST, VPT, false, true>;
+  const int grid = grid_for(c, k, (count >> 3) / VPT + 8, ZS_GRID_WAVES);
   if (grid > c->norm_cap) {
     if (c->d_norm_parts) cudaFree(c->d_norm_parts);
     c->d_norm_parts = nullptr;

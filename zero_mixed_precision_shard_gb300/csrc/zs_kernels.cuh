@@ -45,6 +45,9 @@
 #ifndef ZS_VPT_FIRST_SMALL_N  // ... for the first micro-step (no accumulator read), n <= 2
 #define ZS_VPT_FIRST_SMALL_N 1
 #endif
+#ifndef ZS_NORM_VPT  // vector units per thread of the pass that also forms the clipping norm
+#define ZS_NORM_VPT 1
+#endif
 #ifndef ZS_HACC_VPT  // vector units per thread of the half-accumulator reduce
 #define ZS_HACC_VPT 1
 #endif
@@ -553,13 +556,36 @@ __global__ void ZS_BOUNDS
     }
   }
   if constexpr (NORM) {
-    double total;
-    if (__syncthreads_or(big)) {
-      total = block_sum((double)sqf + sqd);
-    } else {
-      total = block_sum_f(sqf);
+    // one barrier for the flag and the norm: warp sums in fp32 (fp64 only in
+    // a warp that saw a sum above 1e18), then thread 0 adds the warp totals
+    __shared__ float wf[kThreads / 32];
+    __shared__ double wd[kThreads / 32];
+    __shared__ int wbad[kThreads / 32];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+      sqf = __fadd_rn(sqf, __shfl_down_sync(0xffffffffu, sqf, off));
+    if (__any_sync(0xffffffffu, big)) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) sqd += __shfl_down_sync(0xffffffffu, sqd, off);
     }
-    if (threadIdx.x == 0) partials[blockIdx.x] = total;
+    const int wb = __any_sync(0xffffffffu, bad);
+    if ((threadIdx.x & 31) == 0) {
+      wf[threadIdx.x >> 5] = sqf;
+      wd[threadIdx.x >> 5] = sqd;
+      wbad[threadIdx.x >> 5] = wb;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      double total = 0.0;
+      int any = 0;
+      for (int w = 0; w < kThreads / 32; ++w) {
+        total += (double)wf[w] + wd[w];
+        any |= wbad[w];
+      }
+      partials[blockIdx.x] = total;
+      if (any) atomicOr(flag, 1);
+    }
+    return;
   }
   if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(flag, 1);
 }
