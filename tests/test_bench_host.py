@@ -1,0 +1,53 @@
+"""Host-side logic of the benchmark: the algorithmic byte model against the
+workload table, and the rule that recorded ncu traffic is only reported for
+the workload and kernel sources it was captured with.  No GPU."""
+import json
+import os
+
+import bench
+import synth
+
+
+def test_algorithmic_bytes_per_step():
+    # 2·N·G (every gradient once) + 8·(G-1) (fp32 accumulator carried) + 26 (master/m/v r/w, half)
+    want = {"flat-1m-n2": 30, "gpt2-small-n8": 114, "decoder-1.3b-n16": 98,
+            "llama7b-zero3-n64": 154, "llama7b-n1": 98}
+    for name, b in want.items():
+        wl = synth.WORKLOADS[name]
+        assert bench.alg_bytes_per_elem_step(wl.n, wl.g) == b
+    # the half accumulator carries 2-byte values
+    assert bench.alg_bytes_per_elem_step(1, 8, acc_bytes=2) == 2 * 8 + 4 * 7 + 26
+
+
+def test_kernel_bytes_add_up_to_the_step():
+    # materialise path (N >= 4): first + (G-2) later accumulates + last accumulate + update
+    for n, g in ((8, 4), (16, 2), (64, 1)):
+        ks = [bench.kernel_alg_bytes("reduce", n, first=(k == 0)) for k in range(g)]
+        ks.append(bench.kernel_alg_bytes("apply", n))
+        # materialising the last micro-step writes acc (4) and the update reads it back (4)
+        assert sum(ks) == bench.alg_bytes_per_elem_step(n, g) + 8
+    # re-read path (N < 4): the flag pass re-reads the last slices
+    n, g = 1, 8
+    ks = [bench.kernel_alg_bytes("reduce", n, first=(k == 0)) for k in range(g - 1)]
+    ks += [bench.kernel_alg_bytes("check", n), bench.kernel_alg_bytes("apply_recompute", n,
+                                                                        with_acc=True)]
+    assert sum(ks) == bench.alg_bytes_per_elem_step(n, g) + 2 * n
+
+
+def test_recorded_traffic_requires_matching_sources(tmp_path, monkeypatch):
+    rec = json.load(open(os.path.join(bench.ROOT, "profiles", "traffic.json")))
+    assert set(rec["bytes_per_elem"]) >= {"reduce", "check", "apply_recompute", "reduce_first"}
+    # reads measured by ncu never exceed the algorithmic bytes (no re-reads)
+    for k, alg in rec["algorithmic_bytes_per_elem"].items():
+        assert rec["bytes_per_elem"][k] <= alg + 0.01
+    assert bench.recorded_traffic("gpt2-small-n8", "reduce", 1e6) is None
+    # a copy of the repo whose kernel source differs gets no traffic
+    fake = tmp_path / "repo"
+    (fake / "profiles").mkdir(parents=True)
+    (fake / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    for rel in rec["sources_sha256"]:
+        p = fake / rel
+        p.parent.mkdir(parents=True, exist_ok=True)
+        p.write_text("// changed\n")
+    monkeypatch.setattr(bench, "ROOT", str(fake))
+    assert bench.recorded_traffic(rec["workload"], "reduce", 1e6) is None
