@@ -178,3 +178,49 @@ def test_two_phase_clipping_across_shards(zs, ctx):
         close(dev[q][1].cpu().numpy(), states[q].m, "m")
         close(dev[q][2].cpu().numpy(), states[q].v, "v")
         assert ulps(dev[q][3].cpu().numpy().view(np.uint16), states[q].half).max() <= 1
+
+
+@pytest.mark.parametrize("n,G", [(1, 1), (2, 2), (4, 2), (16, 1)])
+def test_fused_norm_of_huge_sums(zs, ctx, n, G):
+    """bf16 gradients near 1e30 (finite; their squares pass the fp32 maximum)
+    beside ordinary ones: the norm fused into the last pass, on the re-read
+    (n < 4) and the materialising (n >= 4) forms, matches the oracle's fp64
+    norm, and the clipped step matches the oracle's state."""
+    rng = np.random.default_rng(100 + n * 3 + G)
+    count = 70_003
+    master0 = (rng.standard_normal(count) * 0.02).astype(np.float32)
+    st = oracle.ShardState.from_master(master0, BF16)
+    hp_v = (1e-3, 0.9, 0.999, 1e-8, 0.01)
+    hp_o, hp = oracle.make_hparams(*hp_v), zs.make_hparams(*hp_v)
+    sc_o = oracle.make_scaler(1.0, 1.0, 1000, 1, False)
+    sc = zs.zs_scaler_init(1.0, 1.0, 1000, 1, False)
+    master = torch.from_numpy(master0.copy()).cuda()
+    m, v = torch.zeros_like(master), torch.zeros_like(master)
+    half = torch.zeros(count, dtype=torch.int16, device="cuda")
+    acc = torch.zeros(count, dtype=torch.float32, device="cuda")
+    t = t_o = 0
+    for s in range(1, 3):
+        vals = [[(rng.standard_normal(count) * 1e-2).astype(np.float32) for _ in range(n)]
+                for _ in range(G)]
+        # both sides of the 1e18 split, in one 8-element vector and alone, and the tail
+        for pos, x in ((5, 1e30), (6, 2e18), (7, 9e17), (4_001, -3e29), (40_000, 1.5e18),
+                       (count - 1, 7e25)):
+            vals[G - 1][n - 1][pos] = x * (1 + s)
+        grads = [[lib_half(x, BF16) for x in micro] for micro in vals]
+        ovf_o, t_o, _, norm_o = oracle.shard_step(grads, BF16, st, hp_o, t_o, sc_o,
+                                                  max_norm=1.0, return_norm=True)
+        dg = [[dev16(x) for x in micro] for micro in grads]
+        for k in range(G - 1):
+            zs.zs_grad_accum(ctx, dg[k], BF16, count, acc, k == 0)
+        ovf, ns, norm = zs.zs_shard_step_clipped(ctx, dg[G - 1], BF16, count, acc, G, master,
+                                                 m, v, half, hp, t + 1, sc, 1.0)
+        if not ovf:
+            t += 1
+        assert ovf == ovf_o == 0 and ns == sc_o.scale
+        assert norm_o > 1e29
+        assert abs(norm - norm_o) <= 1e-6 * norm_o
+    assert t == t_o == 2
+    close(master.cpu().numpy(), st.master, "master")
+    close(m.cpu().numpy(), st.m, "m")
+    close(v.cpu().numpy(), st.v, "v")
+    assert ulps(half.cpu().numpy().view(np.uint16), st.half).max() <= 1

@@ -19,8 +19,9 @@
 //    lifetime at the sizes that matter;
 //  * the N rank pointers travel as a __grid_constant__ parameter block, read
 //    from the constant bank without a local-memory copy;
-//  * the overflow flag is a CTA-wide OR (__syncthreads_or) and one atomicOr
-//    per CTA that saw a non-finite sum.
+//  * the overflow flag is a warp-wide OR and one atomicOr per warp that saw a
+//    non-finite sum: no CTA barrier, so a warp that is done retires without
+//    waiting for the CTA's slowest warp.
 //
 // Arithmetic contract (DeepSpeed Complete Guide, §2.2 and §4.3, under the
 // reading that the accumulator is fp32 and ranks are summed in order):
@@ -63,15 +64,24 @@
 #ifndef ZS_ACC_STREAM  // accumulator L2 hints: 0 default, 1 evict-first, 2 evict-last,
 #define ZS_ACC_STREAM 3 // 3 chosen per call by size (acc_keep)
 #endif
+#ifndef ZS_WARP_FLAG  // 1: the flag is a warp-wide OR and one atomicOr per warp (no CTA
+#define ZS_WARP_FLAG 1  // barrier, so warps retire independently); 0: a CTA-wide OR
+#endif
 #ifndef ZS_CHECK_VPT  // vector units per thread of the flag-only pass
 #define ZS_CHECK_VPT 8
 #endif
 #ifndef ZS_CHECK_WAVES  // grid waves of the flag-only pass (0 = one thread per VPT units)
 #define ZS_CHECK_WAVES 0
 #endif
-#ifndef ZS_MIN_BLOCKS  // __launch_bounds__ minimum resident CTAs per SM (0 = unset)
+#ifndef ZS_MIN_BLOCKS  // __launch_bounds__ minimum resident CTAs per SM (0 leaves it unset)
 #define ZS_MIN_BLOCKS 0
 #endif
+#ifndef ZS_NORM_MIN_BLOCKS  // resident CTAs per SM the norm-forming pass is compiled for: 8 x 256
+#define ZS_NORM_MIN_BLOCKS 8    // threads fill the SM (at most 32 registers); its few extra live
+#endif                          // values would otherwise cost a quarter of the resident warps
+#ifndef ZS_FIRST_MIN_BLOCKS  // resident CTAs per SM the first micro-step's accumulate (one unit
+#define ZS_FIRST_MIN_BLOCKS 8    // per thread, no accumulator read) is compiled for: 32 registers,
+#endif                           // the full SM; the later micro-steps' pass runs best unbounded
 #if ZS_MIN_BLOCKS > 0
 #define ZS_BOUNDS __launch_bounds__(ZS_THREADS, ZS_MIN_BLOCKS)
 #else
@@ -424,6 +434,18 @@ __device__ __forceinline__ double sq8(const float a[8]) {
   return (double)__fadd_rn(__fadd_rn(s01, s23), __fadd_rn(s45, s67));
 }
 
+// OR `bad` into the step's flag: one atomicOr per CTA (or per warp) that saw a
+// non-finite value; a set flag is not written again.
+__device__ __forceinline__ void raise_flag(int32_t* flag, bool bad) {
+#if ZS_WARP_FLAG
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0 &&
+      *reinterpret_cast<volatile int32_t*>(flag) == 0)
+    atomicOr(flag, 1);
+#else
+  if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(flag, 1);
+#endif
+}
+
 // Fixed-order CTA sum of one double per thread; the result is valid in thread 0.
 __device__ __forceinline__ double block_sum(double x) {
   __shared__ double warp_part[kThreads / 32];
@@ -468,7 +490,9 @@ __device__ __forceinline__ double block_sum_f(float x) {
 // VPT vector units per thread per trip, `stride` apart so each load
 // instruction of a warp covers 512 contiguous bytes.
 template <int DT, bool READ_ACC, bool STORE, int VPT, bool HACC = false, bool NORM = false>
-__global__ void ZS_BOUNDS
+__global__ void __launch_bounds__(ZS_THREADS, NORM && !STORE ? ZS_NORM_MIN_BLOCKS
+                                             : VPT == 1 && !NORM && !READ_ACC ? ZS_FIRST_MIN_BLOCKS
+                                                                              : ZS_MIN_BLOCKS)
     k_reduce(const __grid_constant__ SlicePtrs s, int n, float* __restrict__ acc, int64_t count,
              int32_t* __restrict__ flag, double* __restrict__ partials, uint32_t acc_keep) {
   const uint64_t pol = acc_policy(acc_keep);
@@ -476,11 +500,13 @@ __global__ void ZS_BOUNDS
   // to it, and the flag tests the rounded value.
   // NORM: also writes this CTA's sum of squares of the sums to partials[blockIdx.x]
   // (the clipping norm of the last micro-step, fused into its pass): squares
-  // and the CTA reduction in fp32, the CTA total in fp64; a CTA holding a sum
-  // above 1e18 in magnitude (whose square could overflow fp32) reduces in fp64.
+  // and the CTA reduction in fp32, the CTA total in fp64.  A vector holding a
+  // sum above 1e18 in magnitude (whose square could overflow fp32) is squared
+  // after an exact scaling by 2^-80 into a second fp32 sum, which the CTA total
+  // scales back by 2^160 (finite fp32 values stay below 2^128, so the scaled
+  // squares stay below 2^96).
   float sqf = 0.0f;
-  double sqd = 0.0;
-  bool big = false;
+  float sqb = 0.0f;
   const int64_t nvec = count >> 3;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
@@ -521,9 +547,10 @@ __global__ void ZS_BOUNDS
 #pragma unroll
         for (int k = 0; k < 8; ++k) b |= fabsf(a[j][k]) > 1e18f;
         if (b) {
-          big = true;
+          float t[8];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) sqd += (double)a[j][k] * (double)a[j][k];
+          for (int k = 0; k < 8; ++k) t[k] = __fmul_rn(a[j][k], 0x1p-80f);
+          sqb = __fadd_rn(sqb, sq8f(t));
         } else {
           sqf = __fadd_rn(sqf, sq8f(a[j]));
         }
@@ -547,8 +574,8 @@ __global__ void ZS_BOUNDS
       if constexpr (STORE) acc[i] = a;
       if constexpr (NORM) {
         if (fabsf(a) > 1e18f) {
-          big = true;
-          sqd += (double)a * (double)a;
+          const float t = __fmul_rn(a, 0x1p-80f);
+          sqb = __fmaf_rn(t, t, sqb);
         } else {
           sqf = __fmaf_rn(a, a, sqf);
         }
@@ -556,30 +583,31 @@ __global__ void ZS_BOUNDS
     }
   }
   if constexpr (NORM) {
-    // one barrier for the flag and the norm: warp sums in fp32 (fp64 only in
-    // a warp that saw a sum above 1e18), then thread 0 adds the warp totals
+    // one barrier for the flag and the norm: warp sums in fp32, then thread 0
+    // adds the warp totals in fp64
     __shared__ float wf[kThreads / 32];
-    __shared__ double wd[kThreads / 32];
+    __shared__ float wb[kThreads / 32];
     __shared__ int wbad[kThreads / 32];
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
       sqf = __fadd_rn(sqf, __shfl_down_sync(0xffffffffu, sqf, off));
-    if (__any_sync(0xffffffffu, big)) {
+    if (__any_sync(0xffffffffu, sqb != 0.0f)) {
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sqd += __shfl_down_sync(0xffffffffu, sqd, off);
+      for (int off = 16; off > 0; off >>= 1)
+        sqb = __fadd_rn(sqb, __shfl_down_sync(0xffffffffu, sqb, off));
     }
-    const int wb = __any_sync(0xffffffffu, bad);
+    const int wbd = __any_sync(0xffffffffu, bad);
     if ((threadIdx.x & 31) == 0) {
       wf[threadIdx.x >> 5] = sqf;
-      wd[threadIdx.x >> 5] = sqd;
-      wbad[threadIdx.x >> 5] = wb;
+      wb[threadIdx.x >> 5] = sqb;
+      wbad[threadIdx.x >> 5] = wbd;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
       double total = 0.0;
       int any = 0;
       for (int w = 0; w < kThreads / 32; ++w) {
-        total += (double)wf[w] + wd[w];
+        total += (double)wf[w] + (double)wb[w] * 0x1p160;
         any |= wbad[w];
       }
       partials[blockIdx.x] = total;
@@ -587,7 +615,7 @@ __global__ void ZS_BOUNDS
     }
     return;
   }
-  if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(flag, 1);
+  raise_flag(flag, bad);
 }
 
 // Flag-only pass that tests the raw half bit patterns: an element is not
@@ -627,7 +655,7 @@ __global__ void ZS_BOUNDS k_check_bits(const __grid_constant__ SlicePtrs s, int 
       bad |= (b & lo) == lo;
     }
   }
-  if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(flag, 1);
+  raise_flag(flag, bad);
 }
 
 // AdamW + cast.  HAS_ACC: the sum starts from acc (else +0.0f).  RECOMPUTE:
