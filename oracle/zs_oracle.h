@@ -48,9 +48,11 @@
  * accumulator; Adam closed forms at t=1, at every t under a constant gradient
  * and at t=2 for two given gradients; decoupled decay at g=0; the hand-worked
  * scaler trace; half rounding against numpy (fp16) and torch (bf16) over
- * every fp16 pattern and crafted ties; shard union and bucket invariance.
- * Multi-step values under random gradients beyond those closed forms rest on
- * the oracle alone: parity unpinned.
+ * every fp16 pattern and crafted ties; shard union and bucket invariance;
+ * ten-step runs (a skipped step, a halved scale, clipping, both accumulator
+ * formats) against torch.optim.AdamW and clip_grad_norm_ in fp64 fed the same
+ * mean gradient, with master/m/v rounded to fp32 between steps on both sides
+ * (that rounding is the one reading those runs share with this file).
  */
 #ifndef ZS_ORACLE_H
 #define ZS_ORACLE_H

@@ -1,7 +1,8 @@
 """Pins of the CPU oracle to facts fixed outside it: the pages' printed memory
 formulas and figures, closed forms of bias-corrected Adam, exact sums, library
-half conversions, a hand-worked loss-scale trace, and invariants (shard union,
-bucket independence, skip-and-halve).  No GPU."""
+half conversions, a hand-worked loss-scale trace, invariants (shard union,
+bucket independence, skip-and-halve), and multi-step runs against a library
+AdamW (torch.optim.AdamW, clip_grad_norm_) in fp64.  No GPU."""
 import json
 import math
 import os
@@ -656,3 +657,133 @@ def test_random_union_and_bucket_invariance(seed):
                                      part, first=(k == 0))
         acc_b[b:e] = part
     assert acc_b.tobytes() == acc_full[:E].tobytes()
+
+
+# ------------------------------------------ multi-step against a library AdamW
+
+def _f32_sequential_sum(grads, dtype):
+    """Per element: +0.0, then every micro-step's ranks in order, each an IEEE
+    fp32 add (numpy float32 arithmetic, independent of the oracle's C)."""
+    a = np.zeros(grads[0][0].shape[0], np.float32)
+    for micro in grads:
+        for bits in micro:
+            if dtype == FP16:
+                x = bits.view(np.float16).astype(np.float32)
+            else:
+                x = (bits.astype(np.uint32) << 16).view(np.float32)
+            a = (a + x).astype(np.float32)
+    return a
+
+
+@pytest.mark.parametrize("dtype,n,g,max_norm,wd", [(FP16, 3, 2, 0.0, 0.01), (BF16, 2, 3, 0.0, 0.1),
+                                                    (FP16, 4, 1, 0.01, 0.01),
+                                                    (BF16, 1, 2, 1e-3, 0.0)])
+def test_ten_steps_match_torch_adamw(dtype, n, g, max_norm, wd):
+    """Ten steps (one skipped on an injected inf/NaN, the scale halving for fp16)
+    of the oracle against torch.optim.AdamW in fp64 (and clip_grad_norm_ when
+    clipping), fed the unscaled mean gradient acc / (N·G·S) of an fp32 sum taken
+    here, with master, m and v rounded to fp32 after every step on the torch side
+    too.  The two differ only in fp64 rounding order, so the stored fp32 state
+    must agree to one ulp (nearly everywhere bit for bit)."""
+    rng = np.random.default_rng(1000 * n + 10 * g + dtype)
+    count = 4099
+    hp = oracle.make_hparams(1e-3, 0.9, 0.999, 1e-8, wd)
+    lr, b1, b2, eps, wdf = (float(hp.lr), float(hp.beta1), float(hp.beta2), float(hp.eps),
+                            float(hp.weight_decay))
+    master0 = (rng.standard_normal(count) * 0.02).astype(np.float32)
+    st = oracle.ShardState.from_master(master0, dtype)
+    dyn = dtype == FP16
+    sc = oracle.make_scaler(1024.0 if dyn else 1.0, 1.0, 1000, 1, dyn)
+    p = torch.tensor(master0.astype(np.float64), requires_grad=True)
+    opt = torch.optim.AdamW([p], lr=lr, betas=(b1, b2), eps=eps, weight_decay=wdf,
+                            foreach=False)
+    t = 0
+    applied = 0
+    for s in range(1, 11):
+        S = sc.scale
+        grads = [[_lib_half((rng.standard_normal(count) * 1e-3 * S).astype(np.float32), dtype)
+                  for _ in range(n)] for _ in range(g)]
+        if s == 4:
+            grads[g - 1][n - 1][77] = 0x7C00 if dtype == FP16 else 0x7FC0
+        acc = _f32_sequential_sum(grads, dtype)
+        ovf, t, _ = oracle.shard_step(grads, dtype, st, hp, t, sc, max_norm=max_norm)
+        assert ovf == (s == 4)
+        if ovf:
+            continue
+        applied += 1
+        p.grad = torch.from_numpy(acc.astype(np.float64) / (n * g * S))
+        if max_norm > 0:
+            torch.nn.utils.clip_grad_norm_([p], max_norm)
+        opt.step()
+        with torch.no_grad():   # the stored state is fp32
+            p.copy_(p.float().double())
+            for key in ("exp_avg", "exp_avg_sq"):
+                buf = opt.state[p][key]
+                buf.copy_(buf.float().double())
+    assert t == applied == 9
+    if dyn:
+        assert sc.scale == 512.0
+    _same_fp32_state(st, p, opt, dtype)
+
+
+def _same_fp32_state(st, p, opt, dtype):
+    for got, want in ((st.master, p.detach()), (st.m, opt.state[p]["exp_avg"]),
+                      (st.v, opt.state[p]["exp_avg_sq"])):
+        want = want.float().numpy()
+        gi, wi = got.view(np.int32).astype(np.int64), want.view(np.int32).astype(np.int64)
+        assert np.abs(gi - wi).max() <= 1
+        assert (gi == wi).mean() > 0.999
+    assert (st.half == _lib_half(st.master, dtype)).all()
+
+
+def _half_sequential_sum(grads, dtype):
+    """The half accumulator written out with numpy/torch: per micro-step an fp32
+    sum from the rounded accumulator (or +0.0) over the ranks in order, rounded
+    to the half format to nearest even."""
+    a = np.zeros(grads[0][0].shape[0], np.uint16)
+    for k, micro in enumerate(grads):
+        x = np.zeros(a.shape[0], np.float32) if k == 0 else _decode(a, dtype)
+        for bits in micro:
+            x = (x + _decode(bits, dtype)).astype(np.float32)
+        a = _lib_half(x, dtype)
+    return a
+
+
+def _decode(bits, dtype):
+    if dtype == FP16:
+        return bits.view(np.float16).astype(np.float32)
+    return (bits.astype(np.uint32) << 16).view(np.float32)
+
+
+@pytest.mark.parametrize("dtype,n,g", [(FP16, 2, 3), (BF16, 3, 2)])
+def test_half_accumulator_steps_match_torch_adamw(dtype, n, g):
+    """The half-accumulator step: ten steps of the oracle against torch's AdamW
+    in fp64 fed the half sum (written out here) / (N·G·S), fp32 state on both
+    sides."""
+    rng = np.random.default_rng(77 + n + dtype)
+    count = 3001
+    hp = oracle.make_hparams(1e-3, 0.9, 0.999, 1e-8, 0.01)
+    master0 = (rng.standard_normal(count) * 0.02).astype(np.float32)
+    st = oracle.ShardState.from_master(master0, dtype)
+    dyn = dtype == FP16
+    sc = oracle.make_scaler(1024.0 if dyn else 1.0, 1.0, 1000, 1, dyn)
+    p = torch.tensor(master0.astype(np.float64), requires_grad=True)
+    opt = torch.optim.AdamW([p], lr=float(hp.lr), betas=(float(hp.beta1), float(hp.beta2)),
+                            eps=float(hp.eps), weight_decay=float(hp.weight_decay), foreach=False)
+    t = 0
+    for s in range(1, 11):
+        S = sc.scale
+        grads = [[_lib_half((rng.standard_normal(count) * 1e-3 * S).astype(np.float32), dtype)
+                  for _ in range(n)] for _ in range(g)]
+        acc = _half_sequential_sum(grads, dtype)
+        ovf, t, acc_o = oracle.shard_step_halfacc(grads, dtype, st, hp, t, sc)
+        assert ovf == 0 and (acc_o == acc).all()
+        p.grad = torch.from_numpy(_decode(acc, dtype).astype(np.float64) / (n * g * S))
+        opt.step()
+        with torch.no_grad():
+            p.copy_(p.float().double())
+            for key in ("exp_avg", "exp_avg_sq"):
+                buf = opt.state[p][key]
+                buf.copy_(buf.float().double())
+    assert t == 10
+    _same_fp32_state(st, p, opt, dtype)
