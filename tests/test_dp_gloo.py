@@ -1,6 +1,7 @@
 """The multi-rank path on CPU: two gloo ranks each own one shard of a small
-model and step it with dp_shard_step, using the oracle for the per-rank work.
-An overflow injected on one rank must make both ranks skip, and the union of
+model and step it with dp_shard_step (and dp_shard_step_clipped), using the
+oracle for the per-rank work.  An overflow injected on one rank must make both
+ranks skip, clipping must use the norm of the whole model, and the union of
 the two shards must equal the single-process step of all shards.  No GPU."""
 import os
 import socket
@@ -33,7 +34,7 @@ def make_grads(step, scale, psi_pad):
     return out
 
 
-def reference_union():
+def reference_union(max_norm=0.0):
     psi_pad, E = oracle.partition(PSI, N)
     master0 = np.zeros(psi_pad, np.float32)
     master0[:PSI] = np.random.default_rng(99).standard_normal(PSI) * 0.02
@@ -46,16 +47,16 @@ def reference_union():
         full = make_grads(s, sc.scale, psi_pad)
         per = [[[np.ascontiguousarray(x[q * E:(q + 1) * E]) for x in micro] for micro in full]
                for q in range(N)]
-        f, t, _ = oracle.multi_shard_step(per, 0, states, hp, t, sc)
+        f, t, _ = oracle.multi_shard_step(per, 0, states, hp, t, sc, max_norm=max_norm)
         flags.append(f)
     return flags, states, sc.scale, t
 
 
-def worker(rank, port, outdir):
+def worker(rank, port, outdir, max_norm=0.0):
     os.environ["MASTER_ADDR"] = "127.0.0.1"
     os.environ["MASTER_PORT"] = str(port)
     dist.init_process_group("gloo", rank=rank, world_size=N)
-    from zero_mixed_precision_shard_gb300.dp import dp_shard_step
+    from zero_mixed_precision_shard_gb300.dp import dp_shard_step, dp_shard_step_clipped
     psi_pad, E = oracle.partition(PSI, N)
     master0 = np.zeros(psi_pad, np.float32)
     master0[:PSI] = np.random.default_rng(99).standard_normal(PSI) * 0.02
@@ -91,7 +92,21 @@ def worker(rank, port, outdir):
                 t[0] += 1
             return ovf
 
-        flags.append(dp_shard_step(reduce_last, apply, scaler_update, flag))
+        def sumsq(d):
+            d[0] = oracle.grad_sumsq(acc, float(N * G * sc.scale))
+
+        def apply_clipped(f, d):
+            if int(f[0]) == 0:
+                coef = oracle.clip_coef(float(d[0]), max_norm)
+                oracle.adamw_apply_clipped(acc, float(N * G * sc.scale), coef, st.master, st.m,
+                                           st.v, st.half, 0, hp, t[0] + 1)
+
+        if max_norm > 0:
+            d_sumsq = torch.zeros(1, dtype=torch.float64)
+            flags.append(dp_shard_step_clipped(reduce_last, sumsq, apply_clipped, scaler_update,
+                                               flag, d_sumsq))
+        else:
+            flags.append(dp_shard_step(reduce_last, apply, scaler_update, flag))
     np.savez(os.path.join(outdir, f"rank{rank}.npz"), master=st.master, m=st.m, v=st.v,
              half=st.half, flags=np.array(flags), scale=sc.scale, t=t[0])
     dist.destroy_process_group()
@@ -105,9 +120,10 @@ def free_port():
     return p
 
 
-def test_two_gloo_ranks_skip_together(tmp_path):
-    mp.spawn(worker, args=(free_port(), str(tmp_path)), nprocs=N, join=True)
-    flags, states, scale, t = reference_union()
+@pytest.mark.parametrize("max_norm", [0.0, 0.01])
+def test_two_gloo_ranks_skip_together(tmp_path, max_norm):
+    mp.spawn(worker, args=(free_port(), str(tmp_path), max_norm), nprocs=N, join=True)
+    flags, states, scale, t = reference_union(max_norm)
     assert flags == [0, 0, 1, 0, 0, 0]
     for r in range(N):
         d = np.load(tmp_path / f"rank{r}.npz")
@@ -118,7 +134,7 @@ def test_two_gloo_ranks_skip_together(tmp_path):
 
 
 def test_single_process_without_group_is_a_plain_step():
-    from zero_mixed_precision_shard_gb300.dp import dp_shard_step
+    from zero_mixed_precision_shard_gb300.dp import dp_shard_step, dp_shard_step_clipped
     calls = []
     flag = torch.zeros(1, dtype=torch.int32)
     ovf = dp_shard_step(lambda f: calls.append("r"), lambda f: calls.append("a"),
