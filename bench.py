@@ -58,7 +58,39 @@ def kernel_alg_bytes(kind: str, n: int, first: bool = False, with_acc: bool = Fa
         return acc_bytes + 12 + 14
     if kind == "apply_recompute":
         return (4 if with_acc else 0) + 2 * n + 26
+    if kind == "sumsq":   # a separate norm pass: acc and/or the re-read slices
+        return (4 if with_acc else 0) + (2 * n if first else 0)
     raise ValueError(kind)
+
+
+def step_launch_plan(n: int, g: int, dtype: str, acc_kind: str = "fp32", has_acc: bool = True,
+                     clip: float = 0.0, split: bool = False):
+    """(kind, alg bytes per element) of every kernel one step launches, in the
+    order the step launches them (split: the step split at the overflow flag
+    as every rank of a multi-GPU run does, the clipping norm in its own pass)."""
+    if acc_kind == "half":
+        plan = [("reduce_first" if k == 0 else "reduce",
+                 kernel_alg_bytes("reduce", n, first=(k == 0), acc_bytes=2)) for k in range(g)]
+        plan.append(("apply", kernel_alg_bytes("apply", n, acc_bytes=2)))
+        return plan
+    plan = [("reduce_first" if k == 0 else "reduce",
+             kernel_alg_bytes("reduce", n, first=(k == 0))) for k in range(g - 1)]
+    recompute = n < 4 or not has_acc
+    clip_fused = clip > 0 and not split
+    if recompute:
+        # the flag pass reads acc too for bf16, or to fold in the clipping norm
+        with_acc = g > 1 and (dtype == "bf16" or clip_fused)
+        plan.append(("check", kernel_alg_bytes("check", n, with_acc=with_acc)))
+        if clip > 0 and split:
+            plan.append(("sumsq", kernel_alg_bytes("sumsq", n, first=True, with_acc=g > 1)))
+        plan.append(("apply_recompute", kernel_alg_bytes("apply_recompute", n, with_acc=g > 1)))
+    else:
+        plan.append(("reduce_first" if g == 1 else "reduce",
+                     kernel_alg_bytes("reduce", n, first=(g == 1))))
+        if clip > 0 and split:
+            plan.append(("sumsq", kernel_alg_bytes("sumsq", n, with_acc=True)))
+        plan.append(("apply", kernel_alg_bytes("apply", n)))
+    return plan
 
 
 # ---------------------------------------------------------------- device workload
@@ -158,26 +190,27 @@ class DeviceWorkload:
         zs.zs_shard_step_async(ctx, self.slices(wl.g - 1), self.dt, self.E, self.acc, wl.g,
                                self.master, self.m, self.v, self.half, self.hp, None, state)
 
-    def launch_plan(self):
+    def launch_plan(self, split: bool = False):
         """(kind, alg bytes per element) of every kernel one step launches."""
-        n, g = self.wl.n, self.wl.g
-        if self.acc_kind == "half":
-            plan = [("reduce_first" if k == 0 else "reduce",
-                     kernel_alg_bytes("reduce", n, first=(k == 0), acc_bytes=2)) for k in range(g)]
-            plan.append(("apply", kernel_alg_bytes("apply", n, acc_bytes=2)))
-            return plan
+        return step_launch_plan(self.wl.n, self.wl.g, self.wl.dtype, self.acc_kind,
+                                self.acc is not None, self.clip, split)
         plan = [("reduce_first" if k == 0 else "reduce",
                  kernel_alg_bytes("reduce", n, first=(k == 0))) for k in range(g - 1)]
         recompute = n < 4 or self.acc is None
+        clip_fused = self.clip > 0 and not split
         if recompute:
             # the flag pass reads acc too for bf16, or to fold in the clipping norm
-            with_acc = g > 1 and (self.wl.dtype == "bf16" or self.clip > 0)
+            with_acc = g > 1 and (self.wl.dtype == "bf16" or clip_fused)
             plan.append(("check", kernel_alg_bytes("check", n, with_acc=with_acc)))
+            if self.clip > 0 and split:
+                plan.append(("sumsq", kernel_alg_bytes("sumsq", n, first=True, with_acc=g > 1)))
             plan.append(("apply_recompute", kernel_alg_bytes("apply_recompute", n,
                                                              with_acc=g > 1)))
         else:
             plan.append(("reduce_first" if g == 1 else "reduce",
                          kernel_alg_bytes("reduce", n, first=(g == 1))))
+            if self.clip > 0 and split:
+                plan.append(("sumsq", kernel_alg_bytes("sumsq", n, with_acc=True)))
             plan.append(("apply", kernel_alg_bytes("apply", n)))
         return plan
 
@@ -426,10 +459,14 @@ def run_ours(args):
     torch.cuda.synchronize()
     E = W.E
     valid = min(W.valid_end - W.begin, E)
-    flag = torch.zeros(1, dtype=torch.int32, device="cuda") if world > 1 else None
+    split = world > 1 or args.split
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda") if split else None
+    d_sumsq = torch.zeros(1, dtype=torch.float64, device="cuda") if split else None
 
-    if world > 1 and args.acc != "fp32":
-        raise SystemExit("--acc half runs on one GPU")
+    if (world > 1 or args.split) and args.acc != "fp32":
+        raise SystemExit("--acc half runs the fused step on one GPU")
+    if args.split and args.graph:
+        raise SystemExit("--split and --graph are separate modes")
     graph = None
     dstate = None
     if args.graph:
@@ -446,25 +483,39 @@ def run_ours(args):
         if graph is not None:
             graph.replay()
             return 0
-        if world == 1:
+        if world == 1 and not args.split:
             return W.step(ctx)
         # replicas: each rank runs its own copy of the shard step; the one
         # real exchange is the overflow flag, all-reduced on the device before
-        # any state is written, so every rank skips together
-        from zero_mixed_precision_shard_gb300.dp import dp_shard_step
+        # any state is written, so every rank skips together (with clipping,
+        # also the shards' sums of squares, so every rank clips alike)
+        from zero_mixed_precision_shard_gb300.dp import dp_shard_step, dp_shard_step_clipped
+        # the fused call split at the flag: the same re-read form (N < 4) or
+        # materialised form as zs_shard_step chooses, so the same kernels run
+        recompute = wl.n < 4 or W.acc is None
+        last = W.slices(wl.g - 1) if recompute else None
+        acc_in = W.acc if (wl.g > 1 or not recompute) else None
+        div = float(wl.n * wl.g * W.scaler.scale)
 
         def reduce_last(f):
             f.zero_()
-            for k in range(wl.g):
-                if k == wl.g - 1 and W.acc is None:
-                    zs.zs_reduce_check(ctx, W.slices(k), W.dt, E, None, True, f)
-                else:
-                    zs.zs_reduce_check(ctx, W.slices(k), W.dt, E, W.acc, k == 0, f)
+            for k in range(wl.g - 1):
+                zs.zs_reduce_check(ctx, W.slices(k), W.dt, E, W.acc, k == 0, f)
+            if recompute:
+                zs.zs_check_last(ctx, W.slices(wl.g - 1), W.dt, E, acc_in, f)
+            else:
+                zs.zs_reduce_check(ctx, W.slices(wl.g - 1), W.dt, E, W.acc, wl.g == 1, f)
 
         def apply(f):
-            zs.zs_apply(ctx, f, W.slices(wl.g - 1) if W.acc is None else None, W.dt, W.acc, E,
-                        float(wl.n * wl.g * W.scaler.scale), W.master, W.m, W.v, W.half, W.hp,
+            zs.zs_apply(ctx, f, last, W.dt, acc_in, E, div, W.master, W.m, W.v, W.half, W.hp,
                         W.t + 1)
+
+        def sumsq(d):
+            zs.zs_grad_sumsq(ctx, last, W.dt, acc_in, E, div, d)
+
+        def apply_clipped(f, d):
+            zs.zs_apply_clipped(ctx, f, d, args.clip, last, W.dt, acc_in, E, div, W.master,
+                                W.m, W.v, W.half, W.hp, W.t + 1)
 
         def scaler_update(f):
             ovf = zs.zs_scaler_update(ctx, f, W.scaler)
@@ -472,12 +523,15 @@ def run_ours(args):
                 W.t += 1
             return ovf
 
+        if args.clip:
+            return dp_shard_step_clipped(reduce_last, sumsq, apply_clipped, scaler_update, flag,
+                                         d_sumsq)
         return dp_shard_step(reduce_last, apply, scaler_update, flag)
 
     for _ in range(args.warmup):
         one_step()
     torch.cuda.synchronize()
-    plan = W.launch_plan()
+    plan = W.launch_plan(split=split)
     ctx.timing_reset()
     ctx.set_timing(True)
     l0 = ctx.launch_count
@@ -562,8 +616,10 @@ def run_ours(args):
                 "parallelism": "replicas + overflow-flag all-reduce" if world > 1 else "1 GPU",
                 "accumulator": args.acc,
                 "clip_max_norm": args.clip or None,
-                "api": "CUDA graph of zs_grad_accum + zs_shard_step_async" if args.graph
-                       else "zs_grad_accum + zs_shard_step",
+                "api": ("CUDA graph of zs_grad_accum + zs_shard_step_async" if args.graph
+                        else "zs_reduce_check / zs_check_last + zs_apply + zs_scaler_update "
+                             "(split at the flag)" if world > 1 or args.split
+                        else "zs_grad_accum + zs_shard_step"),
                 "l2": "inputs larger than L2 (129 MB): no flush needed",
                 "inputs": "gradients generated once on the device (step-1 values, no "
                           "injections) and reused by every timed step",
@@ -657,6 +713,10 @@ def main(argv=None):
                     help="global-norm gradient clipping at this max norm (zs_shard_step_clipped)")
     ap.add_argument("--graph", action="store_true",
                     help="replay each step from a CUDA graph (device-resident scaler)")
+    ap.add_argument("--split", action="store_true",
+                    help="on one GPU, run the step split at the overflow flag as every rank of a "
+                         "multi-GPU run does (zs_reduce_check / zs_check_last, zs_apply, "
+                         "zs_scaler_update) instead of the fused zs_shard_step")
     ap.add_argument("--elements", type=int, default=None,
                     help="truncate the owned shard to its first ELEMENTS elements (profiling)")
     args = ap.parse_args(argv)

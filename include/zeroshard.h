@@ -159,6 +159,20 @@ zs_status zs_reduce_check(zs_ctx* ctx, const void* const* grads, int32_t n, zs_d
                           int64_t count, float* acc, int32_t first, int32_t* d_flag,
                           cudaStream_t stream);
 
+/* Phase 1 for the last micro-step when the update re-reads it (zs_apply with
+ * grads, which sums acc + the slices again): OR into *d_flag whether any
+ *   (acc ? acc[i] : +0.0f) + grads[0][i] + ... + grads[n-1][i]
+ * is +-inf/NaN, writing nothing else.  acc is NULL for a one-micro-step step.
+ * For fp16 the slices' bit patterns decide (finite halves cannot carry a finite
+ * acc past the fp32 maximum), 2n bytes read per element; bf16 on top of acc
+ * reads acc too.  With zs_reduce_check for micro-steps 1..G-1 and zs_apply for
+ * the update, this is zs_shard_step's re-read form split at the flag, for a
+ * caller that exchanges the flag (all ranks skip together, §4.2) before the
+ * update; it avoids writing and re-reading acc for the last micro-step
+ * (8 bytes per element) when n is small.  Same errors as zs_reduce_check. */
+zs_status zs_check_last(zs_ctx* ctx, const void* const* grads, int32_t n, zs_dtype dt,
+                        int64_t count, const float* acc, int32_t* d_flag, cudaStream_t stream);
+
 /* Phase 2: if *d_flag != 0 nothing is written.  Otherwise, per element,
  *   s = acc[i] (or +0 if acc == NULL), then s += grads[r][i] for r = 0..n-1
  *       when grads != NULL (the last micro-step, re-read instead of stored),

@@ -51,3 +51,27 @@ def test_recorded_traffic_requires_matching_sources(tmp_path, monkeypatch):
         p.write_text("// changed\n")
     monkeypatch.setattr(bench, "ROOT", str(fake))
     assert bench.recorded_traffic(rec["workload"], "reduce", 1e6) is None
+
+
+def test_launch_plans():
+    kinds = lambda plan: [k for k, _ in plan]
+    # Llama-7B, one rank, 8 micro-steps: the re-read form
+    p = bench.step_launch_plan(1, 8, "fp16")
+    assert kinds(p) == ["reduce_first"] + ["reduce"] * 6 + ["check", "apply_recompute"]
+    assert sum(b for _, b in p) == bench.alg_bytes_per_elem_step(1, 8) + 2
+    # the split step launches the same kernels; with clipping the fused form folds the
+    # norm into the flag pass (which then reads acc), the split form adds a norm pass
+    assert bench.step_launch_plan(1, 8, "fp16", split=True) == p
+    fused = dict(bench.step_launch_plan(1, 8, "fp16", clip=1.0))
+    split = dict(bench.step_launch_plan(1, 8, "fp16", clip=1.0, split=True))
+    assert fused["check"] == 6 and split["check"] == 2 and split["sumsq"] == 6
+    # 64 ranks, one micro-step: materialise, then update from acc
+    p = bench.step_launch_plan(64, 1, "fp16")
+    assert kinds(p) == ["reduce_first", "apply"]
+    assert kinds(bench.step_launch_plan(64, 1, "fp16", clip=1.0, split=True)) == \
+        ["reduce_first", "sumsq", "apply"]
+    # bf16 re-read flag pass reads acc as well
+    assert dict(bench.step_launch_plan(2, 3, "bf16"))["check"] == 2 * 2 + 4
+    # half accumulator
+    p = bench.step_launch_plan(1, 8, "fp16", acc_kind="half")
+    assert sum(b for _, b in p) == bench.alg_bytes_per_elem_step(1, 8, acc_bytes=2) + 4

@@ -96,6 +96,7 @@ def _load():
         "zs_ctx_overflow_flag": [vp, ctypes.POINTER(vp)],
         "zs_grad_accum": [vp, pp, i32, i32, i64, vp, i32, vp],
         "zs_reduce_check": [vp, pp, i32, i32, i64, vp, i32, vp, vp],
+        "zs_check_last": [vp, pp, i32, i32, i64, vp, vp, vp],
         "zs_apply": [vp, vp, pp, i32, i32, vp, i64, f32, vp, vp, vp, vp,
                      ctypes.POINTER(zs_adam_hparams), i64, vp],
         "zs_scaler_update": [vp, vp, ctypes.POINTER(zs_scaler), i32p, vp],
@@ -296,6 +297,11 @@ def zs_grad_accum(ctx: Ctx, grads, dt, count: int, acc, first: bool, stream=None
 def zs_reduce_check(ctx: Ctx, grads, dt, count: int, acc, first: bool, d_flag, stream=None):
     ctx.check(lib.zs_reduce_check(ctx.handle, _ptrs(grads), len(grads), _dtype(dt), count,
                                   _addr(acc), 1 if first else 0, _addr(d_flag), _stream(stream)))
+
+
+def zs_check_last(ctx: Ctx, grads, dt, count: int, acc, d_flag, stream=None):
+    ctx.check(lib.zs_check_last(ctx.handle, _ptrs(grads), len(grads), _dtype(dt), count,
+                                _addr(acc), _addr(d_flag), _stream(stream)))
 
 
 def zs_apply(ctx: Ctx, d_flag, grads, dt, acc, count: int, grad_div: float, master, m, v,

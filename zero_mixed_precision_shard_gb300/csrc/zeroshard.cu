@@ -718,6 +718,24 @@ zs_status zs_reduce_check(zs_ctx* c, const void* const* grads, int32_t n, zs_dty
                     stream);
 }
 
+zs_status zs_check_last(zs_ctx* c, const void* const* grads, int32_t n, zs_dtype dt,
+                        int64_t count, const float* acc, int32_t* d_flag, cudaStream_t stream) {
+  NvtxRange nvtx_("zs_check_last");
+  ZS_TRY(check_ctx(c));
+  if (dt != ZS_FP16 && dt != ZS_BF16) return fail(c, ZS_ERR_DTYPE, "unknown dtype %d", (int)dt);
+  if (count < 0) return fail(c, ZS_ERR_ARG, "count < 0");
+  if (d_flag == nullptr) return fail(c, ZS_ERR_ARG, "d_flag is NULL");
+  zs::SlicePtrs sp;
+  ZS_TRY(check_slices(c, grads, n, count, &sp));
+  ZS_TRY(check_array(c, acc, "acc", 0));
+  if (count == 0) return ZS_OK;
+  // fp16: finite halves cannot sum past the fp32 maximum on top of a finite
+  // acc, so the slices decide; bf16 sums on top of acc as the update will
+  const bool with_acc = dt == ZS_BF16 && acc != nullptr;
+  return reduce_any(c, dt, sp, n, with_acc ? const_cast<float*>(acc) : nullptr, count, with_acc,
+                    false, d_flag, stream);
+}
+
 zs_status zs_grad_accum(zs_ctx* c, const void* const* grads, int32_t n, zs_dtype dt,
                         int64_t count, float* acc, int32_t first, cudaStream_t stream) {
   NvtxRange nvtx_("zs_grad_accum");
