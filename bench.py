@@ -156,31 +156,40 @@ class DeviceWorkload:
                 synth.dev_fill_grads(buf.data_ptr(), self.E, self.begin, self.wl, step, k + 1, r,
                                      scale, s, inject=inject, inject_writer=writer)
 
-    def step(self, ctx) -> int:
-        """One optimizer step through the C ABI; returns the overflow flag."""
-        zs, wl = self.zs, self.wl
+    def accum(self, ctx, k: int):
+        """Micro-step k (< G-1) of a step through the C ABI."""
+        zs = self.zs
         if self.acc_kind == "half":
-            for k in range(wl.g - 1):
-                zs.zs_grad_accum_halfacc(ctx, self.slices(k), self.dt, self.E, self.acc, k == 0)
-            ovf, _ = zs.zs_shard_step_halfacc(ctx, self.slices(wl.g - 1), self.dt, self.E,
-                                              self.acc, wl.g, self.master, self.m, self.v,
-                                              self.half, self.hp, self.t + 1, self.scaler)
-            if not ovf:
-                self.t += 1
-            return ovf
-        for k in range(wl.g - 1):
-            zs.zs_grad_accum(ctx, self.slices(k), self.dt, self.E, self.acc, k == 0)
-        if self.clip > 0:
-            ovf, _, self.grad_norm = zs.zs_shard_step_clipped(
-                ctx, self.slices(wl.g - 1), self.dt, self.E, self.acc, wl.g, self.master, self.m,
-                self.v, self.half, self.hp, self.t + 1, self.scaler, self.clip)
+            zs.zs_grad_accum_halfacc(ctx, self.slices(k), self.dt, self.E, self.acc, k == 0)
         else:
-            ovf, _ = zs.zs_shard_step(ctx, self.slices(wl.g - 1), self.dt, self.E, self.acc,
-                                      wl.g, self.master, self.m, self.v, self.half, self.hp,
-                                      self.t + 1, self.scaler)
+            zs.zs_grad_accum(ctx, self.slices(k), self.dt, self.E, self.acc, k == 0)
+
+    def finish(self, ctx) -> int:
+        """The last micro-step and the update (the step's one synchronising
+        call); returns the overflow flag."""
+        zs, wl = self.zs, self.wl
+        last = self.slices(wl.g - 1)
+        if self.acc_kind == "half":
+            ovf, _ = zs.zs_shard_step_halfacc(ctx, last, self.dt, self.E, self.acc, wl.g,
+                                              self.master, self.m, self.v, self.half, self.hp,
+                                              self.t + 1, self.scaler)
+        elif self.clip > 0:
+            ovf, _, self.grad_norm = zs.zs_shard_step_clipped(
+                ctx, last, self.dt, self.E, self.acc, wl.g, self.master, self.m, self.v,
+                self.half, self.hp, self.t + 1, self.scaler, self.clip)
+        else:
+            ovf, _ = zs.zs_shard_step(ctx, last, self.dt, self.E, self.acc, wl.g, self.master,
+                                      self.m, self.v, self.half, self.hp, self.t + 1,
+                                      self.scaler)
         if not ovf:
             self.t += 1
         return ovf
+
+    def step(self, ctx) -> int:
+        """One optimizer step through the C ABI; returns the overflow flag."""
+        for k in range(self.wl.g - 1):
+            self.accum(ctx, k)
+        return self.finish(ctx)
 
     def step_async_calls(self, ctx, state):
         """The calls of one step on the device-resident path (capturable)."""
@@ -595,8 +604,19 @@ def run_ours(args):
 
     # end to end: gradients copied from pinned host memory every micro-step
     e2e = None
-    if not args.skip_e2e and world == 1:
-        e2e = run_e2e(zs, ctx, W, args.e2e_steps)
+    if not args.skip_e2e:
+        if world > 1:
+            dist.barrier()
+        e2e = run_e2e(zs, ctx, W, args.e2e_steps, step_fn=one_step if split else None)
+        if world > 1:  # whole job: every rank's params over the slowest rank's step
+            t = torch.tensor([e2e["ms_per_step"]], dtype=torch.float64, device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e["ms_per_step"] = float(t.item())
+            e2e["value"] = owned_total / (e2e["ms_per_step"] * 1e-3)
+            e2e["h2d_bytes_per_step"] *= world
+            e2e["d2h_bytes_per_step"] *= world
+            e2e["h2d_gbs"] = round(e2e["h2d_bytes_per_step"] / (e2e["ms_per_step"] * 1e-3) / 1e9,
+                                   1)
 
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu:
@@ -619,6 +639,9 @@ def run_ours(args):
                 "api": ("CUDA graph of zs_grad_accum + zs_shard_step_async" if args.graph
                         else "zs_reduce_check / zs_check_last + zs_apply + zs_scaler_update "
                              "(split at the flag)" if world > 1 or args.split
+                        else "zs_grad_accum_halfacc + zs_shard_step_halfacc"
+                        if args.acc == "half"
+                        else "zs_grad_accum + zs_shard_step_clipped" if args.clip
                         else "zs_grad_accum + zs_shard_step"),
                 "l2": "inputs larger than L2 (129 MB): no flush needed",
                 "inputs": "gradients generated once on the device (step-1 values, no "
@@ -645,11 +668,13 @@ def run_ours(args):
     return 0
 
 
-def run_e2e(zs, ctx, W: DeviceWorkload, steps: int):
+def run_e2e(zs, ctx, W: DeviceWorkload, steps: int, step_fn=None):
     """Same step, but every micro-step's N gradient slices are first copied
     from pinned host memory (the values a backward pass would hand over), and
-    the step result (overflow flag, new scale) is read back by zs_shard_step.
-    Copies run on a side stream, one micro-step ahead of the compute."""
+    the step result (overflow flag, new scale) is read back by the step's
+    synchronising call.  Copies run on a side stream, one micro-step ahead of
+    the compute.  step_fn (the step split at the flag, as each rank of a
+    multi-GPU run takes it) instead waits for all G copies, then runs."""
     import torch
     wl = W.wl
     host = torch.empty((wl.n, W.E), dtype=torch.int16, pin_memory=True)
@@ -665,16 +690,20 @@ def run_e2e(zs, ctx, W: DeviceWorkload, steps: int):
                 copy_stream.wait_event(free[k])
                 W.grads[k].copy_(host, non_blocking=True)
                 done[k].record(copy_stream)
+        if step_fn is not None:
+            for k in range(wl.g):
+                compute.wait_event(done[k])
+            step_fn()
+            for k in range(wl.g):
+                free[k].record(compute)
+            return
         for k in range(wl.g - 1):
             compute.wait_event(done[k])
-            zs.zs_grad_accum(ctx, W.slices(k), W.dt, W.E, W.acc, k == 0)
+            W.accum(ctx, k)
             free[k].record(compute)
         compute.wait_event(done[wl.g - 1])
-        ovf, _ = zs.zs_shard_step(ctx, W.slices(wl.g - 1), W.dt, W.E, W.acc, wl.g, W.master,
-                                  W.m, W.v, W.half, W.hp, W.t + 1, W.scaler)
+        W.finish(ctx)
         free[wl.g - 1].record(compute)
-        if not ovf:
-            W.t += 1
 
     for e in free:
         e.record(compute)

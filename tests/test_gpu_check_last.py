@@ -127,3 +127,24 @@ def test_split_step_equals_shard_step_bitwise(zs, ctx, dtype, n, G):
     assert sides[0]["sc"].scale == sides[1]["sc"].scale
     for k in ("master", "m", "v", "half"):
         assert torch.equal(sides[0][k], sides[1][k]), k
+
+
+def test_argument_errors(zs, ctx):
+    x = torch.zeros(64, dtype=torch.float32, device="cuda")
+    h = torch.zeros(64, dtype=torch.int16, device="cuda")
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for args, status in (
+            (([h[1:]], FP16, 8, None, flag), zs.ZS_ERR_ALIGN),     # misaligned slice
+            (([h], FP16, 8, x[1:], flag), zs.ZS_ERR_ALIGN),       # misaligned acc
+            (([h], 7, 8, None, flag), zs.ZS_ERR_DTYPE),
+            (([], FP16, 8, None, flag), zs.ZS_ERR_ARG),            # no ranks
+            (([h] * 257, FP16, 8, None, flag), zs.ZS_ERR_ARG),     # more than 256 ranks
+            (([h], FP16, -8, None, flag), zs.ZS_ERR_ARG),
+            (([h], FP16, 8, None, None), zs.ZS_ERR_ARG)):          # no flag
+        with pytest.raises(zs.ZsError) as e:
+            zs.zs_check_last(ctx, *args)
+        assert e.value.status == status, args[1:3]
+    # an empty range checks nothing and leaves the flag alone
+    flag.fill_(0)
+    zs.zs_check_last(ctx, [h], FP16, 0, None, flag)
+    assert int(flag.item()) == 0
