@@ -327,7 +327,12 @@ __device__ __forceinline__ void adamw1(const AdamArgs& ad, float sum, float& p, 
   v = __fmaf_rn(ad.beta2, v, __fmul_rn(ad.omb2, __fmul_rn(g, g)));
   const float m_hat = __fmaf_rn(m, ad.inv_bc1, __fmul_rn(m, ad.inv_bc1_lo));
   const float v_hat = __fmaf_rn(v, ad.inv_bc2, __fmul_rn(v, ad.inv_bc2_lo));
-  const float upd = __fdiv_rn(m_hat, __fadd_rn(__fsqrt_rn(v_hat), ad.eps));
+  float upd = __fdiv_rn(m_hat, __fadd_rn(__fsqrt_rn(v_hat), ad.eps));
+  // A finite bf16 gradient beyond ~1.8e19 in magnitude squares past the fp32
+  // maximum: v (or v_hat) becomes +inf and the Adam term 0, as in any fp32
+  // Adam; at ~3.4e38 m_hat overflows too and inf/inf would write a NaN into
+  // the weights -- that term is taken as 0 as well.
+  if (upd != upd) upd = 0.0f;
   p = __fmaf_rn(-ad.lr, __fmaf_rn(ad.wd, p, upd), p);
 }
 
