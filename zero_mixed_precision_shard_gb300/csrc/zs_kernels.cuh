@@ -474,22 +474,6 @@ __device__ __forceinline__ float sq8f(const float a[8]) {
   return __fadd_rn(__fadd_rn(s01, s23), __fadd_rn(s45, s67));
 }
 
-// CTA sum of one fp32 per thread: fixed-pattern warp shuffles in fp32, the
-// warp totals added in fp64 by thread 0 (valid there).  GB300's fp64 rate is
-// low, so the per-element work stays in fp32.
-__device__ __forceinline__ double block_sum_f(float x) {
-  __shared__ float warp_part_f[kThreads / 32];
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) x = __fadd_rn(x, __shfl_down_sync(0xffffffffu, x, off));
-  if ((threadIdx.x & 31) == 0) warp_part_f[threadIdx.x >> 5] = x;
-  __syncthreads();
-  double t = 0.0;
-  if (threadIdx.x == 0) {
-    for (int w = 0; w < kThreads / 32; ++w) t += (double)warp_part_f[w];
-  }
-  return t;
-}
-
 // Reduce + accumulate + flag.  READ_ACC: start from acc (else +0.0f).
 // STORE: write the sums back to acc (otherwise only the flag is produced).
 // VPT vector units per thread per trip, `stride` apart so each load
@@ -588,8 +572,12 @@ __global__ void __launch_bounds__(ZS_THREADS, NORM && !STORE ? ZS_NORM_MIN_BLOCK
     }
   }
   if constexpr (NORM) {
-    // one barrier for the flag and the norm: warp sums in fp32, then thread 0
-    // adds the warp totals in fp64
+    // one barrier for the flag and the norm: warp sums in fp32, then warp 0
+    // adds the warp totals in fp32 (fixed tree) and converts once to fp64.
+    // GB300's fp64 pipe is narrow: a per-warp fp64 loop here (about 40 fp64
+    // instructions per CTA) bounded the whole pass.
+    static_assert((kThreads / 32) <= 32 && ((kThreads / 32) & (kThreads / 32 - 1)) == 0,
+                  "warp totals are combined by one warp with a power-of-two tree");
     __shared__ float wf[kThreads / 32];
     __shared__ float wb[kThreads / 32];
     __shared__ int wbad[kThreads / 32];
@@ -608,15 +596,21 @@ __global__ void __launch_bounds__(ZS_THREADS, NORM && !STORE ? ZS_NORM_MIN_BLOCK
       wbad[threadIdx.x >> 5] = wbd;
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-      double total = 0.0;
-      int any = 0;
-      for (int w = 0; w < kThreads / 32; ++w) {
-        total += (double)wf[w] + (double)wb[w] * 0x1p160;
-        any |= wbad[w];
+    if (threadIdx.x < 32) {
+      const int lane = threadIdx.x;
+      constexpr int kWarps = kThreads / 32;
+      float f = lane < kWarps ? wf[lane] : 0.0f;
+      float b = lane < kWarps ? wb[lane] : 0.0f;
+      const int any = __any_sync(0xffffffffu, lane < kWarps && wbad[lane] != 0);
+#pragma unroll
+      for (int off = kWarps / 2; off > 0; off >>= 1) {
+        f = __fadd_rn(f, __shfl_down_sync(0xffffffffu, f, off));
+        b = __fadd_rn(b, __shfl_down_sync(0xffffffffu, b, off));
       }
-      partials[blockIdx.x] = total;
-      if (any) atomicOr(flag, 1);
+      if (lane == 0) {
+        partials[blockIdx.x] = b != 0.0f ? (double)f + (double)b * 0x1p160 : (double)f;
+        if (any) atomicOr(flag, 1);
+      }
     }
     return;
   }
