@@ -560,6 +560,10 @@ def run_ours(args):
     launches = ctx.launch_count - l0
     if graph is not None:  # replays bypass the context's counter: kernels per captured step
         launches = args.steps * (len(plan) + 1)
+    if world > 1:   # every rank's launches
+        n_l = torch.tensor([launches], dtype=torch.int64, device="cuda")
+        dist.all_reduce(n_l)
+        launches = int(n_l.item())
     ms = ev0.elapsed_time(ev1)
     if world > 1:
         t = torch.tensor([ms], dtype=torch.float64, device="cuda")
@@ -633,7 +637,9 @@ def run_ours(args):
                 "params": wl.psi, "owned_params": valid,
                 "shard_len": E, "n_ranks_simulated": wl.n, "accum_steps": wl.g,
                 "grad_dtype": wl.dtype, "optimizer": "AdamW" if wl.weight_decay else "Adam",
-                "parallelism": "replicas + overflow-flag all-reduce" if world > 1 else "1 GPU",
+                "parallelism": ("replicas + overflow-flag all-reduce"
+                                + (" + norm all-reduce" if args.clip else "")) if world > 1
+                               else "1 GPU",
                 "accumulator": args.acc,
                 "clip_max_norm": args.clip or None,
                 "api": ("CUDA graph of zs_grad_accum + zs_shard_step_async" if args.graph
@@ -678,7 +684,7 @@ def run_e2e(zs, ctx, W: DeviceWorkload, steps: int, step_fn=None):
     import torch
     wl = W.wl
     host = torch.empty((wl.n, W.E), dtype=torch.int16, pin_memory=True)
-    host.copy_(W.grads[0].cpu())
+    host.copy_(W.grads[0])   # device -> pinned host directly (no pageable copy)
     copy_stream = torch.cuda.Stream()
     compute = torch.cuda.current_stream()
     done = [torch.cuda.Event() for _ in range(wl.g)]
