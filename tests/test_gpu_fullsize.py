@@ -1,6 +1,8 @@
 """Full-size workloads, in the launch configuration the benchmark times
 (bench.DeviceWorkload: zs_grad_accum for micro-steps 1..G-1, zs_shard_step
-for the last), checked against the oracle on sampled elements.
+for the last), checked against the oracle on sampled elements, for the first
+shard and the last (which holds the padding where there is any, and the
+output layers).
 
 The step is elementwise once the step's overflow flag is known, so the oracle
 replays every step on a sample of the owned shard: 2^16 seeded positions, the
@@ -52,16 +54,20 @@ def half_ulps(a, b):
     return np.abs(ordered(a) - ordered(b))
 
 
-@pytest.mark.parametrize("name", ["gpt2-small-n8", "decoder-1.3b-n16", "llama7b-zero3-n64",
-                                  "llama7b-n1"])
-def test_fullsize_sampled(name):
+@pytest.mark.parametrize("name,shard", [("gpt2-small-n8", 0), ("decoder-1.3b-n16", 0),
+                                        ("llama7b-zero3-n64", 0), ("llama7b-n1", 0),
+                                        # last shards: the padding (GPT-2: 256 elements) and
+                                        # the output layers
+                                        ("gpt2-small-n8", 7), ("decoder-1.3b-n16", 15),
+                                        ("llama7b-zero3-n64", 63)])
+def test_fullsize_sampled(name, shard):
     import bench
     import zero_mixed_precision_shard_gb300 as zs
     torch.cuda.set_device(0)
     wl = synth.WORKLOADS[name]
     steps = min(wl.steps, int(os.environ.get("ZS_FULLSIZE_STEPS", wl.steps)))
     ctx = zs.Ctx()
-    W = bench.DeviceWorkload(wl, shard=0)
+    W = bench.DeviceWorkload(wl, shard=shard)
     E, begin = W.E, W.begin
     valid = W.valid_end - W.begin
     pos = sample_positions(wl, begin, E, valid)
@@ -98,13 +104,14 @@ def test_fullsize_sampled(name):
         assert W.scaler.scale == sc_o.scale, f"step {s}"
         flags.append(ovf)
         if s == min(10, steps):
-            print(f"{name}: state after step {s}: worst error / tolerance = {check_state(1.0):.3f}")
+            print(f"{name} shard {shard}: state after step {s}: worst error / tolerance = "
+                  f"{check_state(1.0):.3f}")
     assert W.t == t_o
     expect = [1 if any(begin <= j.index < begin + E for j in wl.injections_at(s)) else 0
               for s in range(1, steps + 1)]
     assert flags == expect
     if steps > 10:
-        print(f"{name}: state after step {steps}: worst error / tolerance = "
+        print(f"{name} shard {shard}: state after step {steps}: worst error / tolerance = "
               f"{check_state(4.0):.3f}")
     # padding stays zero
     if valid < E:
