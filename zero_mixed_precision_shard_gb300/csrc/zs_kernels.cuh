@@ -14,9 +14,15 @@
 //    sum-of-squares pass, whose partials array has a fixed size);
 //  * the rank slices are loaded 8 (or 4) at a time before the ordered adds,
 //    so each thread has up to 8 independent 16-byte loads outstanding;
-//  * read-once gradient slices, the accumulator and the optimizer state use
-//    evict-first loads/stores (ld/st.global.cs): nothing is re-read within L2
-//    lifetime at the sizes that matter;
+//  * read-once gradient slices and the optimizer state use evict-first
+//    loads/stores (ld/st.global.cs); the accumulator gets an L2 policy per
+//    call: evict-last while it fits in L2 with room to spare (<= 64 MB; the
+//    next micro-step and the update read it back), evict-first above;
+//  * the passes whose few extra live values would cost occupancy (the first
+//    micro-step's accumulate, the flag-only pass that forms the clipping
+//    norm) are compiled for 8 resident CTAs per SM (32 registers);
+//  * per-CTA work stays in fp32: GB300's fp64 pipe is narrow enough that a
+//    few dozen fp64 instructions per CTA bound a streaming pass;
 //  * the N rank pointers travel as a __grid_constant__ parameter block, read
 //    from the constant bank without a local-memory copy;
 //  * the overflow flag is a warp-wide OR and one atomicOr per warp that saw a
