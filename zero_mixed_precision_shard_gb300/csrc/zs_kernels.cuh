@@ -85,6 +85,9 @@
 #ifndef ZS_NORM_MIN_BLOCKS  // resident CTAs per SM the norm-forming pass is compiled for: 8 x 256
 #define ZS_NORM_MIN_BLOCKS 8    // threads fill the SM (at most 32 registers); its few extra live
 #endif                          // values would otherwise cost a quarter of the resident warps
+#ifndef ZS_APPLY_MIN_BLOCKS  // resident CTAs per SM the update is compiled for: 4 keeps every
+#define ZS_APPLY_MIN_BLOCKS 4    // variant at <= 64 registers without spills (the update from acc
+#endif                           // alone held 70, 3 CTAs per SM: 7040 -> 7137 GB/s with the bound)
 #ifndef ZS_FIRST_MIN_BLOCKS  // resident CTAs per SM the first micro-step's accumulate (one unit
 #define ZS_FIRST_MIN_BLOCKS 8    // per thread, no accumulator read) is compiled for: 32 registers,
 #endif                           // the full SM; the later micro-steps' pass runs best unbounded
@@ -668,7 +671,7 @@ __global__ void ZS_BOUNDS k_check_bits(const __grid_constant__ SlicePtrs s, int 
 // thread 0 of CTA 0 also performs the loss-scale update from the flag.
 template <int DT, bool HAS_ACC, bool RECOMPUTE, int VPT, bool CLIP = false, bool DEV = false,
           bool HACC = false>
-__global__ void ZS_BOUNDS
+__global__ void __launch_bounds__(ZS_THREADS, ZS_APPLY_MIN_BLOCKS)
     k_apply(const int32_t* __restrict__ flag, const __grid_constant__ SlicePtrs s, int n,
             const float* __restrict__ acc, float* __restrict__ master, float* __restrict__ mom,
             float* __restrict__ var, uint16_t* __restrict__ half_out, int64_t count,
