@@ -75,3 +75,33 @@ def test_launch_plans():
     # half accumulator
     p = bench.step_launch_plan(1, 8, "fp16", acc_kind="half")
     assert sum(b for _, b in p) == bench.alg_bytes_per_elem_step(1, 8, acc_bytes=2) + 4
+
+
+def _bench_line(args, env=None):
+    import subprocess
+    import sys
+    out = subprocess.run([sys.executable, os.path.join(bench.ROOT, "bench.py")] + args,
+                         capture_output=True, text=True, timeout=600,
+                         env=dict(os.environ, **(env or {})), cwd=bench.ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    return json.loads(lines[-1]) if lines else None
+
+
+def test_reference_arm_line():
+    """--impl reference times the oracle on the host cores and prints the
+    contract's line, with an e2e object that moves no bytes."""
+    d = _bench_line(["--impl", "reference", "--steps", "1", "--warmup", "1"])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC
+    assert d["value"] > 0 and d["unit"] == "params/s" and d["higher_is_better"] is True
+    assert d["config"]["workload"] == bench.DEFAULT_WORKLOAD
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == d["value"]
+    e = d["e2e"]
+    assert e["value"] == d["value"] and e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
+
+
+def test_reference_arm_other_ranks_print_nothing():
+    d = _bench_line(["--impl", "reference", "--steps", "1", "--warmup", "1"],
+                    env={"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
+    assert d is None
