@@ -128,8 +128,11 @@ zs_status zs_scaler_init(zs_scaler* s, float scale, float min_scale, int32_t win
 /* ---------------------------------------------------------------- context */
 
 /* Create a context on the current CUDA device.  It owns: the step's overflow
- * flag (a device int32, zero at creation), a device result word, 32 KB of
- * scratch for the clipping norm's partial sums, and pinned host mirrors.
+ * flag (a device int32, zero at creation), a result word in mapped pinned
+ * host memory (the update kernel writes the step's flag and new scale there;
+ * the synchronising calls read it after the stream sync, with no copy), 32 KB
+ * of scratch for the clipping norm's partial sums, and a pinned mirror of the
+ * norm.
  * *ctx is set to NULL on failure. */
 zs_status zs_ctx_create(zs_ctx** ctx);
 zs_status zs_ctx_destroy(zs_ctx* ctx);

@@ -41,8 +41,11 @@ struct zs_ctx {
   double* d_norm_parts = nullptr;      // scratch: per-CTA norm partials of the fused pass
   int norm_cap = 0;                    // capacity of d_norm_parts (doubles)
   double* h_sumsq = nullptr;           // pinned mirror of d_sumsq
-  zs::StepResult* d_result = nullptr;  // written by the loss-scale update
-  zs::StepResult* h_result = nullptr;  // pinned mirror
+  // the step's result, written by the loss-scale update straight into mapped
+  // pinned host memory (d_result is the device's address of h_result), so the
+  // synchronising calls read it after the stream sync without a copy
+  zs::StepResult* d_result = nullptr;
+  zs::StepResult* h_result = nullptr;
   std::string err;
   std::unordered_map<const void*, int> occupancy;  // resident CTAs per SM, per kernel
   int64_t launches = 0;
@@ -480,9 +483,7 @@ zs_status check_scaler(zs_ctx* c, const zs_scaler* s) {
 
 zs_status finish_step(zs_ctx* c, zs_scaler* scaler, int32_t* overflow_out, float* new_scale_out,
                       int32_t* flag_to_clear, cudaStream_t s) {
-  cudaError_t e = cudaMemcpyAsync(c->h_result, c->d_result, sizeof(zs::StepResult),
-                                  cudaMemcpyDeviceToHost, s);
-  if (e != cudaSuccess) return cuda_fail(c, e, "result copy");
+  cudaError_t e = cudaSuccess;
   if (flag_to_clear) {
     e = cudaMemsetAsync(flag_to_clear, 0, sizeof(int32_t), s);
     if (e != cudaSuccess) return cuda_fail(c, e, "flag reset");
@@ -645,9 +646,13 @@ zs_status zs_ctx_create(zs_ctx** out) {
     e = cudaDeviceGetAttribute(&c->sms, cudaDevAttrMultiProcessorCount, c->device);
   if (e == cudaSuccess) e = cudaMalloc(&c->d_flag, sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMemset(c->d_flag, 0, sizeof(int32_t));
-  if (e == cudaSuccess) e = cudaMalloc(&c->d_result, sizeof(zs::StepResult));
-  if (e == cudaSuccess) e = cudaMemset(c->d_result, 0, sizeof(zs::StepResult));
-  if (e == cudaSuccess) e = cudaMallocHost(&c->h_result, sizeof(zs::StepResult));
+  if (e == cudaSuccess)
+    e = cudaHostAlloc(reinterpret_cast<void**>(&c->h_result), sizeof(zs::StepResult),
+                      cudaHostAllocMapped);
+  if (e == cudaSuccess) {
+    std::memset(c->h_result, 0, sizeof(zs::StepResult));
+    e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&c->d_result), c->h_result, 0);
+  }
   if (e == cudaSuccess) e = cudaMalloc(&c->d_partials, ZS_SUMSQ_MAX_PARTS * sizeof(double));
   if (e == cudaSuccess) e = cudaMalloc(&c->d_sumsq, sizeof(double));
   if (e == cudaSuccess) e = cudaMemset(c->d_sumsq, 0, sizeof(double));
@@ -657,7 +662,6 @@ zs_status zs_ctx_create(zs_ctx** out) {
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     if (c->d_flag) cudaFree(c->d_flag);
-    if (c->d_result) cudaFree(c->d_result);
     if (c->h_result) cudaFreeHost(c->h_result);
     if (c->d_partials) cudaFree(c->d_partials);
     if (c->d_sumsq) cudaFree(c->d_sumsq);
@@ -680,8 +684,7 @@ zs_status zs_ctx_destroy(zs_ctx* c) {
   }
   for (auto ev : c->pool) cudaEventDestroy(ev);
   cudaFree(c->d_flag);
-  cudaFree(c->d_result);
-  cudaFreeHost(c->h_result);
+  cudaFreeHost(c->h_result);  // d_result is its device address
   cudaFree(c->d_partials);
   cudaFree(c->d_sumsq);
   cudaFree(c->d_coef);
