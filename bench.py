@@ -455,9 +455,15 @@ def run_ours(args):
     import zero_mixed_precision_shard_gb300 as zs
 
     world, rank, local = dist_env()
-    torch.cuda.set_device(local)
+    # one rank per GPU; --dist-backend gloo lets several ranks share one GPU (the
+    # exchanges then go through host memory, and no kernel waits on another rank)
+    dev = local % torch.cuda.device_count()
+    torch.cuda.set_device(dev)
     if world > 1:
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        if args.dist_backend == "nccl":
+            dist.init_process_group("nccl", device_id=torch.device("cuda", dev))
+        else:
+            dist.init_process_group("gloo")
     wl = synth.WORKLOADS[args.workload]
     ctx = zs.Ctx()
     probe = copy_probe(zs, ctx) if not args.skip_probe else {}
@@ -544,7 +550,7 @@ def run_ours(args):
     ctx.timing_reset()
     ctx.set_timing(True)
     l0 = ctx.launch_count
-    with ClockSampler(local) as clocks:
+    with ClockSampler(dev) as clocks:
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
@@ -752,6 +758,9 @@ def main(argv=None):
                     help="on one GPU, run the step split at the overflow flag as every rank of a "
                          "multi-GPU run does (zs_reduce_check / zs_check_last, zs_apply, "
                          "zs_scaler_update) instead of the fused zs_shard_step")
+    ap.add_argument("--dist-backend", default="nccl", choices=["nccl", "gloo"],
+                    help="process group of a multi-GPU run (gloo: ranks may share a GPU, for "
+                         "testing the multi-rank path on one)")
     ap.add_argument("--elements", type=int, default=None,
                     help="truncate the owned shard to its first ELEMENTS elements (profiling)")
     args = ap.parse_args(argv)
