@@ -7,6 +7,7 @@ import pytest
 import torch
 
 import oracle
+from _helpers import lib_half, ulps
 
 pytestmark = pytest.mark.gpu
 
@@ -28,13 +29,6 @@ def ctx(zs):
     c.close()
 
 
-def lib_half(x, dtype):
-    x = np.ascontiguousarray(x, dtype=np.float32)
-    if dtype == FP16:
-        return x.astype(np.float16).view(np.uint16)
-    return torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
-
-
 def close(got, want, name, lr=1e-3):
     """1e-6 relative + 1e-9 absolute, the absolute part scaled by lr / 1e-4 above
     the workloads' learning rates (these tests run at lr 1e-3)."""
@@ -43,13 +37,6 @@ def close(got, want, name, lr=1e-3):
     err = np.abs(got - want)
     tol = REL * np.abs(want) + ABS * max(1.0, lr / 1e-4)
     assert (err <= tol).all(), (name, float((err / tol).max()))
-
-
-def ulps(a, b):
-    def o(x):
-        x = x.astype(np.int32)
-        return np.where(x & 0x8000, -(x & 0x7FFF), x & 0x7FFF)
-    return np.abs(o(a) - o(b))
 
 
 # kind, min, max, warmup, total; the rates as the fp32 values the library receives

@@ -7,6 +7,7 @@ import pytest
 import torch
 
 import oracle
+from _helpers import dev16, lib_half
 
 pytestmark = pytest.mark.gpu
 
@@ -26,17 +27,6 @@ def ctx(zs):
     c = zs.Ctx()
     yield c
     c.close()
-
-
-def lib_half(x, dtype):
-    x = np.ascontiguousarray(x, dtype=np.float32)
-    if dtype == FP16:
-        return x.astype(np.float16).view(np.uint16)
-    return torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
-
-
-def dev16(bits):
-    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda()
 
 
 @pytest.mark.parametrize("dtype", [FP16, BF16])

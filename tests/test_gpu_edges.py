@@ -7,6 +7,7 @@ import pytest
 import torch
 
 import oracle
+from _helpers import dev16, host16, lib_half, ulps
 
 pytestmark = pytest.mark.gpu
 
@@ -28,17 +29,6 @@ def ctx(zs):
     c.close()
 
 
-def lib_half(x, dtype):
-    x = np.ascontiguousarray(x, dtype=np.float32)
-    if dtype == FP16:
-        return x.astype(np.float16).view(np.uint16)
-    return torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
-
-
-def dev16(bits):
-    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda()
-
-
 def close(got, want, name, lr=1e-3):
     """1e-6 relative + 1e-9 absolute (scaled by lr / 1e-4 above it); equal
     infinities where the fp32 state no longer holds the value."""
@@ -51,13 +41,6 @@ def close(got, want, name, lr=1e-3):
     err = np.abs(got[f] - want[f])
     tol = REL * np.abs(want[f]) + ABS * max(1.0, lr / 1e-4)
     assert (err <= tol).all(), (name, float((err / tol).max()))
-
-
-def ulps(a, b):
-    def o(x):
-        x = x.astype(np.int32)
-        return np.where(x & 0x8000, -(x & 0x7FFF), x & 0x7FFF)
-    return np.abs(o(a) - o(b))
 
 
 def run_steps(zs, ctx, dtype, n, G, grads_per_step, hp_vals, scale, master0):
@@ -84,10 +67,6 @@ def run_steps(zs, ctx, dtype, n, G, grads_per_step, hp_vals, scale, master0):
             t += 1
     assert t == t_o
     return st, master.cpu().numpy(), m.cpu().numpy(), v.cpu().numpy(), host16(half)
-
-
-def host16(t):
-    return t.cpu().numpy().view(np.uint16)
 
 
 def big_bf16_steps(rng, n, G, count, big, steps=3):

@@ -26,6 +26,7 @@ import torch
 
 import oracle
 import synth
+from _helpers import half_ulps
 
 pytestmark = pytest.mark.gpu
 
@@ -45,13 +46,6 @@ def sample_positions(wl, begin, E, valid):
     if valid < E:
         pos.append(np.array([valid - 1, valid, E - 1]))
     return np.unique(np.concatenate(pos).astype(np.int64))
-
-
-def half_ulps(a, b):
-    def ordered(x):
-        x = x.astype(np.int32)
-        return np.where(x & 0x8000, -(x & 0x7FFF), x & 0x7FFF)
-    return np.abs(ordered(a) - ordered(b))
 
 
 @pytest.mark.parametrize("name,shard", [("gpt2-small-n8", 0), ("decoder-1.3b-n16", 0),

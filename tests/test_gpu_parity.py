@@ -8,6 +8,7 @@ import torch
 
 import oracle
 import synth
+from _helpers import dev16, half_ulps, host16, lib_half
 
 pytestmark = pytest.mark.gpu
 
@@ -27,21 +28,6 @@ def ctx(zs):
     c = zs.Ctx()
     yield c
     c.close()
-
-
-def lib_half(x, dtype):
-    x = np.ascontiguousarray(x, dtype=np.float32)
-    if dtype == FP16:
-        return x.astype(np.float16).view(np.uint16)
-    return torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
-
-
-def dev16(bits):
-    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda()
-
-
-def host16(t):
-    return t.cpu().numpy().view(np.uint16)
 
 
 def rand_grads(rng, n, count, dtype, scale=1024.0):
@@ -65,14 +51,6 @@ def assert_state_close(got, want, name, lr=1e-4):
     bad = err > tol
     assert not bad.any(), (f"{name}: {bad.sum()} elements out of tolerance, worst "
                            f"{(err / tol).max():.3g}x at {np.argmax(err / tol)}")
-
-
-def half_ulps(a, b):
-    """Distance in units in the last place between two half bit-pattern arrays."""
-    def ordered(x):
-        x = x.astype(np.int32)
-        return np.where(x & 0x8000, -(x & 0x7FFF), x & 0x7FFF)
-    return np.abs(ordered(a) - ordered(b))
 
 
 # ---------------------------------------------------------------- reduce

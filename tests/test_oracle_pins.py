@@ -13,6 +13,7 @@ import pytest
 import torch
 
 import oracle
+from _helpers import lib_half as _lib_half
 
 FP16, BF16 = oracle.FP16, oracle.BF16
 
@@ -106,13 +107,6 @@ def test_half_round_trip_all_patterns(dtype):
     ok = ~np.isnan(vals)
     back = oracle.f32_to_half(vals[ok].astype(np.float32), dtype)
     assert (back == bits[ok]).all()
-
-
-def _lib_half(x, dtype):
-    x = np.ascontiguousarray(x, dtype=np.float32)
-    if dtype == FP16:
-        return x.astype(np.float16).view(np.uint16)
-    return torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
 
 
 @pytest.mark.parametrize("dtype", [FP16, BF16])

@@ -11,22 +11,12 @@ tests; it also passes when run alone in a fresh process."""
 import numpy as np
 import pytest
 import torch
+from _helpers import dev16, lib_half
 
 pytestmark = pytest.mark.gpu
 
 FP16, BF16 = 0, 1
 REL = 1e-6
-
-
-def lib_half(x, dtype):
-    x = np.ascontiguousarray(x, dtype=np.float32)
-    if dtype == FP16:
-        return x.astype(np.float16).view(np.uint16)
-    return torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
-
-
-def dev16(bits):
-    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda()
 
 
 @pytest.mark.parametrize("dtype", [FP16, BF16])
