@@ -130,9 +130,9 @@ zs_status zs_scaler_init(zs_scaler* s, float scale, float min_scale, int32_t win
 /* Create a context on the current CUDA device.  It owns: the step's overflow
  * flag (a device int32, zero at creation), a result word in mapped pinned
  * host memory (the update kernel writes the step's flag and new scale there;
- * the synchronising calls read it after the stream sync, with no copy), 32 KB
- * of scratch for the clipping norm's partial sums, and a pinned mirror of the
- * norm.
+ * the synchronising calls read it after the stream sync, with no copy), 8 MB
+ * of scratch for the clipping norm's per-CTA partial sums (sized here, so no
+ * later call allocates device memory), and a pinned mirror of the norm.
  * *ctx is set to NULL on failure. */
 zs_status zs_ctx_create(zs_ctx** ctx);
 zs_status zs_ctx_destroy(zs_ctx* ctx);
@@ -271,7 +271,8 @@ zs_status zs_apply_clipped(zs_ctx* ctx, const int32_t* d_flag, const double* d_s
  * The norm is computed inside the last micro-step's pass (the one that sums
  * into acc, or the flag pass of the re-read path, which then also reads acc),
  * so clipping adds no pass over the shard; its per-CTA partial sums live in
- * context scratch that grows to the grid size on first use. */
+ * the context's fixed scratch (beyond 2^31 elements the pass's grid is capped
+ * at that scratch and each thread takes several vectors). */
 zs_status zs_shard_step_clipped(zs_ctx* ctx, const void* const* grads, int32_t n, zs_dtype dt,
                                 int64_t count, float* acc, int32_t accum_steps, float* master,
                                 float* m, float* v, void* half_out, const zs_adam_hparams* hp,
@@ -291,15 +292,22 @@ zs_status zs_shard_step_clipped(zs_ctx* ctx, const void* const* grads, int32_t n
  * holds until exit, so count is limited to ZS_NOALLOC_MAX_COUNT elements;
  * larger counts return ZS_ERR_LIMIT before any work.  The call allocates
  * nothing: no cudaMalloc, cudaFree or allocating library routine.
- * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  Every call on a device shares the array and
- * leaves its partial sums in it; each call overwrites the slots it reads, so
- * nothing has to start at zero, but calls whose kernels overlap on the GPU
- * (different streams, no ordering) race on it -- serialise them.
+ * Set-up: the first call on a device, with that device current, looks up the
+ * array's device address (cudaGetSymbolAddress) and loads every kernel this
+ * entry point launches (under lazy module loading, the CUDA default, loading
+ * a kernel or a module takes device memory).  Make that first call at
+ * start-up -- a call with count = 0 is enough -- before memory can run short
+ * and before any stream capture.  A device reset (cudaDeviceReset) ends the
+ * context the address belongs to; the first call in the new context repeats
+ * the set-up, so the same start-up rule applies after a reset.
+ * Every call on a device shares the one array and leaves its partial sums in
+ * it; each call overwrites the slots it reads, so nothing has to start at
+ * zero, but calls whose kernels overlap on the GPU (different streams, no
+ * ordering) race on it -- serialise them.
  * Errors: ZS_ERR_ARG / ZS_ERR_ALIGN / ZS_ERR_DTYPE as for zs_grad_sumsq,
  * ZS_ERR_LIMIT for count > ZS_NOALLOC_MAX_COUNT, ZS_ERR_CUDA for a runtime
- * failure (no message: there is no context). */
+ * failure (no message: there is no context), including an error already
+ * pending from earlier work, which is left pending for the caller. */
 #define ZS_NOALLOC_MAX_PARTS 16384
 #define ZS_NOALLOC_ELEMS_PER_PART 16384
 #define ZS_NOALLOC_MAX_COUNT ((int64_t)ZS_NOALLOC_MAX_PARTS * ZS_NOALLOC_ELEMS_PER_PART)
@@ -347,7 +355,8 @@ typedef struct {
  * to the host and the stream is not synchronised.  A whole step -- the
  * zs_grad_accum calls plus this one -- can therefore be captured once in a
  * CUDA graph and replayed every step (make one uncaptured call first so the
- * launch shapes are cached).  Per-kernel timing is not recorded here.
+ * launch shapes are cached).  Per-kernel timing (zs_ctx_set_timing) is
+ * recorded only when `stream` is not capturing.
  * Otherwise identical to zs_shard_step (same kernels, same arithmetic). */
 zs_status zs_shard_step_async(zs_ctx* ctx, const void* const* grads, int32_t n, zs_dtype dt,
                               int64_t count, float* acc, int32_t accum_steps, float* master,

@@ -20,6 +20,11 @@
 
 // Capacity of the per-CTA partial sums of the clipping norm (one double each).
 #define ZS_SUMSQ_MAX_PARTS 4096
+// Capacity of the per-CTA norm partials of the fused last-micro-step pass,
+// allocated with the context (8 MB): one CTA per 2048 elements covers 2^31
+// elements; larger calls cap the grid here and each thread takes several
+// vector units (the pass is grid-stride), so no call allocates.
+#define ZS_NORM_MAX_PARTS (1 << 20)
 // Accumulators up to this size keep an evict-last L2 policy (they are read
 // back by the next micro-step and by the update; L2 is 129 MB on GB300).
 #ifndef ZS_ACC_KEEP_MAX_BYTES
@@ -38,8 +43,7 @@ struct zs_ctx {
   double* d_sumsq = nullptr;           // the step's squared gradient norm (zs_shard_step_clipped)
   float* d_coef = nullptr;             // scratch: clipping coefficient
   zs::AdamArgs* d_args = nullptr;      // scratch: per-step constants of the async step
-  double* d_norm_parts = nullptr;      // scratch: per-CTA norm partials of the fused pass
-  int norm_cap = 0;                    // capacity of d_norm_parts (doubles)
+  double* d_norm_parts = nullptr;      // scratch: ZS_NORM_MAX_PARTS per-CTA norm partials
   double* h_sumsq = nullptr;           // pinned mirror of d_sumsq
   // the step's result, written by the loss-scale update straight into mapped
   // pinned host memory (d_result is the device's address of h_result), so the
@@ -231,22 +235,15 @@ void launch_reduce_k(zs_ctx* c, const zs::SlicePtrs& sp, int32_t n, float* acc, 
 }
 
 // The last micro-step's pass with the clipping norm fused in: per-CTA sums of
-// squares of the final sums into the context's partials (grown on demand).
+// squares of the final sums into the context's partials (a fixed capacity:
+// the grid is capped there, and the pass strides over the rest).
 template <int DT, bool RA, bool ST>
 zs_status launch_reduce_norm_k(zs_ctx* c, const zs::SlicePtrs& sp, int32_t n, float* acc,
                                int64_t count, int32_t* flag, int* nparts, cudaStream_t s) {
   constexpr int VPT = ZS_NORM_VPT;
   auto k = zs::k_reduce<DT, RA, ST, VPT, false, true>;
-  const int grid = grid_for(c, k, (count >> 3) / VPT + 8, ZS_GRID_WAVES);
-  if (grid > c->norm_cap) {
-    if (c->d_norm_parts) cudaFree(c->d_norm_parts);
-    c->d_norm_parts = nullptr;
-    c->norm_cap = 0;
-    const int cap = (grid + 4095) / 4096 * 4096;
-    cudaError_t e = cudaMalloc(&c->d_norm_parts, (size_t)cap * sizeof(double));
-    if (e != cudaSuccess) return cuda_fail(c, e, "norm partials");
-    c->norm_cap = cap;
-  }
+  int grid = grid_for(c, k, (count >> 3) / VPT + 8, ZS_GRID_WAVES);
+  if (grid > ZS_NORM_MAX_PARTS) grid = ZS_NORM_MAX_PARTS;
   k<<<grid, zs::kThreads, 0, s>>>(sp, n, acc, count, flag, c->d_norm_parts,
                                   acc_keep_for(count));
   *nparts = grid;
@@ -659,6 +656,8 @@ zs_status zs_ctx_create(zs_ctx** out) {
   if (e == cudaSuccess) e = cudaMalloc(&c->d_coef, sizeof(float));
   if (e == cudaSuccess) e = cudaMallocHost(&c->h_sumsq, sizeof(double));
   if (e == cudaSuccess) e = cudaMalloc(&c->d_args, sizeof(zs::AdamArgs));
+  if (e == cudaSuccess)
+    e = cudaMalloc(&c->d_norm_parts, (size_t)ZS_NORM_MAX_PARTS * sizeof(double));
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     if (c->d_flag) cudaFree(c->d_flag);
@@ -668,6 +667,7 @@ zs_status zs_ctx_create(zs_ctx** out) {
     if (c->d_coef) cudaFree(c->d_coef);
     if (c->h_sumsq) cudaFreeHost(c->h_sumsq);
     if (c->d_args) cudaFree(c->d_args);
+    if (c->d_norm_parts) cudaFree(c->d_norm_parts);
     delete c;
     return ZS_ERR_CUDA;
   }
@@ -690,7 +690,7 @@ zs_status zs_ctx_destroy(zs_ctx* c) {
   cudaFree(c->d_coef);
   cudaFreeHost(c->h_sumsq);
   cudaFree(c->d_args);
-  if (c->d_norm_parts) cudaFree(c->d_norm_parts);
+  cudaFree(c->d_norm_parts);
   delete c;
   return ZS_OK;
 }
@@ -908,9 +908,15 @@ zs_status zs_shard_step_async(zs_ctx* c, const void* const* grads, int32_t n, zs
   ZS_TRY(check_array(c, half_out, "half_out", count));
   const bool recompute = (n < 4) || acc == nullptr;
   const float* acc_in = (accum_steps > 1 || !recompute) ? acc : nullptr;
-  // the async step is meant for capture: no event timing inside it
+  // per-kernel event timing only outside stream capture (an event recorded
+  // into a graph would be timed once per capture, not per replay)
   const bool timing = c->timing;
-  c->timing = false;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+    (void)cudaGetLastError();  // e.g. the legacy stream while another stream captures
+    cap = cudaStreamCaptureStatusActive;
+  }
+  if (cap != cudaStreamCaptureStatusNone) c->timing = false;
   zs_status st = ZS_OK;
   if (count > 0) {
     if (recompute) {
@@ -921,21 +927,27 @@ zs_status zs_shard_step_async(zs_ctx* c, const void* const* grads, int32_t n, zs
       st = reduce_any(c, dt, sp, n, acc, count, accum_steps > 1, true, c->d_flag, stream);
     }
   }
-  c->timing = timing;
-  ZS_TRY(st);
+  if (st != ZS_OK) {
+    c->timing = timing;
+    return st;
+  }
   zs_lr_schedule sc{};
   if (sched) sc = *sched;
   zs::k_step_prologue<<<1, 32, 0, stream>>>(d_state, n, accum_steps, *hp, sc, sched ? 1 : 0,
                                             c->d_args);
   c->launches += 1;
   uint16_t* ho = static_cast<uint16_t*>(half_out);
-  if (dt == ZS_FP16)
-    apply_dev<ZS_FP16>(c, c->d_flag, sp, recompute ? n : 0, recompute, acc_in, count, master, m,
-                       v, ho, c->d_args, d_state, stream);
-  else
-    apply_dev<ZS_BF16>(c, c->d_flag, sp, recompute ? n : 0, recompute, acc_in, count, master, m,
-                       v, ho, c->d_args, d_state, stream);
-  c->launches += 1;
+  {
+    LaunchScope ls(c, stream, recompute ? ZS_KERNEL_APPLY_RECOMPUTE : ZS_KERNEL_APPLY, count);
+    if (dt == ZS_FP16)
+      apply_dev<ZS_FP16>(c, c->d_flag, sp, recompute ? n : 0, recompute, acc_in, count, master,
+                         m, v, ho, c->d_args, d_state, stream);
+    else
+      apply_dev<ZS_BF16>(c, c->d_flag, sp, recompute ? n : 0, recompute, acc_in, count, master,
+                         m, v, ho, c->d_args, d_state, stream);
+    ls.done();
+  }
+  c->timing = timing;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(c, e, "async step launch");
   e = cudaMemsetAsync(c->d_flag, 0, sizeof(int32_t), stream);
@@ -1251,23 +1263,77 @@ namespace {
 
 constexpr int kNoallocMaxDevices = 64;
 std::mutex g_noalloc_mutex;
-double* g_noalloc_scratch[kNoallocMaxDevices] = {};
+// Per device: the scratch's device address and the id of the CUDA context it
+// was looked up in.  A device reset (cudaDeviceReset) ends that context and
+// the array's address with it; a call under a newer context looks it up again.
+struct NoallocSlot {
+  double* scratch = nullptr;
+  unsigned long long ctx_id = 0;
+};
+NoallocSlot g_noalloc[kNoallocMaxDevices];
 
-// Device address of the static scratch on the current device, looked up once
-// per device with that device current.
+typedef int (*CtxGetCurrentFn)(void** ctx);
+typedef int (*CtxGetIdFn)(void* ctx, unsigned long long* id);
+
+// Id of the calling thread's current CUDA context (0 if none), through the
+// driver entry points the runtime hands out (no link against the driver).
+unsigned long long current_ctx_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(f);
+  });
+  void* c = nullptr;
+  unsigned long long id = 0;
+  if (get_current == nullptr || get_id == nullptr || get_current(&c) != 0 || c == nullptr ||
+      get_id(c, &id) != 0)
+    return 0;
+  return id;
+}
+
+template <int DT, bool HA, bool RC>
+cudaError_t preload_sumsq() {
+  cudaFuncAttributes a;
+  return cudaFuncGetAttributes(&a, zs::k_sumsq<DT, HA, RC>);
+}
+
+// Set-up, once per device (and again after a device reset), with that device
+// current: the static scratch's device address, and every kernel this entry
+// point launches loaded now (under lazy module loading a kernel is otherwise
+// loaded, taking device memory, at its first launch).
 cudaError_t noalloc_scratch(double** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kNoallocMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (g_noalloc_scratch[dev] == nullptr) {
+  NoallocSlot& slot = g_noalloc[dev];
+  if (slot.scratch == nullptr || slot.ctx_id != current_ctx_id()) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, zs_noalloc_partials);
     if (e != cudaSuccess) return e;
-    g_noalloc_scratch[dev] = static_cast<double*>(p);
+    const cudaError_t loads[] = {
+        preload_sumsq<ZS_FP16, true, true>(), preload_sumsq<ZS_FP16, false, true>(),
+        preload_sumsq<ZS_FP16, true, false>(), preload_sumsq<ZS_BF16, true, true>(),
+        preload_sumsq<ZS_BF16, false, true>(), preload_sumsq<ZS_BF16, true, false>()};
+    for (cudaError_t le : loads)
+      if (le != cudaSuccess) return le;
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, zs::k_sumsq_finalize);
+    if (e != cudaSuccess) return e;
+    slot.scratch = static_cast<double*>(p);
+    slot.ctx_id = current_ctx_id();  // the context the lookup ran in
   }
-  *out = g_noalloc_scratch[dev];
+  *out = slot.scratch;
   return cudaSuccess;
 }
 
@@ -1300,6 +1366,8 @@ extern "C" zs_status zs_grad_sumsq_noalloc(const void* const* grads, int32_t n, 
   } else if (count > 0 && acc == nullptr) {
     return ZS_ERR_ARG;
   }
+  // an error left pending by earlier work is the caller's: report it, leave it set
+  if (cudaPeekAtLastError() != cudaSuccess) return ZS_ERR_CUDA;
   double* partials = nullptr;
   if (noalloc_scratch(&partials) != cudaSuccess) return ZS_ERR_CUDA;
   // one CTA (and one partial) per ZS_NOALLOC_ELEMS_PER_PART elements: each
