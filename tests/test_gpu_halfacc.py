@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import oracle
-from _helpers import dev16, lib_half, ulps
+from _helpers import STRESS_LR, assert_close, dev16, lib_half, ulps
 
 pytestmark = pytest.mark.gpu
 
@@ -28,14 +28,9 @@ def ctx(zs):
     c.close()
 
 
-def close(got, want, name, lr=1e-3):
-    """1e-6 relative + 1e-9 absolute, the absolute part scaled by lr / 1e-4 above
-    the workloads' learning rates (these tests run at lr 1e-3)."""
-    got = np.asarray(got, np.float64)
-    want = np.asarray(want, np.float64)
-    err = np.abs(got - want)
-    tol = REL * np.abs(want) + ABS * max(1.0, lr / 1e-4)
-    assert (err <= tol).all(), (name, float((err / tol).max()))
+def close(got, want, name):
+    """1e-6 relative + 1e-9 absolute (these tests run at lr 3e-4)."""
+    assert_close(got, want, name)
 
 
 @pytest.mark.parametrize("dtype", [FP16, BF16])
@@ -49,6 +44,30 @@ def test_halfacc_accumulate_bit_exact(zs, ctx, dtype, n, count):
              for _ in range(n)]
         zs.zs_grad_accum_halfacc(ctx, [dev16(x) for x in g], dtype, count, acc_d, k == 0)
         oracle.reduce_accumulate_half(g, dtype, acc_o, k == 0)
+    assert acc_d.cpu().numpy().view(np.uint16).tobytes() == acc_o.tobytes()
+
+
+@pytest.mark.parametrize("dtype", [FP16, BF16])
+@pytest.mark.parametrize("n", [1, 2])
+def test_halfacc_every_pattern_bit_exact(zs, ctx, dtype, n):
+    """Every finite half pattern as the carried accumulator, with n ranks' halves
+    (the patterns in other orders) added on: the rounded sums must equal the
+    oracle's bit for bit, sums past the half maximum included."""
+    b = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    exp = 0x7C00 if dtype == FP16 else 0x7F80
+    pat = b[(b & exp) != exp]
+    count = pat.size + 3
+    acc0 = np.resize(pat, count)
+    g = [np.resize(np.roll(pat[::-1], 4099 * r), count) for r in range(n)]
+    acc_o = acc0.copy()
+    oracle.reduce_accumulate_half(g, dtype, acc_o, False)
+    acc_d = dev16(acc0)
+    zs.zs_grad_accum_halfacc(ctx, [dev16(x) for x in g], dtype, count, acc_d, False)
+    assert acc_d.cpu().numpy().view(np.uint16).tobytes() == acc_o.tobytes()
+    # the first micro-step: +0 then the ranks in order
+    acc_o = np.zeros(count, np.uint16)
+    oracle.reduce_accumulate_half(g, dtype, acc_o, True)
+    zs.zs_grad_accum_halfacc(ctx, [dev16(x) for x in g], dtype, count, acc_d, True)
     assert acc_d.cpu().numpy().view(np.uint16).tobytes() == acc_o.tobytes()
 
 
@@ -76,7 +95,7 @@ def test_halfacc_shard_steps(zs, ctx, dtype, n, G, count):
     dyn = dtype == FP16
     sc_o = oracle.make_scaler(256.0 if dyn else 1.0, 1.0, 3, 1, dyn)
     sc = zs.zs_scaler_init(sc_o.scale, 1.0, 3, 1, dyn)
-    hp_v = (1e-3, 0.9, 0.999, 1e-8, 0.01)
+    hp_v = (STRESS_LR, 0.9, 0.999, 1e-8, 0.01)
     hp_o, hp = oracle.make_hparams(*hp_v), zs.make_hparams(*hp_v)
     master = torch.from_numpy(master0.copy()).cuda()
     m, v = torch.zeros_like(master), torch.zeros_like(master)

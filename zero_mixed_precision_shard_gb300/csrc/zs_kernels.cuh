@@ -320,6 +320,28 @@ __device__ __forceinline__ uint4 round8_hacc(float a[8], bool* bad) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// Rounds a[] to the half format (two values per conversion instruction) and
+// returns the packed bits; *bad |= any rounded value is not finite, decided
+// from the bits (exponent field all ones).  a[] is left as it was.
+template <int DT>
+__device__ __forceinline__ uint4 pack8_hacc(const float a[8], bool* bad) {
+  constexpr uint32_t lo = DT == ZS_FP16 ? 0x7C00u : 0x7F80u;
+  constexpr uint32_t hi = lo << 16;
+  uint32_t w[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    if constexpr (DT == ZS_FP16) {
+      const __half2 p = __floats2half2_rn(a[2 * k], a[2 * k + 1]);
+      w[k] = *reinterpret_cast<const uint32_t*>(&p);
+    } else {
+      const __nv_bfloat162 p = __floats2bfloat162_rn(a[2 * k], a[2 * k + 1]);
+      w[k] = *reinterpret_cast<const uint32_t*>(&p);
+    }
+    *bad |= ((w[k] & lo) == lo) | ((w[k] & hi) == hi);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 __device__ __forceinline__ void store8_cs(float* p, const float a[8]) {
   __stcs(reinterpret_cast<float4*>(p), make_float4(a[0], a[1], a[2], a[3]));
   __stcs(reinterpret_cast<float4*>(p + 4), make_float4(a[4], a[5], a[6], a[7]));
@@ -533,7 +555,7 @@ __global__ void __launch_bounds__(ZS_THREADS, NORM && !STORE ? ZS_NORM_MIN_BLOCK
     for (int j = 0; j < VPT; ++j) {
       if (!ok[j]) continue;
       if constexpr (HACC) {
-        const uint4 h = round8_hacc<DT>(a[j], &bad);
+        const uint4 h = pack8_hacc<DT>(a[j], &bad);
         if constexpr (STORE) __stcs(reinterpret_cast<uint4*>(acc) + vi[j], h);
       } else {
 #pragma unroll
