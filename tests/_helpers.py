@@ -34,3 +34,24 @@ def half_ulps(a, b):
 
 
 ulps = half_ulps
+
+# The parity bar for the fp32 state after at most 10 steps: 1e-6 relative plus
+# 1e-9 absolute, the same at every learning rate.  The stress tests run at the
+# highest learning rate of the workloads (the 1.3B decoder's 3e-4).
+REL, ABS = 1e-6, 1e-9
+STRESS_LR = 3e-4
+
+
+def tol_ratio(got, want):
+    """Worst |got - want| over the bound (1.0 = at the bound), over finite want."""
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    f = np.isfinite(want)
+    err = np.abs(got[f] - want[f])
+    tol = REL * np.abs(want[f]) + ABS
+    return float((err / tol).max()) if err.size else 0.0
+
+
+def assert_close(got, want, name):
+    r = tol_ratio(got, want)
+    assert r <= 1.0, f"{name}: worst error {r:.3g}x the bound (1e-6 rel + 1e-9 abs)"

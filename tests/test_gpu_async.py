@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from _helpers import lib_half, ulps
+from _helpers import STRESS_LR, assert_close, lib_half, ulps
 
 pytestmark = pytest.mark.gpu
 
@@ -29,18 +29,13 @@ def ctx(zs):
     c.close()
 
 
-def close(got, want, name, lr=1e-3):
-    """1e-6 relative + 1e-9 absolute, the absolute part scaled by lr / 1e-4 above
-    the workloads' learning rates (these tests run at lr 1e-3)."""
-    got = np.asarray(got, np.float64)
-    want = np.asarray(want, np.float64)
-    err = np.abs(got - want)
-    tol = REL * np.abs(want) + ABS * max(1.0, lr / 1e-4)
-    assert (err <= tol).all(), (name, float((err / tol).max()))
+def close(got, want, name):
+    """1e-6 relative + 1e-9 absolute (these tests run at lr 3e-4)."""
+    assert_close(got, want, name)
 
 
 # kind, min, max, warmup, total; the rates as the fp32 values the library receives
-SCHED = (oracle.LR_WARMUP_DECAY, float(np.float32(1e-5)), float(np.float32(1e-3)), 3, 9)
+SCHED = (oracle.LR_WARMUP_DECAY, float(np.float32(1e-5)), float(np.float32(STRESS_LR)), 3, 9)
 
 
 def _run(zs, ctx, dtype, n, G, count, steps, graph, inject):
@@ -106,9 +101,9 @@ def _run(zs, ctx, dtype, n, G, count, steps, graph, inject):
 @pytest.mark.parametrize("dtype", [FP16, BF16])
 @pytest.mark.parametrize("n,G,count", [(1, 3, 20_011), (2, 1, 8_192), (8, 2, 40_003)])
 def test_async_steps_match_oracle(zs, ctx, dtype, n, G, count):
-    _run(zs, ctx, dtype, n, G, count, 12, graph=False, inject={4, 5})
+    _run(zs, ctx, dtype, n, G, count, 10, graph=False, inject={4, 5})
 
 
 @pytest.mark.parametrize("n,G,count", [(1, 3, 20_011), (8, 2, 40_003)])
 def test_graph_replayed_steps_match_oracle(zs, ctx, n, G, count):
-    _run(zs, ctx, FP16, n, G, count, 12, graph=True, inject={6})
+    _run(zs, ctx, FP16, n, G, count, 10, graph=True, inject={6})

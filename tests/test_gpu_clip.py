@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from _helpers import dev16, lib_half, ulps
+from _helpers import STRESS_LR, assert_close, dev16, lib_half, ulps
 
 pytestmark = pytest.mark.gpu
 
@@ -29,14 +29,9 @@ def ctx(zs):
     c.close()
 
 
-def close(got, want, name, lr=1e-3):
-    """1e-6 relative + 1e-9 absolute, the absolute part scaled by lr / 1e-4 above
-    the workloads' learning rates (these tests run at lr 1e-3)."""
-    got = np.asarray(got, np.float64)
-    want = np.asarray(want, np.float64)
-    err = np.abs(got - want)
-    tol = REL * np.abs(want) + ABS * max(1.0, lr / 1e-4)
-    assert (err <= tol).all(), (name, float((err / tol).max()))
+def close(got, want, name):
+    """1e-6 relative + 1e-9 absolute (these tests run at lr 3e-4)."""
+    assert_close(got, want, name)
 
 
 @pytest.mark.parametrize("dtype", [FP16, BF16])
@@ -70,7 +65,7 @@ def test_clipped_shard_steps(zs, ctx, dtype, n, G, count, max_norm):
     rng = np.random.default_rng(n * 7 + G)
     master0 = (rng.standard_normal(count) * 0.02).astype(np.float32)
     st = oracle.ShardState.from_master(master0, dtype)
-    hp_v = (1e-3, 0.9, 0.999, 1e-8, 0.01)
+    hp_v = (STRESS_LR, 0.9, 0.999, 1e-8, 0.01)
     hp_o, hp = oracle.make_hparams(*hp_v), zs.make_hparams(*hp_v)
     dyn = dtype == FP16
     sc_o = oracle.make_scaler(512.0 if dyn else 1.0, 1.0, 1000, 1, dyn)
@@ -113,7 +108,7 @@ def test_large_max_norm_equals_plain_step_bitwise(zs, ctx):
         m, v = torch.zeros_like(master), torch.zeros_like(master)
         half = torch.zeros(count, dtype=torch.int16, device="cuda")
         sc = zs.zs_scaler_init(256.0, 1.0, 1000, 1, True)
-        hp = zs.make_hparams(1e-3, 0.9, 0.999, 1e-8, 0.0)
+        hp = zs.make_hparams(STRESS_LR, 0.9, 0.999, 1e-8, 0.0)
         g = [dev16(lib_half((r2.standard_normal(count) * 2.56).astype(np.float32), FP16))
              for _ in range(n)]
         if clipped:
@@ -133,7 +128,7 @@ def test_two_phase_clipping_across_shards(zs, ctx):
     rng = np.random.default_rng(21)
     psi, n = 40_000, 4
     psi_pad, E = oracle.partition(psi, n)
-    hp_v = (1e-3, 0.9, 0.999, 1e-8, 0.0)
+    hp_v = (STRESS_LR, 0.9, 0.999, 1e-8, 0.0)
     master0 = (rng.standard_normal(psi_pad) * 0.02).astype(np.float32)
     full = [lib_half((rng.standard_normal(psi_pad) * 0.3 * 256).astype(np.float32), FP16)
             for _ in range(n)]
@@ -173,7 +168,7 @@ def test_fused_norm_of_huge_sums(zs, ctx, n, G):
     count = 70_003
     master0 = (rng.standard_normal(count) * 0.02).astype(np.float32)
     st = oracle.ShardState.from_master(master0, BF16)
-    hp_v = (1e-3, 0.9, 0.999, 1e-8, 0.01)
+    hp_v = (STRESS_LR, 0.9, 0.999, 1e-8, 0.01)
     hp_o, hp = oracle.make_hparams(*hp_v), zs.make_hparams(*hp_v)
     sc_o = oracle.make_scaler(1.0, 1.0, 1000, 1, False)
     sc = zs.zs_scaler_init(1.0, 1.0, 1000, 1, False)

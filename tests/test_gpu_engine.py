@@ -7,6 +7,7 @@ import pytest
 import torch
 
 import oracle
+from _helpers import STRESS_LR, assert_close
 
 pytestmark = pytest.mark.gpu
 
@@ -20,11 +21,8 @@ def zs():
     return pkg
 
 
-def close(got, want, lr):
-    got = np.asarray(got, np.float64)
-    want = np.asarray(want, np.float64)
-    tol = 1e-6 * np.abs(want) + 1e-9 * max(1.0, lr / 1e-4)
-    assert (np.abs(got - want) <= tol).all(), float((np.abs(got - want) / tol).max())
+def close(got, want, name):
+    assert_close(got, want, name)
 
 
 @pytest.mark.parametrize("n,G,clip,sched", [(2, 3, 0.0, False), (8, 1, 0.05, True),
@@ -35,7 +33,7 @@ def test_engine_loop_matches_oracle(zs, n, G, clip, sched):
     master0 = (rng.standard_normal(count) * 0.02).astype(np.float32)
     st = oracle.ShardState.from_master(master0, FP16)
     sc_o = oracle.make_scaler(512.0, 1.0, 3, 1, True)
-    lr_max, lr_min, wu, tot = float(np.float32(1e-3)), float(np.float32(1e-4)), 3, 12
+    lr_max, lr_min, wu, tot = float(np.float32(STRESS_LR)), float(np.float32(1e-5)), 3, 12
     schedule = zs.make_schedule(zs.ZS_LR_WARMUP_DECAY, lr_min, lr_max, wu, tot) if sched else None
     ctx = zs.Ctx()
     master = torch.from_numpy(master0.copy()).cuda()
@@ -72,9 +70,9 @@ def test_engine_loop_matches_oracle(zs, n, G, clip, sched):
     state = eng.state()
     assert state["global_steps"] == steps and state["applied_steps"] == t_o == steps - 1
     assert state["micro_steps"] == steps * G and state["scaler"].scale == sc_o.scale
-    close(master.cpu().numpy(), st.master, lr_max)
-    close(m.cpu().numpy(), st.m, lr_max)
-    close(v.cpu().numpy(), st.v, lr_max)
+    close(master.cpu().numpy(), st.master, "master")
+    close(m.cpu().numpy(), st.m, "m")
+    close(v.cpu().numpy(), st.v, "v")
     eng.close()
     ctx.close()
 
