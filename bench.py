@@ -1,15 +1,24 @@
 """Benchmark of the ZeRO shard step on GB300.
 
-One step = one optimizer step of the owned shard: G-1 calls of zs_grad_accum
-(micro-steps 1..G-1, each summing the N simulated ranks' gradient slices onto
-the fp32 accumulator) and one zs_shard_step (last micro-step, overflow
-resolution, AdamW + half cast, loss-scale update).  Inputs are synthetic and
-seeded (synth/), resident in HBM before the timed region.
+One GPU: one step = one optimizer step of the owned shard: G-1 calls of
+zs_grad_accum (micro-steps 1..G-1, each summing the N simulated ranks'
+gradient slices onto the fp32 accumulator) and the step's last call (last
+micro-step, overflow resolution, AdamW + half cast, loss-scale update).  By
+default that call is zs_shard_step_async, which keeps the scale and step count
+on the device (no host round trip per step); --api sync uses zs_shard_step.
+Inputs are synthetic and seeded (synth/), resident in HBM before the timed
+region.  After the headline workload the other target workloads are measured
+in the same run (config.workloads).
 
 Default workload: the Llama-7B-shaped full model on one GPU (N = 1 simulated
 rank, G = 8 micro-steps, fp16 gradients, AdamW), 6,738,415,616 parameters,
 ~229 GB resident.  Output: one JSON line (metric: shard-step params/s, with the
 achieved HBM GB/s of the dominant kernel against the measured peak).
+
+N GPUs (torchrun, one rank per GPU): the ZeRO-2 step with its real exchanges
+(dp.Zero2Step): the workload's parameters partitioned over the N ranks, each
+rank's own full gradients exchanged bucket by bucket, the flag agreed, the
+half copy all-gathered.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle on a bounded sample
@@ -196,6 +205,12 @@ class DeviceWorkload:
         zs, wl = self.zs, self.wl
         for k in range(wl.g - 1):
             zs.zs_grad_accum(ctx, self.slices(k), self.dt, self.E, self.acc, k == 0)
+        self.finish_async(ctx, state)
+
+    def finish_async(self, ctx, state):
+        """The last call of a step on the device-resident path: the scale, Adam's
+        step count and the step's outcome stay in `state` on the device."""
+        zs, wl = self.zs, self.wl
         zs.zs_shard_step_async(ctx, self.slices(wl.g - 1), self.dt, self.E, self.acc, wl.g,
                                self.master, self.m, self.v, self.half, self.hp, None, state)
 
@@ -203,25 +218,6 @@ class DeviceWorkload:
         """(kind, alg bytes per element) of every kernel one step launches."""
         return step_launch_plan(self.wl.n, self.wl.g, self.wl.dtype, self.acc_kind,
                                 self.acc is not None, self.clip, split)
-        plan = [("reduce_first" if k == 0 else "reduce",
-                 kernel_alg_bytes("reduce", n, first=(k == 0))) for k in range(g - 1)]
-        recompute = n < 4 or self.acc is None
-        clip_fused = self.clip > 0 and not split
-        if recompute:
-            # the flag pass reads acc too for bf16, or to fold in the clipping norm
-            with_acc = g > 1 and (self.wl.dtype == "bf16" or clip_fused)
-            plan.append(("check", kernel_alg_bytes("check", n, with_acc=with_acc)))
-            if self.clip > 0 and split:
-                plan.append(("sumsq", kernel_alg_bytes("sumsq", n, first=True, with_acc=g > 1)))
-            plan.append(("apply_recompute", kernel_alg_bytes("apply_recompute", n,
-                                                             with_acc=g > 1)))
-        else:
-            plan.append(("reduce_first" if g == 1 else "reduce",
-                         kernel_alg_bytes("reduce", n, first=(g == 1))))
-            if self.clip > 0 and split:
-                plan.append(("sumsq", kernel_alg_bytes("sumsq", n, with_acc=True)))
-            plan.append(("apply", kernel_alg_bytes("apply", n)))
-        return plan
 
 
 # ---------------------------------------------------------------- clocks
@@ -448,6 +444,369 @@ def run_reference(args):
     return 0
 
 
+API_DESC = {
+    "async": "zs_grad_accum + zs_shard_step_async (scale, step count and outcome stay on the "
+             "device; no host round trip; the state is read back after the timed steps)",
+    "sync": "zs_grad_accum + zs_shard_step (one host round trip per step)",
+    "graph": "CUDA graph of zs_grad_accum + zs_shard_step_async",
+    "split": "zs_reduce_check / zs_check_last + zs_apply + zs_scaler_update (split at the flag)",
+}
+# the other target workloads, measured in the same run after the headline one
+TABLE_WORKLOADS = ("decoder-1.3b-n16", "llama7b-zero3-n64", "gpt2-small-n8")
+
+
+def resolve_api(args, world: int) -> str:
+    if world > 1 or args.split:
+        return "split"
+    if args.graph:
+        return "graph"
+    if args.acc == "half" or args.clip:
+        return "sync"   # the half-accumulator and clipped steps exist as synchronising calls
+    return args.api
+
+
+def make_step(zs, ctx, W: DeviceWorkload, api: str, clip: float = 0.0):
+    """One step of `api` on W's buffers; returns (step function, device state or None)."""
+    import torch
+    wl, E = W.wl, W.E
+    if api == "async":
+        state = zs.DeviceState(W.scaler)
+
+        def one_step():
+            W.step_async_calls(ctx, state)
+        return one_step, state
+    if api == "graph":
+        state = zs.DeviceState(W.scaler)
+        W.step_async_calls(ctx, state)       # uncaptured first call caches launch shapes
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            W.step_async_calls(ctx, state)
+        return graph.replay, state
+    if api == "sync":
+        return (lambda: W.step(ctx)), None
+    # split at the flag, as every rank of a multi-GPU run takes the step: the one
+    # real exchange is the overflow flag, all-reduced on the device before any
+    # state is written, so every rank skips together (with clipping, also the
+    # shards' sums of squares, so every rank clips alike)
+    from zero_mixed_precision_shard_gb300.dp import dp_shard_step, dp_shard_step_clipped
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    d_sumsq = torch.zeros(1, dtype=torch.float64, device="cuda")
+    # the same re-read form (N < 4) or materialised form as zs_shard_step chooses
+    recompute = wl.n < 4 or W.acc is None
+    last = W.slices(wl.g - 1) if recompute else None
+    acc_in = W.acc if (wl.g > 1 or not recompute) else None
+
+    def reduce_last(f):
+        f.zero_()
+        for k in range(wl.g - 1):
+            zs.zs_reduce_check(ctx, W.slices(k), W.dt, E, W.acc, k == 0, f)
+        if recompute:
+            zs.zs_check_last(ctx, W.slices(wl.g - 1), W.dt, E, acc_in, f)
+        else:
+            zs.zs_reduce_check(ctx, W.slices(wl.g - 1), W.dt, E, W.acc, wl.g == 1, f)
+
+    def div():
+        return float(wl.n * wl.g * W.scaler.scale)
+
+    def apply(f):
+        zs.zs_apply(ctx, f, last, W.dt, acc_in, E, div(), W.master, W.m, W.v, W.half, W.hp,
+                    W.t + 1)
+
+    def sumsq(d):
+        zs.zs_grad_sumsq(ctx, last, W.dt, acc_in, E, div(), d)
+
+    def apply_clipped(f, d):
+        zs.zs_apply_clipped(ctx, f, d, clip, last, W.dt, acc_in, E, div(), W.master, W.m, W.v,
+                            W.half, W.hp, W.t + 1)
+
+    def scaler_update(f):
+        ovf = zs.zs_scaler_update(ctx, f, W.scaler)
+        if not ovf:
+            W.t += 1
+        return ovf
+
+    def one_step():
+        if clip:
+            return dp_shard_step_clipped(reduce_last, sumsq, apply_clipped, scaler_update, flag,
+                                         d_sumsq)
+        return dp_shard_step(reduce_last, apply, scaler_update, flag)
+    return one_step, None
+
+
+def kernel_table(zs, ctx, plan):
+    """Per-kernel event times of the timed region, with algorithmic GB/s."""
+    kinds = {}
+    for kind_id, name in enumerate(zs.KERNEL_NAMES):
+        tot, nl, el = ctx.timing(kind_id)
+        if nl:
+            kinds[name] = {"ms": tot, "launches": nl, "elements": el}
+    alg_bytes = {}
+    for name, b in plan:
+        alg_bytes.setdefault(name, []).append(b)
+    for name, d in kinds.items():
+        per_launch = alg_bytes.get(name, [0])
+        avg_b = sum(per_launch) / len(per_launch) if per_launch else 0
+        d["alg_bytes_per_elem"] = avg_b
+        d["gbs"] = avg_b * (d["elements"] / d["launches"]) / (d["ms"] / d["launches"] * 1e-3) / 1e9
+    return kinds
+
+
+def timed_steps(ctx, one_step, steps: int, warmup: int, dev: int, world: int,
+                kernel_timing: bool = True):
+    """W untimed steps, then K steps between CUDA events on the launching
+    stream, bracketed by a barrier and device synchronisation, with per-kernel
+    event timing (unless kernel_timing is False) and nvidia-smi clock samples
+    during the timed region."""
+    import torch
+    import torch.distributed as dist
+    for _ in range(warmup):
+        one_step()
+    torch.cuda.synchronize()
+    ctx.timing_reset()
+    ctx.set_timing(kernel_timing)
+    l0 = ctx.launch_count
+    with ClockSampler(dev) as clocks:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record()
+        for _ in range(steps):
+            one_step()
+        ev1.record()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    ctx.set_timing(False)
+    return ev0.elapsed_time(ev1), ctx.launch_count - l0, clocks.summary()
+
+
+def measure_table_workload(zs, ctx, name: str, args, peak: float, dev: int):
+    """One more target workload in the same run: its own buffers, warm-up,
+    timed steps and clock record, through the default API and the
+    synchronising one (truncated like the headline workload under --elements)."""
+    import torch
+    wl = synth.WORKLOADS[name]
+    W = DeviceWorkload(wl, shard=0, count=args.elements)
+    W.fill_grads(1, wl.scale0, inject=False)
+    torch.cuda.synchronize()
+    valid = min(W.valid_end - W.begin, W.E)
+    step_bytes = alg_bytes_per_elem_step(wl.n, wl.g) * W.E
+    out = {"workload": name + (f" (first {W.E} elements)" if args.elements else ""),
+           "params": wl.psi, "owned_params": valid, "shard_len": W.E, "n_ranks_simulated": wl.n,
+           "accum_steps": wl.g, "grad_dtype": wl.dtype, "alg_bytes_per_step": step_bytes}
+    for api in ("async", "sync"):
+        one_step, state = make_step(zs, ctx, W, api)
+        # the step rate without per-kernel events (an event pair around each of
+        # a short step's launches costs it a few percent), then the same steps
+        # again with them for the per-kernel rates
+        ms, launches, clocks = timed_steps(ctx, one_step, args.steps, args.warmup, dev, 1,
+                                           kernel_timing=False)
+        timed_steps(ctx, one_step, args.steps, 0, dev, 1)
+        per_step = ms / args.steps
+        gbs = step_bytes / (per_step * 1e-3) / 1e9
+        kinds = kernel_table(zs, ctx, W.launch_plan())
+        out[api] = {"api": API_DESC[api], "value": valid / (per_step * 1e-3), "unit": "params/s",
+                    "ms_per_step": round(per_step, 4), "step_gbs": round(gbs, 1),
+                    "step_frac_of_peak": round(gbs / peak, 4), "gpu_launches": launches,
+                    "clocks": clocks,
+                    "kernels": {k: {"gbs": round(d["gbs"], 1), "frac_of_peak":
+                                    round(d["gbs"] / peak, 4), "launches": d["launches"]}
+                                for k, d in kinds.items()}}
+        if state is not None:
+            d = state.read()
+            out[api]["device_state"] = {"iterations": d.iterations, "step": d.step,
+                                        "scale": d.scaler.scale}
+    del W
+    torch.cuda.empty_cache()
+    return out
+
+
+class Zero2Workload:
+    """One real rank of a ZeRO-2 job over the workload's flat parameter buffer
+    (its first `count` parameters with --elements): the buffer is partitioned
+    over the job's ranks, this rank holds its own full flat fp16/bf16 gradient
+    of every micro-step (synthetic, seeded by its rank), its shard's fp32
+    accumulator, master, m and v, its shard's half copy and the full half
+    parameter buffer that the all-gather rebuilds."""
+
+    def __init__(self, zs, ctx, wl: synth.Workload, world: int, rank: int, count=None,
+                 clip: float = 0.0):
+        import torch
+        from zero_mixed_precision_shard_gb300.dp import Zero2Step, ZsShardOps
+        self.wl, self.world, self.rank = wl, world, rank
+        psi = wl.psi if count is None else count
+        self.part = zs.zs_init_partition(psi, world, synth.ALIGN_ELEMS)
+        self.psi = psi
+        P, E = self.part.psi_pad, self.part.shard_len
+        self.E = E
+        b, ve, _ = zs.zs_shard_range(self.part, rank)
+        self.valid = ve - b
+        dev = torch.device("cuda", torch.cuda.current_device())
+        s = torch.cuda.current_stream().cuda_stream
+        self.grads = torch.empty((wl.g, P), dtype=torch.int16, device=dev)
+        for k in range(wl.g):
+            synth.dev_fill_grads(self.grads[k].data_ptr(), P, 0, wl, 1, k + 1, rank, wl.scale0,
+                                 s, inject=False)
+            self.grads[k, psi:].zero_()
+        self.acc = torch.empty(E, dtype=torch.float32, device=dev)
+        self.master = torch.empty(E, dtype=torch.float32, device=dev)
+        synth.dev_fill_master(self.master.data_ptr(), E, b, wl, s)
+        if ve - b < E:
+            self.master[max(ve - b, 0):].zero_()
+        self.m = torch.zeros(E, dtype=torch.float32, device=dev)
+        self.v = torch.zeros(E, dtype=torch.float32, device=dev)
+        self.half_shard = torch.zeros(E, dtype=torch.int16, device=dev)
+        self.half_full = torch.zeros(P, dtype=torch.int16, device=dev)
+        self.scaler = zs.zs_scaler_init(wl.scale0, wl.min_scale, wl.window, wl.hysteresis,
+                                        wl.dynamic)
+        hp = zs.make_hparams(wl.lr, wl.beta1, wl.beta2, wl.eps, wl.weight_decay)
+        self.ops = ZsShardOps(zs, ctx, wl.dtype_code, E, world, wl.g, self.acc, self.master,
+                              self.m, self.v, self.half_shard, hp, self.scaler, clip)
+        bucket = wl.bucket_elems
+        # two receive slots: the next bucket's exchange overlaps this one's sum
+        self.recv = torch.empty(2 * world * min(E, bucket // 64 * 64), dtype=torch.int16,
+                                device=dev)
+        self.flag = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.step_obj = Zero2Step(self.ops, P, E, rank, bucket, self.recv, self.flag,
+                                  torch.zeros(1, dtype=torch.float64, device=dev))
+        self.clip = clip
+
+    def step(self):
+        return self.step_obj.step([self.grads[k] for k in range(self.wl.g)], self.half_full,
+                                  clip=self.clip > 0)
+
+    def launch_plan(self):
+        """(kind, alg bytes per element of the shard) of every kernel a step launches:
+        per micro-step the accumulate of the received slices (split by bucket),
+        the update from the accumulator (and the norm pass when clipping)."""
+        n, g = self.world, self.wl.g
+        plan = [("reduce_first" if k == 0 else "reduce",
+                 kernel_alg_bytes("reduce", n, first=(k == 0))) for k in range(g)]
+        if self.clip > 0:
+            plan.append(("sumsq", kernel_alg_bytes("sumsq", n, with_acc=True)))
+        plan.append(("apply", kernel_alg_bytes("apply", n)))
+        return plan
+
+
+def run_zero2(args, zs, ctx, wl, world: int, rank: int, dev: int, probe):
+    """N > 1: the ZeRO-2 step with its real exchanges on every rank."""
+    import torch
+    import torch.distributed as dist
+    Z = Zero2Workload(zs, ctx, wl, world, rank, args.elements, args.clip)
+    torch.cuda.synchronize()
+    ms, launches, clock_summary = timed_steps(ctx, Z.step, args.steps, args.warmup, dev, world)
+    kinds = kernel_table(zs, ctx, Z.launch_plan())
+    t = torch.tensor([ms], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms = float(t.item())
+    n_l = torch.tensor([launches], dtype=torch.int64, device="cuda")
+    dist.all_reduce(n_l)
+    launches = int(n_l.item())
+    per_step_ms = ms / args.steps
+    value = Z.psi / (per_step_ms * 1e-3)        # every rank's owned params over the slowest step
+    xb = Z.step_obj.exchanged_bytes(wl.g)
+    shard_bytes = (alg_bytes_per_elem_step(world, wl.g) + 8) * Z.E   # + materialised last micro
+    peak, peak_kind = measured_peaks()
+    dom = max(kinds, key=lambda k: kinds[k]["ms"]) if kinds else None
+    roofline = None
+    if dom is not None:
+        per_launch_elems = kinds[dom]["elements"] / kinds[dom]["launches"]
+        roofline = {"bound": "hbm", "kernel": dom, "achieved": round(kinds[dom]["gbs"], 1),
+                    "peak": peak, "unit": "GB/s", "frac": round(kinds[dom]["gbs"] / peak, 4),
+                    "traffic": None, "traffic_unit": "bytes per launch",
+                    "alg_bytes_per_launch": kinds[dom]["alg_bytes_per_elem"] * per_launch_elems,
+                    "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})"}
+    e2e = None
+    if not args.skip_e2e:
+        dist.barrier()
+        e2e = run_e2e_zero2(Z, args.e2e_steps)
+        t = torch.tensor([e2e["ms_per_step"]], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e["ms_per_step"] = float(t.item())
+        e2e["value"] = Z.psi / (e2e["ms_per_step"] * 1e-3)
+        e2e["h2d_bytes_per_step"] *= world
+        e2e["d2h_bytes_per_step"] *= world
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step_ms,
+            "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {
+                "workload": wl.name + (f" (first {Z.psi} parameters)" if args.elements else ""),
+                "params": Z.psi, "shard_len": Z.E, "accum_steps": wl.g, "grad_dtype": wl.dtype,
+                "optimizer": "AdamW" if wl.weight_decay else "Adam",
+                "parallelism": f"ZeRO-2 dp{world}: per micro-step an all-to-all of each "
+                               f"{wl.bucket_elems}-element gradient bucket's shard slices "
+                               "(rank q receives every rank's slice of shard q), fp32 "
+                               "rank-ordered sum in the reduce kernel; flag MAX"
+                               + (" + norm SUM" if args.clip else "")
+                               + " all-reduce; update; all-gather of the half copy",
+                "dist_backend": args.dist_backend,
+                "clip_max_norm": args.clip or None,
+                "api": "dp.Zero2Step over zs_reduce_check, zs_apply"
+                       + ("_clipped + zs_grad_sumsq" if args.clip else "")
+                       + ", zs_scaler_update",
+                "exchange_bytes_per_rank_per_step": xb,
+                "shard_alg_bytes_per_step": shard_bytes,
+                "l2": "inputs larger than L2 (129 MB): no flush needed",
+                "inputs": "every rank's full gradients generated once on the device (step-1 "
+                          "values of its rank, no injections) and reused by every timed step",
+                "copy_probe_gbs": probe,
+                "kernels": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv)
+                                for kk, vv in d.items()} for k, d in kinds.items()},
+            },
+            "roofline": roofline,
+            "clocks": clock_summary,
+            "gpu_launches": launches,
+            "e2e": e2e,
+            "cpu_baseline": None,
+        }
+        print(json.dumps(line), flush=True)
+    ctx.close()
+    dist.destroy_process_group()
+    return 0
+
+
+def run_e2e_zero2(Z: Zero2Workload, steps: int):
+    """The ZeRO-2 step with every micro-step's full flat gradient copied in
+    from pinned host memory first, and the step's result (the overflow flag
+    the loss-scale update returns) read by the host."""
+    import torch
+    host = torch.empty_like(Z.grads[0], device="cpu").pin_memory()
+    host.copy_(Z.grads[0])
+    copy_stream = torch.cuda.Stream()
+    compute = torch.cuda.current_stream()
+
+    def step():
+        ev = []
+        for k in range(Z.wl.g):
+            with torch.cuda.stream(copy_stream):
+                copy_stream.wait_stream(compute)
+                Z.grads[k].copy_(host, non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(copy_stream)
+                ev.append(e)
+        for e in ev:
+            compute.wait_event(e)
+        return Z.step()
+
+    step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    h2d = Z.wl.g * Z.grads.shape[1] * 2
+    return {"value": Z.psi / (ms * 1e-3), "unit": "params/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": 8, "ms_per_step": ms, "steps": steps}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -467,6 +826,17 @@ def run_ours(args):
     wl = synth.WORKLOADS[args.workload]
     ctx = zs.Ctx()
     probe = copy_probe(zs, ctx) if not args.skip_probe else {}
+    if world > 1:
+        if args.acc != "fp32" or args.graph or args.split:
+            raise SystemExit("N > 1 runs the ZeRO-2 step with the fp32 accumulator")
+        return run_zero2(args, zs, ctx, wl, world, rank, dev, probe)
+    api = resolve_api(args, world)
+    if api == "split" and args.acc != "fp32":
+        raise SystemExit("--acc half runs the fused step on one GPU")
+    if args.split and args.graph:
+        raise SystemExit("--split and --graph are separate modes")
+    if api == "graph" and (args.acc != "fp32" or args.clip):
+        raise SystemExit("--graph runs the unclipped fp32-accumulator path on one GPU")
 
     # with several GPUs, rank r owns shard r mod N (a ZeRO job's rank r owns shard r)
     W = DeviceWorkload(wl, shard=rank % wl.n, count=args.elements, acc=args.acc, clip=args.clip)
@@ -474,104 +844,20 @@ def run_ours(args):
     torch.cuda.synchronize()
     E = W.E
     valid = min(W.valid_end - W.begin, E)
-    split = world > 1 or args.split
-    flag = torch.zeros(1, dtype=torch.int32, device="cuda") if split else None
-    d_sumsq = torch.zeros(1, dtype=torch.float64, device="cuda") if split else None
-
-    if (world > 1 or args.split) and args.acc != "fp32":
-        raise SystemExit("--acc half runs the fused step on one GPU")
-    if args.split and args.graph:
-        raise SystemExit("--split and --graph are separate modes")
-    graph = None
-    dstate = None
-    if args.graph:
-        if world > 1 or args.acc != "fp32" or args.clip:
-            raise SystemExit("--graph runs the unclipped fp32-accumulator path on one GPU")
-        dstate = zs.DeviceState(W.scaler)
-        W.step_async_calls(ctx, dstate)      # uncaptured first call caches launch shapes
-        torch.cuda.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            W.step_async_calls(ctx, dstate)
-
-    def one_step():
-        if graph is not None:
-            graph.replay()
-            return 0
-        if world == 1 and not args.split:
-            return W.step(ctx)
-        # replicas: each rank runs its own copy of the shard step; the one
-        # real exchange is the overflow flag, all-reduced on the device before
-        # any state is written, so every rank skips together (with clipping,
-        # also the shards' sums of squares, so every rank clips alike)
-        from zero_mixed_precision_shard_gb300.dp import dp_shard_step, dp_shard_step_clipped
-        # the fused call split at the flag: the same re-read form (N < 4) or
-        # materialised form as zs_shard_step chooses, so the same kernels run
-        recompute = wl.n < 4 or W.acc is None
-        last = W.slices(wl.g - 1) if recompute else None
-        acc_in = W.acc if (wl.g > 1 or not recompute) else None
-        div = float(wl.n * wl.g * W.scaler.scale)
-
-        def reduce_last(f):
-            f.zero_()
-            for k in range(wl.g - 1):
-                zs.zs_reduce_check(ctx, W.slices(k), W.dt, E, W.acc, k == 0, f)
-            if recompute:
-                zs.zs_check_last(ctx, W.slices(wl.g - 1), W.dt, E, acc_in, f)
-            else:
-                zs.zs_reduce_check(ctx, W.slices(wl.g - 1), W.dt, E, W.acc, wl.g == 1, f)
-
-        def apply(f):
-            zs.zs_apply(ctx, f, last, W.dt, acc_in, E, div, W.master, W.m, W.v, W.half, W.hp,
-                        W.t + 1)
-
-        def sumsq(d):
-            zs.zs_grad_sumsq(ctx, last, W.dt, acc_in, E, div, d)
-
-        def apply_clipped(f, d):
-            zs.zs_apply_clipped(ctx, f, d, args.clip, last, W.dt, acc_in, E, div, W.master,
-                                W.m, W.v, W.half, W.hp, W.t + 1)
-
-        def scaler_update(f):
-            ovf = zs.zs_scaler_update(ctx, f, W.scaler)
-            if not ovf:
-                W.t += 1
-            return ovf
-
-        if args.clip:
-            return dp_shard_step_clipped(reduce_last, sumsq, apply_clipped, scaler_update, flag,
-                                         d_sumsq)
-        return dp_shard_step(reduce_last, apply, scaler_update, flag)
-
-    for _ in range(args.warmup):
-        one_step()
-    torch.cuda.synchronize()
-    plan = W.launch_plan(split=split)
-    ctx.timing_reset()
-    ctx.set_timing(True)
-    l0 = ctx.launch_count
-    with ClockSampler(dev) as clocks:
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ev0.record()
-        for _ in range(args.steps):
-            one_step()
-        ev1.record()
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
-    ctx.set_timing(False)
-    launches = ctx.launch_count - l0
-    if graph is not None:  # replays bypass the context's counter: kernels per captured step
+    one_step, state = make_step(zs, ctx, W, api, args.clip)
+    ms, launches, clock_summary = timed_steps(ctx, one_step, args.steps, args.warmup, dev, world)
+    plan = W.launch_plan(split=api == "split")
+    if api == "graph":  # replays bypass the context's counter: kernels per captured step
         launches = args.steps * (len(plan) + 1)
+    dstate = None
+    if state is not None:
+        d = state.read()
+        dstate = {"iterations": d.iterations, "step": d.step, "scale": d.scaler.scale,
+                  "overflow": d.overflow}
     if world > 1:   # every rank's launches
         n_l = torch.tensor([launches], dtype=torch.int64, device="cuda")
         dist.all_reduce(n_l)
         launches = int(n_l.item())
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
         t = torch.tensor([ms], dtype=torch.float64, device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
@@ -584,19 +870,7 @@ def run_ours(args):
     value = owned_total / (per_step_ms * 1e-3)
 
     # per-kernel times and the dominant kernel's roofline
-    kinds = {}
-    for kind_id, name in enumerate(zs.KERNEL_NAMES):
-        tot, nl, el = ctx.timing(kind_id)
-        if nl:
-            kinds[name] = {"ms": tot, "launches": nl, "elements": el}
-    alg_bytes = {}
-    for name, b in plan:
-        alg_bytes.setdefault(name, []).append(b)
-    for name, d in kinds.items():
-        per_launch = alg_bytes.get(name, [0])
-        avg_b = sum(per_launch) / len(per_launch) if per_launch else 0
-        d["alg_bytes_per_elem"] = avg_b
-        d["gbs"] = avg_b * (d["elements"] / d["launches"]) / (d["ms"] / d["launches"] * 1e-3) / 1e9
+    kinds = kernel_table(zs, ctx, plan)
     step_bytes = alg_bytes_per_elem_step(wl.n, wl.g, 2 if args.acc == "half" else 4) * E
     if not kinds:  # graph replay: no per-kernel events inside the graph
         kinds = {"step": {"ms": ms, "launches": args.steps, "elements": E * args.steps,
@@ -617,7 +891,8 @@ def run_ours(args):
     if not args.skip_e2e:
         if world > 1:
             dist.barrier()
-        e2e = run_e2e(zs, ctx, W, args.e2e_steps, step_fn=one_step if split else None)
+        e2e = run_e2e(zs, ctx, W, args.e2e_steps, api,
+                      step_fn=one_step if api == "split" else None)
         if world > 1:  # whole job: every rank's params over the slowest rank's step
             t = torch.tensor([e2e["ms_per_step"]], dtype=torch.float64, device="cuda")
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -627,6 +902,15 @@ def run_ours(args):
             e2e["d2h_bytes_per_step"] *= world
             e2e["h2d_gbs"] = round(e2e["h2d_bytes_per_step"] / (e2e["ms_per_step"] * 1e-3) / 1e9,
                                    1)
+
+    # the other target workloads, each with its own clock record (one GPU only)
+    table = None
+    if (world == 1 and not args.skip_table and args.workload == DEFAULT_WORKLOAD
+            and api == "async"):
+        del W, one_step, state
+        torch.cuda.empty_cache()
+        table = {name: measure_table_workload(zs, ctx, name, args, peak, dev)
+                 for name in TABLE_WORKLOADS}
 
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu:
@@ -648,13 +932,9 @@ def run_ours(args):
                                else "1 GPU",
                 "accumulator": args.acc,
                 "clip_max_norm": args.clip or None,
-                "api": ("CUDA graph of zs_grad_accum + zs_shard_step_async" if args.graph
-                        else "zs_reduce_check / zs_check_last + zs_apply + zs_scaler_update "
-                             "(split at the flag)" if world > 1 or args.split
-                        else "zs_grad_accum_halfacc + zs_shard_step_halfacc"
-                        if args.acc == "half"
-                        else "zs_grad_accum + zs_shard_step_clipped" if args.clip
-                        else "zs_grad_accum + zs_shard_step"),
+                "api": ("zs_grad_accum_halfacc + zs_shard_step_halfacc" if args.acc == "half"
+                        else "zs_grad_accum + zs_shard_step_clipped" if args.clip and api == "sync"
+                        else API_DESC[api]),
                 "l2": "inputs larger than L2 (129 MB): no flush needed",
                 "inputs": "gradients generated once on the device (step-1 values, no "
                           "injections) and reused by every timed step",
@@ -662,13 +942,15 @@ def run_ours(args):
                 "step_gbs": round(step_bytes / (per_step_ms * 1e-3) / 1e9, 1),
                 "step_frac_of_peak": round(step_bytes / (per_step_ms * 1e-3) / 1e9 / peak, 4),
                 "copy_probe_gbs": probe,
+                "device_state_after_timed_steps": dstate,
                 "kernels": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv)
                                 for kk, vv in d.items()} for k, d in kinds.items()},
+                "workloads": table,
             },
             "achieved_gbs": round(step_bytes / (per_step_ms * 1e-3) / 1e9, 1),
             "achieved_frac_of_peak": round(step_bytes / (per_step_ms * 1e-3) / 1e9 / peak, 4),
             "roofline": roofline,
-            "clocks": clocks.summary(),
+            "clocks": clock_summary,
             "gpu_launches": launches,
             "e2e": e2e,
             "cpu_baseline": cpu,
@@ -680,12 +962,14 @@ def run_ours(args):
     return 0
 
 
-def run_e2e(zs, ctx, W: DeviceWorkload, steps: int, step_fn=None):
+def run_e2e(zs, ctx, W: DeviceWorkload, steps: int, api: str = "sync", step_fn=None):
     """Same step, but every micro-step's N gradient slices are first copied
     from pinned host memory (the values a backward pass would hand over), and
-    the step result (overflow flag, new scale) is read back by the step's
-    synchronising call.  Copies run on a side stream, one micro-step ahead of
-    the compute.  step_fn (the step split at the flag, as each rank of a
+    each step's result is read back: on the device-resident path an
+    asynchronous copy of the step state (flag, scale, step count) into pinned
+    host memory, on the synchronising path the flag and scale the step call
+    returns.  Copies run on a side stream, one micro-step ahead of the
+    compute.  step_fn (the step split at the flag, as each rank of a
     multi-GPU run takes it) instead waits for all G copies, then runs."""
     import torch
     wl = W.wl
@@ -695,6 +979,8 @@ def run_e2e(zs, ctx, W: DeviceWorkload, steps: int, step_fn=None):
     compute = torch.cuda.current_stream()
     done = [torch.cuda.Event() for _ in range(wl.g)]
     free = [torch.cuda.Event() for _ in range(wl.g)]
+    state = zs.DeviceState(W.scaler) if api in ("async", "graph") else None
+    result = torch.empty(64, dtype=torch.uint8, pin_memory=True)
 
     def step():
         for k in range(wl.g):
@@ -714,7 +1000,11 @@ def run_e2e(zs, ctx, W: DeviceWorkload, steps: int, step_fn=None):
             W.accum(ctx, k)
             free[k].record(compute)
         compute.wait_event(done[wl.g - 1])
-        W.finish(ctx)
+        if state is not None:
+            W.finish_async(ctx, state)
+            result.copy_(state.buf, non_blocking=True)
+        else:
+            W.finish(ctx)
         free[wl.g - 1].record(compute)
 
     for e in free:
@@ -731,10 +1021,17 @@ def run_e2e(zs, ctx, W: DeviceWorkload, steps: int, step_fn=None):
     ms = a.elapsed_time(b) / steps
     valid = min(W.valid_end - W.begin, W.E)
     h2d = wl.g * wl.n * W.E * 2
-    return {"value": valid / (ms * 1e-3), "unit": "params/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": 8, "ms_per_step": ms, "steps": steps,
-            "h2d_gbs": round(h2d / (ms * 1e-3) / 1e9, 1),
-            "wall_s": round(time.perf_counter() - t0, 2)}
+    d2h = result.numel() if state is not None else 8
+    out = {"value": valid / (ms * 1e-3), "unit": "params/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps,
+           "h2d_gbs": round(h2d / (ms * 1e-3) / 1e9, 1),
+           "wall_s": round(time.perf_counter() - t0, 2)}
+    if state is not None:
+        d = zs.zs_device_state.from_buffer_copy(result.numpy().tobytes())
+        out["last_result"] = {"iterations": d.iterations, "overflow": d.overflow,
+                              "scale": d.scaler.scale}
+        assert d.iterations == steps + 1, "the step results read back are not the last step's"
+    return out
 
 
 def main(argv=None):
@@ -752,15 +1049,22 @@ def main(argv=None):
                     help="accumulator format (half: zs_*_halfacc entry points)")
     ap.add_argument("--clip", type=float, default=0.0,
                     help="global-norm gradient clipping at this max norm (zs_shard_step_clipped)")
+    ap.add_argument("--api", default="async", choices=["async", "sync"],
+                    help="async (default): zs_shard_step_async with the scale and step count on "
+                         "the device, no host round trip per step; sync: zs_shard_step, which "
+                         "returns the flag and scale to the host every step")
+    ap.add_argument("--skip-table", action="store_true",
+                    help="skip the other target workloads measured after the headline one")
     ap.add_argument("--graph", action="store_true",
                     help="replay each step from a CUDA graph (device-resident scaler)")
     ap.add_argument("--split", action="store_true",
-                    help="on one GPU, run the step split at the overflow flag as every rank of a "
-                         "multi-GPU run does (zs_reduce_check / zs_check_last, zs_apply, "
-                         "zs_scaler_update) instead of the fused zs_shard_step")
+                    help="run the step split at the overflow flag, as a caller that exchanges "
+                         "the flag between ranks does (zs_reduce_check / zs_check_last, "
+                         "zs_apply, zs_scaler_update), instead of the fused call")
     ap.add_argument("--dist-backend", default="nccl", choices=["nccl", "gloo"],
-                    help="process group of a multi-GPU run (gloo: ranks may share a GPU, for "
-                         "testing the multi-rank path on one)")
+                    help="process group of a multi-GPU (ZeRO-2) run (gloo: ranks may share a "
+                         "GPU, the exchanges staged through host memory, for testing the "
+                         "multi-rank path on one)")
     ap.add_argument("--elements", type=int, default=None,
                     help="truncate the owned shard to its first ELEMENTS elements (profiling)")
     args = ap.parse_args(argv)

@@ -23,8 +23,8 @@ def run(args):
     return json.loads(lines[0])
 
 
-@pytest.mark.parametrize("mode", [[], ["--split"], ["--graph"], ["--acc", "half"],
-                                  ["--clip", "1.0"]])
+@pytest.mark.parametrize("mode", [["--skip-table"], ["--api", "sync"], ["--split"], ["--graph"],
+                                  ["--acc", "half"], ["--clip", "1.0"]])
 def test_bench_line(mode):
     d = run(["--workload", "llama7b-n1", "--elements", str(1 << 24), "--steps", "3",
              "--warmup", "3", "--e2e-steps", "1", "--skip-cpu", "--skip-probe"] + mode)
@@ -45,3 +45,27 @@ def test_bench_line(mode):
     assert e["value"] > 0 and e["h2d_bytes_per_step"] == 8 * (1 << 24) * 2
     assert e["d2h_bytes_per_step"] > 0
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
+
+
+def test_default_api_keeps_the_step_state_on_the_device_and_measures_the_table():
+    """The default API (zs_shard_step_async, no host round trip) runs every
+    step: the device state read back after the run counts the warm-up and
+    timed steps; the e2e leg reads each step's state back; the other target
+    workloads are measured in the same run, each with its own clock record."""
+    el = 1 << 22
+    d = run(["--elements", str(el), "--steps", "4", "--warmup", "3", "--e2e-steps", "2",
+             "--skip-cpu", "--skip-probe"])
+    c = d["config"]
+    assert "zs_shard_step_async" in c["api"]
+    assert c["device_state_after_timed_steps"]["iterations"] == 3 + 4
+    assert d["e2e"]["d2h_bytes_per_step"] == 64 and d["e2e"]["last_result"]["iterations"] == 3
+    assert set(c["workloads"]) == set(bench.TABLE_WORKLOADS)
+    for name, w in c["workloads"].items():
+        wl = bench.synth.WORKLOADS[name]
+        assert w["shard_len"] == el and w["n_ranks_simulated"] == wl.n
+        for api in ("async", "sync"):
+            a = w[api]
+            assert a["value"] == pytest.approx(el / (a["ms_per_step"] * 1e-3), rel=1e-3)
+            assert a["step_frac_of_peak"] > 0 and "sm_mhz" in a["clocks"]
+            assert a["gpu_launches"] >= 4 * 2
+        assert w["async"]["device_state"]["iterations"] == 3 + 2 * 4   # two timed passes

@@ -7,10 +7,12 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
 #include <unordered_map>
+#include <utility>
 #include <vector>
 
 #include <nvtx3/nvToolsExt.h>
@@ -53,6 +55,7 @@ struct zs_ctx {
   std::string err;
   std::unordered_map<const void*, int> occupancy;  // resident CTAs per SM, per kernel
   int64_t launches = 0;
+  bool pdl = true;  // launch the step's kernels as programmatic dependents
   // timing
   bool timing = false;
   struct Rec {
@@ -154,6 +157,28 @@ struct LaunchScope {
   }
 };
 
+// Launch one of the step's kernels on `s`.  With c->pdl the launch allows
+// programmatic dependent launch: the kernel's CTAs may be scheduled while the
+// previous kernel in the stream is finishing, and each kernel waits
+// (griddepcontrol.wait, its first instruction) until its predecessor has
+// completed and its writes are visible.  This removes the launch gap between
+// the short kernels of a step.
+template <typename... KArgs, typename... Args>
+void launch_k(zs_ctx* c, void (*kernel)(KArgs...), int grid, int block, cudaStream_t s,
+              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)block);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = c->pdl ? 1 : 0;
+  (void)cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 template <typename K>
 int grid_for(zs_ctx* c, K kernel, int64_t items, int waves = ZS_GRID_WAVES) {
   const void* key = reinterpret_cast<const void*>(kernel);
@@ -230,8 +255,8 @@ void launch_reduce_k(zs_ctx* c, const zs::SlicePtrs& sp, int32_t n, float* acc, 
   const int64_t units = (count >> 3) / VPT + 8;
   auto k = zs::k_reduce<DT, RA, ST, VPT>;
   const int waves = ST ? ZS_GRID_WAVES : ZS_CHECK_WAVES;
-  k<<<grid_for(c, k, units, waves), zs::kThreads, 0, s>>>(sp, n, acc, count, flag, nullptr,
-                                                          acc_keep_for(count));
+  launch_k(c, k, grid_for(c, k, units, waves), zs::kThreads, s, sp, n, acc, count, flag,
+           (double*)nullptr, acc_keep_for(count));
 }
 
 // The last micro-step's pass with the clipping norm fused in: per-CTA sums of
@@ -244,8 +269,8 @@ zs_status launch_reduce_norm_k(zs_ctx* c, const zs::SlicePtrs& sp, int32_t n, fl
   auto k = zs::k_reduce<DT, RA, ST, VPT, false, true>;
   int grid = grid_for(c, k, (count >> 3) / VPT + 8, ZS_GRID_WAVES);
   if (grid > ZS_NORM_MAX_PARTS) grid = ZS_NORM_MAX_PARTS;
-  k<<<grid, zs::kThreads, 0, s>>>(sp, n, acc, count, flag, c->d_norm_parts,
-                                  acc_keep_for(count));
+  launch_k(c, k, grid, zs::kThreads, s, sp, n, acc, count, flag, c->d_norm_parts,
+           acc_keep_for(count));
   *nparts = grid;
   return ZS_OK;
 }
@@ -277,13 +302,13 @@ zs_status reduce_norm_any(zs_ctx* c, zs_dtype dt, const zs::SlicePtrs& sp, int32
     // most ZS_SUMSQ_MAX_PARTS chunk sums first (fixed order, deterministic)
     const int64_t chunk = (nparts + ZS_SUMSQ_MAX_PARTS - 1) / ZS_SUMSQ_MAX_PARTS;
     const int blocks = (int)((nparts + chunk - 1) / chunk);
-    zs::k_partials_reduce<<<blocks, zs::kThreads, 0, s>>>(c->d_norm_parts, nparts, chunk,
-                                                         c->d_partials);
+    launch_k(c, zs::k_partials_reduce, blocks, zs::kThreads, s,
+             (const double*)c->d_norm_parts, (int64_t)nparts, chunk, c->d_partials);
     c->launches += 1;
     parts = c->d_partials;
     nparts = blocks;
   }
-  zs::k_sumsq_finalize<<<1, zs::kThreads, 0, s>>>(parts, nparts, 1.0 / (div * div), out);
+  launch_k(c, zs::k_sumsq_finalize, 1, zs::kThreads, s, parts, nparts, 1.0 / (div * div), out);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(c, e, "reduce launch");
   ls.done();
@@ -315,8 +340,8 @@ zs_status launch_reduce(zs_ctx* c, const zs::SlicePtrs& sp, int32_t n, float* ac
     // flag only, from the raw bit patterns (exact here: see k_check_bits)
     constexpr int VPT = ZS_CHECK_VPT;
     auto k = zs::k_check_bits<DT, VPT>;
-    k<<<grid_for(c, k, (count >> 3) / VPT + 8, ZS_CHECK_WAVES), zs::kThreads, 0, s>>>(sp, n, count,
-                                                                                     flag);
+    launch_k(c, k, grid_for(c, k, (count >> 3) / VPT + 8, ZS_CHECK_WAVES), zs::kThreads, s, sp,
+             n, count, flag);
   } else if (read_acc && store) {
     launch_reduce_v<DT, true, true>(c, sp, n, acc, count, flag, s);
   } else if (store) {
@@ -367,14 +392,14 @@ void launch_apply_k(zs_ctx* c, const int32_t* flag, const zs::SlicePtrs& sp, int
   const int64_t units = (count >> 3) / VPT + 8;
   if (coef != nullptr) {
     auto k = zs::k_apply<DT, HA, RC, VPT, true>;
-    k<<<grid_for(c, k, units), zs::kThreads, 0, s>>>(flag, sp, n, acc, master, m, v, ho, count,
-                                                     ad, sc_in, result, coef, nullptr, nullptr,
-                                                     acc_keep_for(count));
+    launch_k(c, k, grid_for(c, k, units), zs::kThreads, s, flag, sp, n, acc, master, m, v, ho,
+             count, ad, sc_in, result, coef, (const zs::AdamArgs*)nullptr,
+             (zs_device_state*)nullptr, acc_keep_for(count));
   } else {
     auto k = zs::k_apply<DT, HA, RC, VPT, false>;
-    k<<<grid_for(c, k, units), zs::kThreads, 0, s>>>(flag, sp, n, acc, master, m, v, ho, count,
-                                                     ad, sc_in, result, nullptr, nullptr,
-                                                     nullptr, acc_keep_for(count));
+    launch_k(c, k, grid_for(c, k, units), zs::kThreads, s, flag, sp, n, acc, master, m, v, ho,
+             count, ad, sc_in, result, (const float*)nullptr, (const zs::AdamArgs*)nullptr,
+             (zs_device_state*)nullptr, acc_keep_for(count));
   }
 }
 
@@ -425,7 +450,7 @@ void launch_sumsq_k(zs_ctx* c, const zs::SlicePtrs& sp, int32_t n, const float* 
   int grid = grid_for(c, k, (count >> 3) + 8, 1);
   if (grid > ZS_SUMSQ_MAX_PARTS) grid = ZS_SUMSQ_MAX_PARTS;
   *nparts = grid;
-  k<<<grid, zs::kThreads, 0, s>>>(sp, n, acc, count, partials);
+  launch_k(c, k, grid, zs::kThreads, s, sp, n, acc, count, partials);
 }
 
 zs_status sumsq_any(zs_ctx* c, zs_dtype dt, const zs::SlicePtrs& sp, int32_t n, bool recompute,
@@ -444,7 +469,8 @@ zs_status sumsq_any(zs_ctx* c, zs_dtype dt, const zs::SlicePtrs& sp, int32_t n, 
     else launch_sumsq_k<ZS_BF16, true, false>(c, sp, n, acc, count, partials, &nparts, s);
   }
   const double div = (double)grad_div;
-  zs::k_sumsq_finalize<<<1, zs::kThreads, 0, s>>>(partials, nparts, 1.0 / (div * div), out);
+  launch_k(c, zs::k_sumsq_finalize, 1, zs::kThreads, s, (const double*)partials, nparts,
+           1.0 / (div * div), out);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(c, e, "sumsq launch");
   ls.done();
@@ -453,7 +479,7 @@ zs_status sumsq_any(zs_ctx* c, zs_dtype dt, const zs::SlicePtrs& sp, int32_t n, 
 }
 
 zs_status clip_coef_launch(zs_ctx* c, const double* d_sumsq, float max_norm, cudaStream_t s) {
-  zs::k_clip_coef<<<1, 32, 0, s>>>(d_sumsq, max_norm, c->d_coef);
+  launch_k(c, zs::k_clip_coef, 1, 32, s, d_sumsq, max_norm, c->d_coef);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(c, e, "clip coefficient launch");
   c->launches += 1;
@@ -482,7 +508,9 @@ zs_status finish_step(zs_ctx* c, zs_scaler* scaler, int32_t* overflow_out, float
                       int32_t* flag_to_clear, cudaStream_t s) {
   cudaError_t e = cudaSuccess;
   if (flag_to_clear) {
-    e = cudaMemsetAsync(flag_to_clear, 0, sizeof(int32_t), s);
+    launch_k(c, zs::k_clear_flag, 1, 32, s, flag_to_clear);
+    c->launches += 1;
+    e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(c, e, "flag reset");
   }
   e = cudaStreamSynchronize(s);
@@ -503,9 +531,9 @@ void launch_apply_dev_k(zs_ctx* c, const int32_t* flag, const zs::SlicePtrs& sp,
   auto k = zs::k_apply<DT, HA, RC, VPT, false, true>;
   const zs::AdamArgs unused{};
   const zs_scaler unused_sc{};
-  k<<<grid_for(c, k, units), zs::kThreads, 0, s>>>(flag, sp, n, acc, master, m, v, ho, count,
-                                                   unused, unused_sc, nullptr, nullptr, ad_dev,
-                                                   st, acc_keep_for(count));
+  launch_k(c, k, grid_for(c, k, units), zs::kThreads, s, flag, sp, n, acc, master, m, v, ho,
+           count, unused, unused_sc, (zs::StepResult*)nullptr, (const float*)nullptr, ad_dev, st,
+           acc_keep_for(count));
 }
 
 template <int DT>
@@ -528,7 +556,8 @@ void launch_reduce_hacc_k(zs_ctx* c, const zs::SlicePtrs& sp, int32_t n, float* 
   constexpr int VPT = ZS_HACC_VPT;
   const int64_t units = (count >> 3) / VPT + 8;
   auto k = zs::k_reduce<DT, RA, true, VPT, true>;
-  k<<<grid_for(c, k, units), zs::kThreads, 0, s>>>(sp, n, acc, count, flag, nullptr, 0u);
+  launch_k(c, k, grid_for(c, k, units), zs::kThreads, s, sp, n, acc, count, flag,
+           (double*)nullptr, 0u);
 }
 
 zs_status reduce_hacc(zs_ctx* c, zs_dtype dt, const zs::SlicePtrs& sp, int32_t n, void* acc,
@@ -559,14 +588,14 @@ zs_status apply_hacc(zs_ctx* c, zs_dtype dt, const int32_t* flag, const void* ac
   const int64_t units = (count >> 3) + 8;
   if (dt == ZS_FP16) {
     auto k = zs::k_apply<ZS_FP16, true, false, 1, false, false, true>;
-    k<<<grid_for(c, k, units), zs::kThreads, 0, s>>>(flag, sp, 0, a, master, m, v, ho, count, ad,
-                                                     *scaler_in, result, nullptr, nullptr,
-                                                     nullptr, 0u);
+    launch_k(c, k, grid_for(c, k, units), zs::kThreads, s, flag, sp, 0, a, master, m, v, ho,
+             count, ad, *scaler_in, result, (const float*)nullptr, (const zs::AdamArgs*)nullptr,
+             (zs_device_state*)nullptr, 0u);
   } else {
     auto k = zs::k_apply<ZS_BF16, true, false, 1, false, false, true>;
-    k<<<grid_for(c, k, units), zs::kThreads, 0, s>>>(flag, sp, 0, a, master, m, v, ho, count, ad,
-                                                     *scaler_in, result, nullptr, nullptr,
-                                                     nullptr, 0u);
+    launch_k(c, k, grid_for(c, k, units), zs::kThreads, s, flag, sp, 0, a, master, m, v, ho,
+             count, ad, *scaler_in, result, (const float*)nullptr, (const zs::AdamArgs*)nullptr,
+             (zs_device_state*)nullptr, 0u);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(c, e, "apply launch");
@@ -638,6 +667,8 @@ zs_status zs_ctx_create(zs_ctx** out) {
   if (out == nullptr) return ZS_ERR_ARG;
   *out = nullptr;
   zs_ctx* c = new zs_ctx();
+  const char* pdl = std::getenv("ZEROSHARD_PDL");
+  c->pdl = !(pdl != nullptr && pdl[0] == '0');
   cudaError_t e = cudaGetDevice(&c->device);
   if (e == cudaSuccess)
     e = cudaDeviceGetAttribute(&c->sms, cudaDevAttrMultiProcessorCount, c->device);
@@ -783,7 +814,7 @@ zs_status zs_scaler_update(zs_ctx* c, const int32_t* d_flag, zs_scaler* scaler,
   if (d_flag == nullptr) return fail(c, ZS_ERR_ARG, "d_flag is NULL");
   ZS_TRY(check_scaler(c, scaler));
   LaunchScope ls(c, stream, ZS_KERNEL_SCALER, 1);
-  zs::k_scaler<<<1, 32, 0, stream>>>(d_flag, *scaler, c->d_result);
+  launch_k(c, zs::k_scaler, 1, 32, stream, d_flag, *scaler, c->d_result);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(c, e, "scaler launch");
   ls.done();
@@ -933,8 +964,8 @@ zs_status zs_shard_step_async(zs_ctx* c, const void* const* grads, int32_t n, zs
   }
   zs_lr_schedule sc{};
   if (sched) sc = *sched;
-  zs::k_step_prologue<<<1, 32, 0, stream>>>(d_state, n, accum_steps, *hp, sc, sched ? 1 : 0,
-                                            c->d_args);
+  launch_k(c, zs::k_step_prologue, 1, 32, stream, (const zs_device_state*)d_state, n,
+           accum_steps, *hp, sc, sched ? 1 : 0, c->d_args);
   c->launches += 1;
   uint16_t* ho = static_cast<uint16_t*>(half_out);
   {
@@ -950,7 +981,9 @@ zs_status zs_shard_step_async(zs_ctx* c, const void* const* grads, int32_t n, zs
   c->timing = timing;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(c, e, "async step launch");
-  e = cudaMemsetAsync(c->d_flag, 0, sizeof(int32_t), stream);
+  launch_k(c, zs::k_clear_flag, 1, 32, stream, c->d_flag);
+  c->launches += 1;
+  e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(c, e, "flag reset");
   return ZS_OK;
 }

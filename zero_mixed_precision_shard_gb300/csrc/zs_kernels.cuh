@@ -101,6 +101,29 @@ namespace zs {
 
 constexpr int kThreads = ZS_THREADS;
 
+// Programmatic dependent launch (sm_90 and later).  The host launches the
+// step's kernels with programmatic stream serialization, so a kernel's CTAs
+// may be scheduled while its predecessor in the stream is still finishing:
+// every kernel first lets its own successor start launching, then waits until
+// its predecessor has completed and its writes are visible, before it touches
+// memory.  Launched without that attribute, both instructions are no-ops.
+//
+// The kernel passes every pointer it will dereference.  Each one is handed to
+// an empty asm statement after the wait: a __restrict__ pointer that no asm
+// can see lets the compiler assume the wait leaves its memory unchanged and
+// move a load through it (e.g. of the step's flag) above the wait, where it
+// would read what the previous kernel has not written yet.
+__device__ __forceinline__ void pdl_escape(const void* p) {
+  asm volatile("" ::"l"(p) : "memory");
+}
+
+template <typename... P>
+__device__ __forceinline__ void pdl_enter(const P*... ptrs) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  (pdl_escape(ptrs), ...);
+}
+
 struct SlicePtrs {
   const uint4* p[ZS_MAX_RANKS];
 };
@@ -427,6 +450,7 @@ __device__ __forceinline__ float lr_at(const zs_lr_schedule& sc, int64_t t) {
 __global__ void k_step_prologue(const zs_device_state* __restrict__ st, int n, int accum_steps,
                                 zs_adam_hparams hp, zs_lr_schedule sched, int has_sched,
                                 AdamArgs* __restrict__ out) {
+  pdl_enter(st, out);
   if (blockIdx.x != 0 || threadIdx.x != 0) return;
   const int64_t t = st->step + 1;
   AdamArgs a;
@@ -515,6 +539,7 @@ __global__ void __launch_bounds__(ZS_THREADS, NORM && !STORE ? ZS_NORM_MIN_BLOCK
                                                                               : ZS_MIN_BLOCKS)
     k_reduce(const __grid_constant__ SlicePtrs s, int n, float* __restrict__ acc, int64_t count,
              int32_t* __restrict__ flag, double* __restrict__ partials, uint32_t acc_keep) {
+  pdl_enter(&s, acc, flag, partials);
   const uint64_t pol = acc_policy(acc_keep);
   // HACC: acc holds count halves of the gradient's format; each sum is rounded
   // to it, and the flag tests the rounded value.
@@ -655,6 +680,7 @@ __global__ void __launch_bounds__(ZS_THREADS, NORM && !STORE ? ZS_NORM_MIN_BLOCK
 template <int DT, int VPT>
 __global__ void ZS_BOUNDS k_check_bits(const __grid_constant__ SlicePtrs s, int n, int64_t count,
                                        int32_t* __restrict__ flag) {
+  pdl_enter(&s, flag);
   constexpr uint32_t lo = DT == ZS_FP16 ? 0x7C00u : 0x7F80u;
   constexpr uint32_t hi = lo << 16;
   const int64_t nvec = count >> 3;
@@ -700,6 +726,7 @@ __global__ void __launch_bounds__(ZS_THREADS, ZS_APPLY_MIN_BLOCKS)
             AdamArgs ad_host, zs_scaler scaler_in, StepResult* __restrict__ result,
             const float* __restrict__ clip_coef, const AdamArgs* __restrict__ ad_dev,
             zs_device_state* __restrict__ dstate, uint32_t acc_keep) {
+  pdl_enter(flag, &s, acc, master, mom, var, half_out, result, clip_coef, ad_dev, dstate);
   const int32_t overflow = *flag;
   const uint64_t pol = acc_policy(acc_keep);
   AdamArgs ad = ad_host;
@@ -792,6 +819,7 @@ template <int DT, bool HAS_ACC, bool RECOMPUTE>
 __global__ void ZS_BOUNDS k_sumsq(const __grid_constant__ SlicePtrs s, int n,
                                   const float* __restrict__ acc, int64_t count,
                                   double* __restrict__ partials) {
+  pdl_enter(&s, acc, partials);
   const int64_t nvec = count >> 3;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
@@ -841,6 +869,7 @@ __global__ void ZS_BOUNDS k_sumsq(const __grid_constant__ SlicePtrs s, int n,
 // contiguous chunk [b*chunk, min((b+1)*chunk, nparts)) into out[b].
 __global__ void k_partials_reduce(const double* __restrict__ partials, int64_t nparts,
                                   int64_t chunk, double* __restrict__ out) {
+  pdl_enter(partials, out);
   const int64_t b0 = (int64_t)blockIdx.x * chunk;
   int64_t b1 = b0 + chunk;
   if (b1 > nparts) b1 = nparts;
@@ -853,6 +882,7 @@ __global__ void k_partials_reduce(const double* __restrict__ partials, int64_t n
 // One CTA: out = (sum of partials, fixed order) / grad_div^2.
 __global__ void k_sumsq_finalize(const double* __restrict__ partials, int nparts, double inv_div2,
                                  double* __restrict__ out) {
+  pdl_enter(partials, out);
   double t = 0.0;
   for (int i = threadIdx.x; i < nparts; i += kThreads) t += partials[i];
   t = block_sum(t);
@@ -862,6 +892,7 @@ __global__ void k_sumsq_finalize(const double* __restrict__ partials, int nparts
 // coef = max_norm / (sqrt(sumsq) + 1e-6) if that is below 1, else 1.
 __global__ void k_clip_coef(const double* __restrict__ sumsq, float max_norm,
                             float* __restrict__ coef) {
+  pdl_enter(sumsq, coef);
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     double c = 1.0;
     if (max_norm > 0.0f) {
@@ -874,7 +905,15 @@ __global__ void k_clip_coef(const double* __restrict__ sumsq, float max_norm,
 
 __global__ void k_scaler(const int32_t* __restrict__ flag, zs_scaler scaler_in,
                          StepResult* __restrict__ result) {
+  pdl_enter(flag, result);
   if (blockIdx.x == 0 && threadIdx.x == 0) scaler_step(scaler_in, *flag, result);
+}
+
+// The step's flag back to 0 once the update has read it (a kernel rather than
+// a memset, so that the stream's chain of dependent launches continues).
+__global__ void k_clear_flag(int32_t* __restrict__ flag) {
+  pdl_enter(flag);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *flag = 0;
 }
 
 // HBM probe: dst = src, 4 independent 16-byte loads per thread per trip.

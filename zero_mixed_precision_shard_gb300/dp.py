@@ -142,9 +142,11 @@ class Exchange:
             raise ValueError("exchanged buffers must be contiguous")
         return t.view(torch.uint8) if t.dtype != torch.uint8 else t
 
-    def all_to_all(self, out, inp, out_splits, in_splits):
+    def all_to_all(self, out, inp, out_splits, in_splits, async_op: bool = False):
         """out: `sum(out_splits)` elements received in rank order; inp: `sum(in_splits)`
-        elements, in_splits[q] of them for rank q (16-bit elements)."""
+        elements, in_splits[q] of them for rank q (16-bit elements).  With
+        async_op (device buffers, not staged) returns the collective's work
+        handle: its wait() orders the current stream after the transfer."""
         if self.world == 1:
             out.copy_(inp)
             return None
@@ -153,7 +155,8 @@ class Exchange:
         osz = [x * item for x in out_splits]
         isz = [x * item for x in in_splits]
         if not self.staged or not out.is_cuda:
-            return self.dist.all_to_all_single(ob, ib, osz, isz, group=self.group)
+            return self.dist.all_to_all_single(ob, ib, osz, isz, group=self.group,
+                                               async_op=async_op)
         ho = ob.cpu()
         self.dist.all_to_all_single(ho, ib.cpu(), osz, isz, group=self.group)
         ob.copy_(ho)
@@ -205,9 +208,15 @@ class Zero2Step:
         self.E = shard_len
         self.plan = bucket_plan(psi_pad, shard_len, self.world, rank, bucket_elems)
         self.longest = max(b.length for b in self.plan)
-        if recv.numel() < self.world * self.longest:
+        slot = self.world * self.longest
+        if recv.numel() < slot:
             raise ValueError("recv must hold world * (longest bucket part) elements")
-        self.recv = recv            # 16-bit buffer, reused by every bucket (stream order)
+        # 16-bit receive slots, reused bucket after bucket in stream order; with
+        # room for two (and device collectives), the exchange of the next
+        # bucket overlaps the sum of this one (§2.2 overlap_comm)
+        self.overlap = (recv.numel() >= 2 * slot and self.world > 1 and not self.x.staged
+                        and recv.is_cuda)
+        self.slots = [recv[:slot], recv[slot:2 * slot]] if self.overlap else [recv[:slot]]
         self.flag = flag
         self.d_sumsq = d_sumsq
 
@@ -222,13 +231,32 @@ class Zero2Step:
     def micro_step(self, grad_flat, first: bool):
         """Exchange one micro-step's flat gradient bucket by bucket and sum the
         received slices of this rank's shard onto the accumulator."""
-        for b in self.plan:
-            rows = self.recv[:self.world * b.length].view(self.world, b.length)
-            self.x.all_to_all(rows.view(-1), grad_flat[b.x0:b.x1], [b.length] * self.world,
-                              list(b.send))
+        pending = None
+
+        def consume(p):
+            work, b, rows = p
+            if work is not None:
+                work.wait()
             if b.length:
                 self.ops.accumulate([rows[r] for r in range(self.world)], b.offset, b.length,
                                     first, self.flag)
+
+        for i, b in enumerate(self.plan):
+            buf = self.slots[i % len(self.slots)]
+            rows = buf[:self.world * b.length].view(self.world, b.length)
+            # a slot is rewritten only after the sum that read it was queued: the
+            # collective waits for the current stream's work before it starts
+            work = self.x.all_to_all(rows.view(-1), grad_flat[b.x0:b.x1],
+                                     [b.length] * self.world, list(b.send),
+                                     async_op=self.overlap)
+            if pending is not None:
+                consume(pending)
+            pending = (work, b, rows)
+            if not self.overlap:
+                consume(pending)
+                pending = None
+        if pending is not None:
+            consume(pending)
 
     def finish(self, half_full, clip: bool = False) -> int:
         """The step's boundary: agree on the flag, update, rescale, rebuild the
