@@ -168,3 +168,25 @@ def test_bucket_plan_covers_every_shard_once(psi_pad, world, bucket):
         assert all(b.offset % 64 == 0 and b.length % 64 == 0 for b in plan)
     with pytest.raises(ValueError):
         bucket_plan(psi_pad, E, world, 0, 63)
+
+
+def test_zero2_single_rank_without_a_process_group():
+    """One rank and no process group: the exchanges are copies, and the step is
+    the oracle's single-shard step."""
+    assert not dist.is_initialized()
+    psi_pad, E = oracle.partition(PSI, 1)
+    m0 = master_init(psi_pad)
+    ops = OracleOps(m0.copy(), 1, 0.0)
+    half_full = torch.zeros(psi_pad, dtype=torch.int16)
+    z = Zero2Step(ops, psi_pad, E, 0, 1024, torch.zeros(1024, dtype=torch.int16),
+                  torch.zeros(1, dtype=torch.int32))
+    st = oracle.ShardState.from_master(m0, 0)
+    sc = oracle.make_scaler(1024.0, window=2)
+    t = 0
+    for s in range(1, 4):
+        g = full_grads(1, s, ops.sc.scale, psi_pad)[0]
+        f = z.step([torch.from_numpy(x.view(np.int16)) for x in g], half_full)
+        f_o, t, _ = oracle.shard_step([[x] for x in g], 0, st, oracle.make_hparams(*HP), t, sc)
+        assert f == f_o
+    assert ops.st.master.tobytes() == st.master.tobytes()
+    assert half_full.numpy().view(np.uint16).tobytes() == st.half.tobytes()
