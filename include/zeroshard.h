@@ -29,6 +29,14 @@
  * (round to nearest even) that an all-gather would consume.  On overflow the
  * step leaves all state untouched and the loss scale is lowered.
  *
+ * With real ranks (one process per GPU), a rank that receives the other ranks'
+ * slices of its shard (e.g. an all-to-all of each gradient bucket's shard
+ * parts) passes the received slices as the n pointers of zs_reduce_check, so
+ * the same rank-ordered fp32 sum runs; the flag (and the clipping norm) is
+ * all-reduced between the reduce and zs_apply, and the half shards are
+ * all-gathered afterwards.  The Python package's dp module does this with
+ * torch.distributed.
+ *
  * Conventions for every call:
  *  - Ownership: every array is caller-owned DEVICE memory on the context's
  *    device; `grads` is a HOST array of n device pointers, read during the

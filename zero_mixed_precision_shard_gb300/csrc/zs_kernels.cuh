@@ -473,6 +473,36 @@ __global__ void k_step_prologue(const zs_device_state* __restrict__ st, int n, i
 
 // ---------------------------------------------------------------- kernels
 
+// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) into L2.
+__device__ __forceinline__ void l2_prefetch(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// With a grid of one thread per vector unit, CTA b reads units
+// [b*kThreads, (b+1)*kThreads).  Warp 0 asks L2 for the units of CTA
+// b + ahead: one bulk prefetch per rank slice and one per array in `extra`
+// (each `extra_bytes` bytes per unit), so the loads of CTAs launched later
+// find their lines in L2.  Addresses past the arrays are not touched.
+template <int NEXTRA>
+__device__ __forceinline__ void prefetch_ahead(int ahead, const SlicePtrs& s, int n, int64_t nvec,
+                                               const void* const (&extra)[NEXTRA],
+                                               const uint32_t (&extra_bytes)[NEXTRA]) {
+  if (ahead <= 0 || threadIdx.x >= 32) return;
+  const int64_t u0 = ((int64_t)blockIdx.x + ahead) * kThreads;
+  if (u0 >= nvec) return;
+  const int64_t units = nvec - u0 < kThreads ? nvec - u0 : kThreads;
+  for (int r = threadIdx.x; r < n + NEXTRA; r += 32) {
+    if (r < n) {
+      l2_prefetch(s.p[r] + u0, (uint32_t)(units * 16));
+    } else {
+      const int e = r - n;
+      if (extra[e] != nullptr)
+        l2_prefetch(static_cast<const char*>(extra[e]) + u0 * extra_bytes[e],
+                    (uint32_t)(units * extra_bytes[e]));
+    }
+  }
+}
+
 // Square of one final gradient sum, accumulated in fp64.  Squares are formed
 // in fp32 unless they would overflow it (|a| > 1e18).
 __device__ __forceinline__ double sq8(const float a[8]) {
@@ -538,7 +568,8 @@ __global__ void __launch_bounds__(ZS_THREADS, NORM && !STORE ? ZS_NORM_MIN_BLOCK
                                              : VPT == 1 && !NORM && !READ_ACC ? ZS_FIRST_MIN_BLOCKS
                                                                               : ZS_MIN_BLOCKS)
     k_reduce(const __grid_constant__ SlicePtrs s, int n, float* __restrict__ acc, int64_t count,
-             int32_t* __restrict__ flag, double* __restrict__ partials, uint32_t acc_keep) {
+             int32_t* __restrict__ flag, double* __restrict__ partials, uint32_t acc_keep,
+             int prefetch_ctas) {
   pdl_enter(&s, acc, flag, partials);
   const uint64_t pol = acc_policy(acc_keep);
   // HACC: acc holds count halves of the gradient's format; each sum is rounded
@@ -555,6 +586,14 @@ __global__ void __launch_bounds__(ZS_THREADS, NORM && !STORE ? ZS_NORM_MIN_BLOCK
   const int64_t nvec = count >> 3;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+  if constexpr (HACC && VPT == 1) {
+    // prefetch_ctas > 0 (the half-accumulator pass over one or two ranks,
+    // which moves only 16-32 bytes of loads per thread and is latency-bound
+    // without it): L2 prefetch of the data of the CTA that many places ahead
+    const void* const ex[1] = {READ_ACC ? static_cast<const void*>(acc) : nullptr};
+    const uint32_t exb[1] = {16u};
+    prefetch_ahead<1>(prefetch_ctas, s, n, nvec, ex, exb);
+  }
   bool bad = false;
   for (int64_t base = tid; base < nvec; base += stride * VPT) {
     int64_t vi[VPT];
