@@ -775,8 +775,8 @@ def run_e2e_zero2(Z: Zero2Workload, steps: int):
     from pinned host memory first, and the step's result (the overflow flag
     the loss-scale update returns) read by the host."""
     import torch
-    host = torch.empty_like(Z.grads[0], device="cpu").pin_memory()
-    host.copy_(Z.grads[0])
+    host = torch.empty(Z.grads.shape[1], dtype=Z.grads.dtype, pin_memory=True)
+    host.copy_(Z.grads[0])   # device -> pinned host directly (no pageable copy)
     copy_stream = torch.cuda.Stream()
     compute = torch.cuda.current_stream()
 

@@ -1,8 +1,9 @@
 """Full-size workloads, in the launch configuration the benchmark times
-(bench.DeviceWorkload: zs_grad_accum for micro-steps 1..G-1, zs_shard_step
-for the last), checked against the oracle on sampled elements, for the first
-shard and the last (which holds the padding where there is any, and the
-output layers).
+(bench.DeviceWorkload: zs_grad_accum for micro-steps 1..G-1, then the last
+call: zs_shard_step, or zs_shard_step_async with the device-resident state as
+the benchmark's default API does), checked against the oracle on sampled
+elements, for the first shard and the last (which holds the padding where
+there is any, and the output layers).
 
 The step is elementwise once the step's overflow flag is known, so the oracle
 replays every step on a sample of the owned shard: 2^16 seeded positions, the
@@ -48,20 +49,30 @@ def sample_positions(wl, begin, E, valid):
     return np.unique(np.concatenate(pos).astype(np.int64))
 
 
-@pytest.mark.parametrize("name,shard", [("gpt2-small-n8", 0), ("decoder-1.3b-n16", 0),
-                                        ("llama7b-zero3-n64", 0), ("llama7b-n1", 0),
-                                        # last shards: the padding (GPT-2: 256 elements) and
-                                        # the output layers
-                                        ("gpt2-small-n8", 7), ("decoder-1.3b-n16", 15),
-                                        ("llama7b-zero3-n64", 63)])
-def test_fullsize_sampled(name, shard):
+@pytest.mark.parametrize("name,shard,api", [("gpt2-small-n8", 0, "sync"),
+                                            ("decoder-1.3b-n16", 0, "sync"),
+                                            ("llama7b-zero3-n64", 0, "sync"),
+                                            ("llama7b-n1", 0, "sync"),
+                                            # last shards: the padding (GPT-2: 256 elements)
+                                            # and the output layers
+                                            ("gpt2-small-n8", 7, "sync"),
+                                            ("decoder-1.3b-n16", 15, "sync"),
+                                            ("llama7b-zero3-n64", 63, "sync"),
+                                            # the benchmark's default API
+                                            ("decoder-1.3b-n16", 0, "async"),
+                                            ("llama7b-zero3-n64", 63, "async"),
+                                            ("llama7b-n1", 0, "async")])
+def test_fullsize_sampled(name, shard, api):
     import bench
     import zero_mixed_precision_shard_gb300 as zs
     torch.cuda.set_device(0)
     wl = synth.WORKLOADS[name]
     steps = min(wl.steps, int(os.environ.get("ZS_FULLSIZE_STEPS", wl.steps)))
+    if api == "async" and name == "llama7b-n1":
+        steps = min(steps, 10)   # to the state check after step 10; the sync case runs all 200
     ctx = zs.Ctx()
     W = bench.DeviceWorkload(wl, shard=shard)
+    state = zs.DeviceState(W.scaler) if api == "async" else None
     E, begin = W.E, W.begin
     valid = W.valid_end - W.begin
     pos = sample_positions(wl, begin, E, valid)
@@ -93,9 +104,18 @@ def test_fullsize_sampled(name, shard):
         scheduled = any(begin <= j.index < begin + E for j in wl.injections_at(s))
         ovf_o, t_o, _ = oracle.shard_step(grads, wl.dtype_code, st, hp_o, t_o, sc_o,
                                           extra_overflow=int(scheduled))
-        ovf = W.step(ctx)
+        if state is None:
+            ovf = W.step(ctx)
+            scale = W.scaler.scale
+        else:
+            W.step_async_calls(ctx, state)
+            d = state.read()
+            ovf, scale = d.overflow, d.scaler.scale
+            assert d.step == t_o and d.iterations == s, f"step {s}"
+            if not ovf:
+                W.t += 1
         assert ovf == ovf_o, f"step {s}"
-        assert W.scaler.scale == sc_o.scale, f"step {s}"
+        assert scale == sc_o.scale, f"step {s}"
         flags.append(ovf)
         if s == min(10, steps):
             print(f"{name} shard {shard}: state after step {s}: worst error / tolerance = "
