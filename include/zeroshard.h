@@ -372,6 +372,24 @@ zs_status zs_shard_step_async(zs_ctx* ctx, const void* const* grads, int32_t n, 
                               const zs_lr_schedule* sched, zs_device_state* d_state,
                               cudaStream_t stream);
 
+/* zs_shard_step_async with global-norm clipping (§4.1 gradient_clipping; §5.1:
+ * engine.step() includes gradient clipping), as zs_shard_step_clipped computes
+ * it: norm = L2 norm of the averaged, unscaled gradient of the owned shard,
+ * coef = max_norm / (norm + 1e-6) when below 1.  The sum of squares is formed
+ * inside the last micro-step's pass, unscaled, and divided by N * G * S on the
+ * device (the scale lives in *d_state).  d_grad_norm (device fp64, 8-byte
+ * aligned, may be NULL) receives the step's norm; on a step that overflows it
+ * is not finite and the step is skipped as in zs_shard_step_async.
+ * max_norm <= 0 disables clipping (the call is then zs_shard_step_async).
+ * Capturable in a CUDA graph like zs_shard_step_async. */
+zs_status zs_shard_step_async_clipped(zs_ctx* ctx, const void* const* grads, int32_t n,
+                                      zs_dtype dt, int64_t count, float* acc,
+                                      int32_t accum_steps, float* master, float* m, float* v,
+                                      void* half_out, const zs_adam_hparams* hp,
+                                      const zs_lr_schedule* sched, float max_norm,
+                                      zs_device_state* d_state, double* d_grad_norm,
+                                      cudaStream_t stream);
+
 /* ---------------------------------------------------------------- engine */
 
 /* The training-loop interface of §5.1 (model_engine.backward(loss) then

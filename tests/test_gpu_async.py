@@ -38,7 +38,7 @@ def close(got, want, name):
 SCHED = (oracle.LR_WARMUP_DECAY, float(np.float32(1e-5)), float(np.float32(STRESS_LR)), 3, 9)
 
 
-def _run(zs, ctx, dtype, n, G, count, steps, graph, inject):
+def _run(zs, ctx, dtype, n, G, count, steps, graph, inject, max_norm=0.0):
     rng = np.random.default_rng(n * 10 + G + (100 if graph else 0))
     master0 = (rng.standard_normal(count) * 0.02).astype(np.float32)
     st = oracle.ShardState.from_master(master0, dtype)
@@ -56,11 +56,17 @@ def _run(zs, ctx, dtype, n, G, count, steps, graph, inject):
     gbuf = torch.zeros((G, n, pad), dtype=torch.int16, device="cuda")
     ptrs = [zs.pointer_array(gbuf[k, r, :count] for r in range(n)) for k in range(G)]
 
+    norm = torch.zeros(1, dtype=torch.float64, device="cuda")
+
     def step_calls():
         for k in range(G - 1):
             zs.zs_grad_accum(ctx, ptrs[k], dtype, count, acc, k == 0)
-        zs.zs_shard_step_async(ctx, ptrs[G - 1], dtype, count, acc, G, master, m, v, half, hp,
-                               sched, state)
+        if max_norm > 0:
+            zs.zs_shard_step_async_clipped(ctx, ptrs[G - 1], dtype, count, acc, G, master, m, v,
+                                           half, hp, sched, max_norm, state, norm)
+        else:
+            zs.zs_shard_step_async(ctx, ptrs[G - 1], dtype, count, acc, G, master, m, v, half,
+                                   hp, sched, state)
 
     g = None
     t_o = 0
@@ -73,7 +79,8 @@ def _run(zs, ctx, dtype, n, G, count, steps, graph, inject):
         gbuf[:, :, :count].copy_(torch.from_numpy(host))
         lr_t = oracle.lr_at(kind, mn, mx, wu, tot, t_o + 1)
         hp_o = oracle.make_hparams(lr_t, 0.9, 0.999, 1e-8, 0.01)
-        ovf_o, t_o, _ = oracle.shard_step(grads, dtype, st, hp_o, t_o, sc_o)
+        ovf_o, t_o, _, norm_o = oracle.shard_step(grads, dtype, st, hp_o, t_o, sc_o,
+                                                  max_norm=max_norm, return_norm=True)
         if graph:
             if g is None:
                 step_calls()               # uncaptured first call: caches launch shapes
@@ -92,6 +99,8 @@ def _run(zs, ctx, dtype, n, G, count, steps, graph, inject):
         assert d.step == t_o and d.iterations == s
         if not ovf_o:
             assert d.lr == np.float32(lr_t)
+            if max_norm > 0:
+                assert abs(norm.item() - norm_o) <= 1e-6 * norm_o, (s, norm.item(), norm_o)
     close(master.cpu().numpy(), st.master, "master")
     close(m.cpu().numpy(), st.m, "m")
     close(v.cpu().numpy(), st.v, "v")
@@ -107,3 +116,19 @@ def test_async_steps_match_oracle(zs, ctx, dtype, n, G, count):
 @pytest.mark.parametrize("n,G,count", [(1, 3, 20_011), (8, 2, 40_003)])
 def test_graph_replayed_steps_match_oracle(zs, ctx, n, G, count):
     _run(zs, ctx, FP16, n, G, count, 10, graph=True, inject={6})
+
+
+@pytest.mark.parametrize("dtype", [FP16, BF16])
+@pytest.mark.parametrize("n,G,count,max_norm", [(1, 3, 20_011, 0.02), (8, 2, 40_003, 0.05),
+                                                (2, 1, 8_192, 1e6)])
+def test_async_clipped_steps_match_oracle(zs, ctx, dtype, n, G, count, max_norm):
+    """The device-resident step with global-norm clipping: the norm formed in
+    the last micro-step's pass and divided by N*G*S on the device, the clipped
+    update, against the oracle's clipped steps (re-read and materialised forms;
+    a max_norm that never clips)."""
+    _run(zs, ctx, dtype, n, G, count, 10, graph=False, inject={4}, max_norm=max_norm)
+
+
+@pytest.mark.parametrize("n,G,count", [(1, 3, 20_011), (8, 2, 40_003)])
+def test_graph_replayed_clipped_steps_match_oracle(zs, ctx, n, G, count):
+    _run(zs, ctx, FP16, n, G, count, 10, graph=True, inject={6}, max_norm=0.03)

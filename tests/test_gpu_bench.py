@@ -24,7 +24,8 @@ def run(args):
 
 
 @pytest.mark.parametrize("mode", [["--skip-table"], ["--api", "sync"], ["--split"], ["--graph"],
-                                  ["--acc", "half"], ["--clip", "1.0"]])
+                                  ["--acc", "half"], ["--clip", "1.0", "--skip-table"],
+                                  ["--clip", "1.0", "--api", "sync"], ["--clip", "1.0", "--graph"]])
 def test_bench_line(mode):
     d = run(["--workload", "llama7b-n1", "--elements", str(1 << 24), "--steps", "3",
              "--warmup", "3", "--e2e-steps", "1", "--skip-cpu", "--skip-probe"] + mode)
@@ -33,7 +34,7 @@ def test_bench_line(mode):
               "roofline", "clocks", "gpu_launches", "e2e"):
         assert k in d, k
     assert d["metric"] == bench.METRIC and d["unit"] == "params/s" and d["n_gpus"] == 1
-    assert d["steps"] == 3 and d["warmup"] == 3 and d["scaling"] == "weak"
+    assert d["steps"] == 3 and d["warmup"] == 3 and d["scaling"] == "strong"
     assert d["value"] == pytest.approx((1 << 24) / (d["ms_per_step"] * 1e-3), rel=1e-6)
     assert d["config"]["workload"].startswith("llama7b-n1")
     r = d["roofline"]

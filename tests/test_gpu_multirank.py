@@ -106,6 +106,90 @@ def oracle_union(world, max_norm):
     return flags, states, sc.scale, t
 
 
+def nccl_one_rank_worker(rank, port, outdir, max_norm, bucket):
+    """zero2_worker's step over a one-rank NCCL group: every exchange is a real
+    NCCL call on device buffers (the all-to-alls posted asynchronously into two
+    receive slots, each waited on by the stream before its sum)."""
+    import torch
+    import torch.distributed as dist
+
+    import oracle
+    import zero_mixed_precision_shard_gb300 as zs
+    from zero_mixed_precision_shard_gb300.dp import Zero2Step, ZsShardOps
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    dist.init_process_group("nccl", rank=0, world_size=1, device_id=dev)
+    part = zs.zs_init_partition(PSI, 1)
+    psi_pad, E = part.psi_pad, part.shard_len
+    m0 = np.zeros(psi_pad, np.float32)
+    m0[:PSI] = np.random.default_rng(7).standard_normal(PSI) * 0.02
+    ctx = zs.Ctx()
+    master = torch.from_numpy(m0.copy()).to(dev)
+    m, v = torch.zeros_like(master), torch.zeros_like(master)
+    acc = torch.zeros_like(master)
+    half_shard = torch.zeros(E, dtype=torch.int16, device=dev)
+    half_full = torch.zeros(psi_pad, dtype=torch.int16, device=dev)
+    sc = zs.zs_scaler_init(1024.0, 1.0, 2, 1, True)
+    ops = ZsShardOps(zs, ctx, zs.ZS_FP16, E, 1, G, acc, master, m, v, half_shard,
+                     zs.make_hparams(*HP), sc, max_norm)
+    recv = torch.zeros(2 * min(E, bucket), dtype=torch.int16, device=dev)
+    z = Zero2Step(ops, psi_pad, E, 0, bucket, recv,
+                  torch.zeros(1, dtype=torch.int32, device=dev),
+                  torch.zeros(1, dtype=torch.float64, device=dev))
+    assert z.overlap and z.x.active and not z.x.staged
+    flags = []
+    for s in range(1, STEPS + 1):
+        g = full_grads(1, s, sc.scale, psi_pad)[0]
+        if s in INJECT:
+            g[INJECT[s][0]][INJECT[s][2]] = 0x7C00     # one rank: the inf is its own
+        dg = [torch.from_numpy(x.view(np.int16)).to(dev) for x in g]
+        flags.append(z.step(dg, half_full, clip=max_norm > 0))
+    torch.cuda.synchronize()
+    np.savez(os.path.join(outdir, "rank0.npz"), master=master.cpu().numpy(),
+             m=m.cpu().numpy(), v=v.cpu().numpy(),
+             half=half_shard.cpu().numpy().view(np.uint16),
+             half_full=half_full.cpu().numpy().view(np.uint16), flags=np.array(flags),
+             scale=sc.scale, t=ops.t)
+    ctx.close()
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("max_norm,bucket", [(0.0, 50_048), (0.01, 1 << 22)])
+def test_zero2_step_over_a_one_rank_nccl_group(tmp_path, max_norm, bucket):
+    """The NCCL form of the exchanges (device all-to-all with two slots and
+    asynchronous posts, device all-reduce and all-gather), on the one GPU as a
+    one-rank group, against the oracle's step of the single shard."""
+    import torch.multiprocessing as mp
+
+    import oracle
+    from _helpers import assert_close, half_ulps
+    mp.spawn(nccl_one_rank_worker, args=(free_port(), str(tmp_path), max_norm, bucket),
+             nprocs=1, join=True)
+    psi_pad, E = oracle.partition(PSI, 1)
+    m0 = np.zeros(psi_pad, np.float32)
+    m0[:PSI] = np.random.default_rng(7).standard_normal(PSI) * 0.02
+    st = oracle.ShardState.from_master(m0, 0)
+    sc = oracle.make_scaler(1024.0, window=2)
+    hp = oracle.make_hparams(*HP)
+    t, flags = 0, []
+    for s in range(1, STEPS + 1):
+        g = full_grads(1, s, sc.scale, psi_pad)[0]
+        if s in INJECT:
+            g[INJECT[s][0]][INJECT[s][2]] = 0x7C00
+        f, t, _ = oracle.shard_step([[x] for x in g], 0, st, hp, t, sc, max_norm=max_norm)
+        flags.append(f)
+    assert flags == [0, 0, 1, 0, 0, 0]
+    d = np.load(tmp_path / "rank0.npz")
+    assert d["flags"].tolist() == flags
+    assert float(d["scale"]) == sc.scale and int(d["t"]) == t
+    for k in ("master", "m", "v"):
+        assert_close(d[k], getattr(st, k), k)
+    assert half_ulps(d["half"], st.half).max() <= 1
+    assert d["half_full"].tobytes() == d["half"].tobytes()    # the one-rank all-gather
+
+
 @pytest.mark.parametrize("max_norm,bucket", [(0.0, 1 << 22), (0.01, 30_016)])
 def test_two_cuda_ranks_zero2_step_equals_the_oracle_union(tmp_path, max_norm, bucket):
     import torch.multiprocessing as mp

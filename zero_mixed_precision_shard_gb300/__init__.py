@@ -117,6 +117,9 @@ def _load():
         "zs_shard_step_async": [vp, pp, i32, i32, i64, vp, i32, vp, vp, vp, vp,
                                 ctypes.POINTER(zs_adam_hparams), ctypes.POINTER(zs_lr_schedule),
                                 vp, vp],
+        "zs_shard_step_async_clipped": [vp, pp, i32, i32, i64, vp, i32, vp, vp, vp, vp,
+                                        ctypes.POINTER(zs_adam_hparams),
+                                        ctypes.POINTER(zs_lr_schedule), f32, vp, vp, vp],
         "zs_grad_sumsq": [vp, pp, i32, i32, vp, i64, f32, vp, vp],
         "zs_grad_sumsq_noalloc": [pp, i32, i32, vp, i64, f32, vp, vp],
         "zs_apply_clipped": [vp, vp, vp, f32, pp, i32, i32, vp, i64, f32, vp, vp, vp, vp,
@@ -406,6 +409,16 @@ def zs_shard_step_async(ctx: Ctx, grads, dt, count: int, acc, accum_steps: int, 
                                       _addr(half_out), ctypes.byref(hp),
                                       ctypes.byref(sched) if sched is not None else None,
                                       _addr(d_state), _stream(stream)))
+
+
+def zs_shard_step_async_clipped(ctx: Ctx, grads, dt, count: int, acc, accum_steps: int, master,
+                                m, v, half_out, hp: zs_adam_hparams, sched, max_norm: float,
+                                d_state, d_grad_norm=None, stream=None):
+    ctx.check(lib.zs_shard_step_async_clipped(
+        ctx.handle, _ptrs(grads), len(grads), _dtype(dt), count, _addr(acc), accum_steps,
+        _addr(master), _addr(m), _addr(v), _addr(half_out), ctypes.byref(hp),
+        ctypes.byref(sched) if sched is not None else None, max_norm, _addr(d_state),
+        _addr(d_grad_norm), _stream(stream)))
 
 
 def zs_grad_accum_halfacc(ctx: Ctx, grads, dt, count: int, acc_half, first: bool, stream=None):

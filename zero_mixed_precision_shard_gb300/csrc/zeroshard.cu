@@ -525,32 +525,49 @@ zs_status finish_step(zs_ctx* c, zs_scaler* scaler, int32_t* overflow_out, float
   return ZS_OK;
 }
 
-template <int DT, bool HA, bool RC>
+template <int DT, bool HA, bool RC, bool CLIP>
 void launch_apply_dev_k(zs_ctx* c, const int32_t* flag, const zs::SlicePtrs& sp, int32_t n,
-                               const float* acc, int64_t count, float* master, float* m, float* v,
-                               uint16_t* ho, const zs::AdamArgs* ad_dev, zs_device_state* st,
-                               cudaStream_t s) {
+                        const float* acc, int64_t count, float* master, float* m, float* v,
+                        uint16_t* ho, const zs::AdamArgs* ad_dev, zs_device_state* st,
+                        const float* coef, cudaStream_t s) {
   constexpr int VPT = ZS_APPLY_VPT;
   const int64_t units = (count >> 3) / VPT + 8;
-  auto k = zs::k_apply<DT, HA, RC, VPT, false, true>;
+  auto k = zs::k_apply<DT, HA, RC, VPT, CLIP, true>;
   const zs::AdamArgs unused{};
   const zs_scaler unused_sc{};
   launch_k(c, k, grid_for(c, k, units), zs::kThreads, s, flag, sp, n, acc, master, m, v, ho,
-           count, unused, unused_sc, (zs::StepResult*)nullptr, (const float*)nullptr, ad_dev, st,
+           count, unused, unused_sc, (zs::StepResult*)nullptr, coef, ad_dev, st,
            acc_keep_for(count));
 }
 
+template <int DT, bool CLIP>
+void apply_dev_c(zs_ctx* c, const int32_t* flag, const zs::SlicePtrs& sp, int32_t n,
+                 bool recompute, const float* acc, int64_t count, float* master, float* m,
+                 float* v, uint16_t* ho, const zs::AdamArgs* ad_dev, zs_device_state* st,
+                 const float* coef, cudaStream_t s) {
+  if (!recompute)
+    launch_apply_dev_k<DT, true, false, CLIP>(c, flag, sp, n, acc, count, master, m, v, ho,
+                                              ad_dev, st, coef, s);
+  else if (acc != nullptr)
+    launch_apply_dev_k<DT, true, true, CLIP>(c, flag, sp, n, acc, count, master, m, v, ho,
+                                             ad_dev, st, coef, s);
+  else
+    launch_apply_dev_k<DT, false, true, CLIP>(c, flag, sp, n, acc, count, master, m, v, ho,
+                                              ad_dev, st, coef, s);
+}
+
+// The device-resident update (clipped with the context's coefficient when coef != NULL).
 template <int DT>
 void apply_dev(zs_ctx* c, const int32_t* flag, const zs::SlicePtrs& sp, int32_t n,
-                      bool recompute, const float* acc, int64_t count, float* master, float* m,
-                      float* v, uint16_t* ho, const zs::AdamArgs* ad_dev, zs_device_state* st,
-                      cudaStream_t s) {
-  if (!recompute)
-    launch_apply_dev_k<DT, true, false>(c, flag, sp, n, acc, count, master, m, v, ho, ad_dev, st, s);
-  else if (acc != nullptr)
-    launch_apply_dev_k<DT, true, true>(c, flag, sp, n, acc, count, master, m, v, ho, ad_dev, st, s);
+               bool recompute, const float* acc, int64_t count, float* master, float* m,
+               float* v, uint16_t* ho, const zs::AdamArgs* ad_dev, zs_device_state* st,
+               const float* coef, cudaStream_t s) {
+  if (coef != nullptr)
+    apply_dev_c<DT, true>(c, flag, sp, n, recompute, acc, count, master, m, v, ho, ad_dev, st,
+                          coef, s);
   else
-    launch_apply_dev_k<DT, false, true>(c, flag, sp, n, acc, count, master, m, v, ho, ad_dev, st, s);
+    apply_dev_c<DT, false>(c, flag, sp, n, recompute, acc, count, master, m, v, ho, ad_dev, st,
+                           nullptr, s);
 }
 
 // Half-precision accumulator variants (always materialise the sums).
@@ -920,12 +937,12 @@ zs_status zs_shard_step_clipped(zs_ctx* c, const void* const* grads, int32_t n, 
                          stream);
 }
 
-zs_status zs_shard_step_async(zs_ctx* c, const void* const* grads, int32_t n, zs_dtype dt,
-                              int64_t count, float* acc, int32_t accum_steps, float* master,
-                              float* m, float* v, void* half_out, const zs_adam_hparams* hp,
-                              const zs_lr_schedule* sched, zs_device_state* d_state,
-                              cudaStream_t stream) {
-  NvtxRange nvtx_("zs_shard_step_async");
+static zs_status shard_step_async_impl(zs_ctx* c, const void* const* grads, int32_t n,
+                                       zs_dtype dt, int64_t count, float* acc,
+                                       int32_t accum_steps, float* master, float* m, float* v,
+                                       void* half_out, const zs_adam_hparams* hp,
+                                       const zs_lr_schedule* sched, zs_device_state* d_state,
+                                       float max_norm, double* d_norm, cudaStream_t stream) {
   ZS_TRY(check_ctx(c));
   if (dt != ZS_FP16 && dt != ZS_BF16) return fail(c, ZS_ERR_DTYPE, "unknown dtype %d", (int)dt);
   if (count < 0) return fail(c, ZS_ERR_ARG, "count < 0");
@@ -935,6 +952,9 @@ zs_status zs_shard_step_async(zs_ctx* c, const void* const* grads, int32_t n, zs
   if (d_state == nullptr) return fail(c, ZS_ERR_ARG, "d_state is NULL");
   if ((reinterpret_cast<uintptr_t>(d_state) & 7u) != 0)
     return fail(c, ZS_ERR_ALIGN, "d_state is not 8-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(d_norm) & 7u) != 0)
+    return fail(c, ZS_ERR_ALIGN, "d_norm is not 8-byte aligned");
+  if (!std::isfinite(max_norm)) return fail(c, ZS_ERR_ARG, "max_norm must be finite");
   ZS_TRY(check_hparams(c, hp, 1));
   if (sched != nullptr && (sched->kind < ZS_LR_CONSTANT || sched->kind > ZS_LR_WARMUP_DECAY ||
                            sched->warmup_steps < 0 || !std::isfinite(sched->min_lr) ||
@@ -948,6 +968,7 @@ zs_status zs_shard_step_async(zs_ctx* c, const void* const* grads, int32_t n, zs
   ZS_TRY(check_array(c, v, "v", count));
   ZS_TRY(check_array(c, half_out, "half_out", count));
   const bool recompute = (n < 4) || acc == nullptr;
+  const bool clip = max_norm > 0.0f;
   const float* acc_in = (accum_steps > 1 || !recompute) ? acc : nullptr;
   // per-kernel event timing only outside stream capture (an event recorded
   // into a graph would be timed once per capture, not per replay)
@@ -959,7 +980,14 @@ zs_status zs_shard_step_async(zs_ctx* c, const void* const* grads, int32_t n, zs
   }
   if (cap != cudaStreamCaptureStatusNone) c->timing = false;
   zs_status st = ZS_OK;
-  if (count > 0) {
+  if (count > 0 && clip) {
+    // the last micro-step's pass also forms the sum of squares of the final
+    // sums, unscaled (grad_div 1): the scale lives on the device, and the
+    // coefficient kernel divides by N*G*S from the step's constants
+    const bool read = recompute ? acc_in != nullptr : accum_steps > 1;
+    st = reduce_norm_any(c, dt, sp, n, recompute ? const_cast<float*>(acc_in) : acc, count, read,
+                         !recompute, c->d_flag, 1.0f, c->d_sumsq, stream);
+  } else if (count > 0) {
     if (recompute) {
       const bool with_acc = (dt == ZS_BF16) && accum_steps > 1;
       st = reduce_any(c, dt, sp, n, with_acc ? acc : nullptr, count, with_acc, false, c->d_flag,
@@ -967,6 +995,9 @@ zs_status zs_shard_step_async(zs_ctx* c, const void* const* grads, int32_t n, zs
     } else {
       st = reduce_any(c, dt, sp, n, acc, count, accum_steps > 1, true, c->d_flag, stream);
     }
+  } else if (clip) {
+    cudaError_t e = cudaMemsetAsync(c->d_sumsq, 0, sizeof(double), stream);
+    if (e != cudaSuccess) st = cuda_fail(c, e, "sumsq reset");
   }
   if (st != ZS_OK) {
     c->timing = timing;
@@ -977,15 +1008,21 @@ zs_status zs_shard_step_async(zs_ctx* c, const void* const* grads, int32_t n, zs
   launch_k(c, zs::k_step_prologue, 1, 32, stream, (const zs_device_state*)d_state, n,
            accum_steps, *hp, sc, sched ? 1 : 0, c->d_args);
   c->launches += 1;
+  if (clip) {
+    launch_k(c, zs::k_clip_coef_dev, 1, 32, stream, (const double*)c->d_sumsq,
+             (const zs::AdamArgs*)c->d_args, max_norm, c->d_coef, d_norm);
+    c->launches += 1;
+  }
   uint16_t* ho = static_cast<uint16_t*>(half_out);
+  const float* coef = clip ? c->d_coef : nullptr;
   {
     LaunchScope ls(c, stream, recompute ? ZS_KERNEL_APPLY_RECOMPUTE : ZS_KERNEL_APPLY, count);
     if (dt == ZS_FP16)
       apply_dev<ZS_FP16>(c, c->d_flag, sp, recompute ? n : 0, recompute, acc_in, count, master,
-                         m, v, ho, c->d_args, d_state, stream);
+                         m, v, ho, c->d_args, d_state, coef, stream);
     else
       apply_dev<ZS_BF16>(c, c->d_flag, sp, recompute ? n : 0, recompute, acc_in, count, master,
-                         m, v, ho, c->d_args, d_state, stream);
+                         m, v, ho, c->d_args, d_state, coef, stream);
     ls.done();
   }
   c->timing = timing;
@@ -996,6 +1033,28 @@ zs_status zs_shard_step_async(zs_ctx* c, const void* const* grads, int32_t n, zs
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(c, e, "flag reset");
   return ZS_OK;
+}
+
+zs_status zs_shard_step_async(zs_ctx* c, const void* const* grads, int32_t n, zs_dtype dt,
+                              int64_t count, float* acc, int32_t accum_steps, float* master,
+                              float* m, float* v, void* half_out, const zs_adam_hparams* hp,
+                              const zs_lr_schedule* sched, zs_device_state* d_state,
+                              cudaStream_t stream) {
+  NvtxRange nvtx_("zs_shard_step_async");
+  return shard_step_async_impl(c, grads, n, dt, count, acc, accum_steps, master, m, v, half_out,
+                               hp, sched, d_state, 0.0f, nullptr, stream);
+}
+
+zs_status zs_shard_step_async_clipped(zs_ctx* c, const void* const* grads, int32_t n,
+                                      zs_dtype dt, int64_t count, float* acc,
+                                      int32_t accum_steps, float* master, float* m, float* v,
+                                      void* half_out, const zs_adam_hparams* hp,
+                                      const zs_lr_schedule* sched, float max_norm,
+                                      zs_device_state* d_state, double* d_grad_norm,
+                                      cudaStream_t stream) {
+  NvtxRange nvtx_("zs_shard_step_async_clipped");
+  return shard_step_async_impl(c, grads, n, dt, count, acc, accum_steps, master, m, v, half_out,
+                               hp, sched, d_state, max_norm, d_grad_norm, stream);
 }
 
 zs_status zs_grad_accum_halfacc(zs_ctx* c, const void* const* grads, int32_t n, zs_dtype dt,

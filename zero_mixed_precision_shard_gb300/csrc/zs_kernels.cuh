@@ -85,6 +85,9 @@
 #ifndef ZS_NORM_MIN_BLOCKS  // resident CTAs per SM the norm-forming pass is compiled for: 8 x 256
 #define ZS_NORM_MIN_BLOCKS 8    // threads fill the SM (at most 32 registers); its few extra live
 #endif                          // values would otherwise cost a quarter of the resident warps
+#ifndef ZS_NORM_STORE_MIN_BLOCKS  // resident CTAs per SM of the materialising pass that forms the
+#define ZS_NORM_STORE_MIN_BLOCKS 0   // clipping norm (0 leaves it unset)
+#endif
 #ifndef ZS_APPLY_MIN_BLOCKS  // resident CTAs per SM the update is compiled for: 4 keeps every
 #define ZS_APPLY_MIN_BLOCKS 4    // variant at <= 64 registers without spills (the update from acc
 #endif                           // alone held 70, 3 CTAs per SM: 7040 -> 7137 GB/s with the bound)
@@ -565,8 +568,9 @@ __device__ __forceinline__ float sq8f(const float a[8]) {
 // instruction of a warp covers 512 contiguous bytes.
 template <int DT, bool READ_ACC, bool STORE, int VPT, bool HACC = false, bool NORM = false>
 __global__ void __launch_bounds__(ZS_THREADS, NORM && !STORE ? ZS_NORM_MIN_BLOCKS
-                                             : VPT == 1 && !NORM && !READ_ACC ? ZS_FIRST_MIN_BLOCKS
-                                                                              : ZS_MIN_BLOCKS)
+                                             : NORM ? ZS_NORM_STORE_MIN_BLOCKS
+                                             : VPT == 1 && !READ_ACC ? ZS_FIRST_MIN_BLOCKS
+                                                                     : ZS_MIN_BLOCKS)
     k_reduce(const __grid_constant__ SlicePtrs s, int n, float* __restrict__ acc, int64_t count,
              int32_t* __restrict__ flag, double* __restrict__ partials, uint32_t acc_keep,
              int prefetch_ctas) {
@@ -939,6 +943,25 @@ __global__ void k_clip_coef(const double* __restrict__ sumsq, float max_norm,
       if (q < 1.0) c = q;
     }
     *coef = (float)c;
+  }
+}
+
+// The device-resident step's coefficient: the sum of squares arrives unscaled
+// (the scale is only known on the device), so norm = sqrt(sumsq_raw) / (N*G*S)
+// with N*G*S from the step's constants; *norm_out (may be null) gets the norm.
+__global__ void k_clip_coef_dev(const double* __restrict__ sumsq_raw,
+                                const AdamArgs* __restrict__ ad, float max_norm,
+                                float* __restrict__ coef, double* __restrict__ norm_out) {
+  pdl_enter(sumsq_raw, ad, coef, norm_out);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    const double norm = sqrt(*sumsq_raw) / (double)ad->grad_div;
+    double c = 1.0;
+    if (max_norm > 0.0f) {
+      const double q = (double)max_norm / (norm + 1e-6);
+      if (q < 1.0) c = q;
+    }
+    *coef = (float)c;
+    if (norm_out != nullptr) *norm_out = norm;
   }
 }
 

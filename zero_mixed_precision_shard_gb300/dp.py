@@ -133,7 +133,10 @@ class Exchange:
         self.group = group
         self.dist = dist
         self.world = _world(group)
-        self.staged = dist.get_backend(group) == "gloo" if self.world > 1 else False
+        # with a process group every exchange is a collective, one rank included
+        # (a one-rank NCCL group runs the same calls); without one they are copies
+        self.active = dist.is_available() and dist.is_initialized()
+        self.staged = self.active and dist.get_backend(group) == "gloo"
 
     @staticmethod
     def _bytes(t):
@@ -147,7 +150,7 @@ class Exchange:
         elements, in_splits[q] of them for rank q (16-bit elements).  With
         async_op (device buffers, not staged) returns the collective's work
         handle: its wait() orders the current stream after the transfer."""
-        if self.world == 1:
+        if not self.active:
             out.copy_(inp)
             return None
         item = inp.element_size()
@@ -163,7 +166,7 @@ class Exchange:
 
     def all_gather(self, out, inp):
         """out = every rank's `inp`, concatenated in rank order."""
-        if self.world == 1:
+        if not self.active:
             out.copy_(inp)
             return None
         ob, ib = self._bytes(out), self._bytes(inp)
@@ -174,7 +177,7 @@ class Exchange:
         ob.copy_(ho)
 
     def all_reduce(self, t, op: str):
-        if self.world == 1:
+        if not self.active:
             return None
         o = self.dist.ReduceOp.MAX if op == "max" else self.dist.ReduceOp.SUM
         if not self.staged or not t.is_cuda:
@@ -214,7 +217,7 @@ class Zero2Step:
         # 16-bit receive slots, reused bucket after bucket in stream order; with
         # room for two (and device collectives), the exchange of the next
         # bucket overlaps the sum of this one (§2.2 overlap_comm)
-        self.overlap = (recv.numel() >= 2 * slot and self.world > 1 and not self.x.staged
+        self.overlap = (recv.numel() >= 2 * slot and self.x.active and not self.x.staged
                         and recv.is_cuda)
         self.slots = [recv[:slot], recv[slot:2 * slot]] if self.overlap else [recv[:slot]]
         self.flag = flag
