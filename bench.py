@@ -918,7 +918,7 @@ def run_ours(args):
     # the other target workloads, each with its own clock record (one GPU only)
     table = None
     if (world == 1 and not args.skip_table and args.workload == DEFAULT_WORKLOAD
-            and api == "async"):
+            and api == "async" and not args.clip):
         del W, one_step, state
         torch.cuda.empty_cache()
         table = {name: measure_table_workload(zs, ctx, name, args, peak, dev)

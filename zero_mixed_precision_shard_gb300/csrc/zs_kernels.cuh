@@ -85,9 +85,9 @@
 #ifndef ZS_NORM_MIN_BLOCKS  // resident CTAs per SM the norm-forming pass is compiled for: 8 x 256
 #define ZS_NORM_MIN_BLOCKS 8    // threads fill the SM (at most 32 registers); its few extra live
 #endif                          // values would otherwise cost a quarter of the resident warps
-#ifndef ZS_NORM_STORE_MIN_BLOCKS  // resident CTAs per SM of the materialising pass that forms the
-#define ZS_NORM_STORE_MIN_BLOCKS 0   // clipping norm (0 leaves it unset)
-#endif
+#ifndef ZS_NORM_STORE_MIN_BLOCKS  // resident CTAs per SM the materialising pass that forms the
+#define ZS_NORM_STORE_MIN_BLOCKS 6   // clipping norm is compiled for: 1.3B clipped 6825 -> 6940 GB/s
+#endif                               // (8 CTAs: 6694; the 64-rank first pass 7013 -> 7036 at 6)
 #ifndef ZS_APPLY_MIN_BLOCKS  // resident CTAs per SM the update is compiled for: 4 keeps every
 #define ZS_APPLY_MIN_BLOCKS 4    // variant at <= 64 registers without spills (the update from acc
 #endif                           // alone held 70, 3 CTAs per SM: 7040 -> 7137 GB/s with the bound)
