@@ -69,14 +69,22 @@ def kernel_alg_bytes(kind: str, n: int, first: bool = False, with_acc: bool = Fa
         return (4 if with_acc else 0) + 2 * n + 26
     if kind == "sumsq":   # a separate norm pass: acc and/or the re-read slices
         return (4 if with_acc else 0) + (2 * n if first else 0)
+    if kind == "update_oop":   # last micro-step + flag + update, state written out of place
+        return (4 if with_acc else 0) + 2 * n + 26
     raise ValueError(kind)
 
 
 def step_launch_plan(n: int, g: int, dtype: str, acc_kind: str = "fp32", has_acc: bool = True,
-                     clip: float = 0.0, split: bool = False):
+                     clip: float = 0.0, split: bool = False, oop: bool = False):
     """(kind, alg bytes per element) of every kernel one step launches, in the
     order the step launches them (split: the step split at the overflow flag
-    as every rank of a multi-GPU run does, the clipping norm in its own pass)."""
+    as every rank of a multi-GPU run does, the clipping norm in its own pass;
+    oop: the out-of-place step, whose last pass is the update)."""
+    if oop:
+        plan = [("reduce_first" if k == 0 else "reduce",
+                 kernel_alg_bytes("reduce", n, first=(k == 0))) for k in range(g - 1)]
+        plan.append(("update_oop", kernel_alg_bytes("update_oop", n, with_acc=g > 1)))
+        return plan
     if acc_kind == "half":
         plan = [("reduce_first" if k == 0 else "reduce",
                  kernel_alg_bytes("reduce", n, first=(k == 0), acc_bytes=2)) for k in range(g)]
@@ -223,10 +231,34 @@ class DeviceWorkload:
             zs.zs_shard_step_async(ctx, self.slices(wl.g - 1), self.dt, self.E, self.acc, wl.g,
                                    self.master, self.m, self.v, self.half, self.hp, None, state)
 
-    def launch_plan(self, split: bool = False):
+    def launch_plan(self, split: bool = False, oop: bool = False):
         """(kind, alg bytes per element) of every kernel one step launches."""
         return step_launch_plan(self.wl.n, self.wl.g, self.wl.dtype, self.acc_kind,
-                                self.acc is not None, self.clip, split)
+                                self.acc is not None, self.clip, split, oop)
+
+    def step_oop_calls(self, ctx, state):
+        """One step of the device-resident out-of-place form."""
+        zs, wl = self.zs, self.wl
+        for k in range(wl.g - 1):
+            zs.zs_grad_accum(ctx, self.slices(k), self.dt, self.E, self.acc, k == 0)
+        self.finish_oop(ctx, state)
+
+    def finish_oop(self, ctx, state):
+        """The last call of an out-of-place step (the second state set is
+        allocated on first use; state.buf names the current set)."""
+        import torch
+        zs, wl = self.zs, self.wl
+        if not hasattr(self, "_pairs"):
+            E = self.E
+            self.master2 = torch.empty(E, dtype=torch.float32, device=self.dev)
+            self.m2 = torch.empty(E, dtype=torch.float32, device=self.dev)
+            self.v2 = torch.empty(E, dtype=torch.float32, device=self.dev)
+            self.half2 = torch.empty(E, dtype=torch.int16, device=self.dev)
+            self._pairs = [zs.pointer_array(x) for x in ((self.master, self.master2),
+                                                         (self.m, self.m2), (self.v, self.v2),
+                                                         (self.half, self.half2))]
+        zs.zs_shard_step_async_oop(ctx, self.slices(wl.g - 1), self.dt, self.E, self.acc, wl.g,
+                                   *self._pairs, self.hp, None, state)
 
 
 # ---------------------------------------------------------------- clocks
@@ -456,6 +488,8 @@ def run_reference(args):
 API_DESC = {
     "async": "zs_grad_accum + zs_shard_step_async (scale, step count and outcome stay on the "
              "device; no host round trip; the state is read back after the timed steps)",
+    "async_oop": "zs_grad_accum + zs_shard_step_async_oop (device-resident, state written out "
+                 "of place: the last micro-step, the flag and the update in one pass)",
     "sync": "zs_grad_accum + zs_shard_step (one host round trip per step)",
     "graph": "CUDA graph of zs_grad_accum + zs_shard_step_async",
     "split": "zs_reduce_check / zs_check_last + zs_apply + zs_scaler_update (split at the flag)",
@@ -478,11 +512,12 @@ def make_step(zs, ctx, W: DeviceWorkload, api: str, clip: float = 0.0):
     """One step of `api` on W's buffers; returns (step function, device state or None)."""
     import torch
     wl, E = W.wl, W.E
-    if api == "async":
+    if api in ("async", "async_oop"):
         state = zs.DeviceState(W.scaler)
+        calls = W.step_oop_calls if api == "async_oop" else W.step_async_calls
 
         def one_step():
-            W.step_async_calls(ctx, state)
+            calls(ctx, state)
         return one_step, state
     if api == "graph":
         state = zs.DeviceState(W.scaler)
@@ -605,7 +640,7 @@ def measure_table_workload(zs, ctx, name: str, args, peak: float, dev: int):
     out = {"workload": name + (f" (first {W.E} elements)" if args.elements else ""),
            "params": wl.psi, "owned_params": valid, "shard_len": W.E, "n_ranks_simulated": wl.n,
            "accum_steps": wl.g, "grad_dtype": wl.dtype, "alg_bytes_per_step": step_bytes}
-    for api in ("async", "sync"):
+    for api in ("async", "async_oop", "sync"):
         one_step, state = make_step(zs, ctx, W, api)
         # the step rate without per-kernel events (an event pair around each of
         # a short step's launches costs it a few percent), then the same steps
@@ -615,7 +650,7 @@ def measure_table_workload(zs, ctx, name: str, args, peak: float, dev: int):
         timed_steps(ctx, one_step, args.steps, 0, dev, 1)
         per_step = ms / args.steps
         gbs = step_bytes / (per_step * 1e-3) / 1e9
-        kinds = kernel_table(zs, ctx, W.launch_plan())
+        kinds = kernel_table(zs, ctx, W.launch_plan(oop=api == "async_oop"))
         out[api] = {"api": API_DESC[api], "value": valid / (per_step * 1e-3), "unit": "params/s",
                     "ms_per_step": round(per_step, 4), "step_gbs": round(gbs, 1),
                     "step_frac_of_peak": round(gbs / peak, 4), "gpu_launches": launches,
@@ -846,6 +881,8 @@ def run_ours(args):
         raise SystemExit("--split and --graph are separate modes")
     if api == "graph" and args.acc != "fp32":
         raise SystemExit("--graph runs the fp32-accumulator path on one GPU")
+    if api == "async_oop" and (args.clip or args.acc != "fp32"):
+        raise SystemExit("--api async_oop runs the unclipped fp32-accumulator step")
 
     # with several GPUs, rank r owns shard r mod N (a ZeRO job's rank r owns shard r)
     W = DeviceWorkload(wl, shard=rank % wl.n, count=args.elements, acc=args.acc, clip=args.clip)
@@ -855,7 +892,7 @@ def run_ours(args):
     valid = min(W.valid_end - W.begin, E)
     one_step, state = make_step(zs, ctx, W, api, args.clip)
     ms, launches, clock_summary = timed_steps(ctx, one_step, args.steps, args.warmup, dev, world)
-    plan = W.launch_plan(split=api == "split")
+    plan = W.launch_plan(split=api == "split", oop=api == "async_oop")
     if api == "graph":  # replays bypass the context's counter: the kernels of a captured step
         # (the streaming ones, the prologue and the flag reset; with clipping the
         # norm's finalize and the coefficient, and the fold of many partials)
@@ -994,7 +1031,7 @@ def run_e2e(zs, ctx, W: DeviceWorkload, steps: int, api: str = "sync", step_fn=N
     compute = torch.cuda.current_stream()
     done = [torch.cuda.Event() for _ in range(wl.g)]
     free = [torch.cuda.Event() for _ in range(wl.g)]
-    state = zs.DeviceState(W.scaler) if api in ("async", "graph") else None
+    state = zs.DeviceState(W.scaler) if api in ("async", "async_oop", "graph") else None
     result = torch.empty(64, dtype=torch.uint8, pin_memory=True)
 
     def step():
@@ -1016,7 +1053,7 @@ def run_e2e(zs, ctx, W: DeviceWorkload, steps: int, api: str = "sync", step_fn=N
             free[k].record(compute)
         compute.wait_event(done[wl.g - 1])
         if state is not None:
-            W.finish_async(ctx, state)
+            (W.finish_oop if api == "async_oop" else W.finish_async)(ctx, state)
             result.copy_(state.buf, non_blocking=True)
         else:
             W.finish(ctx)
@@ -1064,10 +1101,12 @@ def main(argv=None):
                     help="accumulator format (half: zs_*_halfacc entry points)")
     ap.add_argument("--clip", type=float, default=0.0,
                     help="global-norm gradient clipping at this max norm (zs_shard_step_clipped)")
-    ap.add_argument("--api", default="async", choices=["async", "sync"],
+    ap.add_argument("--api", default="async", choices=["async", "async_oop", "sync"],
                     help="async (default): zs_shard_step_async with the scale and step count on "
-                         "the device, no host round trip per step; sync: zs_shard_step, which "
-                         "returns the flag and scale to the host every step")
+                         "the device, no host round trip per step; async_oop: the same with the "
+                         "state written out of place (needs a second master/m/v/half set); "
+                         "sync: zs_shard_step, which returns the flag and scale to the host "
+                         "every step")
     ap.add_argument("--skip-table", action="store_true",
                     help="skip the other target workloads measured after the headline one")
     ap.add_argument("--graph", action="store_true",

@@ -350,7 +350,8 @@ typedef struct {
 typedef struct {
   zs_scaler scaler;    /* loss-scale state (§4.2) */
   int32_t overflow;    /* 1 if the last step was skipped */
-  int32_t pad_;
+  int32_t buf;         /* out-of-place step: which of the two state buffers holds the
+                          current state (flipped by every applied step); 0 otherwise */
   int64_t step;        /* applied updates so far */
   int64_t iterations;  /* steps run so far, skipped ones included */
   float lr;            /* learning rate of the last applied update */
@@ -389,6 +390,46 @@ zs_status zs_shard_step_async_clipped(zs_ctx* ctx, const void* const* grads, int
                                       const zs_lr_schedule* sched, float max_norm,
                                       zs_device_state* d_state, double* d_grad_norm,
                                       cudaStream_t stream);
+
+/* ---------------------------------------------------------------- out-of-place step */
+
+/* The step with the optimizer state written out of place (§2.1, §2.2, §4.2):
+ * the last micro-step's sums (acc + the n slices, as zs_shard_step adds them),
+ * the overflow check and the AdamW update run as ONE pass that reads the
+ * current master/m/v and writes the new values into a second set of buffers;
+ * after that pass the step's flag is complete, and only a clean step makes
+ * the written set current -- an overflowing step leaves the current set
+ * untouched and its written set is garbage, so the skip semantics are those
+ * of zs_shard_step.  Nothing is written twice: per element the step moves
+ * exactly the algorithmic bytes (2*n*G + 8*(G-1) + 26), against + 8 (the
+ * accumulator written and read back) or + 2*n (the last slices read twice) for
+ * zs_shard_step, at the cost of a second master/m/v/half set (14 bytes per
+ * element of the owned shard).  No clipping (its norm is needed before the
+ * update).  Micro-steps 1..G-1 go through zs_grad_accum as usual.
+ *
+ * zs_shard_step_oop: reads master_in/m_in/v_in, writes master_out/m_out/v_out
+ * and half_out; updates *scaler; *overflow_out == 0 means the *_out buffers
+ * (and half_out) now hold the state and the caller swaps its pointers;
+ * synchronises `stream`.  acc may be NULL when accum_steps == 1.  The six
+ * state arrays (and half_out) must not overlap. */
+zs_status zs_shard_step_oop(zs_ctx* ctx, const void* const* grads, int32_t n, zs_dtype dt,
+                            int64_t count, const float* acc, int32_t accum_steps,
+                            const float* master_in, const float* m_in, const float* v_in,
+                            float* master_out, float* m_out, float* v_out, void* half_out,
+                            const zs_adam_hparams* hp, int64_t step, zs_scaler* scaler,
+                            int32_t* overflow_out, float* new_scale_out, cudaStream_t stream);
+
+/* The device-resident form (as zs_shard_step_async: no host round trip,
+ * capturable): master, m, v and half are HOST arrays of two device pointers
+ * each; d_state->buf says which set is current (0 or 1, initialise it to 0 with
+ * the state in set 0); a clean step writes set buf ^ 1 and flips d_state->buf,
+ * an overflowing one leaves it. */
+zs_status zs_shard_step_async_oop(zs_ctx* ctx, const void* const* grads, int32_t n, zs_dtype dt,
+                                  int64_t count, const float* acc, int32_t accum_steps,
+                                  float* const* master, float* const* m, float* const* v,
+                                  void* const* half, const zs_adam_hparams* hp,
+                                  const zs_lr_schedule* sched, zs_device_state* d_state,
+                                  cudaStream_t stream);
 
 /* ---------------------------------------------------------------- engine */
 
@@ -454,7 +495,8 @@ typedef enum {
   ZS_KERNEL_COPY = 5,            /* roofline probe */
   ZS_KERNEL_SUMSQ = 6,           /* clipping: sum of squares (+ its finalize) */
   ZS_KERNEL_REDUCE_FIRST = 7,    /* first micro-step: sum of n slices into acc (+ flag) */
-  ZS_KERNEL_KINDS = 8
+  ZS_KERNEL_UPDATE_OOP = 8,      /* out-of-place step: last micro-step + flag + update */
+  ZS_KERNEL_KINDS = 9
 } zs_kernel_kind;
 
 /* When enabled, each launch is bracketed by CUDA events on its stream. */

@@ -105,3 +105,14 @@ def test_reference_arm_other_ranks_print_nothing():
     d = _bench_line(["--impl", "reference", "--steps", "1", "--warmup", "1"],
                     env={"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
     assert d is None
+
+
+def test_out_of_place_plan_moves_exactly_the_algorithmic_bytes():
+    """The out-of-place step writes the state once and reads every gradient
+    once: its launches move 2·N·G + 8·(G-1) + 26 bytes per element, nothing more."""
+    for name in ("flat-1m-n2", "gpt2-small-n8", "decoder-1.3b-n16", "llama7b-zero3-n64",
+                 "llama7b-n1"):
+        wl = synth.WORKLOADS[name]
+        plan = bench.step_launch_plan(wl.n, wl.g, wl.dtype, oop=True)
+        assert [k for k, _ in plan][-1] == "update_oop"
+        assert sum(b for _, b in plan) == bench.alg_bytes_per_elem_step(wl.n, wl.g)

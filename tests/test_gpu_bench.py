@@ -25,7 +25,8 @@ def run(args):
 
 @pytest.mark.parametrize("mode", [["--skip-table"], ["--api", "sync"], ["--split"], ["--graph"],
                                   ["--acc", "half"], ["--clip", "1.0", "--skip-table"],
-                                  ["--clip", "1.0", "--api", "sync"], ["--clip", "1.0", "--graph"]])
+                                  ["--clip", "1.0", "--api", "sync"], ["--clip", "1.0", "--graph"],
+                                  ["--api", "async_oop", "--skip-table"]])
 def test_bench_line(mode):
     d = run(["--workload", "llama7b-n1", "--elements", str(1 << 24), "--steps", "3",
              "--warmup", "3", "--e2e-steps", "1", "--skip-cpu", "--skip-probe"] + mode)
@@ -64,9 +65,10 @@ def test_default_api_keeps_the_step_state_on_the_device_and_measures_the_table()
     for name, w in c["workloads"].items():
         wl = bench.synth.WORKLOADS[name]
         assert w["shard_len"] == el and w["n_ranks_simulated"] == wl.n
-        for api in ("async", "sync"):
+        for api in ("async", "async_oop", "sync"):
             a = w[api]
             assert a["value"] == pytest.approx(el / (a["ms_per_step"] * 1e-3), rel=1e-3)
             assert a["step_frac_of_peak"] > 0 and "sm_mhz" in a["clocks"]
             assert a["gpu_launches"] >= 4 * 2
         assert w["async"]["device_state"]["iterations"] == 3 + 2 * 4   # two timed passes
+        assert "update_oop" in w["async_oop"]["kernels"]

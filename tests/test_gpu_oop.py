@@ -1,0 +1,184 @@
+"""The out-of-place step (zs_shard_step_oop, zs_shard_step_async_oop): the
+last micro-step's sums, the overflow check and the AdamW update in one pass
+that writes a second set of state buffers, committed only on a clean step.
+
+It adds the same fp32 sums in the same order and runs the same update
+arithmetic as zs_shard_step, so its state must equal the in-place step's bit
+for bit, step after step, including the skipped steps (where the current set
+must stay untouched); and it is held to the oracle like every other form.
+Random stress inputs at lr 3e-4, at most 10 steps, re-read (n < 4) and
+materialising (n >= 4) counterparts, fp16 and bf16, ragged tails."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from _helpers import STRESS_LR, assert_close, dev16, half_ulps, host16, lib_half
+
+pytestmark = pytest.mark.gpu
+
+FP16, BF16 = 0, 1
+
+
+@pytest.fixture(scope="module")
+def zs():
+    import zero_mixed_precision_shard_gb300 as pkg
+    torch.cuda.set_device(0)
+    return pkg
+
+
+@pytest.fixture(scope="module")
+def ctx(zs):
+    c = zs.Ctx()
+    yield c
+    c.close()
+
+
+def rand_grads(rng, n, count, dtype, scale):
+    return [lib_half((rng.standard_normal(count) * 1e-3 * scale *
+                      np.exp2(rng.integers(-4, 4, count))).astype(np.float32), dtype)
+            for _ in range(n)]
+
+
+def state_set(master0, count):
+    master = torch.from_numpy(master0.copy()).cuda()
+    return {"p": master, "m": torch.zeros_like(master), "v": torch.zeros_like(master),
+            "h": torch.zeros(count, dtype=torch.int16, device="cuda")}
+
+
+@pytest.mark.parametrize("dtype", [FP16, BF16])
+@pytest.mark.parametrize("n,G,count", [(1, 1, 4099), (2, 3, 10007), (4, 1, 8200),
+                                       (16, 2, 20011), (64, 1, 777)])
+def test_oop_steps_equal_the_in_place_step_and_the_oracle(zs, ctx, dtype, n, G, count):
+    rng = np.random.default_rng(n * 31 + G + 7 * dtype)
+    master0 = (rng.standard_normal(count) * 0.02).astype(np.float32)
+    hp_vals = (STRESS_LR, 0.9, 0.999, 1e-8, 0.01)
+    hp, hp_o = zs.make_hparams(*hp_vals), oracle.make_hparams(*hp_vals)
+    dyn = dtype == FP16
+    sc_o = oracle.make_scaler(1024.0 if dyn else 1.0, 1.0, 3, 1, dyn)
+    sc_a = zs.zs_scaler_init(sc_o.scale, 1.0, 3, 1, dyn)     # in place
+    sc_b = zs.zs_scaler_init(sc_o.scale, 1.0, 3, 1, dyn)     # out of place
+    st = oracle.ShardState.from_master(master0, dtype)
+    ref = state_set(master0, count)
+    bufs = [state_set(master0, count), state_set(np.zeros_like(master0), count)]
+    cur = 0
+    acc_a = torch.zeros(count, dtype=torch.float32, device="cuda")
+    acc_b = torch.zeros(count, dtype=torch.float32, device="cuda")
+    t = t_o = 0
+    inf = 0x7C00 if dtype == FP16 else 0x7F80
+    for s in range(1, 11):
+        grads = [rand_grads(rng, n, count, dtype, sc_o.scale) for _ in range(G)]
+        if s in (3, 7):
+            k = G - 1 if s == 3 else 0            # the last micro-step, then an earlier one
+            grads[k][n - 1][count // 3] = inf
+        ovf_o, t_o, _ = oracle.shard_step(grads, dtype, st, hp_o, t_o, sc_o)
+        dg = [[dev16(x) for x in micro] for micro in grads]
+        for k in range(G - 1):
+            zs.zs_grad_accum(ctx, dg[k], dtype, count, acc_a, k == 0)
+        ovf_a, _ = zs.zs_shard_step(ctx, dg[G - 1], dtype, count, acc_a, G, ref["p"], ref["m"],
+                                    ref["v"], ref["h"], hp, t + 1, sc_a)
+        for k in range(G - 1):
+            zs.zs_grad_accum(ctx, dg[k], dtype, count, acc_b, k == 0)
+        src, dst = bufs[cur], bufs[cur ^ 1]
+        before = [x.clone() for x in (src["p"], src["m"], src["v"])]
+        ovf_b, scale_b = zs.zs_shard_step_oop(ctx, dg[G - 1], dtype, count,
+                                              acc_b if G > 1 else None, G, src["p"], src["m"],
+                                              src["v"], dst["p"], dst["m"], dst["v"], dst["h"],
+                                              hp, t + 1, sc_b)
+        assert ovf_a == ovf_b == ovf_o, f"step {s}"
+        assert scale_b == sc_a.scale == sc_o.scale
+        assert (sc_b.clean_count, sc_b.hyst_left) == (sc_o.clean_count, sc_o.hyst_left)
+        if ovf_b:
+            for x, y in zip(before, (src["p"], src["m"], src["v"])):
+                assert torch.equal(x, y)          # the current set is untouched
+        else:
+            cur ^= 1
+            t += 1
+        now = bufs[cur]
+        for k in ("p", "m", "v"):
+            assert torch.equal(now[k], ref[k]), (s, k)
+        if t:
+            assert torch.equal(now["h"], ref["h"])
+    assert t == t_o
+    now = bufs[cur]
+    assert_close(now["p"].cpu().numpy(), st.master, "master")
+    assert_close(now["m"].cpu().numpy(), st.m, "m")
+    assert_close(now["v"].cpu().numpy(), st.v, "v")
+    assert half_ulps(host16(now["h"]), st.half).max() <= 1
+
+
+@pytest.mark.parametrize("graph", [False, True])
+@pytest.mark.parametrize("n,G,count", [(1, 3, 20_011), (8, 2, 40_003), (64, 1, 4_103)])
+def test_async_oop_steps_match_oracle(zs, ctx, n, G, count, graph):
+    """The device-resident form: the buffer index in the device state flips on
+    every applied step; against the oracle with a WarmupDecayLR schedule, an
+    overflow and a CUDA-graph replay."""
+    dtype = FP16
+    rng = np.random.default_rng(n + 10 * G + (100 if graph else 0))
+    master0 = (rng.standard_normal(count) * 0.02).astype(np.float32)
+    st = oracle.ShardState.from_master(master0, dtype)
+    sc_o = oracle.make_scaler(512.0, 1.0, 2, 1, True)
+    kind, mn, mx, wu, tot = (oracle.LR_WARMUP_DECAY, float(np.float32(1e-5)),
+                             float(np.float32(STRESS_LR)), 3, 9)
+    sched = zs.make_schedule(kind, mn, mx, wu, tot)
+    hp = zs.make_hparams(mx, 0.9, 0.999, 1e-8, 0.01)
+    state = zs.DeviceState(zs.zs_scaler_init(sc_o.scale, 1.0, 2, 1, True))
+    sets = [state_set(master0, count), state_set(np.zeros_like(master0), count)]
+    acc = torch.zeros(count, dtype=torch.float32, device="cuda")
+    pad = (count + 7) // 8 * 8
+    gbuf = torch.zeros((G, n, pad), dtype=torch.int16, device="cuda")
+    ptrs = [zs.pointer_array(gbuf[k, r, :count] for r in range(n)) for k in range(G)]
+    pairs = {k: zs.pointer_array([sets[0][k], sets[1][k]]) for k in ("p", "m", "v", "h")}
+
+    def step_calls():
+        for k in range(G - 1):
+            zs.zs_grad_accum(ctx, ptrs[k], dtype, count, acc, k == 0)
+        zs.zs_shard_step_async_oop(ctx, ptrs[G - 1], dtype, count, acc, G, pairs["p"],
+                                   pairs["m"], pairs["v"], pairs["h"], hp, sched, state)
+
+    g = None
+    t_o = 0
+    for s in range(1, 11):
+        grads = [[lib_half((rng.standard_normal(count) * 1e-2 * sc_o.scale).astype(np.float32),
+                           dtype) for _ in range(n)] for _ in range(G)]
+        if s == 5:
+            grads[G - 1][n - 1][count - 1] = 0x7C00
+        host = np.stack([np.stack(mc) for mc in grads]).view(np.int16)
+        gbuf[:, :, :count].copy_(torch.from_numpy(host))
+        lr_t = oracle.lr_at(kind, mn, mx, wu, tot, t_o + 1)
+        ovf_o, t_o, _ = oracle.shard_step(grads, dtype, st,
+                                          oracle.make_hparams(lr_t, 0.9, 0.999, 1e-8, 0.01),
+                                          t_o, sc_o)
+        if graph and g is None:
+            step_calls()                 # the first step uncaptured, then capture the rest
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                step_calls()
+        elif graph:
+            g.replay()
+        else:
+            step_calls()
+        d = state.read()
+        assert d.overflow == ovf_o and d.scaler.scale == sc_o.scale, f"step {s}"
+        assert d.step == t_o and d.iterations == s and d.buf == t_o % 2
+    cur = sets[state.read().buf]
+    assert_close(cur["p"].cpu().numpy(), st.master, "master")
+    assert_close(cur["m"].cpu().numpy(), st.m, "m")
+    assert_close(cur["v"].cpu().numpy(), st.v, "v")
+    assert half_ulps(host16(cur["h"]), st.half).max() <= 1
+
+
+def test_oop_rejects_overlapping_buffers(zs, ctx):
+    count = 64
+    a = torch.zeros(4 * count, dtype=torch.float32, device="cuda")
+    h = torch.zeros(count, dtype=torch.int16, device="cuda")
+    g = [torch.zeros(count, dtype=torch.int16, device="cuda")]
+    sc = zs.zs_scaler_init(1.0, 1.0, 10, 1, False)
+    hp = zs.make_hparams(1e-4)
+    p_in, m_in, v_in, p_out = a[:count], a[count:2 * count], a[2 * count:3 * count], a[3 * count:]
+    # m_out aliasing m_in: refused before any work
+    with pytest.raises(zs.ZsError) as e:
+        zs.zs_shard_step_oop(ctx, g, FP16, count, None, 1, p_in, m_in, v_in, p_out, m_in,
+                             a[count + 8:2 * count + 8], h, hp, 1, sc)
+    assert e.value.status == zs.ZS_ERR_ARG

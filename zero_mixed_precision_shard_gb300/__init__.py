@@ -21,9 +21,9 @@ ZS_FP16, ZS_BF16 = 0, 1
 ZS_MAX_RANKS = 256
 ZS_DEFAULT_ALIGN = 64
 (ZS_KERNEL_REDUCE, ZS_KERNEL_CHECK, ZS_KERNEL_APPLY, ZS_KERNEL_APPLY_RECOMPUTE, ZS_KERNEL_SCALER,
- ZS_KERNEL_COPY, ZS_KERNEL_SUMSQ, ZS_KERNEL_REDUCE_FIRST) = range(8)
+ ZS_KERNEL_COPY, ZS_KERNEL_SUMSQ, ZS_KERNEL_REDUCE_FIRST, ZS_KERNEL_UPDATE_OOP) = range(9)
 KERNEL_NAMES = ["reduce", "check", "apply", "apply_recompute", "scaler", "copy", "sumsq",
-                "reduce_first"]
+                "reduce_first", "update_oop"]
 _STATUS = {0: "ZS_OK", -1: "ZS_ERR_ARG", -2: "ZS_ERR_ALIGN", -3: "ZS_ERR_DTYPE", -4: "ZS_ERR_CUDA",
            -5: "ZS_ERR_TIMEOUT", -6: "ZS_ERR_LIMIT"}
 
@@ -58,7 +58,7 @@ class zs_lr_schedule(ctypes.Structure):
 
 
 class zs_device_state(ctypes.Structure):
-    _fields_ = [("scaler", zs_scaler), ("overflow", ctypes.c_int32), ("pad_", ctypes.c_int32),
+    _fields_ = [("scaler", zs_scaler), ("overflow", ctypes.c_int32), ("buf", ctypes.c_int32),
                 ("step", ctypes.c_int64),
                 ("iterations", ctypes.c_int64), ("lr", ctypes.c_float),
                 ("grad_div", ctypes.c_float)]
@@ -120,6 +120,12 @@ def _load():
         "zs_shard_step_async_clipped": [vp, pp, i32, i32, i64, vp, i32, vp, vp, vp, vp,
                                         ctypes.POINTER(zs_adam_hparams),
                                         ctypes.POINTER(zs_lr_schedule), f32, vp, vp, vp],
+        "zs_shard_step_oop": [vp, pp, i32, i32, i64, vp, i32, vp, vp, vp, vp, vp, vp, vp,
+                              ctypes.POINTER(zs_adam_hparams), i64, ctypes.POINTER(zs_scaler),
+                              i32p, ctypes.POINTER(ctypes.c_float), vp],
+        "zs_shard_step_async_oop": [vp, pp, i32, i32, i64, vp, i32, pp, pp, pp, pp,
+                                    ctypes.POINTER(zs_adam_hparams),
+                                    ctypes.POINTER(zs_lr_schedule), vp, vp],
         "zs_grad_sumsq": [vp, pp, i32, i32, vp, i64, f32, vp, vp],
         "zs_grad_sumsq_noalloc": [pp, i32, i32, vp, i64, f32, vp, vp],
         "zs_apply_clipped": [vp, vp, vp, f32, pp, i32, i32, vp, i64, f32, vp, vp, vp, vp,
@@ -419,6 +425,30 @@ def zs_shard_step_async_clipped(ctx: Ctx, grads, dt, count: int, acc, accum_step
         _addr(master), _addr(m), _addr(v), _addr(half_out), ctypes.byref(hp),
         ctypes.byref(sched) if sched is not None else None, max_norm, _addr(d_state),
         _addr(d_grad_norm), _stream(stream)))
+
+
+def zs_shard_step_oop(ctx: Ctx, grads, dt, count: int, acc, accum_steps: int, master_in, m_in,
+                      v_in, master_out, m_out, v_out, half_out, hp: zs_adam_hparams, step: int,
+                      scaler: zs_scaler, stream=None):
+    """Returns (overflow, new_scale); on overflow == 0 the *_out buffers hold the
+    new state.  *scaler is updated in place."""
+    ovf = ctypes.c_int32()
+    ns = ctypes.c_float()
+    ctx.check(lib.zs_shard_step_oop(ctx.handle, _ptrs(grads), len(grads), _dtype(dt), count,
+                                    _addr(acc), accum_steps, _addr(master_in), _addr(m_in),
+                                    _addr(v_in), _addr(master_out), _addr(m_out), _addr(v_out),
+                                    _addr(half_out), ctypes.byref(hp), step, ctypes.byref(scaler),
+                                    ctypes.byref(ovf), ctypes.byref(ns), _stream(stream)))
+    return ovf.value, ns.value
+
+
+def zs_shard_step_async_oop(ctx: Ctx, grads, dt, count: int, acc, accum_steps: int, master,
+                            m, v, half, hp: zs_adam_hparams, sched, d_state, stream=None):
+    """master, m, v, half: pairs of buffers; d_state.buf names the current one."""
+    ctx.check(lib.zs_shard_step_async_oop(
+        ctx.handle, _ptrs(grads), len(grads), _dtype(dt), count, _addr(acc), accum_steps,
+        _ptrs(master), _ptrs(m), _ptrs(v), _ptrs(half), ctypes.byref(hp),
+        ctypes.byref(sched) if sched is not None else None, _addr(d_state), _stream(stream)))
 
 
 def zs_grad_accum_halfacc(ctx: Ctx, grads, dt, count: int, acc_half, first: bool, stream=None):

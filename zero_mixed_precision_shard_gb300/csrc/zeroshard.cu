@@ -570,6 +570,44 @@ void apply_dev(zs_ctx* c, const int32_t* flag, const zs::SlicePtrs& sp, int32_t 
                            nullptr, s);
 }
 
+// Out-of-place step: the update kernel and its commit.
+template <int DT, bool HA, bool DEV>
+void launch_oop_k(zs_ctx* c, const zs::SlicePtrs& sp, int32_t n, const float* acc,
+                  const zs::OopBufs& b, int64_t count, const zs::AdamArgs& ad,
+                  const zs::AdamArgs* ad_dev, const zs_device_state* st, int32_t* flag,
+                  cudaStream_t s) {
+  auto k = zs::k_update_oop<DT, HA, DEV>;
+  launch_k(c, k, grid_for(c, k, (count >> 3) + 8), zs::kThreads, s, sp, n, acc, b, count, ad,
+           ad_dev, st, flag, acc_keep_for(count));
+}
+
+template <bool DEV>
+zs_status update_oop(zs_ctx* c, zs_dtype dt, const zs::SlicePtrs& sp, int32_t n,
+                     const float* acc, const zs::OopBufs& b, int64_t count,
+                     const zs::AdamArgs& ad, const zs::AdamArgs* ad_dev,
+                     const zs_device_state* st, cudaStream_t s) {
+  LaunchScope ls(c, s, ZS_KERNEL_UPDATE_OOP, count);
+  if (count > 0) {
+    if (dt == ZS_FP16) {
+      if (acc) launch_oop_k<ZS_FP16, true, DEV>(c, sp, n, acc, b, count, ad, ad_dev, st, c->d_flag, s);
+      else launch_oop_k<ZS_FP16, false, DEV>(c, sp, n, acc, b, count, ad, ad_dev, st, c->d_flag, s);
+    } else {
+      if (acc) launch_oop_k<ZS_BF16, true, DEV>(c, sp, n, acc, b, count, ad, ad_dev, st, c->d_flag, s);
+      else launch_oop_k<ZS_BF16, false, DEV>(c, sp, n, acc, b, count, ad, ad_dev, st, c->d_flag, s);
+    }
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(c, e, "out-of-place update launch");
+  if (count > 0) ls.done();
+  return ZS_OK;
+}
+
+// [a, a + la) and [b, b + lb) share a byte.
+bool overlaps(const void* a, int64_t la, const void* b, int64_t lb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return la > 0 && lb > 0 && x < y + (uintptr_t)lb && y < x + (uintptr_t)la;
+}
+
 // Half-precision accumulator variants (always materialise the sums).
 template <int DT, bool RA>
 void launch_reduce_hacc_k(zs_ctx* c, const zs::SlicePtrs& sp, int32_t n, float* acc,
@@ -1055,6 +1093,134 @@ zs_status zs_shard_step_async_clipped(zs_ctx* c, const void* const* grads, int32
   NvtxRange nvtx_("zs_shard_step_async_clipped");
   return shard_step_async_impl(c, grads, n, dt, count, acc, accum_steps, master, m, v, half_out,
                                hp, sched, d_state, max_norm, d_grad_norm, stream);
+}
+
+// Checks shared by the out-of-place calls: the step's arguments and the two
+// buffer sets (16-byte aligned, each of count elements, no overlap between them).
+// h[0] may be NULL (the synchronising call writes one half copy only).
+static zs_status check_oop(zs_ctx* c, const void* const* grads, int32_t n, zs_dtype dt,
+                           int64_t count, const float* acc, int32_t accum_steps,
+                           const float* const p[2], const float* const m[2],
+                           const float* const v[2], const void* const h[2], zs::SlicePtrs* sp) {
+  if (dt != ZS_FP16 && dt != ZS_BF16) return fail(c, ZS_ERR_DTYPE, "unknown dtype %d", (int)dt);
+  if (count < 0) return fail(c, ZS_ERR_ARG, "count < 0");
+  if (accum_steps < 1) return fail(c, ZS_ERR_ARG, "accum_steps must be >= 1");
+  if (accum_steps > 1 && acc == nullptr && count > 0)
+    return fail(c, ZS_ERR_ARG, "acc is required when accum_steps > 1");
+  ZS_TRY(check_slices(c, grads, n, count, sp));
+  ZS_TRY(check_array(c, acc, "acc", 0));
+  const char* names[8] = {"master[0]", "master[1]", "m[0]", "m[1]", "v[0]", "v[1]",
+                          "half[0]", "half[1]"};
+  const void* arr[8] = {p[0], p[1], m[0], m[1], v[0], v[1], h[0], h[1]};
+  const int64_t bytes[8] = {4 * count, 4 * count, 4 * count, 4 * count,
+                            4 * count, 4 * count, 2 * count, 2 * count};
+  for (int i = 0; i < 8; ++i)
+    if (i != 6 || h[0] != nullptr) ZS_TRY(check_array(c, arr[i], names[i], count));
+  for (int i = 0; i < 8; ++i)
+    for (int j = i + 1; j < 8; ++j)
+      if (arr[i] != nullptr && arr[j] != nullptr && overlaps(arr[i], bytes[i], arr[j], bytes[j]))
+        return fail(c, ZS_ERR_ARG, "%s and %s overlap", names[i], names[j]);
+  return ZS_OK;
+}
+
+zs_status zs_shard_step_oop(zs_ctx* c, const void* const* grads, int32_t n, zs_dtype dt,
+                            int64_t count, const float* acc, int32_t accum_steps,
+                            const float* master_in, const float* m_in, const float* v_in,
+                            float* master_out, float* m_out, float* v_out, void* half_out,
+                            const zs_adam_hparams* hp, int64_t step, zs_scaler* scaler,
+                            int32_t* overflow_out, float* new_scale_out, cudaStream_t stream) {
+  NvtxRange nvtx_("zs_shard_step_oop");
+  ZS_TRY(check_ctx(c));
+  ZS_TRY(check_hparams(c, hp, step));
+  ZS_TRY(check_scaler(c, scaler));
+  zs::SlicePtrs sp;
+  const float* pp[2] = {master_in, master_out};
+  const float* mm[2] = {m_in, m_out};
+  const float* vv[2] = {v_in, v_out};
+  const void* hh[2] = {nullptr, half_out};  // the previous half copy is not read
+  ZS_TRY(check_oop(c, grads, n, dt, count, accum_steps > 1 ? acc : nullptr, accum_steps, pp, mm,
+                   vv, hh, &sp));
+  const double div = (double)n * (double)accum_steps * (double)scaler->scale;
+  const float grad_div = (float)div;
+  if (!(grad_div > 0.0f) || !std::isfinite(grad_div))
+    return fail(c, ZS_ERR_ARG, "n * accum_steps * scale is not a positive finite fp32");
+  const zs::AdamArgs ad = adam_args(hp, step, grad_div);
+  zs::OopBufs b;
+  b.p[0] = const_cast<float*>(master_in);
+  b.p[1] = master_out;
+  b.m[0] = const_cast<float*>(m_in);
+  b.m[1] = m_out;
+  b.v[0] = const_cast<float*>(v_in);
+  b.v[1] = v_out;
+  b.h[0] = nullptr;
+  b.h[1] = static_cast<uint16_t*>(half_out);
+  ZS_TRY(update_oop<false>(c, dt, sp, n, accum_steps > 1 ? acc : nullptr, b, count, ad, nullptr,
+                           nullptr, stream));
+  launch_k(c, zs::k_commit_oop<false>, 1, 32, stream, c->d_flag, (zs_device_state*)nullptr,
+           (const zs::AdamArgs*)nullptr, *scaler, c->d_result);
+  c->launches += 1;
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(c, e, "commit launch");
+  return finish_step(c, scaler, overflow_out, new_scale_out, nullptr, stream);
+}
+
+zs_status zs_shard_step_async_oop(zs_ctx* c, const void* const* grads, int32_t n, zs_dtype dt,
+                                  int64_t count, const float* acc, int32_t accum_steps,
+                                  float* const* master, float* const* m, float* const* v,
+                                  void* const* half, const zs_adam_hparams* hp,
+                                  const zs_lr_schedule* sched, zs_device_state* d_state,
+                                  cudaStream_t stream) {
+  NvtxRange nvtx_("zs_shard_step_async_oop");
+  ZS_TRY(check_ctx(c));
+  if (master == nullptr || m == nullptr || v == nullptr || half == nullptr)
+    return fail(c, ZS_ERR_ARG, "a buffer pair is NULL");
+  if (d_state == nullptr) return fail(c, ZS_ERR_ARG, "d_state is NULL");
+  if ((reinterpret_cast<uintptr_t>(d_state) & 7u) != 0)
+    return fail(c, ZS_ERR_ALIGN, "d_state is not 8-byte aligned");
+  ZS_TRY(check_hparams(c, hp, 1));
+  if (sched != nullptr && (sched->kind < ZS_LR_CONSTANT || sched->kind > ZS_LR_WARMUP_DECAY ||
+                           sched->warmup_steps < 0 || !std::isfinite(sched->min_lr) ||
+                           !std::isfinite(sched->max_lr)))
+    return fail(c, ZS_ERR_ARG, "bad learning-rate schedule");
+  zs::SlicePtrs sp;
+  const float* pp[2] = {master[0], master[1]};
+  const float* mm[2] = {m[0], m[1]};
+  const float* vv[2] = {v[0], v[1]};
+  const void* hh[2] = {half[0], half[1]};
+  const float* acc_in = accum_steps > 1 ? acc : nullptr;
+  ZS_TRY(check_oop(c, grads, n, dt, count, acc_in, accum_steps, pp, mm, vv, hh, &sp));
+  zs_lr_schedule sc{};
+  if (sched) sc = *sched;
+  // per-kernel event timing only outside stream capture
+  const bool timing = c->timing;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+    (void)cudaGetLastError();
+    cap = cudaStreamCaptureStatusActive;
+  }
+  if (cap != cudaStreamCaptureStatusNone) c->timing = false;
+  launch_k(c, zs::k_step_prologue, 1, 32, stream, (const zs_device_state*)d_state, n,
+           accum_steps, *hp, sc, sched ? 1 : 0, c->d_args);
+  c->launches += 1;
+  zs::OopBufs b;
+  for (int i = 0; i < 2; ++i) {
+    b.p[i] = master[i];
+    b.m[i] = m[i];
+    b.v[i] = v[i];
+    b.h[i] = static_cast<uint16_t*>(half[i]);
+  }
+  const zs::AdamArgs unused{};
+  zs_status st = update_oop<true>(c, dt, sp, n, acc_in, b, count, unused, c->d_args, d_state,
+                                  stream);
+  c->timing = timing;
+  ZS_TRY(st);
+  const zs_scaler unused_sc{};
+  launch_k(c, zs::k_commit_oop<true>, 1, 32, stream, c->d_flag, d_state,
+           (const zs::AdamArgs*)c->d_args, unused_sc, (zs::StepResult*)nullptr);
+  c->launches += 1;
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(c, e, "commit launch");
+  return ZS_OK;
 }
 
 zs_status zs_grad_accum_halfacc(zs_ctx* c, const void* const* grads, int32_t n, zs_dtype dt,

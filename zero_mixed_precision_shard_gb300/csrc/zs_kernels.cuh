@@ -85,6 +85,9 @@
 #ifndef ZS_NORM_MIN_BLOCKS  // resident CTAs per SM the norm-forming pass is compiled for: 8 x 256
 #define ZS_NORM_MIN_BLOCKS 8    // threads fill the SM (at most 32 registers); its few extra live
 #endif                          // values would otherwise cost a quarter of the resident warps
+#ifndef ZS_OOP_MIN_BLOCKS  // resident CTAs per SM the out-of-place update is compiled for
+#define ZS_OOP_MIN_BLOCKS ZS_APPLY_MIN_BLOCKS
+#endif
 #ifndef ZS_NORM_STORE_MIN_BLOCKS  // resident CTAs per SM the materialising pass that forms the
 #define ZS_NORM_STORE_MIN_BLOCKS 6   // clipping norm is compiled for: 1.3B clipped 6825 -> 6940 GB/s
 #endif                               // (8 CTAs: 6694; the 64-rank first pass 7013 -> 7036 at 6)
@@ -851,6 +854,115 @@ __global__ void __launch_bounds__(ZS_THREADS, ZS_APPLY_MIN_BLOCKS)
     var[i] = v;
     half_out[i] = (uint16_t)float_to_half_bits<DT>(p);
   }
+}
+
+// ---------------------------------------------------------------- out-of-place step
+
+// The two state buffers of the out-of-place step: the step reads set `cur` and
+// writes set `cur ^ 1`; only a clean step makes the written set current.
+struct OopBufs {
+  float* p[2];
+  float* m[2];
+  float* v[2];
+  uint16_t* h[2];
+};
+
+// The last micro-step, the overflow check and the update in one pass, out of
+// place: s = (acc or +0) + the n slices in rank order (the same fp32 sums as
+// the other forms), the flag ORed with any non-finite s, and AdamW from the
+// current buffers into the other ones -- written whatever the flag turns out
+// to be, since nothing is committed until k_commit_oop has seen the whole
+// step's flag.  DEV: the step's constants come from k_step_prologue and the
+// current buffer index from the device state; otherwise from the host (cur 0).
+template <int DT, bool HAS_ACC, bool DEV>
+__global__ void __launch_bounds__(ZS_THREADS, ZS_OOP_MIN_BLOCKS)
+    k_update_oop(const __grid_constant__ SlicePtrs s, int n, const float* __restrict__ acc,
+                 const __grid_constant__ OopBufs b, int64_t count, AdamArgs ad_host,
+                 const AdamArgs* __restrict__ ad_dev, const zs_device_state* __restrict__ dstate,
+                 int32_t* __restrict__ flag, uint32_t acc_keep) {
+  pdl_enter(&s, acc, &b, ad_dev, dstate, flag);
+  const uint64_t pol = acc_policy(acc_keep);
+  AdamArgs ad = ad_host;
+  int cur = 0;
+  if constexpr (DEV) {
+    ad = *ad_dev;
+    cur = dstate->buf & 1;
+  }
+  const float* __restrict__ pin = b.p[cur];
+  const float* __restrict__ min_ = b.m[cur];
+  const float* __restrict__ vin = b.v[cur];
+  float* __restrict__ pout = b.p[cur ^ 1];
+  float* __restrict__ mout = b.m[cur ^ 1];
+  float* __restrict__ vout = b.v[cur ^ 1];
+  uint16_t* __restrict__ hout = b.h[cur ^ 1];
+  const int64_t nvec = count >> 3;
+  const int64_t stride = (int64_t)gridDim.x * kThreads;
+  const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+  bool bad = false;
+  for (int64_t base = tid; base < nvec; base += stride) {
+    int64_t vi[1] = {base};
+    bool ok[1] = {true};
+    float a[1][8];
+    float p[8], m[8], v[8];
+    if (HAS_ACC) {
+      acc_ld(acc + base * 8, a[0], pol);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) a[0][k] = 0.0f;
+    }
+    load8(pin + base * 8, p);
+    load8(min_ + base * 8, m);
+    load8(vin + base * 8, v);
+    sum_slices<DT, 1>(s, n, vi, ok, a);
+    uint32_t h[4];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      bad |= not_finite(a[0][k]);
+      adamw1<false>(ad, a[0][k], p[k], m[k], v[k]);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      h[k] = float_to_half_bits<DT>(p[2 * k]) | (float_to_half_bits<DT>(p[2 * k + 1]) << 16);
+    store8_cs(pout + base * 8, p);
+    store8_cs(mout + base * 8, m);
+    store8_cs(vout + base * 8, v);
+    __stcs(reinterpret_cast<uint4*>(hout) + base, make_uint4(h[0], h[1], h[2], h[3]));
+  }
+  const int64_t tail = count - nvec * 8;
+  if (tid < tail) {
+    const int64_t i = nvec * 8 + tid;
+    float a = HAS_ACC ? acc[i] : 0.0f;
+    a = sum_slices1<DT>(s, n, i, a);
+    bad |= not_finite(a);
+    float p = pin[i], m = min_[i], v = vin[i];
+    adamw1<false>(ad, a, p, m, v);
+    pout[i] = p;
+    mout[i] = m;
+    vout[i] = v;
+    hout[i] = (uint16_t)float_to_half_bits<DT>(p);
+  }
+  raise_flag(flag, bad);
+}
+
+// Commit of the out-of-place step (one thread, after the whole update grid):
+// the loss-scale update from the step's flag; on a clean step the written
+// buffers become current (DEV: the device state's index flips and Adam's step
+// count advances; otherwise the host swaps on the returned result); then the
+// flag is cleared for the next step.
+template <bool DEV>
+__global__ void k_commit_oop(int32_t* __restrict__ flag, zs_device_state* __restrict__ dstate,
+                             const AdamArgs* __restrict__ ad_dev, zs_scaler scaler_in,
+                             StepResult* __restrict__ result) {
+  pdl_enter(flag, dstate, ad_dev, result);
+  if (blockIdx.x != 0 || threadIdx.x != 0) return;
+  const int32_t overflow = *flag;
+  if constexpr (DEV) {
+    device_state_step(dstate, overflow, *ad_dev);
+    if (!overflow) dstate->buf = (dstate->buf & 1) ^ 1;
+  } else {
+    scaler_step(scaler_in, overflow, result);
+  }
+  *flag = 0;
 }
 
 // ---------------------------------------------------------------- clipping
