@@ -1,6 +1,8 @@
 /* A plain C caller of libzeroshard: no Python, no torch.  Reads a step's
  * inputs from a file, runs G micro-steps through zs_grad_accum and
  * zs_shard_step with cudaMalloc'ed buffers, and writes the updated state.
+ * With a third argument "oop" the last call is zs_shard_step_oop instead: the
+ * new state lands in a second set of buffers, which a clean step makes current.
  *
  * Input file:  int64 count, n, g; float scale; float lr, beta1, beta2, eps, wd;
  *              g*n*count uint16 gradients (micro-step major); count float master.
@@ -24,7 +26,8 @@
   } while (0)
 
 int main(int argc, char** argv) {
-  CHECK(argc == 3);
+  CHECK(argc == 3 || argc == 4);
+  const int oop = argc == 4;
   FILE* in = fopen(argv[1], "rb");
   CHECK(in != NULL);
   int64_t hdr[3];
@@ -71,10 +74,28 @@ int main(int argc, char** argv) {
   }
   int32_t ovf = -1;
   float new_scale = 0.0f;
-  zs_status st = zs_shard_step(ctx, (const void* const*)(dgrad + (g - 1) * n), (int32_t)n,
-                               ZS_FP16, count, acc, (int32_t)g, master, m, v, half, &hp, 1, &sc,
-                               &ovf, &new_scale, 0);
-  if (st != ZS_OK) fprintf(stderr, "zs_shard_step: %s\n", zs_last_error(ctx));
+  zs_status st;
+  if (!oop) {
+    st = zs_shard_step(ctx, (const void* const*)(dgrad + (g - 1) * n), (int32_t)n, ZS_FP16, count,
+                       acc, (int32_t)g, master, m, v, half, &hp, 1, &sc, &ovf, &new_scale, 0);
+  } else {
+    float *master2, *m2, *v2;
+    void* half2;
+    CHECK(cudaMalloc((void**)&master2, count * 4) == cudaSuccess);
+    CHECK(cudaMalloc((void**)&m2, count * 4) == cudaSuccess);
+    CHECK(cudaMalloc((void**)&v2, count * 4) == cudaSuccess);
+    CHECK(cudaMalloc(&half2, count * 2) == cudaSuccess);
+    st = zs_shard_step_oop(ctx, (const void* const*)(dgrad + (g - 1) * n), (int32_t)n, ZS_FP16,
+                           count, acc, (int32_t)g, master, m, v, master2, m2, v2, half2, &hp, 1,
+                           &sc, &ovf, &new_scale, 0);
+    if (st == ZS_OK && ovf == 0) { /* the written set is now the state */
+      master = master2;
+      m = m2;
+      v = v2;
+      half = half2;
+    }
+  }
+  if (st != ZS_OK) fprintf(stderr, "step: %s\n", zs_last_error(ctx));
   CHECK(st == ZS_OK);
 
   float* out = (float*)malloc(count * 4);

@@ -1,6 +1,7 @@
 """The C ABI from plain C: tests/c_abi_main.c links libzeroshard.so and the
 CUDA runtime only (no Python, no torch), runs one step with cudaMalloc'ed
-buffers, and its output is compared with the oracle."""
+buffers (in place, or out of place with the caller swapping to the written
+set), and its output is compared with the oracle."""
 import os
 import subprocess
 
@@ -26,7 +27,8 @@ def build_c_caller(tmp_path):
     return exe
 
 
-def test_plain_c_caller_matches_oracle(tmp_path):
+@pytest.mark.parametrize("form", ["in_place", "oop"])
+def test_plain_c_caller_matches_oracle(tmp_path, form):
     exe = build_c_caller(tmp_path)
     rng = np.random.default_rng(77)
     count, n, g, scale = 50_003, 3, 2, 1024.0
@@ -40,7 +42,7 @@ def test_plain_c_caller_matches_oracle(tmp_path):
         fh.write(np.ascontiguousarray(grads).tobytes())
         fh.write(master0.tobytes())
     out = tmp_path / "out.bin"
-    subprocess.check_call([exe, str(inp), str(out)])
+    subprocess.check_call([exe, str(inp), str(out)] + (["oop"] if form == "oop" else []))
     raw = open(out, "rb").read()
     ovf = np.frombuffer(raw[:4], np.int32)[0]
     new_scale = np.frombuffer(raw[4:8], np.float32)[0]
