@@ -113,11 +113,14 @@ def step_launch_plan(n: int, g: int, dtype: str, acc_kind: str = "fp32", has_acc
 # ---------------------------------------------------------------- device workload
 
 class DeviceWorkload:
-    """HBM-resident buffers of one owned shard of a workload: G x N gradient
-    slices (half), the fp32 accumulator, fp32 master / m / v and the half copy."""
+    """HBM-resident buffers of one owned shard of a workload: the gradient
+    slices (half) of N ranks for each of `grad_buffers` micro-steps (None: all
+    G; micro-step k reads buffer k mod grad_buffers, as a training loop refills
+    one buffer while another is reduced), the fp32 accumulator, fp32 master /
+    m / v and the half copy."""
 
     def __init__(self, wl: synth.Workload, shard: int = 0, device=None, count: int | None = None,
-                 acc: str = "fp32", clip: float = 0.0):
+                 acc: str = "fp32", clip: float = 0.0, grad_buffers: int | None = None):
         import torch
         import zero_mixed_precision_shard_gb300 as zs
         self.zs = zs
@@ -128,7 +131,8 @@ class DeviceWorkload:
         self.begin, self.valid_end, _ = zs.zs_shard_range(self.part, shard)
         self.E = self.part.shard_len if count is None else count
         E, n, g = self.E, wl.n, wl.g
-        self.grads = torch.empty((g, n, E), dtype=torch.int16, device=self.dev)
+        self.nbuf = g if grad_buffers is None else max(1, min(g, grad_buffers))
+        self.grads = torch.empty((self.nbuf, n, E), dtype=torch.int16, device=self.dev)
         self.acc_kind = acc
         self.clip = clip
         if acc == "half":
@@ -152,26 +156,33 @@ class DeviceWorkload:
         return self.wl.dtype_code
 
     def slices(self, k: int):
+        """Host array of the N slice pointers micro-step k reads."""
         if not hasattr(self, "_ptr_arrays"):
             self._ptr_arrays = [self.zs.pointer_array(self.grads[j, r] for r in range(self.wl.n))
-                                for j in range(self.wl.g)]
-        return self._ptr_arrays[k]
+                                for j in range(self.nbuf)]
+        return self._ptr_arrays[k % self.nbuf]
 
     def slice_tensors(self, k: int):
-        return [self.grads[k, r] for r in range(self.wl.n)]
+        return [self.grads[k % self.nbuf, r] for r in range(self.wl.n)]
 
-    def fill_grads(self, step: int, scale: float, inject: bool = True):
+    def fill_micro(self, step: int, k: int, scale: float, inject: bool = True):
+        """Write micro-step k's gradients of `step` into the buffer it reads."""
         import torch
         s = torch.cuda.current_stream().cuda_stream
-        for k in range(self.wl.g):
-            for r in range(self.wl.n):
-                buf = self.grads[k, r]
+        for r in range(self.wl.n):
+            buf = self.grads[k % self.nbuf, r]
 
-                def writer(off, bits, buf=buf):
-                    buf[off] = int(np.array(bits, np.uint16).view(np.int16))
+            def writer(off, bits, buf=buf):
+                buf[off] = int(np.array(bits, np.uint16).view(np.int16))
 
-                synth.dev_fill_grads(buf.data_ptr(), self.E, self.begin, self.wl, step, k + 1, r,
-                                     scale, s, inject=inject, inject_writer=writer)
+            synth.dev_fill_grads(buf.data_ptr(), self.E, self.begin, self.wl, step, k + 1, r,
+                                 scale, s, inject=inject, inject_writer=writer)
+
+    def fill_grads(self, step: int, scale: float, inject: bool = True):
+        """Every buffer: micro-step b's values in buffer b (all G micro-steps when
+        each has its own buffer)."""
+        for k in range(self.nbuf):
+            self.fill_micro(step, k, scale, inject)
 
     def accum(self, ctx, k: int):
         """Micro-step k (< G-1) of a step through the C ABI."""
@@ -505,7 +516,17 @@ def resolve_api(args, world: int) -> str:
         return "graph"
     if args.acc == "half":
         return "sync"   # the half-accumulator step exists as a synchronising call
+    if args.api == "auto":   # decided once the workload's buffers are allocated
+        return "async" if args.clip else "auto"
     return args.api
+
+
+def oop_fits(E: int, margin: int = 4 << 30) -> bool:
+    """Whether the out-of-place step's second master/m/v/half set (14 bytes per
+    owned element) fits in the device memory still free."""
+    import torch
+    torch.cuda.synchronize()
+    return torch.cuda.mem_get_info()[0] > 14 * E + margin
 
 
 def make_step(zs, ctx, W: DeviceWorkload, api: str, clip: float = 0.0):
@@ -632,7 +653,7 @@ def measure_table_workload(zs, ctx, name: str, args, peak: float, dev: int):
     synchronising one (truncated like the headline workload under --elements)."""
     import torch
     wl = synth.WORKLOADS[name]
-    W = DeviceWorkload(wl, shard=0, count=args.elements)
+    W = DeviceWorkload(wl, shard=0, count=args.elements, grad_buffers=2)
     W.fill_grads(1, wl.scale0, inject=False)
     torch.cuda.synchronize()
     valid = min(W.valid_end - W.begin, W.E)
@@ -640,19 +661,22 @@ def measure_table_workload(zs, ctx, name: str, args, peak: float, dev: int):
     out = {"workload": name + (f" (first {W.E} elements)" if args.elements else ""),
            "params": wl.psi, "owned_params": valid, "shard_len": W.E, "n_ranks_simulated": wl.n,
            "accum_steps": wl.g, "grad_dtype": wl.dtype, "alg_bytes_per_step": step_bytes}
+    # these steps take 0.3-2.5 ms: at least 100 of them, so that one stall of the
+    # host (which the synchronising API waits on every step) cannot dominate
+    steps = max(args.steps, 100)
     for api in ("async", "async_oop", "sync"):
         one_step, state = make_step(zs, ctx, W, api)
         # the step rate without per-kernel events (an event pair around each of
         # a short step's launches costs it a few percent), then the same steps
         # again with them for the per-kernel rates
-        ms, launches, clocks = timed_steps(ctx, one_step, args.steps, args.warmup, dev, 1,
+        ms, launches, clocks = timed_steps(ctx, one_step, steps, args.warmup, dev, 1,
                                            kernel_timing=False)
-        timed_steps(ctx, one_step, args.steps, 0, dev, 1)
-        per_step = ms / args.steps
+        timed_steps(ctx, one_step, steps, 0, dev, 1)
+        per_step = ms / steps
         gbs = step_bytes / (per_step * 1e-3) / 1e9
         kinds = kernel_table(zs, ctx, W.launch_plan(oop=api == "async_oop"))
         out[api] = {"api": API_DESC[api], "value": valid / (per_step * 1e-3), "unit": "params/s",
-                    "ms_per_step": round(per_step, 4), "step_gbs": round(gbs, 1),
+                    "steps": steps, "ms_per_step": round(per_step, 6), "step_gbs": round(gbs, 1),
                     "step_frac_of_peak": round(gbs / peak, 4), "gpu_launches": launches,
                     "clocks": clocks,
                     "kernels": {k: {"gbs": round(d["gbs"], 1), "frac_of_peak":
@@ -884,10 +908,14 @@ def run_ours(args):
     if api == "async_oop" and (args.clip or args.acc != "fp32"):
         raise SystemExit("--api async_oop runs the unclipped fp32-accumulator step")
 
-    # with several GPUs, rank r owns shard r mod N (a ZeRO job's rank r owns shard r)
-    W = DeviceWorkload(wl, shard=rank % wl.n, count=args.elements, acc=args.acc, clip=args.clip)
+    # two gradient buffers alternate across the micro-steps (the split form reads
+    # every micro-step's slices in one call, so it keeps one buffer each)
+    W = DeviceWorkload(wl, shard=0, count=args.elements, acc=args.acc, clip=args.clip,
+                       grad_buffers=None if api == "split" else 2)
     W.fill_grads(1, wl.scale0, inject=False)
     torch.cuda.synchronize()
+    if api == "auto":
+        api = "async_oop" if oop_fits(W.E) else "async"
     E = W.E
     valid = min(W.valid_end - W.begin, E)
     one_step, state = make_step(zs, ctx, W, api, args.clip)
@@ -954,8 +982,13 @@ def run_ours(args):
 
     # the other target workloads, each with its own clock record (one GPU only)
     table = None
+    inputs_desc = ("gradients generated once on the device (step-1 values, no injections) and "
+                   "reused by every timed step; "
+                   + (f"{W.nbuf} gradient buffers alternate across the {wl.g} micro-steps, each "
+                      "micro-step reading its N slices from HBM" if W.nbuf < wl.g
+                      else "one gradient buffer per micro-step"))
     if (world == 1 and not args.skip_table and args.workload == DEFAULT_WORKLOAD
-            and api == "async" and not args.clip):
+            and args.api == "auto" and api in ("async", "async_oop") and not args.clip):
         del W, one_step, state
         torch.cuda.empty_cache()
         table = {name: measure_table_workload(zs, ctx, name, args, peak, dev)
@@ -988,8 +1021,7 @@ def run_ours(args):
                                                    "zs_shard_step_async_clipped")
                         if args.clip else API_DESC[api]),
                 "l2": "inputs larger than L2 (129 MB): no flush needed",
-                "inputs": "gradients generated once on the device (step-1 values, no "
-                          "injections) and reused by every timed step",
+                "inputs": inputs_desc,
                 "alg_bytes_per_step": step_bytes,
                 "step_gbs": round(step_bytes / (per_step_ms * 1e-3) / 1e9, 1),
                 "step_frac_of_peak": round(step_bytes / (per_step_ms * 1e-3) / 1e9 / peak, 4),
@@ -1025,39 +1057,47 @@ def run_e2e(zs, ctx, W: DeviceWorkload, steps: int, api: str = "sync", step_fn=N
     multi-GPU run takes it) instead waits for all G copies, then runs."""
     import torch
     wl = W.wl
+    nb = W.nbuf
     host = torch.empty((wl.n, W.E), dtype=torch.int16, pin_memory=True)
     host.copy_(W.grads[0])   # device -> pinned host directly (no pageable copy)
     copy_stream = torch.cuda.Stream()
     compute = torch.cuda.current_stream()
-    done = [torch.cuda.Event() for _ in range(wl.g)]
-    free = [torch.cuda.Event() for _ in range(wl.g)]
+    done = [torch.cuda.Event() for _ in range(nb)]   # buffer b filled
+    free = [torch.cuda.Event() for _ in range(nb)]   # buffer b consumed
     state = zs.DeviceState(W.scaler) if api in ("async", "async_oop", "graph") else None
     result = torch.empty(64, dtype=torch.uint8, pin_memory=True)
 
+    def copy_in(k):
+        b = k % nb
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(free[b])
+            W.grads[b].copy_(host, non_blocking=True)
+            done[b].record(copy_stream)
+        return b
+
     def step():
-        for k in range(wl.g):
-            with torch.cuda.stream(copy_stream):
-                copy_stream.wait_event(free[k])
-                W.grads[k].copy_(host, non_blocking=True)
-                done[k].record(copy_stream)
-        if step_fn is not None:
+        if step_fn is not None:   # every micro-step has its own buffer here
             for k in range(wl.g):
-                compute.wait_event(done[k])
+                copy_in(k)
+            for b in range(nb):
+                compute.wait_event(done[b])
             step_fn()
-            for k in range(wl.g):
-                free[k].record(compute)
+            for b in range(nb):
+                free[b].record(compute)
             return
-        for k in range(wl.g - 1):
-            compute.wait_event(done[k])
-            W.accum(ctx, k)
-            free[k].record(compute)
-        compute.wait_event(done[wl.g - 1])
-        if state is not None:
-            (W.finish_oop if api == "async_oop" else W.finish_async)(ctx, state)
-            result.copy_(state.buf, non_blocking=True)
-        else:
-            W.finish(ctx)
-        free[wl.g - 1].record(compute)
+        # micro-step k's copy waits only for the micro-step that last read its
+        # buffer, so it runs while the compute stream reduces micro-step k-1
+        for k in range(wl.g):
+            b = copy_in(k)
+            compute.wait_event(done[b])
+            if k < wl.g - 1:
+                W.accum(ctx, k)
+            elif state is not None:
+                (W.finish_oop if api == "async_oop" else W.finish_async)(ctx, state)
+                result.copy_(state.buf, non_blocking=True)
+            else:
+                W.finish(ctx)
+            free[b].record(compute)
 
     for e in free:
         e.record(compute)
@@ -1101,12 +1141,13 @@ def main(argv=None):
                     help="accumulator format (half: zs_*_halfacc entry points)")
     ap.add_argument("--clip", type=float, default=0.0,
                     help="global-norm gradient clipping at this max norm (zs_shard_step_clipped)")
-    ap.add_argument("--api", default="async", choices=["async", "async_oop", "sync"],
-                    help="async (default): zs_shard_step_async with the scale and step count on "
-                         "the device, no host round trip per step; async_oop: the same with the "
-                         "state written out of place (needs a second master/m/v/half set); "
-                         "sync: zs_shard_step, which returns the flag and scale to the host "
-                         "every step")
+    ap.add_argument("--api", default="auto", choices=["auto", "async", "async_oop", "sync"],
+                    help="auto (default): async_oop where its second state set fits in HBM, "
+                         "else async; async: zs_shard_step_async with the scale and step count "
+                         "on the device, no host round trip per step; async_oop: the same with "
+                         "the state written out of place (one pass for the last micro-step and "
+                         "the update); sync: zs_shard_step, which returns the flag and scale to "
+                         "the host every step")
     ap.add_argument("--skip-table", action="store_true",
                     help="skip the other target workloads measured after the headline one")
     ap.add_argument("--graph", action="store_true",

@@ -1,9 +1,10 @@
 """Full-size workloads, in the launch configuration the benchmark times
 (bench.DeviceWorkload: zs_grad_accum for micro-steps 1..G-1, then the last
-call: zs_shard_step, or zs_shard_step_async with the device-resident state as
-the benchmark's default API does), checked against the oracle on sampled
-elements, for the first shard and the last (which holds the padding where
-there is any, and the output layers).
+call: zs_shard_step, zs_shard_step_async with the device-resident state, or
+zs_shard_step_async_oop with the state written out of place, as the
+benchmark's default does where the second state set fits), checked against
+the oracle on sampled elements, for the first shard and the last (which holds
+the padding where there is any, and the output layers).
 
 The step is elementwise once the step's overflow flag is known, so the oracle
 replays every step on a sample of the owned shard: 2^16 seeded positions, the
@@ -58,21 +59,29 @@ def sample_positions(wl, begin, E, valid):
                                             ("gpt2-small-n8", 7, "sync"),
                                             ("decoder-1.3b-n16", 15, "sync"),
                                             ("llama7b-zero3-n64", 63, "sync"),
-                                            # the benchmark's default API
+                                            # the device-resident step, in place and
+                                            # out of place (the benchmark's default
+                                            # where the second state set fits)
                                             ("decoder-1.3b-n16", 0, "async"),
                                             ("llama7b-zero3-n64", 63, "async"),
-                                            ("llama7b-n1", 0, "async")])
+                                            ("llama7b-n1", 0, "async"),
+                                            ("decoder-1.3b-n16", 0, "async_oop"),
+                                            ("llama7b-zero3-n64", 63, "async_oop"),
+                                            ("llama7b-n1", 0, "async_oop")])
 def test_fullsize_sampled(name, shard, api):
     import bench
     import zero_mixed_precision_shard_gb300 as zs
     torch.cuda.set_device(0)
     wl = synth.WORKLOADS[name]
     steps = min(wl.steps, int(os.environ.get("ZS_FULLSIZE_STEPS", wl.steps)))
-    if api == "async" and name == "llama7b-n1":
+    if api != "sync" and name == "llama7b-n1":
         steps = min(steps, 10)   # to the state check after step 10; the sync case runs all 200
     ctx = zs.Ctx()
-    W = bench.DeviceWorkload(wl, shard=shard)
-    state = zs.DeviceState(W.scaler) if api == "async" else None
+    # the out-of-place case holds two gradient buffers, refilled micro-step by
+    # micro-step as a training loop does (the Llama-7B one: 243 GB with both
+    # state sets; one buffer per micro-step would not fit)
+    W = bench.DeviceWorkload(wl, shard=shard, grad_buffers=2 if api == "async_oop" else None)
+    state = zs.DeviceState(W.scaler) if api != "sync" else None
     E, begin = W.E, W.begin
     valid = W.valid_end - W.begin
     pos = sample_positions(wl, begin, E, valid)
@@ -84,8 +93,13 @@ def test_fullsize_sampled(name, shard, api):
     pos_d = torch.from_numpy(pos).cuda()
     flags = []
 
+    def current(k):
+        if api == "async_oop" and state.read().buf == 1:
+            return getattr(W, k + "2")
+        return getattr(W, k)
+
     def check_state(slack):
-        got = {k: getattr(W, k).index_select(0, pos_d).cpu().numpy()
+        got = {k: current(k).index_select(0, pos_d).cpu().numpy()
                for k in ("master", "m", "v", "half")}
         worst = 0.0
         for k in ("master", "m", "v"):
@@ -98,7 +112,8 @@ def test_fullsize_sampled(name, shard, api):
         return worst
 
     for s in range(1, steps + 1):
-        W.fill_grads(s, sc_o.scale, inject=True)
+        if api != "async_oop":
+            W.fill_grads(s, sc_o.scale, inject=True)
         grads = [[synth.host_grad_bits(wl, gidx, s, k + 1, r, sc_o.scale) for r in range(wl.n)]
                  for k in range(wl.g)]
         scheduled = any(begin <= j.index < begin + E for j in wl.injections_at(s))
@@ -108,7 +123,15 @@ def test_fullsize_sampled(name, shard, api):
             ovf = W.step(ctx)
             scale = W.scaler.scale
         else:
-            W.step_async_calls(ctx, state)
+            if api == "async_oop":
+                for k in range(wl.g):
+                    W.fill_micro(s, k, sc_o.scale, inject=True)
+                    if k < wl.g - 1:
+                        W.accum(ctx, k)
+                    else:
+                        W.finish_oop(ctx, state)
+            else:
+                W.step_async_calls(ctx, state)
             d = state.read()
             ovf, scale = d.overflow, d.scaler.scale
             assert d.step == t_o and d.iterations == s, f"step {s}"
@@ -129,7 +152,7 @@ def test_fullsize_sampled(name, shard, api):
               f"{check_state(4.0):.3f}")
     # padding stays zero
     if valid < E:
-        tail = W.master[valid:]
+        tail = current("master")[valid:]
         assert torch.count_nonzero(tail).item() == 0
     ctx.close()
     del W
