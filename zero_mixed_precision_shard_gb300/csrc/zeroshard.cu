@@ -379,10 +379,13 @@ zs::AdamArgs adam_args(const zs_adam_hparams* hp, int64_t step, float grad_div) 
   const double t = (double)step;
   const double ib1 = 1.0 / (1.0 - std::pow((double)hp->beta1, t));
   const double ib2 = 1.0 / (1.0 - std::pow((double)hp->beta2, t));
+  const double sb2 = std::sqrt(ib2);
   a.inv_bc1 = (float)ib1;
   a.inv_bc2 = (float)ib2;
   a.inv_bc1_lo = (float)(ib1 - (double)a.inv_bc1);
   a.inv_bc2_lo = (float)(ib2 - (double)a.inv_bc2);
+  a.sbc2 = (float)sb2;
+  a.sbc2_lo = (float)(sb2 - (double)a.sbc2);
   a.grad_div = grad_div;
   return a;
 }

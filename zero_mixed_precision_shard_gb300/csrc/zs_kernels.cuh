@@ -136,11 +136,12 @@ struct SlicePtrs {
 
 // Per-launch constants of the AdamW update, computed on the host once per
 // call (bias corrections in double, rounded to fp32).
-// The bias corrections 1/(1-beta^t) are carried as fp32 pairs (hi + lo) so
-// that their rounding does not bias every element of a step the same way.
+// The bias corrections 1/(1-beta1^t), 1/(1-beta2^t) and its square root are
+// carried as fp32 pairs (hi + lo) so that their rounding does not bias every
+// element of a step the same way.
 struct AdamArgs {
   float lr, beta1, omb1, beta2, omb2, eps, wd, inv_bc1, inv_bc2, grad_div;
-  float inv_bc1_lo, inv_bc2_lo;
+  float inv_bc1_lo, inv_bc2_lo, sbc2, sbc2_lo;
 };
 
 // Result of the loss-scale update, written by one thread of the update kernel.
@@ -384,14 +385,33 @@ __device__ __forceinline__ void adamw1(const AdamArgs& ad, float sum, float& p, 
   float g = __fdiv_rn(sum, ad.grad_div);
   if constexpr (CLIP) g = __fmul_rn(g, coef);
   m = __fmaf_rn(ad.beta1, m, __fmul_rn(ad.omb1, g));
-  v = __fmaf_rn(ad.beta2, v, __fmul_rn(ad.omb2, __fmul_rn(g, g)));
+  const float v_old = v;
+  v = __fmaf_rn(ad.beta2, v_old, __fmul_rn(ad.omb2, __fmul_rn(g, g)));
   const float m_hat = __fmaf_rn(m, ad.inv_bc1, __fmul_rn(m, ad.inv_bc1_lo));
   const float v_hat = __fmaf_rn(v, ad.inv_bc2, __fmul_rn(v, ad.inv_bc2_lo));
-  float upd = __fdiv_rn(m_hat, __fadd_rn(__fsqrt_rn(v_hat), ad.eps));
-  // A finite bf16 gradient beyond ~1.8e19 in magnitude squares past the fp32
-  // maximum: v (or v_hat) becomes +inf and the Adam term 0, as in any fp32
-  // Adam; at ~3.4e38 m_hat overflows too and inf/inf would write a NaN into
-  // the weights -- that term is taken as 0 as well.
+  float root = __fsqrt_rn(v_hat);
+  if (!(root <= 3.402823466e38f)) {
+    // +inf, or NaN where v is +inf and the low part of 1/(1-beta2^t) is
+    // negative.  Only bf16 gradients reach here (|g| from ~1.8e19 on).  g*g may have
+    // passed the fp32 maximum where (1-beta2)*g*g does not: form v with
+    // (1-beta2)*g first.  v_hat passes the maximum up to 1000x (t = 1) before
+    // v does: take sqrt(v_hat) as sqrt(v) * sqrt(1/(1-beta2^t)).  And where
+    // the new v itself is +inf (the state keeps it so, as the fp64 definition
+    // rounded to fp32 does) this step's root is still finite:
+    // sqrt(beta2*v_old + (1-beta2)*g^2) = |g| * sqrt(beta2*(v_old/g)/g + (1-beta2))
+    v = __fmaf_rn(ad.beta2, v_old, __fmul_rn(__fmul_rn(ad.omb2, g), g));
+    float sv = __fsqrt_rn(v);
+    if (sv == __int_as_float(0x7f800000) && g != 0.0f)
+      sv = __fmul_rn(fabsf(g), __fsqrt_rn(__fmaf_rn(ad.beta2,
+                                                    __fdiv_rn(__fdiv_rn(v_old, g), g),
+                                                    ad.omb2)));
+    // (v_old = +inf leaves the root +inf: no inf*lo term)
+    root = sv <= 3.402823466e38f ? __fmaf_rn(sv, ad.sbc2, __fmul_rn(sv, ad.sbc2_lo)) : sv;
+  }
+  float upd = __fdiv_rn(m_hat, __fadd_rn(root, ad.eps));
+  // once v is +inf the Adam term is m_hat / inf = 0 (decay alone moves the
+  // weight, as the fp64 definition does); a NaN from inf/inf would only arise
+  // past every finite input and is taken as 0
   if (upd != upd) upd = 0.0f;
   p = __fmaf_rn(-ad.lr, __fmaf_rn(ad.wd, p, upd), p);
 }
@@ -469,10 +489,13 @@ __global__ void k_step_prologue(const zs_device_state* __restrict__ st, int n, i
   a.wd = hp.weight_decay;
   const double ib1 = 1.0 / (1.0 - pow((double)hp.beta1, (double)t));
   const double ib2 = 1.0 / (1.0 - pow((double)hp.beta2, (double)t));
+  const double sb2 = sqrt(ib2);
   a.inv_bc1 = (float)ib1;
   a.inv_bc2 = (float)ib2;
   a.inv_bc1_lo = (float)(ib1 - (double)a.inv_bc1);
   a.inv_bc2_lo = (float)(ib2 - (double)a.inv_bc2);
+  a.sbc2 = (float)sb2;
+  a.sbc2_lo = (float)(sb2 - (double)a.sbc2);
   a.grad_div = (float)((double)n * (double)accum_steps * (double)st->scaler.scale);
   *out = a;
 }
