@@ -71,15 +71,24 @@ def kernel_alg_bytes(kind: str, n: int, first: bool = False, with_acc: bool = Fa
         return (4 if with_acc else 0) + (2 * n if first else 0)
     if kind == "update_oop":   # last micro-step + flag + update, state written out of place
         return (4 if with_acc else 0) + 2 * n + 26
+    if kind == "fused":   # last micro-step + flag + grid barrier + update, one kernel
+        return (4 if with_acc else 0) + 2 * n + 26
     raise ValueError(kind)
 
 
 def step_launch_plan(n: int, g: int, dtype: str, acc_kind: str = "fp32", has_acc: bool = True,
-                     clip: float = 0.0, split: bool = False, oop: bool = False):
+                     clip: float = 0.0, split: bool = False, oop: bool = False,
+                     fused: bool = False):
     """(kind, alg bytes per element) of every kernel one step launches, in the
     order the step launches them (split: the step split at the overflow flag
     as every rank of a multi-GPU run does, the clipping norm in its own pass;
-    oop: the out-of-place step, whose last pass is the update)."""
+    oop: the out-of-place step, whose last pass is the update; fused: the
+    shard fits the fused step, whose last call is one kernel in every form)."""
+    if fused:
+        plan = [("reduce_first" if k == 0 else "reduce",
+                 kernel_alg_bytes("reduce", n, first=(k == 0))) for k in range(g - 1)]
+        plan.append(("fused", kernel_alg_bytes("fused", n, with_acc=g > 1)))
+        return plan
     if oop:
         plan = [("reduce_first" if k == 0 else "reduce",
                  kernel_alg_bytes("reduce", n, first=(k == 0))) for k in range(g - 1)]
@@ -242,10 +251,18 @@ class DeviceWorkload:
             zs.zs_shard_step_async(ctx, self.slices(wl.g - 1), self.dt, self.E, self.acc, wl.g,
                                    self.master, self.m, self.v, self.half, self.hp, None, state)
 
-    def launch_plan(self, split: bool = False, oop: bool = False):
+    def launch_plan(self, split: bool = False, oop: bool = False, fused: bool = False):
         """(kind, alg bytes per element) of every kernel one step launches."""
         return step_launch_plan(self.wl.n, self.wl.g, self.wl.dtype, self.acc_kind,
-                                self.acc is not None, self.clip, split, oop)
+                                self.acc is not None, self.clip, split, oop, fused)
+
+    def takes_fused(self, ctx, api: str) -> bool:
+        """Whether `api`'s last call runs as the fused single-kernel step here:
+        the unclipped fp32-accumulator forms, when the shard fits one
+        co-resident grid (and the context has the fused step on)."""
+        return (api in ("async", "async_oop", "graph", "sync") and self.acc_kind == "fp32"
+                and not self.clip and self.E <= ctx.fused_capacity
+                and os.environ.get("ZEROSHARD_FUSED", "1") != "0")
 
     def step_oop_calls(self, ctx, state):
         """One step of the device-resident out-of-place form."""
@@ -506,7 +523,7 @@ API_DESC = {
     "split": "zs_reduce_check / zs_check_last + zs_apply + zs_scaler_update (split at the flag)",
 }
 # the other target workloads, measured in the same run after the headline one
-TABLE_WORKLOADS = ("decoder-1.3b-n16", "llama7b-zero3-n64", "gpt2-small-n8")
+TABLE_WORKLOADS = ("decoder-1.3b-n16", "llama7b-zero3-n64", "gpt2-small-n8", "flat-1m-n2")
 
 
 def resolve_api(args, world: int) -> str:
@@ -674,7 +691,8 @@ def measure_table_workload(zs, ctx, name: str, args, peak: float, dev: int):
         timed_steps(ctx, one_step, steps, 0, dev, 1)
         per_step = ms / steps
         gbs = step_bytes / (per_step * 1e-3) / 1e9
-        kinds = kernel_table(zs, ctx, W.launch_plan(oop=api == "async_oop"))
+        kinds = kernel_table(zs, ctx, W.launch_plan(oop=api == "async_oop",
+                                                    fused=W.takes_fused(ctx, api)))
         out[api] = {"api": API_DESC[api], "value": valid / (per_step * 1e-3), "unit": "params/s",
                     "steps": steps, "ms_per_step": round(per_step, 6), "step_gbs": round(gbs, 1),
                     "step_frac_of_peak": round(gbs / peak, 4), "gpu_launches": launches,
@@ -920,11 +938,14 @@ def run_ours(args):
     valid = min(W.valid_end - W.begin, E)
     one_step, state = make_step(zs, ctx, W, api, args.clip)
     ms, launches, clock_summary = timed_steps(ctx, one_step, args.steps, args.warmup, dev, world)
-    plan = W.launch_plan(split=api == "split", oop=api == "async_oop")
+    fused = W.takes_fused(ctx, api)
+    plan = W.launch_plan(split=api == "split", oop=api == "async_oop", fused=fused)
     if api == "graph":  # replays bypass the context's counter: the kernels of a captured step
         # (the streaming ones, the prologue and the flag reset; with clipping the
-        # norm's finalize and the coefficient, and the fold of many partials)
-        extra = 2 + (2 + (1 if W.E // (8 * 256) > 4096 else 0) if args.clip else 0)
+        # norm's finalize and the coefficient, and the fold of many partials;
+        # the fused step is one kernel)
+        extra = 0 if fused else 2 + (2 + (1 if W.E // (8 * 256) > 4096 else 0) if args.clip
+                                     else 0)
         launches = args.steps * (len(plan) + extra)
     dstate = None
     if state is not None:

@@ -73,7 +73,7 @@ typedef enum {
   ZS_ERR_ALIGN = -2,   /* a device pointer not 16-byte aligned */
   ZS_ERR_DTYPE = -3,   /* dtype is neither ZS_FP16 nor ZS_BF16 */
   ZS_ERR_CUDA = -4,    /* a CUDA runtime error (message in zs_last_error) */
-  ZS_ERR_TIMEOUT = -5, /* reserved: a bounded device wait gave up */
+  ZS_ERR_TIMEOUT = -5, /* a bounded device wait gave up (the fused step's barrier) */
   ZS_ERR_LIMIT = -6    /* count beyond ZS_NOALLOC_MAX_COUNT (zs_grad_sumsq_noalloc) */
 } zs_status;
 
@@ -140,10 +140,41 @@ zs_status zs_scaler_init(zs_scaler* s, float scale, float min_scale, int32_t win
  * host memory (the update kernel writes the step's flag and new scale there;
  * the synchronising calls read it after the stream sync, with no copy), 8 MB
  * of scratch for the clipping norm's per-CTA partial sums (sized here, so no
- * later call allocates device memory), and a pinned mirror of the norm.
+ * later call allocates device memory), a pinned mirror of the norm, and the
+ * fused step's grid barrier (16 device bytes) with its timeout word (mapped
+ * pinned).  Environment: ZEROSHARD_PDL=0 launches the step's kernels without
+ * programmatic dependent launch; ZEROSHARD_FUSED=0 starts the context with
+ * the fused step off (zs_ctx_set_fused).
  * *ctx is set to NULL on failure. */
 zs_status zs_ctx_create(zs_ctx** ctx);
 zs_status zs_ctx_destroy(zs_ctx* ctx);
+
+/* The fused step (§2.2, §4.2: the step's overflow resolved before any state
+ * is written, here by a grid barrier inside one kernel).
+ * zs_shard_step, zs_shard_step_async, zs_shard_step_oop and
+ * zs_shard_step_async_oop (not the clipped forms) run the whole last call of
+ * a step as ONE cooperative kernel when one thread per 8 owned elements fits a
+ * grid whose CTAs are all resident at once (on GB300 about 1.2M elements):
+ * each thread loads its elements' last micro-step sums (acc + the n slices, in
+ * the order zs_grad_accum adds them) and their state into registers, the grid
+ * ORs the overflow flag, one grid barrier resolves it, and a clean step
+ * applies the same AdamW arithmetic from the registers; an overflow writes no
+ * state.  Results are bit for bit those of the multi-kernel path.  The barrier
+ * wait is bounded: a CTA that waits longer than wait_ns gives up and writes
+ * nothing, and the context's next call (the synchronising forms: the call
+ * itself) returns ZS_ERR_TIMEOUT after resetting the barrier and the flag;
+ * the state of that step is then undefined.
+ * mode: ZS_FUSED_OFF (always the multi-kernel path), ZS_FUSED_ON (default),
+ * ZS_FUSED_TEST_TIMEOUT (as ON, but the barrier waits for one CTA more than
+ * the grid has, so every fused step's wait runs out: for testing the timeout
+ * path).  wait_ns <= 0 keeps the default of one second. */
+#define ZS_FUSED_OFF 0
+#define ZS_FUSED_ON 1
+#define ZS_FUSED_TEST_TIMEOUT 2
+zs_status zs_ctx_set_fused(zs_ctx* ctx, int32_t mode, int64_t wait_ns);
+/* The largest count the fused step takes on this context's device (any
+ * dtype, accumulator or form); larger shards take the multi-kernel path. */
+zs_status zs_ctx_fused_capacity(zs_ctx* ctx, int64_t* elements);
 /* Message of the last failed call on ctx ("" if none).  Valid until the next call. */
 const char* zs_last_error(const zs_ctx* ctx);
 /* Device address of the context's step overflow flag: zs_grad_accum ORs into
@@ -213,10 +244,13 @@ zs_status zs_scaler_update(zs_ctx* ctx, const int32_t* d_flag, zs_scaler* scaler
  * state, applies AdamW with grad_div = n * accum_steps * scaler->scale,
  * updates *scaler, writes *overflow_out and *new_scale_out (either may be
  * NULL), clears the context flag and synchronises `stream`.
- * acc may be NULL only when accum_steps == 1.  When n < 4 (or acc is NULL)
- * the last slices are checked, then re-read by the update (2n bytes per
- * element) instead of summed into acc and read back (8 bytes per element).
- * The caller advances `step` only if *overflow_out == 0. */
+ * acc may be NULL only when accum_steps == 1.  A shard that fits the fused
+ * step (zs_ctx_set_fused) takes it: one kernel, the sums held in registers
+ * across a grid barrier, acc read (accum_steps > 1) and never written.
+ * Otherwise, when n < 4 (or acc is NULL) the last slices are checked, then
+ * re-read by the update (2n bytes per element) instead of summed into acc and
+ * read back (8 bytes per element).  Either way acc holds no defined sums
+ * afterwards.  The caller advances `step` only if *overflow_out == 0. */
 zs_status zs_shard_step(zs_ctx* ctx, const void* const* grads, int32_t n, zs_dtype dt,
                         int64_t count, float* acc, int32_t accum_steps, float* master, float* m,
                         float* v, void* half_out, const zs_adam_hparams* hp, int64_t step,
@@ -399,8 +433,9 @@ zs_status zs_shard_step_async_clipped(zs_ctx* ctx, const void* const* grads, int
  * current master/m/v and writes the new values into a second set of buffers;
  * after that pass the step's flag is complete, and only a clean step makes
  * the written set current -- an overflowing step leaves the current set
- * untouched and its written set is garbage, so the skip semantics are those
- * of zs_shard_step.  Nothing is written twice: per element the step moves
+ * untouched and its written set is garbage (the fused step, for shards that
+ * fit it, writes nothing on an overflow), so the skip semantics are those of
+ * zs_shard_step.  Nothing is written twice: per element the step moves
  * exactly the algorithmic bytes (2*n*G + 8*(G-1) + 26), against + 8 (the
  * accumulator written and read back) or + 2*n (the last slices read twice) for
  * zs_shard_step, at the cost of a second master/m/v/half set (14 bytes per
@@ -496,7 +531,8 @@ typedef enum {
   ZS_KERNEL_SUMSQ = 6,           /* clipping: sum of squares (+ its finalize) */
   ZS_KERNEL_REDUCE_FIRST = 7,    /* first micro-step: sum of n slices into acc (+ flag) */
   ZS_KERNEL_UPDATE_OOP = 8,      /* out-of-place step: last micro-step + flag + update */
-  ZS_KERNEL_KINDS = 9
+  ZS_KERNEL_FUSED = 9,           /* fused step: last micro-step + flag + barrier + update */
+  ZS_KERNEL_KINDS = 10
 } zs_kernel_kind;
 
 /* When enabled, each launch is bracketed by CUDA events on its stream. */

@@ -116,3 +116,14 @@ def test_out_of_place_plan_moves_exactly_the_algorithmic_bytes():
         plan = bench.step_launch_plan(wl.n, wl.g, wl.dtype, oop=True)
         assert [k for k, _ in plan][-1] == "update_oop"
         assert sum(b for _, b in plan) == bench.alg_bytes_per_elem_step(wl.n, wl.g)
+
+
+def test_fused_plan_moves_exactly_the_algorithmic_bytes():
+    """The fused step (shards that fit one co-resident grid): the carried
+    micro-steps, then one kernel; nothing is read twice or written twice."""
+    for name in ("flat-1m-n2", "gpt2-small-n8", "decoder-1.3b-n16"):
+        wl = synth.WORKLOADS[name]
+        plan = bench.step_launch_plan(wl.n, wl.g, wl.dtype, fused=True)
+        assert [k for k, _ in plan] == ["reduce_first"] * (wl.g > 1) + ["reduce"] * max(
+            0, wl.g - 2) + ["fused"]
+        assert sum(b for _, b in plan) == bench.alg_bytes_per_elem_step(wl.n, wl.g)

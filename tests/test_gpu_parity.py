@@ -23,9 +23,12 @@ def zs():
     return pkg
 
 
-@pytest.fixture(scope="module")
-def ctx(zs):
+@pytest.fixture(scope="module", params=["fused", "multi"])
+def ctx(zs, request):
+    """Every test runs with the fused single-kernel step (where the shard fits
+    one co-resident grid) and with the multi-kernel path."""
     c = zs.Ctx()
+    c.set_fused(zs.ZS_FUSED_ON if request.param == "fused" else zs.ZS_FUSED_OFF)
     yield c
     c.close()
 
@@ -536,3 +539,29 @@ def test_two_contexts_on_two_streams(zs):
     for a, b in zip(o1, o2):
         for x, y in zip(a, b):
             assert torch.equal(x, y)
+
+
+def test_timing_skips_launches_captured_into_a_graph(zs):
+    """With timing on, a launch captured into a CUDA graph records no events
+    (they would be timed once per capture, and could not be waited on after
+    the graph is gone): the counters hold the uncaptured launches only and stay
+    readable after the graph is destroyed."""
+    ctx = zs.Ctx()
+    ctx.set_timing(True)
+    count = 4096
+    g = [torch.zeros(count, dtype=torch.int16, device="cuda")]
+    acc = torch.zeros(count, dtype=torch.float32, device="cuda")
+    zs.zs_grad_accum(ctx, g, FP16, count, acc, True)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        zs.zs_grad_accum(ctx, g, FP16, count, acc, False)
+    graph.replay()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert ctx.timing(zs.ZS_KERNEL_REDUCE_FIRST)[1] == 1
+    assert ctx.timing(zs.ZS_KERNEL_REDUCE)[1] == 0
+    del graph
+    zs.zs_grad_accum(ctx, g, FP16, count, acc, False)
+    assert ctx.timing(zs.ZS_KERNEL_REDUCE)[1] == 1
+    ctx.close()

@@ -21,9 +21,11 @@ ZS_FP16, ZS_BF16 = 0, 1
 ZS_MAX_RANKS = 256
 ZS_DEFAULT_ALIGN = 64
 (ZS_KERNEL_REDUCE, ZS_KERNEL_CHECK, ZS_KERNEL_APPLY, ZS_KERNEL_APPLY_RECOMPUTE, ZS_KERNEL_SCALER,
- ZS_KERNEL_COPY, ZS_KERNEL_SUMSQ, ZS_KERNEL_REDUCE_FIRST, ZS_KERNEL_UPDATE_OOP) = range(9)
+ ZS_KERNEL_COPY, ZS_KERNEL_SUMSQ, ZS_KERNEL_REDUCE_FIRST, ZS_KERNEL_UPDATE_OOP,
+ ZS_KERNEL_FUSED) = range(10)
 KERNEL_NAMES = ["reduce", "check", "apply", "apply_recompute", "scaler", "copy", "sumsq",
-                "reduce_first", "update_oop"]
+                "reduce_first", "update_oop", "fused"]
+ZS_FUSED_OFF, ZS_FUSED_ON, ZS_FUSED_TEST_TIMEOUT = 0, 1, 2
 _STATUS = {0: "ZS_OK", -1: "ZS_ERR_ARG", -2: "ZS_ERR_ALIGN", -3: "ZS_ERR_DTYPE", -4: "ZS_ERR_CUDA",
            -5: "ZS_ERR_TIMEOUT", -6: "ZS_ERR_LIMIT"}
 
@@ -135,6 +137,8 @@ def _load():
                                   f32, i32p, ctypes.POINTER(ctypes.c_float),
                                   ctypes.POINTER(ctypes.c_float), vp],
         "zs_ctx_set_timing": [vp, i32],
+        "zs_ctx_set_fused": [vp, i32, i64],
+        "zs_ctx_fused_capacity": [vp, i64p],
         "zs_ctx_timing": [vp, i32, ctypes.POINTER(ctypes.c_double), i64p, i64p],
         "zs_ctx_timing_reset": [vp],
         "zs_ctx_launch_count": [vp, i64p],
@@ -226,6 +230,17 @@ class Ctx:
 
     def set_timing(self, enable: bool):
         self.check(lib.zs_ctx_set_timing(self.handle, 1 if enable else 0))
+
+    def set_fused(self, mode: int, wait_ns: int = 0):
+        """ZS_FUSED_OFF / ZS_FUSED_ON / ZS_FUSED_TEST_TIMEOUT; wait_ns <= 0: the default."""
+        self.check(lib.zs_ctx_set_fused(self.handle, mode, wait_ns))
+
+    @property
+    def fused_capacity(self) -> int:
+        """The largest count the fused step takes on this device."""
+        n = ctypes.c_int64()
+        self.check(lib.zs_ctx_fused_capacity(self.handle, ctypes.byref(n)))
+        return n.value
 
     def timing(self, kind: int):
         ms, n, el = ctypes.c_double(), ctypes.c_int64(), ctypes.c_int64()

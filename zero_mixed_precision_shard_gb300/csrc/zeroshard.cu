@@ -4,6 +4,7 @@
 // the kernels of zs_kernels.cuh.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -37,6 +38,10 @@
 #define ZS_ACC_KEEP_MAX_BYTES (64ll << 20)
 #endif
 
+// How long a CTA of the fused step waits at its grid barrier before it gives
+// up (the wait normally lasts microseconds: every CTA is co-resident).
+#define ZS_DEFAULT_WAIT_NS 1000000000ull
+
 static inline uint32_t acc_keep_for(int64_t count) {
   return count * 4 <= ZS_ACC_KEEP_MAX_BYTES ? 1u : 0u;
 }
@@ -56,6 +61,13 @@ struct zs_ctx {
   // synchronising calls read it after the stream sync without a copy
   zs::StepResult* d_result = nullptr;
   zs::StepResult* h_result = nullptr;
+  // the fused step: its grid barrier, and a mapped pinned word that a fused
+  // step whose bounded wait ran out sets (d_fused_err is its device address)
+  zs::FusedSync* d_sync = nullptr;
+  int32_t* h_fused_err = nullptr;
+  int32_t* d_fused_err = nullptr;
+  int32_t fused_mode = ZS_FUSED_ON;
+  uint64_t wait_ns = ZS_DEFAULT_WAIT_NS;
   std::string err;
   std::unordered_map<const void*, int> occupancy;  // resident CTAs per SM, per kernel
   int64_t launches = 0;
@@ -132,7 +144,20 @@ void fold_finished(zs_ctx* c) {
   c->pending.resize(keep);
 }
 
-// Bracket one launch with events when timing is on.
+// Whether `s` is capturing into a graph (also when the query itself fails,
+// e.g. on the legacy stream while another stream captures).
+bool stream_capturing(cudaStream_t s) {
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return true;
+  }
+  return cap != cudaStreamCaptureStatusNone;
+}
+
+// Bracket one launch with events when timing is on -- never on a capturing
+// stream: an event recorded into a graph would be timed once per capture, not
+// per replay, and could not be waited on once the graph is gone.
 struct LaunchScope {
   zs_ctx* c;
   cudaStream_t s;
@@ -141,7 +166,7 @@ struct LaunchScope {
   cudaEvent_t start = nullptr;
   LaunchScope(zs_ctx* c_, cudaStream_t s_, int kind_, int64_t el)
       : c(c_), s(s_), kind(kind_), elements(el) {
-    if (c->timing) {
+    if (c->timing && !stream_capturing(s)) {
       start = take_event(c);
       if (start) cudaEventRecord(start, s);
     }
@@ -183,21 +208,24 @@ void launch_k(zs_ctx* c, void (*kernel)(KArgs...), int grid, int block, cudaStre
   (void)cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Resident CTAs per SM of `kernel` at kThreads threads (cached per kernel).
 template <typename K>
-int grid_for(zs_ctx* c, K kernel, int64_t items, int waves = ZS_GRID_WAVES) {
+int resident_ctas(zs_ctx* c, K kernel) {
   const void* key = reinterpret_cast<const void*>(kernel);
   auto it = c->occupancy.find(key);
-  int per_sm;
-  if (it == c->occupancy.end()) {
-    per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, zs::kThreads, 0) !=
-            cudaSuccess ||
-        per_sm < 1)
-      per_sm = 1;
-    c->occupancy.emplace(key, per_sm);
-  } else {
-    per_sm = it->second;
-  }
+  if (it != c->occupancy.end()) return it->second;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, zs::kThreads, 0) !=
+          cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  c->occupancy.emplace(key, per_sm);
+  return per_sm;
+}
+
+template <typename K>
+int grid_for(zs_ctx* c, K kernel, int64_t items, int waves = ZS_GRID_WAVES) {
+  const int per_sm = resident_ctas(c, kernel);
   int64_t need = (items + zs::kThreads - 1) / zs::kThreads;
   if (need < 1) need = 1;
   if (waves > 0) {
@@ -206,6 +234,26 @@ int grid_for(zs_ctx* c, K kernel, int64_t items, int waves = ZS_GRID_WAVES) {
   }
   if (need > 0x7fffffff) need = 0x7fffffff;
   return (int)need;
+}
+
+// A fused step of this context gave up its bounded grid wait: that step's
+// state is undefined.  Once the device is idle the barrier and the step's flag
+// are reset, so the context stays usable; the call reports ZS_ERR_TIMEOUT.
+zs_status fused_timeout(zs_ctx* c) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemset(c->d_sync, 0, sizeof(zs::FusedSync));
+  if (e == cudaSuccess) e = cudaMemset(c->d_flag, 0, sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  *reinterpret_cast<volatile int32_t*>(c->h_fused_err) = 0;
+  if (e != cudaSuccess) return cuda_fail(c, e, "reset after a fused-step timeout");
+  return fail(c, ZS_ERR_TIMEOUT,
+              "a fused step's grid barrier wait ran out (limit %llu ns): that step wrote at most "
+              "part of the state; the barrier and the flag have been reset",
+              (unsigned long long)c->wait_ns);
+}
+
+bool fused_timed_out(const zs_ctx* c) {
+  return c->h_fused_err != nullptr && *reinterpret_cast<volatile int32_t*>(c->h_fused_err) != 0;
 }
 
 zs_status check_ctx(zs_ctx* c) {
@@ -217,6 +265,7 @@ zs_status check_ctx(zs_ctx* c) {
     return fail(c, ZS_ERR_ARG, "current device %d is not the context's device %d", dev,
                 c->device);
   c->err.clear();
+  if (fused_timed_out(c)) return fused_timeout(c);
   return ZS_OK;
 }
 
@@ -368,26 +417,7 @@ zs_status reduce_any(zs_ctx* c, zs_dtype dt, const zs::SlicePtrs& sp, int32_t n,
 }
 
 zs::AdamArgs adam_args(const zs_adam_hparams* hp, int64_t step, float grad_div) {
-  zs::AdamArgs a;
-  a.lr = hp->lr;
-  a.beta1 = hp->beta1;
-  a.omb1 = 1.0f - hp->beta1;
-  a.beta2 = hp->beta2;
-  a.omb2 = 1.0f - hp->beta2;
-  a.eps = hp->eps;
-  a.wd = hp->weight_decay;
-  const double t = (double)step;
-  const double ib1 = 1.0 / (1.0 - std::pow((double)hp->beta1, t));
-  const double ib2 = 1.0 / (1.0 - std::pow((double)hp->beta2, t));
-  const double sb2 = std::sqrt(ib2);
-  a.inv_bc1 = (float)ib1;
-  a.inv_bc2 = (float)ib2;
-  a.inv_bc1_lo = (float)(ib1 - (double)a.inv_bc1);
-  a.inv_bc2_lo = (float)(ib2 - (double)a.inv_bc2);
-  a.sbc2 = (float)sb2;
-  a.sbc2_lo = (float)(sb2 - (double)a.sbc2);
-  a.grad_div = grad_div;
-  return a;
+  return zs::make_adam_args(hp->lr, *hp, step, grad_div);
 }
 
 template <int DT, bool HA, bool RC>
@@ -528,6 +558,16 @@ zs_status finish_step(zs_ctx* c, zs_scaler* scaler, int32_t* overflow_out, float
   return ZS_OK;
 }
 
+// finish_step after a fused step: its bounded wait may have run out, in
+// which case the loss-scale result was not written.
+zs_status finish_fused_step(zs_ctx* c, zs_scaler* scaler, int32_t* overflow_out,
+                            float* new_scale_out, cudaStream_t s) {
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(c, e, "step synchronisation");
+  if (fused_timed_out(c)) return fused_timeout(c);
+  return finish_step(c, scaler, overflow_out, new_scale_out, nullptr, s);
+}
+
 template <int DT, bool HA, bool RC, bool CLIP>
 void launch_apply_dev_k(zs_ctx* c, const int32_t* flag, const zs::SlicePtrs& sp, int32_t n,
                         const float* acc, int64_t count, float* master, float* m, float* v,
@@ -603,6 +643,97 @@ zs_status update_oop(zs_ctx* c, zs_dtype dt, const zs::SlicePtrs& sp, int32_t n,
   if (e != cudaSuccess) return cuda_fail(c, e, "out-of-place update launch");
   if (count > 0) ls.done();
   return ZS_OK;
+}
+
+// A cooperative launch (every CTA co-resident, or the launch fails), without
+// the programmatic-dependent attribute: the kernel starts once its predecessor
+// in the stream has completed.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_coop(void (*kernel)(KArgs...), int grid, cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)zs::kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// The arguments of one fused step (k_step_fused) besides the kernel choice.
+struct FusedCall {
+  zs::SlicePtrs sp;
+  int32_t n = 0;
+  const float* acc = nullptr;  // the carried micro-steps' sums, or NULL (accum_steps == 1)
+  zs::OopBufs b{};             // in place: both entries of each pair equal
+  int64_t count = 0;
+  zs::AdamArgs ad{};           // host constants (not DEV)
+  zs_scaler scaler{};          // scaler before the step (not DEV)
+  zs_device_state* dstate = nullptr;
+  zs_adam_hparams hp{};
+  zs_lr_schedule sched{};
+  int32_t has_sched = 0;
+  int32_t accum_steps = 1;
+};
+
+template <int DT, bool HA, bool DEV, bool FLIP>
+int fused_launch_k(zs_ctx* c, const FusedCall& f, cudaStream_t s, cudaError_t* e) {
+  auto k = zs::k_step_fused<DT, HA, DEV, FLIP>;
+  const int64_t per_grid = (int64_t)resident_ctas(c, k) * c->sms;
+  int64_t grid = ((f.count >> 3) + zs::kThreads - 1) / zs::kThreads;
+  if (grid < 1) grid = 1;
+  if (grid > per_grid) return 0;
+  // ZS_FUSED_TEST_TIMEOUT: the barrier waits for one CTA more than the grid has
+  const unsigned expect = (unsigned)grid + (c->fused_mode == ZS_FUSED_TEST_TIMEOUT ? 1u : 0u);
+  LaunchScope ls(c, s, ZS_KERNEL_FUSED, f.count);
+  *e = launch_coop(k, (int)grid, s, f.sp, f.n, f.acc, f.b, f.count, f.ad, f.scaler,
+                   DEV ? (zs::StepResult*)nullptr : c->d_result, f.dstate, f.hp, f.sched,
+                   f.has_sched, f.accum_steps, c->d_args, c->d_flag, c->d_sync, expect,
+                   (uint64_t)c->wait_ns, c->d_fused_err);
+  if (*e == cudaSuccess) ls.done();
+  return (int)grid;
+}
+
+// The whole last call of a step as ONE kernel where it applies (the mode is on,
+// there is work, and one 8-element unit per thread fits a co-resident grid).
+// Returns false to take the multi-pass path; otherwise *st is the launch's status.
+template <bool DEV, bool FLIP>
+bool try_fused(zs_ctx* c, zs_dtype dt, const FusedCall& f, cudaStream_t s, zs_status* st) {
+  if (c->fused_mode == ZS_FUSED_OFF || f.count <= 0) return false;
+  cudaError_t e = cudaSuccess;
+  int grid;
+  if (dt == ZS_FP16)
+    grid = f.acc ? fused_launch_k<ZS_FP16, true, DEV, FLIP>(c, f, s, &e)
+                 : fused_launch_k<ZS_FP16, false, DEV, FLIP>(c, f, s, &e);
+  else
+    grid = f.acc ? fused_launch_k<ZS_BF16, true, DEV, FLIP>(c, f, s, &e)
+                 : fused_launch_k<ZS_BF16, false, DEV, FLIP>(c, f, s, &e);
+  if (grid == 0) return false;
+  *st = e == cudaSuccess ? ZS_OK : cuda_fail(c, e, "fused step launch");
+  return true;
+}
+
+// Co-resident CTAs per SM of the fused step: the fewest over its variants.
+template <bool DEV, bool FLIP>
+int fused_resident(zs_ctx* c) {
+  int r = resident_ctas(c, zs::k_step_fused<ZS_FP16, true, DEV, FLIP>);
+  r = std::min(r, resident_ctas(c, zs::k_step_fused<ZS_FP16, false, DEV, FLIP>));
+  r = std::min(r, resident_ctas(c, zs::k_step_fused<ZS_BF16, true, DEV, FLIP>));
+  return std::min(r, resident_ctas(c, zs::k_step_fused<ZS_BF16, false, DEV, FLIP>));
+}
+
+zs::OopBufs in_place_bufs(float* master, float* m, float* v, void* half_out) {
+  zs::OopBufs b;
+  for (int i = 0; i < 2; ++i) {
+    b.p[i] = master;
+    b.m[i] = m;
+    b.v[i] = v;
+    b.h[i] = static_cast<uint16_t*>(half_out);
+  }
+  return b;
 }
 
 // [a, a + la) and [b, b + lb) share a byte.
@@ -737,6 +868,8 @@ zs_status zs_ctx_create(zs_ctx** out) {
   zs_ctx* c = new zs_ctx();
   const char* pdl = std::getenv("ZEROSHARD_PDL");
   c->pdl = !(pdl != nullptr && pdl[0] == '0');
+  const char* fused = std::getenv("ZEROSHARD_FUSED");
+  if (fused != nullptr && fused[0] == '0') c->fused_mode = ZS_FUSED_OFF;
   cudaError_t e = cudaGetDevice(&c->device);
   if (e == cudaSuccess)
     e = cudaDeviceGetAttribute(&c->sms, cudaDevAttrMultiProcessorCount, c->device);
@@ -757,6 +890,15 @@ zs_status zs_ctx_create(zs_ctx** out) {
   if (e == cudaSuccess) e = cudaMalloc(&c->d_args, sizeof(zs::AdamArgs));
   if (e == cudaSuccess)
     e = cudaMalloc(&c->d_norm_parts, (size_t)ZS_NORM_MAX_PARTS * sizeof(double));
+  if (e == cudaSuccess) e = cudaMalloc(&c->d_sync, sizeof(zs::FusedSync));
+  if (e == cudaSuccess) e = cudaMemset(c->d_sync, 0, sizeof(zs::FusedSync));
+  if (e == cudaSuccess)
+    e = cudaHostAlloc(reinterpret_cast<void**>(&c->h_fused_err), sizeof(int32_t),
+                      cudaHostAllocMapped);
+  if (e == cudaSuccess) {
+    *c->h_fused_err = 0;
+    e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&c->d_fused_err), c->h_fused_err, 0);
+  }
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     if (c->d_flag) cudaFree(c->d_flag);
@@ -767,6 +909,8 @@ zs_status zs_ctx_create(zs_ctx** out) {
     if (c->h_sumsq) cudaFreeHost(c->h_sumsq);
     if (c->d_args) cudaFree(c->d_args);
     if (c->d_norm_parts) cudaFree(c->d_norm_parts);
+    if (c->d_sync) cudaFree(c->d_sync);
+    if (c->h_fused_err) cudaFreeHost(c->h_fused_err);
     delete c;
     return ZS_ERR_CUDA;
   }
@@ -776,8 +920,7 @@ zs_status zs_ctx_create(zs_ctx** out) {
 
 zs_status zs_ctx_destroy(zs_ctx* c) {
   if (c == nullptr) return ZS_ERR_ARG;
-  for (auto& r : c->pending) {
-    cudaEventSynchronize(r.stop);
+  for (auto& r : c->pending) {  // released by the runtime once complete
     cudaEventDestroy(r.start);
     cudaEventDestroy(r.stop);
   }
@@ -790,11 +933,32 @@ zs_status zs_ctx_destroy(zs_ctx* c) {
   cudaFreeHost(c->h_sumsq);
   cudaFree(c->d_args);
   cudaFree(c->d_norm_parts);
+  cudaFree(c->d_sync);
+  cudaFreeHost(c->h_fused_err);  // d_fused_err is its device address
   delete c;
   return ZS_OK;
 }
 
 const char* zs_last_error(const zs_ctx* c) { return c ? c->err.c_str() : "null context"; }
+
+zs_status zs_ctx_fused_capacity(zs_ctx* c, int64_t* elements) {
+  if (c == nullptr || elements == nullptr) return ZS_ERR_ARG;
+  int r = fused_resident<false, false>(c);
+  r = std::min(r, fused_resident<true, false>(c));
+  r = std::min(r, fused_resident<true, true>(c));
+  // one 8-element unit per thread; the < 8 tail elements ride on CTA 0
+  *elements = (int64_t)r * c->sms * zs::kThreads * 8 + 7;
+  return ZS_OK;
+}
+
+zs_status zs_ctx_set_fused(zs_ctx* c, int32_t mode, int64_t wait_ns) {
+  if (c == nullptr) return ZS_ERR_ARG;
+  if (mode != ZS_FUSED_OFF && mode != ZS_FUSED_ON && mode != ZS_FUSED_TEST_TIMEOUT)
+    return fail(c, ZS_ERR_ARG, "unknown fused mode %d", (int)mode);
+  c->fused_mode = mode;
+  c->wait_ns = wait_ns > 0 ? (uint64_t)wait_ns : ZS_DEFAULT_WAIT_NS;
+  return ZS_OK;
+}
 
 zs_status zs_ctx_overflow_flag(zs_ctx* c, int32_t** d_flag) {
   if (c == nullptr || d_flag == nullptr) return ZS_ERR_ARG;
@@ -919,6 +1083,22 @@ static zs_status shard_step_impl(zs_ctx* c, const void* const* grads, int32_t n,
   const bool recompute = (n < 4) || acc == nullptr;
   const bool clip = max_norm > 0.0f;
   const float* acc_in = (accum_steps > 1 || !recompute) ? acc : nullptr;
+  if (!clip) {
+    FusedCall f;
+    f.sp = sp;
+    f.n = n;
+    f.acc = accum_steps > 1 ? acc : nullptr;
+    f.b = in_place_bufs(master, m, v, half_out);
+    f.count = count;
+    f.ad = ad;
+    f.scaler = *scaler;
+    f.accum_steps = accum_steps;
+    zs_status fst = ZS_OK;
+    if (try_fused<false, false>(c, dt, f, stream, &fst)) {
+      ZS_TRY(fst);
+      return finish_fused_step(c, scaler, overflow_out, new_scale_out, stream);
+    }
+  }
   if (count > 0 && clip) {
     // the last micro-step's pass also produces the clipping norm: materialise
     // (sums into acc) or, on the re-read path, sums acc + the last slices
@@ -1021,6 +1201,25 @@ static zs_status shard_step_async_impl(zs_ctx* c, const void* const* grads, int3
   }
   if (cap != cudaStreamCaptureStatusNone) c->timing = false;
   zs_status st = ZS_OK;
+  if (!clip) {
+    FusedCall f;
+    f.sp = sp;
+    f.n = n;
+    f.acc = accum_steps > 1 ? acc : nullptr;
+    f.b = in_place_bufs(master, m, v, half_out);
+    f.count = count;
+    f.dstate = d_state;
+    f.hp = *hp;
+    if (sched) {
+      f.sched = *sched;
+      f.has_sched = 1;
+    }
+    f.accum_steps = accum_steps;
+    if (try_fused<true, false>(c, dt, f, stream, &st)) {
+      c->timing = timing;
+      return st;
+    }
+  }
   if (count > 0 && clip) {
     // the last micro-step's pass also forms the sum of squares of the final
     // sums, unscaled (grad_div 1): the scale lives on the device, and the
@@ -1157,6 +1356,22 @@ zs_status zs_shard_step_oop(zs_ctx* c, const void* const* grads, int32_t n, zs_d
   b.v[1] = v_out;
   b.h[0] = nullptr;
   b.h[1] = static_cast<uint16_t*>(half_out);
+  {
+    FusedCall f;
+    f.sp = sp;
+    f.n = n;
+    f.acc = accum_steps > 1 ? acc : nullptr;
+    f.b = b;
+    f.count = count;
+    f.ad = ad;
+    f.scaler = *scaler;
+    f.accum_steps = accum_steps;
+    zs_status fst = ZS_OK;
+    if (try_fused<false, false>(c, dt, f, stream, &fst)) {
+      ZS_TRY(fst);
+      return finish_fused_step(c, scaler, overflow_out, new_scale_out, stream);
+    }
+  }
   ZS_TRY(update_oop<false>(c, dt, sp, n, accum_steps > 1 ? acc : nullptr, b, count, ad, nullptr,
                            nullptr, stream));
   launch_k(c, zs::k_commit_oop<false>, 1, 32, stream, c->d_flag, (zs_device_state*)nullptr,
@@ -1202,9 +1417,6 @@ zs_status zs_shard_step_async_oop(zs_ctx* c, const void* const* grads, int32_t n
     cap = cudaStreamCaptureStatusActive;
   }
   if (cap != cudaStreamCaptureStatusNone) c->timing = false;
-  launch_k(c, zs::k_step_prologue, 1, 32, stream, (const zs_device_state*)d_state, n,
-           accum_steps, *hp, sc, sched ? 1 : 0, c->d_args);
-  c->launches += 1;
   zs::OopBufs b;
   for (int i = 0; i < 2; ++i) {
     b.p[i] = master[i];
@@ -1212,6 +1424,27 @@ zs_status zs_shard_step_async_oop(zs_ctx* c, const void* const* grads, int32_t n
     b.v[i] = v[i];
     b.h[i] = static_cast<uint16_t*>(half[i]);
   }
+  {
+    FusedCall f;
+    f.sp = sp;
+    f.n = n;
+    f.acc = acc_in;
+    f.b = b;
+    f.count = count;
+    f.dstate = d_state;
+    f.hp = *hp;
+    f.sched = sc;
+    f.has_sched = sched ? 1 : 0;
+    f.accum_steps = accum_steps;
+    zs_status fst = ZS_OK;
+    if (try_fused<true, true>(c, dt, f, stream, &fst)) {
+      c->timing = timing;
+      return fst;
+    }
+  }
+  launch_k(c, zs::k_step_prologue, 1, 32, stream, (const zs_device_state*)d_state, n,
+           accum_steps, *hp, sc, sched ? 1 : 0, c->d_args);
+  c->launches += 1;
   const zs::AdamArgs unused{};
   zs_status st = update_oop<true>(c, dt, sp, n, acc_in, b, count, unused, c->d_args, d_state,
                                   stream);
@@ -1476,13 +1709,22 @@ zs_status zs_ctx_set_timing(zs_ctx* c, int32_t enable) {
   return ZS_OK;
 }
 
+// Folds every pending record into the totals, waiting for each.  A record
+// whose events cannot be read is dropped (its events destroyed) and reported
+// after the rest have been folded.
 static zs_status drain_timing(zs_ctx* c) {
+  cudaError_t first = cudaSuccess;
   for (auto& r : c->pending) {
-    cudaError_t e = cudaEventSynchronize(r.stop);
-    if (e != cudaSuccess) return cuda_fail(c, e, "event synchronise");
     float ms = 0.0f;
-    e = cudaEventElapsedTime(&ms, r.start, r.stop);
-    if (e != cudaSuccess) return cuda_fail(c, e, "event elapsed time");
+    cudaError_t e = cudaEventSynchronize(r.stop);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, r.start, r.stop);
+    if (e != cudaSuccess) {
+      if (first == cudaSuccess) first = e;
+      (void)cudaGetLastError();
+      cudaEventDestroy(r.start);
+      cudaEventDestroy(r.stop);
+      continue;
+    }
     c->total_ms[r.kind] += ms;
     c->total_launches[r.kind] += 1;
     c->total_elements[r.kind] += r.elements;
@@ -1490,7 +1732,7 @@ static zs_status drain_timing(zs_ctx* c) {
     c->pool.push_back(r.stop);
   }
   c->pending.clear();
-  return ZS_OK;
+  return first == cudaSuccess ? ZS_OK : cuda_fail(c, first, "timing events");
 }
 
 zs_status zs_ctx_timing(zs_ctx* c, int32_t kind, double* total_ms, int64_t* launches,

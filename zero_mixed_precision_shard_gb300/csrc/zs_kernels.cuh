@@ -97,6 +97,9 @@
 #ifndef ZS_FIRST_MIN_BLOCKS  // resident CTAs per SM the first micro-step's accumulate (one unit
 #define ZS_FIRST_MIN_BLOCKS 8    // per thread, no accumulator read) is compiled for: 32 registers,
 #endif                           // the full SM; the later micro-steps' pass runs best unbounded
+#ifndef ZS_FUSED_MIN_BLOCKS  // resident CTAs per SM the fused step is compiled for (its
+#define ZS_FUSED_MIN_BLOCKS 3    // capacity: this x SMs x 256 threads x 8 elements); at 4 the
+#endif                           // 32 values a thread holds across the barrier spill
 #if ZS_MIN_BLOCKS > 0
 #define ZS_BOUNDS __launch_bounds__(ZS_THREADS, ZS_MIN_BLOCKS)
 #else
@@ -471,24 +474,35 @@ __device__ __forceinline__ float lr_at(const zs_lr_schedule& sc, int64_t t) {
   return (float)(mx * rest);
 }
 
-// Per-step constants of the update from the device-resident state: Adam's t,
-// the scheduled learning rate, the bias corrections and N*G*S.
-__global__ void k_step_prologue(const zs_device_state* __restrict__ st, int n, int accum_steps,
-                                zs_adam_hparams hp, zs_lr_schedule sched, int has_sched,
-                                AdamArgs* __restrict__ out) {
-  pdl_enter(st, out);
-  if (blockIdx.x != 0 || threadIdx.x != 0) return;
-  const int64_t t = st->step + 1;
+// b^t for an integer t >= 0 by square-and-multiply in fp64: at most 2*63
+// multiplies (34 at t = 1e5).  A general fp64 power takes microseconds on
+// one thread of GB300's narrow fp64 pipe; this takes a fraction of one.  The
+// host and the device run the same operations (IEEE multiplies), so both
+// form the same bias corrections bit for bit.
+__host__ __device__ inline double pow_int(double b, int64_t t) {
+  double r = 1.0;
+  for (; t > 0; t >>= 1) {
+    if (t & 1) r *= b;
+    b *= b;
+  }
+  return r;
+}
+
+// The step's constants from the hyper-parameters, Adam's t and N*G*S (host or
+// one device thread): 1/(1-beta1^t), 1/(1-beta2^t) and its square root in
+// fp64, each carried as an fp32 pair.
+__host__ __device__ inline AdamArgs make_adam_args(float lr, const zs_adam_hparams& hp,
+                                                   int64_t t, float grad_div) {
   AdamArgs a;
-  a.lr = has_sched ? lr_at(sched, t) : hp.lr;
+  a.lr = lr;
   a.beta1 = hp.beta1;
   a.omb1 = 1.0f - hp.beta1;
   a.beta2 = hp.beta2;
   a.omb2 = 1.0f - hp.beta2;
   a.eps = hp.eps;
   a.wd = hp.weight_decay;
-  const double ib1 = 1.0 / (1.0 - pow((double)hp.beta1, (double)t));
-  const double ib2 = 1.0 / (1.0 - pow((double)hp.beta2, (double)t));
+  const double ib1 = 1.0 / (1.0 - pow_int((double)hp.beta1, t));
+  const double ib2 = 1.0 / (1.0 - pow_int((double)hp.beta2, t));
   const double sb2 = sqrt(ib2);
   a.inv_bc1 = (float)ib1;
   a.inv_bc2 = (float)ib2;
@@ -496,8 +510,27 @@ __global__ void k_step_prologue(const zs_device_state* __restrict__ st, int n, i
   a.inv_bc2_lo = (float)(ib2 - (double)a.inv_bc2);
   a.sbc2 = (float)sb2;
   a.sbc2_lo = (float)(sb2 - (double)a.sbc2);
-  a.grad_div = (float)((double)n * (double)accum_steps * (double)st->scaler.scale);
-  *out = a;
+  a.grad_div = grad_div;
+  return a;
+}
+
+// Per-step constants of the update from the device-resident state: Adam's t,
+// the scheduled learning rate, the bias corrections and N*G*S (one thread).
+__device__ __forceinline__ AdamArgs device_step_args(const zs_device_state* st, int n,
+                                                     int accum_steps, const zs_adam_hparams& hp,
+                                                     const zs_lr_schedule& sched,
+                                                     int has_sched) {
+  const int64_t t = st->step + 1;
+  return make_adam_args(has_sched ? lr_at(sched, t) : hp.lr, hp, t,
+                        (float)((double)n * (double)accum_steps * (double)st->scaler.scale));
+}
+
+__global__ void k_step_prologue(const zs_device_state* __restrict__ st, int n, int accum_steps,
+                                zs_adam_hparams hp, zs_lr_schedule sched, int has_sched,
+                                AdamArgs* __restrict__ out) {
+  pdl_enter(st, out);
+  if (blockIdx.x != 0 || threadIdx.x != 0) return;
+  *out = device_step_args(st, n, accum_steps, hp, sched, has_sched);
 }
 
 // ---------------------------------------------------------------- kernels
@@ -986,6 +1019,181 @@ __global__ void k_commit_oop(int32_t* __restrict__ flag, zs_device_state* __rest
     scaler_step(scaler_in, overflow, result);
   }
   *flag = 0;
+}
+
+// ---------------------------------------------------------------- fused step
+
+// Grid-wide barrier of the fused step (context scratch, zeroed at creation).
+// A launch's CTAs read `gen` before they arrive; the last CTA to arrive
+// resolves the step and advances `gen`, which releases the others.
+struct FusedSync {
+  unsigned int arrived;  // CTAs of the running launch that have arrived
+  unsigned int gen;      // launches resolved so far
+  int32_t overflow;      // the step's flag as the last CTA to arrive read it
+  int32_t pad_;
+};
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ unsigned int ld_acquire(const unsigned int* p) {
+  unsigned int x;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(x) : "l"(p) : "memory");
+  return x;
+}
+
+// The step's constants as another CTA wrote them in this launch (read through
+// L2 only).
+__device__ __forceinline__ AdamArgs load_args_cg(const AdamArgs* p) {
+  AdamArgs a;
+  const float* src = reinterpret_cast<const float*>(p);
+  float* dst = reinterpret_cast<float*>(&a);
+#pragma unroll
+  for (int k = 0; k < (int)(sizeof(AdamArgs) / sizeof(float)); ++k) dst[k] = __ldcg(src + k);
+  return a;
+}
+
+// The whole step of a shard whose 8-element units fit one co-resident grid
+// (one unit per thread, launched cooperatively): the last micro-step's sums
+// s = (acc or +0) + the n slices in rank order and the current master / m / v
+// are loaded into registers; the flag is ORed over the grid; one bounded grid
+// barrier; then, on a clean step only, AdamW from the registers into the
+// output set (the same arithmetic as every other form).  Nothing is written on
+// an overflow, so the in-place state needs no second pass.  The last CTA to
+// arrive reads and clears the flag (the earlier micro-steps' ORs included) and
+// performs the loss-scale update: DEV, into the device state (flipping its
+// buffer index on a clean step when FLIP); otherwise into `result`.  DEV: CTA
+// 0 forms the step's constants from the device state before it arrives.
+// b.X[cur] is read and b.X[cur ^ 1] written (cur = the device state's index
+// with FLIP, else 0; an in-place step passes the same buffers in both).
+// A CTA whose wait passes wait_ns gives up: it writes nothing and sets *err.
+// `expect` is the number of arrivals that resolve the step (the grid size).
+template <int DT, bool HAS_ACC, bool DEV, bool FLIP>
+__global__ void __launch_bounds__(ZS_THREADS, ZS_FUSED_MIN_BLOCKS)
+    k_step_fused(const __grid_constant__ SlicePtrs s, int n, const float* acc,
+                 const __grid_constant__ OopBufs b, int64_t count, AdamArgs ad_host,
+                 zs_scaler scaler_in, StepResult* result, zs_device_state* dstate,
+                 zs_adam_hparams hp, zs_lr_schedule sched, int has_sched, int accum_steps,
+                 AdamArgs* ad_slot, int32_t* flag, FusedSync* sync, unsigned int expect,
+                 uint64_t wait_ns, int32_t* err) {
+  // Launched without the programmatic-dependent attribute (it starts once its
+  // predecessor has completed), and it lets no successor start early either:
+  // no griddepcontrol here, so no other grid's CTAs take SM room while it runs.
+  __shared__ int s_go;
+  unsigned int gen0 = 0;
+  if (threadIdx.x == 0) gen0 = ld_acquire(&sync->gen);
+  int cur = 0;
+  if constexpr (DEV && FLIP) cur = dstate->buf & 1;
+  const int64_t nvec = count >> 3;
+  const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+  const bool unit = tid < nvec;
+  const bool tail = tid < count - nvec * 8;
+  const int64_t ti = nvec * 8 + tid;
+  float a[1][8], p[8], m[8], v[8];
+  float at = 0.0f, pt = 0.0f, mt = 0.0f, vt = 0.0f;
+  bool bad = false;
+  if (unit) {
+    if (HAS_ACC) {
+      load8(acc + tid * 8, a[0]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) a[0][k] = 0.0f;
+    }
+    load8(b.p[cur] + tid * 8, p);
+    load8(b.m[cur] + tid * 8, m);
+    load8(b.v[cur] + tid * 8, v);
+    const int64_t vi[1] = {tid};
+    const bool ok[1] = {true};
+    sum_slices<DT, 1>(s, n, vi, ok, a);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) bad |= not_finite(a[0][k]);
+  }
+  if (tail) {
+    at = sum_slices1<DT>(s, n, ti, HAS_ACC ? acc[ti] : 0.0f);
+    bad |= not_finite(at);
+    pt = b.p[cur][ti];
+    mt = b.m[cur][ti];
+    vt = b.v[cur][ti];
+  }
+  if constexpr (DEV) {
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+      *ad_slot = device_step_args(dstate, n, accum_steps, hp, sched, has_sched);
+  }
+  const int any_bad = __syncthreads_or(bad);
+  if (threadIdx.x == 0) {
+    if (any_bad) atomicOr(flag, 1);
+    __threadfence();
+    int go = 0;
+    const unsigned int prev = atomicAdd(&sync->arrived, 1u);
+    if (prev == expect - 1u) {
+      // last to arrive: every CTA's flag bits (and CTA 0's constants) are visible
+      __threadfence();
+      const int32_t ovf = atomicExch(flag, 0) != 0 ? 1 : 0;
+      if constexpr (DEV) {
+        device_state_step(dstate, ovf, load_args_cg(ad_slot));
+        if (FLIP && !ovf) dstate->buf = cur ^ 1;
+      } else {
+        if (result != nullptr) scaler_step(scaler_in, ovf, result);
+      }
+      sync->overflow = ovf;
+      sync->arrived = 0u;
+      __threadfence();
+      atomicAdd(&sync->gen, 1u);
+      go = !ovf;
+    } else {
+      const uint64_t t0 = global_ns();
+      bool released = false;
+      for (;;) {
+        if (ld_acquire(&sync->gen) != gen0) {
+          released = true;
+          break;
+        }
+        if (global_ns() - t0 > wait_ns) break;
+        __nanosleep(32);
+      }
+      if (released) {
+        go = __ldcg(&sync->overflow) == 0;
+      } else {
+        *reinterpret_cast<volatile int32_t*>(err) = 1;
+      }
+    }
+    s_go = go;
+  }
+  __syncthreads();
+  if (!s_go) return;
+  AdamArgs ad = ad_host;
+  if constexpr (DEV) {
+    // one L2 read of the constants per CTA (every thread reading them hits one
+    // L2 line from every warp of the grid), shared through shared memory
+    constexpr int kArgWords = (int)(sizeof(AdamArgs) / sizeof(float));
+    __shared__ float s_args[kArgWords];
+    if (threadIdx.x < kArgWords)
+      s_args[threadIdx.x] = __ldcg(reinterpret_cast<const float*>(ad_slot) + threadIdx.x);
+    __syncthreads();
+    ad = *reinterpret_cast<const AdamArgs*>(s_args);
+  }
+  if (unit) {
+    uint32_t h[4];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) adamw1<false>(ad, a[0][k], p[k], m[k], v[k]);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      h[k] = float_to_half_bits<DT>(p[2 * k]) | (float_to_half_bits<DT>(p[2 * k + 1]) << 16);
+    store8_cs(b.p[cur ^ 1] + tid * 8, p);
+    store8_cs(b.m[cur ^ 1] + tid * 8, m);
+    store8_cs(b.v[cur ^ 1] + tid * 8, v);
+    __stcs(reinterpret_cast<uint4*>(b.h[cur ^ 1]) + tid, make_uint4(h[0], h[1], h[2], h[3]));
+  }
+  if (tail) {
+    adamw1<false>(ad, at, pt, mt, vt);
+    b.p[cur ^ 1][ti] = pt;
+    b.m[cur ^ 1][ti] = mt;
+    b.v[cur ^ 1][ti] = vt;
+    b.h[cur ^ 1][ti] = (uint16_t)float_to_half_bits<DT>(pt);
+  }
 }
 
 // ---------------------------------------------------------------- clipping
