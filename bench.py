@@ -371,19 +371,31 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def code_digest(path: str) -> str:
+    """sha256 of a C/CUDA source with its comments, trailing blanks and blank
+    lines removed: recorded counters stay tied to the code, not to its comments
+    (the kernel sources hold no string literal with a comment marker)."""
+    import hashlib
+    import re
+    with open(path, encoding="utf-8") as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    lines = [ln.rstrip() for ln in text.splitlines()]
+    return hashlib.sha256("\n".join(ln for ln in lines if ln).encode()).hexdigest()
+
+
 def recorded_traffic(workload: str, kind: str, elements_per_launch: float):
     """DRAM bytes per launch of `kind` from the ncu summary in profiles/traffic.json,
     scaled by elements; None unless that capture was taken of this workload
-    with the kernel sources as they are now."""
-    import hashlib
+    with the kernel sources' code as it is now."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             rec = json.load(f)
-        for rel, digest in rec["sources_sha256"].items():
-            with open(os.path.join(ROOT, rel), "rb") as f:
-                if hashlib.sha256(f.read()).hexdigest() != digest:
-                    return None
+        for rel, digest in rec["sources_code_sha256"].items():
+            if code_digest(os.path.join(ROOT, rel)) != digest:
+                return None
         if rec.get("workload") != workload:
             return None
         per = rec["bytes_per_elem"].get(kind)

@@ -48,8 +48,12 @@
  *    count may be any value >= 0 (a ragged tail is handled).
  *  - Limits: 1 <= n <= ZS_MAX_RANKS.
  *  - Ordering: all work is issued on `stream` in order; only zs_shard_step,
- *    zs_shard_step_clipped, zs_shard_step_halfacc, zs_scaler_update and
- *    zs_ctx_timing synchronise that stream (zs_shard_step_async never does).
+ *    zs_shard_step_clipped, zs_shard_step_halfacc, zs_shard_step_oop,
+ *    zs_scaler_update and zs_ctx_timing synchronise that stream
+ *    (zs_shard_step_async and zs_shard_step_async_oop never do).  The steps of
+ *    one context share its flag, scratch and the fused step's barrier: issue
+ *    them in stream order (one stream, or streams ordered by events); steps
+ *    that must overlap use a context each.
  *  - Errors: a non-zero zs_status; zs_last_error(ctx) gives the message.
  *    Overflow of the gradients is a result, not an error.
  *  - Threads: a context is used by one host thread at a time.

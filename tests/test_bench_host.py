@@ -45,11 +45,16 @@ def test_recorded_traffic_requires_matching_sources(tmp_path, monkeypatch):
     fake = tmp_path / "repo"
     (fake / "profiles").mkdir(parents=True)
     (fake / "profiles" / "traffic.json").write_text(json.dumps(rec))
-    for rel in rec["sources_sha256"]:
+    for rel in rec["sources_code_sha256"]:
+        src = open(os.path.join(bench.ROOT, rel)).read()
         p = fake / rel
         p.parent.mkdir(parents=True, exist_ok=True)
-        p.write_text("// changed\n")
+        # comments and blank lines do not change the code the counters describe
+        p.write_text("// a comment\n\n" + src.replace("\n", "  \n") + "/* another */\n")
     monkeypatch.setattr(bench, "ROOT", str(fake))
+    assert bench.recorded_traffic(rec["workload"], "reduce", 1e6) > 0
+    for rel in rec["sources_code_sha256"]:
+        (fake / rel).write_text(open(os.path.join(bench.ROOT, rel)).read() + "int changed;\n")
     assert bench.recorded_traffic(rec["workload"], "reduce", 1e6) is None
 
 

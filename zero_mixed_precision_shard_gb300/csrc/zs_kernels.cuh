@@ -27,7 +27,10 @@
 //    from the constant bank without a local-memory copy;
 //  * the overflow flag is a warp-wide OR and one atomicOr per warp that saw a
 //    non-finite sum: no CTA barrier, so a warp that is done retires without
-//    waiting for the CTA's slowest warp.
+//    waiting for the CTA's slowest warp;
+//  * a shard small enough for one co-resident grid takes the whole last call
+//    as one cooperative kernel (k_step_fused): its values stay in registers
+//    across a grid barrier whose waits are bounded by %globaltimer.
 //
 // Arithmetic contract (DeepSpeed Complete Guide, §2.2 and §4.3, under the
 // reading that the accumulator is fp32 and ranks are summed in order):
