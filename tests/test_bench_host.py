@@ -41,20 +41,27 @@ def test_recorded_traffic_requires_matching_sources(tmp_path, monkeypatch):
     for k, alg in rec["algorithmic_bytes_per_elem"].items():
         assert rec["bytes_per_elem"][k] <= alg + 0.01
     assert bench.recorded_traffic("gpt2-small-n8", "reduce", 1e6) is None
-    # a copy of the repo whose kernel source differs gets no traffic
+    # a copy of the repo whose record was taken on its own sources
     fake = tmp_path / "repo"
     (fake / "profiles").mkdir(parents=True)
-    (fake / "profiles" / "traffic.json").write_text(json.dumps(rec))
     for rel in rec["sources_code_sha256"]:
-        src = open(os.path.join(bench.ROOT, rel)).read()
         p = fake / rel
         p.parent.mkdir(parents=True, exist_ok=True)
-        # comments and blank lines do not change the code the counters describe
-        p.write_text("// a comment\n\n" + src.replace("\n", "  \n") + "/* another */\n")
+        p.write_text(open(os.path.join(bench.ROOT, rel)).read())
+    rec = dict(rec, sources_code_sha256={rel: bench.code_digest(str(fake / rel))
+                                         for rel in rec["sources_code_sha256"]})
+    (fake / "profiles" / "traffic.json").write_text(json.dumps(rec))
     monkeypatch.setattr(bench, "ROOT", str(fake))
-    assert bench.recorded_traffic(rec["workload"], "reduce", 1e6) > 0
+    per = rec["bytes_per_elem"]["reduce"]
+    assert bench.recorded_traffic(rec["workload"], "reduce", 1e6) == per * 1e6
+    # comments and blank lines do not change the code the counters describe
     for rel in rec["sources_code_sha256"]:
-        (fake / rel).write_text(open(os.path.join(bench.ROOT, rel)).read() + "int changed;\n")
+        src = (fake / rel).read_text()
+        (fake / rel).write_text("// a comment\n\n" + src.replace("\n", "  \n") + "/* more */\n")
+    assert bench.recorded_traffic(rec["workload"], "reduce", 1e6) == per * 1e6
+    # a change of the code voids the record
+    for rel in rec["sources_code_sha256"]:
+        (fake / rel).write_text((fake / rel).read_text() + "int changed;\n")
     assert bench.recorded_traffic(rec["workload"], "reduce", 1e6) is None
 
 

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <climits>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -68,6 +69,7 @@ struct zs_ctx {
   int32_t* d_fused_err = nullptr;
   int32_t fused_mode = ZS_FUSED_ON;
   uint64_t wait_ns = ZS_DEFAULT_WAIT_NS;
+  int64_t coop_max_grid = INT64_MAX;  // lowered when the runtime refuses a cooperative grid
   std::string err;
   std::unordered_map<const void*, int> occupancy;  // resident CTAs per SM, per kernel
   int64_t launches = 0;
@@ -170,6 +172,11 @@ struct LaunchScope {
       start = take_event(c);
       if (start) cudaEventRecord(start, s);
     }
+  }
+  // the launch did not happen: hand the start event back
+  void cancel() {
+    if (start) c->pool.push_back(start);
+    start = nullptr;
   }
   void done() {
     c->launches += 1;
@@ -685,7 +692,7 @@ int fused_launch_k(zs_ctx* c, const FusedCall& f, cudaStream_t s, cudaError_t* e
   const int64_t per_grid = (int64_t)resident_ctas(c, k) * c->sms;
   int64_t grid = ((f.count >> 3) + zs::kThreads - 1) / zs::kThreads;
   if (grid < 1) grid = 1;
-  if (grid > per_grid) return 0;
+  if (grid > per_grid || grid > c->coop_max_grid) return 0;
   // ZS_FUSED_TEST_TIMEOUT: the barrier waits for one CTA more than the grid has
   const unsigned expect = (unsigned)grid + (c->fused_mode == ZS_FUSED_TEST_TIMEOUT ? 1u : 0u);
   LaunchScope ls(c, s, ZS_KERNEL_FUSED, f.count);
@@ -693,7 +700,16 @@ int fused_launch_k(zs_ctx* c, const FusedCall& f, cudaStream_t s, cudaError_t* e
                    DEV ? (zs::StepResult*)nullptr : c->d_result, f.dstate, f.hp, f.sched,
                    f.has_sched, f.accum_steps, c->d_args, c->d_flag, c->d_sync, expect,
                    (uint64_t)c->wait_ns, c->d_fused_err);
+  if (*e == cudaErrorCooperativeLaunchTooLarge) {
+    // fewer SMs than the occupancy query assumed (e.g. a share of the GPU under
+    // MPS): nothing was launched; the multi-kernel path takes the step
+    (void)cudaGetLastError();
+    ls.cancel();
+    c->coop_max_grid = grid - 1;
+    return 0;
+  }
   if (*e == cudaSuccess) ls.done();
+  else ls.cancel();
   return (int)grid;
 }
 
