@@ -760,8 +760,17 @@ class Zero2Workload:
         self.scaler = zs.zs_scaler_init(wl.scale0, wl.min_scale, wl.window, wl.hysteresis,
                                         wl.dynamic)
         hp = zs.make_hparams(wl.lr, wl.beta1, wl.beta2, wl.eps, wl.weight_decay)
+        # unclipped steps apply the last micro-step out of place, bucket by bucket,
+        # where the second master/m/v/half set (14 B per shard element) fits
+        second = None
+        self.oop = clip <= 0 and oop_fits(E)
+        if self.oop:
+            p2 = torch.zeros(E, dtype=torch.float32, device=dev)
+            second = (p2, torch.zeros_like(p2), torch.zeros_like(p2),
+                      torch.zeros(E, dtype=torch.int16, device=dev))
         self.ops = ZsShardOps(zs, ctx, wl.dtype_code, E, world, wl.g, self.acc, self.master,
-                              self.m, self.v, self.half_shard, hp, self.scaler, clip)
+                              self.m, self.v, self.half_shard, hp, self.scaler, clip,
+                              second=second)
         bucket = wl.bucket_elems
         # two receive slots: the next bucket's exchange overlaps this one's sum
         self.recv = torch.empty(2 * world * min(E, bucket // 64 * 64), dtype=torch.int16,
@@ -778,8 +787,11 @@ class Zero2Workload:
     def launch_plan(self):
         """(kind, alg bytes per element of the shard) of every kernel a step launches:
         per micro-step the accumulate of the received slices (split by bucket),
-        the update from the accumulator (and the norm pass when clipping)."""
+        the update from the accumulator (and the norm pass when clipping); out of
+        place, the last micro-step's buckets are summed and applied in one pass."""
         n, g = self.world, self.wl.g
+        if self.oop:
+            return step_launch_plan(n, g, self.wl.dtype, oop=True)
         plan = [("reduce_first" if k == 0 else "reduce",
                  kernel_alg_bytes("reduce", n, first=(k == 0))) for k in range(g)]
         if self.clip > 0:
@@ -805,7 +817,8 @@ def run_zero2(args, zs, ctx, wl, world: int, rank: int, dev: int, probe):
     per_step_ms = ms / args.steps
     value = Z.psi / (per_step_ms * 1e-3)        # every rank's owned params over the slowest step
     xb = Z.step_obj.exchanged_bytes(wl.g)
-    shard_bytes = (alg_bytes_per_elem_step(world, wl.g) + 8) * Z.E   # + materialised last micro
+    # + the materialised last micro-step unless it is applied out of place
+    shard_bytes = (alg_bytes_per_elem_step(world, wl.g) + (0 if Z.oop else 8)) * Z.E
     peak, peak_kind = measured_peaks()
     dom = max(kinds, key=lambda k: kinds[k]["ms"]) if kinds else None
     roofline = None
@@ -844,8 +857,10 @@ def run_zero2(args, zs, ctx, wl, world: int, rank: int, dev: int, probe):
                                + " all-reduce; update; all-gather of the half copy",
                 "dist_backend": args.dist_backend,
                 "clip_max_norm": args.clip or None,
-                "api": "dp.Zero2Step over zs_reduce_check, zs_apply"
-                       + ("_clipped + zs_grad_sumsq" if args.clip else "")
+                "api": "dp.Zero2Step over zs_reduce_check, "
+                       + ("zs_update_oop (the last micro-step per bucket, out of place)"
+                          if Z.oop else "zs_apply"
+                          + ("_clipped + zs_grad_sumsq" if args.clip else ""))
                        + ", zs_scaler_update",
                 "exchange_bytes_per_rank_per_step": xb,
                 "shard_alg_bytes_per_step": shard_bytes,

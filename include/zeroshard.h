@@ -34,8 +34,10 @@
  * parts) passes the received slices as the n pointers of zs_reduce_check, so
  * the same rank-ordered fp32 sum runs; the flag (and the clipping norm) is
  * all-reduced between the reduce and zs_apply, and the half shards are
- * all-gathered afterwards.  The Python package's dp module does this with
- * torch.distributed.
+ * all-gathered afterwards.  Unclipped steps can instead pass the last
+ * micro-step's received slices to zs_update_oop bucket by bucket (sum, flag
+ * and update into a second state set in one pass), all-reduce the flag and
+ * commit.  The Python package's dp module does this with torch.distributed.
  *
  * Conventions for every call:
  *  - Ownership: every array is caller-owned DEVICE memory on the context's
@@ -469,6 +471,27 @@ zs_status zs_shard_step_async_oop(zs_ctx* ctx, const void* const* grads, int32_t
                                   void* const* half, const zs_adam_hparams* hp,
                                   const zs_lr_schedule* sched, zs_device_state* d_state,
                                   cudaStream_t stream);
+
+/* Two-phase form of the out-of-place step, for a flag that spans several
+ * buckets, shards or GPUs (§2.2: each rank updates its shard as the reduced
+ * buckets arrive; §4.2: all ranks skip together).  For one range of the
+ * shard: s = acc[i] (or +0 if acc == NULL) + grads[0][i] + ... in rank order,
+ * as zs_grad_accum adds them; OR into *d_flag whether any s is non-finite;
+ * then AdamW with g = s / grad_div (grad_div = N * G * scale, N the ranks
+ * summed, G the micro-steps) from master_in/m_in/v_in into
+ * master_out/m_out/v_out and half_out -- written whatever the flag.  Call it
+ * per range (buckets of the last micro-step, as they arrive) with the same
+ * d_flag, all-reduce (MAX) the flag across the ranks, and pass it to
+ * zs_scaler_update: on 0 the *_out buffers hold the state (swap the sets);
+ * otherwise they are garbage and the *_in buffers are untouched.  Ranges are
+ * offsets into the same shard arrays (16-byte aligned: multiples of 4
+ * elements).  The in and out sets must not overlap.  Does not synchronise.
+ * Errors as zs_shard_step_oop. */
+zs_status zs_update_oop(zs_ctx* ctx, const void* const* grads, int32_t n, zs_dtype dt,
+                        int64_t count, const float* acc, float grad_div, const float* master_in,
+                        const float* m_in, const float* v_in, float* master_out, float* m_out,
+                        float* v_out, void* half_out, const zs_adam_hparams* hp, int64_t step,
+                        int32_t* d_flag, cudaStream_t stream);
 
 /* ---------------------------------------------------------------- engine */
 

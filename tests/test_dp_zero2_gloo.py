@@ -6,7 +6,9 @@ flag (and the norm when clipping), update, and all-gather the half copy.
 The per-rank compute here is the oracle, so the test checks the exchanges:
 every rank's shard state, and the gathered half parameters, must equal the
 oracle's single-process union of all shards bit for bit, with an overflow on
-one rank skipping the step on all.  Also the bucket plan's host arithmetic.
+one rank skipping the step on all; in place, and with the last micro-step
+summed and applied out of place bucket by bucket, then committed by the
+agreed flag.  Also the bucket plan's host arithmetic.
 No GPU."""
 import os
 import socket
@@ -72,10 +74,13 @@ class OracleOps:
     def __init__(self, master_shard, world, max_norm):
         self.st = oracle.ShardState.from_master(master_shard, 0)
         self.acc = np.zeros(master_shard.shape[0], np.float32)
-        self.half_shard = torch.from_numpy(self.st.half.view(np.int16))  # shares memory
         self.hp = oracle.make_hparams(*HP)
         self.sc = oracle.make_scaler(1024.0, window=2)
         self.world, self.max_norm, self.t = world, max_norm, 0
+
+    @property
+    def half_shard(self):
+        return torch.from_numpy(self.st.half.view(np.int16))   # shares memory
 
     def div(self):
         return float(self.world * G * self.sc.scale)
@@ -102,13 +107,40 @@ class OracleOps:
         return ovf
 
 
-def worker(rank, world, port, outdir, max_norm, bucket):
+class OracleOpsOOP(OracleOps):
+    """The same compute, with the last micro-step summed and applied out of
+    place into a second state set per bucket and committed by the flag."""
+    oop = True
+
+    def __init__(self, master_shard, world, max_norm):
+        super().__init__(master_shard, world, max_norm)
+        self.other = self.st.copy()
+
+    def update_oop(self, rows, offset, length, flag):
+        r = slice(offset, offset + length)
+        a = np.zeros(length, np.float32) if G == 1 else self.acc[r].copy()
+        oracle.reduce_accumulate([x.numpy().view(np.uint16) for x in rows], 0, a, G == 1)
+        flag[0] = flag[0] | oracle.any_nonfinite_f32(a)
+        dst = self.other
+        for k in ("master", "m", "v"):
+            getattr(dst, k)[r] = getattr(self.st, k)[r]
+        oracle.adamw_apply(a, self.div(), dst.master[r], dst.m[r], dst.v[r], dst.half[r], 0,
+                           self.hp, self.t + 1)
+
+    def commit_oop(self, flag):
+        ovf = self.scaler_update(flag)
+        if not ovf:
+            self.st, self.other = self.other, self.st
+        return ovf
+
+
+def worker(rank, world, port, outdir, max_norm, bucket, oop=False):
     os.environ["MASTER_ADDR"] = "127.0.0.1"
     os.environ["MASTER_PORT"] = str(port)
     dist.init_process_group("gloo", rank=rank, world_size=world)
     psi_pad, E = oracle.partition(PSI, world)
     m0 = master_init(psi_pad)
-    ops = OracleOps(m0[rank * E:(rank + 1) * E], world, max_norm)
+    ops = (OracleOpsOOP if oop else OracleOps)(m0[rank * E:(rank + 1) * E], world, max_norm)
     half_full = torch.from_numpy(oracle.f32_to_half(m0, 0).view(np.int16).copy())
     recv = torch.zeros(world * min(E, bucket), dtype=torch.int16)
     z = Zero2Step(ops, psi_pad, E, rank, bucket, recv, torch.zeros(1, dtype=torch.int32),
@@ -132,11 +164,17 @@ def free_port():
     return p
 
 
-@pytest.mark.parametrize("world,max_norm,bucket", [(2, 0.0, 1 << 20), (2, 0.01, 640),
-                                                   (3, 0.0, 1024), (3, 0.05, 64)])
-def test_zero2_ranks_equal_the_oracle_union(tmp_path, world, max_norm, bucket):
-    mp.spawn(worker, args=(world, free_port(), str(tmp_path), max_norm, bucket), nprocs=world,
-             join=True)
+@pytest.mark.parametrize("world,max_norm,bucket,oop", [(2, 0.0, 1 << 20, False),
+                                                       (2, 0.01, 640, False),
+                                                       (3, 0.0, 1024, False),
+                                                       (3, 0.05, 64, False),
+                                                       (2, 0.0, 640, True), (3, 0.0, 64, True),
+                                                       (3, 0.05, 1024, True)])
+def test_zero2_ranks_equal_the_oracle_union(tmp_path, world, max_norm, bucket, oop):
+    """oop: the last micro-step out of place per bucket (unclipped steps; a
+    clipped step with such ops materialises as before)."""
+    mp.spawn(worker, args=(world, free_port(), str(tmp_path), max_norm, bucket, oop),
+             nprocs=world, join=True)
     flags, states, scale, t = reference_union(world, max_norm)
     assert flags == [0, 0, 1, 0, 0, 0]
     union_half = np.concatenate([st.half for st in states])

@@ -6,7 +6,8 @@ the library: each rank holds its own full flat fp16 gradient per micro-step,
 sends every bucket's part of shard q to rank q, sums what it receives with
 the library's reduce kernel, agrees on the flag (and the clipping norm),
 updates its shard and all-gathers the half copy; both ranks' state and the
-gathered half parameters are compared with the oracle's union of all shards.
+gathered half parameters are compared with the oracle's union of all shards,
+in place and with the last micro-step applied out of place per bucket.
 Then the benchmark's multi-GPU run, launched as a multi-GPU run is (torchrun,
 one process per rank): the one JSON line reports the whole job."""
 import json
@@ -44,7 +45,17 @@ def full_grads(world, step, scale, psi_pad):
     return out
 
 
-def zero2_worker(rank, world, port, outdir, max_norm, bucket):
+def second_set(E, dev, oop):
+    """The out-of-place step's second master/m/v/half set (None: in place)."""
+    import torch
+    if not oop:
+        return None
+    p = torch.zeros(E, dtype=torch.float32, device=dev)
+    return (p, torch.zeros_like(p), torch.zeros_like(p),
+            torch.zeros(E, dtype=torch.int16, device=dev))
+
+
+def zero2_worker(rank, world, port, outdir, max_norm, bucket, oop=False):
     import torch
     import torch.distributed as dist
 
@@ -68,7 +79,7 @@ def zero2_worker(rank, world, port, outdir, max_norm, bucket):
     half_full = torch.from_numpy(oracle.f32_to_half(m0, 0).view(np.int16).copy()).to(dev)
     sc = zs.zs_scaler_init(1024.0, 1.0, 2, 1, True)
     ops = ZsShardOps(zs, ctx, zs.ZS_FP16, E, world, G, acc, master, m, v, half_shard,
-                     zs.make_hparams(*HP), sc, max_norm)
+                     zs.make_hparams(*HP), sc, max_norm, second=second_set(E, dev, oop))
     recv = torch.zeros(world * min(E, bucket), dtype=torch.int16, device=dev)
     z = Zero2Step(ops, psi_pad, E, rank, bucket, recv,
                   torch.zeros(1, dtype=torch.int32, device=dev),
@@ -79,9 +90,9 @@ def zero2_worker(rank, world, port, outdir, max_norm, bucket):
         dg = [torch.from_numpy(x.view(np.int16)).to(dev) for x in g]
         flags.append(z.step(dg, half_full, clip=max_norm > 0))
     torch.cuda.synchronize()
-    np.savez(os.path.join(outdir, f"rank{rank}.npz"), master=master.cpu().numpy(),
-             m=m.cpu().numpy(), v=v.cpu().numpy(),
-             half=half_shard.cpu().numpy().view(np.uint16),
+    np.savez(os.path.join(outdir, f"rank{rank}.npz"), master=ops.master.cpu().numpy(),
+             m=ops.m.cpu().numpy(), v=ops.v.cpu().numpy(),
+             half=ops.half_shard.cpu().numpy().view(np.uint16),
              half_full=half_full.cpu().numpy().view(np.uint16), flags=np.array(flags),
              scale=sc.scale, t=ops.t, sent=z.exchanged_bytes(G)["grad_sent"])
     ctx.close()
@@ -106,7 +117,7 @@ def oracle_union(world, max_norm):
     return flags, states, sc.scale, t
 
 
-def nccl_one_rank_worker(rank, port, outdir, max_norm, bucket):
+def nccl_one_rank_worker(rank, port, outdir, max_norm, bucket, oop=False):
     """zero2_worker's step over a one-rank NCCL group: every exchange is a real
     NCCL call on device buffers (the all-to-alls posted asynchronously into two
     receive slots, each waited on by the stream before its sum)."""
@@ -133,7 +144,7 @@ def nccl_one_rank_worker(rank, port, outdir, max_norm, bucket):
     half_full = torch.zeros(psi_pad, dtype=torch.int16, device=dev)
     sc = zs.zs_scaler_init(1024.0, 1.0, 2, 1, True)
     ops = ZsShardOps(zs, ctx, zs.ZS_FP16, E, 1, G, acc, master, m, v, half_shard,
-                     zs.make_hparams(*HP), sc, max_norm)
+                     zs.make_hparams(*HP), sc, max_norm, second=second_set(E, dev, oop))
     recv = torch.zeros(2 * min(E, bucket), dtype=torch.int16, device=dev)
     z = Zero2Step(ops, psi_pad, E, 0, bucket, recv,
                   torch.zeros(1, dtype=torch.int32, device=dev),
@@ -147,25 +158,27 @@ def nccl_one_rank_worker(rank, port, outdir, max_norm, bucket):
         dg = [torch.from_numpy(x.view(np.int16)).to(dev) for x in g]
         flags.append(z.step(dg, half_full, clip=max_norm > 0))
     torch.cuda.synchronize()
-    np.savez(os.path.join(outdir, "rank0.npz"), master=master.cpu().numpy(),
-             m=m.cpu().numpy(), v=v.cpu().numpy(),
-             half=half_shard.cpu().numpy().view(np.uint16),
+    np.savez(os.path.join(outdir, "rank0.npz"), master=ops.master.cpu().numpy(),
+             m=ops.m.cpu().numpy(), v=ops.v.cpu().numpy(),
+             half=ops.half_shard.cpu().numpy().view(np.uint16),
              half_full=half_full.cpu().numpy().view(np.uint16), flags=np.array(flags),
              scale=sc.scale, t=ops.t)
     ctx.close()
     dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("max_norm,bucket", [(0.0, 50_048), (0.01, 1 << 22)])
-def test_zero2_step_over_a_one_rank_nccl_group(tmp_path, max_norm, bucket):
+@pytest.mark.parametrize("max_norm,bucket,oop", [(0.0, 50_048, False), (0.01, 1 << 22, False),
+                                                (0.0, 50_048, True)])
+def test_zero2_step_over_a_one_rank_nccl_group(tmp_path, max_norm, bucket, oop):
     """The NCCL form of the exchanges (device all-to-all with two slots and
     asynchronous posts, device all-reduce and all-gather), on the one GPU as a
-    one-rank group, against the oracle's step of the single shard."""
+    one-rank group, against the oracle's step of the single shard (oop: the
+    last micro-step applied out of place per bucket, then committed)."""
     import torch.multiprocessing as mp
 
     import oracle
     from _helpers import assert_close, half_ulps
-    mp.spawn(nccl_one_rank_worker, args=(free_port(), str(tmp_path), max_norm, bucket),
+    mp.spawn(nccl_one_rank_worker, args=(free_port(), str(tmp_path), max_norm, bucket, oop),
              nprocs=1, join=True)
     psi_pad, E = oracle.partition(PSI, 1)
     m0 = np.zeros(psi_pad, np.float32)
@@ -190,12 +203,13 @@ def test_zero2_step_over_a_one_rank_nccl_group(tmp_path, max_norm, bucket):
     assert d["half_full"].tobytes() == d["half"].tobytes()    # the one-rank all-gather
 
 
-@pytest.mark.parametrize("max_norm,bucket", [(0.0, 1 << 22), (0.01, 30_016)])
-def test_two_cuda_ranks_zero2_step_equals_the_oracle_union(tmp_path, max_norm, bucket):
+@pytest.mark.parametrize("max_norm,bucket,oop", [(0.0, 1 << 22, False), (0.01, 30_016, False),
+                                                (0.0, 30_016, True)])
+def test_two_cuda_ranks_zero2_step_equals_the_oracle_union(tmp_path, max_norm, bucket, oop):
     import torch.multiprocessing as mp
     from _helpers import assert_close, half_ulps
     world = 2
-    mp.spawn(zero2_worker, args=(world, free_port(), str(tmp_path), max_norm, bucket),
+    mp.spawn(zero2_worker, args=(world, free_port(), str(tmp_path), max_norm, bucket, oop),
              nprocs=world, join=True)
     flags, states, scale, t = oracle_union(world, max_norm)
     assert flags == [0, 0, 1, 0, 0, 0]
@@ -250,7 +264,10 @@ def test_two_ranks_on_one_gpu(workload, elements, extra):
     assert c["exchange_bytes_per_rank_per_step"]["grad_sent"] == wl.g * E * 2
     assert c["exchange_bytes_per_rank_per_step"]["grad_received"] == wl.g * E * 2
     assert d["gpu_launches"] >= 2 * 3 * (wl.g + 1)
-    assert set(c["kernels"]) >= {"reduce_first", "apply"}
+    # unclipped: the last micro-step applied out of place per bucket (the second
+    # state set fits); clipped: the materialised sums, then the update
+    last = "apply" if extra else "update_oop"
+    assert set(c["kernels"]) >= {"reduce_first", last} and ("update_oop" in c["api"]) != bool(extra)
     e = d["e2e"]
     assert e["h2d_bytes_per_step"] == 2 * wl.g * 2 * E * 2 and e["value"] > 0
     assert d["cpu_baseline"] is None                 # rank 0 at N = 1 only

@@ -185,3 +185,53 @@ def test_oop_rejects_overlapping_buffers(zs, ctx):
         zs.zs_shard_step_oop(ctx, g, FP16, count, None, 1, p_in, m_in, v_in, p_out, m_in,
                              a[count + 8:2 * count + 8], h, hp, 1, sc)
     assert e.value.status == zs.ZS_ERR_ARG
+
+
+@pytest.mark.parametrize("n,G,count", [(3, 2, 10_007), (2, 1, 8_192)])
+def test_two_phase_update_oop_equals_the_one_call_form(zs, ctx, n, G, count):
+    """zs_update_oop over two ranges with one flag, then zs_scaler_update on
+    that flag: the written set equals zs_shard_step_oop's bit for bit, and
+    the flag and scale agree, skipped steps included."""
+    dtype = FP16
+    rng = np.random.default_rng(n * 7 + G)
+    master0 = (rng.standard_normal(count) * 0.02).astype(np.float32)
+    hp_vals = (STRESS_LR, 0.9, 0.999, 1e-8, 0.01)
+    hp = zs.make_hparams(*hp_vals)
+    sc_a = zs.zs_scaler_init(1024.0, 1.0, 2, 1, True)   # one call
+    sc_b = zs.zs_scaler_init(1024.0, 1.0, 2, 1, True)   # two phases
+    a_sets = [state_set(master0, count), state_set(np.zeros_like(master0), count)]
+    b_sets = [state_set(master0, count), state_set(np.zeros_like(master0), count)]
+    acc_a = torch.zeros(count, dtype=torch.float32, device="cuda")
+    acc_b = torch.zeros_like(acc_a)
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cut = 4096
+    cur = t = 0
+    for s in range(1, 7):
+        grads = [rand_grads(rng, n, count, dtype, sc_a.scale) for _ in range(G)]
+        if s == 3:
+            grads[G - 1][0][count - 5] = 0x7C00      # in the second range
+        dg = [[dev16(x) for x in micro] for micro in grads]
+        for k in range(G - 1):
+            zs.zs_grad_accum(ctx, dg[k], dtype, count, acc_a, k == 0)
+        src, dst = a_sets[cur], a_sets[cur ^ 1]
+        ovf_a, _ = zs.zs_shard_step_oop(ctx, dg[G - 1], dtype, count, acc_a if G > 1 else None,
+                                        G, src["p"], src["m"], src["v"], dst["p"], dst["m"],
+                                        dst["v"], dst["h"], hp, t + 1, sc_a)
+        flag.zero_()
+        for k in range(G - 1):
+            zs.zs_reduce_check(ctx, dg[k], dtype, count, acc_b, k == 0, flag)
+        src, dst = b_sets[cur], b_sets[cur ^ 1]
+        div = float(n * G * sc_b.scale)
+        for lo, hi in ((0, cut), (cut, count)):
+            r = slice(lo, hi)
+            zs.zs_update_oop(ctx, [g[r] for g in dg[G - 1]], dtype, hi - lo,
+                             acc_b[r] if G > 1 else None, div, src["p"][r], src["m"][r],
+                             src["v"][r], dst["p"][r], dst["m"][r], dst["v"][r], dst["h"][r], hp,
+                             t + 1, flag)
+        ovf_b = zs.zs_scaler_update(ctx, flag, sc_b)
+        assert ovf_a == ovf_b == (1 if s == 3 else 0) and sc_a.scale == sc_b.scale, s
+        if not ovf_a:
+            cur ^= 1
+            t += 1
+            for k in ("p", "m", "v", "h"):
+                assert torch.equal(a_sets[cur][k], b_sets[cur][k]), (s, k)

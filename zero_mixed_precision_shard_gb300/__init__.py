@@ -136,6 +136,8 @@ def _load():
                                   ctypes.POINTER(zs_adam_hparams), i64, ctypes.POINTER(zs_scaler),
                                   f32, i32p, ctypes.POINTER(ctypes.c_float),
                                   ctypes.POINTER(ctypes.c_float), vp],
+        "zs_update_oop": [vp, pp, i32, i32, i64, vp, f32, vp, vp, vp, vp, vp, vp, vp,
+                          ctypes.POINTER(zs_adam_hparams), i64, vp, vp],
         "zs_ctx_set_timing": [vp, i32],
         "zs_ctx_set_fused": [vp, i32, i64],
         "zs_ctx_fused_capacity": [vp, i64p],
@@ -455,6 +457,18 @@ def zs_shard_step_oop(ctx: Ctx, grads, dt, count: int, acc, accum_steps: int, ma
                                     _addr(half_out), ctypes.byref(hp), step, ctypes.byref(scaler),
                                     ctypes.byref(ovf), ctypes.byref(ns), _stream(stream)))
     return ovf.value, ns.value
+
+
+def zs_update_oop(ctx: Ctx, grads, dt, count: int, acc, grad_div: float, master_in, m_in, v_in,
+                  master_out, m_out, v_out, half_out, hp: zs_adam_hparams, step: int, d_flag,
+                  stream=None):
+    """The two-phase out-of-place update of one range: ORs its flag into d_flag
+    and writes the *_out buffers whatever the flag (the commit is the caller's,
+    after zs_scaler_update)."""
+    ctx.check(lib.zs_update_oop(ctx.handle, _ptrs(grads), len(grads), _dtype(dt), count,
+                                _addr(acc), grad_div, _addr(master_in), _addr(m_in), _addr(v_in),
+                                _addr(master_out), _addr(m_out), _addr(v_out), _addr(half_out),
+                                ctypes.byref(hp), step, _addr(d_flag), _stream(stream)))
 
 
 def zs_shard_step_async_oop(ctx: Ctx, grads, dt, count: int, acc, accum_steps: int, master,

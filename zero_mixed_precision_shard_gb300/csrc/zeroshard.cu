@@ -635,15 +635,16 @@ template <bool DEV>
 zs_status update_oop(zs_ctx* c, zs_dtype dt, const zs::SlicePtrs& sp, int32_t n,
                      const float* acc, const zs::OopBufs& b, int64_t count,
                      const zs::AdamArgs& ad, const zs::AdamArgs* ad_dev,
-                     const zs_device_state* st, cudaStream_t s) {
+                     const zs_device_state* st, cudaStream_t s, int32_t* flag = nullptr) {
+  if (flag == nullptr) flag = c->d_flag;
   LaunchScope ls(c, s, ZS_KERNEL_UPDATE_OOP, count);
   if (count > 0) {
     if (dt == ZS_FP16) {
-      if (acc) launch_oop_k<ZS_FP16, true, DEV>(c, sp, n, acc, b, count, ad, ad_dev, st, c->d_flag, s);
-      else launch_oop_k<ZS_FP16, false, DEV>(c, sp, n, acc, b, count, ad, ad_dev, st, c->d_flag, s);
+      if (acc) launch_oop_k<ZS_FP16, true, DEV>(c, sp, n, acc, b, count, ad, ad_dev, st, flag, s);
+      else launch_oop_k<ZS_FP16, false, DEV>(c, sp, n, acc, b, count, ad, ad_dev, st, flag, s);
     } else {
-      if (acc) launch_oop_k<ZS_BF16, true, DEV>(c, sp, n, acc, b, count, ad, ad_dev, st, c->d_flag, s);
-      else launch_oop_k<ZS_BF16, false, DEV>(c, sp, n, acc, b, count, ad, ad_dev, st, c->d_flag, s);
+      if (acc) launch_oop_k<ZS_BF16, true, DEV>(c, sp, n, acc, b, count, ad, ad_dev, st, flag, s);
+      else launch_oop_k<ZS_BF16, false, DEV>(c, sp, n, acc, b, count, ad, ad_dev, st, flag, s);
     }
   }
   cudaError_t e = cudaGetLastError();
@@ -1396,6 +1397,37 @@ zs_status zs_shard_step_oop(zs_ctx* c, const void* const* grads, int32_t n, zs_d
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(c, e, "commit launch");
   return finish_step(c, scaler, overflow_out, new_scale_out, nullptr, stream);
+}
+
+zs_status zs_update_oop(zs_ctx* c, const void* const* grads, int32_t n, zs_dtype dt,
+                        int64_t count, const float* acc, float grad_div, const float* master_in,
+                        const float* m_in, const float* v_in, float* master_out, float* m_out,
+                        float* v_out, void* half_out, const zs_adam_hparams* hp, int64_t step,
+                        int32_t* d_flag, cudaStream_t stream) {
+  NvtxRange nvtx_("zs_update_oop");
+  ZS_TRY(check_ctx(c));
+  ZS_TRY(check_hparams(c, hp, step));
+  if (d_flag == nullptr) return fail(c, ZS_ERR_ARG, "d_flag is NULL");
+  if (!(grad_div > 0.0f) || !std::isfinite(grad_div))
+    return fail(c, ZS_ERR_ARG, "grad_div must be a positive finite number");
+  zs::SlicePtrs sp;
+  const float* pp[2] = {master_in, master_out};
+  const float* mm[2] = {m_in, m_out};
+  const float* vv[2] = {v_in, v_out};
+  const void* hh[2] = {nullptr, half_out};
+  ZS_TRY(check_oop(c, grads, n, dt, count, acc, acc ? 2 : 1, pp, mm, vv, hh, &sp));
+  if (count == 0) return ZS_OK;
+  const zs::AdamArgs ad = adam_args(hp, step, grad_div);
+  zs::OopBufs b;
+  b.p[0] = const_cast<float*>(master_in);
+  b.p[1] = master_out;
+  b.m[0] = const_cast<float*>(m_in);
+  b.m[1] = m_out;
+  b.v[0] = const_cast<float*>(v_in);
+  b.v[1] = v_out;
+  b.h[0] = nullptr;
+  b.h[1] = static_cast<uint16_t*>(half_out);
+  return update_oop<false>(c, dt, sp, n, acc, b, count, ad, nullptr, nullptr, stream, d_flag);
 }
 
 zs_status zs_shard_step_async_oop(zs_ctx* c, const void* const* grads, int32_t n, zs_dtype dt,

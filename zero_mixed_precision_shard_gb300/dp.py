@@ -199,6 +199,17 @@ class Zero2Step:
           None), writing nothing if flag != 0;
       scaler_update(flag) -> int: the loss-scale update; returns the overflow;
       half_shard: this rank's half copy of its shard (the all-gather's input).
+    Ops that hold a second state set (oop = True) also provide
+      update_oop(rows, offset, length, flag): the last micro-step's sums of a
+          range (acc, or +0 when G = 1, + the rows in rank order), the flag,
+          and the update from the current set into the other one, written
+          whatever the flag;
+      commit_oop(flag) -> int: the loss-scale update; on a clean step the
+          written set becomes current.  Returns the overflow.
+    Unclipped steps then take the last micro-step out of place, bucket by
+    bucket as the exchange delivers it: the sum is never written back, and no
+    pass over the shard follows the exchange (the clipping norm needs every
+    final sum before the update, so clipped steps materialise).
     The library's kernels are the ops on GPUs (ZsShardOps); the tests also
     drive this choreography with the oracle as the ops, on CPU."""
 
@@ -231,18 +242,23 @@ class Zero2Step:
         gather = self.E * (self.world - 1) * elem_bytes
         return {"grad_sent": sent, "grad_received": recv, "param_gather_received": gather}
 
-    def micro_step(self, grad_flat, first: bool):
+    def micro_step(self, grad_flat, first: bool, oop_last: bool = False):
         """Exchange one micro-step's flat gradient bucket by bucket and sum the
-        received slices of this rank's shard onto the accumulator."""
+        received slices of this rank's shard onto the accumulator (oop_last:
+        the step's last micro-step, summed and applied out of place per bucket)."""
         pending = None
 
         def consume(p):
             work, b, rows = p
             if work is not None:
                 work.wait()
-            if b.length:
-                self.ops.accumulate([rows[r] for r in range(self.world)], b.offset, b.length,
-                                    first, self.flag)
+            if not b.length:
+                return
+            r = [rows[q] for q in range(self.world)]
+            if oop_last:
+                self.ops.update_oop(r, b.offset, b.length, self.flag)
+            else:
+                self.ops.accumulate(r, b.offset, b.length, first, self.flag)
 
         for i, b in enumerate(self.plan):
             buf = self.slots[i % len(self.slots)]
@@ -276,28 +292,50 @@ class Zero2Step:
             self.x.all_gather(half_full, self.ops.half_shard)
         return ovf
 
+    def finish_oop(self, half_full) -> int:
+        """The boundary of an out-of-place step: agree on the flag, commit (or
+        keep the current set), rescale, rebuild the half parameters."""
+        self.x.all_reduce(self.flag, "max")
+        ovf = self.ops.commit_oop(self.flag)
+        if not ovf:
+            self.x.all_gather(half_full, self.ops.half_shard)
+        return ovf
+
     def step(self, grads, half_full, clip: bool = False) -> int:
         """A whole step: grads[k] is this rank's flat gradient of micro-step k."""
         self.flag.zero_()
+        oop = getattr(self.ops, "oop", False) and not clip
         for k, g in enumerate(grads):
-            self.micro_step(g, k == 0)
-        return self.finish(half_full, clip)
+            self.micro_step(g, k == 0, oop_last=oop and k == len(grads) - 1)
+        return self.finish_oop(half_full) if oop else self.finish(half_full, clip)
 
 
 class ZsShardOps:
     """Zero2Step's local compute through the library (the C ABI): the
     accumulate is zs_reduce_check on the received rows, the norm
     zs_grad_sumsq, the update zs_apply / zs_apply_clipped from the
-    accumulator, the scale zs_scaler_update."""
+    accumulator, the scale zs_scaler_update.  With a second state set
+    (`second` = (master, m, v, half_shard)) unclipped steps apply the last
+    micro-step out of place (zs_update_oop per bucket, then the commit)."""
 
     def __init__(self, zs, ctx, dt, count: int, world: int, accum_steps: int, acc, master, m, v,
-                 half_shard, hp, scaler, max_norm: float = 0.0):
+                 half_shard, hp, scaler, max_norm: float = 0.0, second=None):
         self.zs, self.ctx, self.dt = zs, ctx, dt
         self.count, self.world, self.g = count, world, accum_steps
-        self.acc, self.master, self.m, self.v = acc, master, m, v
-        self.half_shard = half_shard
+        self.acc = acc
+        self.sets = [(master, m, v, half_shard)]
+        if second is not None:
+            self.sets.append(tuple(second))
+        self.cur = 0
+        self.oop = second is not None
         self.hp, self.scaler, self.max_norm = hp, scaler, max_norm
         self.t = 0
+
+    # the current state set
+    master = property(lambda self: self.sets[self.cur][0])
+    m = property(lambda self: self.sets[self.cur][1])
+    v = property(lambda self: self.sets[self.cur][2])
+    half_shard = property(lambda self: self.sets[self.cur][3])
 
     def _div(self) -> float:
         return float(self.world * self.g * self.scaler.scale)
@@ -323,4 +361,18 @@ class ZsShardOps:
         ovf = self.zs.zs_scaler_update(self.ctx, flag, self.scaler)
         if not ovf:
             self.t += 1
+        return ovf
+
+    def update_oop(self, rows, offset, length, flag):
+        src, dst = self.sets[self.cur], self.sets[self.cur ^ 1]
+        r = slice(offset, offset + length)
+        acc = self.acc[r] if self.g > 1 else None
+        self.zs.zs_update_oop(self.ctx, rows, self.dt, length, acc, self._div(), src[0][r],
+                              src[1][r], src[2][r], dst[0][r], dst[1][r], dst[2][r], dst[3][r],
+                              self.hp, self.t + 1, flag)
+
+    def commit_oop(self, flag) -> int:
+        ovf = self.scaler_update(flag)
+        if not ovf:
+            self.cur ^= 1
         return ovf
