@@ -258,10 +258,10 @@ class DeviceWorkload:
 
     def takes_fused(self, ctx, api: str) -> bool:
         """Whether `api`'s last call runs as the fused single-kernel step here:
-        the unclipped fp32-accumulator forms, when the shard fits one
+        the fp32-accumulator forms (clipped or not), when the shard fits one
         co-resident grid (and the context has the fused step on)."""
         return (api in ("async", "async_oop", "graph", "sync") and self.acc_kind == "fp32"
-                and not self.clip and self.E <= ctx.fused_capacity
+                and self.E <= ctx.fused_capacity
                 and os.environ.get("ZEROSHARD_FUSED", "1") != "0")
 
     def step_oop_calls(self, ctx, state):

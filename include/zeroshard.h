@@ -157,15 +157,18 @@ zs_status zs_ctx_destroy(zs_ctx* ctx);
 
 /* The fused step (§2.2, §4.2: the step's overflow resolved before any state
  * is written, here by a grid barrier inside one kernel).
- * zs_shard_step, zs_shard_step_async, zs_shard_step_oop and
- * zs_shard_step_async_oop (not the clipped forms) run the whole last call of
- * a step as ONE cooperative kernel when one thread per 8 owned elements fits a
- * grid whose CTAs are all resident at once (on GB300 about 1.2M elements):
- * each thread loads its elements' last micro-step sums (acc + the n slices, in
- * the order zs_grad_accum adds them) and their state into registers, the grid
- * ORs the overflow flag, one grid barrier resolves it, and a clean step
- * applies the same AdamW arithmetic from the registers; an overflow writes no
- * state.  Results are bit for bit those of the multi-kernel path.  The barrier
+ * zs_shard_step, zs_shard_step_async, zs_shard_step_oop,
+ * zs_shard_step_async_oop, zs_shard_step_clipped and
+ * zs_shard_step_async_clipped run the whole last call of a step as ONE
+ * cooperative kernel when one thread per 8 owned elements fits a grid whose
+ * CTAs are all resident at once (zs_ctx_fused_capacity: about 0.93M elements
+ * on GB300): each thread loads its elements' last micro-step sums (acc + the
+ * n slices, in the order zs_grad_accum adds them) and their state into
+ * registers, the grid ORs the overflow flag (and, clipped, each CTA's total
+ * of squares, folded by the last CTA in the order of the norm pass), one grid
+ * barrier resolves it, and a clean step applies the same AdamW arithmetic
+ * from the registers; an overflow writes no state.  Results (norm included)
+ * are bit for bit those of the multi-kernel path.  The barrier
  * wait is bounded: a CTA that waits longer than wait_ns gives up and writes
  * nothing, and the context's next call (the synchronising forms: the call
  * itself) returns ZS_ERR_TIMEOUT after resetting the barrier and the flag;

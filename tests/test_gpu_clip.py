@@ -22,9 +22,13 @@ def zs():
     return pkg
 
 
-@pytest.fixture(scope="module")
-def ctx(zs):
+@pytest.fixture(scope="module", params=["fused", "multi"])
+def ctx(zs, request):
+    """Every test runs with the fused single-kernel step (where the shard fits
+    one co-resident grid; the norm then travels with its grid barrier) and
+    with the multi-kernel path."""
     c = zs.Ctx()
+    c.set_fused(zs.ZS_FUSED_ON if request.param == "fused" else zs.ZS_FUSED_OFF)
     yield c
     c.close()
 

@@ -366,3 +366,63 @@ def test_device_state_step_equals_the_synchronising_step_bitwise(zs, mode):
             same_state(a, b, s)
     finally:
         ctx.close()
+
+
+@pytest.mark.parametrize("form", ["sync", "async"])
+@pytest.mark.parametrize("n,G,count,max_norm", [(1, 3, 50_001, 0.05), (2, 1, 8_191, 0.01),
+                                                (5, 2, 524_288, 0.02), (3, 1, 7, 1e-6)])
+def test_fused_clipped_steps_equal_the_multi_kernel_path(zs, ctxs, form, n, G, count, max_norm):
+    """The clipped forms through the fused kernel: each CTA's total of squares
+    travels with the grid barrier and the last CTA folds the totals in the
+    norm pass's order, so the norm, the coefficient and every state buffer
+    equal the multi-kernel path's bit for bit, step after step (an overflow
+    included), and the state stays within the oracle's bound."""
+    on, off = ctxs
+    dtype = FP16
+    rng = np.random.default_rng(7 * n + G + count % 101)
+    master0 = (rng.standard_normal(count) * 0.02).astype(np.float32)
+    hp, hp_o = zs.make_hparams(*HP), oracle.make_hparams(*HP)
+    st = oracle.ShardState.from_master(master0, dtype)
+    sc_o = oracle.make_scaler(1024.0, 1.0, 3, 1, True)
+    sets = {c: state_set(master0, count) for c in ("on", "off")}
+    accs = {c: torch.zeros(count, dtype=torch.float32, device="cuda") for c in ("on", "off")}
+    scs = {c: zs.zs_scaler_init(1024.0, 1.0, 3, 1, True) for c in ("on", "off")}
+    states = {c: zs.DeviceState(zs.zs_scaler_init(1024.0, 1.0, 3, 1, True)) for c in ("on", "off")}
+    norms = {c: torch.zeros(1, dtype=torch.float64, device="cuda") for c in ("on", "off")}
+    f0 = fused_launches(zs, on)
+    t = t_o = 0
+    for s in range(1, 7):
+        grads = [rand_grads(rng, n, count, dtype, sc_o.scale) for _ in range(G)]
+        if s == 3:
+            grads[G - 1][n - 1][count // 2] = 0x7C00
+        ovf_o, t_o, _, norm_o = oracle.shard_step(grads, dtype, st, hp_o, t_o, sc_o,
+                                                  max_norm=max_norm, return_norm=True)
+        dg = [[dev16(x) for x in micro] for micro in grads]
+        res = {}
+        for name, ctx in (("on", on), ("off", off)):
+            b, acc = sets[name], accs[name]
+            for k in range(G - 1):
+                zs.zs_grad_accum(ctx, dg[k], dtype, count, acc, k == 0)
+            a = acc if G > 1 else None
+            if form == "sync":
+                res[name] = zs.zs_shard_step_clipped(ctx, dg[G - 1], dtype, count, a, G, b["p"],
+                                                     b["m"], b["v"], b["h"], hp, t + 1,
+                                                     scs[name], max_norm)
+            else:
+                zs.zs_shard_step_async_clipped(ctx, dg[G - 1], dtype, count, a, G, b["p"],
+                                               b["m"], b["v"], b["h"], hp, None, max_norm,
+                                               states[name], norms[name])
+                d = states[name].read()
+                res[name] = (d.overflow, d.scaler.scale, norms[name].item())
+        assert res["on"][:2] == res["off"][:2] == (ovf_o, sc_o.scale), s
+        if not ovf_o:
+            assert res["on"][2] == res["off"][2], s          # the norm, bit for bit
+            assert abs(res["on"][2] - norm_o) <= 1e-6 * norm_o
+            t += 1
+        same_state(sets["on"], sets["off"], s)
+    assert t == t_o
+    assert fused_launches(zs, on) - f0 == 6
+    got = sets["on"]
+    assert_close(got["p"].cpu().numpy(), st.master, "master")
+    assert_close(got["m"].cpu().numpy(), st.m, "m")
+    assert_close(got["v"].cpu().numpy(), st.v, "v")

@@ -685,11 +685,14 @@ struct FusedCall {
   zs_lr_schedule sched{};
   int32_t has_sched = 0;
   int32_t accum_steps = 1;
+  float max_norm = 0.0f;       // clipping (> 0): the fused kernel forms the norm too
+  double inv_div2 = 1.0;       // 1 / grad_div^2 (host constants) for the squared norm
+  double* norm_out = nullptr;  // device forms: the step's norm (may be NULL)
 };
 
-template <int DT, bool HA, bool DEV, bool FLIP>
+template <int DT, bool HA, bool DEV, bool FLIP, bool CLIP>
 int fused_launch_k(zs_ctx* c, const FusedCall& f, cudaStream_t s, cudaError_t* e) {
-  auto k = zs::k_step_fused<DT, HA, DEV, FLIP>;
+  auto k = zs::k_step_fused<DT, HA, DEV, FLIP, CLIP>;
   const int64_t per_grid = (int64_t)resident_ctas(c, k) * c->sms;
   int64_t grid = ((f.count >> 3) + zs::kThreads - 1) / zs::kThreads;
   if (grid < 1) grid = 1;
@@ -700,7 +703,8 @@ int fused_launch_k(zs_ctx* c, const FusedCall& f, cudaStream_t s, cudaError_t* e
   *e = launch_coop(k, (int)grid, s, f.sp, f.n, f.acc, f.b, f.count, f.ad, f.scaler,
                    DEV ? (zs::StepResult*)nullptr : c->d_result, f.dstate, f.hp, f.sched,
                    f.has_sched, f.accum_steps, c->d_args, c->d_flag, c->d_sync, expect,
-                   (uint64_t)c->wait_ns, c->d_fused_err);
+                   (uint64_t)c->wait_ns, c->d_fused_err, f.max_norm, f.inv_div2,
+                   c->d_norm_parts, c->d_sumsq, f.norm_out);
   if (*e == cudaErrorCooperativeLaunchTooLarge) {
     // fewer SMs than the occupancy query assumed (e.g. a share of the GPU under
     // MPS): nothing was launched; the multi-kernel path takes the step
@@ -717,29 +721,29 @@ int fused_launch_k(zs_ctx* c, const FusedCall& f, cudaStream_t s, cudaError_t* e
 // The whole last call of a step as ONE kernel where it applies (the mode is on,
 // there is work, and one 8-element unit per thread fits a co-resident grid).
 // Returns false to take the multi-pass path; otherwise *st is the launch's status.
-template <bool DEV, bool FLIP>
+template <bool DEV, bool FLIP, bool CLIP = false>
 bool try_fused(zs_ctx* c, zs_dtype dt, const FusedCall& f, cudaStream_t s, zs_status* st) {
   if (c->fused_mode == ZS_FUSED_OFF || f.count <= 0) return false;
   cudaError_t e = cudaSuccess;
   int grid;
   if (dt == ZS_FP16)
-    grid = f.acc ? fused_launch_k<ZS_FP16, true, DEV, FLIP>(c, f, s, &e)
-                 : fused_launch_k<ZS_FP16, false, DEV, FLIP>(c, f, s, &e);
+    grid = f.acc ? fused_launch_k<ZS_FP16, true, DEV, FLIP, CLIP>(c, f, s, &e)
+                 : fused_launch_k<ZS_FP16, false, DEV, FLIP, CLIP>(c, f, s, &e);
   else
-    grid = f.acc ? fused_launch_k<ZS_BF16, true, DEV, FLIP>(c, f, s, &e)
-                 : fused_launch_k<ZS_BF16, false, DEV, FLIP>(c, f, s, &e);
+    grid = f.acc ? fused_launch_k<ZS_BF16, true, DEV, FLIP, CLIP>(c, f, s, &e)
+                 : fused_launch_k<ZS_BF16, false, DEV, FLIP, CLIP>(c, f, s, &e);
   if (grid == 0) return false;
   *st = e == cudaSuccess ? ZS_OK : cuda_fail(c, e, "fused step launch");
   return true;
 }
 
 // Co-resident CTAs per SM of the fused step: the fewest over its variants.
-template <bool DEV, bool FLIP>
+template <bool DEV, bool FLIP, bool CLIP>
 int fused_resident(zs_ctx* c) {
-  int r = resident_ctas(c, zs::k_step_fused<ZS_FP16, true, DEV, FLIP>);
-  r = std::min(r, resident_ctas(c, zs::k_step_fused<ZS_FP16, false, DEV, FLIP>));
-  r = std::min(r, resident_ctas(c, zs::k_step_fused<ZS_BF16, true, DEV, FLIP>));
-  return std::min(r, resident_ctas(c, zs::k_step_fused<ZS_BF16, false, DEV, FLIP>));
+  int r = resident_ctas(c, zs::k_step_fused<ZS_FP16, true, DEV, FLIP, CLIP>);
+  r = std::min(r, resident_ctas(c, zs::k_step_fused<ZS_FP16, false, DEV, FLIP, CLIP>));
+  r = std::min(r, resident_ctas(c, zs::k_step_fused<ZS_BF16, true, DEV, FLIP, CLIP>));
+  return std::min(r, resident_ctas(c, zs::k_step_fused<ZS_BF16, false, DEV, FLIP, CLIP>));
 }
 
 zs::OopBufs in_place_bufs(float* master, float* m, float* v, void* half_out) {
@@ -960,9 +964,11 @@ const char* zs_last_error(const zs_ctx* c) { return c ? c->err.c_str() : "null c
 
 zs_status zs_ctx_fused_capacity(zs_ctx* c, int64_t* elements) {
   if (c == nullptr || elements == nullptr) return ZS_ERR_ARG;
-  int r = fused_resident<false, false>(c);
-  r = std::min(r, fused_resident<true, false>(c));
-  r = std::min(r, fused_resident<true, true>(c));
+  int r = fused_resident<false, false, false>(c);
+  r = std::min(r, fused_resident<true, false, false>(c));
+  r = std::min(r, fused_resident<true, true, false>(c));
+  r = std::min(r, fused_resident<false, false, true>(c));
+  r = std::min(r, fused_resident<true, false, true>(c));
   // one 8-element unit per thread; the < 8 tail elements ride on CTA 0
   *elements = (int64_t)r * c->sms * zs::kThreads * 8 + 7;
   return ZS_OK;
@@ -1100,7 +1106,7 @@ static zs_status shard_step_impl(zs_ctx* c, const void* const* grads, int32_t n,
   const bool recompute = (n < 4) || acc == nullptr;
   const bool clip = max_norm > 0.0f;
   const float* acc_in = (accum_steps > 1 || !recompute) ? acc : nullptr;
-  if (!clip) {
+  {
     FusedCall f;
     f.sp = sp;
     f.n = n;
@@ -1110,10 +1116,24 @@ static zs_status shard_step_impl(zs_ctx* c, const void* const* grads, int32_t n,
     f.ad = ad;
     f.scaler = *scaler;
     f.accum_steps = accum_steps;
+    f.max_norm = max_norm;
+    f.inv_div2 = 1.0 / (div * div);
     zs_status fst = ZS_OK;
-    if (try_fused<false, false>(c, dt, f, stream, &fst)) {
+    const bool fused = clip ? try_fused<false, false, true>(c, dt, f, stream, &fst)
+                            : try_fused<false, false>(c, dt, f, stream, &fst);
+    if (fused) {
       ZS_TRY(fst);
-      return finish_fused_step(c, scaler, overflow_out, new_scale_out, stream);
+      if (clip) {
+        cudaError_t e = cudaMemcpyAsync(c->h_sumsq, c->d_sumsq, sizeof(double),
+                                        cudaMemcpyDeviceToHost, stream);
+        if (e != cudaSuccess) return cuda_fail(c, e, "sumsq copy");
+      }
+      ZS_TRY(finish_fused_step(c, scaler, overflow_out, new_scale_out, stream));
+      if (grad_norm_out) {
+        *grad_norm_out = 0.0f;
+        if (clip && c->h_result->overflow == 0) *grad_norm_out = (float)std::sqrt(*c->h_sumsq);
+      }
+      return ZS_OK;
     }
   }
   if (count > 0 && clip) {
@@ -1218,7 +1238,7 @@ static zs_status shard_step_async_impl(zs_ctx* c, const void* const* grads, int3
   }
   if (cap != cudaStreamCaptureStatusNone) c->timing = false;
   zs_status st = ZS_OK;
-  if (!clip) {
+  {
     FusedCall f;
     f.sp = sp;
     f.n = n;
@@ -1232,7 +1252,11 @@ static zs_status shard_step_async_impl(zs_ctx* c, const void* const* grads, int3
       f.has_sched = 1;
     }
     f.accum_steps = accum_steps;
-    if (try_fused<true, false>(c, dt, f, stream, &st)) {
+    f.max_norm = max_norm;
+    f.norm_out = d_norm;
+    const bool fused = clip ? try_fused<true, false, true>(c, dt, f, stream, &st)
+                            : try_fused<true, false>(c, dt, f, stream, &st);
+    if (fused) {
       c->timing = timing;
       return st;
     }

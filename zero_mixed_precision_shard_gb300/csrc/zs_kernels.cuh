@@ -624,6 +624,90 @@ __device__ __forceinline__ float sq8f(const float a[8]) {
   return __fadd_rn(__fadd_rn(s01, s23), __fadd_rn(s45, s67));
 }
 
+// The clipping norm's squares of one 8-element unit of final sums, added to
+// the thread's fp32 sums: a unit holding a sum above 1e18 in magnitude (whose
+// square could overflow fp32) is squared after an exact scaling by 2^-80 into
+// the second sum, which the CTA total scales back by 2^160 (finite fp32
+// values stay below 2^128, so the scaled squares stay below 2^96).
+__device__ __forceinline__ void norm_add8(const float a[8], float& sqf, float& sqb) {
+  bool b = false;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) b |= fabsf(a[k]) > 1e18f;
+  if (b) {
+    float t[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) t[k] = __fmul_rn(a[k], 0x1p-80f);
+    sqb = __fadd_rn(sqb, sq8f(t));
+  } else {
+    sqf = __fadd_rn(sqf, sq8f(a));
+  }
+}
+
+// The same for one tail element.
+__device__ __forceinline__ void norm_add1(float a, float& sqf, float& sqb) {
+  if (fabsf(a) > 1e18f) {
+    const float t = __fmul_rn(a, 0x1p-80f);
+    sqb = __fmaf_rn(t, t, sqb);
+  } else {
+    sqf = __fmaf_rn(a, a, sqf);
+  }
+}
+
+// The CTA's total of the threads' squares, with the OR of their `bad`, in one
+// CTA barrier: warp sums in fp32, then warp 0 adds the warp totals in fp32
+// (fixed tree) and converts once to fp64.  GB300's fp64 pipe is narrow: a
+// per-warp fp64 loop here (about 40 fp64 instructions per CTA) bounded the
+// whole pass.  Valid in thread 0 only.
+__device__ __forceinline__ double cta_norm_total(float sqf, float sqb, bool bad,
+                                                 bool* any_bad) {
+  static_assert((kThreads / 32) <= 32 && ((kThreads / 32) & (kThreads / 32 - 1)) == 0,
+                "warp totals are combined by one warp with a power-of-two tree");
+  __shared__ float wf[kThreads / 32];
+  __shared__ float wb[kThreads / 32];
+  __shared__ int wbad[kThreads / 32];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1)
+    sqf = __fadd_rn(sqf, __shfl_down_sync(0xffffffffu, sqf, off));
+  if (__any_sync(0xffffffffu, sqb != 0.0f)) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+      sqb = __fadd_rn(sqb, __shfl_down_sync(0xffffffffu, sqb, off));
+  }
+  const int wbd = __any_sync(0xffffffffu, bad);
+  if ((threadIdx.x & 31) == 0) {
+    wf[threadIdx.x >> 5] = sqf;
+    wb[threadIdx.x >> 5] = sqb;
+    wbad[threadIdx.x >> 5] = wbd;
+  }
+  __syncthreads();
+  double total = 0.0;
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    constexpr int kWarps = kThreads / 32;
+    float f = lane < kWarps ? wf[lane] : 0.0f;
+    float b = lane < kWarps ? wb[lane] : 0.0f;
+    const int any = __any_sync(0xffffffffu, lane < kWarps && wbad[lane] != 0);
+#pragma unroll
+    for (int off = kWarps / 2; off > 0; off >>= 1) {
+      f = __fadd_rn(f, __shfl_down_sync(0xffffffffu, f, off));
+      b = __fadd_rn(b, __shfl_down_sync(0xffffffffu, b, off));
+    }
+    total = b != 0.0f ? (double)f + (double)b * 0x1p160 : (double)f;
+    *any_bad = any != 0;
+  }
+  return total;
+}
+
+// Fixed-order fp64 sum of nparts CTA totals by the whole CTA (each thread
+// strides over them, then block_sum); valid in thread 0.  CG: read through L2
+// only (totals written by other CTAs of the same launch).
+template <bool CG>
+__device__ __forceinline__ double fold_partials(const double* partials, int nparts) {
+  double t = 0.0;
+  for (int i = threadIdx.x; i < nparts; i += kThreads) t += CG ? __ldcg(partials + i) : partials[i];
+  return block_sum(t);
+}
+
 // Reduce + accumulate + flag.  READ_ACC: start from acc (else +0.0f).
 // STORE: write the sums back to acc (otherwise only the flag is produced).
 // VPT vector units per thread per trip, `stride` apart so each load
@@ -692,19 +776,7 @@ __global__ void __launch_bounds__(ZS_THREADS, NORM && !STORE ? ZS_NORM_MIN_BLOCK
         for (int k = 0; k < 8; ++k) bad |= not_finite(a[j][k]);
         if constexpr (STORE) acc_st(acc + vi[j] * 8, a[j], pol);
       }
-      if constexpr (NORM) {
-        bool b = false;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) b |= fabsf(a[j][k]) > 1e18f;
-        if (b) {
-          float t[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) t[k] = __fmul_rn(a[j][k], 0x1p-80f);
-          sqb = __fadd_rn(sqb, sq8f(t));
-        } else {
-          sqf = __fadd_rn(sqf, sq8f(a[j]));
-        }
-      }
+      if constexpr (NORM) norm_add8(a[j], sqf, sqb);
     }
   }
   const int64_t tail = count - nvec * 8;
@@ -722,56 +794,16 @@ __global__ void __launch_bounds__(ZS_THREADS, NORM && !STORE ? ZS_NORM_MIN_BLOCK
       a = sum_slices1<DT>(s, n, i, a);
       bad |= not_finite(a);
       if constexpr (STORE) acc[i] = a;
-      if constexpr (NORM) {
-        if (fabsf(a) > 1e18f) {
-          const float t = __fmul_rn(a, 0x1p-80f);
-          sqb = __fmaf_rn(t, t, sqb);
-        } else {
-          sqf = __fmaf_rn(a, a, sqf);
-        }
-      }
+      if constexpr (NORM) norm_add1(a, sqf, sqb);
     }
   }
   if constexpr (NORM) {
-    // one barrier for the flag and the norm: warp sums in fp32, then warp 0
-    // adds the warp totals in fp32 (fixed tree) and converts once to fp64.
-    // GB300's fp64 pipe is narrow: a per-warp fp64 loop here (about 40 fp64
-    // instructions per CTA) bounded the whole pass.
-    static_assert((kThreads / 32) <= 32 && ((kThreads / 32) & (kThreads / 32 - 1)) == 0,
-                  "warp totals are combined by one warp with a power-of-two tree");
-    __shared__ float wf[kThreads / 32];
-    __shared__ float wb[kThreads / 32];
-    __shared__ int wbad[kThreads / 32];
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-      sqf = __fadd_rn(sqf, __shfl_down_sync(0xffffffffu, sqf, off));
-    if (__any_sync(0xffffffffu, sqb != 0.0f)) {
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1)
-        sqb = __fadd_rn(sqb, __shfl_down_sync(0xffffffffu, sqb, off));
-    }
-    const int wbd = __any_sync(0xffffffffu, bad);
-    if ((threadIdx.x & 31) == 0) {
-      wf[threadIdx.x >> 5] = sqf;
-      wb[threadIdx.x >> 5] = sqb;
-      wbad[threadIdx.x >> 5] = wbd;
-    }
-    __syncthreads();
-    if (threadIdx.x < 32) {
-      const int lane = threadIdx.x;
-      constexpr int kWarps = kThreads / 32;
-      float f = lane < kWarps ? wf[lane] : 0.0f;
-      float b = lane < kWarps ? wb[lane] : 0.0f;
-      const int any = __any_sync(0xffffffffu, lane < kWarps && wbad[lane] != 0);
-#pragma unroll
-      for (int off = kWarps / 2; off > 0; off >>= 1) {
-        f = __fadd_rn(f, __shfl_down_sync(0xffffffffu, f, off));
-        b = __fadd_rn(b, __shfl_down_sync(0xffffffffu, b, off));
-      }
-      if (lane == 0) {
-        partials[blockIdx.x] = b != 0.0f ? (double)f + (double)b * 0x1p160 : (double)f;
-        if (any) atomicOr(flag, 1);
-      }
+    // one barrier for the flag and the norm
+    bool any = false;
+    const double total = cta_norm_total(sqf, sqb, bad, &any);
+    if (threadIdx.x == 0) {
+      partials[blockIdx.x] = total;
+      if (any) atomicOr(flag, 1);
     }
     return;
   }
@@ -1024,6 +1056,17 @@ __global__ void k_commit_oop(int32_t* __restrict__ flag, zs_device_state* __rest
   *flag = 0;
 }
 
+// The clipping coefficient from the squared norm of the mean gradient:
+// max_norm / (norm + 1e-6) when that is below 1, else 1 (max_norm <= 0: 1).
+__device__ __forceinline__ float clip_coef_of_norm(double norm, float max_norm) {
+  double c = 1.0;
+  if (max_norm > 0.0f) {
+    const double q = (double)max_norm / (norm + 1e-6);
+    if (q < 1.0) c = q;
+  }
+  return (float)c;
+}
+
 // ---------------------------------------------------------------- fused step
 
 // Grid-wide barrier of the fused step (context scratch, zeroed at creation).
@@ -1033,7 +1076,7 @@ struct FusedSync {
   unsigned int arrived;  // CTAs of the running launch that have arrived
   unsigned int gen;      // launches resolved so far
   int32_t overflow;      // the step's flag as the last CTA to arrive read it
-  int32_t pad_;
+  float coef;            // the step's clipping coefficient (clipped steps)
 };
 
 __device__ __forceinline__ uint64_t global_ns() {
@@ -1070,22 +1113,31 @@ __device__ __forceinline__ AdamArgs load_args_cg(const AdamArgs* p) {
 // performs the loss-scale update: DEV, into the device state (flipping its
 // buffer index on a clean step when FLIP); otherwise into `result`.  DEV: CTA
 // 0 forms the step's constants from the device state before it arrives.
+// CLIP: each CTA writes its total of the squares of its sums to partials[]
+// before it arrives (as the norm-forming pass does, same CTA partition), and
+// the last CTA folds them in the same fixed order and forms the coefficient
+// (DEV: norm = sqrt(total) / (N*G*S) into *norm_out; else *sumsq_out = total *
+// inv_div2 and the coefficient from its root), which the others read after the
+// barrier.
 // b.X[cur] is read and b.X[cur ^ 1] written (cur = the device state's index
 // with FLIP, else 0; an in-place step passes the same buffers in both).
 // A CTA whose wait passes wait_ns gives up: it writes nothing and sets *err.
 // `expect` is the number of arrivals that resolve the step (the grid size).
-template <int DT, bool HAS_ACC, bool DEV, bool FLIP>
+template <int DT, bool HAS_ACC, bool DEV, bool FLIP, bool CLIP>
 __global__ void __launch_bounds__(ZS_THREADS, ZS_FUSED_MIN_BLOCKS)
     k_step_fused(const __grid_constant__ SlicePtrs s, int n, const float* acc,
                  const __grid_constant__ OopBufs b, int64_t count, AdamArgs ad_host,
                  zs_scaler scaler_in, StepResult* result, zs_device_state* dstate,
                  zs_adam_hparams hp, zs_lr_schedule sched, int has_sched, int accum_steps,
                  AdamArgs* ad_slot, int32_t* flag, FusedSync* sync, unsigned int expect,
-                 uint64_t wait_ns, int32_t* err) {
+                 uint64_t wait_ns, int32_t* err, float max_norm, double inv_div2,
+                 double* partials, double* sumsq_out, double* norm_out) {
   // Launched without the programmatic-dependent attribute (it starts once its
   // predecessor has completed), and it lets no successor start early either:
   // no griddepcontrol here, so no other grid's CTAs take SM room while it runs.
   __shared__ int s_go;
+  __shared__ int s_last;
+  __shared__ float s_coef;
   unsigned int gen0 = 0;
   if (threadIdx.x == 0) gen0 = ld_acquire(&sync->gen);
   int cur = 0;
@@ -1097,6 +1149,7 @@ __global__ void __launch_bounds__(ZS_THREADS, ZS_FUSED_MIN_BLOCKS)
   const int64_t ti = nvec * 8 + tid;
   float a[1][8], p[8], m[8], v[8];
   float at = 0.0f, pt = 0.0f, mt = 0.0f, vt = 0.0f;
+  float sqf = 0.0f, sqb = 0.0f;
   bool bad = false;
   if (unit) {
     if (HAS_ACC) {
@@ -1113,10 +1166,12 @@ __global__ void __launch_bounds__(ZS_THREADS, ZS_FUSED_MIN_BLOCKS)
     sum_slices<DT, 1>(s, n, vi, ok, a);
 #pragma unroll
     for (int k = 0; k < 8; ++k) bad |= not_finite(a[0][k]);
+    if constexpr (CLIP) norm_add8(a[0], sqf, sqb);
   }
   if (tail) {
     at = sum_slices1<DT>(s, n, ti, HAS_ACC ? acc[ti] : 0.0f);
     bad |= not_finite(at);
+    if constexpr (CLIP) norm_add1(at, sqf, sqb);
     pt = b.p[cur][ti];
     mt = b.m[cur][ti];
     vt = b.v[cur][ti];
@@ -1125,15 +1180,44 @@ __global__ void __launch_bounds__(ZS_THREADS, ZS_FUSED_MIN_BLOCKS)
     if (blockIdx.x == 0 && threadIdx.x == 0)
       *ad_slot = device_step_args(dstate, n, accum_steps, hp, sched, has_sched);
   }
-  const int any_bad = __syncthreads_or(bad);
+  int any_bad = 0;
+  if constexpr (CLIP) {
+    bool anyb = false;
+    const double total = cta_norm_total(sqf, sqb, bad, &anyb);
+    if (threadIdx.x == 0) {
+      partials[blockIdx.x] = total;
+      any_bad = anyb;
+    }
+  } else {
+    any_bad = __syncthreads_or(bad);
+  }
   if (threadIdx.x == 0) {
     if (any_bad) atomicOr(flag, 1);
     __threadfence();
-    int go = 0;
     const unsigned int prev = atomicAdd(&sync->arrived, 1u);
-    if (prev == expect - 1u) {
-      // last to arrive: every CTA's flag bits (and CTA 0's constants) are visible
-      __threadfence();
+    s_last = prev == expect - 1u;
+    // last to arrive: every CTA's flag bits, partials and (DEV) CTA 0's
+    // constants are visible after this fence
+    if (s_last) __threadfence();
+  }
+  __syncthreads();
+  if (s_last) {
+    float coef = 1.0f;
+    if constexpr (CLIP) {
+      const double t = fold_partials<true>(partials, (int)gridDim.x);
+      if (threadIdx.x == 0) {
+        if constexpr (DEV) {
+          const double norm = sqrt(t) / (double)load_args_cg(ad_slot).grad_div;
+          coef = clip_coef_of_norm(norm, max_norm);
+          if (norm_out != nullptr) *norm_out = norm;
+        } else {
+          const double sumsq = t * inv_div2;
+          coef = clip_coef_of_norm(sqrt(sumsq), max_norm);
+          *sumsq_out = sumsq;
+        }
+      }
+    }
+    if (threadIdx.x == 0) {
       const int32_t ovf = atomicExch(flag, 0) != 0 ? 1 : 0;
       if constexpr (DEV) {
         device_state_step(dstate, ovf, load_args_cg(ad_slot));
@@ -1142,31 +1226,36 @@ __global__ void __launch_bounds__(ZS_THREADS, ZS_FUSED_MIN_BLOCKS)
         if (result != nullptr) scaler_step(scaler_in, ovf, result);
       }
       sync->overflow = ovf;
+      sync->coef = coef;
       sync->arrived = 0u;
       __threadfence();
       atomicAdd(&sync->gen, 1u);
-      go = !ovf;
+      s_go = !ovf;
+      s_coef = coef;
+    }
+  } else if (threadIdx.x == 0) {
+    int go = 0;
+    const uint64_t t0 = global_ns();
+    bool released = false;
+    for (;;) {
+      if (ld_acquire(&sync->gen) != gen0) {
+        released = true;
+        break;
+      }
+      if (global_ns() - t0 > wait_ns) break;
+      __nanosleep(32);
+    }
+    if (released) {
+      go = __ldcg(&sync->overflow) == 0;
+      s_coef = __ldcg(&sync->coef);
     } else {
-      const uint64_t t0 = global_ns();
-      bool released = false;
-      for (;;) {
-        if (ld_acquire(&sync->gen) != gen0) {
-          released = true;
-          break;
-        }
-        if (global_ns() - t0 > wait_ns) break;
-        __nanosleep(32);
-      }
-      if (released) {
-        go = __ldcg(&sync->overflow) == 0;
-      } else {
-        *reinterpret_cast<volatile int32_t*>(err) = 1;
-      }
+      *reinterpret_cast<volatile int32_t*>(err) = 1;
     }
     s_go = go;
   }
   __syncthreads();
   if (!s_go) return;
+  const float coef = s_coef;
   AdamArgs ad = ad_host;
   if constexpr (DEV) {
     // one L2 read of the constants per CTA (every thread reading them hits one
@@ -1181,7 +1270,7 @@ __global__ void __launch_bounds__(ZS_THREADS, ZS_FUSED_MIN_BLOCKS)
   if (unit) {
     uint32_t h[4];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) adamw1<false>(ad, a[0][k], p[k], m[k], v[k]);
+    for (int k = 0; k < 8; ++k) adamw1<CLIP>(ad, a[0][k], p[k], m[k], v[k], coef);
 #pragma unroll
     for (int k = 0; k < 4; ++k)
       h[k] = float_to_half_bits<DT>(p[2 * k]) | (float_to_half_bits<DT>(p[2 * k + 1]) << 16);
@@ -1191,7 +1280,7 @@ __global__ void __launch_bounds__(ZS_THREADS, ZS_FUSED_MIN_BLOCKS)
     __stcs(reinterpret_cast<uint4*>(b.h[cur ^ 1]) + tid, make_uint4(h[0], h[1], h[2], h[3]));
   }
   if (tail) {
-    adamw1<false>(ad, at, pt, mt, vt);
+    adamw1<CLIP>(ad, at, pt, mt, vt, coef);
     b.p[cur ^ 1][ti] = pt;
     b.m[cur ^ 1][ti] = mt;
     b.v[cur ^ 1][ti] = vt;
@@ -1272,9 +1361,7 @@ __global__ void k_partials_reduce(const double* __restrict__ partials, int64_t n
 __global__ void k_sumsq_finalize(const double* __restrict__ partials, int nparts, double inv_div2,
                                  double* __restrict__ out) {
   pdl_enter(partials, out);
-  double t = 0.0;
-  for (int i = threadIdx.x; i < nparts; i += kThreads) t += partials[i];
-  t = block_sum(t);
+  const double t = fold_partials<false>(partials, nparts);
   if (threadIdx.x == 0) *out = t * inv_div2;
 }
 
@@ -1282,14 +1369,7 @@ __global__ void k_sumsq_finalize(const double* __restrict__ partials, int nparts
 __global__ void k_clip_coef(const double* __restrict__ sumsq, float max_norm,
                             float* __restrict__ coef) {
   pdl_enter(sumsq, coef);
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    double c = 1.0;
-    if (max_norm > 0.0f) {
-      const double q = (double)max_norm / (sqrt(*sumsq) + 1e-6);
-      if (q < 1.0) c = q;
-    }
-    *coef = (float)c;
-  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) *coef = clip_coef_of_norm(sqrt(*sumsq), max_norm);
 }
 
 // The device-resident step's coefficient: the sum of squares arrives unscaled
@@ -1301,12 +1381,7 @@ __global__ void k_clip_coef_dev(const double* __restrict__ sumsq_raw,
   pdl_enter(sumsq_raw, ad, coef, norm_out);
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     const double norm = sqrt(*sumsq_raw) / (double)ad->grad_div;
-    double c = 1.0;
-    if (max_norm > 0.0f) {
-      const double q = (double)max_norm / (norm + 1e-6);
-      if (q < 1.0) c = q;
-    }
-    *coef = (float)c;
+    *coef = clip_coef_of_norm(norm, max_norm);
     if (norm_out != nullptr) *norm_out = norm;
   }
 }
