@@ -1,8 +1,12 @@
 /* A plain C caller of libzeroshard: no Python, no torch.  Reads a step's
  * inputs from a file, runs G micro-steps through zs_grad_accum and
  * zs_shard_step with cudaMalloc'ed buffers, and writes the updated state.
- * With a third argument "oop" the last call is zs_shard_step_oop instead: the
- * new state lands in a second set of buffers, which a clean step makes current.
+ * A third argument picks another form of the last call: "oop" is
+ * zs_shard_step_oop (the new state lands in a second set of buffers, which a
+ * clean step makes current); "multi" is zs_shard_step with the fused
+ * single-kernel step turned off (zs_ctx_set_fused); "twophase" is
+ * zs_update_oop over two ranges with the context's flag, then
+ * zs_scaler_update on that flag.
  *
  * Input file:  int64 count, n, g; float scale; float lr, beta1, beta2, eps, wd;
  *              g*n*count uint16 gradients (micro-step major); count float master.
@@ -12,6 +16,7 @@
 #include <stdint.h>
 #include <stdio.h>
 #include <stdlib.h>
+#include <string.h>
 
 #include <cuda_runtime.h>
 
@@ -27,7 +32,11 @@
 
 int main(int argc, char** argv) {
   CHECK(argc == 3 || argc == 4);
-  const int oop = argc == 4;
+  const char* form = argc == 4 ? argv[3] : "";
+  const int oop = strcmp(form, "oop") == 0;
+  const int multi = strcmp(form, "multi") == 0;
+  const int twophase = strcmp(form, "twophase") == 0;
+  CHECK(argc == 3 || oop || multi || twophase);
   FILE* in = fopen(argv[1], "rb");
   CHECK(in != NULL);
   int64_t hdr[3];
@@ -63,6 +72,7 @@ int main(int argc, char** argv) {
 
   zs_ctx* ctx = NULL;
   CHECK(zs_ctx_create(&ctx) == ZS_OK);
+  if (multi) CHECK(zs_ctx_set_fused(ctx, ZS_FUSED_OFF, 0) == ZS_OK);
   zs_scaler sc;
   CHECK(zs_scaler_init(&sc, f[0], 1.0f, 1000, 1, 1) == ZS_OK);
   zs_adam_hparams hp = {f[1], f[2], f[3], f[4], f[5]};
@@ -75,7 +85,37 @@ int main(int argc, char** argv) {
   int32_t ovf = -1;
   float new_scale = 0.0f;
   zs_status st;
-  if (!oop) {
+  if (twophase) {
+    /* two ranges of the last micro-step, each summed, flagged and updated into
+     * the second set; the context's flag decides the commit */
+    float *master2, *m2, *v2;
+    uint16_t* half2;
+    CHECK(cudaMalloc((void**)&master2, count * 4) == cudaSuccess);
+    CHECK(cudaMalloc((void**)&m2, count * 4) == cudaSuccess);
+    CHECK(cudaMalloc((void**)&v2, count * 4) == cudaSuccess);
+    CHECK(cudaMalloc((void**)&half2, count * 2) == cudaSuccess);
+    int32_t* d_flag = NULL;
+    CHECK(zs_ctx_overflow_flag(ctx, &d_flag) == ZS_OK);
+    const int64_t cut = count / 2 / 64 * 64;
+    const float div = (float)n * (float)g * sc.scale;
+    st = ZS_OK;
+    for (int part = 0; part < 2 && st == ZS_OK; ++part) {
+      const int64_t lo = part ? cut : 0, len = part ? count - cut : cut;
+      const void* rows[256];
+      for (int64_t r = 0; r < n; ++r) rows[r] = (const uint16_t*)dgrad[(g - 1) * n + r] + lo;
+      st = zs_update_oop(ctx, rows, (int32_t)n, ZS_FP16, len, g > 1 ? acc + lo : NULL, div,
+                         master + lo, m + lo, v + lo, master2 + lo, m2 + lo, v2 + lo, half2 + lo,
+                         &hp, 1, d_flag, 0);
+    }
+    if (st == ZS_OK) st = zs_scaler_update(ctx, d_flag, &sc, &ovf, 0);
+    new_scale = sc.scale;
+    if (st == ZS_OK && ovf == 0) {
+      master = master2;
+      m = m2;
+      v = v2;
+      half = half2;
+    }
+  } else if (!oop) {
     st = zs_shard_step(ctx, (const void* const*)(dgrad + (g - 1) * n), (int32_t)n, ZS_FP16, count,
                        acc, (int32_t)g, master, m, v, half, &hp, 1, &sc, &ovf, &new_scale, 0);
   } else {

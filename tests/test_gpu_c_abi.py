@@ -1,7 +1,9 @@
 """The C ABI from plain C: tests/c_abi_main.c links libzeroshard.so and the
 CUDA runtime only (no Python, no torch), runs one step with cudaMalloc'ed
-buffers (in place, or out of place with the caller swapping to the written
-set), and its output is compared with the oracle."""
+buffers (in place through the fused step or the multi-kernel path, out of
+place with the caller swapping to the written set, or the two-phase
+out-of-place update over two ranges), and its output is compared with the
+oracle."""
 import os
 import subprocess
 
@@ -27,7 +29,7 @@ def build_c_caller(tmp_path):
     return exe
 
 
-@pytest.mark.parametrize("form", ["in_place", "oop"])
+@pytest.mark.parametrize("form", ["in_place", "oop", "multi", "twophase"])
 def test_plain_c_caller_matches_oracle(tmp_path, form):
     exe = build_c_caller(tmp_path)
     rng = np.random.default_rng(77)
@@ -42,7 +44,7 @@ def test_plain_c_caller_matches_oracle(tmp_path, form):
         fh.write(np.ascontiguousarray(grads).tobytes())
         fh.write(master0.tobytes())
     out = tmp_path / "out.bin"
-    subprocess.check_call([exe, str(inp), str(out)] + (["oop"] if form == "oop" else []))
+    subprocess.check_call([exe, str(inp), str(out)] + ([] if form == "in_place" else [form]))
     raw = open(out, "rb").read()
     ovf = np.frombuffer(raw[:4], np.int32)[0]
     new_scale = np.frombuffer(raw[4:8], np.float32)[0]
