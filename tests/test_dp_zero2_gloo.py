@@ -10,6 +10,7 @@ one rank skipping the step on all; in place, and with the last micro-step
 summed and applied out of place bucket by bucket, then committed by the
 agreed flag.  Also the bucket plan's host arithmetic.
 No GPU."""
+import datetime
 import os
 import socket
 
@@ -52,14 +53,14 @@ def master_init(psi_pad):
 HP = (1e-3, 0.9, 0.999, 1e-8, 0.01)
 
 
-def reference_union(world, max_norm):
+def reference_union(world, max_norm, steps=STEPS):
     psi_pad, E = oracle.partition(PSI, world)
     m0 = master_init(psi_pad)
     states = [oracle.ShardState.from_master(m0[q * E:(q + 1) * E], 0) for q in range(world)]
     hp = oracle.make_hparams(*HP)
     sc = oracle.make_scaler(1024.0, window=2)
     t, flags = 0, []
-    for s in range(1, STEPS + 1):
+    for s in range(1, steps + 1):
         g = full_grads(world, s, sc.scale, psi_pad)
         per = [[[np.ascontiguousarray(g[r][k][q * E:(q + 1) * E]) for r in range(world)]
                 for k in range(G)] for q in range(world)]
@@ -228,3 +229,48 @@ def test_zero2_single_rank_without_a_process_group():
         assert f == f_o
     assert ops.st.master.tobytes() == st.master.tobytes()
     assert half_full.numpy().view(np.uint16).tobytes() == st.half.tobytes()
+
+
+FAIL_AT = 5
+
+
+def failing_worker(rank, world, port, outdir):
+    """Rank 1 fails on the host before step FAIL_AT's exchange (an exception,
+    then the process exits); rank 0 must learn it from its next collective,
+    which ends with an error within the group's timeout instead of waiting
+    forever, its state that of the steps before."""
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world,
+                            timeout=datetime.timedelta(seconds=20))
+    psi_pad, E = oracle.partition(PSI, world)
+    m0 = master_init(psi_pad)
+    ops = OracleOps(m0[rank * E:(rank + 1) * E], world, 0.0)
+    half_full = torch.from_numpy(oracle.f32_to_half(m0, 0).view(np.int16).copy())
+    z = Zero2Step(ops, psi_pad, E, rank, 1024, torch.zeros(world * 1024, dtype=torch.int16),
+                  torch.zeros(1, dtype=torch.int32))
+    applied, error = 0, ""
+    try:
+        for s in range(1, STEPS + 1):
+            if rank == 1 and s == FAIL_AT:
+                raise RuntimeError("rank 1 failed before its exchange")
+            g = full_grads(world, s, ops.sc.scale, psi_pad)[rank]
+            z.step([torch.from_numpy(x.view(np.int16)) for x in g], half_full)
+            applied = s
+    except Exception as e:  # the failure as each rank sees it
+        error = f"{type(e).__name__}: {e}"[:300]
+    np.savez(os.path.join(outdir, f"rank{rank}.npz"), master=ops.st.master, applied=applied,
+             error=error, t=ops.t)
+    os._exit(0)   # no teardown of a broken group
+
+
+def test_a_rank_that_fails_ends_the_others_next_exchange(tmp_path):
+    mp.spawn(failing_worker, args=(2, free_port(), str(tmp_path)), nprocs=2, join=True)
+    r0, r1 = (np.load(tmp_path / f"rank{r}.npz") for r in range(2))
+    assert "rank 1 failed" in str(r1["error"]) and int(r1["applied"]) == FAIL_AT - 1
+    assert str(r0["error"]) != ""                     # its exchange ended with an error
+    assert int(r0["applied"]) == FAIL_AT - 1
+    # rank 0 holds exactly the state of the steps before the failure (one of them skipped)
+    _, states, _, t = reference_union(2, 0.0, steps=FAIL_AT - 1)
+    assert int(r0["t"]) == t == FAIL_AT - 2
+    assert r0["master"].tobytes() == states[0].master.tobytes()
