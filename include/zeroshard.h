@@ -176,7 +176,9 @@ zs_status zs_ctx_destroy(zs_ctx* ctx);
  * mode: ZS_FUSED_OFF (always the multi-kernel path), ZS_FUSED_ON (default),
  * ZS_FUSED_TEST_TIMEOUT (as ON, but the barrier waits for one CTA more than
  * the grid has, so every fused step's wait runs out: for testing the timeout
- * path).  wait_ns <= 0 keeps the default of one second. */
+ * path).  wait_ns <= 0 keeps the default of one second.  A device without
+ * cooperative launches starts with the fused step off, and turning it on
+ * there returns ZS_ERR_ARG. */
 #define ZS_FUSED_OFF 0
 #define ZS_FUSED_ON 1
 #define ZS_FUSED_TEST_TIMEOUT 2

@@ -110,22 +110,24 @@ def test_oop_steps_equal_the_in_place_step_and_the_oracle(zs, ctx, dtype, n, G, 
     assert half_ulps(host16(now["h"]), st.half).max() <= 1
 
 
+@pytest.mark.parametrize("dtype", [FP16, BF16])
 @pytest.mark.parametrize("graph", [False, True])
 @pytest.mark.parametrize("n,G,count", [(1, 3, 20_011), (8, 2, 40_003), (64, 1, 4_103)])
-def test_async_oop_steps_match_oracle(zs, ctx, n, G, count, graph):
+def test_async_oop_steps_match_oracle(zs, ctx, n, G, count, graph, dtype):
     """The device-resident form: the buffer index in the device state flips on
     every applied step; against the oracle with a WarmupDecayLR schedule, an
-    overflow and a CUDA-graph replay."""
-    dtype = FP16
-    rng = np.random.default_rng(n + 10 * G + (100 if graph else 0))
+    overflow and a CUDA-graph replay (fp16 with a dynamic scale, bf16 with a
+    static one)."""
+    rng = np.random.default_rng(n + 10 * G + (100 if graph else 0) + 1000 * dtype)
     master0 = (rng.standard_normal(count) * 0.02).astype(np.float32)
     st = oracle.ShardState.from_master(master0, dtype)
-    sc_o = oracle.make_scaler(512.0, 1.0, 2, 1, True)
+    dyn = dtype == FP16
+    sc_o = oracle.make_scaler(512.0 if dyn else 1.0, 1.0, 2, 1, dyn)
     kind, mn, mx, wu, tot = (oracle.LR_WARMUP_DECAY, float(np.float32(1e-5)),
                              float(np.float32(STRESS_LR)), 3, 9)
     sched = zs.make_schedule(kind, mn, mx, wu, tot)
     hp = zs.make_hparams(mx, 0.9, 0.999, 1e-8, 0.01)
-    state = zs.DeviceState(zs.zs_scaler_init(sc_o.scale, 1.0, 2, 1, True))
+    state = zs.DeviceState(zs.zs_scaler_init(sc_o.scale, 1.0, 2, 1, dyn))
     sets = [state_set(master0, count), state_set(np.zeros_like(master0), count)]
     acc = torch.zeros(count, dtype=torch.float32, device="cuda")
     pad = (count + 7) // 8 * 8
@@ -145,7 +147,7 @@ def test_async_oop_steps_match_oracle(zs, ctx, n, G, count, graph):
         grads = [[lib_half((rng.standard_normal(count) * 1e-2 * sc_o.scale).astype(np.float32),
                            dtype) for _ in range(n)] for _ in range(G)]
         if s == 5:
-            grads[G - 1][n - 1][count - 1] = 0x7C00
+            grads[G - 1][n - 1][count - 1] = 0x7C00 if dyn else 0x7F80
         host = np.stack([np.stack(mc) for mc in grads]).view(np.int16)
         gbuf[:, :, :count].copy_(torch.from_numpy(host))
         lr_t = oracle.lr_at(kind, mn, mx, wu, tot, t_o + 1)
@@ -235,3 +237,29 @@ def test_two_phase_update_oop_equals_the_one_call_form(zs, ctx, n, G, count):
             t += 1
             for k in ("p", "m", "v", "h"):
                 assert torch.equal(a_sets[cur][k], b_sets[cur][k]), (s, k)
+
+
+def test_update_oop_rejects_bad_arguments(zs, ctx):
+    """Rejected before any work: no flag, a non-positive grad_div, the in and
+    out sets overlapping, a range start off the 16-byte grid."""
+    count = 256
+    a = torch.zeros(8 * count, dtype=torch.float32, device="cuda")
+    h = torch.zeros(2 * count, dtype=torch.int16, device="cuda")
+    g = [torch.zeros(2 * count, dtype=torch.int16, device="cuda")]
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    hp = zs.make_hparams(1e-4)
+    sets = [a[k * count:(k + 1) * count] for k in range(6)]
+
+    def call(grads=g, div=2.0, d_flag=flag, s=sets, half=h[:count], n=count):
+        zs.zs_update_oop(ctx, grads, FP16, n, None, div, *s, half, hp, 1, d_flag)
+
+    call()                                            # well-formed: accepted
+    for kw, status in (({"d_flag": None}, zs.ZS_ERR_ARG), ({"div": 0.0}, zs.ZS_ERR_ARG),
+                       ({"div": float("inf")}, zs.ZS_ERR_ARG),
+                       ({"s": sets[:3] + [sets[0]] + sets[4:]}, zs.ZS_ERR_ARG),
+                       ({"grads": [g[0][1:count + 1]]}, zs.ZS_ERR_ALIGN),
+                       ({"s": [a[1:count + 1]] + sets[1:]}, zs.ZS_ERR_ALIGN)):
+        with pytest.raises(zs.ZsError) as e:
+            call(**kw)
+        assert e.value.status == status, kw
+    assert flag.item() == 0

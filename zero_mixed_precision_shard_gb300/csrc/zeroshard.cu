@@ -894,6 +894,9 @@ zs_status zs_ctx_create(zs_ctx** out) {
   cudaError_t e = cudaGetDevice(&c->device);
   if (e == cudaSuccess)
     e = cudaDeviceGetAttribute(&c->sms, cudaDevAttrMultiProcessorCount, c->device);
+  int coop = 0;
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, c->device);
+  if (coop == 0) c->fused_mode = ZS_FUSED_OFF;  // no cooperative launches: multi-kernel path
   if (e == cudaSuccess) e = cudaMalloc(&c->d_flag, sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMemset(c->d_flag, 0, sizeof(int32_t));
   if (e == cudaSuccess)
@@ -978,6 +981,11 @@ zs_status zs_ctx_set_fused(zs_ctx* c, int32_t mode, int64_t wait_ns) {
   if (c == nullptr) return ZS_ERR_ARG;
   if (mode != ZS_FUSED_OFF && mode != ZS_FUSED_ON && mode != ZS_FUSED_TEST_TIMEOUT)
     return fail(c, ZS_ERR_ARG, "unknown fused mode %d", (int)mode);
+  int coop = 0;
+  if (mode != ZS_FUSED_OFF &&
+      (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, c->device) != cudaSuccess ||
+       coop == 0))
+    return fail(c, ZS_ERR_ARG, "device %d has no cooperative launches", c->device);
   c->fused_mode = mode;
   c->wait_ns = wait_ns > 0 ? (uint64_t)wait_ns : ZS_DEFAULT_WAIT_NS;
   return ZS_OK;
