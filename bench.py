@@ -70,7 +70,7 @@ def kernel_alg_bytes(kind: str, n: int, first: bool = False, with_acc: bool = Fa
     if kind == "sumsq":   # a separate norm pass: acc and/or the re-read slices
         return (4 if with_acc else 0) + (2 * n if first else 0)
     if kind == "update_oop":   # last micro-step + flag + update, state written out of place
-        return (4 if with_acc else 0) + 2 * n + 26
+        return (acc_bytes if with_acc else 0) + 2 * n + 26
     if kind == "fused":   # last micro-step + flag + grid barrier + update, one kernel
         return (4 if with_acc else 0) + 2 * n + 26
     raise ValueError(kind)
@@ -90,9 +90,12 @@ def step_launch_plan(n: int, g: int, dtype: str, acc_kind: str = "fp32", has_acc
         plan.append(("fused", kernel_alg_bytes("fused", n, with_acc=g > 1)))
         return plan
     if oop:
+        ab = 2 if acc_kind == "half" else 4
         plan = [("reduce_first" if k == 0 else "reduce",
-                 kernel_alg_bytes("reduce", n, first=(k == 0))) for k in range(g - 1)]
-        plan.append(("update_oop", kernel_alg_bytes("update_oop", n, with_acc=g > 1)))
+                 kernel_alg_bytes("reduce", n, first=(k == 0), acc_bytes=ab))
+                for k in range(g - 1)]
+        plan.append(("update_oop", kernel_alg_bytes("update_oop", n, with_acc=g > 1,
+                                                    acc_bytes=ab)))
         return plan
     if acc_kind == "half":
         plan = [("reduce_first" if k == 0 else "reduce",
@@ -144,6 +147,7 @@ class DeviceWorkload:
         self.grads = torch.empty((self.nbuf, n, E), dtype=torch.int16, device=self.dev)
         self.acc_kind = acc
         self.clip = clip
+        self.hacc_oop = False   # set by the caller once every buffer is allocated
         if acc == "half":
             self.acc = torch.empty(E, dtype=torch.int16, device=self.dev)
         else:
@@ -206,7 +210,22 @@ class DeviceWorkload:
         call); returns the overflow flag."""
         zs, wl = self.zs, self.wl
         last = self.slices(wl.g - 1)
-        if self.acc_kind == "half":
+        if self.acc_kind == "half" and self.hacc_oop:
+            # out of place where the second state set fits: the last micro-step,
+            # its rounding to the half format, the flag and the update in one pass
+            if not hasattr(self, "_hset"):
+                import torch
+                self._hset = (torch.empty_like(self.master), torch.empty_like(self.m),
+                              torch.empty_like(self.v), torch.empty_like(self.half))
+            dst = self._hset
+            ovf, _ = zs.zs_shard_step_halfacc_oop(ctx, last, self.dt, self.E,
+                                                  self.acc if wl.g > 1 else None, wl.g,
+                                                  self.master, self.m, self.v, *dst, self.hp,
+                                                  self.t + 1, self.scaler)
+            if not ovf:
+                self._hset = (self.master, self.m, self.v, self.half)
+                self.master, self.m, self.v, self.half = dst
+        elif self.acc_kind == "half":
             ovf, _ = zs.zs_shard_step_halfacc(ctx, last, self.dt, self.E, self.acc, wl.g,
                                               self.master, self.m, self.v, self.half, self.hp,
                                               self.t + 1, self.scaler)
@@ -961,12 +980,14 @@ def run_ours(args):
     torch.cuda.synchronize()
     if api == "auto":
         api = "async_oop" if oop_fits(W.E) else "async"
+    # the half-accumulator step out of place where its second state set fits
+    hacc_oop = W.hacc_oop = args.acc == "half" and oop_fits(W.E)
     E = W.E
     valid = min(W.valid_end - W.begin, E)
     one_step, state = make_step(zs, ctx, W, api, args.clip)
     ms, launches, clock_summary = timed_steps(ctx, one_step, args.steps, args.warmup, dev, world)
     fused = W.takes_fused(ctx, api)
-    plan = W.launch_plan(split=api == "split", oop=api == "async_oop", fused=fused)
+    plan = W.launch_plan(split=api == "split", oop=api == "async_oop" or hacc_oop, fused=fused)
     if api == "graph":  # replays bypass the context's counter: the kernels of a captured step
         # (the streaming ones, the prologue and the flag reset; with clipping the
         # norm's finalize and the coefficient, and the fold of many partials;
@@ -1063,7 +1084,9 @@ def run_ours(args):
                                else "1 GPU",
                 "accumulator": args.acc,
                 "clip_max_norm": args.clip or None,
-                "api": ("zs_grad_accum_halfacc + zs_shard_step_halfacc" if args.acc == "half"
+                "api": ("zs_grad_accum_halfacc + zs_shard_step_halfacc"
+                        + ("_oop (the second state set fits)" if hacc_oop else "")
+                        if args.acc == "half"
                         else "zs_grad_accum + zs_shard_step_clipped" if args.clip and api == "sync"
                         else API_DESC[api].replace("zs_shard_step_async",
                                                    "zs_shard_step_async_clipped")

@@ -290,6 +290,23 @@ zs_status zs_shard_step_halfacc(zs_ctx* ctx, const void* const* grads, int32_t n
                                 int32_t* overflow_out, float* new_scale_out,
                                 cudaStream_t stream);
 
+/* The half-accumulator step with the state written out of place, as
+ * zs_shard_step_oop is to zs_shard_step: the last micro-step's sums (acc_half
+ * widened + the n slices, rounded to the 2-byte format as every micro-step's
+ * are), the overflow check (on the rounded sums) and the AdamW update in one
+ * pass from master_in/m_in/v_in into master_out/m_out/v_out and half_out (the
+ * last micro-step's sums are never written to acc_half); *overflow_out == 0 means the
+ * *_out buffers hold the state.  acc_half may be NULL when accum_steps ==
+ * 1.  Synchronises `stream`. */
+zs_status zs_shard_step_halfacc_oop(zs_ctx* ctx, const void* const* grads, int32_t n,
+                                    zs_dtype dt, int64_t count, const void* acc_half,
+                                    int32_t accum_steps, const float* master_in,
+                                    const float* m_in, const float* v_in, float* master_out,
+                                    float* m_out, float* v_out, void* half_out,
+                                    const zs_adam_hparams* hp, int64_t step, zs_scaler* scaler,
+                                    int32_t* overflow_out, float* new_scale_out,
+                                    cudaStream_t stream);
+
 /* ---------------------------------------------------------------- clipping */
 
 /* Global-norm gradient clipping (§4.1 gradient_clipping; §5.1: engine.step()

@@ -130,6 +130,14 @@ def test_out_of_place_plan_moves_exactly_the_algorithmic_bytes():
         assert sum(b for _, b in plan) == bench.alg_bytes_per_elem_step(wl.n, wl.g)
 
 
+def test_half_accumulator_oop_plan_moves_exactly_the_algorithmic_bytes():
+    for name in ("gpt2-small-n8", "decoder-1.3b-n16", "llama7b-n1"):
+        wl = synth.WORKLOADS[name]
+        plan = bench.step_launch_plan(wl.n, wl.g, wl.dtype, acc_kind="half", oop=True)
+        assert [k for k, _ in plan][-1] == "update_oop"
+        assert sum(b for _, b in plan) == bench.alg_bytes_per_elem_step(wl.n, wl.g, acc_bytes=2)
+
+
 def test_fused_plan_moves_exactly_the_algorithmic_bytes():
     """The fused step (shards that fit one co-resident grid): the carried
     micro-steps, then one kernel; nothing is read twice or written twice."""

@@ -121,3 +121,66 @@ def test_halfacc_shard_steps(zs, ctx, dtype, n, G, count):
     close(m.cpu().numpy(), st.m, "m")
     close(v.cpu().numpy(), st.v, "v")
     assert ulps(half.cpu().numpy().view(np.uint16), st.half).max() <= 1
+
+
+@pytest.mark.parametrize("dtype", [FP16, BF16])
+@pytest.mark.parametrize("n,G,count", [(1, 8, 30_011), (4, 2, 20_000), (16, 1, 5_003)])
+def test_halfacc_oop_steps_equal_the_in_place_step_and_the_oracle(zs, ctx, dtype, n, G, count):
+    """zs_shard_step_halfacc_oop: the last micro-step's sums rounded to the
+    accumulator's format, flagged and applied out of place in one pass.  The
+    written set equals the in-place half-accumulator step's state bit for bit,
+    step after step (an overflow, and a sum that rounds past the half maximum,
+    included: the current set stays untouched), and the oracle's within the bound."""
+    rng = np.random.default_rng(n * 5 + G + 50 * dtype)
+    master0 = (rng.standard_normal(count) * 0.02).astype(np.float32)
+    st = oracle.ShardState.from_master(master0, dtype)
+    dyn = dtype == FP16
+    sc_o = oracle.make_scaler(256.0 if dyn else 1.0, 1.0, 3, 1, dyn)
+    sc_a = zs.zs_scaler_init(sc_o.scale, 1.0, 3, 1, dyn)
+    sc_b = zs.zs_scaler_init(sc_o.scale, 1.0, 3, 1, dyn)
+    hp_v = (STRESS_LR, 0.9, 0.999, 1e-8, 0.01)
+    hp_o, hp = oracle.make_hparams(*hp_v), zs.make_hparams(*hp_v)
+
+    def state(m0):
+        p = torch.from_numpy(m0.copy()).cuda()
+        return [p, torch.zeros_like(p), torch.zeros_like(p),
+                torch.zeros(count, dtype=torch.int16, device="cuda")]
+    ref = state(master0)
+    sets = [state(master0), state(np.zeros_like(master0))]
+    acc_a = torch.zeros(count, dtype=torch.int16, device="cuda")
+    acc_b = torch.zeros_like(acc_a)
+    cur = t = t_o = 0
+    big = 40_000.0 if dtype == FP16 else 2.0e38    # two of them round past the half maximum
+    for s in range(1, 9):
+        grads = [[lib_half((rng.standard_normal(count) * 1e-2 * sc_o.scale).astype(np.float32),
+                           dtype) for _ in range(n)] for _ in range(G)]
+        if s == 4:
+            grads[0][n - 1][count // 3] = 0x7E00 if dtype == FP16 else 0x7FC0
+        if s == 6 and n * G > 1:
+            grads[0][0][7] = grads[G - 1][n - 1][7] = lib_half(np.float32([big]), dtype)[0]
+        ovf_o, t_o, _ = oracle.shard_step_halfacc(grads, dtype, st, hp_o, t_o, sc_o)
+        dg = [[dev16(x) for x in micro] for micro in grads]
+        for k in range(G - 1):
+            zs.zs_grad_accum_halfacc(ctx, dg[k], dtype, count, acc_a, k == 0)
+            zs.zs_grad_accum_halfacc(ctx, dg[k], dtype, count, acc_b, k == 0)
+        ovf_a, ns_a = zs.zs_shard_step_halfacc(ctx, dg[G - 1], dtype, count, acc_a, G, *ref, hp,
+                                               t + 1, sc_a)
+        src, dst = sets[cur], sets[cur ^ 1]
+        before = [x.clone() for x in src]
+        ovf_b, ns_b = zs.zs_shard_step_halfacc_oop(ctx, dg[G - 1], dtype, count,
+                                                   acc_b if G > 1 else None, G, *src[:3],
+                                                   *dst, hp, t + 1, sc_b)
+        assert ovf_a == ovf_b == ovf_o and ns_a == ns_b == sc_o.scale, f"step {s}"
+        if ovf_b:
+            assert all(torch.equal(x, y) for x, y in zip(before, src))
+        else:
+            cur ^= 1
+            t += 1
+        for k in range(3):
+            assert torch.equal(sets[cur][k], ref[k]), (s, k)
+        if t:
+            assert torch.equal(sets[cur][3], ref[3])
+    assert t == t_o
+    close(sets[cur][0].cpu().numpy(), st.master, "master")
+    close(sets[cur][1].cpu().numpy(), st.m, "m")
+    close(sets[cur][2].cpu().numpy(), st.v, "v")

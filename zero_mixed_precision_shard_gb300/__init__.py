@@ -138,6 +138,10 @@ def _load():
                                   ctypes.POINTER(ctypes.c_float), vp],
         "zs_update_oop": [vp, pp, i32, i32, i64, vp, f32, vp, vp, vp, vp, vp, vp, vp,
                           ctypes.POINTER(zs_adam_hparams), i64, vp, vp],
+        "zs_shard_step_halfacc_oop": [vp, pp, i32, i32, i64, vp, i32, vp, vp, vp, vp, vp, vp,
+                                      vp, ctypes.POINTER(zs_adam_hparams), i64,
+                                      ctypes.POINTER(zs_scaler), i32p,
+                                      ctypes.POINTER(ctypes.c_float), vp],
         "zs_ctx_set_timing": [vp, i32],
         "zs_ctx_set_fused": [vp, i32, i64],
         "zs_ctx_fused_capacity": [vp, i64p],
@@ -496,6 +500,21 @@ def zs_shard_step_halfacc(ctx: Ctx, grads, dt, count: int, acc_half, accum_steps
                                         _addr(v), _addr(half_out), ctypes.byref(hp), step,
                                         ctypes.byref(scaler), ctypes.byref(ovf),
                                         ctypes.byref(ns), _stream(stream)))
+    return ovf.value, ns.value
+
+
+def zs_shard_step_halfacc_oop(ctx: Ctx, grads, dt, count: int, acc_half, accum_steps: int,
+                              master_in, m_in, v_in, master_out, m_out, v_out, half_out,
+                              hp: zs_adam_hparams, step: int, scaler: zs_scaler, stream=None):
+    """Returns (overflow, new_scale); on overflow == 0 the *_out buffers hold the
+    new state.  *scaler is updated in place."""
+    ovf = ctypes.c_int32()
+    ns = ctypes.c_float()
+    ctx.check(lib.zs_shard_step_halfacc_oop(
+        ctx.handle, _ptrs(grads), len(grads), _dtype(dt), count, _addr(acc_half), accum_steps,
+        _addr(master_in), _addr(m_in), _addr(v_in), _addr(master_out), _addr(m_out),
+        _addr(v_out), _addr(half_out), ctypes.byref(hp), step, ctypes.byref(scaler),
+        ctypes.byref(ovf), ctypes.byref(ns), _stream(stream)))
     return ovf.value, ns.value
 
 

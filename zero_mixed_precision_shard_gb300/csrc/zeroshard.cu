@@ -621,12 +621,12 @@ void apply_dev(zs_ctx* c, const int32_t* flag, const zs::SlicePtrs& sp, int32_t 
 }
 
 // Out-of-place step: the update kernel and its commit.
-template <int DT, bool HA, bool DEV>
+template <int DT, bool HA, bool DEV, bool HACC = false>
 void launch_oop_k(zs_ctx* c, const zs::SlicePtrs& sp, int32_t n, const float* acc,
                   const zs::OopBufs& b, int64_t count, const zs::AdamArgs& ad,
                   const zs::AdamArgs* ad_dev, const zs_device_state* st, int32_t* flag,
                   cudaStream_t s) {
-  auto k = zs::k_update_oop<DT, HA, DEV>;
+  auto k = zs::k_update_oop<DT, HA, DEV, HACC>;
   launch_k(c, k, grid_for(c, k, (count >> 3) + 8), zs::kThreads, s, sp, n, acc, b, count, ad,
            ad_dev, st, flag, acc_keep_for(count));
 }
@@ -1583,6 +1583,60 @@ zs_status zs_shard_step_halfacc(zs_ctx* c, const void* const* grads, int32_t n, 
   ZS_TRY(apply_hacc(c, dt, c->d_flag, acc_half, count, ad, master, m, v, half_out, scaler,
                     c->d_result, stream));
   return finish_step(c, scaler, overflow_out, new_scale_out, c->d_flag, stream);
+}
+
+zs_status zs_shard_step_halfacc_oop(zs_ctx* c, const void* const* grads, int32_t n,
+                                    zs_dtype dt, int64_t count, const void* acc_half,
+                                    int32_t accum_steps, const float* master_in,
+                                    const float* m_in, const float* v_in, float* master_out,
+                                    float* m_out, float* v_out, void* half_out,
+                                    const zs_adam_hparams* hp, int64_t step, zs_scaler* scaler,
+                                    int32_t* overflow_out, float* new_scale_out,
+                                    cudaStream_t stream) {
+  NvtxRange nvtx_("zs_shard_step_halfacc_oop");
+  ZS_TRY(check_ctx(c));
+  ZS_TRY(check_hparams(c, hp, step));
+  ZS_TRY(check_scaler(c, scaler));
+  zs::SlicePtrs sp;
+  const float* pp[2] = {master_in, master_out};
+  const float* mm[2] = {m_in, m_out};
+  const float* vv[2] = {v_in, v_out};
+  const void* hh[2] = {nullptr, half_out};
+  const float* acc = accum_steps > 1 ? static_cast<const float*>(acc_half) : nullptr;
+  ZS_TRY(check_oop(c, grads, n, dt, count, acc, accum_steps, pp, mm, vv, hh, &sp));
+  const double div = (double)n * (double)accum_steps * (double)scaler->scale;
+  const float grad_div = (float)div;
+  if (!(grad_div > 0.0f) || !std::isfinite(grad_div))
+    return fail(c, ZS_ERR_ARG, "n * accum_steps * scale is not a positive finite fp32");
+  const zs::AdamArgs ad = adam_args(hp, step, grad_div);
+  zs::OopBufs b;
+  b.p[0] = const_cast<float*>(master_in);
+  b.p[1] = master_out;
+  b.m[0] = const_cast<float*>(m_in);
+  b.m[1] = m_out;
+  b.v[0] = const_cast<float*>(v_in);
+  b.v[1] = v_out;
+  b.h[0] = nullptr;
+  b.h[1] = static_cast<uint16_t*>(half_out);
+  if (count > 0) {
+    LaunchScope ls(c, stream, ZS_KERNEL_UPDATE_OOP, count);
+    if (dt == ZS_FP16) {
+      if (acc) launch_oop_k<ZS_FP16, true, false, true>(c, sp, n, acc, b, count, ad, nullptr, nullptr, c->d_flag, stream);
+      else launch_oop_k<ZS_FP16, false, false, true>(c, sp, n, acc, b, count, ad, nullptr, nullptr, c->d_flag, stream);
+    } else {
+      if (acc) launch_oop_k<ZS_BF16, true, false, true>(c, sp, n, acc, b, count, ad, nullptr, nullptr, c->d_flag, stream);
+      else launch_oop_k<ZS_BF16, false, false, true>(c, sp, n, acc, b, count, ad, nullptr, nullptr, c->d_flag, stream);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(c, e, "out-of-place update launch");
+    ls.done();
+  }
+  launch_k(c, zs::k_commit_oop<false>, 1, 32, stream, c->d_flag, (zs_device_state*)nullptr,
+           (const zs::AdamArgs*)nullptr, *scaler, c->d_result);
+  c->launches += 1;
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(c, e, "commit launch");
+  return finish_step(c, scaler, overflow_out, new_scale_out, nullptr, stream);
 }
 
 zs_status zs_grad_sumsq(zs_ctx* c, const void* const* grads, int32_t n, zs_dtype dt,

@@ -965,7 +965,10 @@ struct OopBufs {
 // to be, since nothing is committed until k_commit_oop has seen the whole
 // step's flag.  DEV: the step's constants come from k_step_prologue and the
 // current buffer index from the device state; otherwise from the host (cur 0).
-template <int DT, bool HAS_ACC, bool DEV>
+// HACC: acc holds the carried micro-steps in the gradient's 2-byte format, and
+// the final sums are rounded to it (as every micro-step's are) before the flag
+// and the update read them.
+template <int DT, bool HAS_ACC, bool DEV, bool HACC = false>
 __global__ void __launch_bounds__(ZS_THREADS, ZS_OOP_MIN_BLOCKS)
     k_update_oop(const __grid_constant__ SlicePtrs s, int n, const float* __restrict__ acc,
                  const __grid_constant__ OopBufs b, int64_t count, AdamArgs ad_host,
@@ -996,7 +999,11 @@ __global__ void __launch_bounds__(ZS_THREADS, ZS_OOP_MIN_BLOCKS)
     float a[1][8];
     float p[8], m[8], v[8];
     if (HAS_ACC) {
-      acc_ld(acc + base * 8, a[0], pol);
+      if constexpr (HACC) {
+        load8_hacc<DT>(acc, base, a[0]);
+      } else {
+        acc_ld(acc + base * 8, a[0], pol);
+      }
     } else {
 #pragma unroll
       for (int k = 0; k < 8; ++k) a[0][k] = 0.0f;
@@ -1005,10 +1012,11 @@ __global__ void __launch_bounds__(ZS_THREADS, ZS_OOP_MIN_BLOCKS)
     load8(min_ + base * 8, m);
     load8(vin + base * 8, v);
     sum_slices<DT, 1>(s, n, vi, ok, a);
+    if constexpr (HACC) (void)round8_hacc<DT>(a[0], &bad);
     uint32_t h[4];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      bad |= not_finite(a[0][k]);
+      if constexpr (!HACC) bad |= not_finite(a[0][k]);
       adamw1<false>(ad, a[0][k], p[k], m[k], v[k]);
     }
 #pragma unroll
@@ -1022,8 +1030,14 @@ __global__ void __launch_bounds__(ZS_THREADS, ZS_OOP_MIN_BLOCKS)
   const int64_t tail = count - nvec * 8;
   if (tid < tail) {
     const int64_t i = nvec * 8 + tid;
-    float a = HAS_ACC ? acc[i] : 0.0f;
+    float a;
+    if constexpr (HACC) {
+      a = HAS_ACC ? half_bits_to_float<DT>(reinterpret_cast<const uint16_t*>(acc)[i]) : 0.0f;
+    } else {
+      a = HAS_ACC ? acc[i] : 0.0f;
+    }
     a = sum_slices1<DT>(s, n, i, a);
+    if constexpr (HACC) a = half_bits_to_float<DT>(float_to_half_bits<DT>(a));
     bad |= not_finite(a);
     float p = pin[i], m = min_[i], v = vin[i];
     adamw1<false>(ad, a, p, m, v);
