@@ -1,8 +1,9 @@
 """Full-size workloads, in the launch configuration the benchmark times
 (bench.DeviceWorkload: zs_grad_accum for micro-steps 1..G-1, then the last
-call: zs_shard_step, zs_shard_step_async with the device-resident state, or
+call: zs_shard_step, zs_shard_step_async with the device-resident state,
 zs_shard_step_async_oop with the state written out of place, as the
-benchmark's default does where the second state set fits), checked against
+benchmark's default does where the second state set fits, or the half
+accumulator's zs_shard_step_halfacc_oop as its --acc half run), checked against
 the oracle on sampled elements, for the first shard and the last (which holds
 the padding where there is any, and the output layers).
 
@@ -67,7 +68,10 @@ def sample_positions(wl, begin, E, valid):
                                             ("llama7b-n1", 0, "async"),
                                             ("decoder-1.3b-n16", 0, "async_oop"),
                                             ("llama7b-zero3-n64", 63, "async_oop"),
-                                            ("llama7b-n1", 0, "async_oop")])
+                                            ("llama7b-n1", 0, "async_oop"),
+                                            # the half accumulator, out of place (the
+                                            # benchmark's --acc half run)
+                                            ("llama7b-n1", 0, "hacc_oop")])
 def test_fullsize_sampled(name, shard, api):
     import bench
     import zero_mixed_precision_shard_gb300 as zs
@@ -80,8 +84,12 @@ def test_fullsize_sampled(name, shard, api):
     # the out-of-place case holds two gradient buffers, refilled micro-step by
     # micro-step as a training loop does (the Llama-7B one: 243 GB with both
     # state sets; one buffer per micro-step would not fit)
-    W = bench.DeviceWorkload(wl, shard=shard, grad_buffers=2 if api == "async_oop" else None)
-    state = zs.DeviceState(W.scaler) if api != "sync" else None
+    refill = api in ("async_oop", "hacc_oop")
+    W = bench.DeviceWorkload(wl, shard=shard, grad_buffers=2 if refill else None,
+                             acc="half" if api == "hacc_oop" else "fp32")
+    W.hacc_oop = api == "hacc_oop"
+    state = zs.DeviceState(W.scaler) if api not in ("sync", "hacc_oop") else None
+    step_o = oracle.shard_step_halfacc if api == "hacc_oop" else oracle.shard_step
     E, begin = W.E, W.begin
     valid = W.valid_end - W.begin
     pos = sample_positions(wl, begin, E, valid)
@@ -112,14 +120,23 @@ def test_fullsize_sampled(name, shard, api):
         return worst
 
     for s in range(1, steps + 1):
-        if api != "async_oop":
+        if not refill:
             W.fill_grads(s, sc_o.scale, inject=True)
         grads = [[synth.host_grad_bits(wl, gidx, s, k + 1, r, sc_o.scale) for r in range(wl.n)]
                  for k in range(wl.g)]
         scheduled = any(begin <= j.index < begin + E for j in wl.injections_at(s))
-        ovf_o, t_o, _ = oracle.shard_step(grads, wl.dtype_code, st, hp_o, t_o, sc_o,
-                                          extra_overflow=int(scheduled))
-        if state is None:
+        ovf_o, t_o, _ = step_o(grads, wl.dtype_code, st, hp_o, t_o, sc_o,
+                               extra_overflow=int(scheduled))
+        if api == "hacc_oop":
+            # refilled micro-step by micro-step; the last call swaps W's state
+            # buffers to the written set on a clean step
+            for k in range(wl.g):
+                W.fill_micro(s, k, sc_o.scale, inject=True)
+                if k < wl.g - 1:
+                    W.accum(ctx, k)
+            ovf = W.finish(ctx)
+            scale = W.scaler.scale
+        elif state is None:
             ovf = W.step(ctx)
             scale = W.scaler.scale
         else:
