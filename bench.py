@@ -551,6 +551,8 @@ API_DESC = {
                  "of place: the last micro-step, the flag and the update in one pass)",
     "sync": "zs_grad_accum + zs_shard_step (one host round trip per step)",
     "graph": "CUDA graph of zs_grad_accum + zs_shard_step_async",
+    "graph_oop": "zs_grad_accum + zs_shard_step_async_oop captured once in a CUDA graph and "
+                 "replayed (no host launch work per step: the step's GPU rate)",
     "split": "zs_reduce_check / zs_check_last + zs_apply + zs_scaler_update (split at the flag)",
 }
 # the other target workloads, measured in the same run after the headline one
@@ -588,13 +590,14 @@ def make_step(zs, ctx, W: DeviceWorkload, api: str, clip: float = 0.0):
         def one_step():
             calls(ctx, state)
         return one_step, state
-    if api == "graph":
+    if api in ("graph", "graph_oop"):
         state = zs.DeviceState(W.scaler)
-        W.step_async_calls(ctx, state)       # uncaptured first call caches launch shapes
+        calls = W.step_oop_calls if api == "graph_oop" else W.step_async_calls
+        calls(ctx, state)       # uncaptured first call caches launch shapes (and buffers)
         torch.cuda.synchronize()
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
-            W.step_async_calls(ctx, state)
+            calls(ctx, state)
         return graph.replay, state
     if api == "sync":
         return (lambda: W.step(ctx)), None
@@ -712,18 +715,21 @@ def measure_table_workload(zs, ctx, name: str, args, peak: float, dev: int):
     # these steps take 0.3-2.5 ms: at least 100 of them, so that one stall of the
     # host (which the synchronising API waits on every step) cannot dominate
     steps = max(args.steps, 100)
-    for api in ("async", "async_oop", "sync"):
+    for api in ("async", "async_oop", "sync", "graph_oop"):
         one_step, state = make_step(zs, ctx, W, api)
         # the step rate without per-kernel events (an event pair around each of
         # a short step's launches costs it a few percent), then the same steps
-        # again with them for the per-kernel rates
+        # again with them for the per-kernel rates (none inside a graph replay)
         ms, launches, clocks = timed_steps(ctx, one_step, steps, args.warmup, dev, 1,
                                            kernel_timing=False)
         timed_steps(ctx, one_step, steps, 0, dev, 1)
         per_step = ms / steps
         gbs = step_bytes / (per_step * 1e-3) / 1e9
-        kinds = kernel_table(zs, ctx, W.launch_plan(oop=api == "async_oop",
-                                                    fused=W.takes_fused(ctx, api)))
+        oop = api in ("async_oop", "graph_oop")
+        plan = W.launch_plan(oop=oop, fused=W.takes_fused(ctx, "async_oop" if oop else api))
+        if api == "graph_oop":   # replays bypass the context's launch counter
+            launches = steps * (len(plan) + (0 if W.takes_fused(ctx, "async_oop") else 2))
+        kinds = kernel_table(zs, ctx, plan)
         out[api] = {"api": API_DESC[api], "value": valid / (per_step * 1e-3), "unit": "params/s",
                     "steps": steps, "ms_per_step": round(per_step, 6), "step_gbs": round(gbs, 1),
                     "step_frac_of_peak": round(gbs / peak, 4), "gpu_launches": launches,

@@ -84,3 +84,7 @@ def test_default_api_keeps_the_step_state_on_the_device_and_measures_the_table()
             assert a["gpu_launches"] >= 100 * 2 and a["steps"] == 100
         assert w["async"]["device_state"]["iterations"] == 3 + 2 * 100   # two timed passes
         assert "update_oop" in w["async_oop"]["kernels"]
+        # the same out-of-place step replayed from a CUDA graph: its GPU rate
+        g = w["graph_oop"]
+        assert g["value"] > 0 and g["step_frac_of_peak"] > 0 and g["gpu_launches"] >= 100 * 2
+        assert g["device_state"]["iterations"] == 1 + 3 + 2 * 100
