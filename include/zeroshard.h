@@ -169,10 +169,14 @@ zs_status zs_ctx_destroy(zs_ctx* ctx);
  * barrier resolves it, and a clean step applies the same AdamW arithmetic
  * from the registers; an overflow writes no state.  Results (norm included)
  * are bit for bit those of the multi-kernel path.  The barrier
- * wait is bounded: a CTA that waits longer than wait_ns gives up and writes
- * nothing, and the context's next call (the synchronising forms: the call
- * itself) returns ZS_ERR_TIMEOUT after resetting the barrier and the flag;
- * the state of that step is then undefined.
+ * relies on every CTA of the grid being resident at once, which the
+ * cooperative launch provides; its wait is bounded for the cases it may not
+ * (e.g. fused steps of several contexts running at the same time): a CTA that
+ * waits longer than wait_ns gives up and writes nothing, and the context's
+ * next call (the synchronising forms: the call itself) returns
+ * ZS_ERR_TIMEOUT after resetting the barrier and the flag; the state of that
+ * step is then undefined.  Run fused steps of different contexts in order,
+ * or turn the fused step off where they must overlap.
  * mode: ZS_FUSED_OFF (always the multi-kernel path), ZS_FUSED_ON (default),
  * ZS_FUSED_TEST_TIMEOUT (as ON, but the barrier waits for one CTA more than
  * the grid has, so every fused step's wait runs out: for testing the timeout
