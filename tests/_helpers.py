@@ -55,3 +55,16 @@ def tol_ratio(got, want):
 def assert_close(got, want, name):
     r = tol_ratio(got, want)
     assert r <= 1.0, f"{name}: worst error {r:.3g}x the bound (1e-6 rel + 1e-9 abs)"
+
+
+def assert_half_close(got_half, got_master, want_half, want_master, dtype, name="half"):
+    """The half copy is the round-to-nearest-even of the library's own fp32
+    master, every element; and within 1 ulp of the oracle's half copy wherever
+    the oracle's master is at least 1e-6 in magnitude.  Below that the master's
+    1e-9 absolute bound spans more than a bf16 ulp (bf16 keeps fp32's exponent
+    range), so two masters within the bar may round 2 ulps apart there."""
+    got_half = np.asarray(got_half).view(np.uint16)
+    assert (got_half == lib_half(np.asarray(got_master, np.float32), dtype)).all(), name
+    u = half_ulps(got_half, want_half)
+    big = np.abs(np.asarray(want_master)) >= 1e-6
+    assert u[big].max(initial=0) <= 1, name

@@ -690,11 +690,11 @@ struct FusedCall {
   double* norm_out = nullptr;  // device forms: the step's norm (may be NULL)
 };
 
-template <int DT, bool HA, bool DEV, bool FLIP, bool CLIP>
+template <int DT, bool HA, bool DEV, bool FLIP, bool CLIP, int EPT>
 int fused_launch_k(zs_ctx* c, const FusedCall& f, cudaStream_t s, cudaError_t* e) {
-  auto k = zs::k_step_fused<DT, HA, DEV, FLIP, CLIP>;
+  auto k = zs::k_step_fused<DT, HA, DEV, FLIP, CLIP, EPT>;
   const int64_t per_grid = (int64_t)resident_ctas(c, k) * c->sms;
-  int64_t grid = ((f.count >> 3) + zs::kThreads - 1) / zs::kThreads;
+  int64_t grid = ((f.count / EPT) + zs::kThreads - 1) / zs::kThreads;
   if (grid < 1) grid = 1;
   if (grid > per_grid || grid > c->coop_max_grid) return 0;
   // ZS_FUSED_TEST_TIMEOUT: the barrier waits for one CTA more than the grid has
@@ -721,17 +721,25 @@ int fused_launch_k(zs_ctx* c, const FusedCall& f, cudaStream_t s, cudaError_t* e
 // The whole last call of a step as ONE kernel where it applies (the mode is on,
 // there is work, and one 8-element unit per thread fits a co-resident grid).
 // Returns false to take the multi-pass path; otherwise *st is the launch's status.
+template <bool DEV, bool FLIP, bool CLIP, int EPT>
+int fused_dispatch(zs_ctx* c, zs_dtype dt, const FusedCall& f, cudaStream_t s, cudaError_t* e) {
+  if (dt == ZS_FP16)
+    return f.acc ? fused_launch_k<ZS_FP16, true, DEV, FLIP, CLIP, EPT>(c, f, s, e)
+                 : fused_launch_k<ZS_FP16, false, DEV, FLIP, CLIP, EPT>(c, f, s, e);
+  return f.acc ? fused_launch_k<ZS_BF16, true, DEV, FLIP, CLIP, EPT>(c, f, s, e)
+               : fused_launch_k<ZS_BF16, false, DEV, FLIP, CLIP, EPT>(c, f, s, e);
+}
+
 template <bool DEV, bool FLIP, bool CLIP = false>
 bool try_fused(zs_ctx* c, zs_dtype dt, const FusedCall& f, cudaStream_t s, zs_status* st) {
   if (c->fused_mode == ZS_FUSED_OFF || f.count <= 0) return false;
   cudaError_t e = cudaSuccess;
-  int grid;
-  if (dt == ZS_FP16)
-    grid = f.acc ? fused_launch_k<ZS_FP16, true, DEV, FLIP, CLIP>(c, f, s, &e)
-                 : fused_launch_k<ZS_FP16, false, DEV, FLIP, CLIP>(c, f, s, &e);
-  else
-    grid = f.acc ? fused_launch_k<ZS_BF16, true, DEV, FLIP, CLIP>(c, f, s, &e)
-                 : fused_launch_k<ZS_BF16, false, DEV, FLIP, CLIP>(c, f, s, &e);
+  int grid = 0;
+  // 4-element units (twice the threads, for latency) where they fit one
+  // co-resident grid; else 8-element units (the clipped forms always: their
+  // norm keeps the norm pass's CTA partition)
+  if constexpr (!CLIP) grid = fused_dispatch<DEV, FLIP, false, 4>(c, dt, f, s, &e);
+  if (grid == 0) grid = fused_dispatch<DEV, FLIP, CLIP, 8>(c, dt, f, s, &e);
   if (grid == 0) return false;
   *st = e == cudaSuccess ? ZS_OK : cuda_fail(c, e, "fused step launch");
   return true;
@@ -740,10 +748,10 @@ bool try_fused(zs_ctx* c, zs_dtype dt, const FusedCall& f, cudaStream_t s, zs_st
 // Co-resident CTAs per SM of the fused step: the fewest over its variants.
 template <bool DEV, bool FLIP, bool CLIP>
 int fused_resident(zs_ctx* c) {
-  int r = resident_ctas(c, zs::k_step_fused<ZS_FP16, true, DEV, FLIP, CLIP>);
-  r = std::min(r, resident_ctas(c, zs::k_step_fused<ZS_FP16, false, DEV, FLIP, CLIP>));
-  r = std::min(r, resident_ctas(c, zs::k_step_fused<ZS_BF16, true, DEV, FLIP, CLIP>));
-  return std::min(r, resident_ctas(c, zs::k_step_fused<ZS_BF16, false, DEV, FLIP, CLIP>));
+  int r = resident_ctas(c, zs::k_step_fused<ZS_FP16, true, DEV, FLIP, CLIP, 8>);
+  r = std::min(r, resident_ctas(c, zs::k_step_fused<ZS_FP16, false, DEV, FLIP, CLIP, 8>));
+  r = std::min(r, resident_ctas(c, zs::k_step_fused<ZS_BF16, true, DEV, FLIP, CLIP, 8>));
+  return std::min(r, resident_ctas(c, zs::k_step_fused<ZS_BF16, false, DEV, FLIP, CLIP, 8>));
 }
 
 zs::OopBufs in_place_bufs(float* master, float* m, float* v, void* half_out) {

@@ -100,6 +100,9 @@
 #ifndef ZS_FIRST_MIN_BLOCKS  // resident CTAs per SM the first micro-step's accumulate (one unit
 #define ZS_FIRST_MIN_BLOCKS 8    // per thread, no accumulator read) is compiled for: 32 registers,
 #endif                           // the full SM; the later micro-steps' pass runs best unbounded
+#ifndef ZS_FUSED4_MIN_BLOCKS  // the same for its 4-element-unit form (16 values held per
+#define ZS_FUSED4_MIN_BLOCKS 4    // thread across the barrier instead of 32)
+#endif
 #ifndef ZS_FUSED_MIN_BLOCKS  // resident CTAs per SM the fused step is compiled for (its
 #define ZS_FUSED_MIN_BLOCKS 3    // capacity: this x SMs x 256 threads x 8 elements); at 4 the
 #endif                           // 32 values a thread holds across the barrier spill
@@ -1116,6 +1119,70 @@ __device__ __forceinline__ AdamArgs load_args_cg(const AdamArgs* p) {
   return a;
 }
 
+// Units of EPT (8 or 4) consecutive elements for the fused step: element
+// order and per-element arithmetic are the same for both widths.
+template <int DT>
+__device__ __forceinline__ void add4(float a[4], const uint2 h) {
+  a[0] = __fadd_rn(a[0], half_bits_to_float<DT>(h.x & 0xFFFFu));
+  a[1] = __fadd_rn(a[1], half_bits_to_float<DT>(h.x >> 16));
+  a[2] = __fadd_rn(a[2], half_bits_to_float<DT>(h.y & 0xFFFFu));
+  a[3] = __fadd_rn(a[3], half_bits_to_float<DT>(h.y >> 16));
+}
+
+// a[0..EPT) += slice_0[u] + ... + slice_{n-1}[u] in rank order (unit u of EPT
+// elements); 8 loads are issued before their adds.
+template <int DT, int EPT>
+__device__ __forceinline__ void sum_unit(const SlicePtrs& s, int n, int64_t u, float (&a)[EPT]) {
+  if constexpr (EPT == 8) {
+    const int64_t vi[1] = {u};
+    const bool ok[1] = {true};
+    sum_slices<DT, 1>(s, n, vi, ok, *reinterpret_cast<float(*)[1][8]>(&a));
+  } else {
+    static_assert(EPT == 4, "units of 8 or 4 elements");
+    int r = 0;
+    for (; r + 8 <= n; r += 8) {
+      uint2 h[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) h[c] = __ldcs(reinterpret_cast<const uint2*>(s.p[r + c]) + u);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) add4<DT>(a, h[c]);
+    }
+    for (; r < n; ++r) add4<DT>(a, __ldcs(reinterpret_cast<const uint2*>(s.p[r]) + u));
+  }
+}
+
+template <int EPT>
+__device__ __forceinline__ void load_unit(const float* p, int64_t u, float (&a)[EPT]) {
+  if constexpr (EPT == 8) {
+    load8(p + u * 8, a);
+  } else {
+    const float4 x = *reinterpret_cast<const float4*>(p + u * 4);
+    a[0] = x.x; a[1] = x.y; a[2] = x.z; a[3] = x.w;
+  }
+}
+
+template <int EPT>
+__device__ __forceinline__ void store_unit(float* p, int64_t u, const float (&a)[EPT]) {
+  if constexpr (EPT == 8) {
+    store8_cs(p + u * 8, a);
+  } else {
+    __stcs(reinterpret_cast<float4*>(p + u * 4), make_float4(a[0], a[1], a[2], a[3]));
+  }
+}
+
+template <int DT, int EPT>
+__device__ __forceinline__ void store_half_unit(uint16_t* h, int64_t u, const float (&p)[EPT]) {
+  uint32_t w[EPT / 2];
+#pragma unroll
+  for (int k = 0; k < EPT / 2; ++k)
+    w[k] = float_to_half_bits<DT>(p[2 * k]) | (float_to_half_bits<DT>(p[2 * k + 1]) << 16);
+  if constexpr (EPT == 8) {
+    __stcs(reinterpret_cast<uint4*>(h) + u, make_uint4(w[0], w[1], w[2], w[3]));
+  } else {
+    __stcs(reinterpret_cast<uint2*>(h) + u, make_uint2(w[0], w[1]));
+  }
+}
+
 // The whole step of a shard whose 8-element units fit one co-resident grid
 // (one unit per thread, launched cooperatively): the last micro-step's sums
 // s = (acc or +0) + the n slices in rank order and the current master / m / v
@@ -1137,8 +1204,8 @@ __device__ __forceinline__ AdamArgs load_args_cg(const AdamArgs* p) {
 // with FLIP, else 0; an in-place step passes the same buffers in both).
 // A CTA whose wait passes wait_ns gives up: it writes nothing and sets *err.
 // `expect` is the number of arrivals that resolve the step (the grid size).
-template <int DT, bool HAS_ACC, bool DEV, bool FLIP, bool CLIP>
-__global__ void __launch_bounds__(ZS_THREADS, ZS_FUSED_MIN_BLOCKS)
+template <int DT, bool HAS_ACC, bool DEV, bool FLIP, bool CLIP, int EPT = 8>
+__global__ void __launch_bounds__(ZS_THREADS, EPT == 8 ? ZS_FUSED_MIN_BLOCKS : ZS_FUSED4_MIN_BLOCKS)
     k_step_fused(const __grid_constant__ SlicePtrs s, int n, const float* acc,
                  const __grid_constant__ OopBufs b, int64_t count, AdamArgs ad_host,
                  zs_scaler scaler_in, StepResult* result, zs_device_state* dstate,
@@ -1149,6 +1216,9 @@ __global__ void __launch_bounds__(ZS_THREADS, ZS_FUSED_MIN_BLOCKS)
   // Launched without the programmatic-dependent attribute (it starts once its
   // predecessor has completed), and it lets no successor start early either:
   // no griddepcontrol here, so no other grid's CTAs take SM room while it runs.
+  // EPT: elements per thread (8; or 4, twice the threads for shards that fit,
+  // unclipped only: the norm keeps the norm pass's 8-element CTA partition).
+  static_assert(EPT == 8 || (EPT == 4 && !CLIP), "4-element units are unclipped only");
   __shared__ int s_go;
   __shared__ int s_last;
   __shared__ float s_coef;
@@ -1156,31 +1226,29 @@ __global__ void __launch_bounds__(ZS_THREADS, ZS_FUSED_MIN_BLOCKS)
   if (threadIdx.x == 0) gen0 = ld_acquire(&sync->gen);
   int cur = 0;
   if constexpr (DEV && FLIP) cur = dstate->buf & 1;
-  const int64_t nvec = count >> 3;
+  const int64_t nvec = count / EPT;
   const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
   const bool unit = tid < nvec;
-  const bool tail = tid < count - nvec * 8;
-  const int64_t ti = nvec * 8 + tid;
-  float a[1][8], p[8], m[8], v[8];
+  const bool tail = tid < count - nvec * EPT;
+  const int64_t ti = nvec * EPT + tid;
+  float a[EPT], p[EPT], m[EPT], v[EPT];
   float at = 0.0f, pt = 0.0f, mt = 0.0f, vt = 0.0f;
   float sqf = 0.0f, sqb = 0.0f;
   bool bad = false;
   if (unit) {
     if (HAS_ACC) {
-      load8(acc + tid * 8, a[0]);
+      load_unit<EPT>(acc, tid, a);
     } else {
 #pragma unroll
-      for (int k = 0; k < 8; ++k) a[0][k] = 0.0f;
+      for (int k = 0; k < EPT; ++k) a[k] = 0.0f;
     }
-    load8(b.p[cur] + tid * 8, p);
-    load8(b.m[cur] + tid * 8, m);
-    load8(b.v[cur] + tid * 8, v);
-    const int64_t vi[1] = {tid};
-    const bool ok[1] = {true};
-    sum_slices<DT, 1>(s, n, vi, ok, a);
+    load_unit<EPT>(b.p[cur], tid, p);
+    load_unit<EPT>(b.m[cur], tid, m);
+    load_unit<EPT>(b.v[cur], tid, v);
+    sum_unit<DT, EPT>(s, n, tid, a);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) bad |= not_finite(a[0][k]);
-    if constexpr (CLIP) norm_add8(a[0], sqf, sqb);
+    for (int k = 0; k < EPT; ++k) bad |= not_finite(a[k]);
+    if constexpr (CLIP) norm_add8(a, sqf, sqb);
   }
   if (tail) {
     at = sum_slices1<DT>(s, n, ti, HAS_ACC ? acc[ti] : 0.0f);
@@ -1282,16 +1350,12 @@ __global__ void __launch_bounds__(ZS_THREADS, ZS_FUSED_MIN_BLOCKS)
     ad = *reinterpret_cast<const AdamArgs*>(s_args);
   }
   if (unit) {
-    uint32_t h[4];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) adamw1<CLIP>(ad, a[0][k], p[k], m[k], v[k], coef);
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-      h[k] = float_to_half_bits<DT>(p[2 * k]) | (float_to_half_bits<DT>(p[2 * k + 1]) << 16);
-    store8_cs(b.p[cur ^ 1] + tid * 8, p);
-    store8_cs(b.m[cur ^ 1] + tid * 8, m);
-    store8_cs(b.v[cur ^ 1] + tid * 8, v);
-    __stcs(reinterpret_cast<uint4*>(b.h[cur ^ 1]) + tid, make_uint4(h[0], h[1], h[2], h[3]));
+    for (int k = 0; k < EPT; ++k) adamw1<CLIP>(ad, a[k], p[k], m[k], v[k], coef);
+    store_unit<EPT>(b.p[cur ^ 1], tid, p);
+    store_unit<EPT>(b.m[cur ^ 1], tid, m);
+    store_unit<EPT>(b.v[cur ^ 1], tid, v);
+    store_half_unit<DT, EPT>(b.h[cur ^ 1], tid, p);
   }
   if (tail) {
     adamw1<CLIP>(ad, at, pt, mt, vt, coef);
