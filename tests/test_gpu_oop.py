@@ -189,29 +189,30 @@ def test_oop_rejects_overlapping_buffers(zs, ctx):
     assert e.value.status == zs.ZS_ERR_ARG
 
 
-@pytest.mark.parametrize("n,G,count", [(3, 2, 10_007), (2, 1, 8_192)])
-def test_two_phase_update_oop_equals_the_one_call_form(zs, ctx, n, G, count):
+@pytest.mark.parametrize("dtype", [FP16, BF16])
+@pytest.mark.parametrize("n,G,count", [(3, 2, 10_007), (2, 1, 8_192), (16, 2, 3_001)])
+def test_two_phase_update_oop_equals_the_one_call_form(zs, ctx, n, G, count, dtype):
     """zs_update_oop over two ranges with one flag, then zs_scaler_update on
     that flag: the written set equals zs_shard_step_oop's bit for bit, and
     the flag and scale agree, skipped steps included."""
-    dtype = FP16
-    rng = np.random.default_rng(n * 7 + G)
+    rng = np.random.default_rng(n * 7 + G + 100 * dtype)
     master0 = (rng.standard_normal(count) * 0.02).astype(np.float32)
     hp_vals = (STRESS_LR, 0.9, 0.999, 1e-8, 0.01)
     hp = zs.make_hparams(*hp_vals)
-    sc_a = zs.zs_scaler_init(1024.0, 1.0, 2, 1, True)   # one call
-    sc_b = zs.zs_scaler_init(1024.0, 1.0, 2, 1, True)   # two phases
+    dyn = dtype == FP16
+    sc_a = zs.zs_scaler_init(1024.0 if dyn else 1.0, 1.0, 2, 1, dyn)   # one call
+    sc_b = zs.zs_scaler_init(1024.0 if dyn else 1.0, 1.0, 2, 1, dyn)   # two phases
     a_sets = [state_set(master0, count), state_set(np.zeros_like(master0), count)]
     b_sets = [state_set(master0, count), state_set(np.zeros_like(master0), count)]
     acc_a = torch.zeros(count, dtype=torch.float32, device="cuda")
     acc_b = torch.zeros_like(acc_a)
     flag = torch.zeros(1, dtype=torch.int32, device="cuda")
-    cut = 4096
+    cut = count // 2 // 64 * 64     # a 64-element boundary: both ranges stay 16-byte aligned
     cur = t = 0
     for s in range(1, 7):
         grads = [rand_grads(rng, n, count, dtype, sc_a.scale) for _ in range(G)]
         if s == 3:
-            grads[G - 1][0][count - 5] = 0x7C00      # in the second range
+            grads[G - 1][0][count - 5] = 0x7C00 if dyn else 0x7F80   # in the second range
         dg = [[dev16(x) for x in micro] for micro in grads]
         for k in range(G - 1):
             zs.zs_grad_accum(ctx, dg[k], dtype, count, acc_a, k == 0)
