@@ -249,9 +249,8 @@ class DeviceWorkload:
 
     def step_async_calls(self, ctx, state):
         """The calls of one step on the device-resident path (capturable)."""
-        zs, wl = self.zs, self.wl
-        for k in range(wl.g - 1):
-            zs.zs_grad_accum(ctx, self.slices(k), self.dt, self.E, self.acc, k == 0)
+        for k in range(self.wl.g - 1):
+            self.accum(ctx, k)
         self.finish_async(ctx, state)
 
     def finish_async(self, ctx, state):
@@ -259,7 +258,11 @@ class DeviceWorkload:
         step count and the step's outcome stay in `state` on the device (with
         clipping, the norm in a device word too)."""
         zs, wl = self.zs, self.wl
-        if self.clip > 0:
+        if self.acc_kind == "half":
+            zs.zs_shard_step_halfacc_async(ctx, self.slices(wl.g - 1), self.dt, self.E, self.acc,
+                                           wl.g, self.master, self.m, self.v, self.half, self.hp,
+                                           None, state)
+        elif self.clip > 0:
             if not hasattr(self, "d_norm"):
                 import torch
                 self.d_norm = torch.zeros(1, dtype=torch.float64, device=self.dev)
@@ -285,9 +288,8 @@ class DeviceWorkload:
 
     def step_oop_calls(self, ctx, state):
         """One step of the device-resident out-of-place form."""
-        zs, wl = self.zs, self.wl
-        for k in range(wl.g - 1):
-            zs.zs_grad_accum(ctx, self.slices(k), self.dt, self.E, self.acc, k == 0)
+        for k in range(self.wl.g - 1):
+            self.accum(ctx, k)
         self.finish_oop(ctx, state)
 
     def finish_oop(self, ctx, state):
@@ -304,8 +306,10 @@ class DeviceWorkload:
             self._pairs = [zs.pointer_array(x) for x in ((self.master, self.master2),
                                                          (self.m, self.m2), (self.v, self.v2),
                                                          (self.half, self.half2))]
-        zs.zs_shard_step_async_oop(ctx, self.slices(wl.g - 1), self.dt, self.E, self.acc, wl.g,
-                                   *self._pairs, self.hp, None, state)
+        step = (zs.zs_shard_step_halfacc_async_oop if self.acc_kind == "half"
+                else zs.zs_shard_step_async_oop)
+        step(ctx, self.slices(wl.g - 1), self.dt, self.E, self.acc, wl.g, *self._pairs, self.hp,
+             None, state)
 
 
 # ---------------------------------------------------------------- clocks
@@ -555,6 +559,28 @@ API_DESC = {
                  "replayed (no host launch work per step: the step's GPU rate)",
     "split": "zs_reduce_check / zs_check_last + zs_apply + zs_scaler_update (split at the flag)",
 }
+HALF_API_DESC = {
+    "async": "zs_grad_accum_halfacc + zs_shard_step_halfacc_async (half-precision carried "
+             "sums; scale, step count and outcome stay on the device)",
+    "async_oop": "zs_grad_accum_halfacc + zs_shard_step_halfacc_async_oop (half-precision "
+                 "carried sums, device-resident, state written out of place)",
+}
+
+
+def api_desc(api: str, acc: str, clip: float, hacc_oop: bool) -> str:
+    """The entry points one step of `api` calls, as the bench line names them."""
+    if acc == "half":
+        if api != "sync":
+            return HALF_API_DESC[api]
+        return ("zs_grad_accum_halfacc + zs_shard_step_halfacc"
+                + ("_oop (the second state set fits)" if hacc_oop else ""))
+    if clip and api == "sync":
+        return "zs_grad_accum + zs_shard_step_clipped"
+    if clip:
+        return API_DESC[api].replace("zs_shard_step_async", "zs_shard_step_async_clipped")
+    return API_DESC[api]
+
+
 # the other target workloads, measured in the same run after the headline one
 TABLE_WORKLOADS = ("decoder-1.3b-n16", "llama7b-zero3-n64", "gpt2-small-n8", "flat-1m-n2")
 
@@ -564,8 +590,6 @@ def resolve_api(args, world: int) -> str:
         return "split"
     if args.graph:
         return "graph"
-    if args.acc == "half":
-        return "sync"   # the half-accumulator step exists as a synchronising call
     if args.api == "auto":   # decided once the workload's buffers are allocated
         return "async" if args.clip else "auto"
     return args.api
@@ -975,8 +999,8 @@ def run_ours(args):
         raise SystemExit("--split and --graph are separate modes")
     if api == "graph" and args.acc != "fp32":
         raise SystemExit("--graph runs the fp32-accumulator path on one GPU")
-    if api == "async_oop" and (args.clip or args.acc != "fp32"):
-        raise SystemExit("--api async_oop runs the unclipped fp32-accumulator step")
+    if api == "async_oop" and args.clip:
+        raise SystemExit("--api async_oop runs the unclipped step")
 
     # two gradient buffers alternate across the micro-steps (the split form reads
     # every micro-step's slices in one call, so it keeps one buffer each)
@@ -986,8 +1010,9 @@ def run_ours(args):
     torch.cuda.synchronize()
     if api == "auto":
         api = "async_oop" if oop_fits(W.E) else "async"
-    # the half-accumulator step out of place where its second state set fits
-    hacc_oop = W.hacc_oop = args.acc == "half" and oop_fits(W.E)
+    # the synchronising half-accumulator step out of place where its second
+    # state set fits (the device-resident forms name their own form in `api`)
+    hacc_oop = W.hacc_oop = args.acc == "half" and api == "sync" and oop_fits(W.E)
     E = W.E
     valid = min(W.valid_end - W.begin, E)
     one_step, state = make_step(zs, ctx, W, api, args.clip)
@@ -1090,13 +1115,7 @@ def run_ours(args):
                                else "1 GPU",
                 "accumulator": args.acc,
                 "clip_max_norm": args.clip or None,
-                "api": ("zs_grad_accum_halfacc + zs_shard_step_halfacc"
-                        + ("_oop (the second state set fits)" if hacc_oop else "")
-                        if args.acc == "half"
-                        else "zs_grad_accum + zs_shard_step_clipped" if args.clip and api == "sync"
-                        else API_DESC[api].replace("zs_shard_step_async",
-                                                   "zs_shard_step_async_clipped")
-                        if args.clip else API_DESC[api]),
+                "api": api_desc(api, args.acc, args.clip, hacc_oop),
                 "l2": "inputs larger than L2 (129 MB): no flush needed",
                 "inputs": inputs_desc,
                 "alg_bytes_per_step": step_bytes,

@@ -519,6 +519,28 @@ zs_status zs_update_oop(zs_ctx* ctx, const void* const* grads, int32_t n, zs_dty
                         float* v_out, void* half_out, const zs_adam_hparams* hp, int64_t step,
                         int32_t* d_flag, cudaStream_t stream);
 
+/* The half-accumulator step without a host round trip, as zs_shard_step_async
+ * is to zs_shard_step (scale, Adam's step count and learning rate in
+ * *d_state; capturable in a CUDA graph): in place (the last micro-step summed
+ * into acc_half, then the update from it), or out of place
+ * (zs_shard_step_halfacc_async_oop: master, m, v and half are HOST arrays of
+ * two device pointers, d_state->buf names the current set; a clean step
+ * writes set buf ^ 1 and flips it).  Same kernels and arithmetic as the
+ * synchronising forms: bit-identical results. */
+zs_status zs_shard_step_halfacc_async(zs_ctx* ctx, const void* const* grads, int32_t n,
+                                      zs_dtype dt, int64_t count, void* acc_half,
+                                      int32_t accum_steps, float* master, float* m, float* v,
+                                      void* half_out, const zs_adam_hparams* hp,
+                                      const zs_lr_schedule* sched, zs_device_state* d_state,
+                                      cudaStream_t stream);
+zs_status zs_shard_step_halfacc_async_oop(zs_ctx* ctx, const void* const* grads, int32_t n,
+                                          zs_dtype dt, int64_t count, const void* acc_half,
+                                          int32_t accum_steps, float* const* master,
+                                          float* const* m, float* const* v, void* const* half,
+                                          const zs_adam_hparams* hp,
+                                          const zs_lr_schedule* sched,
+                                          zs_device_state* d_state, cudaStream_t stream);
+
 /* ---------------------------------------------------------------- engine */
 
 /* The training-loop interface of §5.1 (model_engine.backward(loss) then

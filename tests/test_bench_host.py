@@ -147,3 +147,19 @@ def test_fused_plan_moves_exactly_the_algorithmic_bytes():
         assert [k for k, _ in plan] == ["reduce_first"] * (wl.g > 1) + ["reduce"] * max(
             0, wl.g - 2) + ["fused"]
         assert sum(b for _, b in plan) == bench.alg_bytes_per_elem_step(wl.n, wl.g)
+
+
+def test_bench_line_names_the_entry_points_each_api_calls():
+    """The half-accumulator forms name the halfacc entry points (and only they
+    do); clipping names the clipped forms; the split step is the same either way."""
+    for api in ("async", "async_oop", "sync"):
+        assert "halfacc" in bench.api_desc(api, "half", 0.0, api == "sync")
+    assert bench.api_desc("sync", "half", 0.0, True).startswith(
+        "zs_grad_accum_halfacc + zs_shard_step_halfacc_oop")
+    assert bench.api_desc("sync", "half", 0.0, False).endswith("zs_shard_step_halfacc")
+    for api in bench.API_DESC:
+        assert "halfacc" not in bench.api_desc(api, "fp32", 0.0, False)
+        assert bench.api_desc(api, "fp32", 0.0, False) == bench.API_DESC[api]
+    assert bench.api_desc("sync", "fp32", 1.0, False) == "zs_grad_accum + zs_shard_step_clipped"
+    assert "zs_shard_step_async_clipped_oop" in bench.api_desc("async_oop", "fp32", 1.0, False)
+    assert bench.api_desc("split", "fp32", 1.0, False) == bench.API_DESC["split"]

@@ -24,7 +24,9 @@ def run(args):
 
 
 @pytest.mark.parametrize("mode", [["--skip-table"], ["--api", "sync"], ["--split"], ["--graph"],
-                                  ["--acc", "half"], ["--clip", "1.0", "--skip-table"],
+                                  ["--acc", "half"], ["--acc", "half", "--api", "sync"],
+                                  ["--acc", "half", "--api", "async"],
+                                  ["--clip", "1.0", "--skip-table"],
                                   ["--clip", "1.0", "--api", "sync"], ["--clip", "1.0", "--graph"],
                                   ["--api", "async_oop", "--skip-table"]])
 def test_bench_line(mode):
@@ -47,6 +49,9 @@ def test_bench_line(mode):
     assert e["value"] > 0 and e["h2d_bytes_per_step"] == 8 * (1 << 24) * 2
     assert e["d2h_bytes_per_step"] > 0
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
+    if "half" in mode:   # every half-accumulator form names its own entry points
+        assert "halfacc" in d["config"]["api"]
+        assert d["config"]["accumulator"] == "half"
 
 
 def test_small_shard_runs_the_fused_step():

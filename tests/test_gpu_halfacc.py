@@ -184,3 +184,85 @@ def test_halfacc_oop_steps_equal_the_in_place_step_and_the_oracle(zs, ctx, dtype
     close(sets[cur][0].cpu().numpy(), st.master, "master")
     close(sets[cur][1].cpu().numpy(), st.m, "m")
     close(sets[cur][2].cpu().numpy(), st.v, "v")
+
+
+@pytest.mark.parametrize("form", ["async", "async_oop"])
+@pytest.mark.parametrize("graph", [False, True])
+@pytest.mark.parametrize("dtype", [FP16, BF16])
+def test_halfacc_device_state_steps_equal_the_synchronising_step(zs, ctx, form, graph, dtype):
+    """zs_shard_step_halfacc_async (in place) and _async_oop: the scale, Adam's
+    step count and the outcome on the device, no host round trip, eager or
+    replayed from a CUDA graph.  The same kernels and constants as the
+    synchronising half-accumulator step: the state equals it bit for bit,
+    step after step (an overflow included), and the oracle's within the bound."""
+    n, G, count = 4, 2, 20_011
+    rng = np.random.default_rng(77 + dtype + (10 if graph else 0) + (100 if form == "async_oop" else 0))
+    master0 = (rng.standard_normal(count) * 0.02).astype(np.float32)
+    st = oracle.ShardState.from_master(master0, dtype)
+    dyn = dtype == FP16
+    sc_o = oracle.make_scaler(256.0 if dyn else 1.0, 1.0, 3, 1, dyn)
+    sc = zs.zs_scaler_init(sc_o.scale, 1.0, 3, 1, dyn)
+    state = zs.DeviceState(zs.zs_scaler_init(sc_o.scale, 1.0, 3, 1, dyn))
+    hp_v = (STRESS_LR, 0.9, 0.999, 1e-8, 0.01)
+    hp_o, hp = oracle.make_hparams(*hp_v), zs.make_hparams(*hp_v)
+
+    def state_bufs(m0):
+        p = torch.from_numpy(m0.copy()).cuda()
+        return [p, torch.zeros_like(p), torch.zeros_like(p),
+                torch.zeros(count, dtype=torch.int16, device="cuda")]
+    ref = state_bufs(master0)                       # the synchronising step
+    sets = [state_bufs(master0), state_bufs(np.zeros_like(master0))]
+    pairs = [zs.pointer_array([sets[0][k], sets[1][k]]) for k in range(4)]
+    acc_r = torch.zeros(count, dtype=torch.int16, device="cuda")
+    acc_d = torch.zeros_like(acc_r)
+    pad = (count + 7) // 8 * 8
+    gbuf = torch.zeros((G, n, pad), dtype=torch.int16, device="cuda")
+    ptrs = [zs.pointer_array(gbuf[k, r, :count] for r in range(n)) for k in range(G)]
+
+    def device_step():
+        for k in range(G - 1):
+            zs.zs_grad_accum_halfacc(ctx, ptrs[k], dtype, count, acc_d, k == 0)
+        if form == "async":
+            zs.zs_shard_step_halfacc_async(ctx, ptrs[G - 1], dtype, count, acc_d, G, *sets[0],
+                                           hp, None, state)
+        else:
+            zs.zs_shard_step_halfacc_async_oop(ctx, ptrs[G - 1], dtype, count, acc_d, G,
+                                               *pairs, hp, None, state)
+
+    g = None
+    t = t_o = 0
+    for s in range(1, 9):
+        grads = [[lib_half((rng.standard_normal(count) * 1e-2 * sc_o.scale).astype(np.float32),
+                           dtype) for _ in range(n)] for _ in range(G)]
+        if s == 4:
+            grads[G - 1][n - 1][count // 3] = 0x7E00 if dyn else 0x7FC0
+        host = np.stack([np.stack(mc) for mc in grads]).view(np.int16)
+        gbuf[:, :, :count].copy_(torch.from_numpy(host))
+        ovf_o, t_o, _ = oracle.shard_step_halfacc(grads, dtype, st, hp_o, t_o, sc_o)
+        dg = [[dev16(x) for x in micro] for micro in grads]
+        for k in range(G - 1):
+            zs.zs_grad_accum_halfacc(ctx, dg[k], dtype, count, acc_r, k == 0)
+        ovf, _ = zs.zs_shard_step_halfacc(ctx, dg[G - 1], dtype, count, acc_r, G, *ref, hp,
+                                          t + 1, sc)
+        if graph and g is None:
+            device_step()                 # the first step uncaptured, then capture the rest
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                device_step()
+        elif graph:
+            g.replay()
+        else:
+            device_step()
+        d = state.read()
+        assert d.overflow == ovf == ovf_o and d.scaler.scale == sc.scale == sc_o.scale, s
+        t += 0 if ovf else 1
+        assert d.step == t == t_o and d.iterations == s
+        cur = sets[d.buf] if form == "async_oop" else sets[0]
+        for k in range(3):
+            assert torch.equal(cur[k], ref[k]), (s, k)
+        if t:
+            assert torch.equal(cur[3], ref[3])
+    close(ref[0].cpu().numpy(), st.master, "master")
+    close(ref[1].cpu().numpy(), st.m, "m")
+    close(ref[2].cpu().numpy(), st.v, "v")

@@ -142,6 +142,12 @@ def _load():
                                       vp, ctypes.POINTER(zs_adam_hparams), i64,
                                       ctypes.POINTER(zs_scaler), i32p,
                                       ctypes.POINTER(ctypes.c_float), vp],
+        "zs_shard_step_halfacc_async": [vp, pp, i32, i32, i64, vp, i32, vp, vp, vp, vp,
+                                        ctypes.POINTER(zs_adam_hparams),
+                                        ctypes.POINTER(zs_lr_schedule), vp, vp],
+        "zs_shard_step_halfacc_async_oop": [vp, pp, i32, i32, i64, vp, i32, pp, pp, pp, pp,
+                                            ctypes.POINTER(zs_adam_hparams),
+                                            ctypes.POINTER(zs_lr_schedule), vp, vp],
         "zs_ctx_set_timing": [vp, i32],
         "zs_ctx_set_fused": [vp, i32, i64],
         "zs_ctx_fused_capacity": [vp, i64p],
@@ -516,6 +522,25 @@ def zs_shard_step_halfacc_oop(ctx: Ctx, grads, dt, count: int, acc_half, accum_s
         _addr(v_out), _addr(half_out), ctypes.byref(hp), step, ctypes.byref(scaler),
         ctypes.byref(ovf), ctypes.byref(ns), _stream(stream)))
     return ovf.value, ns.value
+
+
+def zs_shard_step_halfacc_async(ctx: Ctx, grads, dt, count: int, acc_half, accum_steps: int,
+                                master, m, v, half_out, hp: zs_adam_hparams, sched, d_state,
+                                stream=None):
+    ctx.check(lib.zs_shard_step_halfacc_async(
+        ctx.handle, _ptrs(grads), len(grads), _dtype(dt), count, _addr(acc_half), accum_steps,
+        _addr(master), _addr(m), _addr(v), _addr(half_out), ctypes.byref(hp),
+        ctypes.byref(sched) if sched is not None else None, _addr(d_state), _stream(stream)))
+
+
+def zs_shard_step_halfacc_async_oop(ctx: Ctx, grads, dt, count: int, acc_half,
+                                    accum_steps: int, master, m, v, half, hp: zs_adam_hparams,
+                                    sched, d_state, stream=None):
+    """master, m, v, half: pairs of buffers; d_state.buf names the current one."""
+    ctx.check(lib.zs_shard_step_halfacc_async_oop(
+        ctx.handle, _ptrs(grads), len(grads), _dtype(dt), count, _addr(acc_half), accum_steps,
+        _ptrs(master), _ptrs(m), _ptrs(v), _ptrs(half), ctypes.byref(hp),
+        ctypes.byref(sched) if sched is not None else None, _addr(d_state), _stream(stream)))
 
 
 class Engine:

@@ -805,25 +805,43 @@ zs_status reduce_hacc(zs_ctx* c, zs_dtype dt, const zs::SlicePtrs& sp, int32_t n
   return ZS_OK;
 }
 
-zs_status apply_hacc(zs_ctx* c, zs_dtype dt, const int32_t* flag, const void* acc, int64_t count,
-                     const zs::AdamArgs& ad, float* master, float* m, float* v, void* half_out,
-                     const zs_scaler* scaler_in, zs::StepResult* result, cudaStream_t s) {
-  LaunchScope ls(c, s, ZS_KERNEL_APPLY, count);
+template <int DT, bool DEV>
+void launch_apply_hacc_k(zs_ctx* c, const int32_t* flag, const float* a, int64_t count,
+                         const zs::AdamArgs& ad, float* master, float* m, float* v, uint16_t* ho,
+                         const zs_scaler& sc_in, zs::StepResult* result,
+                         const zs::AdamArgs* ad_dev, zs_device_state* st, cudaStream_t s) {
   zs::SlicePtrs sp;
   std::memset(&sp, 0, sizeof sp);
+  auto k = zs::k_apply<DT, true, false, 1, false, DEV, true>;
+  launch_k(c, k, grid_for(c, k, (count >> 3) + 8), zs::kThreads, s, flag, sp, 0, a, master, m, v,
+           ho, count, ad, sc_in, result, (const float*)nullptr, ad_dev, st, 0u);
+}
+
+// The update from the half accumulator: host constants and the scale update
+// into `result` (ad_dev == NULL), or the device-resident form (constants from
+// ad_dev, the state in st).
+zs_status apply_hacc(zs_ctx* c, zs_dtype dt, const int32_t* flag, const void* acc, int64_t count,
+                     const zs::AdamArgs& ad, float* master, float* m, float* v, void* half_out,
+                     const zs_scaler* scaler_in, zs::StepResult* result, cudaStream_t s,
+                     const zs::AdamArgs* ad_dev = nullptr, zs_device_state* st = nullptr) {
+  LaunchScope ls(c, s, ZS_KERNEL_APPLY, count);
   const float* a = static_cast<const float*>(acc);
   uint16_t* ho = static_cast<uint16_t*>(half_out);
-  const int64_t units = (count >> 3) + 8;
-  if (dt == ZS_FP16) {
-    auto k = zs::k_apply<ZS_FP16, true, false, 1, false, false, true>;
-    launch_k(c, k, grid_for(c, k, units), zs::kThreads, s, flag, sp, 0, a, master, m, v, ho,
-             count, ad, *scaler_in, result, (const float*)nullptr, (const zs::AdamArgs*)nullptr,
-             (zs_device_state*)nullptr, 0u);
+  const zs_scaler sc_in = scaler_in ? *scaler_in : zs_scaler{};
+  if (ad_dev != nullptr) {
+    if (dt == ZS_FP16)
+      launch_apply_hacc_k<ZS_FP16, true>(c, flag, a, count, ad, master, m, v, ho, sc_in, result,
+                                         ad_dev, st, s);
+    else
+      launch_apply_hacc_k<ZS_BF16, true>(c, flag, a, count, ad, master, m, v, ho, sc_in, result,
+                                         ad_dev, st, s);
   } else {
-    auto k = zs::k_apply<ZS_BF16, true, false, 1, false, false, true>;
-    launch_k(c, k, grid_for(c, k, units), zs::kThreads, s, flag, sp, 0, a, master, m, v, ho,
-             count, ad, *scaler_in, result, (const float*)nullptr, (const zs::AdamArgs*)nullptr,
-             (zs_device_state*)nullptr, 0u);
+    if (dt == ZS_FP16)
+      launch_apply_hacc_k<ZS_FP16, false>(c, flag, a, count, ad, master, m, v, ho, sc_in, result,
+                                          nullptr, nullptr, s);
+    else
+      launch_apply_hacc_k<ZS_BF16, false>(c, flag, a, count, ad, master, m, v, ho, sc_in, result,
+                                          nullptr, nullptr, s);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(c, e, "apply launch");
@@ -1645,6 +1663,109 @@ zs_status zs_shard_step_halfacc_oop(zs_ctx* c, const void* const* grads, int32_t
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(c, e, "commit launch");
   return finish_step(c, scaler, overflow_out, new_scale_out, nullptr, stream);
+}
+
+// Checks shared by the device-resident half-accumulator calls.
+static zs_status check_device_args(zs_ctx* c, const zs_adam_hparams* hp,
+                                   const zs_lr_schedule* sched, const zs_device_state* d_state) {
+  if (d_state == nullptr) return fail(c, ZS_ERR_ARG, "d_state is NULL");
+  if ((reinterpret_cast<uintptr_t>(d_state) & 7u) != 0)
+    return fail(c, ZS_ERR_ALIGN, "d_state is not 8-byte aligned");
+  ZS_TRY(check_hparams(c, hp, 1));
+  if (sched != nullptr && (sched->kind < ZS_LR_CONSTANT || sched->kind > ZS_LR_WARMUP_DECAY ||
+                           sched->warmup_steps < 0 || !std::isfinite(sched->min_lr) ||
+                           !std::isfinite(sched->max_lr)))
+    return fail(c, ZS_ERR_ARG, "bad learning-rate schedule");
+  return ZS_OK;
+}
+
+zs_status zs_shard_step_halfacc_async(zs_ctx* c, const void* const* grads, int32_t n,
+                                      zs_dtype dt, int64_t count, void* acc_half,
+                                      int32_t accum_steps, float* master, float* m, float* v,
+                                      void* half_out, const zs_adam_hparams* hp,
+                                      const zs_lr_schedule* sched, zs_device_state* d_state,
+                                      cudaStream_t stream) {
+  NvtxRange nvtx_("zs_shard_step_halfacc_async");
+  ZS_TRY(check_ctx(c));
+  if (dt != ZS_FP16 && dt != ZS_BF16) return fail(c, ZS_ERR_DTYPE, "unknown dtype %d", (int)dt);
+  if (count < 0) return fail(c, ZS_ERR_ARG, "count < 0");
+  if (accum_steps < 1) return fail(c, ZS_ERR_ARG, "accum_steps must be >= 1");
+  ZS_TRY(check_device_args(c, hp, sched, d_state));
+  zs::SlicePtrs sp;
+  ZS_TRY(check_slices(c, grads, n, count, &sp));
+  ZS_TRY(check_array(c, acc_half, "acc_half", count));
+  ZS_TRY(check_array(c, master, "master", count));
+  ZS_TRY(check_array(c, m, "m", count));
+  ZS_TRY(check_array(c, v, "v", count));
+  ZS_TRY(check_array(c, half_out, "half_out", count));
+  if (count > 0)
+    ZS_TRY(reduce_hacc(c, dt, sp, n, acc_half, count, accum_steps > 1, c->d_flag, stream));
+  zs_lr_schedule sc{};
+  if (sched) sc = *sched;
+  launch_k(c, zs::k_step_prologue, 1, 32, stream, (const zs_device_state*)d_state, n,
+           accum_steps, *hp, sc, sched ? 1 : 0, c->d_args);
+  c->launches += 1;
+  const zs::AdamArgs unused{};
+  ZS_TRY(apply_hacc(c, dt, c->d_flag, acc_half, count, unused, master, m, v, half_out, nullptr,
+                    nullptr, stream, c->d_args, d_state));
+  launch_k(c, zs::k_clear_flag, 1, 32, stream, c->d_flag);
+  c->launches += 1;
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? ZS_OK : cuda_fail(c, e, "flag reset");
+}
+
+zs_status zs_shard_step_halfacc_async_oop(zs_ctx* c, const void* const* grads, int32_t n,
+                                          zs_dtype dt, int64_t count, const void* acc_half,
+                                          int32_t accum_steps, float* const* master,
+                                          float* const* m, float* const* v, void* const* half,
+                                          const zs_adam_hparams* hp,
+                                          const zs_lr_schedule* sched,
+                                          zs_device_state* d_state, cudaStream_t stream) {
+  NvtxRange nvtx_("zs_shard_step_halfacc_async_oop");
+  ZS_TRY(check_ctx(c));
+  if (master == nullptr || m == nullptr || v == nullptr || half == nullptr)
+    return fail(c, ZS_ERR_ARG, "a buffer pair is NULL");
+  ZS_TRY(check_device_args(c, hp, sched, d_state));
+  zs::SlicePtrs sp;
+  const float* pp[2] = {master[0], master[1]};
+  const float* mm[2] = {m[0], m[1]};
+  const float* vv[2] = {v[0], v[1]};
+  const void* hh[2] = {half[0], half[1]};
+  const float* acc = accum_steps > 1 ? static_cast<const float*>(acc_half) : nullptr;
+  ZS_TRY(check_oop(c, grads, n, dt, count, acc, accum_steps, pp, mm, vv, hh, &sp));
+  zs_lr_schedule sc{};
+  if (sched) sc = *sched;
+  launch_k(c, zs::k_step_prologue, 1, 32, stream, (const zs_device_state*)d_state, n,
+           accum_steps, *hp, sc, sched ? 1 : 0, c->d_args);
+  c->launches += 1;
+  zs::OopBufs b;
+  for (int i = 0; i < 2; ++i) {
+    b.p[i] = master[i];
+    b.m[i] = m[i];
+    b.v[i] = v[i];
+    b.h[i] = static_cast<uint16_t*>(half[i]);
+  }
+  if (count > 0) {
+    LaunchScope ls(c, stream, ZS_KERNEL_UPDATE_OOP, count);
+    const zs::AdamArgs unused{};
+    const zs::AdamArgs* ad = c->d_args;
+    if (dt == ZS_FP16) {
+      if (acc) launch_oop_k<ZS_FP16, true, true, true>(c, sp, n, acc, b, count, unused, ad, d_state, c->d_flag, stream);
+      else launch_oop_k<ZS_FP16, false, true, true>(c, sp, n, acc, b, count, unused, ad, d_state, c->d_flag, stream);
+    } else {
+      if (acc) launch_oop_k<ZS_BF16, true, true, true>(c, sp, n, acc, b, count, unused, ad, d_state, c->d_flag, stream);
+      else launch_oop_k<ZS_BF16, false, true, true>(c, sp, n, acc, b, count, unused, ad, d_state, c->d_flag, stream);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(c, e, "out-of-place update launch");
+    ls.done();
+  }
+  const zs_scaler unused_sc{};
+  launch_k(c, zs::k_commit_oop<true>, 1, 32, stream, c->d_flag, d_state,
+           (const zs::AdamArgs*)c->d_args, unused_sc, (zs::StepResult*)nullptr);
+  c->launches += 1;
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? ZS_OK : cuda_fail(c, e, "commit launch");
 }
 
 zs_status zs_grad_sumsq(zs_ctx* c, const void* const* grads, int32_t n, zs_dtype dt,
