@@ -603,8 +603,22 @@ def oop_fits(E: int, margin: int = 4 << 30) -> bool:
     return torch.cuda.mem_get_info()[0] > 14 * E + margin
 
 
-def make_step(zs, ctx, W: DeviceWorkload, api: str, clip: float = 0.0):
-    """One step of `api` on W's buffers; returns (step function, device state or None)."""
+def graph_steps_per_replay(step_bytes: float, steps: int, peak_gbs: float = 6781.0) -> int:
+    """Steps captured in one CUDA graph: 1 while a step keeps the GPU busy far
+    longer than the host takes to replay a graph (~12 us per replay from
+    Python), else enough for ~0.5 ms of work per replay, at most 50, and a
+    divisor of `steps` so that exactly `steps` steps are timed."""
+    est_us = step_bytes / (peak_gbs * 1e3)
+    if est_us >= 200.0:
+        return 1
+    want = min(50, max(1, int(500.0 / max(est_us, 1e-3))), steps)
+    return next(r for r in range(want, 0, -1) if steps % r == 0)
+
+
+def make_step(zs, ctx, W: DeviceWorkload, api: str, clip: float = 0.0, per_replay: int = 1):
+    """One step of `api` on W's buffers; returns (step function, device state or
+    None).  The graph forms capture `per_replay` consecutive steps, so their
+    step function runs that many."""
     import torch
     wl, E = W.wl, W.E
     if api in ("async", "async_oop"):
@@ -621,7 +635,8 @@ def make_step(zs, ctx, W: DeviceWorkload, api: str, clip: float = 0.0):
         torch.cuda.synchronize()
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
-            calls(ctx, state)
+            for _ in range(per_replay):
+                calls(ctx, state)
         return graph.replay, state
     if api == "sync":
         return (lambda: W.step(ctx)), None
@@ -693,14 +708,17 @@ def kernel_table(zs, ctx, plan):
 
 
 def timed_steps(ctx, one_step, steps: int, warmup: int, dev: int, world: int,
-                kernel_timing: bool = True):
+                kernel_timing: bool = True, per_call: int = 1):
     """W untimed steps, then K steps between CUDA events on the launching
     stream, bracketed by a barrier and device synchronisation, with per-kernel
     event timing (unless kernel_timing is False) and nvidia-smi clock samples
-    during the timed region."""
+    during the timed region.  one_step runs `per_call` steps (a graph of
+    several steps): W is rounded up to whole calls, K must be whole calls."""
     import torch
     import torch.distributed as dist
-    for _ in range(warmup):
+    if steps % per_call:
+        raise ValueError(f"{steps} steps are not whole calls of {per_call}")
+    for _ in range(-(-warmup // per_call)):
         one_step()
     torch.cuda.synchronize()
     ctx.timing_reset()
@@ -712,7 +730,7 @@ def timed_steps(ctx, one_step, steps: int, warmup: int, dev: int, world: int,
         torch.cuda.synchronize()
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         ev0.record()
-        for _ in range(steps):
+        for _ in range(steps // per_call):
             one_step()
         ev1.record()
         torch.cuda.synchronize()
@@ -740,13 +758,16 @@ def measure_table_workload(zs, ctx, name: str, args, peak: float, dev: int):
     # host (which the synchronising API waits on every step) cannot dominate
     steps = max(args.steps, 100)
     for api in ("async", "async_oop", "sync", "graph_oop"):
-        one_step, state = make_step(zs, ctx, W, api)
+        # a graph of several steps where one step is shorter than the host's
+        # replay call (the step's GPU rate, not the host's)
+        per = graph_steps_per_replay(step_bytes, steps) if api == "graph_oop" else 1
+        one_step, state = make_step(zs, ctx, W, api, per_replay=per)
         # the step rate without per-kernel events (an event pair around each of
         # a short step's launches costs it a few percent), then the same steps
         # again with them for the per-kernel rates (none inside a graph replay)
         ms, launches, clocks = timed_steps(ctx, one_step, steps, args.warmup, dev, 1,
-                                           kernel_timing=False)
-        timed_steps(ctx, one_step, steps, 0, dev, 1)
+                                           kernel_timing=False, per_call=per)
+        timed_steps(ctx, one_step, steps, 0, dev, 1, per_call=per)
         per_step = ms / steps
         gbs = step_bytes / (per_step * 1e-3) / 1e9
         oop = api in ("async_oop", "graph_oop")
@@ -757,10 +778,12 @@ def measure_table_workload(zs, ctx, name: str, args, peak: float, dev: int):
         out[api] = {"api": API_DESC[api], "value": valid / (per_step * 1e-3), "unit": "params/s",
                     "steps": steps, "ms_per_step": round(per_step, 6), "step_gbs": round(gbs, 1),
                     "step_frac_of_peak": round(gbs / peak, 4), "gpu_launches": launches,
-                    "clocks": clocks,
+                    "warmup_steps": -(-args.warmup // per) * per, "clocks": clocks,
                     "kernels": {k: {"gbs": round(d["gbs"], 1), "frac_of_peak":
                                     round(d["gbs"] / peak, 4), "launches": d["launches"]}
                                 for k, d in kinds.items()}}
+        if per > 1:
+            out[api]["steps_per_replay"] = per
         if state is not None:
             d = state.read()
             out[api]["device_state"] = {"iterations": d.iterations, "step": d.step,
@@ -1015,8 +1038,12 @@ def run_ours(args):
     hacc_oop = W.hacc_oop = args.acc == "half" and api == "sync" and oop_fits(W.E)
     E = W.E
     valid = min(W.valid_end - W.begin, E)
-    one_step, state = make_step(zs, ctx, W, api, args.clip)
-    ms, launches, clock_summary = timed_steps(ctx, one_step, args.steps, args.warmup, dev, world)
+    # a graph of several steps where one step is shorter than the host's replay
+    per = (graph_steps_per_replay(alg_bytes_per_elem_step(wl.n, wl.g) * E, args.steps)
+           if api == "graph" else 1)
+    one_step, state = make_step(zs, ctx, W, api, args.clip, per_replay=per)
+    ms, launches, clock_summary = timed_steps(ctx, one_step, args.steps, args.warmup, dev, world,
+                                              per_call=per)
     fused = W.takes_fused(ctx, api)
     plan = W.launch_plan(split=api == "split", oop=api == "async_oop" or hacc_oop, fused=fused)
     if api == "graph":  # replays bypass the context's counter: the kernels of a captured step
@@ -1116,6 +1143,9 @@ def run_ours(args):
                 "accumulator": args.acc,
                 "clip_max_norm": args.clip or None,
                 "api": api_desc(api, args.acc, args.clip, hacc_oop),
+                # graph replays of several steps each (warm-up rounded up to whole replays)
+                **({"steps_per_replay": per, "warmup_steps_run": -(-args.warmup // per) * per}
+                   if per > 1 else {}),
                 "l2": "inputs larger than L2 (129 MB): no flush needed",
                 "inputs": inputs_desc,
                 "alg_bytes_per_step": step_bytes,

@@ -163,3 +163,19 @@ def test_bench_line_names_the_entry_points_each_api_calls():
     assert bench.api_desc("sync", "fp32", 1.0, False) == "zs_grad_accum + zs_shard_step_clipped"
     assert "zs_shard_step_async_clipped_oop" in bench.api_desc("async_oop", "fp32", 1.0, False)
     assert bench.api_desc("split", "fp32", 1.0, False) == bench.API_DESC["split"]
+
+
+def test_graph_replays_several_steps_only_where_a_step_is_short():
+    """Steps of ~2 us (the 2^20-parameter workload) go 50 to a replay; steps of
+    hundreds of microseconds or more go one to a replay; the count always
+    divides the timed steps."""
+    small = 524288 * 30
+    assert bench.graph_steps_per_replay(small, 2000) == 50
+    assert bench.graph_steps_per_replay(small, 3) == 3
+    assert bench.graph_steps_per_replay(small, 98) == 49
+    for sb in (15555008 * 114, 82232704 * 98, 6738415616 * 98):
+        assert bench.graph_steps_per_replay(sb, 20) == 1
+    for steps in (1, 7, 100, 2000):
+        for sb in (1e3, small, 4e8, 1e12):
+            r = bench.graph_steps_per_replay(sb, steps)
+            assert 1 <= r <= 50 and steps % r == 0

@@ -64,6 +64,19 @@ def test_small_shard_runs_the_fused_step():
     assert d["value"] > 0 and d["e2e"]["value"] > 0
 
 
+def test_graph_of_a_short_step_replays_several_steps():
+    """A step far shorter than the host's replay call is captured several to a
+    graph: exactly K steps are timed, the warm-up is whole replays, and the
+    device state counts every step."""
+    d = run(["--workload", "flat-1m-n2", "--graph", "--steps", "100", "--warmup", "3",
+             "--e2e-steps", "2", "--skip-cpu", "--skip-probe", "--skip-table"])
+    c = d["config"]
+    per = c["steps_per_replay"]
+    assert per > 1 and 100 % per == 0 and c["warmup_steps_run"] == per
+    assert d["steps"] == 100 and d["gpu_launches"] == 100      # one fused kernel per step
+    assert c["device_state_after_timed_steps"]["iterations"] == 1 + per + 100
+
+
 def test_default_api_keeps_the_step_state_on_the_device_and_measures_the_table():
     """The default API (zs_shard_step_async, no host round trip) runs every
     step: the device state read back after the run counts the warm-up and
@@ -92,4 +105,6 @@ def test_default_api_keeps_the_step_state_on_the_device_and_measures_the_table()
         # the same out-of-place step replayed from a CUDA graph: its GPU rate
         g = w["graph_oop"]
         assert g["value"] > 0 and g["step_frac_of_peak"] > 0 and g["gpu_launches"] >= 100 * 2
-        assert g["device_state"]["iterations"] == 1 + 3 + 2 * 100
+        # the uncaptured first call, whole replays of warm-up, two timed passes
+        assert g["warmup_steps"] >= 3 and g["warmup_steps"] % g.get("steps_per_replay", 1) == 0
+        assert g["device_state"]["iterations"] == 1 + g["warmup_steps"] + 2 * 100

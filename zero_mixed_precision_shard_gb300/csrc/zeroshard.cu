@@ -696,7 +696,8 @@ int fused_launch_k(zs_ctx* c, const FusedCall& f, cudaStream_t s, cudaError_t* e
   const int64_t per_grid = (int64_t)resident_ctas(c, k) * c->sms;
   int64_t grid = ((f.count / EPT) + zs::kThreads - 1) / zs::kThreads;
   if (grid < 1) grid = 1;
-  if (grid > per_grid || grid > c->coop_max_grid) return 0;
+  // the barrier counts arrivals in 16 bits (a co-resident grid is far smaller)
+  if (grid > per_grid || grid > c->coop_max_grid || grid > 0xFFFE) return 0;
   // ZS_FUSED_TEST_TIMEOUT: the barrier waits for one CTA more than the grid has
   const unsigned expect = (unsigned)grid + (c->fused_mode == ZS_FUSED_TEST_TIMEOUT ? 1u : 0u);
   LaunchScope ls(c, s, ZS_KERNEL_FUSED, f.count);

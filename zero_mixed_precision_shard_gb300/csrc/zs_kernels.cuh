@@ -1086,14 +1086,17 @@ __device__ __forceinline__ float clip_coef_of_norm(double norm, float max_norm) 
 
 // ---------------------------------------------------------------- fused step
 
-// Grid-wide barrier of the fused step (context scratch, zeroed at creation).
-// A launch's CTAs read `gen` before they arrive; the last CTA to arrive
-// resolves the step and advances `gen`, which releases the others.
+// Grid-wide barrier of the fused step (context scratch, zeroed at creation and
+// after a wait that ran out).  A CTA arrives with one acquire-release add on
+// `arrived`: 1 in the low 16 bits, and 1 in the high 16 bits when its sums
+// hold a non-finite value.  The last CTA to arrive resolves the step and
+// releases the others with one 64-bit release store of `rel`, which carries
+// all they need: bits 0-30 count the launches resolved so far (mod 2^31),
+// bit 31 is the step's overflow, bits 32-63 the clipping coefficient.
 struct FusedSync {
-  unsigned int arrived;  // CTAs of the running launch that have arrived
-  unsigned int gen;      // launches resolved so far
-  int32_t overflow;      // the step's flag as the last CTA to arrive read it
-  float coef;            // the step's clipping coefficient (clipped steps)
+  unsigned int arrived;
+  unsigned int pad_;
+  unsigned long long rel;
 };
 
 __device__ __forceinline__ uint64_t global_ns() {
@@ -1102,21 +1105,23 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
-__device__ __forceinline__ unsigned int ld_acquire(const unsigned int* p) {
-  unsigned int x;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(x) : "l"(p) : "memory");
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long x;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(x) : "l"(p) : "memory");
   return x;
 }
 
-// The step's constants as another CTA wrote them in this launch (read through
-// L2 only).
-__device__ __forceinline__ AdamArgs load_args_cg(const AdamArgs* p) {
-  AdamArgs a;
-  const float* src = reinterpret_cast<const float*>(p);
-  float* dst = reinterpret_cast<float*>(&a);
-#pragma unroll
-  for (int k = 0; k < (int)(sizeof(AdamArgs) / sizeof(float)); ++k) dst[k] = __ldcg(src + k);
-  return a;
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long x) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(x) : "memory");
+}
+
+__device__ __forceinline__ unsigned int atom_add_acq_rel(unsigned int* p, unsigned int v) {
+  unsigned int old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(p), "r"(v)
+               : "memory");
+  return old;
 }
 
 // Units of EPT (8 or 4) consecutive elements for the fused step: element
@@ -1186,24 +1191,26 @@ __device__ __forceinline__ void store_half_unit(uint16_t* h, int64_t u, const fl
 // The whole step of a shard whose 8-element units fit one co-resident grid
 // (one unit per thread, launched cooperatively): the last micro-step's sums
 // s = (acc or +0) + the n slices in rank order and the current master / m / v
-// are loaded into registers; the flag is ORed over the grid; one bounded grid
+// are loaded into registers; each CTA tests its sums; one bounded grid
 // barrier; then, on a clean step only, AdamW from the registers into the
 // output set (the same arithmetic as every other form).  Nothing is written on
 // an overflow, so the in-place state needs no second pass.  The last CTA to
-// arrive reads and clears the flag (the earlier micro-steps' ORs included) and
-// performs the loss-scale update: DEV, into the device state (flipping its
-// buffer index on a clean step when FLIP); otherwise into `result`.  DEV: CTA
-// 0 forms the step's constants from the device state before it arrives.
-// CLIP: each CTA writes its total of the squares of its sums to partials[]
-// before it arrives (as the norm-forming pass does, same CTA partition), and
-// the last CTA folds them in the same fixed order and forms the coefficient
-// (DEV: norm = sqrt(total) / (N*G*S) into *norm_out; else *sumsq_out = total *
-// inv_div2 and the coefficient from its root), which the others read after the
-// barrier.
+// arrive resolves the flag (the earlier micro-steps' flag word, as the launch
+// found it, and the count of CTAs that saw a non-finite sum), clears the flag
+// word, releases the others, and then performs the loss-scale update: DEV,
+// into the device state (flipping its buffer index on a clean step when
+// FLIP); otherwise into `result`.  DEV: every CTA forms the step's constants
+// from the device state before it arrives.  CLIP: each CTA writes its total of
+// the squares of its sums to partials[] before it arrives (as the norm-forming
+// pass does, same CTA partition), and the last CTA folds them in the same
+// fixed order and forms the coefficient, released with the flag (DEV: norm =
+// sqrt(total) / (N*G*S) into *norm_out; else *sumsq_out = total * inv_div2 and
+// the coefficient from its root).
 // b.X[cur] is read and b.X[cur ^ 1] written (cur = the device state's index
 // with FLIP, else 0; an in-place step passes the same buffers in both).
 // A CTA whose wait passes wait_ns gives up: it writes nothing and sets *err.
-// `expect` is the number of arrivals that resolve the step (the grid size).
+// `expect` is the number of arrivals that resolve the step (the grid size,
+// below 2^16).
 template <int DT, bool HAS_ACC, bool DEV, bool FLIP, bool CLIP, int EPT = 8>
 __global__ void __launch_bounds__(ZS_THREADS, EPT == 8 ? ZS_FUSED_MIN_BLOCKS : ZS_FUSED4_MIN_BLOCKS)
     k_step_fused(const __grid_constant__ SlicePtrs s, int n, const float* acc,
@@ -1222,8 +1229,16 @@ __global__ void __launch_bounds__(ZS_THREADS, EPT == 8 ? ZS_FUSED_MIN_BLOCKS : Z
   __shared__ int s_go;
   __shared__ int s_last;
   __shared__ float s_coef;
-  unsigned int gen0 = 0;
-  if (threadIdx.x == 0) gen0 = ld_acquire(&sync->gen);
+  __shared__ AdamArgs s_ad;  // DEV: the step's constants, formed by this CTA's thread 0
+  // thread 0: the barrier word and the earlier micro-steps' flag as this launch
+  // found them (their kernels have completed; no CTA writes either before the
+  // last one has arrived)
+  unsigned long long rel0 = 0;
+  int32_t flag0 = 0;
+  if (threadIdx.x == 0) {
+    rel0 = ld_acquire_u64(&sync->rel);
+    flag0 = __ldcg(flag);
+  }
   int cur = 0;
   if constexpr (DEV && FLIP) cur = dstate->buf & 1;
   const int64_t nvec = count / EPT;
@@ -1259,8 +1274,13 @@ __global__ void __launch_bounds__(ZS_THREADS, EPT == 8 ? ZS_FUSED_MIN_BLOCKS : Z
     vt = b.v[cur][ti];
   }
   if constexpr (DEV) {
-    if (blockIdx.x == 0 && threadIdx.x == 0)
-      *ad_slot = device_step_args(dstate, n, accum_steps, hp, sched, has_sched);
+    // every CTA forms the constants from the state this launch found (the last
+    // CTA writes the state only after all have arrived): nothing to read back
+    // after the barrier.  CTA 0 also leaves them in the context's slot.
+    if (threadIdx.x == 0) {
+      s_ad = device_step_args(dstate, n, accum_steps, hp, sched, has_sched);
+      if (blockIdx.x == 0) *ad_slot = s_ad;
+    }
   }
   int any_bad = 0;
   if constexpr (CLIP) {
@@ -1273,54 +1293,61 @@ __global__ void __launch_bounds__(ZS_THREADS, EPT == 8 ? ZS_FUSED_MIN_BLOCKS : Z
   } else {
     any_bad = __syncthreads_or(bad);
   }
+  // arrival (thread 0): the release orders this CTA's partial (CLIP) before it;
+  // the last CTA's acquire sees every CTA's, and the count of bad CTAs
+  unsigned int bad_ctas = 0;
   if (threadIdx.x == 0) {
-    if (any_bad) atomicOr(flag, 1);
-    __threadfence();
-    const unsigned int prev = atomicAdd(&sync->arrived, 1u);
-    s_last = prev == expect - 1u;
-    // last to arrive: every CTA's flag bits, partials and (DEV) CTA 0's
-    // constants are visible after this fence
-    if (s_last) __threadfence();
+    const unsigned int prev = atom_add_acq_rel(&sync->arrived, any_bad ? 0x10001u : 1u);
+    s_last = (prev & 0xFFFFu) == expect - 1u;
+    bad_ctas = (prev >> 16) + (any_bad ? 1u : 0u);
+    if (CLIP && s_last) __threadfence();  // the partials, for the whole CTA's fold
   }
   __syncthreads();
   if (s_last) {
     float coef = 1.0f;
+    double clip_val = 0.0;
     if constexpr (CLIP) {
       const double t = fold_partials<true>(partials, (int)gridDim.x);
       if (threadIdx.x == 0) {
         if constexpr (DEV) {
-          const double norm = sqrt(t) / (double)load_args_cg(ad_slot).grad_div;
-          coef = clip_coef_of_norm(norm, max_norm);
-          if (norm_out != nullptr) *norm_out = norm;
+          clip_val = sqrt(t) / (double)s_ad.grad_div;  // the norm
+          coef = clip_coef_of_norm(clip_val, max_norm);
         } else {
-          const double sumsq = t * inv_div2;
-          coef = clip_coef_of_norm(sqrt(sumsq), max_norm);
-          *sumsq_out = sumsq;
+          clip_val = t * inv_div2;  // the squared norm
+          coef = clip_coef_of_norm(sqrt(clip_val), max_norm);
         }
       }
     }
     if (threadIdx.x == 0) {
-      const int32_t ovf = atomicExch(flag, 0) != 0 ? 1 : 0;
+      const int32_t ovf = (flag0 != 0 || bad_ctas != 0) ? 1 : 0;
+      // reset for the next launch, then release: nothing the waiting CTAs need
+      // comes after this store
+      sync->arrived = 0u;
+      if (flag0 != 0) *flag = 0;
+      st_release_u64(&sync->rel,
+                     (unsigned long long)(((unsigned int)rel0 + 1u) & 0x7FFFFFFFu) |
+                         ((unsigned long long)ovf << 31) |
+                         ((unsigned long long)__float_as_uint(coef) << 32));
+      // the step's outcome, read once the kernel has completed
       if constexpr (DEV) {
-        device_state_step(dstate, ovf, load_args_cg(ad_slot));
+        device_state_step(dstate, ovf, s_ad);
         if (FLIP && !ovf) dstate->buf = cur ^ 1;
+        if (CLIP && norm_out != nullptr) *norm_out = clip_val;
       } else {
         if (result != nullptr) scaler_step(scaler_in, ovf, result);
+        if (CLIP) *sumsq_out = clip_val;
       }
-      sync->overflow = ovf;
-      sync->coef = coef;
-      sync->arrived = 0u;
-      __threadfence();
-      atomicAdd(&sync->gen, 1u);
       s_go = !ovf;
       s_coef = coef;
     }
   } else if (threadIdx.x == 0) {
-    int go = 0;
-    const uint64_t t0 = global_ns();
+    const unsigned int gen0 = (unsigned int)rel0 & 0x7FFFFFFFu;
+    unsigned long long x = 0;
     bool released = false;
+    const uint64_t t0 = global_ns();
     for (;;) {
-      if (ld_acquire(&sync->gen) != gen0) {
+      x = ld_acquire_u64(&sync->rel);
+      if (((unsigned int)x & 0x7FFFFFFFu) != gen0) {
         released = true;
         break;
       }
@@ -1328,27 +1355,18 @@ __global__ void __launch_bounds__(ZS_THREADS, EPT == 8 ? ZS_FUSED_MIN_BLOCKS : Z
       __nanosleep(32);
     }
     if (released) {
-      go = __ldcg(&sync->overflow) == 0;
-      s_coef = __ldcg(&sync->coef);
+      s_go = ((x >> 31) & 1u) == 0;
+      s_coef = __uint_as_float((unsigned int)(x >> 32));
     } else {
       *reinterpret_cast<volatile int32_t*>(err) = 1;
+      s_go = 0;
     }
-    s_go = go;
   }
   __syncthreads();
   if (!s_go) return;
   const float coef = s_coef;
   AdamArgs ad = ad_host;
-  if constexpr (DEV) {
-    // one L2 read of the constants per CTA (every thread reading them hits one
-    // L2 line from every warp of the grid), shared through shared memory
-    constexpr int kArgWords = (int)(sizeof(AdamArgs) / sizeof(float));
-    __shared__ float s_args[kArgWords];
-    if (threadIdx.x < kArgWords)
-      s_args[threadIdx.x] = __ldcg(reinterpret_cast<const float*>(ad_slot) + threadIdx.x);
-    __syncthreads();
-    ad = *reinterpret_cast<const AdamArgs*>(s_args);
-  }
+  if constexpr (DEV) ad = s_ad;
   if (unit) {
 #pragma unroll
     for (int k = 0; k < EPT; ++k) adamw1<CLIP>(ad, a[k], p[k], m[k], v[k], coef);
