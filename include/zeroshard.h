@@ -164,9 +164,12 @@ zs_status zs_ctx_destroy(zs_ctx* ctx);
  * CTAs are all resident at once (zs_ctx_fused_capacity: about 0.93M elements
  * on GB300): each thread loads its elements' last micro-step sums (acc + the
  * n slices, in the order zs_grad_accum adds them) and their state into
- * registers, the grid ORs the overflow flag (and, clipped, each CTA's total
- * of squares, folded by the last CTA in the order of the norm pass), one grid
- * barrier resolves it, and a clean step applies the same AdamW arithmetic
+ * registers, each CTA arrives at one grid barrier counting whether its sums
+ * hold a non-finite value (clipped: after writing its total of squares); the
+ * last CTA to arrive forms the step's flag from that count and the earlier
+ * micro-steps' flag (and, clipped, folds the totals in the order of the norm
+ * pass), clears the flag and releases the grid, and a clean step applies the
+ * same AdamW arithmetic
  * from the registers; an overflow writes no state.  Results (norm included)
  * are bit for bit those of the multi-kernel path.  The barrier
  * relies on every CTA of the grid being resident at once, which the
