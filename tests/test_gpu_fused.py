@@ -68,10 +68,14 @@ def same_state(a, b, where):
 
 
 def inject(grads, s, G, n, count, dtype):
-    """An inf on the last micro-step at step 3, on the first at step 7."""
+    """An inf on the last micro-step at step 3, on the first at step 7; at
+    step 5 NaNs every 997 elements of the last micro-step, so that every CTA
+    of a large grid arrives at the barrier with a non-finite sum."""
     if s in (3, 7):
         k = G - 1 if s == 3 else 0
         grads[k][n - 1][count // 3] = 0x7C00 if dtype == FP16 else 0x7F80
+    if s == 5:
+        grads[G - 1][0][::997] = 0x7E00 if dtype == FP16 else 0x7FC0
 
 
 @pytest.mark.parametrize("dtype", [FP16, BF16])
