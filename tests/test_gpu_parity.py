@@ -541,6 +541,29 @@ def test_two_contexts_on_two_streams(zs):
             assert torch.equal(x, y)
 
 
+def test_default_stream_is_the_current_torch_stream(zs):
+    """A call given no stream launches on the calling thread's current torch
+    stream: the default one, or the one a `torch.cuda.stream` block makes
+    current (the work is then ordered on it alone)."""
+    assert zs._stream(None) == torch.cuda.current_stream().cuda_stream
+    side = torch.cuda.Stream()
+    ctx = zs.Ctx()
+    try:
+        count = 1 << 20
+        g = [torch.full((count,), 0x3C00, dtype=torch.int16, device="cuda")]   # fp16 1.0
+        acc = torch.zeros(count, dtype=torch.float32, device="cuda")
+        torch.cuda.synchronize()
+        with torch.cuda.stream(side):
+            assert zs._stream(None) == side.cuda_stream != torch.cuda.default_stream().cuda_stream
+            for k in range(3):
+                zs.zs_grad_accum(ctx, g, FP16, count, acc, k == 0)
+        side.synchronize()
+        assert torch.all(acc == 3.0)
+        assert zs._stream(None) == torch.cuda.current_stream().cuda_stream
+    finally:
+        ctx.close()
+
+
 def test_timing_skips_launches_captured_into_a_graph(zs):
     """With timing on, a launch captured into a CUDA graph records no events
     (they would be timed once per capture, and could not be waited on after

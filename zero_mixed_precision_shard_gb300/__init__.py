@@ -175,10 +175,20 @@ def _addr(x) -> int | None:
     return x.data_ptr()
 
 
+def _current_stream() -> int:
+    """The calling thread's current torch stream on the current device, as a
+    cudaStream_t (a Stream object costs a few microseconds to build; a short
+    step is launched in about as long)."""
+    import torch
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None:
+        return raw(torch._C._cuda_getDevice())
+    return torch.cuda.current_stream().cuda_stream
+
+
 def _stream(s) -> int | None:
     if s is None:
-        import torch
-        return torch.cuda.current_stream().cuda_stream
+        return _current_stream()
     if isinstance(s, int):
         return s
     return s.cuda_stream
