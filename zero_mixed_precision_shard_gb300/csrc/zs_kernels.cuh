@@ -1295,9 +1295,21 @@ __global__ void __launch_bounds__(ZS_THREADS, EPT == 8 ? ZS_FUSED_MIN_BLOCKS : Z
   }
   // arrival (thread 0): the release orders this CTA's partial (CLIP) before it;
   // the last CTA's acquire sees every CTA's, and the count of bad CTAs
+  unsigned int prev = 0;
+  if (threadIdx.x == 0) prev = atom_add_acq_rel(&sync->arrived, any_bad ? 0x10001u : 1u);
+  AdamArgs ad = ad_host;
+  if constexpr (DEV) ad = s_ad;
+  if constexpr (!CLIP) {
+    // unclipped, the update does not depend on the barrier's outcome (an
+    // overflow just writes none of it): form it while the grid arrives
+    if (unit) {
+#pragma unroll
+      for (int k = 0; k < EPT; ++k) adamw1<false>(ad, a[k], p[k], m[k], v[k]);
+    }
+    if (tail) adamw1<false>(ad, at, pt, mt, vt);
+  }
   unsigned int bad_ctas = 0;
   if (threadIdx.x == 0) {
-    const unsigned int prev = atom_add_acq_rel(&sync->arrived, any_bad ? 0x10001u : 1u);
     s_last = (prev & 0xFFFFu) == expect - 1u;
     bad_ctas = (prev >> 16) + (any_bad ? 1u : 0u);
     if (CLIP && s_last) __threadfence();  // the partials, for the whole CTA's fold
@@ -1364,19 +1376,21 @@ __global__ void __launch_bounds__(ZS_THREADS, EPT == 8 ? ZS_FUSED_MIN_BLOCKS : Z
   }
   __syncthreads();
   if (!s_go) return;
-  const float coef = s_coef;
-  AdamArgs ad = ad_host;
-  if constexpr (DEV) ad = s_ad;
-  if (unit) {
+  if constexpr (CLIP) {
+    const float coef = s_coef;
+    if (unit) {
 #pragma unroll
-    for (int k = 0; k < EPT; ++k) adamw1<CLIP>(ad, a[k], p[k], m[k], v[k], coef);
+      for (int k = 0; k < EPT; ++k) adamw1<true>(ad, a[k], p[k], m[k], v[k], coef);
+    }
+    if (tail) adamw1<true>(ad, at, pt, mt, vt, coef);
+  }
+  if (unit) {
     store_unit<EPT>(b.p[cur ^ 1], tid, p);
     store_unit<EPT>(b.m[cur ^ 1], tid, m);
     store_unit<EPT>(b.v[cur ^ 1], tid, v);
     store_half_unit<DT, EPT>(b.h[cur ^ 1], tid, p);
   }
   if (tail) {
-    adamw1<CLIP>(ad, at, pt, mt, vt, coef);
     b.p[cur ^ 1][ti] = pt;
     b.m[cur ^ 1][ti] = mt;
     b.v[cur ^ 1][ti] = vt;
