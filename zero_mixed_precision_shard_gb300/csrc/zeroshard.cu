@@ -653,21 +653,24 @@ zs_status update_oop(zs_ctx* c, zs_dtype dt, const zs::SlicePtrs& sp, int32_t n,
   return ZS_OK;
 }
 
-// A cooperative launch (every CTA co-resident, or the launch fails), without
-// the programmatic-dependent attribute: the kernel starts once its predecessor
-// in the stream has completed.
+// A cooperative launch (every CTA co-resident, or the launch fails); with
+// c->pdl also a programmatic dependent of its predecessor, like the step's
+// other kernels.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_coop(void (*kernel)(KArgs...), int grid, cudaStream_t s, Args&&... args) {
+cudaError_t launch_coop(zs_ctx* c, void (*kernel)(KArgs...), int grid, cudaStream_t s,
+                        Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3((unsigned)zs::kThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = c->pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
@@ -701,7 +704,7 @@ int fused_launch_k(zs_ctx* c, const FusedCall& f, cudaStream_t s, cudaError_t* e
   // ZS_FUSED_TEST_TIMEOUT: the barrier waits for one CTA more than the grid has
   const unsigned expect = (unsigned)grid + (c->fused_mode == ZS_FUSED_TEST_TIMEOUT ? 1u : 0u);
   LaunchScope ls(c, s, ZS_KERNEL_FUSED, f.count);
-  *e = launch_coop(k, (int)grid, s, f.sp, f.n, f.acc, f.b, f.count, f.ad, f.scaler,
+  *e = launch_coop(c, k, (int)grid, s, f.sp, f.n, f.acc, f.b, f.count, f.ad, f.scaler,
                    DEV ? (zs::StepResult*)nullptr : c->d_result, f.dstate, f.hp, f.sched,
                    f.has_sched, f.accum_steps, c->d_args, c->d_flag, c->d_sync, expect,
                    (uint64_t)c->wait_ns, c->d_fused_err, f.max_norm, f.inv_div2,

@@ -1220,9 +1220,12 @@ __global__ void __launch_bounds__(ZS_THREADS, EPT == 8 ? ZS_FUSED_MIN_BLOCKS : Z
                  AdamArgs* ad_slot, int32_t* flag, FusedSync* sync, unsigned int expect,
                  uint64_t wait_ns, int32_t* err, float max_norm, double inv_div2,
                  double* partials, double* sumsq_out, double* norm_out) {
-  // Launched without the programmatic-dependent attribute (it starts once its
-  // predecessor has completed), and it lets no successor start early either:
-  // no griddepcontrol here, so no other grid's CTAs take SM room while it runs.
+  // As a programmatic dependent: its CTAs are placed while the predecessor
+  // drains and wait here for its completion.  The successor may be placed
+  // once every CTA of this grid has triggered, that is once the whole grid is
+  // resident, so no later grid takes room the barrier needs.
+  pdl_enter(&s, acc, &b, dstate, ad_slot, flag, sync, err, partials, sumsq_out, norm_out,
+            result);
   // EPT: elements per thread (8; or 4, twice the threads for shards that fit,
   // unclipped only: the norm keeps the norm pass's 8-element CTA partition).
   static_assert(EPT == 8 || (EPT == 4 && !CLIP), "4-element units are unclipped only");
