@@ -72,7 +72,7 @@ def kernel_alg_bytes(kind: str, n: int, first: bool = False, with_acc: bool = Fa
     if kind == "update_oop":   # last micro-step + flag + update, state written out of place
         return (acc_bytes if with_acc else 0) + 2 * n + 26
     if kind == "fused":   # last micro-step + flag + grid barrier + update, one kernel
-        return (4 if with_acc else 0) + 2 * n + 26
+        return (acc_bytes if with_acc else 0) + 2 * n + 26
     raise ValueError(kind)
 
 
@@ -85,9 +85,11 @@ def step_launch_plan(n: int, g: int, dtype: str, acc_kind: str = "fp32", has_acc
     oop: the out-of-place step, whose last pass is the update; fused: the
     shard fits the fused step, whose last call is one kernel in every form)."""
     if fused:
+        ab = 2 if acc_kind == "half" else 4
         plan = [("reduce_first" if k == 0 else "reduce",
-                 kernel_alg_bytes("reduce", n, first=(k == 0))) for k in range(g - 1)]
-        plan.append(("fused", kernel_alg_bytes("fused", n, with_acc=g > 1)))
+                 kernel_alg_bytes("reduce", n, first=(k == 0), acc_bytes=ab))
+                for k in range(g - 1)]
+        plan.append(("fused", kernel_alg_bytes("fused", n, with_acc=g > 1, acc_bytes=ab)))
         return plan
     if oop:
         ab = 2 if acc_kind == "half" else 4
@@ -280,9 +282,9 @@ class DeviceWorkload:
 
     def takes_fused(self, ctx, api: str) -> bool:
         """Whether `api`'s last call runs as the fused single-kernel step here:
-        the fp32-accumulator forms (clipped or not), when the shard fits one
+        every form (clipped or not, either accumulator), when the shard fits one
         co-resident grid (and the context has the fused step on)."""
-        return (api in ("async", "async_oop", "graph", "sync") and self.acc_kind == "fp32"
+        return (api in ("async", "async_oop", "graph", "sync")
                 and self.E <= ctx.fused_capacity
                 and os.environ.get("ZEROSHARD_FUSED", "1") != "0")
 

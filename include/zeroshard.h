@@ -158,8 +158,10 @@ zs_status zs_ctx_destroy(zs_ctx* ctx);
 /* The fused step (§2.2, §4.2: the step's overflow resolved before any state
  * is written, here by a grid barrier inside one kernel).
  * zs_shard_step, zs_shard_step_async, zs_shard_step_oop,
- * zs_shard_step_async_oop, zs_shard_step_clipped and
- * zs_shard_step_async_clipped run the whole last call of a step as ONE
+ * zs_shard_step_async_oop, zs_shard_step_clipped,
+ * zs_shard_step_async_clipped and the four zs_shard_step_halfacc forms (the
+ * sums rounded to the accumulator's format first) run the whole last call of
+ * a step as ONE
  * cooperative kernel when one thread per 8 owned elements fits a grid whose
  * CTAs are all resident at once (zs_ctx_fused_capacity: about 0.93M elements
  * on GB300): each thread loads its elements' last micro-step sums (acc + the
@@ -288,8 +290,11 @@ zs_status zs_shard_step(zs_ctx* ctx, const void* const* grads, int32_t n, zs_dty
 zs_status zs_grad_accum_halfacc(zs_ctx* ctx, const void* const* grads, int32_t n, zs_dtype dt,
                                 int64_t count, void* acc_half, int32_t first,
                                 cudaStream_t stream);
-/* The last call of a step with the half accumulator (always sums the last
- * micro-step into acc_half, then updates from it); otherwise as zs_shard_step. */
+/* The last call of a step with the half accumulator; otherwise as
+ * zs_shard_step.  The multi-kernel path sums the last micro-step into acc_half
+ * (rounded) and updates from it; a shard that fits the fused step rounds the
+ * same sums in registers and leaves acc_half unwritten.  Either way acc_half
+ * holds no defined sums after the call. */
 zs_status zs_shard_step_halfacc(zs_ctx* ctx, const void* const* grads, int32_t n, zs_dtype dt,
                                 int64_t count, void* acc_half, int32_t accum_steps,
                                 float* master, float* m, float* v, void* half_out,

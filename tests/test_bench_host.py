@@ -147,6 +147,9 @@ def test_fused_plan_moves_exactly_the_algorithmic_bytes():
         assert [k for k, _ in plan] == ["reduce_first"] * (wl.g > 1) + ["reduce"] * max(
             0, wl.g - 2) + ["fused"]
         assert sum(b for _, b in plan) == bench.alg_bytes_per_elem_step(wl.n, wl.g)
+        half = bench.step_launch_plan(wl.n, wl.g, wl.dtype, acc_kind="half", fused=True)
+        assert [k for k, _ in half] == [k for k, _ in plan]
+        assert sum(b for _, b in half) == bench.alg_bytes_per_elem_step(wl.n, wl.g, acc_bytes=2)
 
 
 def test_bench_line_names_the_entry_points_each_api_calls():

@@ -21,9 +21,12 @@ def zs():
     return pkg
 
 
-@pytest.fixture(scope="module")
-def ctx(zs):
+@pytest.fixture(scope="module", params=["fused", "multi"])
+def ctx(zs, request):
+    """Every test runs with the fused single-kernel step (the shards here fit
+    one co-resident grid) and with the multi-kernel path."""
     c = zs.Ctx()
+    c.set_fused(zs.ZS_FUSED_ON if request.param == "fused" else zs.ZS_FUSED_OFF)
     yield c
     c.close()
 
@@ -266,3 +269,88 @@ def test_halfacc_device_state_steps_equal_the_synchronising_step(zs, ctx, form, 
     close(ref[0].cpu().numpy(), st.master, "master")
     close(ref[1].cpu().numpy(), st.m, "m")
     close(ref[2].cpu().numpy(), st.v, "v")
+
+
+@pytest.mark.parametrize("form", ["sync", "oop", "async", "async_oop"])
+@pytest.mark.parametrize("dtype", [FP16, BF16])
+@pytest.mark.parametrize("n,G,count", [(1, 1, 4099), (2, 3, 65_541), (16, 2, 20_011),
+                                       (3, 1, 900_001)])
+def test_halfacc_fused_step_equals_the_multi_kernel_path(zs, form, dtype, n, G, count):
+    """The half-accumulator forms' last call as one fused kernel (4-element
+    units, or 8 for the 900,001-element shard): the last micro-step's sums
+    rounded to the accumulator's format before the flag and the update, as the
+    half-accumulator passes round them.  Every step's state equals the
+    multi-kernel path's bit for bit (a NaN step and a sum that rounds past the
+    half maximum included), one fused launch a step."""
+    on, off = zs.Ctx(), zs.Ctx()
+    try:
+        off.set_fused(zs.ZS_FUSED_OFF)
+        on.set_timing(True)
+        rng = np.random.default_rng(900 + 10 * n + G + dtype + 100 * len(form))
+        master0 = (rng.standard_normal(count) * 0.02).astype(np.float32)
+        dyn = dtype == FP16
+        hp = zs.make_hparams(STRESS_LR, 0.9, 0.999, 1e-8, 0.01)
+        big = 40_000.0 if dtype == FP16 else 2.0e38
+
+        def bufs(m0):
+            p = torch.from_numpy(m0.copy()).cuda()
+            return [p, torch.zeros_like(p), torch.zeros_like(p),
+                    torch.zeros(count, dtype=torch.int16, device="cuda")]
+        run = {}
+        for name, ctx in (("on", on), ("off", off)):
+            sets = [bufs(master0), bufs(np.zeros_like(master0))]
+            run[name] = {"ctx": ctx, "sets": sets, "cur": 0, "t": 0,
+                         "acc": torch.zeros(count, dtype=torch.int16, device="cuda"),
+                         "sc": zs.zs_scaler_init(256.0 if dyn else 1.0, 1.0, 3, 1, dyn),
+                         "state": zs.DeviceState(zs.zs_scaler_init(256.0 if dyn else 1.0, 1.0,
+                                                                   3, 1, dyn)),
+                         "pairs": [zs.pointer_array([sets[0][k], sets[1][k]])
+                                   for k in range(4)]}
+        f0 = on.timing(zs.ZS_KERNEL_FUSED)[1]
+        for s in range(1, 7):
+            grads = [[lib_half((rng.standard_normal(count) * 1e-2 * 256.0).astype(np.float32),
+                               dtype) for _ in range(n)] for _ in range(G)]
+            if s == 3:
+                grads[G - 1][n - 1][count // 3] = 0x7E00 if dyn else 0x7FC0
+            if s == 5 and n * G > 1:
+                grads[0][0][7] = grads[G - 1][n - 1][7] = lib_half(np.float32([big]), dtype)[0]
+            dg = [[dev16(x) for x in micro] for micro in grads]
+            out = {}
+            for name, r in run.items():
+                ctx, acc, sets = r["ctx"], r["acc"], r["sets"]
+                for k in range(G - 1):
+                    zs.zs_grad_accum_halfacc(ctx, dg[k], dtype, count, acc, k == 0)
+                cur = sets[r["cur"]]
+                if form == "sync":
+                    out[name] = zs.zs_shard_step_halfacc(ctx, dg[G - 1], dtype, count, acc, G,
+                                                         *cur, hp, r["t"] + 1, r["sc"])
+                elif form == "oop":
+                    dst = sets[r["cur"] ^ 1]
+                    out[name] = zs.zs_shard_step_halfacc_oop(
+                        ctx, dg[G - 1], dtype, count, acc if G > 1 else None, G, *cur[:3],
+                        *dst, hp, r["t"] + 1, r["sc"])
+                    if not out[name][0]:
+                        r["cur"] ^= 1
+                elif form == "async":
+                    zs.zs_shard_step_halfacc_async(ctx, dg[G - 1], dtype, count, acc, G, *cur,
+                                                   hp, None, r["state"])
+                else:
+                    zs.zs_shard_step_halfacc_async_oop(ctx, dg[G - 1], dtype, count,
+                                                       acc if G > 1 else None, G, *r["pairs"],
+                                                       hp, None, r["state"])
+                if form in ("async", "async_oop"):
+                    d = r["state"].read()
+                    out[name] = (d.overflow, d.scaler.scale, d.step)
+                    if form == "async_oop":
+                        r["cur"] = d.buf & 1
+                if not out[name][0]:
+                    r["t"] += 1
+            assert out["on"] == out["off"], f"step {s}"
+            a, b = run["on"], run["off"]
+            for k in range(4):
+                assert torch.equal(a["sets"][a["cur"]][k], b["sets"][b["cur"]][k]), (s, k)
+        assert on.timing(zs.ZS_KERNEL_FUSED)[1] - f0 == 6      # one launch a step
+        assert run["on"]["t"] == run["off"]["t"] == (4 if n * G > 1 else 5)
+    finally:
+        on.close()
+        off.close()

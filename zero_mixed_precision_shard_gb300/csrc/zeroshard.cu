@@ -691,11 +691,12 @@ struct FusedCall {
   float max_norm = 0.0f;       // clipping (> 0): the fused kernel forms the norm too
   double inv_div2 = 1.0;       // 1 / grad_div^2 (host constants) for the squared norm
   double* norm_out = nullptr;  // device forms: the step's norm (may be NULL)
+  bool hacc = false;           // acc holds halves (the half accumulator; unclipped)
 };
 
-template <int DT, bool HA, bool DEV, bool FLIP, bool CLIP, int EPT>
+template <int DT, bool HA, bool DEV, bool FLIP, bool CLIP, int EPT, bool HACC = false>
 int fused_launch_k(zs_ctx* c, const FusedCall& f, cudaStream_t s, cudaError_t* e) {
-  auto k = zs::k_step_fused<DT, HA, DEV, FLIP, CLIP, EPT>;
+  auto k = zs::k_step_fused<DT, HA, DEV, FLIP, CLIP, EPT, HACC>;
   const int64_t per_grid = (int64_t)resident_ctas(c, k) * c->sms;
   int64_t grid = ((f.count / EPT) + zs::kThreads - 1) / zs::kThreads;
   if (grid < 1) grid = 1;
@@ -727,6 +728,15 @@ int fused_launch_k(zs_ctx* c, const FusedCall& f, cudaStream_t s, cudaError_t* e
 // Returns false to take the multi-pass path; otherwise *st is the launch's status.
 template <bool DEV, bool FLIP, bool CLIP, int EPT>
 int fused_dispatch(zs_ctx* c, zs_dtype dt, const FusedCall& f, cudaStream_t s, cudaError_t* e) {
+  if constexpr (!CLIP) {
+    if (f.hacc) {
+      if (dt == ZS_FP16)
+        return f.acc ? fused_launch_k<ZS_FP16, true, DEV, FLIP, false, EPT, true>(c, f, s, e)
+                     : fused_launch_k<ZS_FP16, false, DEV, FLIP, false, EPT, true>(c, f, s, e);
+      return f.acc ? fused_launch_k<ZS_BF16, true, DEV, FLIP, false, EPT, true>(c, f, s, e)
+                   : fused_launch_k<ZS_BF16, false, DEV, FLIP, false, EPT, true>(c, f, s, e);
+    }
+  }
   if (dt == ZS_FP16)
     return f.acc ? fused_launch_k<ZS_FP16, true, DEV, FLIP, CLIP, EPT>(c, f, s, e)
                  : fused_launch_k<ZS_FP16, false, DEV, FLIP, CLIP, EPT>(c, f, s, e);
@@ -755,7 +765,12 @@ int fused_resident(zs_ctx* c) {
   int r = resident_ctas(c, zs::k_step_fused<ZS_FP16, true, DEV, FLIP, CLIP, 8>);
   r = std::min(r, resident_ctas(c, zs::k_step_fused<ZS_FP16, false, DEV, FLIP, CLIP, 8>));
   r = std::min(r, resident_ctas(c, zs::k_step_fused<ZS_BF16, true, DEV, FLIP, CLIP, 8>));
-  return std::min(r, resident_ctas(c, zs::k_step_fused<ZS_BF16, false, DEV, FLIP, CLIP, 8>));
+  r = std::min(r, resident_ctas(c, zs::k_step_fused<ZS_BF16, false, DEV, FLIP, CLIP, 8>));
+  if constexpr (!CLIP) {  // the half-accumulator forms
+    r = std::min(r, resident_ctas(c, zs::k_step_fused<ZS_FP16, true, DEV, FLIP, false, 8, true>));
+    r = std::min(r, resident_ctas(c, zs::k_step_fused<ZS_BF16, true, DEV, FLIP, false, 8, true>));
+  }
+  return r;
 }
 
 zs::OopBufs in_place_bufs(float* master, float* m, float* v, void* half_out) {
@@ -1608,6 +1623,23 @@ zs_status zs_shard_step_halfacc(zs_ctx* c, const void* const* grads, int32_t n, 
   if (!(grad_div > 0.0f) || !std::isfinite(grad_div))
     return fail(c, ZS_ERR_ARG, "n * accum_steps * scale is not a positive finite fp32");
   const zs::AdamArgs ad = adam_args(hp, step, grad_div);
+  {
+    FusedCall f;
+    f.sp = sp;
+    f.n = n;
+    f.acc = accum_steps > 1 ? static_cast<const float*>(acc_half) : nullptr;
+    f.b = in_place_bufs(master, m, v, half_out);
+    f.count = count;
+    f.ad = ad;
+    f.scaler = *scaler;
+    f.accum_steps = accum_steps;
+    f.hacc = true;
+    zs_status fst = ZS_OK;
+    if (try_fused<false, false>(c, dt, f, stream, &fst)) {
+      ZS_TRY(fst);
+      return finish_fused_step(c, scaler, overflow_out, new_scale_out, stream);
+    }
+  }
   if (count > 0)
     ZS_TRY(reduce_hacc(c, dt, sp, n, acc_half, count, accum_steps > 1, c->d_flag, stream));
   ZS_TRY(apply_hacc(c, dt, c->d_flag, acc_half, count, ad, master, m, v, half_out, scaler,
@@ -1648,6 +1680,23 @@ zs_status zs_shard_step_halfacc_oop(zs_ctx* c, const void* const* grads, int32_t
   b.v[1] = v_out;
   b.h[0] = nullptr;
   b.h[1] = static_cast<uint16_t*>(half_out);
+  {
+    FusedCall f;
+    f.sp = sp;
+    f.n = n;
+    f.acc = acc;
+    f.b = b;
+    f.count = count;
+    f.ad = ad;
+    f.scaler = *scaler;
+    f.accum_steps = accum_steps;
+    f.hacc = true;
+    zs_status fst = ZS_OK;
+    if (try_fused<false, false>(c, dt, f, stream, &fst)) {
+      ZS_TRY(fst);
+      return finish_fused_step(c, scaler, overflow_out, new_scale_out, stream);
+    }
+  }
   if (count > 0) {
     LaunchScope ls(c, stream, ZS_KERNEL_UPDATE_OOP, count);
     if (dt == ZS_FP16) {
@@ -1702,10 +1751,26 @@ zs_status zs_shard_step_halfacc_async(zs_ctx* c, const void* const* grads, int32
   ZS_TRY(check_array(c, m, "m", count));
   ZS_TRY(check_array(c, v, "v", count));
   ZS_TRY(check_array(c, half_out, "half_out", count));
-  if (count > 0)
-    ZS_TRY(reduce_hacc(c, dt, sp, n, acc_half, count, accum_steps > 1, c->d_flag, stream));
   zs_lr_schedule sc{};
   if (sched) sc = *sched;
+  {
+    FusedCall f;
+    f.sp = sp;
+    f.n = n;
+    f.acc = accum_steps > 1 ? static_cast<const float*>(acc_half) : nullptr;
+    f.b = in_place_bufs(master, m, v, half_out);
+    f.count = count;
+    f.dstate = d_state;
+    f.hp = *hp;
+    f.sched = sc;
+    f.has_sched = sched ? 1 : 0;
+    f.accum_steps = accum_steps;
+    f.hacc = true;
+    zs_status fst = ZS_OK;
+    if (try_fused<true, false>(c, dt, f, stream, &fst)) return fst;
+  }
+  if (count > 0)
+    ZS_TRY(reduce_hacc(c, dt, sp, n, acc_half, count, accum_steps > 1, c->d_flag, stream));
   launch_k(c, zs::k_step_prologue, 1, 32, stream, (const zs_device_state*)d_state, n,
            accum_steps, *hp, sc, sched ? 1 : 0, c->d_args);
   c->launches += 1;
@@ -1739,9 +1804,6 @@ zs_status zs_shard_step_halfacc_async_oop(zs_ctx* c, const void* const* grads, i
   ZS_TRY(check_oop(c, grads, n, dt, count, acc, accum_steps, pp, mm, vv, hh, &sp));
   zs_lr_schedule sc{};
   if (sched) sc = *sched;
-  launch_k(c, zs::k_step_prologue, 1, 32, stream, (const zs_device_state*)d_state, n,
-           accum_steps, *hp, sc, sched ? 1 : 0, c->d_args);
-  c->launches += 1;
   zs::OopBufs b;
   for (int i = 0; i < 2; ++i) {
     b.p[i] = master[i];
@@ -1749,6 +1811,25 @@ zs_status zs_shard_step_halfacc_async_oop(zs_ctx* c, const void* const* grads, i
     b.v[i] = v[i];
     b.h[i] = static_cast<uint16_t*>(half[i]);
   }
+  {
+    FusedCall f;
+    f.sp = sp;
+    f.n = n;
+    f.acc = acc;
+    f.b = b;
+    f.count = count;
+    f.dstate = d_state;
+    f.hp = *hp;
+    f.sched = sc;
+    f.has_sched = sched ? 1 : 0;
+    f.accum_steps = accum_steps;
+    f.hacc = true;
+    zs_status fst = ZS_OK;
+    if (try_fused<true, true>(c, dt, f, stream, &fst)) return fst;
+  }
+  launch_k(c, zs::k_step_prologue, 1, 32, stream, (const zs_device_state*)d_state, n,
+           accum_steps, *hp, sc, sched ? 1 : 0, c->d_args);
+  c->launches += 1;
   if (count > 0) {
     LaunchScope ls(c, stream, ZS_KERNEL_UPDATE_OOP, count);
     const zs::AdamArgs unused{};

@@ -1166,6 +1166,20 @@ __device__ __forceinline__ void load_unit(const float* p, int64_t u, float (&a)[
   }
 }
 
+// EPT half-format accumulator values of unit u, widened (exact).
+template <int DT, int EPT>
+__device__ __forceinline__ void load_half_unit(const float* acc_half, int64_t u, float (&a)[EPT]) {
+  if constexpr (EPT == 8) {
+    load8_hacc<DT>(acc_half, u, a);
+  } else {
+    const uint2 h = __ldcs(reinterpret_cast<const uint2*>(acc_half) + u);
+    a[0] = half_bits_to_float<DT>(h.x & 0xFFFFu);
+    a[1] = half_bits_to_float<DT>(h.x >> 16);
+    a[2] = half_bits_to_float<DT>(h.y & 0xFFFFu);
+    a[3] = half_bits_to_float<DT>(h.y >> 16);
+  }
+}
+
 template <int EPT>
 __device__ __forceinline__ void store_unit(float* p, int64_t u, const float (&a)[EPT]) {
   if constexpr (EPT == 8) {
@@ -1211,7 +1225,10 @@ __device__ __forceinline__ void store_half_unit(uint16_t* h, int64_t u, const fl
 // A CTA whose wait passes wait_ns gives up: it writes nothing and sets *err.
 // `expect` is the number of arrivals that resolve the step (the grid size,
 // below 2^16).
-template <int DT, bool HAS_ACC, bool DEV, bool FLIP, bool CLIP, int EPT = 8>
+// HACC: acc holds halves of the gradient's format (the half accumulator); each
+// sum is rounded to that format before the flag and the update, as the
+// half-accumulator passes round it.
+template <int DT, bool HAS_ACC, bool DEV, bool FLIP, bool CLIP, int EPT = 8, bool HACC = false>
 __global__ void __launch_bounds__(ZS_THREADS, EPT == 8 ? ZS_FUSED_MIN_BLOCKS : ZS_FUSED4_MIN_BLOCKS)
     k_step_fused(const __grid_constant__ SlicePtrs s, int n, const float* acc,
                  const __grid_constant__ OopBufs b, int64_t count, AdamArgs ad_host,
@@ -1229,6 +1246,7 @@ __global__ void __launch_bounds__(ZS_THREADS, EPT == 8 ? ZS_FUSED_MIN_BLOCKS : Z
   // EPT: elements per thread (8; or 4, twice the threads for shards that fit,
   // unclipped only: the norm keeps the norm pass's 8-element CTA partition).
   static_assert(EPT == 8 || (EPT == 4 && !CLIP), "4-element units are unclipped only");
+  static_assert(!(HACC && CLIP), "the half accumulator has no clipped form");
   __shared__ int s_go;
   __shared__ int s_last;
   __shared__ float s_coef;
@@ -1255,7 +1273,8 @@ __global__ void __launch_bounds__(ZS_THREADS, EPT == 8 ? ZS_FUSED_MIN_BLOCKS : Z
   bool bad = false;
   if (unit) {
     if (HAS_ACC) {
-      load_unit<EPT>(acc, tid, a);
+      if constexpr (HACC) load_half_unit<DT, EPT>(acc, tid, a);
+      else load_unit<EPT>(acc, tid, a);
     } else {
 #pragma unroll
       for (int k = 0; k < EPT; ++k) a[k] = 0.0f;
@@ -1264,12 +1283,20 @@ __global__ void __launch_bounds__(ZS_THREADS, EPT == 8 ? ZS_FUSED_MIN_BLOCKS : Z
     load_unit<EPT>(b.m[cur], tid, m);
     load_unit<EPT>(b.v[cur], tid, v);
     sum_unit<DT, EPT>(s, n, tid, a);
+    if constexpr (HACC) {
+#pragma unroll
+      for (int k = 0; k < EPT; ++k) a[k] = half_bits_to_float<DT>(float_to_half_bits<DT>(a[k]));
+    }
 #pragma unroll
     for (int k = 0; k < EPT; ++k) bad |= not_finite(a[k]);
     if constexpr (CLIP) norm_add8(a, sqf, sqb);
   }
   if (tail) {
-    at = sum_slices1<DT>(s, n, ti, HAS_ACC ? acc[ti] : 0.0f);
+    float a0 = 0.0f;
+    if (HAS_ACC)
+      a0 = HACC ? half_bits_to_float<DT>(reinterpret_cast<const uint16_t*>(acc)[ti]) : acc[ti];
+    at = sum_slices1<DT>(s, n, ti, a0);
+    if constexpr (HACC) at = half_bits_to_float<DT>(float_to_half_bits<DT>(at));
     bad |= not_finite(at);
     if constexpr (CLIP) norm_add1(at, sqf, sqb);
     pt = b.p[cur][ti];
