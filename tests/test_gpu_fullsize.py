@@ -3,7 +3,9 @@
 call: zs_shard_step, zs_shard_step_async with the device-resident state,
 zs_shard_step_async_oop with the state written out of place, as the
 benchmark's default does where the second state set fits, or the half
-accumulator's zs_shard_step_halfacc_oop as its --acc half run), checked against
+accumulator's zs_shard_step_halfacc_oop and zs_shard_step_halfacc_async_oop,
+the latter as its --acc half run; the 2^20-parameter workload's shards take
+the fused single-kernel step), checked against
 the oracle on sampled elements, for the first shard and the last (which holds
 the padding where there is any, and the output layers).
 
@@ -69,9 +71,16 @@ def sample_positions(wl, begin, E, valid):
                                             ("decoder-1.3b-n16", 0, "async_oop"),
                                             ("llama7b-zero3-n64", 63, "async_oop"),
                                             ("llama7b-n1", 0, "async_oop"),
-                                            # the half accumulator, out of place (the
-                                            # benchmark's --acc half run)
-                                            ("llama7b-n1", 0, "hacc_oop")])
+                                            # the half accumulator, out of place: the
+                                            # synchronising step and the device-resident
+                                            # one (the benchmark's --acc half run)
+                                            ("llama7b-n1", 0, "hacc_oop"),
+                                            ("llama7b-n1", 0, "hacc_async_oop"),
+                                            # the 2^20-parameter workload: every step is
+                                            # one fused kernel (shard 0 holds the inf)
+                                            ("flat-1m-n2", 0, "async_oop"),
+                                            ("flat-1m-n2", 0, "async"),
+                                            ("flat-1m-n2", 1, "sync")])
 def test_fullsize_sampled(name, shard, api):
     import bench
     import zero_mixed_precision_shard_gb300 as zs
@@ -84,12 +93,14 @@ def test_fullsize_sampled(name, shard, api):
     # the out-of-place case holds two gradient buffers, refilled micro-step by
     # micro-step as a training loop does (the Llama-7B one: 243 GB with both
     # state sets; one buffer per micro-step would not fit)
-    refill = api in ("async_oop", "hacc_oop")
+    oop_dev = api in ("async_oop", "hacc_async_oop")   # out of place, device state
+    refill = oop_dev or api == "hacc_oop"
+    hacc = api.startswith("hacc")
     W = bench.DeviceWorkload(wl, shard=shard, grad_buffers=2 if refill else None,
-                             acc="half" if api == "hacc_oop" else "fp32")
+                             acc="half" if hacc else "fp32")
     W.hacc_oop = api == "hacc_oop"
     state = zs.DeviceState(W.scaler) if api not in ("sync", "hacc_oop") else None
-    step_o = oracle.shard_step_halfacc if api == "hacc_oop" else oracle.shard_step
+    step_o = oracle.shard_step_halfacc if hacc else oracle.shard_step
     E, begin = W.E, W.begin
     valid = W.valid_end - W.begin
     pos = sample_positions(wl, begin, E, valid)
@@ -102,7 +113,7 @@ def test_fullsize_sampled(name, shard, api):
     flags = []
 
     def current(k):
-        if api == "async_oop" and state.read().buf == 1:
+        if oop_dev and state.read().buf == 1:
             return getattr(W, k + "2")
         return getattr(W, k)
 
@@ -140,7 +151,7 @@ def test_fullsize_sampled(name, shard, api):
             ovf = W.step(ctx)
             scale = W.scaler.scale
         else:
-            if api == "async_oop":
+            if oop_dev:
                 for k in range(wl.g):
                     W.fill_micro(s, k, sc_o.scale, inject=True)
                     if k < wl.g - 1:
