@@ -578,6 +578,8 @@ def api_desc(api: str, acc: str, clip: float, hacc_oop: bool) -> str:
                 + ("_oop (the second state set fits)" if hacc_oop else ""))
     if clip and api == "sync":
         return "zs_grad_accum + zs_shard_step_clipped"
+    if clip and api in ("async_oop", "graph_oop"):
+        raise ValueError("the out-of-place step has no clipped form")
     if clip:
         return API_DESC[api].replace("zs_shard_step_async", "zs_shard_step_async_clipped")
     return API_DESC[api]

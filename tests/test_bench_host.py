@@ -4,6 +4,8 @@ the workload and kernel sources it was captured with.  No GPU."""
 import json
 import os
 
+import pytest
+
 import bench
 import synth
 
@@ -164,7 +166,11 @@ def test_bench_line_names_the_entry_points_each_api_calls():
         assert "halfacc" not in bench.api_desc(api, "fp32", 0.0, False)
         assert bench.api_desc(api, "fp32", 0.0, False) == bench.API_DESC[api]
     assert bench.api_desc("sync", "fp32", 1.0, False) == "zs_grad_accum + zs_shard_step_clipped"
-    assert "zs_shard_step_async_clipped_oop" in bench.api_desc("async_oop", "fp32", 1.0, False)
+    assert "zs_shard_step_async_clipped" in bench.api_desc("async", "fp32", 1.0, False)
+    assert "zs_shard_step_async_clipped" in bench.api_desc("graph", "fp32", 1.0, False)
+    for api in ("async_oop", "graph_oop"):     # no clipped out-of-place entry point
+        with pytest.raises(ValueError):
+            bench.api_desc(api, "fp32", 1.0, False)
     assert bench.api_desc("split", "fp32", 1.0, False) == bench.API_DESC["split"]
 
 
