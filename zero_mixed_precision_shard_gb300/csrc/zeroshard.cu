@@ -74,6 +74,7 @@ struct zs_ctx {
   std::unordered_map<const void*, int> occupancy;  // resident CTAs per SM, per kernel
   int64_t launches = 0;
   bool pdl = true;  // launch the step's kernels as programmatic dependents
+  bool coop_pdl = true;  // the fused step's cooperative launch too (off once refused)
   // timing
   bool timing = false;
   struct Rec {
@@ -655,7 +656,7 @@ zs_status update_oop(zs_ctx* c, zs_dtype dt, const zs::SlicePtrs& sp, int32_t n,
 
 // A cooperative launch (every CTA co-resident, or the launch fails); with
 // c->pdl also a programmatic dependent of its predecessor, like the step's
-// other kernels.
+// other kernels, unless the driver refused that pair before.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_coop(zs_ctx* c, void (*kernel)(KArgs...), int grid, cudaStream_t s,
                         Args&&... args) {
@@ -670,8 +671,18 @@ cudaError_t launch_coop(zs_ctx* c, void (*kernel)(KArgs...), int grid, cudaStrea
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = c->pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  cfg.numAttrs = c->pdl && c->coop_pdl ? 2 : 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+  if (cfg.numAttrs == 2 && (e == cudaErrorNotSupported || e == cudaErrorInvalidValue)) {
+    // a driver that refuses the pair of attributes: from now on a plain
+    // cooperative launch (the kernel then starts once its predecessor has
+    // completed; its griddepcontrol instructions do nothing)
+    (void)cudaGetLastError();
+    c->coop_pdl = false;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kernel, args...);
+  }
+  return e;
 }
 
 // The arguments of one fused step (k_step_fused) besides the kernel choice.
