@@ -8,10 +8,12 @@ FP16, BF16 = 0, 1
 
 
 def lib_half(x, dtype):
-    """fp32 values -> half bit patterns, rounded by numpy (fp16) or torch (bf16)."""
+    """fp32 values -> half bit patterns, rounded by numpy (fp16) or torch (bf16);
+    values past the format's range round to infinity, as IEEE rounding does."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     if dtype == FP16:
-        return x.astype(np.float16).view(np.uint16)
+        with np.errstate(over="ignore"):
+            return x.astype(np.float16).view(np.uint16)
     return torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
 
 
