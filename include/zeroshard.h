@@ -527,14 +527,19 @@ zs_status zs_update_oop(zs_ctx* ctx, const void* const* grads, int32_t n, zs_dty
                         float* v_out, void* half_out, const zs_adam_hparams* hp, int64_t step,
                         int32_t* d_flag, cudaStream_t stream);
 
-/* The half-accumulator step without a host round trip, as zs_shard_step_async
- * is to zs_shard_step (scale, Adam's step count and learning rate in
- * *d_state; capturable in a CUDA graph): in place (the last micro-step summed
- * into acc_half, then the update from it), or out of place
- * (zs_shard_step_halfacc_async_oop: master, m, v and half are HOST arrays of
- * two device pointers, d_state->buf names the current set; a clean step
- * writes set buf ^ 1 and flips it).  Same kernels and arithmetic as the
- * synchronising forms: bit-identical results. */
+/* The half-accumulator step (§2.2's 2-byte gradients, §4.2's skipped
+ * overflow) without a host round trip, as zs_shard_step_async is to
+ * zs_shard_step: the scale, Adam's step count and the learning rate are read
+ * from and written to *d_state on the device, nothing is copied to the host,
+ * the stream is not synchronised, and the whole step can be captured in a
+ * CUDA graph.  In place, or out of place (zs_shard_step_halfacc_async_oop:
+ * master, m, v and half are HOST arrays of two device pointers, d_state->buf
+ * names the current set; a clean step writes set buf ^ 1 and flips it; acc_half
+ * may be NULL when accum_steps == 1).  acc_half holds no defined sums after
+ * the call.  Same kernels and arithmetic as the synchronising forms:
+ * bit-identical results.  Errors as zs_shard_step_async (argument checks
+ * before any launch; a fused step whose barrier wait ran out is reported by
+ * the context's next call). */
 zs_status zs_shard_step_halfacc_async(zs_ctx* ctx, const void* const* grads, int32_t n,
                                       zs_dtype dt, int64_t count, void* acc_half,
                                       int32_t accum_steps, float* master, float* m, float* v,
