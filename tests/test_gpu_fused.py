@@ -85,15 +85,19 @@ def inject(grads, s, G, n, count, dtype):
                                        # either side of the switch from 4- to 8-element
                                        # units (4 CTAs per SM x 152 SMs x 256 x 4)
                                        (1, 1, 622_591), (2, 2, 622_597), (3, 1, 900_001)])
+@pytest.mark.parametrize("hyst,consec", [(1, False), (2, False), (2, True)])
 def test_fused_sync_steps_equal_the_multi_kernel_path_and_the_oracle(zs, ctxs, dtype, n, G,
-                                                                     count):
+                                                                     count, hyst, consec):
+    """Ten steps, overflows at steps 3, 5 and 7, under the loss scaler's
+    hysteresis 1 and 2 (consecutive or not): the fused step's last CTA runs
+    the same scaler as the multi-kernel path."""
     on, off = ctxs
     rng = np.random.default_rng(1000 * n + 10 * G + dtype + count % 97)
     master0 = (rng.standard_normal(count) * 0.02).astype(np.float32)
     hp, hp_o = zs.make_hparams(*HP), oracle.make_hparams(*HP)
     dyn = dtype == FP16
-    sc_o = oracle.make_scaler(1024.0 if dyn else 1.0, 1.0, 3, 1, dyn)
-    sc = {c: zs.zs_scaler_init(sc_o.scale, 1.0, 3, 1, dyn) for c in ("on", "off")}
+    sc_o = oracle.make_scaler(1024.0 if dyn else 1.0, 1.0, 3, hyst, dyn, consec)
+    sc = {c: zs.zs_scaler_init(sc_o.scale, 1.0, 3, hyst, dyn, consec) for c in ("on", "off")}
     st = oracle.ShardState.from_master(master0, dtype)
     sets = {"on": state_set(master0, count), "off": state_set(master0, count)}
     accs = {c: torch.zeros(count, dtype=torch.float32, device="cuda") for c in ("on", "off")}
@@ -340,7 +344,8 @@ def test_set_fused_rejects_unknown_modes(zs):
 
 
 @pytest.mark.parametrize("mode", ["fused", "multi"])
-def test_device_state_step_equals_the_synchronising_step_bitwise(zs, mode):
+@pytest.mark.parametrize("hyst", [1, 2])
+def test_device_state_step_equals_the_synchronising_step_bitwise(zs, mode, hyst):
     """The device forms compute the step's constants (bias corrections by
     square-and-multiply in fp64, the same operations as the host) on the
     device: zs_shard_step_async and zs_shard_step give the same state bit for
@@ -352,8 +357,8 @@ def test_device_state_step_equals_the_synchronising_step_bitwise(zs, mode):
         n, G, count, dtype = 2, 2, 20_011, FP16
         master0 = (rng.standard_normal(count) * 0.02).astype(np.float32)
         hp = zs.make_hparams(*HP)
-        sc = zs.zs_scaler_init(1024.0, 1.0, 2, 1, True)
-        state = zs.DeviceState(zs.zs_scaler_init(1024.0, 1.0, 2, 1, True))
+        sc = zs.zs_scaler_init(1024.0, 1.0, 2, hyst, True)
+        state = zs.DeviceState(zs.zs_scaler_init(1024.0, 1.0, 2, hyst, True))
         a, b = state_set(master0, count), state_set(master0, count)
         acc_a = torch.zeros(count, dtype=torch.float32, device="cuda")
         acc_b = torch.zeros_like(acc_a)
@@ -370,6 +375,7 @@ def test_device_state_step_equals_the_synchronising_step_bitwise(zs, mode):
                                    b["h"], hp, None, state)
             d = state.read()
             assert (d.overflow, d.scaler.scale) == (ovf, sc.scale), s
+            assert (d.scaler.hyst_left, d.scaler.clean_count) == (sc.hyst_left, sc.clean_count)
             t += 0 if ovf else 1
             assert d.step == t
             same_state(a, b, s)
