@@ -441,3 +441,60 @@ def test_fused_clipped_steps_equal_the_multi_kernel_path(zs, ctxs, form, n, G, c
     assert_close(got["p"].cpu().numpy(), st.master, "master")
     assert_close(got["m"].cpu().numpy(), st.m, "m")
     assert_close(got["v"].cpu().numpy(), st.v, "v")
+
+
+@pytest.mark.parametrize("count,dtype", [(524_291, FP16), (900_001, BF16)])
+def test_many_fused_steps_equal_the_multi_kernel_path(zs, count, dtype):
+    """501 device-state out-of-place steps, 50 to each CUDA graph replay (the
+    benchmark's launch pattern for a short step), 4- and 8-element units:
+    every one of them resolved by the fused grid barrier the way the
+    multi-kernel path resolves it.  Two replays run with an inf in the
+    gradients (100 overflowing steps in a row, under hysteresis 2); at the end
+    the current state set, the scale and the step counts are equal bit for bit."""
+    n, per, replays = 2, 50, 10
+    rng = np.random.default_rng(count)
+    master0 = (rng.standard_normal(count) * 0.02).astype(np.float32)
+    pad = (count + 7) // 8 * 8
+    host = np.zeros((n, pad), np.uint16)
+    host[:, :count] = np.stack(rand_grads(rng, n, count, dtype, 1024.0))
+    gbuf = torch.from_numpy(host.view(np.int16)).cuda()
+    hp = zs.make_hparams(*HP)
+    inf = 0x7C00 if dtype == FP16 else 0x7F80
+    runs = []
+    for mode in (zs.ZS_FUSED_ON, zs.ZS_FUSED_OFF):
+        ctx = zs.Ctx()
+        ctx.set_fused(mode)
+        sets = [state_set(master0, count), state_set(np.zeros_like(master0), count)]
+        pairs = [zs.pointer_array([sets[0][k], sets[1][k]]) for k in ("p", "m", "v", "h")]
+        ptrs = zs.pointer_array(gbuf[r, :count] for r in range(n))
+        dyn = dtype == FP16
+        state = zs.DeviceState(zs.zs_scaler_init(1024.0 if dyn else 1.0, 1.0, 7, 2, dyn))
+
+        def step():
+            zs.zs_shard_step_async_oop(ctx, ptrs, dtype, count, None, 1, *pairs, hp, None, state)
+        step()                                   # uncaptured: caches the launch shapes
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(per):
+                step()
+        runs.append((ctx, sets, state, g))
+    for r in range(replays):
+        if r in (3, 7):
+            gbuf[1, 12_345] = inf
+        for _, _, _, g in runs:
+            g.replay()
+        torch.cuda.synchronize()
+        if r in (3, 7):
+            gbuf[1, 12_345] = int(host[1, 12_345].astype(np.int16))
+    (c_on, s_on, d_on, _), (c_off, s_off, d_off, _) = runs
+    a, b = d_on.read(), d_off.read()
+    assert a.iterations == b.iterations == 1 + per * replays
+    assert (a.step, a.buf, a.scaler.scale, a.scaler.hyst_left, a.scaler.clean_count) == \
+        (b.step, b.buf, b.scaler.scale, b.scaler.hyst_left, b.scaler.clean_count)
+    assert a.step == 1 + per * (replays - 2)                 # the two inf replays skipped
+    same_state(s_on[a.buf & 1], s_off[b.buf & 1], "after 501 steps")
+    assert not torch.equal(s_on[a.buf & 1]["p"], torch.from_numpy(master0).cuda())
+    for ctx, _, _, g in runs:
+        del g
+        ctx.close()
